@@ -1,0 +1,361 @@
+"""Benchmark: one affinity-aware MoE layer forward per step on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--config NAME] [--impl ours|reference]
+
+A step is one whole layer forward (route + lookup/count + permute + grouped
+FFN + shared FFN + combine) over one batch of synthetic tokens, inputs
+resident in HBM.  Prints one JSON line (rank 0).  With N > 1 (torchrun) each
+rank runs an independent replica of the layer: the path has no exchange step
+on one device, so there is no collective on the data path ("weak" scaling).
+
+``--impl reference`` times the CPU oracle (plain numpy, float64) on the host
+cores on a bounded sample of the same workload, as the reference arm.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+import workloads as wl  # noqa: E402
+
+METRIC = "MoE-layer tokens/s (route+permute+grouped FFN+combine), % of HBM/TC roofline"
+
+
+def _peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return dict(hbm_gbs=float(d["hbm_gbs"]), bf16_tflops=float(d["bf16_tflops"]),
+                    bf16_tflops_sustained=float(d.get("bf16_tflops_sustained", d["bf16_tflops"])),
+                    source="measured")
+    return dict(hbm_gbs=6800.0, bf16_tflops=1900.0, bf16_tflops_sustained=1700.0, source="fallback")
+
+
+class ClockSampler:
+    """nvidia-smi clock/throttle samples every 200 ms while the timed region runs."""
+
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.dev = device_index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            uuid = str(torch.cuda.get_device_properties(self.dev).uuid)
+            sel = uuid if uuid.startswith("GPU-") else ("GPU-" + uuid)
+        except Exception:
+            sel = str(self.dev)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.QUERY}", "--format=csv,noheader,nounits", "-lms", "200",
+                 "-i", sel], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *a):
+        if self.proc is None:
+            return
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except Exception:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        self.lines = [ln for ln in out.splitlines() if ln.strip()]
+
+    def summary(self):
+        if not self.lines:
+            return None
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            f = [x.strip() for x in ln.split(",")]
+            try:
+                sm.append(float(f[1]))
+                mx = float(f[2])
+            except (ValueError, IndexError):
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def _dist():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if torch.cuda.is_available():
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend)
+    return world, rank, local
+
+
+def _barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def _max_over_ranks(world, v: float) -> float:
+    if world == 1:
+        return v
+    import torch.distributed as dist
+    t = torch.tensor([v], dtype=torch.float64, device="cuda" if torch.cuda.is_available() else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def _flops_bytes(spec, P):
+    """Algorithmic flops and bytes of each step for one layer forward."""
+    s = 2 if spec.dtype == "bf16" else 4
+    sr = 2 if spec.router_dtype == "bf16" else 4
+    T, H, E, I, k = spec.T, spec.H, spec.E, spec.I, spec.k_max
+    return {
+        "route": dict(flops=2 * T * H * E, bytes=T * H * s + E * H * sr + T * k * 8),
+        "permute": dict(bytes=4 * T * k * 2 + 4 * P + 4 * T * k + T * H * s + P * H * s),
+        "grouped_ffn": dict(flops=6 * H * I * P),
+        "shared_ffn": dict(flops=6 * H * spec.I_shared * T),
+        "combine": dict(bytes=P * H * s + 8 * T * k + T * H * s * (2 if spec.I_shared else 1)),
+    }
+
+
+def cpu_oracle_rate(d, n_tokens: int, weights64=None):
+    """Tokens/s of the CPU oracle on the first n_tokens of the workload."""
+    import oracle
+    spec = d["spec"]
+    if weights64 is None:
+        weights64 = _weights64(d)
+    sl = slice(0, n_tokens)
+    t0 = time.perf_counter()
+    oracle.moe_layer(d["x"][sl], weights64["w_router"], d["token_ids"][sl], d["lut"], d["expert_rank"],
+                     d["k_per_token"][sl], weights64["w13"], weights64["w2"], spec.R, spec.dtype,
+                     spec.k_max, weights64["ws13"], weights64["ws2"])
+    dt = time.perf_counter() - t0
+    return n_tokens / dt, dt
+
+
+def _weights64(d):
+    """float64 numpy copies of the weights (exact), made once outside any timing."""
+    f = lambda t: None if t is None else t.to(torch.float64).numpy()  # noqa: E731
+    return {k: f(d[k]) for k in ("w_router", "w13", "w2", "ws13", "ws2")}
+
+
+def _cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except Exception:
+        return os.cpu_count()
+
+
+def run_reference(args, world, rank):
+    """The oracle as the reference arm: each step is a bounded sample of the workload."""
+    if rank != 0:
+        return
+    spec = wl.CONFIGS[args.config]
+    d = wl.make_inputs(spec)
+    w64 = _weights64(d)
+    n = args.ref_tokens
+    for _ in range(args.warmup):
+        cpu_oracle_rate(d, n, w64)
+    times = []
+    for _ in range(args.steps):
+        _, dt = cpu_oracle_rate(d, n, w64)
+        times.append(dt)
+    total = sum(times)
+    value = n * args.steps / total
+    sample = f"first {n} of {spec.T} tokens of {spec.name} per step (float64 numpy oracle)"
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1000 * total / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": _config(spec),
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": _cores(), "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def _config(spec):
+    return {"workload": spec.name, "T": spec.T, "H": spec.H, "E": spec.E, "top_k": spec.k_max,
+            "I": spec.I, "I_shared": spec.I_shared, "R": spec.R, "dtype": spec.dtype,
+            "router_dtype": spec.router_dtype,
+            "l2": "inputs larger than L2: expert weights (>1 GB) are streamed every step",
+            "parallelism": "replicas"}
+
+
+def run_ours(args, world, rank, local):
+    from token_expert_routing_gb300 import MoELayer, _abi
+
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    spec = wl.CONFIGS[args.config]
+    d = wl.make_inputs(spec)
+    layer = MoELayer(d["w_router"], d["w13"], d["w2"], d["expert_rank"], d["lut"], spec.R, spec.k_max,
+                     d["ws13"], d["ws2"], device=dev)
+    x = d["x"].to(dev)
+    ids = d["token_ids"].to(dev)
+    per_token = bool(spec.k_choices)
+    kpt = d["k_per_token"].to(dev) if per_token else None
+    k = None if per_token else spec.k
+    P = int(d["k_per_token"].sum())
+    stream = torch.cuda.current_stream(dev)
+
+    def step(marks=None):
+        return layer.forward(x, ids, kpt, k, P, stream=stream, marks=marks)
+
+    for _ in range(args.warmup):
+        step()
+    _abi.semmoe_check_errors()
+
+    # device-timed region: K whole-layer steps, inputs resident in HBM
+    all_marks = [[] for _ in range(args.steps)]
+    launches0 = _abi.semmoe_kernel_launches()
+    _barrier(world)
+    torch.cuda.synchronize(dev)
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local) as clocks:
+        start.record(stream)
+        for i in range(args.steps):
+            step(all_marks[i])
+        end.record(stream)
+        torch.cuda.synchronize(dev)
+    _barrier(world)
+    launches = _abi.semmoe_kernel_launches() - launches0
+    _abi.semmoe_check_errors()
+    ms = start.elapsed_time(end)
+    ms_max = _max_over_ranks(world, ms)
+
+    stage_ms = {}
+    for marks in all_marks:
+        for (_, a), (name, b) in zip(marks[:-1], marks[1:]):
+            stage_ms.setdefault(name, []).append(a.elapsed_time(b))
+    stage_avg = {n: sum(v) / len(v) for n, v in stage_ms.items()}
+
+    # end to end through the public API: pinned host inputs in, host output back
+    x_h = d["x"].pin_memory()
+    ids_h = d["token_ids"].pin_memory()
+    k_h = d["k_per_token"].pin_memory() if per_token else None
+    out_h = torch.empty(spec.T, spec.H, dtype=d["x"].dtype).pin_memory()
+    for _ in range(args.warmup):
+        layer.forward_host(x_h, ids_h, k_h, k, out_h, stream=stream)
+    _barrier(world)
+    torch.cuda.synchronize(dev)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        layer.forward_host(x_h, ids_h, k_h, k, out_h, stream=stream)
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    e2e_ms = _max_over_ranks(world, e0.elapsed_time(e1))
+    h2d = x_h.numel() * x_h.element_size() + ids_h.numel() * 4 + (k_h.numel() * 4 if per_token else 0)
+    d2h = out_h.numel() * out_h.element_size()
+
+    if rank != 0:
+        return
+    peaks = _peaks()
+    fb = _flops_bytes(spec, P)
+    ffn_ms = stage_avg["grouped_ffn"]
+    achieved = fb["grouped_ffn"]["flops"] / (ffn_ms * 1e-3) / 1e12
+    roofline = {
+        "kernel": "semmoe_grouped_ffn (GEMM1+SwiGLU, GEMM2)",
+        "bound": "tensor", "achieved": achieved, "peak": peaks["bf16_tflops_sustained"], "unit": "TFLOP/s",
+        "frac": achieved / peaks["bf16_tflops_sustained"], "traffic": None,
+        "peak_source": f"{peaks['source']} (sustained bf16)",
+    }
+    stages = {}
+    for name, avg in stage_avg.items():
+        ent = {"ms": avg}
+        f = fb.get(name, {})
+        if "flops" in f:
+            ent["tflops"] = f["flops"] / (avg * 1e-3) / 1e12
+            ent["frac_tensor"] = ent["tflops"] / peaks["bf16_tflops_sustained"]
+        if "bytes" in f:
+            ent["gbs"] = f["bytes"] / (avg * 1e-3) / 1e9
+            ent["frac_hbm"] = ent["gbs"] / peaks["hbm_gbs"]
+        stages[name] = ent
+
+    cpu = None
+    if not args.no_cpu_baseline:
+        n_cpu = min(args.cpu_tokens, spec.T)
+        rate, dt = cpu_oracle_rate(d, n_cpu)
+        cpu = {"value": rate, "unit": "tokens/s", "cores": _cores(), "kind": "oracle",
+               "sample": f"first {n_cpu} of {spec.T} tokens of {spec.name}, one pass "
+                         f"({dt:.1f} s, float64 numpy oracle)"}
+
+    total_tokens = spec.T * args.steps * world
+    line = {
+        "metric": METRIC, "value": total_tokens / (ms_max * 1e-3), "unit": "tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_max / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": spec.dtype,
+        "data": "synthetic", "config": _config(spec),
+        "e2e": {"value": total_tokens / (e2e_ms * 1e-3), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h},
+        "gpu_launches": launches,
+        "roofline": roofline,
+        "stages": stages,
+        "cpu_baseline": cpu,
+        "clocks": clocks.summary(),
+        "local_activation_rate": None,
+    }
+    res = layer.forward(x, ids, kpt, k, P, stream=stream)
+    counts = res.counts.cpu().numpy()
+    line["local_activation_rate"] = float(np.trace(counts) / counts.sum())
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--config", default=wl.BENCH_CONFIG, choices=sorted(wl.CONFIGS))
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--ref-tokens", type=int, default=512,
+                    help="tokens per step of the CPU oracle sample")
+    ap.add_argument("--cpu-tokens", type=int, default=4096,
+                    help="tokens of the one-pass CPU oracle baseline (capped at T)")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)   # at least 3 untimed warm-up steps
+    world, rank, local = _dist()
+    try:
+        if args.impl == "reference":
+            run_reference(args, world, rank)
+        else:
+            run_ours(args, world, rank, local)
+    finally:
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,241 @@
+/*
+ * semmoe.h -- C ABI of the affinity-aware MoE layer forward on one GPU.
+ *
+ * The layer follows two systems described in
+ *   [SP]  "Semantic Parallelism: Redefining Efficient MoE Inference via
+ *          Model-Data Co-Scheduling" (Sem-MoE; summaries in Korean (ko),
+ *          German (de) and Japanese (ja)), and
+ *   [MP]  "MoE-Prism: Disentangling Monolithic Experts for Elastic MoE
+ *          Services via Model-System Co-Designs" (Korean summary).
+ * One forward is six steps, each one call below, all asynchronous on one
+ * CUDA stream:
+ *   semmoe_route            router GEMM, fp32 softmax, per-token top-k
+ *   semmoe_affinity_lookup  token id -> predicted logical rank
+ *   semmoe_remote_count     activations per (source rank, destination rank)
+ *   semmoe_permute          stable sort of (token, expert) pairs by
+ *                           (destination rank, expert) + row gather
+ *   semmoe_grouped_ffn      per-expert SwiGLU FFN over the sorted rows
+ *   semmoe_shared_ffn       dense SwiGLU of the shared experts (optional)
+ *   semmoe_combine          un-permute and gate-weighted sum
+ *
+ * Conventions (every call):
+ *  - Pointers marked [device] are CUDA device pointers owned by the caller;
+ *    the library never allocates, frees or retains them.  Pointers marked
+ *    [host] are ordinary host memory.
+ *  - Arrays are dense and row-major; the last dimension is contiguous.
+ *    Activation/weight pointers must be 16-byte aligned; workspaces 256-byte.
+ *  - `stream` is a cudaStream_t (NULL = the legacy default stream).  Calls only
+ *    enqueue work; none synchronises the host except semmoe_check_errors.
+ *  - dtype: SEMMOE_F32 (fp32 activations and expert weights) or SEMMOE_BF16
+ *    (bf16 storage, fp32 accumulation).
+ *  - Return value: SEMMOE_OK or an error code.  Arguments are validated on
+ *    the host before anything is enqueued; on error nothing is enqueued and
+ *    semmoe_last_error() (thread-local) describes the problem.
+ *  - Data errors that only the device can see (an expert index >= E, a token
+ *    id >= V, a table value >= R, k_t outside [1, k_max], more pairs than P,
+ *    a non-finite logit) never fault: the offending element is skipped or
+ *    clamped, a bit is set in a device error word, and the next
+ *    semmoe_check_errors() reports SEMMOE_ERR_DEVICE_CHECK.
+ *
+ * Notation: T tokens, H hidden, E experts, I expert intermediate, R logical
+ * ranks, k_t the per-token budget (k of the token's request), k_max its
+ * maximum, pair id p = t*k_max + j for slot j < k_t, P = sum_t k_t.
+ */
+#ifndef SEMMOE_H
+#define SEMMOE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+enum {
+  SEMMOE_OK = 0,
+  SEMMOE_ERR_INVALID_ARG = 1,    /* bad pointer, size, alignment or workspace */
+  SEMMOE_ERR_UNSUPPORTED = 2,    /* shape/dtype outside the supported set, or not sm_103 */
+  SEMMOE_ERR_CUDA = 3,           /* a CUDA runtime/driver call failed */
+  SEMMOE_ERR_DEVICE_CHECK = 4,   /* a kernel saw invalid data (see the device error word) */
+  SEMMOE_ERR_DEVICE_TIMEOUT = 5  /* a bounded wait inside a kernel ran out */
+};
+
+enum { SEMMOE_F32 = 0, SEMMOE_BF16 = 1 };
+
+/* Device error word bits reported through semmoe_check_errors(). */
+enum {
+  SEMMOE_DEVERR_EXPERT = 1,      /* expert index outside [0, E) */
+  SEMMOE_DEVERR_TOKEN_ID = 2,    /* token id outside [0, V) */
+  SEMMOE_DEVERR_LUT = 4,         /* table value outside [0, R) */
+  SEMMOE_DEVERR_K = 8,           /* k_t outside [1, k_max] */
+  SEMMOE_DEVERR_PAIRS = 16,      /* more live pairs than the P passed in, or a bad pair index */
+  SEMMOE_DEVERR_TIMEOUT = 32,    /* a bounded in-kernel wait gave up */
+  SEMMOE_DEVERR_NONFINITE = 64   /* a non-finite router logit */
+};
+
+/* Message of the last failing call on this host thread ("" if none). */
+const char* semmoe_last_error(void);
+
+/* Library version, major*10000 + minor*100 + patch. */
+int semmoe_version(void);
+
+/* Number of kernels this library has launched in this process (all devices,
+ * all threads), counted on the host at each launch.  Not a device query. */
+unsigned long long semmoe_kernel_launches(void);
+
+/*
+ * Synchronise `stream`, then read and clear the device error words of the
+ * current device.  Returns SEMMOE_OK, SEMMOE_ERR_DEVICE_CHECK,
+ * SEMMOE_ERR_DEVICE_TIMEOUT or SEMMOE_ERR_CUDA.  If `bits` is not NULL
+ * [host], the OR of the SEMMOE_DEVERR_* bits seen is stored there.
+ */
+int semmoe_check_errors(void* stream, int* bits);
+
+/*
+ * semmoe_route -- router GEMM, fp32 softmax and per-token top-k.
+ *
+ * The router ("gate") scores every expert for every token and activates a
+ * few ([SP] ko §1; [MP] §1); [MP] §1, §2 B and §5 let each request run with
+ * its own routing budget k in one batch, so k is given per token.
+ *
+ *   logits[t,e] = sum_h x[t,h] * w_router[e,h]                 (fp32 accumulation)
+ *   experts are ordered by logit, descending; equal logits keep the lower
+ *   index first (-0.0 equals +0.0); slot j < k_t holds the j-th of that order
+ *   gates: w[t,j] = exp(l_j - m) / sum_{i<k_t} exp(l_i - m),  m = max selected
+ *   (the fp32 softmax renormalised over the selected experts)
+ *
+ * x          [device] [T,H], x_dtype (SEMMOE_F32 or SEMMOE_BF16)
+ * w_router   [device] [E,H], w_dtype (SEMMOE_F32 or SEMMOE_BF16)
+ * logits_in  [device] [T,E] fp32 or NULL.  If set, x and w_router are not
+ *            read (may be NULL) and these logits are routed as given.
+ * logits_out [device] [T,E] fp32 or NULL: receives the logits used.
+ * k_per_token[device] [T] int32 in [1,k_max], or NULL to use k_uniform.
+ * k_uniform  budget of every token when k_per_token is NULL (1..k_max).
+ * topk_idx   [device] [T,k_max] int32 out: slot j < k_t = expert, else -1.
+ * topk_w     [device] [T,k_max] fp32 out: gates, 0 in padding slots.
+ * Limits: 1 <= k_max <= E <= 256; T >= 0 (T = 0 enqueues nothing).
+ */
+int semmoe_route(const void* x, int x_dtype, const void* w_router, int w_dtype,
+                 const float* logits_in, float* logits_out,
+                 const int32_t* k_per_token, int k_uniform,
+                 int T, int H, int E, int k_max,
+                 int32_t* topk_idx, float* topk_w, void* stream);
+
+/*
+ * semmoe_affinity_lookup -- predicted logical rank of each token from its id.
+ *
+ * [SP] ja §2.3: a lightweight table, built offline from the token-expert
+ * affinity ([SP] de §2 A), maps a token to its expert group and device:
+ *   pred_rank[t] = lut[token_ids[t]].
+ *
+ * token_ids [device] [T] int32 in [0,V);  lut [device] [V] int32 in [0,R)
+ * pred_rank [device] [T] int32 out (an out-of-range id or value gives 0 and
+ *           sets a device error bit).
+ */
+int semmoe_affinity_lookup(const int32_t* token_ids, const int32_t* lut, int V, int R,
+                           int T, int32_t* pred_rank, void* stream);
+
+/*
+ * semmoe_remote_count -- activations by (predicted source rank, destination
+ * rank); the remote ones per source rank.
+ *
+ * A pair (t, j) is a local activation when its expert is hosted on the
+ * token's own rank, remote otherwise; [SP] ko §3-§4 and de §4 measure the
+ * local activation rate.  counts[src][dst] += 1 for every live pair with
+ * src = pred_rank[t], dst = expert_rank[topk_idx[t,j]];
+ * remote[src] = sum_{dst != src} counts[src][dst];  LAR = trace(counts) / P.
+ * counts is also the send-count table of an expert-parallel all-to-all.
+ *
+ * topk_idx    [device] [T,k_max] int32 (-1 = padding slot, skipped)
+ * pred_rank   [device] [T] int32;  expert_rank [device] [E] int32 in [0,R)
+ * counts      [device] [R,R] int32 out (overwritten);  remote [device] [R] int32 out
+ * Limits: 1 <= R <= 64.
+ */
+int semmoe_remote_count(const int32_t* topk_idx, const int32_t* pred_rank,
+                        const int32_t* expert_rank, int T, int k_max, int E, int R,
+                        int32_t* counts, int32_t* remote, void* stream);
+
+/*
+ * semmoe_permute -- the single-device form of the Shuffled-Reduce-Scatter
+ * token shuffle: tokens go to the rank hosting their target experts
+ * ([SP] ko §2.2, de §2 B, ja §2.2 B).  Experts are laid out rank-major, the
+ * physical order that [SP] ja §2.2 A obtains by shuffling gate columns:
+ * phys(e) = position of e when experts are sorted by (expert_rank[e], e).
+ * Pairs are sorted stably by phys(topk_idx[p]) (ties keep increasing p), and
+ * each sorted row receives its token's activation row.
+ *
+ * topk_idx       [device] [T,k_max] int32 (-1 = padding slot)
+ * expert_rank    [device] [E] int32 in [0,R)
+ * x              [device] [T,H] dtype, or NULL to skip the row gather
+ * P              number of live pairs (sum_t k_t), known to the caller
+ * expert_offsets [device] [E+1] int32 out: row range of physical bucket b
+ * rank_offsets   [device] [R+1] int32 out: row range of rank r
+ * phys_to_expert [device] [E]   int32 out: expert in physical bucket b
+ * expert_counts  [device] [E]   int32 out: pairs per expert (logical order)
+ * sorted_to_pair [device] [P]   int32 out: pair id of sorted row q
+ * pair_to_sorted [device] [T*k_max] int32 out: sorted row of pair p, -1 for padding
+ * x_perm         [device] [P,H] dtype out (x_perm[q] = x[sorted_to_pair[q] / k_max]),
+ *                or NULL when x is NULL
+ * ws, ws_bytes   [device] workspace of at least semmoe_permute_workspace_size()
+ * Limits: 1 <= E <= 256, 1 <= R <= E, 1 <= k_max <= E.
+ */
+size_t semmoe_permute_workspace_size(int T, int k_max, int E);
+int semmoe_permute(const int32_t* topk_idx, const int32_t* expert_rank,
+                   const void* x, int dtype, int T, int H, int E, int R, int k_max, int P,
+                   int32_t* expert_offsets, int32_t* rank_offsets, int32_t* phys_to_expert,
+                   int32_t* expert_counts, int32_t* sorted_to_pair, int32_t* pair_to_sorted,
+                   void* x_perm, void* ws, size_t ws_bytes, void* stream);
+
+/*
+ * semmoe_grouped_ffn -- SwiGLU expert FFN over the sorted rows.
+ *
+ * The activated experts' computation ([SP] ko §1; [MP] §2 A: an expert is a
+ * set of intermediate neurons).  Rows [expert_offsets[b], expert_offsets[b+1])
+ * belong to expert e = phys_to_expert[b]:
+ *   h = silu(x W1_e^T) * (x W3_e^T),  silu(z) = z / (1 + exp(-z)),  h stored in dtype
+ *   y = h W2_e^T, stored in dtype
+ *
+ * x_perm  [device] [P,H] dtype
+ * w13     [device] [E,2I,H] dtype: rows 0..I-1 = W1_e (gate), I..2I-1 = W3_e (up)
+ * w2      [device] [E,H,I] dtype
+ * y_perm  [device] [P,H] dtype out
+ * ws      [device] workspace of at least semmoe_grouped_ffn_workspace_size()
+ * Limits: H % 8 == 0 and I % 8 == 0 (16-byte rows for bf16 tensor-core tiles).
+ */
+size_t semmoe_grouped_ffn_workspace_size(int P, int I, int dtype);
+int semmoe_grouped_ffn(const void* x_perm, const int32_t* expert_offsets,
+                       const int32_t* phys_to_expert, const void* w13, const void* w2,
+                       int dtype, int P, int E, int H, int I,
+                       void* y_perm, void* ws, size_t ws_bytes, void* stream);
+
+/*
+ * semmoe_shared_ffn -- the shared experts (applied to every token with gate 1,
+ * their weights concatenated along the intermediate dimension I_s):
+ *   y_shared = (silu(x Ws1^T) * (x Ws3^T)) Ws2^T.
+ * x [device] [T,H]; ws13 [device] [2*I_s,H]; ws2 [device] [H,I_s];
+ * y_shared [device] [T,H] out; ws workspace of semmoe_shared_ffn_workspace_size().
+ */
+size_t semmoe_shared_ffn_workspace_size(int T, int I_s, int dtype);
+int semmoe_shared_ffn(const void* x, const void* ws13, const void* ws2, int dtype,
+                      int T, int H, int I_s, void* y_shared, void* ws, size_t ws_bytes,
+                      void* stream);
+
+/*
+ * semmoe_combine -- the single-device form of the Shuffled-Allgather: expert
+ * results return to the original token order ([SP] de §2 B, ja §2.2 B) and
+ * are mixed by the gates:
+ *   out[t] = y_shared[t] + sum_{j<k_t} topk_w[t,j] * y_perm[pair_to_sorted[t*k_max+j]]
+ * summed in that order in fp32, stored in dtype.
+ *
+ * y_perm [device] [P,H]; pair_to_sorted [device] [T*k_max] (-1 = padding, skipped);
+ * topk_w [device] [T,k_max] fp32; y_shared [device] [T,H] or NULL;
+ * out [device] [T,H] dtype out.
+ */
+int semmoe_combine(const void* y_perm, const int32_t* pair_to_sorted, const float* topk_w,
+                   const void* y_shared, int dtype, int T, int H, int k_max, int P,
+                   void* out, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* SEMMOE_H */

@@ -1,0 +1,120 @@
+"""The C-ABI library builds, loads and exports every declared entry point;
+host-side validation rejects bad arguments before any CUDA call (CPU only)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "semmoe.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from token_expert_routing_gb300 import build, _abi
+    build.build()
+    return _abi.lib()
+
+
+def declared_functions():
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(semmoe_\w+)\s*\(", src)))
+
+
+def test_every_declared_symbol_is_exported(lib):
+    from token_expert_routing_gb300 import _abi
+    names = declared_functions()
+    assert len(names) >= 13
+    for n in names:
+        assert hasattr(lib, n), n
+        assert n in _abi.SIGNATURES, f"{n} missing from the Python binding"
+
+
+def test_version(lib):
+    assert lib.semmoe_version() >= 100
+
+
+def test_workspace_sizes(lib):
+    assert lib.semmoe_permute_workspace_size(4096, 6, 64) >= 4096 * 6 // 2048 * 64 * 4
+    assert lib.semmoe_permute_workspace_size(4096, 6, 64) % 256 == 0
+    assert lib.semmoe_grouped_ffn_workspace_size(24576, 1408, 1) >= 24576 * 1408 * 2
+    assert lib.semmoe_grouped_ffn_workspace_size(-1, 8, 1) == 0
+    assert lib.semmoe_shared_ffn_workspace_size(10, 16, 0) >= 10 * 16 * 4
+
+
+def _err(lib):
+    return lib.semmoe_last_error().decode()
+
+
+def test_route_validation(lib):
+    # E outside [1, 256]
+    rc = lib.semmoe_route(None, 1, None, 0, None, None, None, 2, 16, 64, 0, 2, None, None, None)
+    assert rc == 1 and "E" in _err(lib)
+    rc = lib.semmoe_route(None, 1, None, 0, None, None, None, 2, 16, 64, 300, 2, None, None, None)
+    assert rc == 1
+    # k_max > E
+    rc = lib.semmoe_route(None, 1, None, 0, None, None, None, 2, 16, 64, 8, 9, None, None, None)
+    assert rc == 1 and "k_max" in _err(lib)
+    # k_uniform outside [1, k_max]
+    rc = lib.semmoe_route(None, 1, None, 0, None, None, None, 0, 16, 64, 8, 2, None, None, None)
+    assert rc == 1 and "k_uniform" in _err(lib)
+    # null outputs
+    rc = lib.semmoe_route(None, 1, None, 0, None, None, None, 2, 16, 64, 8, 2, None, None, None)
+    assert rc == 1 and "null" in _err(lib)
+    # T = 0 is a no-op
+    assert lib.semmoe_route(None, 1, None, 0, None, None, None, 2, 0, 64, 8, 2, None, None, None) == 0
+
+
+def test_permute_validation(lib):
+    p = ctypes.c_void_p(256)
+    # P larger than T * k_max
+    rc = lib.semmoe_permute(p, p, None, 1, 4, 8, 8, 2, 2, 9, p, p, p, p, p, p, None, p, 1 << 20, None)
+    assert rc == 1 and "P" in _err(lib)
+    # undersized workspace
+    rc = lib.semmoe_permute(p, p, None, 1, 4, 8, 8, 2, 2, 8, p, p, p, p, p, p, None, p, 4, None)
+    assert rc == 1 and "workspace" in _err(lib)
+    # misaligned workspace
+    rc = lib.semmoe_permute(p, p, None, 1, 4, 8, 8, 2, 2, 8, p, p, p, p, p, p, None,
+                            ctypes.c_void_p(260), 1 << 20, None)
+    assert rc == 1
+    # x without x_perm
+    rc = lib.semmoe_permute(p, p, p, 1, 4, 8, 8, 2, 2, 8, p, p, p, p, p, p, None, p, 1 << 20, None)
+    assert rc == 1 and "x_perm" in _err(lib)
+    # R > E
+    rc = lib.semmoe_permute(p, p, None, 1, 4, 8, 4, 5, 2, 8, p, p, p, p, p, p, None, p, 1 << 20, None)
+    assert rc == 1
+
+
+def test_ffn_and_combine_validation(lib):
+    p = ctypes.c_void_p(1 << 12)
+    # I not a multiple of 8
+    rc = lib.semmoe_grouped_ffn(p, p, p, p, p, 1, 64, 4, 128, 100, p, p, 1 << 30, None)
+    assert rc == 1 and "multiples of 8" in _err(lib)
+    # bad dtype
+    rc = lib.semmoe_grouped_ffn(p, p, p, p, p, 7, 64, 4, 128, 128, p, p, 1 << 30, None)
+    assert rc == 1
+    # workspace too small
+    rc = lib.semmoe_shared_ffn(p, p, p, 1, 64, 128, 256, p, p, 16, None)
+    assert rc == 1 and "workspace" in _err(lib)
+    # misaligned y
+    rc = lib.semmoe_combine(ctypes.c_void_p(4), p, p, None, 1, 4, 128, 2, 8, p, None)
+    assert rc == 1
+    # H * 2 bytes not a multiple of 16
+    rc = lib.semmoe_combine(p, p, p, None, 1, 4, 12, 2, 8, p, None)
+    assert rc == 1
+
+
+def test_remote_count_validation(lib):
+    p = ctypes.c_void_p(256)
+    rc = lib.semmoe_remote_count(p, p, p, 4, 2, 8, 65, p, p, None)
+    assert rc == 1 and "R" in _err(lib)
+
+
+def test_product_path_fails_loudly_without_library(monkeypatch):
+    from token_expert_routing_gb300 import _abi
+    monkeypatch.setattr(_abi, "LIB_PATH", "/nonexistent/libsemmoe.so")
+    monkeypatch.setattr(_abi, "_lib", None)
+    with pytest.raises(RuntimeError, match="missing"):
+        _abi.lib()

@@ -1,0 +1,180 @@
+"""Per-kernel parity of the CUDA path (through the C ABI) with the oracle,
+including the degenerate cases: ties and signed zeros, per-token budgets,
+E = 1, T = 1, k = E, empty experts, every token on one expert, empty ranks,
+and data errors that the kernels must report instead of faulting."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from parity_utils import GATE_ATOL, LOGIT_TOL, max_rel, np_
+
+pytestmark = pytest.mark.gpu
+
+i32 = dict(dtype=torch.int32, device="cuda")
+
+
+def abi():
+    from token_expert_routing_gb300 import _abi
+    return _abi
+
+
+def route_logits_in(logits, k, k_max):
+    T, E = logits.shape
+    li = torch.as_tensor(logits, dtype=torch.float32).cuda()
+    kpt = torch.as_tensor(k, dtype=torch.int32).cuda()
+    idx = torch.empty(T, k_max, **i32)
+    w = torch.empty(T, k_max, dtype=torch.float32, device="cuda")
+    abi().semmoe_route(None, None, li, None, kpt, 0, T, 0, E, k_max, idx, w)
+    assert abi().semmoe_check_errors() == 0
+    return np_(idx), np_(w)
+
+
+@pytest.mark.parametrize("T,E,k_max", [(1, 1, 1), (1, 8, 8), (333, 3, 2), (1000, 8, 8), (517, 64, 6),
+                                       (300, 256, 24), (64, 256, 256), (97, 40, 33)])
+def test_route_topk_ties_signed_zeros_per_token_k(T, E, k_max):
+    rng = np.random.default_rng(T + E)
+    logits = (rng.integers(-4, 5, size=(T, E)) * 0.25).astype(np.float32)
+    z = rng.random((T, E)) < 0.2
+    logits[z] = np.where(rng.random(z.sum()) < 0.5, np.float32(0.0), np.float32(-0.0))
+    k = rng.integers(1, k_max + 1, size=T).astype(np.int32)
+    idx, w = route_logits_in(logits, k, k_max)
+    ref_idx, ref_w = oracle.topk_route(logits, k, k_max)
+    np.testing.assert_array_equal(idx, ref_idx)
+    np.testing.assert_allclose(w, ref_w, rtol=0, atol=GATE_ATOL)
+
+
+@pytest.mark.parametrize("xd,wd", [(torch.float32, torch.float32), (torch.bfloat16, torch.float32),
+                                   (torch.bfloat16, torch.bfloat16), (torch.float32, torch.bfloat16)])
+@pytest.mark.parametrize("T,H,E", [(1, 64, 8), (77, 200, 64), (130, 2048, 256)])
+def test_route_gemm(xd, wd, T, H, E):
+    rng = np.random.default_rng(H + E)
+    x = torch.from_numpy(rng.standard_normal((T, H)).astype(np.float32) / np.sqrt(H)).to(xd)
+    wr = torch.from_numpy(rng.standard_normal((E, H)).astype(np.float32) / np.sqrt(H)).to(wd)
+    k_max = min(6, E)
+    idx = torch.empty(T, k_max, **i32)
+    w = torch.empty(T, k_max, dtype=torch.float32, device="cuda")
+    lg = torch.empty(T, E, dtype=torch.float32, device="cuda")
+    abi().semmoe_route(x.cuda(), wr.cuda(), None, lg, None, k_max, T, H, E, k_max, idx, w)
+    assert abi().semmoe_check_errors() == 0
+    assert max_rel(np_(lg), oracle.router_logits(x, wr)) < LOGIT_TOL
+    ref_idx, ref_w = oracle.topk_route(np_(lg), np.full(T, k_max), k_max)
+    np.testing.assert_array_equal(np_(idx), ref_idx)
+    np.testing.assert_allclose(np_(w), ref_w, rtol=0, atol=GATE_ATOL)
+
+
+def _route_random(rng, T, E, k_max, skew=None, per_token=True):
+    l = rng.standard_normal((T, E)).astype(np.float32)
+    if skew is not None:
+        l[:, skew] += 50.0
+    k = rng.integers(1, k_max + 1, size=T) if per_token else np.full(T, k_max)
+    idx, _ = oracle.topk_route(l, k, k_max)
+    return idx.astype(np.int32), k.astype(np.int32)
+
+
+@pytest.mark.parametrize("T,E,R,k_max,skew,H,placement", [
+    (1, 1, 1, 1, None, 8, "mod"),
+    (1, 8, 4, 3, None, 16, "mod"),
+    (5000, 64, 8, 6, None, 64, "mod"),
+    (3000, 16, 4, 5, 3, 32, "random"),        # every token picks expert 3 first
+    (2049, 10, 5, 4, 9, 8, "unbalanced"),     # ragged chunk, ranks without experts
+    (700, 256, 8, 24, None, 16, "mod"),
+    (300, 12, 3, 12, None, 16, "mod"),         # k = E
+])
+def test_permute_and_counts(T, E, R, k_max, skew, H, placement):
+    rng = np.random.default_rng(T * 7 + E)
+    idx, k = _route_random(rng, T, E, k_max, skew)
+    if placement == "mod":
+        er = (np.arange(E) % R).astype(np.int32)
+    elif placement == "random":
+        er = rng.permutation(np.arange(E) % R).astype(np.int32)
+    else:
+        er = np.minimum(rng.integers(0, 2, size=E), R - 1).astype(np.int32) * (R - 1)
+    P = int(k.sum())
+    x = torch.from_numpy(rng.standard_normal((T, H)).astype(np.float32)).to(torch.bfloat16)
+    outs = []
+    for _ in range(2):  # two runs must be byte-identical (no write races)
+        d_idx = torch.from_numpy(idx).cuda()
+        eo, ro = torch.empty(E + 1, **i32), torch.empty(R + 1, **i32)
+        p2e, ec = torch.empty(E, **i32), torch.empty(E, **i32)
+        s2p, p2s = torch.empty(max(P, 1), **i32), torch.empty(T * k_max, **i32)
+        xp = torch.empty(P, H, dtype=torch.bfloat16, device="cuda")
+        ws = torch.empty(abi().semmoe_permute_workspace_size(T, k_max, E), dtype=torch.uint8, device="cuda")
+        abi().semmoe_permute(d_idx, torch.from_numpy(er).cuda(), x.cuda(), T, H, E, R, k_max, P, eo, ro, p2e,
+                             ec, s2p, p2s, xp, ws)
+        assert abi().semmoe_check_errors() == 0
+        outs.append([np_(t) for t in (eo, ro, p2e, ec, s2p[:P], p2s, xp)])
+    for a, b in zip(*outs):
+        np.testing.assert_array_equal(a, b)
+    ref = oracle.permute(idx, k, er, R, x)
+    for key, got in zip(("expert_offsets", "rank_offsets", "phys_to_expert", "expert_counts",
+                         "sorted_to_pair", "pair_to_sorted", "x_perm"), outs[0]):
+        np.testing.assert_array_equal(got, ref[key], err_msg=key)
+
+    # remote counter and lookup on the same routing
+    V = 500
+    lut = rng.integers(0, R, size=V).astype(np.int32)
+    ids = rng.integers(0, V, size=T).astype(np.int32)
+    pred = torch.empty(T, **i32)
+    abi().semmoe_affinity_lookup(torch.from_numpy(ids).cuda(), torch.from_numpy(lut).cuda(), V, R, T, pred)
+    counts, remote = torch.empty(R, R, **i32), torch.empty(R, **i32)
+    abi().semmoe_remote_count(torch.from_numpy(idx).cuda(), pred, torch.from_numpy(er).cuda(), T, k_max, E, R,
+                              counts, remote)
+    assert abi().semmoe_check_errors() == 0
+    rp = oracle.affinity_lookup(ids, lut)
+    np.testing.assert_array_equal(np_(pred), rp)
+    rc, rr = oracle.remote_count(idx, k, rp, er, R)
+    np.testing.assert_array_equal(np_(counts), rc)
+    np.testing.assert_array_equal(np_(remote), rr)
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("shared", [False, True])
+def test_combine(dtype, shared):
+    rng = np.random.default_rng(3)
+    T, H, E, k_max = 333, 136 if dtype == "bf16" else 132, 16, 5
+    tdt = torch.bfloat16 if dtype == "bf16" else torch.float32
+    idx, k = _route_random(rng, T, E, k_max)
+    _, w = oracle.topk_route(rng.standard_normal((T, E)), k, k_max)
+    perm = oracle.permute(idx, k, np.arange(E) % 4, 4)
+    P = int(k.sum())
+    y = torch.from_numpy(rng.standard_normal((P, H)).astype(np.float32)).to(tdt)
+    ys = torch.from_numpy(rng.standard_normal((T, H)).astype(np.float32)).to(tdt) if shared else None
+    out = torch.empty(T, H, dtype=tdt, device="cuda")
+    abi().semmoe_combine(y.cuda(), torch.from_numpy(perm["pair_to_sorted"].astype(np.int32)).cuda(),
+                         torch.from_numpy(w.astype(np.float32)).cuda(), None if ys is None else ys.cuda(),
+                         T, H, k_max, P, out)
+    assert abi().semmoe_check_errors() == 0
+    ref = oracle.combine(y, perm["pair_to_sorted"], w, k, dtype, ys)
+    assert max_rel(np_(out), ref) < (1e-6 if dtype == "f32" else 8e-3)
+
+
+def test_data_errors_are_reported_not_faulted():
+    """A token id beyond the vocabulary and a table value beyond R are caught
+    by the kernels' own bounds checks and reported after a sync."""
+    T, V, R = 64, 100, 4
+    ids = torch.arange(T, dtype=torch.int32)
+    ids[5] = V + 7                       # out of range
+    lut = torch.zeros(V, dtype=torch.int32)
+    lut[3] = R                           # out of range
+    pred = torch.empty(T, **i32)
+    abi().semmoe_affinity_lookup(ids.cuda(), lut.cuda(), V, R, T, pred)
+    with pytest.raises(abi().SemMoEError) as ei:
+        abi().semmoe_check_errors()
+    assert ei.value.code == abi().SEMMOE_ERR_DEVICE_CHECK
+    assert int(pred[5]) == 0 and int(pred[3]) == 0
+    # the error word was cleared by the check
+    assert abi().semmoe_check_errors() == 0
+
+
+def test_bad_budget_is_clamped_and_reported():
+    T, E, k_max = 8, 8, 4
+    li = torch.randn(T, E, device="cuda")
+    kpt = torch.full((T,), 2, **i32)
+    kpt[1] = 9
+    idx = torch.empty(T, k_max, **i32)
+    w = torch.empty(T, k_max, dtype=torch.float32, device="cuda")
+    abi().semmoe_route(None, None, li, None, kpt, 0, T, 0, E, k_max, idx, w)
+    with pytest.raises(abi().SemMoEError):
+        abi().semmoe_check_errors()
+    assert (idx[1] >= 0).all()           # clamped to k_max

@@ -1,0 +1,114 @@
+// Un-permute + gate-weighted combine: the single-device form of the
+// Shuffled-Allgather, which brings the expert results back to the original
+// token order (Semantic Parallelism (de) §2 B, (ja) §2.2 B):
+//   out[t] = y_shared[t] + sum_{j<k_t} w[t,j] * y_perm[pair_to_sorted[t*k_max+j]]
+// summed in that order in fp32.  One warp per token row, 16-byte vectors.
+#include "common.cuh"
+#include "internal.h"
+
+namespace semmoe {
+namespace {
+
+__device__ int g_err;
+__device__ __forceinline__ void flag(int bit) { atomicOr(&g_err, bit); }
+
+constexpr int kThreads = 256;
+constexpr int kWarps = kThreads / 32;
+
+template <typename T> struct Vec16;
+template <> struct Vec16<float> {
+  static constexpr int N = 4;
+  __device__ static void load(const float* p, float* v) {
+    float4 a = *reinterpret_cast<const float4*>(p);
+    v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
+  }
+  __device__ static void store(float* p, const float* v) {
+    *reinterpret_cast<float4*>(p) = make_float4(v[0], v[1], v[2], v[3]);
+  }
+};
+template <> struct Vec16<__nv_bfloat16> {
+  static constexpr int N = 8;
+  __device__ static void load(const __nv_bfloat16* p, float* v) {
+    uint4 a = *reinterpret_cast<const uint4*>(p);
+    const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&a);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      float2 f = __bfloat1622float2(h[i]);
+      v[2 * i] = f.x; v[2 * i + 1] = f.y;
+    }
+  }
+  __device__ static void store(__nv_bfloat16* p, const float* v) {
+    uint4 a;
+    __nv_bfloat162* h = reinterpret_cast<__nv_bfloat162*>(&a);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) h[i] = __floats2bfloat162_rn(v[2 * i], v[2 * i + 1]);
+    *reinterpret_cast<uint4*>(p) = a;
+  }
+};
+
+template <typename T>
+__global__ void __launch_bounds__(kThreads)
+combine_kernel(const T* __restrict__ y_perm, const int32_t* __restrict__ pair_to_sorted,
+               const float* __restrict__ topk_w, const T* __restrict__ y_shared, int T_, int H, int k_max,
+               int P, T* __restrict__ out) {
+  using V = Vec16<T>;
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  for (int t = blockIdx.x * kWarps + warp; t < T_; t += gridDim.x * kWarps) {
+    const int32_t* q_row = pair_to_sorted + (size_t)t * k_max;
+    const float* w_row = topk_w + (size_t)t * k_max;
+    for (int c = lane * V::N; c < H; c += 32 * V::N) {
+      float acc[V::N];
+      if (y_shared != nullptr) {
+        V::load(y_shared + (size_t)t * H + c, acc);
+      } else {
+#pragma unroll
+        for (int i = 0; i < V::N; ++i) acc[i] = 0.f;
+      }
+      for (int j = 0; j < k_max; ++j) {
+        const int q = q_row[j];
+        if (q < 0) continue;
+        if (q >= P) {
+          if (c == lane * V::N) flag(SEMMOE_DEVERR_PAIRS);
+          continue;
+        }
+        const float w = w_row[j];
+        float v[V::N];
+        V::load(y_perm + (size_t)q * H + c, v);
+#pragma unroll
+        for (int i = 0; i < V::N; ++i) acc[i] = fmaf(w, v[i], acc[i]);
+      }
+      V::store(out + (size_t)t * H + c, acc);
+    }
+  }
+}
+
+int sm_count() {
+  int dev = 0, n = 148;
+  if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+  return n;
+}
+
+}  // namespace
+
+int combine_take_errors(cudaStream_t s, int* bits) { return take_error_word(g_err, s, bits); }
+
+cudaError_t launch_combine(const void* y_perm, const int32_t* pair_to_sorted, const float* topk_w,
+                           const void* y_shared, int dtype, int T, int H, int k_max, int P, void* out,
+                           cudaStream_t s) {
+  if (T == 0) return cudaSuccess;
+  int blocks = (T + kWarps - 1) / kWarps;
+  const int cap = sm_count() * 16;
+  if (blocks > cap) blocks = cap;
+  if (dtype == SEMMOE_BF16)
+    combine_kernel<__nv_bfloat16><<<blocks, kThreads, 0, s>>>(
+        static_cast<const __nv_bfloat16*>(y_perm), pair_to_sorted, topk_w,
+        static_cast<const __nv_bfloat16*>(y_shared), T, H, k_max, P, static_cast<__nv_bfloat16*>(out));
+  else
+    combine_kernel<float><<<blocks, kThreads, 0, s>>>(static_cast<const float*>(y_perm), pair_to_sorted, topk_w,
+                                                      static_cast<const float*>(y_shared), T, H, k_max, P,
+                                                      static_cast<float*>(out));
+  count_launches(1);
+  return cudaGetLastError();
+}
+
+}  // namespace semmoe

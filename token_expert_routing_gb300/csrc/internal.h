@@ -1,0 +1,49 @@
+// Launchers behind the C ABI (host code; arguments already validated).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace semmoe {
+
+// Adds n to the library-wide count of kernel launches (see semmoe_kernel_launches).
+void count_launches(int n);
+
+// Each translation unit keeps its own device error word; these read and clear it.
+int route_take_errors(cudaStream_t s, int* bits);
+int permute_take_errors(cudaStream_t s, int* bits);
+int ffn_take_errors(cudaStream_t s, int* bits);
+int combine_take_errors(cudaStream_t s, int* bits);
+
+cudaError_t launch_route(const void* x, int x_dtype, const void* w, int w_dtype,
+                         const float* logits_in, float* logits_out, const int32_t* k_per_token,
+                         int k_uniform, int T, int H, int E, int k_max, int32_t* topk_idx,
+                         float* topk_w, cudaStream_t s);
+
+cudaError_t launch_affinity_lookup(const int32_t* token_ids, const int32_t* lut, int V, int R,
+                                   int T, int32_t* pred, cudaStream_t s);
+
+cudaError_t launch_remote_count(const int32_t* topk_idx, const int32_t* pred,
+                                const int32_t* expert_rank, int T, int k_max, int E, int R,
+                                int32_t* counts, int32_t* remote, cudaStream_t s);
+
+size_t permute_ws_bytes(int T, int k_max, int E);
+cudaError_t launch_permute(const int32_t* topk_idx, const int32_t* expert_rank, const void* x,
+                           int dtype, int T, int H, int E, int R, int k_max, int P,
+                           int32_t* expert_offsets, int32_t* rank_offsets,
+                           int32_t* phys_to_expert, int32_t* expert_counts,
+                           int32_t* sorted_to_pair, int32_t* pair_to_sorted, void* x_perm,
+                           void* ws, cudaStream_t s);
+
+size_t ffn_ws_bytes(int P, int I, int dtype);
+// offsets == nullptr: one group of rows [0, P) using expert 0 of w13/w2.
+cudaError_t launch_ffn(const void* x, const int32_t* offsets, const int32_t* phys_to_expert,
+                       const void* w13, const void* w2, int dtype, int P, int E, int H, int I,
+                       void* y, void* ws, cudaStream_t s);
+
+cudaError_t launch_combine(const void* y_perm, const int32_t* pair_to_sorted, const float* topk_w,
+                           const void* y_shared, int dtype, int T, int H, int k_max, int P,
+                           void* out, cudaStream_t s);
+
+}  // namespace semmoe

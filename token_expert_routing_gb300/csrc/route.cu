@@ -1,0 +1,300 @@
+// Router GEMM + fp32 softmax + per-token top-k; token-id affinity lookup;
+// per-(source rank, destination rank) activation counts.
+//
+// Router: the gate that scores experts per token (Semantic Parallelism (ko)
+// §1, MoE-Prism (ko) §1) with a per-request budget k (MoE-Prism (ko) §2 B).
+// Lookup table: Semantic Parallelism (ja) §2.3.  Local activation rate:
+// Semantic Parallelism (ko) §3-§4.
+#include <math.h>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace semmoe {
+namespace {
+
+__device__ int g_err;  // SEMMOE_DEVERR_* bits seen by this file's kernels
+
+__device__ __forceinline__ void flag(int bit) { atomicOr(&g_err, bit); }
+
+constexpr int kRouteThreads = 256;
+constexpr int kRouteTok = 32;   // tokens per block
+constexpr int kRouteEC = 64;    // experts per GEMM chunk
+constexpr int kRouteHK = 32;    // hidden elements per k step
+constexpr int kRouteMaxE = 256;
+constexpr int kWarps = kRouteThreads / 32;
+
+// Shared-memory layout of route_kernel (floats unless noted):
+//   lg   [kRouteTok][Epad]        logits of the block's tokens
+//   xs   [kRouteTok][kRouteHK+1]  x tile (fp32)
+//   ws   [kRouteEC][kRouteHK+1]   router-weight tile (fp32)
+//   sel_v[kWarps][k_max], sel_e[kWarps][k_max] (int)
+__host__ __device__ inline size_t route_smem_bytes(int E, int k_max) {
+  int Epad = (E + 31) / 32 * 32;
+  return sizeof(float) * ((size_t)kRouteTok * Epad + (size_t)(kRouteTok + kRouteEC) * (kRouteHK + 1)) +
+         (size_t)kWarps * k_max * (sizeof(float) + sizeof(int));
+}
+
+template <typename TX, typename TW>
+__global__ void __launch_bounds__(kRouteThreads)
+route_kernel(const TX* __restrict__ x, const TW* __restrict__ w, const float* __restrict__ logits_in,
+             float* __restrict__ logits_out, const int32_t* __restrict__ k_per_token, int k_uniform,
+             int T, int H, int E, int k_max, int32_t* __restrict__ topk_idx,
+             float* __restrict__ topk_w) {
+  extern __shared__ __align__(16) unsigned char smem_raw[];
+  const int Epad = (E + 31) / 32 * 32;
+  float* lg = reinterpret_cast<float*>(smem_raw);
+  float* xs = lg + kRouteTok * Epad;
+  float* wsm = xs + kRouteTok * (kRouteHK + 1);
+  float* sel_v = wsm + kRouteEC * (kRouteHK + 1);
+  int* sel_e = reinterpret_cast<int*>(sel_v + kWarps * k_max);
+
+  const int tid = threadIdx.x;
+  const int t0 = blockIdx.x * kRouteTok;
+
+  if (logits_in != nullptr) {
+    for (int i = tid; i < kRouteTok * Epad; i += kRouteThreads) {
+      int tl = i / Epad, e = i % Epad;
+      int t = t0 + tl;
+      lg[i] = (t < T && e < E) ? logits_in[(size_t)t * E + e] : -INFINITY;
+    }
+  } else {
+    // logits[t, e] = sum_h x[t, h] * w[e, h]; thread = 2 tokens x 4 experts.
+    const int ty = tid / 16, tx = tid % 16;
+    for (int ec0 = 0; ec0 < E; ec0 += kRouteEC) {
+      float acc[2][4] = {};
+      for (int k0 = 0; k0 < H; k0 += kRouteHK) {
+        for (int i = tid; i < kRouteTok * kRouteHK; i += kRouteThreads) {
+          int r = i / kRouteHK, k = i % kRouteHK;
+          int t = t0 + r, h = k0 + k;
+          xs[r * (kRouteHK + 1) + k] = (t < T && h < H) ? to_f32(x[(size_t)t * H + h]) : 0.f;
+        }
+        for (int i = tid; i < kRouteEC * kRouteHK; i += kRouteThreads) {
+          int r = i / kRouteHK, k = i % kRouteHK;
+          int e = ec0 + r, h = k0 + k;
+          wsm[r * (kRouteHK + 1) + k] = (e < E && h < H) ? to_f32(w[(size_t)e * H + h]) : 0.f;
+        }
+        __syncthreads();
+#pragma unroll 8
+        for (int k = 0; k < kRouteHK; ++k) {
+          float a0 = xs[(ty * 2 + 0) * (kRouteHK + 1) + k];
+          float a1 = xs[(ty * 2 + 1) * (kRouteHK + 1) + k];
+#pragma unroll
+          for (int b = 0; b < 4; ++b) {
+            float bv = wsm[(tx + 16 * b) * (kRouteHK + 1) + k];
+            acc[0][b] = fmaf(a0, bv, acc[0][b]);
+            acc[1][b] = fmaf(a1, bv, acc[1][b]);
+          }
+        }
+        __syncthreads();
+      }
+#pragma unroll
+      for (int a = 0; a < 2; ++a)
+#pragma unroll
+        for (int b = 0; b < 4; ++b) {
+          int tl = ty * 2 + a, e = ec0 + tx + 16 * b;
+          if (e < Epad) lg[tl * Epad + e] = (e < E) ? acc[a][b] : -INFINITY;
+          if (logits_out != nullptr && e < E && t0 + tl < T)
+            logits_out[(size_t)(t0 + tl) * E + e] = acc[a][b];
+        }
+    }
+  }
+  __syncthreads();
+
+  // Top-k_t per token, one warp per token: repeated warp argmax over
+  // (logit descending, expert index ascending), skipping taken experts.
+  const int warp = tid / 32, lane = tid % 32;
+  float* my_v = sel_v + warp * k_max;
+  int* my_e = sel_e + warp * k_max;
+  const int nper = Epad / 32;
+  for (int tl = warp; tl < kRouteTok; tl += kWarps) {
+    const int t = t0 + tl;
+    if (t >= T) break;
+    int kt = k_per_token != nullptr ? k_per_token[t] : k_uniform;
+    if (kt < 1 || kt > k_max) {
+      if (lane == 0) flag(SEMMOE_DEVERR_K);
+      kt = kt < 1 ? 1 : k_max;
+    }
+    float v[kRouteMaxE / 32];
+#pragma unroll
+    for (int i = 0; i < kRouteMaxE / 32; ++i) {
+      float val = -INFINITY;
+      int e = lane + 32 * i;
+      if (i < nper && e < E) {
+        val = lg[tl * Epad + e];
+        if (!isfinite(val)) {
+          flag(SEMMOE_DEVERR_NONFINITE);
+          val = -INFINITY;
+        }
+      }
+      v[i] = val;
+    }
+    unsigned taken = 0;
+    for (int j = 0; j < kt; ++j) {
+      float bv = -INFINITY;
+      int be = 0x7fffffff;
+#pragma unroll
+      for (int i = 0; i < kRouteMaxE / 32; ++i) {
+        int e = lane + 32 * i;
+        if (i < nper && e < E && !((taken >> i) & 1u)) {
+          if (v[i] > bv || (v[i] == bv && e < be)) { bv = v[i]; be = e; }
+        }
+      }
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) {
+        float ov = __shfl_xor_sync(0xffffffffu, bv, off);
+        int oe = __shfl_xor_sync(0xffffffffu, be, off);
+        if (ov > bv || (ov == bv && oe < be)) { bv = ov; be = oe; }
+      }
+      if (be >= E) {  // only when fewer than kt finite candidates exist
+        if (lane == 0) flag(SEMMOE_DEVERR_NONFINITE);
+        be = -1;
+      } else if ((be & 31) == lane) {
+        taken |= 1u << (be >> 5);
+      }
+      if (lane == 0) { my_v[j] = bv; my_e[j] = be; }
+    }
+    __syncwarp();
+    // gates: softmax over the selected logits, renormalised (fp32)
+    const float m = my_v[0];
+    float part = 0.f;
+    for (int j = lane; j < kt; j += 32) part += (my_e[j] >= 0) ? expf(my_v[j] - m) : 0.f;
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) part += __shfl_xor_sync(0xffffffffu, part, off);
+    const float inv_den = part;
+    for (int j = lane; j < k_max; j += 32) {
+      int e = -1;
+      float g = 0.f;
+      if (j < kt && my_e[j] >= 0) {
+        e = my_e[j];
+        g = expf(my_v[j] - m) / inv_den;
+      }
+      topk_idx[(size_t)t * k_max + j] = e;
+      topk_w[(size_t)t * k_max + j] = g;
+    }
+    __syncwarp();
+  }
+}
+
+__global__ void affinity_lookup_kernel(const int32_t* __restrict__ ids, const int32_t* __restrict__ lut,
+                                       int V, int R, int T, int32_t* __restrict__ pred) {
+  for (int t = blockIdx.x * blockDim.x + threadIdx.x; t < T; t += gridDim.x * blockDim.x) {
+    int id = ids[t];
+    int r = 0;
+    if (id < 0 || id >= V) {
+      flag(SEMMOE_DEVERR_TOKEN_ID);
+    } else {
+      r = lut[id];
+      if (r < 0 || r >= R) {
+        flag(SEMMOE_DEVERR_LUT);
+        r = 0;
+      }
+    }
+    pred[t] = r;
+  }
+}
+
+constexpr int kMaxR = 64;
+
+__global__ void remote_count_kernel(const int32_t* __restrict__ topk_idx, const int32_t* __restrict__ pred,
+                                    const int32_t* __restrict__ expert_rank, int T, int k_max, int E,
+                                    int R, int32_t* __restrict__ counts) {
+  __shared__ int c[kMaxR * kMaxR];
+  for (int i = threadIdx.x; i < R * R; i += blockDim.x) c[i] = 0;
+  __syncthreads();
+  const long long n = (long long)T * k_max;
+  for (long long p = blockIdx.x * (long long)blockDim.x + threadIdx.x; p < n;
+       p += (long long)gridDim.x * blockDim.x) {
+    int e = topk_idx[p];
+    if (e < 0) continue;
+    if (e >= E) { flag(SEMMOE_DEVERR_EXPERT); continue; }
+    int src = pred[p / k_max];
+    int dst = expert_rank[e];
+    if (src < 0 || src >= R || dst < 0 || dst >= R) { flag(SEMMOE_DEVERR_LUT); continue; }
+    atomicAdd(&c[src * R + dst], 1);
+  }
+  __syncthreads();
+  for (int i = threadIdx.x; i < R * R; i += blockDim.x)
+    if (c[i]) atomicAdd(&counts[i], c[i]);
+}
+
+__global__ void remote_finalize_kernel(const int32_t* __restrict__ counts, int R,
+                                       int32_t* __restrict__ remote) {
+  int src = threadIdx.x;
+  if (src >= R) return;
+  int s = 0;
+  for (int d = 0; d < R; ++d)
+    if (d != src) s += counts[src * R + d];
+  remote[src] = s;
+}
+
+template <typename TX, typename TW>
+cudaError_t launch_route_t(const void* x, const void* w, const float* li, float* lo, const int32_t* kpt,
+                           int ku, int T, int H, int E, int k_max, int32_t* idx, float* wt,
+                           cudaStream_t s) {
+  size_t sm = route_smem_bytes(E, k_max);
+  auto kern = route_kernel<TX, TW>;
+  if (sm > 48 * 1024) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
+    if (e != cudaSuccess) return e;
+  }
+  dim3 grid((T + kRouteTok - 1) / kRouteTok);
+  kern<<<grid, kRouteThreads, sm, s>>>(static_cast<const TX*>(x), static_cast<const TW*>(w), li, lo, kpt,
+                                       ku, T, H, E, k_max, idx, wt);
+  count_launches(1);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+int route_take_errors(cudaStream_t s, int* bits) { return take_error_word(g_err, s, bits); }
+
+cudaError_t launch_route(const void* x, int x_dtype, const void* w, int w_dtype, const float* logits_in,
+                         float* logits_out, const int32_t* kpt, int k_uniform, int T, int H, int E,
+                         int k_max, int32_t* topk_idx, float* topk_w, cudaStream_t s) {
+  if (T == 0) return cudaSuccess;
+  if (logits_in != nullptr)  // x and w unused
+    return launch_route_t<float, float>(nullptr, nullptr, logits_in, logits_out, kpt, k_uniform, T, H, E,
+                                        k_max, topk_idx, topk_w, s);
+  if (x_dtype == SEMMOE_BF16 && w_dtype == SEMMOE_F32)
+    return launch_route_t<__nv_bfloat16, float>(x, w, nullptr, logits_out, kpt, k_uniform, T, H, E, k_max,
+                                                topk_idx, topk_w, s);
+  if (x_dtype == SEMMOE_BF16 && w_dtype == SEMMOE_BF16)
+    return launch_route_t<__nv_bfloat16, __nv_bfloat16>(x, w, nullptr, logits_out, kpt, k_uniform, T, H, E,
+                                                        k_max, topk_idx, topk_w, s);
+  if (x_dtype == SEMMOE_F32 && w_dtype == SEMMOE_F32)
+    return launch_route_t<float, float>(x, w, nullptr, logits_out, kpt, k_uniform, T, H, E, k_max, topk_idx,
+                                        topk_w, s);
+  return launch_route_t<float, __nv_bfloat16>(x, w, nullptr, logits_out, kpt, k_uniform, T, H, E, k_max,
+                                              topk_idx, topk_w, s);
+}
+
+cudaError_t launch_affinity_lookup(const int32_t* ids, const int32_t* lut, int V, int R, int T, int32_t* pred,
+                                   cudaStream_t s) {
+  if (T == 0) return cudaSuccess;
+  int blocks = (T + 255) / 256;
+  if (blocks > 4096) blocks = 4096;
+  affinity_lookup_kernel<<<blocks, 256, 0, s>>>(ids, lut, V, R, T, pred);
+  count_launches(1);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_remote_count(const int32_t* topk_idx, const int32_t* pred, const int32_t* expert_rank, int T,
+                                int k_max, int E, int R, int32_t* counts, int32_t* remote, cudaStream_t s) {
+  cudaError_t e = cudaMemsetAsync(counts, 0, sizeof(int32_t) * R * R, s);
+  if (e != cudaSuccess) return e;
+  long long n = (long long)T * k_max;
+  if (n > 0) {
+    long long blocks = (n + 1023) / 1024;
+    if (blocks > 1024) blocks = 1024;
+    remote_count_kernel<<<(int)blocks, 256, 0, s>>>(topk_idx, pred, expert_rank, T, k_max, E, R, counts);
+    count_launches(1);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
+  remote_finalize_kernel<<<1, kMaxR, 0, s>>>(counts, R, remote);
+  count_launches(1);
+  return cudaGetLastError();
+}
+
+}  // namespace semmoe

@@ -1,0 +1,156 @@
+"""One affinity-aware MoE layer forward on one GPU, through the C ABI.
+
+``MoELayer.forward`` enqueues the six library calls on the current stream:
+route -> affinity lookup -> remote count -> permute -> grouped FFN (+ shared
+FFN) -> combine.  Torch only provides device memory and the stream; every
+step runs in the library's kernels, and nothing synchronises the host.
+"""
+from __future__ import annotations
+
+from dataclasses import dataclass
+from typing import Optional
+
+import torch
+
+from . import _abi as abi
+
+
+@dataclass
+class LayerOutput:
+    out: torch.Tensor
+    logits: Optional[torch.Tensor]
+    topk_idx: torch.Tensor
+    topk_w: torch.Tensor
+    pred_rank: torch.Tensor
+    counts: torch.Tensor
+    remote: torch.Tensor
+    expert_offsets: torch.Tensor
+    rank_offsets: torch.Tensor
+    phys_to_expert: torch.Tensor
+    expert_counts: torch.Tensor
+    sorted_to_pair: torch.Tensor
+    pair_to_sorted: torch.Tensor
+    x_perm: torch.Tensor
+    y_perm: torch.Tensor
+    y_shared: Optional[torch.Tensor]
+
+
+class MoELayer:
+    """Weights and tables of one MoE layer, resident on a CUDA device.
+
+    w_router [E,H] (fp32 or bf16), w13 [E,2I,H], w2 [E,H,I] (activation type),
+    expert_rank [E] and lut [V] int32, R logical ranks, k_max the largest budget;
+    ws13 [2*I_s,H] / ws2 [H,I_s] optional shared experts.
+    """
+
+    def __init__(self, w_router, w13, w2, expert_rank, lut, R: int, k_max: int, ws13=None, ws2=None,
+                 device="cuda"):
+        dev = torch.device(device)
+        c = lambda t: None if t is None else t.to(dev).contiguous()  # noqa: E731
+        self.w_router, self.w13, self.w2 = c(w_router), c(w13), c(w2)
+        self.expert_rank = c(expert_rank).to(torch.int32)
+        self.lut = c(lut).to(torch.int32)
+        self.ws13, self.ws2 = c(ws13), c(ws2)
+        self.E, twoI, self.H = self.w13.shape
+        self.I = twoI // 2
+        self.I_s = 0 if ws13 is None else self.ws13.shape[0] // 2
+        self.R, self.k_max, self.V = R, k_max, self.lut.shape[0]
+        self.dtype = self.w13.dtype
+        self.device = dev
+        self._ws = {}
+
+    def _workspace(self, key, nbytes):
+        buf = self._ws.get(key)
+        if buf is None or buf.numel() < nbytes:
+            buf = torch.empty(max(nbytes, 256), dtype=torch.uint8, device=self.device)
+            self._ws[key] = buf
+        return buf
+
+    def forward(self, x, token_ids, k_per_token=None, k: Optional[int] = None, P: Optional[int] = None,
+                logits_in=None, keep_logits: bool = False, stream=None, marks=None) -> LayerOutput:
+        """x [T,H] (activation type) and token_ids [T] int32 on the device.
+
+        Budgets: ``k`` for every token, or ``k_per_token`` [T] int32 on the device
+        together with ``P`` = its sum (known to the caller, so no host sync).
+        ``marks``: optional list; a CUDA event is recorded on the stream after
+        each step and appended as (step name, event), for per-step timing.
+        """
+        s = torch.cuda.current_stream() if stream is None else stream
+
+        def mark(name):
+            if marks is not None:
+                ev = torch.cuda.Event(enable_timing=True)
+                ev.record(s)
+                marks.append((name, ev))
+
+        mark("start")
+        T = x.shape[0]
+        H, E, I, R, k_max = self.H, self.E, self.I, self.R, self.k_max
+        dev = self.device
+        if k_per_token is None:
+            if k is None:
+                raise ValueError("give k or k_per_token")
+            P = T * k
+        elif P is None:
+            raise ValueError("k_per_token needs P = sum(k_per_token)")
+        i32 = dict(dtype=torch.int32, device=dev)
+        logits = torch.empty(T, E, dtype=torch.float32, device=dev) if keep_logits else None
+        topk_idx = torch.empty(T, k_max, **i32)
+        topk_w = torch.empty(T, k_max, dtype=torch.float32, device=dev)
+        abi.semmoe_route(x, self.w_router, logits_in, logits, k_per_token, k or 0, T, H, E, k_max,
+                         topk_idx, topk_w, stream)
+        mark("route")
+        pred = torch.empty(T, **i32)
+        abi.semmoe_affinity_lookup(token_ids, self.lut, self.V, R, T, pred, stream)
+        counts = torch.empty(R, R, **i32)
+        remote = torch.empty(R, **i32)
+        abi.semmoe_remote_count(topk_idx, pred, self.expert_rank, T, k_max, E, R, counts, remote, stream)
+        mark("lookup_count")
+        expert_offsets = torch.empty(E + 1, **i32)
+        rank_offsets = torch.empty(R + 1, **i32)
+        phys_to_expert = torch.empty(E, **i32)
+        expert_counts = torch.empty(E, **i32)
+        sorted_to_pair = torch.empty(max(P, 1), **i32)
+        pair_to_sorted = torch.empty(T * k_max, **i32)
+        x_perm = torch.empty(P, H, dtype=x.dtype, device=dev)
+        ws = self._workspace("permute", abi.semmoe_permute_workspace_size(T, k_max, E))
+        abi.semmoe_permute(topk_idx, self.expert_rank, x, T, H, E, R, k_max, P, expert_offsets,
+                           rank_offsets, phys_to_expert, expert_counts, sorted_to_pair, pair_to_sorted,
+                           x_perm, ws, stream)
+        mark("permute")
+        y_perm = torch.empty(P, H, dtype=x.dtype, device=dev)
+        dcode = abi.dtype_code(self.w13)
+        ws = self._workspace("ffn", abi.semmoe_grouped_ffn_workspace_size(P, I, dcode))
+        abi.semmoe_grouped_ffn(x_perm, expert_offsets, phys_to_expert, self.w13, self.w2, P, E, H, I,
+                               y_perm, ws, stream)
+        mark("grouped_ffn")
+        y_shared = None
+        if self.ws13 is not None:
+            y_shared = torch.empty(T, H, dtype=x.dtype, device=dev)
+            ws = self._workspace("shared", abi.semmoe_shared_ffn_workspace_size(T, self.I_s, dcode))
+            abi.semmoe_shared_ffn(x, self.ws13, self.ws2, T, H, self.I_s, y_shared, ws, stream)
+            mark("shared_ffn")
+        out = torch.empty(T, H, dtype=x.dtype, device=dev)
+        abi.semmoe_combine(y_perm, pair_to_sorted, topk_w, y_shared, T, H, k_max, P, out, stream)
+        mark("combine")
+        return LayerOutput(out, logits, topk_idx, topk_w, pred, counts, remote, expert_offsets,
+                           rank_offsets, phys_to_expert, expert_counts, sorted_to_pair[:P],
+                           pair_to_sorted, x_perm, y_perm, y_shared)
+
+    def forward_host(self, x_host, ids_host, k_host=None, k: Optional[int] = None, out_host=None,
+                     stream=None) -> torch.Tensor:
+        """End-to-end call on host tensors (ideally pinned): copy the inputs in,
+        run the layer, copy ``out`` back.  Returns the host output tensor."""
+        s = torch.cuda.current_stream() if stream is None else stream
+        with torch.cuda.stream(s):
+            x = x_host.to(self.device, non_blocking=True)
+            ids = ids_host.to(self.device, non_blocking=True)
+            kpt, P = None, None
+            if k_host is not None:
+                kpt = k_host.to(self.device, non_blocking=True)
+                P = int(k_host.sum())
+            res = self.forward(x, ids, kpt, k, P, stream=s)
+            if out_host is None:
+                out_host = torch.empty(res.out.shape, dtype=res.out.dtype, pin_memory=True)
+            out_host.copy_(res.out, non_blocking=True)
+        return out_host
