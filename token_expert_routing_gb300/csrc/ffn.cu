@@ -1,5 +1,9 @@
-// Grouped-FFN dispatch: fp32 runs on CUDA cores (ffn_simt.cu); bf16 runs on
-// the tensor cores (ffn_tc.cu).
+// Grouped-FFN dispatch: bf16 runs on the tensor cores (ffn_tc.cu); fp32 runs
+// on CUDA cores (ffn_simt.cu).  Setting SEMMOE_FFN_IMPL=simt in the
+// environment runs bf16 on the CUDA-core kernel as well (a slow cross-check).
+#include <stdlib.h>
+#include <string.h>
+
 #include "common.cuh"
 #include "internal.h"
 
@@ -8,9 +12,15 @@ namespace semmoe {
 cudaError_t launch_ffn_simt(const void* x, const int32_t* offsets, const int32_t* p2e, const void* w13,
                             const void* w2, int dtype, int P, int E, int H, int I, void* y, void* ws,
                             cudaStream_t s);
+cudaError_t launch_ffn_tc(const void* x, const int32_t* offsets, const int32_t* p2e, const void* w13,
+                          const void* w2, int P, int E, int H, int I, void* y, void* ws, cudaStream_t s);
 int ffn_simt_take_errors(cudaStream_t s, int* bits);
+int ffn_tc_take_errors(cudaStream_t s, int* bits);
 
-int ffn_take_errors(cudaStream_t s, int* bits) { return ffn_simt_take_errors(s, bits); }
+int ffn_take_errors(cudaStream_t s, int* bits) {
+  if (ffn_simt_take_errors(s, bits)) return -1;
+  return ffn_tc_take_errors(s, bits);
+}
 
 // Workspace: the SwiGLU activation h [P, I] in the activation type.
 size_t ffn_ws_bytes(int P, int I, int dtype) {
@@ -18,9 +28,15 @@ size_t ffn_ws_bytes(int P, int I, int dtype) {
   return align_up((size_t)(P > 0 ? P : 1) * I * es, 256);
 }
 
+static bool force_simt() {
+  const char* v = getenv("SEMMOE_FFN_IMPL");
+  return v != nullptr && strcmp(v, "simt") == 0;
+}
+
 cudaError_t launch_ffn(const void* x, const int32_t* offsets, const int32_t* p2e, const void* w13,
                        const void* w2, int dtype, int P, int E, int H, int I, void* y, void* ws,
                        cudaStream_t s) {
+  if (dtype == SEMMOE_BF16 && !force_simt()) return launch_ffn_tc(x, offsets, p2e, w13, w2, P, E, H, I, y, ws, s);
   return launch_ffn_simt(x, offsets, p2e, w13, w2, dtype, P, E, H, I, y, ws, s);
 }
 
