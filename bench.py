@@ -260,23 +260,27 @@ def run_ours(args, world, rank, local):
     stage_avg = {n: sum(v) / len(v) for n, v in stage_ms.items()}
 
     # end to end through the public API: pinned host inputs in, host output back
-    x_h = d["x"].pin_memory()
-    ids_h = d["token_ids"].pin_memory()
-    k_h = d["k_per_token"].pin_memory() if per_token else None
-    out_h = torch.empty(spec.T, spec.H, dtype=d["x"].dtype).pin_memory()
-    for _ in range(args.warmup):
-        layer.forward_host(x_h, ids_h, k_h, k, out_h, stream=stream)
-    _barrier(world)
-    torch.cuda.synchronize(dev)
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for _ in range(args.steps):
-        layer.forward_host(x_h, ids_h, k_h, k, out_h, stream=stream)
-    e1.record(stream)
-    torch.cuda.synchronize(dev)
-    e2e_ms = _max_over_ranks(world, e0.elapsed_time(e1))
-    h2d = x_h.numel() * x_h.element_size() + ids_h.numel() * 4 + (k_h.numel() * 4 if per_token else 0)
-    d2h = out_h.numel() * out_h.element_size()
+    e2e = None
+    if not args.no_e2e:
+        x_h = d["x"].pin_memory()
+        ids_h = d["token_ids"].pin_memory()
+        k_h = d["k_per_token"].pin_memory() if per_token else None
+        out_h = torch.empty(spec.T, spec.H, dtype=d["x"].dtype).pin_memory()
+        for _ in range(args.warmup):
+            layer.forward_host(x_h, ids_h, k_h, k, out_h, stream=stream)
+        _barrier(world)
+        torch.cuda.synchronize(dev)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(args.steps):
+            layer.forward_host(x_h, ids_h, k_h, k, out_h, stream=stream)
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        e2e_ms = _max_over_ranks(world, e0.elapsed_time(e1))
+        h2d = x_h.numel() * x_h.element_size() + ids_h.numel() * 4 + (k_h.numel() * 4 if per_token else 0)
+        d2h = out_h.numel() * out_h.element_size()
+        e2e = {"value": spec.T * args.steps * world / (e2e_ms * 1e-3), "unit": "tokens/s",
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
 
     if rank != 0:
         return
@@ -316,8 +320,7 @@ def run_ours(args, world, rank, local):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_max / args.steps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": spec.dtype,
         "data": "synthetic", "config": _config(spec),
-        "e2e": {"value": total_tokens / (e2e_ms * 1e-3), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": d2h},
+        "e2e": e2e,
         "gpu_launches": launches,
         "roofline": roofline,
         "stages": stages,
@@ -343,6 +346,7 @@ def main():
     ap.add_argument("--cpu-tokens", type=int, default=4096,
                     help="tokens of the one-pass CPU oracle baseline (capped at T)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true", help="skip the end-to-end (host buffers) timing")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)   # at least 3 untimed warm-up steps
     world, rank, local = _dist()
