@@ -187,6 +187,35 @@ int semmoe_permute(const int32_t* topk_idx, const int32_t* expert_rank,
                    void* x_perm, void* ws, size_t ws_bytes, void* stream);
 
 /*
+ * semmoe_permute_noalloc -- semmoe_permute for callers that cannot allocate
+ * device memory.  The pages have no counterpart of this call: it exists for
+ * callers that own no allocator, such as a plugin inside a host engine that
+ * manages every byte of device memory itself and gives the plugin no
+ * allocation hook, or a latency-critical serving loop that forbids cudaMalloc
+ * after start-up because it can synchronise the whole device.
+ *
+ * Same arguments, outputs and errors as semmoe_permute, minus the workspace:
+ * the scratch (per-chunk bucket counts, ceil(T*k_max / 2048) * E * 4 bytes)
+ * lives in a static 1 MiB device array compiled into the library, which every
+ * GPU that loads the library holds until the process exits.  Sizes whose
+ * scratch exceeds 1 MiB are rejected with SEMMOE_ERR_INVALID_ARG (use
+ * semmoe_permute with a workspace instead).  The call makes no cudaMalloc,
+ * cudaFree or other allocating call.
+ *
+ * The first call on each device looks up the array's device address (once,
+ * with that device current) and caches it; make that first call before any
+ * stream capture.  All calls share the one array and it keeps the last call's
+ * contents (the kernels overwrite whatever they read), so two calls that
+ * overlap on the GPU -- on different streams, or from different threads --
+ * race on it; order them on one stream.
+ */
+int semmoe_permute_noalloc(const int32_t* topk_idx, const int32_t* expert_rank,
+                           const void* x, int dtype, int T, int H, int E, int R, int k_max, int P,
+                           int32_t* expert_offsets, int32_t* rank_offsets, int32_t* phys_to_expert,
+                           int32_t* expert_counts, int32_t* sorted_to_pair, int32_t* pair_to_sorted,
+                           void* x_perm, void* stream);
+
+/*
  * semmoe_grouped_ffn -- SwiGLU expert FFN over the sorted rows.
  *
  * The activated experts' computation ([SP] ko §1; [MP] §2 A: an expert is a

@@ -35,6 +35,8 @@ SIGNATURES = {
     "semmoe_permute_workspace_size": (_sz, [_i, _i, _i]),
     "semmoe_permute": (_i, [_vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _i, _vp, _vp, _vp, _vp, _vp, _vp,
                             _vp, _vp, _sz, _vp]),
+    "semmoe_permute_noalloc": (_i, [_vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _i, _vp, _vp, _vp, _vp, _vp,
+                                    _vp, _vp, _vp]),
     "semmoe_grouped_ffn_workspace_size": (_sz, [_i, _i, _i]),
     "semmoe_grouped_ffn": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _vp, _vp, _sz, _vp]),
     "semmoe_shared_ffn_workspace_size": (_sz, [_i, _i, _i]),
@@ -149,6 +151,18 @@ def semmoe_permute(topk_idx, expert_rank, x, T, H, E, R, k_max, P, expert_offset
                                 _p(expert_offsets), _p(rank_offsets), _p(phys_to_expert),
                                 _p(expert_counts), _p(sorted_to_pair), _p(pair_to_sorted), _p(x_perm),
                                 _p(ws), ws.numel() * ws.element_size(), _stream(stream)))
+
+
+def semmoe_permute_noalloc(topk_idx, expert_rank, x, T, H, E, R, k_max, P, expert_offsets, rank_offsets,
+                           phys_to_expert, expert_counts, sorted_to_pair, pair_to_sorted, x_perm,
+                           stream=None):
+    """semmoe_permute without a workspace: for callers that cannot allocate
+    device memory (the scratch is a static 1 MiB array inside the library)."""
+    d = dtype_code(x) if x is not None else SEMMOE_F32
+    _check(lib().semmoe_permute_noalloc(_p(topk_idx), _p(expert_rank), _p(x), d, T, H, E, R, k_max, P,
+                                        _p(expert_offsets), _p(rank_offsets), _p(phys_to_expert),
+                                        _p(expert_counts), _p(sorted_to_pair), _p(pair_to_sorted),
+                                        _p(x_perm), _stream(stream)))
 
 
 def semmoe_grouped_ffn_workspace_size(P, I, dtype: int) -> int:

@@ -172,6 +172,39 @@ int semmoe_permute(const int32_t* topk_idx, const int32_t* expert_rank, const vo
                      "semmoe_permute");
 }
 
+int semmoe_permute_noalloc(const int32_t* topk_idx, const int32_t* expert_rank, const void* x, int dtype, int T,
+                           int H, int E, int R, int k_max, int P, int32_t* expert_offsets, int32_t* rank_offsets,
+                           int32_t* phys_to_expert, int32_t* expert_counts, int32_t* sorted_to_pair,
+                           int32_t* pair_to_sorted, void* x_perm, void* stream) {
+  REQUIRE(T >= 0, "semmoe_permute_noalloc: T = %d < 0", T);
+  REQUIRE(E >= 1 && E <= 256, "semmoe_permute_noalloc: E = %d outside [1, 256]", E);
+  REQUIRE(R >= 1 && R <= E, "semmoe_permute_noalloc: R = %d outside [1, E]", R);
+  REQUIRE(k_max >= 1 && k_max <= E, "semmoe_permute_noalloc: k_max = %d outside [1, E]", k_max);
+  REQUIRE((long long)T * k_max < (1LL << 31), "semmoe_permute_noalloc: T * k_max too large");
+  REQUIRE(permute_ws_bytes(T, k_max, E) <= permute_noalloc_max_scratch(),
+          "semmoe_permute_noalloc: T=%d, k_max=%d, E=%d need %zu bytes of scratch; the built-in scratch holds "
+          "%zu bytes (use semmoe_permute with a caller workspace)",
+          T, k_max, E, permute_ws_bytes(T, k_max, E), permute_noalloc_max_scratch());
+  REQUIRE(P >= 0 && (long long)P <= (long long)T * k_max, "semmoe_permute_noalloc: P = %d outside [0, T*k_max]", P);
+  REQUIRE(expert_rank && expert_offsets && rank_offsets && phys_to_expert && expert_counts,
+          "semmoe_permute_noalloc: null table pointer");
+  REQUIRE(T == 0 || (topk_idx && pair_to_sorted), "semmoe_permute_noalloc: null topk_idx or pair_to_sorted");
+  REQUIRE(P == 0 || sorted_to_pair, "semmoe_permute_noalloc: null sorted_to_pair");
+  REQUIRE((x == nullptr) == (x_perm == nullptr),
+          "semmoe_permute_noalloc: x and x_perm must both be set or both NULL");
+  if (x != nullptr) {
+    REQUIRE(valid_dtype(dtype), "semmoe_permute_noalloc: bad dtype %d", dtype);
+    REQUIRE(H >= 1 && (H * elem_size(dtype)) % 16 == 0,
+            "semmoe_permute_noalloc: H * elem size must be a multiple of 16");
+    REQUIRE(aligned(x, 16) && aligned(x_perm, 16), "semmoe_permute_noalloc: x / x_perm not 16-byte aligned");
+  }
+  CHECK_DEVICE("semmoe_permute_noalloc");
+  return cuda_status(launch_permute_noalloc(topk_idx, expert_rank, x, dtype, T, H, E, R, k_max, P, expert_offsets,
+                                            rank_offsets, phys_to_expert, expert_counts, sorted_to_pair,
+                                            pair_to_sorted, x_perm, static_cast<cudaStream_t>(stream)),
+                     "semmoe_permute_noalloc");
+}
+
 size_t semmoe_grouped_ffn_workspace_size(int P, int I, int dtype) {
   if (P < 0 || I < 1 || !valid_dtype(dtype)) return 0;
   return ffn_ws_bytes(P, I, dtype);

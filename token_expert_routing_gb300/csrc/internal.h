@@ -36,6 +36,14 @@ cudaError_t launch_permute(const int32_t* topk_idx, const int32_t* expert_rank, 
                            int32_t* sorted_to_pair, int32_t* pair_to_sorted, void* x_perm,
                            void* ws, cudaStream_t s);
 
+// semmoe_permute with its scratch in a static device array (no allocation).
+size_t permute_noalloc_max_scratch();
+cudaError_t launch_permute_noalloc(const int32_t* topk_idx, const int32_t* expert_rank, const void* x,
+                                   int dtype, int T, int H, int E, int R, int k_max, int P,
+                                   int32_t* expert_offsets, int32_t* rank_offsets, int32_t* phys_to_expert,
+                                   int32_t* expert_counts, int32_t* sorted_to_pair, int32_t* pair_to_sorted,
+                                   void* x_perm, cudaStream_t s);
+
 size_t ffn_ws_bytes(int P, int I, int dtype);
 // offsets == nullptr: one group of rows [0, P) using expert 0 of w13/w2.
 cudaError_t launch_ffn(const void* x, const int32_t* offsets, const int32_t* phys_to_expert,

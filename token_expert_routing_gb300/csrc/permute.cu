@@ -12,8 +12,16 @@
 //                    match + per-warp bucket counts) and writes both maps
 // then perm_gather copies x rows into sorted order (one warp per row,
 // 16-byte vectors).
+#include <mutex>
+
 #include "common.cuh"
 #include "internal.h"
+
+// Scratch of semmoe_permute_noalloc: the per-chunk bucket counts live in this
+// file-scope device array instead of a caller workspace.  Every GPU that loads
+// the library holds it until the process exits.
+static constexpr size_t kNoAllocScratchBytes = 1u << 20;  // 1 MiB
+static __device__ __align__(256) int32_t g_noalloc_scratch[kNoAllocScratchBytes / sizeof(int32_t)];
 
 namespace semmoe {
 namespace {
@@ -229,6 +237,42 @@ cudaError_t launch_permute(const int32_t* topk_idx, const int32_t* expert_rank, 
     count_launches(1);
   }
   return cudaGetLastError();
+}
+
+size_t permute_noalloc_max_scratch() { return kNoAllocScratchBytes; }
+
+// Device address of g_noalloc_scratch on the current device.  In host code the
+// array's name is only a host-side stand-in, so the address is looked up once
+// per device (with that device current) and cached.
+static cudaError_t noalloc_scratch_address(void** out) {
+  static std::mutex mu;
+  static void* addr[64] = {};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lock(mu);
+  if (addr[dev] == nullptr) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+    if (e != cudaSuccess) return e;
+    addr[dev] = p;
+  }
+  *out = addr[dev];
+  return cudaSuccess;
+}
+
+cudaError_t launch_permute_noalloc(const int32_t* topk_idx, const int32_t* expert_rank, const void* x, int dtype,
+                                   int T, int H, int E, int R, int k_max, int P, int32_t* expert_offsets,
+                                   int32_t* rank_offsets, int32_t* phys_to_expert, int32_t* expert_counts,
+                                   int32_t* sorted_to_pair, int32_t* pair_to_sorted, void* x_perm, cudaStream_t s) {
+  void* scratch = nullptr;
+  cudaError_t e = noalloc_scratch_address(&scratch);
+  if (e != cudaSuccess) return e;
+  // The kernels overwrite every scratch entry they later read (the zero-pair
+  // case clears its one row), so stale contents of an earlier call never leak.
+  return launch_permute(topk_idx, expert_rank, x, dtype, T, H, E, R, k_max, P, expert_offsets, rank_offsets,
+                        phys_to_expert, expert_counts, sorted_to_pair, pair_to_sorted, x_perm, scratch, s);
 }
 
 }  // namespace semmoe
