@@ -104,8 +104,8 @@ int semmoe_check_errors(void* stream, int* bits);
  *   gates: w[t,j] = exp(l_j - m) / sum_{i<k_t} exp(l_i - m),  m = max selected
  *   (the fp32 softmax renormalised over the selected experts)
  *
- * x          [device] [T,H], x_dtype (SEMMOE_F32 or SEMMOE_BF16)
- * w_router   [device] [E,H], w_dtype (SEMMOE_F32 or SEMMOE_BF16)
+ * x          [device] [T,H], x_dtype (SEMMOE_F32 or SEMMOE_BF16), 16-byte aligned
+ * w_router   [device] [E,H], w_dtype (SEMMOE_F32 or SEMMOE_BF16), 16-byte aligned
  * logits_in  [device] [T,E] fp32 or NULL.  If set, x and w_router are not
  *            read (may be NULL) and these logits are routed as given.
  * logits_out [device] [T,E] fp32 or NULL: receives the logits used.
@@ -113,13 +113,21 @@ int semmoe_check_errors(void* stream, int* bits);
  * k_uniform  budget of every token when k_per_token is NULL (1..k_max).
  * topk_idx   [device] [T,k_max] int32 out: slot j < k_t = expert, else -1.
  * topk_w     [device] [T,k_max] fp32 out: gates, 0 in padding slots.
+ * ws         [device] workspace of semmoe_route_workspace_size() bytes (may be
+ *            NULL when that size is 256, i.e. the CUDA-core path).
  * Limits: 1 <= k_max <= E <= 256; T >= 0 (T = 0 enqueues nothing).
+ *
+ * bf16 activations (H % 8 == 0) run the GEMM on the tensor cores; an fp32
+ * router weight is then split exactly into three bf16 parts (hi + mid + lo)
+ * whose products with the bf16 activations are exact, summed in fp32.  fp32
+ * activations run a CUDA-core fp32 GEMM fused with the top-k.
  */
+size_t semmoe_route_workspace_size(int T, int H, int E, int x_dtype, int w_dtype);
 int semmoe_route(const void* x, int x_dtype, const void* w_router, int w_dtype,
                  const float* logits_in, float* logits_out,
                  const int32_t* k_per_token, int k_uniform,
                  int T, int H, int E, int k_max,
-                 int32_t* topk_idx, float* topk_w, void* stream);
+                 int32_t* topk_idx, float* topk_w, void* ws, size_t ws_bytes, void* stream);
 
 /*
  * semmoe_affinity_lookup -- predicted logical rank of each token from its id.

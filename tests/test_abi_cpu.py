@@ -50,21 +50,21 @@ def _err(lib):
 
 def test_route_validation(lib):
     # E outside [1, 256]
-    rc = lib.semmoe_route(None, 1, None, 0, None, None, None, 2, 16, 64, 0, 2, None, None, None)
+    rc = lib.semmoe_route(None, 1, None, 0, None, None, None, 2, 16, 64, 0, 2, None, None, None, 0, None)
     assert rc == 1 and "E" in _err(lib)
-    rc = lib.semmoe_route(None, 1, None, 0, None, None, None, 2, 16, 64, 300, 2, None, None, None)
+    rc = lib.semmoe_route(None, 1, None, 0, None, None, None, 2, 16, 64, 300, 2, None, None, None, 0, None)
     assert rc == 1
     # k_max > E
-    rc = lib.semmoe_route(None, 1, None, 0, None, None, None, 2, 16, 64, 8, 9, None, None, None)
+    rc = lib.semmoe_route(None, 1, None, 0, None, None, None, 2, 16, 64, 8, 9, None, None, None, 0, None)
     assert rc == 1 and "k_max" in _err(lib)
     # k_uniform outside [1, k_max]
-    rc = lib.semmoe_route(None, 1, None, 0, None, None, None, 0, 16, 64, 8, 2, None, None, None)
+    rc = lib.semmoe_route(None, 1, None, 0, None, None, None, 0, 16, 64, 8, 2, None, None, None, 0, None)
     assert rc == 1 and "k_uniform" in _err(lib)
     # null outputs
-    rc = lib.semmoe_route(None, 1, None, 0, None, None, None, 2, 16, 64, 8, 2, None, None, None)
+    rc = lib.semmoe_route(None, 1, None, 0, None, None, None, 2, 16, 64, 8, 2, None, None, None, 0, None)
     assert rc == 1 and "null" in _err(lib)
     # T = 0 is a no-op
-    assert lib.semmoe_route(None, 1, None, 0, None, None, None, 2, 0, 64, 8, 2, None, None, None) == 0
+    assert lib.semmoe_route(None, 1, None, 0, None, None, None, 2, 0, 64, 8, 2, None, None, None, 0, None) == 0
 
 
 def test_permute_validation(lib):

@@ -29,7 +29,8 @@ SIGNATURES = {
     "semmoe_version": (_i, []),
     "semmoe_kernel_launches": (ctypes.c_ulonglong, []),
     "semmoe_check_errors": (_i, [_vp, ctypes.POINTER(_i)]),
-    "semmoe_route": (_i, [_vp, _i, _vp, _i, _vp, _vp, _vp, _i, _i, _i, _i, _i, _vp, _vp, _vp]),
+    "semmoe_route_workspace_size": (_sz, [_i, _i, _i, _i, _i]),
+    "semmoe_route": (_i, [_vp, _i, _vp, _i, _vp, _vp, _vp, _i, _i, _i, _i, _i, _vp, _vp, _vp, _sz, _vp]),
     "semmoe_affinity_lookup": (_i, [_vp, _vp, _i, _i, _i, _vp, _vp]),
     "semmoe_remote_count": (_i, [_vp, _vp, _vp, _i, _i, _i, _i, _vp, _vp, _vp]),
     "semmoe_permute_workspace_size": (_sz, [_i, _i, _i]),
@@ -121,13 +122,22 @@ def semmoe_check_errors(stream=None) -> int:
     return bits.value
 
 
+def semmoe_route_workspace_size(T, H, E, x_dtype: int, w_dtype: int) -> int:
+    return lib().semmoe_route_workspace_size(T, H, E, x_dtype, w_dtype)
+
+
 def semmoe_route(x, w_router, logits_in, logits_out, k_per_token, k_uniform, T, H, E, k_max,
-                 topk_idx, topk_w, stream=None):
+                 topk_idx, topk_w, ws=None, stream=None):
+    """Router GEMM + top-k.  ``ws`` defaults to a fresh workspace of the size
+    the library asks for (pass one to avoid the allocation)."""
     xd = dtype_code(x) if x is not None else SEMMOE_F32
     wd = dtype_code(w_router) if w_router is not None else SEMMOE_F32
+    if ws is None:
+        n = semmoe_route_workspace_size(T, max(H, 1), E, xd, wd)
+        ws = torch.empty(n, dtype=torch.uint8, device=topk_idx.device)
     _check(lib().semmoe_route(_p(x), xd, _p(w_router), wd, _p(logits_in), _p(logits_out),
                               _p(k_per_token), k_uniform, T, H, E, k_max, _p(topk_idx), _p(topk_w),
-                              _stream(stream)))
+                              _p(ws), ws.numel() * ws.element_size(), _stream(stream)))
 
 
 def semmoe_affinity_lookup(token_ids, lut, V, R, T, pred_rank, stream=None):

@@ -85,9 +85,15 @@ int semmoe_check_errors(void* stream, int* bits) {
   return SEMMOE_OK;
 }
 
+size_t semmoe_route_workspace_size(int T, int H, int E, int x_dtype, int w_dtype) {
+  if (T < 0 || H < 1 || E < 1 || !valid_dtype(x_dtype) || !valid_dtype(w_dtype)) return 0;
+  const size_t b = route_ws_bytes(T, H, E, x_dtype, w_dtype);
+  return b > 0 ? b : 256;
+}
+
 int semmoe_route(const void* x, int x_dtype, const void* w_router, int w_dtype, const float* logits_in,
                  float* logits_out, const int32_t* k_per_token, int k_uniform, int T, int H, int E, int k_max,
-                 int32_t* topk_idx, float* topk_w, void* stream) {
+                 int32_t* topk_idx, float* topk_w, void* ws, size_t ws_bytes, void* stream) {
   REQUIRE(T >= 0, "semmoe_route: T = %d < 0", T);
   REQUIRE(E >= 1 && E <= 256, "semmoe_route: E = %d outside [1, 256]", E);
   REQUIRE(k_max >= 1 && k_max <= E, "semmoe_route: k_max = %d outside [1, E = %d]", k_max, E);
@@ -100,8 +106,10 @@ int semmoe_route(const void* x, int x_dtype, const void* w_router, int w_dtype, 
     REQUIRE(x != nullptr && w_router != nullptr, "semmoe_route: null x or w_router without logits_in");
     REQUIRE(valid_dtype(x_dtype) && valid_dtype(w_dtype), "semmoe_route: bad dtype (%d, %d)", x_dtype, w_dtype);
     REQUIRE(H >= 1, "semmoe_route: H = %d < 1", H);
-    REQUIRE(aligned(x, elem_size(x_dtype)) && aligned(w_router, elem_size(w_dtype)),
-            "semmoe_route: misaligned x or w_router");
+    REQUIRE(aligned(x, 16) && aligned(w_router, 16), "semmoe_route: x and w_router must be 16-byte aligned");
+    const size_t need = route_ws_bytes(T, H, E, x_dtype, w_dtype);
+    REQUIRE(need == 0 || (ws != nullptr && aligned(ws, 256) && ws_bytes >= need),
+            "semmoe_route: workspace null, not 256-byte aligned or below %zu bytes", need);
   } else {
     REQUIRE(aligned(logits_in, 4), "semmoe_route: misaligned logits_in");
   }
@@ -109,7 +117,7 @@ int semmoe_route(const void* x, int x_dtype, const void* w_router, int w_dtype, 
           "semmoe_route: misaligned output or k_per_token");
   CHECK_DEVICE("semmoe_route");
   return cuda_status(launch_route(x, x_dtype, w_router, w_dtype, logits_in, logits_out, k_per_token, k_uniform, T,
-                                  H, E, k_max, topk_idx, topk_w, static_cast<cudaStream_t>(stream)),
+                                  H, E, k_max, topk_idx, topk_w, ws, static_cast<cudaStream_t>(stream)),
                      "semmoe_route");
 }
 

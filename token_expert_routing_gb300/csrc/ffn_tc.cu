@@ -22,14 +22,14 @@
 // bit of the device error word and an abort flag, after which every role
 // stops, in-flight TMA loads and MMAs are drained (again with a bound), and
 // TMEM is freed before the CTA exits.
-#include <cuda.h>
-#include <cudaTypedefs.h>
-
 #include "common.cuh"
 #include "internal.h"
+#include "tc_common.cuh"
 
 namespace semmoe {
 namespace {
+
+using namespace tc;
 
 __device__ int g_err;
 
@@ -45,7 +45,6 @@ constexpr int THREADS = 192;
 constexpr uint32_t ACC_COLS = 256;      // fp32 accumulator columns per buffer
 constexpr uint32_t TMEM_COLS = 512;     // two buffers: all of TMEM
 constexpr int MAX_GROUPS = 256;
-constexpr uint64_t kWaitNs = 2000000000ull;  // bound on any single wait: 2 s
 
 struct Shared {
   uint64_t full[STAGES], empty[STAGES], tfull[2], tempty[2], done;
@@ -59,142 +58,7 @@ struct Shared {
 
 constexpr size_t kSmemBytes = 1024 + (size_t)STAGES * STAGE_BYTES + sizeof(Shared);
 
-// Instruction descriptor, kind::f16: D fp32 (bits 4-5 = 1), A bf16 (bits 7-9 = 1),
-// B bf16 (bits 10-12 = 1), both K-major (bits 15, 16 = 0), N >> 3 at bits 17-22,
-// M >> 4 at bits 24-28.
-constexpr uint32_t kIdesc = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(BN >> 3) << 17) |
-                            ((uint32_t)(BM >> 4) << 24);
-
-// ---------------------------------------------------------------------------
-// PTX wrappers
-// ---------------------------------------------------------------------------
-__device__ __forceinline__ uint32_t smem_u32(const void* p) {
-  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
-}
-
-__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
-  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
-}
-
-__device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, uint32_t bytes) {
-  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
-               : "memory");
-}
-
-__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
-  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
-}
-
-__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(ok)
-      : "r"(smem_u32(bar)), "r"(parity)
-      : "memory");
-  return ok != 0;
-}
-
-// Wait for the phase of `bar` with parity `parity`.  Returns false when the CTA
-// is aborting (abort flag seen) or the bound ran out (then raises the flag).
-__device__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag) {
-  if (mbar_try_wait(bar, parity)) return true;
-  const uint64_t t0 = globaltimer_ns();
-  while (true) {
-    if (mbar_try_wait(bar, parity)) return true;
-    if (*abort_flag) return false;
-    if (globaltimer_ns() - t0 > kWaitNs) {
-      atomicOr(&g_err, SEMMOE_DEVERR_TIMEOUT);
-      *abort_flag = 1;
-      return false;
-    }
-  }
-}
-
-// Teardown wait: ignores the abort flag, still bounded.
-__device__ void mbar_drain(uint64_t* bar, uint32_t parity) {
-  const uint64_t t0 = globaltimer_ns();
-  while (!mbar_try_wait(bar, parity)) {
-    if (globaltimer_ns() - t0 > kWaitNs) {
-      atomicOr(&g_err, SEMMOE_DEVERR_TIMEOUT);
-      return;
-    }
-  }
-}
-
-__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, uint64_t* bar, int c0, int c1) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4}], [%2];" ::"r"(
-          smem_u32(dst)),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(c0), "r"(c1)
-      : "memory");
-}
-
-__device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, uint64_t* bar, int c0, int c1,
-                                            int c2) {
-  asm volatile(
-      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(
-          smem_u32(dst)),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(c0), "r"(c1), "r"(c2)
-      : "memory");
-}
-
-__device__ __forceinline__ void tma_load_4d(void* dst, const CUtensorMap* map, uint64_t* bar, int c0, int c1,
-                                            int c2, int c3) {
-  asm volatile(
-      "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4, %5, %6}], [%2];" ::"r"(
-          smem_u32(dst)),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(c0), "r"(c1), "r"(c2), "r"(c3)
-      : "memory");
-}
-
-__device__ __forceinline__ void prefetch_map(const CUtensorMap* map) {
-  asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
-}
-
-__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
-__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
-
-// Shared-memory matrix descriptor of a K-major bf16 tile written by TMA with
-// 128-byte swizzling: rows of 128 bytes, 8-row swizzle atoms 1024 bytes apart.
-__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
-  return (uint64_t)((saddr & 0x3FFFFu) >> 4)   // start address >> 4      (bits 0-13)
-         | ((uint64_t)1 << 16)                  // leading byte offset, unused for swizzled K-major
-         | ((uint64_t)(1024 >> 4) << 32)        // stride byte offset >> 4 (bits 32-45)
-         | ((uint64_t)1 << 46)                  // descriptor version      (bits 46-47)
-         | ((uint64_t)2 << 61);                 // swizzle: 128 B          (bits 61-63)
-}
-
-__device__ __forceinline__ void tc_mma(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "l"(adesc), "l"(bdesc), "r"(kIdesc), "r"(accumulate)
-      : "memory");
-}
-
-__device__ __forceinline__ void tc_commit(uint64_t* bar) {
-  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
-               : "memory");
-}
-
-// 32 consecutive fp32 columns of this warp's 32 TMEM lanes (one lane per thread).
-__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
-  asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
-      "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
-      "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
-      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
-        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
-        "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
-        "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
-      : "r"(taddr));
-}
-
-__device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+constexpr uint32_t kIdesc = idesc_bf16_f32(BM, BN);
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
@@ -240,7 +104,7 @@ ffn_tc_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__
     }
     mbar_init(&sh.done, 1);
     sh.abort_flag = 0;
-    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    mbar_init_fence();
     prefetch_map(&map_a);
     prefetch_map(&map_b);
   }
@@ -249,10 +113,7 @@ ffn_tc_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__
   __syncthreads();
 
   if (warp == 1) {  // whole warp: allocate all 512 TMEM columns
-    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(&sh.tmem_base)),
-                 "r"(TMEM_COLS)
-                 : "memory");
-    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    tmem_alloc(&sh.tmem_base, TMEM_COLS);
   }
   if (warp == 0) {  // exclusive prefix of m-tiles per group, 8 groups per lane
     int cnt[8], sum = 0;
@@ -286,9 +147,9 @@ ffn_tc_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__
       sh.total_mtiles = incl;
     }
   }
-  tc_fence_before();
+  fence_before();
   __syncthreads();
-  tc_fence_after();
+  fence_after();
 
   const uint32_t tmem = sh.tmem_base;
   const int total = sh.total_mtiles * n_tiles;
@@ -307,7 +168,7 @@ ffn_tc_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__
         for (int kb = 0; kb < kb_n; ++kb) {
           const int s = it % STAGES;
           const uint32_t ph = (it / STAGES) & 1;
-          if (!mbar_wait(&sh.empty[s], ph ^ 1, abort_flag)) { ok = false; break; }
+          if (!mbar_wait(&sh.empty[s], ph ^ 1, abort_flag, &g_err)) { ok = false; break; }
           mbar_expect_tx(&sh.full[s], STAGE_BYTES);
           tma_load_2d(stage_a + s * A_BYTES, &map_a, &sh.full[s], kb * BK, row0);
           if (GLU) {
@@ -323,7 +184,7 @@ ffn_tc_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__
       }
       if (*abort_flag) {  // no TMA write may still be landing when the CTA exits
         for (uint32_t j = it > (uint32_t)STAGES ? it - STAGES : 0; j < it; ++j)
-          mbar_drain(&sh.full[j % STAGES], (j / STAGES) & 1);
+          mbar_drain(&sh.full[j % STAGES], (j / STAGES) & 1, &g_err);
       }
     }
   } else if (warp == 1) {
@@ -333,28 +194,28 @@ ffn_tc_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__
       for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
         if (*abort_flag) break;
         const uint32_t a = acc_it & 1, aph = (acc_it >> 1) & 1;
-        if (!mbar_wait(&sh.tempty[a], aph ^ 1, abort_flag)) break;
-        tc_fence_after();
+        if (!mbar_wait(&sh.tempty[a], aph ^ 1, abort_flag, &g_err)) break;
+        fence_after();
         const uint32_t d = tmem + a * ACC_COLS;
         bool ok = true;
         for (int kb = 0; kb < kb_n; ++kb) {
           const int s = it % STAGES;
           const uint32_t ph = (it / STAGES) & 1;
-          if (!mbar_wait(&sh.full[s], ph, abort_flag)) { ok = false; break; }
-          tc_fence_after();
+          if (!mbar_wait(&sh.full[s], ph, abort_flag, &g_err)) { ok = false; break; }
+          fence_after();
           const uint32_t sa = smem_u32(stage_a + s * A_BYTES), sb = smem_u32(stage_b + s * B_BYTES);
 #pragma unroll
           for (int k = 0; k < BK / UK; ++k)
-            tc_mma(d, sw128_desc(sa + k * UK * 2), sw128_desc(sb + k * UK * 2), (kb | k) != 0);
-          tc_commit(&sh.empty[s]);  // frees the stage once these MMAs have read it
+            mma_bf16(d, sw128_desc(sa + k * UK * 2), sw128_desc(sb + k * UK * 2), kIdesc, (kb | k) != 0);
+          commit(&sh.empty[s]);  // frees the stage once these MMAs have read it
           ++it;
         }
         if (!ok) break;
-        tc_commit(&sh.tfull[a]);    // accumulator ready for the epilogue
+        commit(&sh.tfull[a]);    // accumulator ready for the epilogue
         ++acc_it;
       }
-      tc_commit(&sh.done);          // every MMA issued above has completed ...
-      mbar_drain(&sh.done, 0);      // ... before TMEM can be released
+      commit(&sh.done);          // every MMA issued above has completed ...
+      mbar_drain(&sh.done, 0, &g_err);      // ... before TMEM can be released
     }
   } else {
     // ---------------- epilogue (warps 2..5) ----------------
@@ -367,10 +228,10 @@ ffn_tc_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__
       decode_mtile(sh, G, mt, row0, rows, e);
       const uint32_t a = acc_it & 1, aph = (acc_it >> 1) & 1;
       int ok = 1;
-      if (lane == 0) ok = mbar_wait(&sh.tfull[a], aph, abort_flag);
+      if (lane == 0) ok = mbar_wait(&sh.tfull[a], aph, abort_flag, &g_err);
       ok = __shfl_sync(0xffffffffu, ok, 0);  // keep the warp converged for tcgen05.ld
       if (!ok) break;
-      tc_fence_after();
+      fence_after();
       const uint32_t t_row = tmem + ((uint32_t)(q * 32) << 16) + a * ACC_COLS;
       const bool row_ok = r < rows;
       __nv_bfloat16* orow = out + (size_t)(row0 + (row_ok ? r : 0)) * N;
@@ -423,55 +284,24 @@ ffn_tc_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__
           }
         }
       }
-      tc_fence_before();
+      fence_before();
       mbar_arrive(&sh.tempty[a]);
       ++acc_it;
     }
   }
 
-  tc_fence_before();
+  fence_before();
   __syncthreads();
   if (warp == 1) {
     __syncwarp();
-    tc_fence_after();
-    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(TMEM_COLS) : "memory");
+    fence_after();
+    tmem_dealloc(tmem, TMEM_COLS);
   }
 }
 
 // ---------------------------------------------------------------------------
 // host side
 // ---------------------------------------------------------------------------
-PFN_cuTensorMapEncodeTiled_v12000 encoder() {
-  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-  if (fn == nullptr) {
-    void* p = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
-            cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
-  }
-  return fn;
-}
-
-// bf16 tensor map with 128-byte swizzle; dims/strides innermost first, strides in bytes.
-bool make_map(CUtensorMap* m, const void* base, int rank, const cuuint64_t* dims, const cuuint64_t* strides,
-              const cuuint32_t* box) {
-  auto enc = encoder();
-  if (enc == nullptr) return false;
-  cuuint32_t estr[4] = {1, 1, 1, 1};
-  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank, const_cast<void*>(base), dims, strides, box, estr,
-                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  return r == CUDA_SUCCESS;
-}
-
-int sm_count() {
-  int dev = 0, n = 148;
-  if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
-  return n;
-}
-
 template <bool GLU>
 cudaError_t launch_one(const CUtensorMap& ma, const CUtensorMap& mb, const int32_t* offsets, const int32_t* p2e,
                        int G, int P, int E, int N, int K, int n_tiles, __nv_bfloat16* out, cudaStream_t s) {
@@ -501,25 +331,25 @@ cudaError_t launch_ffn_tc(const void* x, const int32_t* offsets, const int32_t* 
     const cuuint64_t dims[2] = {(cuuint64_t)H, (cuuint64_t)P};
     const cuuint64_t str[1] = {(cuuint64_t)H * es};
     const cuuint32_t box[2] = {BK, BM};
-    if (!make_map(&ma1, x, 2, dims, str, box)) return cudaErrorInvalidValue;
+    if (!make_map_bf16(&ma1, x, 2, dims, str, box)) return cudaErrorInvalidValue;
   }
   {
     const cuuint64_t dims[4] = {(cuuint64_t)H, (cuuint64_t)I, 2, (cuuint64_t)E};
     const cuuint64_t str[3] = {(cuuint64_t)H * es, (cuuint64_t)I * H * es, (cuuint64_t)2 * I * H * es};
     const cuuint32_t box[4] = {BK, 128, 1, 1};
-    if (!make_map(&mb1, w13, 4, dims, str, box)) return cudaErrorInvalidValue;
+    if (!make_map_bf16(&mb1, w13, 4, dims, str, box)) return cudaErrorInvalidValue;
   }
   {
     const cuuint64_t dims[2] = {(cuuint64_t)I, (cuuint64_t)P};
     const cuuint64_t str[1] = {(cuuint64_t)I * es};
     const cuuint32_t box[2] = {BK, BM};
-    if (!make_map(&ma2, ws, 2, dims, str, box)) return cudaErrorInvalidValue;
+    if (!make_map_bf16(&ma2, ws, 2, dims, str, box)) return cudaErrorInvalidValue;
   }
   {
     const cuuint64_t dims[3] = {(cuuint64_t)I, (cuuint64_t)H, (cuuint64_t)E};
     const cuuint64_t str[2] = {(cuuint64_t)I * es, (cuuint64_t)H * I * es};
     const cuuint32_t box[3] = {BK, BN, 1};
-    if (!make_map(&mb2, w2, 3, dims, str, box)) return cudaErrorInvalidValue;
+    if (!make_map_bf16(&mb2, w2, 3, dims, str, box)) return cudaErrorInvalidValue;
   }
   __nv_bfloat16* h = static_cast<__nv_bfloat16*>(ws);
   cudaError_t e = launch_one<true>(ma1, mb1, offsets, p2e, G, P, E, I, H, (I + 127) / 128, h, s);

@@ -16,10 +16,16 @@ int permute_take_errors(cudaStream_t s, int* bits);
 int ffn_take_errors(cudaStream_t s, int* bits);
 int combine_take_errors(cudaStream_t s, int* bits);
 
+size_t route_ws_bytes(int T, int H, int E, int x_dtype, int w_dtype);
+// Tensor-core router (route_tc.cu): fp32 logits of bf16 activations.
+int route_tc_take_errors(cudaStream_t s, int* bits);
+size_t route_tc_split_bytes(int H, int E, int w_dtype);
+cudaError_t launch_route_logits_tc(const void* x, const void* w, int w_dtype, int T, int H, int E, float* logits,
+                                   void* split, cudaStream_t s);
 cudaError_t launch_route(const void* x, int x_dtype, const void* w, int w_dtype,
                          const float* logits_in, float* logits_out, const int32_t* k_per_token,
                          int k_uniform, int T, int H, int E, int k_max, int32_t* topk_idx,
-                         float* topk_w, cudaStream_t s);
+                         float* topk_w, void* ws, cudaStream_t s);
 
 cudaError_t launch_affinity_lookup(const int32_t* token_ids, const int32_t* lut, int V, int R,
                                    int T, int32_t* pred, cudaStream_t s);

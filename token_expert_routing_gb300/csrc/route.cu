@@ -247,13 +247,35 @@ cudaError_t launch_route_t(const void* x, const void* w, const float* li, float*
 
 }  // namespace
 
-int route_take_errors(cudaStream_t s, int* bits) { return take_error_word(g_err, s, bits); }
+int route_take_errors(cudaStream_t s, int* bits) {
+  if (take_error_word(g_err, s, bits)) return -1;
+  return route_tc_take_errors(s, bits);
+}
+
+// bf16 activations with 16-byte rows take the tensor-core router; the rest the
+// CUDA-core kernel that fuses the GEMM with the top-k.
+static bool route_on_tensor_cores(int x_dtype, int H) { return x_dtype == SEMMOE_BF16 && H % 8 == 0; }
+
+// Workspace: [fp32 logits T x E][three-part bf16 split of an fp32 router weight].
+size_t route_ws_bytes(int T, int H, int E, int x_dtype, int w_dtype) {
+  if (!route_on_tensor_cores(x_dtype, H)) return 0;
+  return align_up((size_t)(T > 0 ? T : 1) * E * sizeof(float), 256) + route_tc_split_bytes(H, E, w_dtype);
+}
 
 cudaError_t launch_route(const void* x, int x_dtype, const void* w, int w_dtype, const float* logits_in,
-                         float* logits_out, const int32_t* kpt, int k_uniform, int T, int H, int E,
-                         int k_max, int32_t* topk_idx, float* topk_w, cudaStream_t s) {
+                         float* logits_out, const int32_t* kpt, int k_uniform, int T, int H, int E, int k_max,
+                         int32_t* topk_idx, float* topk_w, void* ws, cudaStream_t s) {
   if (T == 0) return cudaSuccess;
-  if (logits_in != nullptr)  // x and w unused
+  if (logits_in == nullptr && route_on_tensor_cores(x_dtype, H)) {
+    unsigned char* w8 = static_cast<unsigned char*>(ws);
+    float* lg = logits_out != nullptr ? logits_out : reinterpret_cast<float*>(w8);
+    void* split = w8 + align_up((size_t)T * E * sizeof(float), 256);
+    cudaError_t e = launch_route_logits_tc(x, w, w_dtype, T, H, E, lg, split, s);
+    if (e != cudaSuccess) return e;
+    logits_in = lg;
+    logits_out = nullptr;
+  }
+  if (logits_in != nullptr)  // top-k of the given logits (x and w unused)
     return launch_route_t<float, float>(nullptr, nullptr, logits_in, logits_out, kpt, k_uniform, T, H, E,
                                         k_max, topk_idx, topk_w, s);
   if (x_dtype == SEMMOE_BF16 && w_dtype == SEMMOE_F32)

@@ -97,8 +97,10 @@ class MoELayer:
         logits = torch.empty(T, E, dtype=torch.float32, device=dev) if keep_logits else None
         topk_idx = torch.empty(T, k_max, **i32)
         topk_w = torch.empty(T, k_max, dtype=torch.float32, device=dev)
+        ws = self._workspace("route", abi.semmoe_route_workspace_size(
+            T, H, E, abi.dtype_code(x), abi.dtype_code(self.w_router)))
         abi.semmoe_route(x, self.w_router, logits_in, logits, k_per_token, k or 0, T, H, E, k_max,
-                         topk_idx, topk_w, stream)
+                         topk_idx, topk_w, ws, stream)
         mark("route")
         pred = torch.empty(T, **i32)
         abi.semmoe_affinity_lookup(token_ids, self.lut, self.V, R, T, pred, stream)
