@@ -178,3 +178,25 @@ def test_bad_budget_is_clamped_and_reported():
     with pytest.raises(abi().SemMoEError):
         abi().semmoe_check_errors()
     assert (idx[1] >= 0).all()           # clamped to k_max
+
+
+def test_remote_count_large_pair_list():
+    """Pair lists above 2^20 take the multi-CTA counting path."""
+    rng = np.random.default_rng(77)
+    T, E, R, k_max, V = 140_000, 64, 8, 8, 5000
+    idx = np.stack([rng.permutation(E)[:k_max] for _ in range(64)])[rng.integers(0, 64, size=T)]
+    k = rng.integers(1, k_max + 1, size=T)
+    idx = np.where(np.arange(k_max)[None, :] < k[:, None], idx, -1).astype(np.int32)
+    er = (np.arange(E) % R).astype(np.int32)
+    lut = rng.integers(0, R, size=V).astype(np.int32)
+    ids = rng.integers(0, V, size=T).astype(np.int32)
+    pred = torch.empty(T, **i32)
+    abi().semmoe_affinity_lookup(torch.from_numpy(ids).cuda(), torch.from_numpy(lut).cuda(), V, R, T, pred)
+    counts, remote = torch.empty(R, R, **i32), torch.empty(R, **i32)
+    abi().semmoe_remote_count(torch.from_numpy(idx).cuda(), pred, torch.from_numpy(er).cuda(), T, k_max, E, R,
+                              counts, remote)
+    assert abi().semmoe_check_errors() == 0
+    rp = oracle.affinity_lookup(ids, lut)
+    rc, rr = oracle.remote_count(idx, k, rp, er, R)
+    np.testing.assert_array_equal(np_(counts), rc)
+    np.testing.assert_array_equal(np_(remote), rr)

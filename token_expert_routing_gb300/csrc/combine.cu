@@ -46,38 +46,81 @@ template <> struct Vec16<__nv_bfloat16> {
   }
 };
 
-template <typename T>
+// One warp per token.  The token's (sorted row, gate) pairs are held by lanes
+// 0..k_max-1 and broadcast with shuffles; every lane accumulates CH 16-byte
+// chunks per pass (chunks lane, lane+32, ...), so a pass keeps CH * k_t
+// independent gathers in flight per lane.
+template <typename T, int CH>
 __global__ void __launch_bounds__(kThreads)
 combine_kernel(const T* __restrict__ y_perm, const int32_t* __restrict__ pair_to_sorted,
                const float* __restrict__ topk_w, const T* __restrict__ y_shared, int T_, int H, int k_max,
                int P, T* __restrict__ out) {
   using V = Vec16<T>;
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  const int kk = k_max < 32 ? k_max : 32;
   for (int t = blockIdx.x * kWarps + warp; t < T_; t += gridDim.x * kWarps) {
     const int32_t* q_row = pair_to_sorted + (size_t)t * k_max;
     const float* w_row = topk_w + (size_t)t * k_max;
-    for (int c = lane * V::N; c < H; c += 32 * V::N) {
-      float acc[V::N];
-      if (y_shared != nullptr) {
-        V::load(y_shared + (size_t)t * H + c, acc);
-      } else {
+    int q_l = -1;
+    float w_l = 0.f;
+    if (lane < kk) {
+      q_l = q_row[lane];
+      w_l = w_row[lane];
+      if (q_l >= P) { flag(SEMMOE_DEVERR_PAIRS); q_l = -1; }
+    }
+    for (int base = 0; base < H; base += 32 * V::N * CH) {
+      float acc[CH][V::N];
 #pragma unroll
-        for (int i = 0; i < V::N; ++i) acc[i] = 0.f;
+      for (int u = 0; u < CH; ++u) {
+        const int c = base + (u * 32 + lane) * V::N;
+        if (y_shared != nullptr && c < H) {
+          V::load(y_shared + (size_t)t * H + c, acc[u]);
+        } else {
+#pragma unroll
+          for (int i = 0; i < V::N; ++i) acc[u][i] = 0.f;
+        }
       }
-      for (int j = 0; j < k_max; ++j) {
+#pragma unroll 2
+      for (int j = 0; j < kk; ++j) {
+        const int q = __shfl_sync(0xffffffffu, q_l, j);
+        const float w = __shfl_sync(0xffffffffu, w_l, j);
+        if (q < 0) continue;
+        float v[CH][V::N];
+#pragma unroll
+        for (int u = 0; u < CH; ++u) {
+          const int c = base + (u * 32 + lane) * V::N;
+          if (c < H) V::load(y_perm + (size_t)q * H + c, v[u]);
+        }
+#pragma unroll
+        for (int u = 0; u < CH; ++u) {
+          const int c = base + (u * 32 + lane) * V::N;
+          if (c < H) {
+#pragma unroll
+            for (int i = 0; i < V::N; ++i) acc[u][i] = fmaf(w, v[u][i], acc[u][i]);
+          }
+        }
+      }
+      for (int j = 32; j < k_max; ++j) {  // budgets above 32 experts: read the slot directly
         const int q = q_row[j];
         if (q < 0) continue;
-        if (q >= P) {
-          if (c == lane * V::N) flag(SEMMOE_DEVERR_PAIRS);
-          continue;
-        }
+        if (q >= P) { flag(SEMMOE_DEVERR_PAIRS); continue; }
         const float w = w_row[j];
-        float v[V::N];
-        V::load(y_perm + (size_t)q * H + c, v);
 #pragma unroll
-        for (int i = 0; i < V::N; ++i) acc[i] = fmaf(w, v[i], acc[i]);
+        for (int u = 0; u < CH; ++u) {
+          const int c = base + (u * 32 + lane) * V::N;
+          if (c < H) {
+            float v[V::N];
+            V::load(y_perm + (size_t)q * H + c, v);
+#pragma unroll
+            for (int i = 0; i < V::N; ++i) acc[u][i] = fmaf(w, v[i], acc[u][i]);
+          }
+        }
       }
-      V::store(out + (size_t)t * H + c, acc);
+#pragma unroll
+      for (int u = 0; u < CH; ++u) {
+        const int c = base + (u * 32 + lane) * V::N;
+        if (c < H) V::store(out + (size_t)t * H + c, acc[u]);
+      }
     }
   }
 }
@@ -100,11 +143,11 @@ cudaError_t launch_combine(const void* y_perm, const int32_t* pair_to_sorted, co
   const int cap = sm_count() * 16;
   if (blocks > cap) blocks = cap;
   if (dtype == SEMMOE_BF16)
-    combine_kernel<__nv_bfloat16><<<blocks, kThreads, 0, s>>>(
+    combine_kernel<__nv_bfloat16, 2><<<blocks, kThreads, 0, s>>>(
         static_cast<const __nv_bfloat16*>(y_perm), pair_to_sorted, topk_w,
         static_cast<const __nv_bfloat16*>(y_shared), T, H, k_max, P, static_cast<__nv_bfloat16*>(out));
   else
-    combine_kernel<float><<<blocks, kThreads, 0, s>>>(static_cast<const float*>(y_perm), pair_to_sorted, topk_w,
+    combine_kernel<float, 2><<<blocks, kThreads, 0, s>>>(static_cast<const float*>(y_perm), pair_to_sorted, topk_w,
                                                       static_cast<const float*>(y_shared), T, H, k_max, P,
                                                       static_cast<float*>(out));
   count_launches(1);

@@ -5,6 +5,8 @@
 #include <cuda_bf16.h>
 #include <stdint.h>
 
+#include <atomic>
+
 #include "semmoe.h"
 
 namespace semmoe {
@@ -55,6 +57,20 @@ inline int take_error_word(const Sym& sym, cudaStream_t s, int* bits) {
 // host helpers
 // ---------------------------------------------------------------------------
 inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+// Raise `kernel`'s dynamic shared-memory limit to `bytes` once per device;
+// `done` is a per-call-site bit mask of devices already set.
+template <typename K>
+inline cudaError_t ensure_smem_limit(K kernel, int bytes, std::atomic<unsigned long long>& done) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const unsigned long long bit = dev < 64 ? (1ull << dev) : 0ull;
+  if (bit && (done.load(std::memory_order_relaxed) & bit)) return cudaSuccess;
+  e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e == cudaSuccess && bit) done.fetch_or(bit, std::memory_order_relaxed);
+  return e;
+}
 inline int ceil_div(int a, int b) { return (a + b - 1) / b; }
 
 }  // namespace semmoe

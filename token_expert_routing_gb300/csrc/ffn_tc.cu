@@ -306,7 +306,8 @@ template <bool GLU>
 cudaError_t launch_one(const CUtensorMap& ma, const CUtensorMap& mb, const int32_t* offsets, const int32_t* p2e,
                        int G, int P, int E, int N, int K, int n_tiles, __nv_bfloat16* out, cudaStream_t s) {
   auto kern = ffn_tc_kernel<GLU>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
+  static std::atomic<unsigned long long> smem_set{0};
+  cudaError_t e = ensure_smem_limit(kern, (int)kSmemBytes, smem_set);
   if (e != cudaSuccess) return e;
   const long long max_tiles = ((long long)(P + BM - 1) / BM + G) * n_tiles;
   int grid = sm_count();

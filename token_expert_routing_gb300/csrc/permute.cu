@@ -4,12 +4,12 @@
 // (de) §2 B, (ja) §2.2 B).  The rank-major expert order is the physical
 // layout that (ja) §2.2 A obtains by shuffling the gate matrix's columns.
 //
-// Three passes over the pair ids, none waiting on another CTA:
+// Two passes over the pair ids, neither waiting on another CTA:
 //   1. perm_hist:    each CTA counts its chunk of pairs per physical bucket
-//   2. perm_scan:    one CTA turns the [chunk][bucket] counts into bucket
-//                    offsets and per-chunk starting positions
-//   3. perm_scatter: each CTA ranks its pairs stably within its chunk (warp
-//                    match + per-warp bucket counts) and writes both maps
+//   2. perm_scatter: each CTA scans the [chunk][bucket] counts for its own
+//                    starting positions, ranks its pairs stably within the
+//                    chunk (warp match + per-warp bucket counts) and writes
+//                    both maps; CTA 0 writes the bucket and rank tables
 // then perm_gather copies x rows into sorted order (one warp per row,
 // 16-byte vectors).
 #include <mutex>
@@ -80,64 +80,64 @@ perm_hist_kernel(const int32_t* __restrict__ topk_idx, const int32_t* __restrict
   for (int b = threadIdx.x; b < E; b += kThreads) hist[(size_t)blockIdx.x * E + b] = h[b];
 }
 
-// One CTA: column-wise exclusive scan of hist (in place -> per-chunk start
-// offsets), bucket offsets, and the small per-expert / per-rank tables.
-__global__ void __launch_bounds__(kThreads)
-perm_scan_kernel(int32_t* __restrict__ hist, int nchunks, const int32_t* __restrict__ expert_rank, int E,
-                 int R, int P, int32_t* __restrict__ expert_offsets, int32_t* __restrict__ rank_offsets,
-                 int32_t* __restrict__ phys_to_expert, int32_t* __restrict__ expert_counts) {
-  __shared__ int rank_s[kMaxE], phys_s[kMaxE], total[kMaxE], excl[kMaxE + 1];
-  physical_positions(expert_rank, E, R, rank_s, phys_s);
-  const int b = threadIdx.x;
-  if (b < E) {
-    int run = 0;
-    for (int c = 0; c < nchunks; ++c) {
-      int v = hist[(size_t)c * E + b];
-      hist[(size_t)c * E + b] = run;
-      run += v;
-    }
-    total[b] = run;
-  }
-  __syncthreads();
-  if (threadIdx.x == 0) {  // E <= 256 buckets: a serial scan is cheapest here
-    int s = 0;
-    for (int i = 0; i < E; ++i) { excl[i] = s; s += total[i]; }
-    excl[E] = s;
-    if (s != P) flag(SEMMOE_DEVERR_PAIRS);
-  }
-  __syncthreads();
-  if (b < E) {
-    const int off = excl[b];
-    for (int c = 0; c < nchunks; ++c) hist[(size_t)c * E + b] += off;
-    expert_offsets[b] = off;
-  }
-  if (b == 0) expert_offsets[E] = excl[E];
-  for (int e = threadIdx.x; e < E; e += kThreads) {
-    phys_to_expert[phys_s[e]] = e;
-    expert_counts[e] = total[phys_s[e]];
-  }
-  for (int r = threadIdx.x; r <= R; r += kThreads) {
-    int nb = 0;  // buckets of ranks below r
-    for (int e = 0; e < E; ++e) nb += rank_s[e] < r;
-    rank_offsets[r] = excl[nb];
-  }
-}
-
+// Each CTA ranks the pairs of its chunk.  Its starting position in every bucket
+// is derived from the per-chunk histograms of pass 1: it sums, per bucket, the
+// counts of all chunks (totals) and of the chunks before its own, and scans the
+// totals over buckets.  CTA 0 also writes the bucket / rank tables.  Nothing
+// waits on another CTA: every CTA recomputes the (small) scan for itself.
 __global__ void __launch_bounds__(kThreads)
 perm_scatter_kernel(const int32_t* __restrict__ topk_idx, const int32_t* __restrict__ expert_rank,
-                    long long n_pairs, int E, int R, int P, const int32_t* __restrict__ chunk_off,
+                    long long n_pairs, int nchunks, int E, int R, int P, const int32_t* __restrict__ hist,
+                    int32_t* __restrict__ expert_offsets, int32_t* __restrict__ rank_offsets,
+                    int32_t* __restrict__ phys_to_expert, int32_t* __restrict__ expert_counts,
                     int32_t* __restrict__ sorted_to_pair, int32_t* __restrict__ pair_to_sorted) {
-  __shared__ int rank_s[kMaxE], phys_s[kMaxE], run[kMaxE];
+  __shared__ int rank_s[kMaxE], phys_s[kMaxE], run[kMaxE], total[kMaxE], scan[kThreads];
   __shared__ int wcnt[kWarps][kMaxE];
   physical_positions(expert_rank, E, R, rank_s, phys_s);
-  for (int i = threadIdx.x; i < E; i += kThreads) {
-    run[i] = chunk_off[(size_t)blockIdx.x * E + i];
-    for (int w = 0; w < kWarps; ++w) wcnt[w][i] = 0;
+  const int tid = threadIdx.x;
+  if (tid < E) {
+    int before = 0, tot = 0;
+    for (int c = 0; c < nchunks; ++c) {
+      const int v = hist[(size_t)c * E + tid];
+      before += c < (int)blockIdx.x ? v : 0;
+      tot += v;
+    }
+    total[tid] = tot;
+    run[tid] = before;
+    for (int w = 0; w < kWarps; ++w) wcnt[w][tid] = 0;
+  }
+  scan[tid] = tid < E ? total[tid] : 0;
+  __syncthreads();
+  for (int d = 1; d < kThreads; d <<= 1) {  // inclusive scan of the bucket totals
+    const int v = tid >= d ? scan[tid - d] : 0;
+    __syncthreads();
+    scan[tid] += v;
+    __syncthreads();
+  }
+  const int sum = scan[kThreads - 1];
+  if (tid < E) run[tid] += scan[tid] - total[tid];  // bucket start + rows of earlier chunks
+  if (blockIdx.x == 0) {
+    if (tid < E) {
+      expert_offsets[tid] = scan[tid] - total[tid];
+      phys_to_expert[phys_s[tid]] = tid;
+      expert_counts[tid] = total[phys_s[tid]];
+    }
+    if (tid == 0) {
+      expert_offsets[E] = sum;
+      if (sum != P) flag(SEMMOE_DEVERR_PAIRS);
+    }
+    if (tid <= R) {
+      int nb = 0;  // buckets of ranks below r = tid
+      for (int e = 0; e < E; ++e) nb += rank_s[e] < tid;
+      rank_offsets[tid] = nb == 0 ? 0 : scan[nb - 1];
+    }
   }
   __syncthreads();
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  (void)lane;
   const long long base = (long long)blockIdx.x * kChunk;
   for (int r = 0; r < kRounds; ++r) {
+    if (base + (long long)r * kThreads >= n_pairs) break;  // uniform across the CTA
     const long long p = base + (long long)r * kThreads + threadIdx.x;
     int key = E;  // E = "no bucket" (padding slot or past the end)
     if (p < n_pairs) {
@@ -161,9 +161,9 @@ perm_scatter_kernel(const int32_t* __restrict__ topk_idx, const int32_t* __restr
     }
     __syncthreads();
     for (int b = threadIdx.x; b < E; b += kThreads) {
-      int s = 0;
-      for (int w = 0; w < kWarps; ++w) { s += wcnt[w][b]; wcnt[w][b] = 0; }
-      run[b] += s;
+      int s2 = 0;
+      for (int w = 0; w < kWarps; ++w) { s2 += wcnt[w][b]; wcnt[w][b] = 0; }
+      run[b] += s2;
     }
     __syncthreads();
   }
@@ -215,18 +215,11 @@ cudaError_t launch_permute(const int32_t* topk_idx, const int32_t* expert_rank, 
   if (n_pairs > 0) {
     perm_hist_kernel<<<nc, kThreads, 0, s>>>(topk_idx, expert_rank, n_pairs, E, R, hist);
     count_launches(1);
-  } else {
-    cudaError_t e = cudaMemsetAsync(hist, 0, sizeof(int32_t) * E, s);
-    if (e != cudaSuccess) return e;
   }
-  perm_scan_kernel<<<1, kThreads, 0, s>>>(hist, n_pairs > 0 ? nc : 1, expert_rank, E, R, P, expert_offsets,
-                                          rank_offsets, phys_to_expert, expert_counts);
+  perm_scatter_kernel<<<n_pairs > 0 ? nc : 1, kThreads, 0, s>>>(
+      topk_idx, expert_rank, n_pairs, n_pairs > 0 ? nc : 0, E, R, P, hist, expert_offsets, rank_offsets,
+      phys_to_expert, expert_counts, sorted_to_pair, pair_to_sorted);
   count_launches(1);
-  if (n_pairs > 0) {
-    perm_scatter_kernel<<<nc, kThreads, 0, s>>>(topk_idx, expert_rank, n_pairs, E, R, P, hist, sorted_to_pair,
-                                                pair_to_sorted);
-    count_launches(1);
-  }
   if (x != nullptr && x_perm != nullptr && P > 0) {
     const int row_bytes = H * (dtype == SEMMOE_BF16 ? 2 : 4);
     int blocks = (P + kWarps - 1) / kWarps;
@@ -269,8 +262,8 @@ cudaError_t launch_permute_noalloc(const int32_t* topk_idx, const int32_t* exper
   void* scratch = nullptr;
   cudaError_t e = noalloc_scratch_address(&scratch);
   if (e != cudaSuccess) return e;
-  // The kernels overwrite every scratch entry they later read (the zero-pair
-  // case clears its one row), so stale contents of an earlier call never leak.
+  // The kernels write every scratch entry before they read it, so stale contents of an
+  // earlier call never leak into this one.
   return launch_permute(topk_idx, expert_rank, x, dtype, T, H, E, R, k_max, P, expert_offsets, rank_offsets,
                         phys_to_expert, expert_counts, sorted_to_pair, pair_to_sorted, x_perm, scratch, s);
 }

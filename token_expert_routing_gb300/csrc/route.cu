@@ -218,6 +218,37 @@ __global__ void remote_count_kernel(const int32_t* __restrict__ topk_idx, const 
     if (c[i]) atomicAdd(&counts[i], c[i]);
 }
 
+// One CTA does the whole count when the pair list is small enough: no memset,
+// no global atomics, and the per-source remote sums in the same launch.
+constexpr int kCountThreads = 1024;
+constexpr long long kOneBlockPairs = 1LL << 20;
+
+__global__ void __launch_bounds__(kCountThreads)
+remote_count_one_block_kernel(const int32_t* __restrict__ topk_idx, const int32_t* __restrict__ pred,
+                              const int32_t* __restrict__ expert_rank, int T, int k_max, int E, int R,
+                              int32_t* __restrict__ counts, int32_t* __restrict__ remote) {
+  __shared__ int c[kMaxR * kMaxR];
+  for (int i = threadIdx.x; i < R * R; i += kCountThreads) c[i] = 0;
+  __syncthreads();
+  const long long n = (long long)T * k_max;
+#pragma unroll 4
+  for (long long p = threadIdx.x; p < n; p += kCountThreads) {
+    const int e = topk_idx[p];
+    if (e < 0) continue;
+    if (e >= E) { flag(SEMMOE_DEVERR_EXPERT); continue; }
+    const int src = pred[p / k_max], dst = expert_rank[e];
+    if (src < 0 || src >= R || dst < 0 || dst >= R) { flag(SEMMOE_DEVERR_LUT); continue; }
+    atomicAdd(&c[src * R + dst], 1);
+  }
+  __syncthreads();
+  for (int i = threadIdx.x; i < R * R; i += kCountThreads) counts[i] = c[i];
+  if (threadIdx.x < R) {
+    int sum = 0;
+    for (int d = 0; d < R; ++d) sum += d != (int)threadIdx.x ? c[threadIdx.x * R + d] : 0;
+    remote[threadIdx.x] = sum;
+  }
+}
+
 __global__ void remote_finalize_kernel(const int32_t* __restrict__ counts, int R,
                                        int32_t* __restrict__ remote) {
   int src = threadIdx.x;
@@ -234,8 +265,9 @@ cudaError_t launch_route_t(const void* x, const void* w, const float* li, float*
                            cudaStream_t s) {
   size_t sm = route_smem_bytes(E, k_max);
   auto kern = route_kernel<TX, TW>;
-  if (sm > 48 * 1024) {
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
+  if (sm > 48 * 1024) {  // raise the limit once to the largest layout (E = k_max = 256)
+    static std::atomic<unsigned long long> smem_set{0};
+    cudaError_t e = ensure_smem_limit(kern, (int)route_smem_bytes(kRouteMaxE, kRouteMaxE), smem_set);
     if (e != cudaSuccess) return e;
   }
   dim3 grid((T + kRouteTok - 1) / kRouteTok);
@@ -303,17 +335,21 @@ cudaError_t launch_affinity_lookup(const int32_t* ids, const int32_t* lut, int V
 
 cudaError_t launch_remote_count(const int32_t* topk_idx, const int32_t* pred, const int32_t* expert_rank, int T,
                                 int k_max, int E, int R, int32_t* counts, int32_t* remote, cudaStream_t s) {
+  long long n = (long long)T * k_max;
+  if (n <= kOneBlockPairs) {
+    remote_count_one_block_kernel<<<1, kCountThreads, 0, s>>>(topk_idx, pred, expert_rank, T, k_max, E, R, counts,
+                                                              remote);
+    count_launches(1);
+    return cudaGetLastError();
+  }
   cudaError_t e = cudaMemsetAsync(counts, 0, sizeof(int32_t) * R * R, s);
   if (e != cudaSuccess) return e;
-  long long n = (long long)T * k_max;
-  if (n > 0) {
-    long long blocks = (n + 1023) / 1024;
-    if (blocks > 1024) blocks = 1024;
-    remote_count_kernel<<<(int)blocks, 256, 0, s>>>(topk_idx, pred, expert_rank, T, k_max, E, R, counts);
-    count_launches(1);
-    e = cudaGetLastError();
-    if (e != cudaSuccess) return e;
-  }
+  long long blocks = (n + 1023) / 1024;
+  if (blocks > 1024) blocks = 1024;
+  remote_count_kernel<<<(int)blocks, 256, 0, s>>>(topk_idx, pred, expert_rank, T, k_max, E, R, counts);
+  count_launches(1);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
   remote_finalize_kernel<<<1, kMaxR, 0, s>>>(counts, R, remote);
   count_launches(1);
   return cudaGetLastError();

@@ -227,11 +227,13 @@ cudaError_t launch_route_logits_tc(const void* x, const void* w, int w_dtype, in
   dim3 grid((T + BM - 1) / BM, n_pass);
   cudaError_t e;
   if (S == 3) {
-    e = cudaFuncSetAttribute(route_tc_kernel<3>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
+    static std::atomic<unsigned long long> smem_set{0};
+    e = ensure_smem_limit(route_tc_kernel<3>, (int)kSmemBytes, smem_set);
     if (e != cudaSuccess) return e;
     route_tc_kernel<3><<<grid, THREADS, kSmemBytes, s>>>(mx, mw, T, H, E, EC, logits);
   } else {
-    e = cudaFuncSetAttribute(route_tc_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
+    static std::atomic<unsigned long long> smem_set{0};
+    e = ensure_smem_limit(route_tc_kernel<1>, (int)kSmemBytes, smem_set);
     if (e != cudaSuccess) return e;
     route_tc_kernel<1><<<grid, THREADS, kSmemBytes, s>>>(mx, mw, T, H, E, EC, logits);
   }
