@@ -203,11 +203,11 @@ int semmoe_permute(const int32_t* topk_idx, const int32_t* expert_rank,
  * after start-up because it can synchronise the whole device.
  *
  * Same arguments, outputs and errors as semmoe_permute, minus the workspace:
- * the scratch (per-chunk bucket counts, ceil(T*k_max / 2048) * E * 4 bytes)
- * lives in a static 1 MiB device array compiled into the library, which every
- * GPU that loads the library holds until the process exits.  Sizes whose
- * scratch exceeds 1 MiB are rejected with SEMMOE_ERR_INVALID_ARG (use
- * semmoe_permute with a workspace instead).  The call makes no cudaMalloc,
+ * the scratch (per-chunk bucket counts: at most 96 chunks * E * 4 bytes) lives
+ * in a static 96 KiB device array compiled into the library, which every GPU
+ * that loads the library holds until the process exits.  That covers every
+ * E <= 256; sizes beyond it (E > 256, T*k_max >= 2^31) are rejected with
+ * SEMMOE_ERR_INVALID_ARG before anything runs.  The call makes no cudaMalloc,
  * cudaFree or other allocating call.
  *
  * The first call on each device looks up the array's device address (once,

@@ -200,3 +200,28 @@ def test_remote_count_large_pair_list():
     rc, rr = oracle.remote_count(idx, k, rp, er, R)
     np.testing.assert_array_equal(np_(counts), rc)
     np.testing.assert_array_equal(np_(remote), rr)
+
+
+@pytest.mark.parametrize("E,k_max,wd", [(64, 8, torch.float32), (40, 16, torch.float32),
+                                        (256, 16, torch.bfloat16), (256, 24, torch.float32),
+                                        (128, 8, torch.bfloat16)])
+def test_route_tensor_core_per_token_budgets(E, k_max, wd):
+    """bf16 activations: the tensor-core router, with the top-k fused into its
+    epilogue when every expert fits one pass and k_max <= 16, else a separate
+    top-k kernel; per-token budgets and ties from duplicated router rows."""
+    rng = np.random.default_rng(E * 31 + k_max)
+    T, H = 515, 256
+    x = torch.from_numpy(rng.standard_normal((T, H)).astype(np.float32) / np.sqrt(H)).to(torch.bfloat16)
+    w = rng.standard_normal((E, H)).astype(np.float32) / np.sqrt(H)
+    w[E // 2] = w[3]                      # two experts with identical logits: ties
+    wr = torch.from_numpy(w).to(wd)
+    kpt = rng.integers(1, k_max + 1, size=T).astype(np.int32)
+    idx = torch.empty(T, k_max, **i32)
+    gw = torch.empty(T, k_max, dtype=torch.float32, device="cuda")
+    lg = torch.empty(T, E, dtype=torch.float32, device="cuda")
+    abi().semmoe_route(x.cuda(), wr.cuda(), None, lg, torch.from_numpy(kpt).cuda(), 0, T, H, E, k_max, idx, gw)
+    assert abi().semmoe_check_errors() == 0
+    assert max_rel(np_(lg), oracle.router_logits(x, wr)) < LOGIT_TOL
+    ref_idx, ref_w = oracle.topk_route(np_(lg), kpt, k_max)
+    np.testing.assert_array_equal(np_(idx), ref_idx)
+    np.testing.assert_allclose(np_(gw), ref_w, rtol=0, atol=GATE_ATOL)

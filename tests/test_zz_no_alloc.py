@@ -19,14 +19,18 @@ import torch
 
 
 def test_noalloc_rejects_sizes_beyond_its_static_scratch():
+    """The static scratch is sized for E <= 256 experts; larger sizes are refused
+    on the host with a clear message, before any device work."""
     from token_expert_routing_gb300 import _abi, build
     build.build()
     lib = _abi.lib()
     p = ctypes.c_void_p(256)
-    # 2,000,000 tokens x 8 slots x 256 experts needs ~7.8 MB of scratch > 1 MiB
-    rc = lib.semmoe_permute_noalloc(p, p, None, 1, 2_000_000, 8, 256, 8, 8, 16, p, p, p, p, p, p, None, None)
+    rc = lib.semmoe_permute_noalloc(p, p, None, 1, 4096, 8, 300, 8, 8, 16, p, p, p, p, p, p, None, None)
     assert rc == _abi.SEMMOE_ERR_INVALID_ARG
-    assert "scratch" in lib.semmoe_last_error().decode()
+    assert "E = 300" in lib.semmoe_last_error().decode()
+    rc = lib.semmoe_permute_noalloc(p, p, None, 1, 1 << 28, 16, 256, 8, 8, 16, p, p, p, p, p, p, None, None)
+    assert rc == _abi.SEMMOE_ERR_INVALID_ARG
+    assert "too large" in lib.semmoe_last_error().decode()
 
 
 def _routing(rng, T, E, k_max):

@@ -20,7 +20,9 @@
 // Scratch of semmoe_permute_noalloc: the per-chunk bucket counts live in this
 // file-scope device array instead of a caller workspace.  Every GPU that loads
 // the library holds it until the process exits.
-static constexpr size_t kNoAllocScratchBytes = 1u << 20;  // 1 MiB
+// The permute splits the pairs into at most 96 chunks, so it needs at most
+// 96 * E * 4 bytes of scratch: 96 KiB covers every E up to the 256 it accepts.
+static constexpr size_t kNoAllocScratchBytes = 96u * 256u * 4u;  // 96 KiB
 static __device__ __align__(256) int32_t g_noalloc_scratch[kNoAllocScratchBytes / sizeof(int32_t)];
 
 namespace semmoe {
@@ -31,11 +33,20 @@ __device__ __forceinline__ void flag(int bit) { atomicOr(&g_err, bit); }
 
 constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
-constexpr int kRounds = 8;
-constexpr int kChunk = kThreads * kRounds;  // pairs per CTA
 constexpr int kMaxE = 256;
+constexpr int kTargetChunks = 96;  // enough CTAs to cover the GPU, few enough to scan cheaply
+static_assert(kTargetChunks * kMaxE * 4 <= kNoAllocScratchBytes, "no-alloc scratch too small");
 
-inline int n_chunks(long long n_pairs) { return (int)((n_pairs + kChunk - 1) / kChunk); }
+// Pairs per CTA: a multiple of kThreads (one "round" each) giving about
+// kTargetChunks chunks.
+inline int rounds_per_chunk(long long n_pairs) {
+  const long long r = (n_pairs + (long long)kTargetChunks * kThreads - 1) / ((long long)kTargetChunks * kThreads);
+  return r < 1 ? 1 : (int)r;
+}
+inline int n_chunks(long long n_pairs) {
+  const long long chunk = (long long)rounds_per_chunk(n_pairs) * kThreads;
+  return (int)((n_pairs + chunk - 1) / chunk);
+}
 
 // phys_s[e] = position of expert e in the (expert_rank[e], e) order.
 __device__ void physical_positions(const int32_t* __restrict__ expert_rank, int E, int R, int* rank_s,
@@ -62,13 +73,14 @@ __device__ void physical_positions(const int32_t* __restrict__ expert_rank, int 
 
 __global__ void __launch_bounds__(kThreads)
 perm_hist_kernel(const int32_t* __restrict__ topk_idx, const int32_t* __restrict__ expert_rank,
-                 long long n_pairs, int E, int R, int32_t* __restrict__ hist) {
+                 long long n_pairs, int rounds, int E, int R, int32_t* __restrict__ hist) {
   __shared__ int rank_s[kMaxE], phys_s[kMaxE], h[kMaxE];
   physical_positions(expert_rank, E, R, rank_s, phys_s);
   for (int b = threadIdx.x; b < E; b += kThreads) h[b] = 0;
   __syncthreads();
-  const long long base = (long long)blockIdx.x * kChunk;
-  for (int i = threadIdx.x; i < kChunk; i += kThreads) {
+  const int chunk = rounds * kThreads;
+  const long long base = (long long)blockIdx.x * chunk;
+  for (int i = threadIdx.x; i < chunk; i += kThreads) {
     long long p = base + i;
     if (p >= n_pairs) break;
     int e = topk_idx[p];
@@ -87,7 +99,8 @@ perm_hist_kernel(const int32_t* __restrict__ topk_idx, const int32_t* __restrict
 // waits on another CTA: every CTA recomputes the (small) scan for itself.
 __global__ void __launch_bounds__(kThreads)
 perm_scatter_kernel(const int32_t* __restrict__ topk_idx, const int32_t* __restrict__ expert_rank,
-                    long long n_pairs, int nchunks, int E, int R, int P, const int32_t* __restrict__ hist,
+                    long long n_pairs, int rounds, int nchunks, int E, int R, int P,
+                    const int32_t* __restrict__ hist,
                     int32_t* __restrict__ expert_offsets, int32_t* __restrict__ rank_offsets,
                     int32_t* __restrict__ phys_to_expert, int32_t* __restrict__ expert_counts,
                     int32_t* __restrict__ sorted_to_pair, int32_t* __restrict__ pair_to_sorted) {
@@ -135,8 +148,8 @@ perm_scatter_kernel(const int32_t* __restrict__ topk_idx, const int32_t* __restr
   __syncthreads();
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   (void)lane;
-  const long long base = (long long)blockIdx.x * kChunk;
-  for (int r = 0; r < kRounds; ++r) {
+  const long long base = (long long)blockIdx.x * rounds * kThreads;
+  for (int r = 0; r < rounds; ++r) {
     if (base + (long long)r * kThreads >= n_pairs) break;  // uniform across the CTA
     const long long p = base + (long long)r * kThreads + threadIdx.x;
     int key = E;  // E = "no bucket" (padding slot or past the end)
@@ -213,11 +226,13 @@ cudaError_t launch_permute(const int32_t* topk_idx, const int32_t* expert_rank, 
   const int nc = n_chunks(n_pairs > 0 ? n_pairs : 1);
   int32_t* hist = static_cast<int32_t*>(ws);
   if (n_pairs > 0) {
-    perm_hist_kernel<<<nc, kThreads, 0, s>>>(topk_idx, expert_rank, n_pairs, E, R, hist);
+    perm_hist_kernel<<<nc, kThreads, 0, s>>>(topk_idx, expert_rank, n_pairs, rounds_per_chunk(n_pairs), E, R,
+                                             hist);
     count_launches(1);
   }
   perm_scatter_kernel<<<n_pairs > 0 ? nc : 1, kThreads, 0, s>>>(
-      topk_idx, expert_rank, n_pairs, n_pairs > 0 ? nc : 0, E, R, P, hist, expert_offsets, rank_offsets,
+      topk_idx, expert_rank, n_pairs, rounds_per_chunk(n_pairs), n_pairs > 0 ? nc : 0, E, R, P, hist,
+      expert_offsets, rank_offsets,
       phys_to_expert, expert_counts, sorted_to_pair, pair_to_sorted);
   count_launches(1);
   if (x != nullptr && x_perm != nullptr && P > 0) {

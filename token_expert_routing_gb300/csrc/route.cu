@@ -231,14 +231,28 @@ remote_count_one_block_kernel(const int32_t* __restrict__ topk_idx, const int32_
   for (int i = threadIdx.x; i < R * R; i += kCountThreads) c[i] = 0;
   __syncthreads();
   const long long n = (long long)T * k_max;
-#pragma unroll 4
-  for (long long p = threadIdx.x; p < n; p += kCountThreads) {
-    const int e = topk_idx[p];
-    if (e < 0) continue;
-    if (e >= E) { flag(SEMMOE_DEVERR_EXPERT); continue; }
-    const int src = pred[p / k_max], dst = expert_rank[e];
-    if (src < 0 || src >= R || dst < 0 || dst >= R) { flag(SEMMOE_DEVERR_LUT); continue; }
-    atomicAdd(&c[src * R + dst], 1);
+  constexpr int B = 8;  // pairs per thread per batch: all their loads are issued before any use
+  for (long long p0 = threadIdx.x; p0 < n; p0 += (long long)B * kCountThreads) {
+    int e[B], src[B], dst[B];
+#pragma unroll
+    for (int u = 0; u < B; ++u) {
+      const long long p = p0 + (long long)u * kCountThreads;
+      e[u] = p < n ? topk_idx[p] : -1;
+    }
+#pragma unroll
+    for (int u = 0; u < B; ++u) {
+      const long long p = p0 + (long long)u * kCountThreads;
+      const bool ok = e[u] >= 0 && e[u] < E;
+      src[u] = ok ? pred[p / k_max] : 0;
+      dst[u] = ok ? expert_rank[e[u]] : 0;
+    }
+#pragma unroll
+    for (int u = 0; u < B; ++u) {
+      if (e[u] < 0) continue;
+      if (e[u] >= E) { flag(SEMMOE_DEVERR_EXPERT); continue; }
+      if (src[u] < 0 || src[u] >= R || dst[u] < 0 || dst[u] >= R) { flag(SEMMOE_DEVERR_LUT); continue; }
+      atomicAdd(&c[src[u] * R + dst[u]], 1);
+    }
   }
   __syncthreads();
   for (int i = threadIdx.x; i < R * R; i += kCountThreads) counts[i] = c[i];
@@ -300,9 +314,13 @@ cudaError_t launch_route(const void* x, int x_dtype, const void* w, int w_dtype,
   if (T == 0) return cudaSuccess;
   if (logits_in == nullptr && route_on_tensor_cores(x_dtype, H)) {
     unsigned char* w8 = static_cast<unsigned char*>(ws);
-    float* lg = logits_out != nullptr ? logits_out : reinterpret_cast<float*>(w8);
     void* split = w8 + align_up((size_t)T * E * sizeof(float), 256);
-    cudaError_t e = launch_route_logits_tc(x, w, w_dtype, T, H, E, lg, split, s);
+    if (route_tc_fuses_topk(E, k_max, w_dtype))  // GEMM, top-k and gates in one kernel
+      return launch_route_logits_tc(x, w, w_dtype, T, H, E, logits_out, split, kpt, k_uniform, k_max, topk_idx,
+                                    topk_w, s);
+    float* lg = logits_out != nullptr ? logits_out : reinterpret_cast<float*>(w8);
+    cudaError_t e = launch_route_logits_tc(x, w, w_dtype, T, H, E, lg, split, nullptr, 0, k_max, nullptr,
+                                           nullptr, s);
     if (e != cudaSuccess) return e;
     logits_in = lg;
     logits_out = nullptr;

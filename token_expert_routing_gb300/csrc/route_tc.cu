@@ -13,7 +13,9 @@
 //
 // One CTA per (128-token tile, pass of EC experts); warp 0 issues TMA, warp 1
 // allocates TMEM and issues the MMAs, warps 2..5 read the accumulator and write
-// fp32 logits.  Waits are bounded as in the grouped-FFN kernel.
+// fp32 logits.  When every expert fits one pass and k_max <= 16, the epilogue
+// also does the top-k and the gates (one token per thread), so the logits never
+// go through memory.  Waits are bounded as in the grouped-FFN kernel.
 #include "common.cuh"
 #include "internal.h"
 #include "tc_common.cuh"
@@ -69,10 +71,20 @@ __global__ void split_router_kernel(const float* __restrict__ w, int E, int H, i
   }
 }
 
-template <int S>
+// Outputs of the fused top-k (every field unused unless TOPK).
+struct TopkOut {
+  const int32_t* k_per_token;  // nullable: k_uniform then
+  int k_uniform, k_max;
+  int32_t* topk_idx;
+  float* topk_w;
+};
+
+constexpr int KREG = 16;  // largest k_max the fused top-k keeps in registers
+
+template <int S, bool TOPK>
 __global__ void __launch_bounds__(THREADS, 1)
 route_tc_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_constant__ CUtensorMap map_w, int T, int H,
-                int E, int EC, float* __restrict__ logits) {
+                int E, int EC, float* __restrict__ logits, TopkOut tk) {
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   const uint32_t pad = (1024u - (smem_u32(smem_raw) & 1023u)) & 1023u;
   unsigned char* stage_a = smem_raw + pad;
@@ -147,7 +159,15 @@ route_tc_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_constant
     if (ok) {
       fence_after();
       const uint32_t trow = tmem + ((uint32_t)(q * 32) << 16);
-      float* lrow = logits + (size_t)(t < T ? t : 0) * E;
+      float* lrow = logits != nullptr ? logits + (size_t)(t < T ? t : 0) * E : nullptr;
+      // Fused top-k (single pass, experts in ascending order): a register list
+      // sorted by logit descending; a new logit enters only if strictly larger
+      // than the last entry and bubbles past strictly smaller ones, so equal
+      // logits keep the lower expert index first.
+      float bv[TOPK ? KREG : 1];
+      int be[TOPK ? KREG : 1];
+#pragma unroll
+      for (int i = 0; i < (TOPK ? KREG : 1); ++i) { bv[i] = -INFINITY; be[i] = -1; }
       for (int c = 0; c < EC; c += 16) {
         uint32_t v0[16], v1[16], v2[16];
         tmem_ld16(trow + c, v0);
@@ -163,8 +183,49 @@ route_tc_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_constant
             if (e < E) {
               float l = __uint_as_float(v0[i]);
               if (S == 3) l = (l + __uint_as_float(v1[i])) + __uint_as_float(v2[i]);
-              lrow[e] = l;
+              if (lrow != nullptr) lrow[e] = l;
+              if (TOPK) {
+                if (!isfinite(l)) {
+                  atomicOr(&g_err, SEMMOE_DEVERR_NONFINITE);
+                  l = -INFINITY;
+                }
+                if (l > bv[KREG - 1]) {
+                  bv[KREG - 1] = l;
+                  be[KREG - 1] = e;
+#pragma unroll
+                  for (int j = KREG - 1; j > 0; --j) {
+                    if (bv[j] > bv[j - 1]) {
+                      const float tv = bv[j]; bv[j] = bv[j - 1]; bv[j - 1] = tv;
+                      const int te = be[j]; be[j] = be[j - 1]; be[j - 1] = te;
+                    }
+                  }
+                }
+              }
             }
+          }
+        }
+      }
+      if (TOPK && t < T) {
+        int kt = tk.k_per_token != nullptr ? tk.k_per_token[t] : tk.k_uniform;
+        if (kt < 1 || kt > tk.k_max) {
+          atomicOr(&g_err, SEMMOE_DEVERR_K);
+          kt = kt < 1 ? 1 : tk.k_max;
+        }
+        // gates: softmax over the selected logits, renormalised (fp32)
+        const float m = bv[0];
+        float den = 0.f;
+#pragma unroll
+        for (int j = 0; j < KREG; ++j)
+          if (j < kt && be[j] >= 0) den += expf(bv[j] - m);
+        int32_t* irow = tk.topk_idx + (size_t)t * tk.k_max;
+        float* wrow = tk.topk_w + (size_t)t * tk.k_max;
+#pragma unroll
+        for (int j = 0; j < KREG; ++j) {
+          if (j < tk.k_max) {
+            const bool live = j < kt && be[j] >= 0;
+            if (j < kt && be[j] < 0) atomicOr(&g_err, SEMMOE_DEVERR_NONFINITE);
+            irow[j] = live ? be[j] : -1;
+            wrow[j] = live ? expf(bv[j] - m) / den : 0.f;
           }
         }
       }
@@ -191,10 +252,20 @@ size_t route_tc_split_bytes(int H, int E, int w_dtype) {
   return align_up((size_t)n_pass * 3 * EC * H * 2, 256);
 }
 
-// x [T,H] bf16 (H % 8 == 0); w [E,H] fp32 or bf16; logits [T,E] fp32 out;
-// split: workspace of route_tc_split_bytes() (fp32 weight only).
+// Whether the top-k can run in the router kernel's epilogue: every expert in
+// one pass and k_max within the register list.
+bool route_tc_fuses_topk(int E, int k_max, int w_dtype) {
+  const int S = w_dtype == SEMMOE_F32 ? 3 : 1;
+  return E <= experts_per_pass(E, S) && k_max <= KREG;
+}
+
+// x [T,H] bf16 (H % 8 == 0); w [E,H] fp32 or bf16; split: workspace of
+// route_tc_split_bytes() (fp32 weight only).  Writes logits [T,E] (nullable
+// when topk_idx is set) and, when topk_idx != nullptr (only if
+// route_tc_fuses_topk), the top-k indices and gates.
 cudaError_t launch_route_logits_tc(const void* x, const void* w, int w_dtype, int T, int H, int E, float* logits,
-                                   void* split, cudaStream_t s) {
+                                   void* split, const int32_t* k_per_token, int k_uniform, int k_max,
+                                   int32_t* topk_idx, float* topk_w, cudaStream_t s) {
   const int S = w_dtype == SEMMOE_F32 ? 3 : 1;
   const int EC = experts_per_pass(E, S), n_pass = (E + EC - 1) / EC;
   const void* wb = w;
@@ -224,19 +295,22 @@ cudaError_t launch_route_logits_tc(const void* x, const void* w, int w_dtype, in
     const cuuint32_t box[2] = {BK, (cuuint32_t)(S * EC)};
     if (!make_map_bf16(&mw, wb, 2, dims, str, box)) return cudaErrorInvalidValue;
   }
+  const TopkOut tk{k_per_token, k_uniform, k_max, topk_idx, topk_w};
+  const bool topk = topk_idx != nullptr;
   dim3 grid((T + BM - 1) / BM, n_pass);
   cudaError_t e;
-  if (S == 3) {
-    static std::atomic<unsigned long long> smem_set{0};
-    e = ensure_smem_limit(route_tc_kernel<3>, (int)kSmemBytes, smem_set);
-    if (e != cudaSuccess) return e;
-    route_tc_kernel<3><<<grid, THREADS, kSmemBytes, s>>>(mx, mw, T, H, E, EC, logits);
-  } else {
-    static std::atomic<unsigned long long> smem_set{0};
-    e = ensure_smem_limit(route_tc_kernel<1>, (int)kSmemBytes, smem_set);
-    if (e != cudaSuccess) return e;
-    route_tc_kernel<1><<<grid, THREADS, kSmemBytes, s>>>(mx, mw, T, H, E, EC, logits);
-  }
+#define SEMMOE_ROUTE_TC_LAUNCH(S_, K_)                                                   \
+  do {                                                                                   \
+    static std::atomic<unsigned long long> smem_set{0};                                  \
+    e = ensure_smem_limit(route_tc_kernel<S_, K_>, (int)kSmemBytes, smem_set);           \
+    if (e != cudaSuccess) return e;                                                      \
+    route_tc_kernel<S_, K_><<<grid, THREADS, kSmemBytes, s>>>(mx, mw, T, H, E, EC, logits, tk); \
+  } while (0)
+  if (S == 3 && topk) SEMMOE_ROUTE_TC_LAUNCH(3, true);
+  else if (S == 3) SEMMOE_ROUTE_TC_LAUNCH(3, false);
+  else if (topk) SEMMOE_ROUTE_TC_LAUNCH(1, true);
+  else SEMMOE_ROUTE_TC_LAUNCH(1, false);
+#undef SEMMOE_ROUTE_TC_LAUNCH
   count_launches(1);
   return cudaGetLastError();
 }
