@@ -20,10 +20,9 @@ size_t route_ws_bytes(int T, int H, int E, int x_dtype, int w_dtype);
 // Tensor-core router (route_tc.cu): fp32 logits of bf16 activations.
 int route_tc_take_errors(cudaStream_t s, int* bits);
 size_t route_tc_split_bytes(int H, int E, int w_dtype);
-bool route_tc_fuses_topk(int E, int k_max, int w_dtype);
-cudaError_t launch_route_logits_tc(const void* x, const void* w, int w_dtype, int T, int H, int E, float* logits,
-                                   void* split, const int32_t* k_per_token, int k_uniform, int k_max,
-                                   int32_t* topk_idx, float* topk_w, cudaStream_t s);
+int route_tc_k_slices(int T, int H, int E, int w_dtype);
+cudaError_t launch_route_logits_tc(const void* x, const void* w, int w_dtype, int T, int H, int E, float* partials,
+                                   int ks, void* split, cudaStream_t s);
 cudaError_t launch_route(const void* x, int x_dtype, const void* w, int w_dtype,
                          const float* logits_in, float* logits_out, const int32_t* k_per_token,
                          int k_uniform, int T, int H, int E, int k_max, int32_t* topk_idx,

@@ -35,6 +35,82 @@ __host__ __device__ inline size_t route_smem_bytes(int E, int k_max) {
          (size_t)kWarps * k_max * (sizeof(float) + sizeof(int));
 }
 
+// One warp selects token t's experts from its E logits (shared or global
+// memory; the sum of `ks` partial rows slice_stride floats apart, added in
+// slice order, copied to logits_out when that is set): k_t rounds of a warp argmax over (logit descending, expert index
+// ascending), skipping experts already taken; then the gates, the softmax of
+// the selected logits renormalised over the selection (fp32).  my_v / my_e:
+// k_max floats / ints of scratch for this warp.
+__device__ void warp_topk(const float* row, int ks, size_t slice_stride, float* logits_out, int E, int t,
+                          const int32_t* __restrict__ k_per_token, int k_uniform, int k_max, float* my_v, int* my_e,
+                          int32_t* __restrict__ topk_idx, float* __restrict__ topk_w) {
+  const int lane = threadIdx.x % 32;
+  const int nper = (E + 31) / 32;
+  int kt = k_per_token != nullptr ? k_per_token[t] : k_uniform;
+  if (kt < 1 || kt > k_max) {
+    if (lane == 0) flag(SEMMOE_DEVERR_K);
+    kt = kt < 1 ? 1 : k_max;
+  }
+  float v[kRouteMaxE / 32];
+#pragma unroll
+  for (int i = 0; i < kRouteMaxE / 32; ++i) {
+    float val = -INFINITY;
+    const int e = lane + 32 * i;
+    if (i < nper && e < E) {
+      val = row[e];
+      for (int k = 1; k < ks; ++k) val += row[(size_t)k * slice_stride + e];  // K slices in order
+      if (logits_out != nullptr) logits_out[e] = val;
+      if (!isfinite(val)) {
+        flag(SEMMOE_DEVERR_NONFINITE);
+        val = -INFINITY;
+      }
+    }
+    v[i] = val;
+  }
+  unsigned taken = 0;
+  for (int j = 0; j < kt; ++j) {
+    float bv = -INFINITY;
+    int be = 0x7fffffff;
+#pragma unroll
+    for (int i = 0; i < kRouteMaxE / 32; ++i) {
+      const int e = lane + 32 * i;
+      if (i < nper && e < E && !((taken >> i) & 1u)) {
+        if (v[i] > bv || (v[i] == bv && e < be)) { bv = v[i]; be = e; }
+      }
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+      const float ov = __shfl_xor_sync(0xffffffffu, bv, off);
+      const int oe = __shfl_xor_sync(0xffffffffu, be, off);
+      if (ov > bv || (ov == bv && oe < be)) { bv = ov; be = oe; }
+    }
+    if (be >= E) {  // fewer than kt finite logits
+      if (lane == 0) flag(SEMMOE_DEVERR_NONFINITE);
+      be = -1;
+    } else if ((be & 31) == lane) {
+      taken |= 1u << (be >> 5);
+    }
+    if (lane == 0) { my_v[j] = bv; my_e[j] = be; }
+  }
+  __syncwarp();
+  const float m = my_v[0];
+  float den = 0.f;
+  for (int j = lane; j < kt; j += 32) den += my_e[j] >= 0 ? expf(my_v[j] - m) : 0.f;
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) den += __shfl_xor_sync(0xffffffffu, den, off);
+  for (int j = lane; j < k_max; j += 32) {
+    int e = -1;
+    float g = 0.f;
+    if (j < kt && my_e[j] >= 0) {
+      e = my_e[j];
+      g = expf(my_v[j] - m) / den;
+    }
+    topk_idx[(size_t)t * k_max + j] = e;
+    topk_w[(size_t)t * k_max + j] = g;
+  }
+  __syncwarp();
+}
+
 template <typename TX, typename TW>
 __global__ void __launch_bounds__(kRouteThreads)
 route_kernel(const TX* __restrict__ x, const TW* __restrict__ w, const float* __restrict__ logits_in,
@@ -101,79 +177,33 @@ route_kernel(const TX* __restrict__ x, const TW* __restrict__ w, const float* __
   }
   __syncthreads();
 
-  // Top-k_t per token, one warp per token: repeated warp argmax over
-  // (logit descending, expert index ascending), skipping taken experts.
-  const int warp = tid / 32, lane = tid % 32;
-  float* my_v = sel_v + warp * k_max;
-  int* my_e = sel_e + warp * k_max;
-  const int nper = Epad / 32;
+  // Top-k_t per token, one warp per token.
+  const int warp = tid / 32;
   for (int tl = warp; tl < kRouteTok; tl += kWarps) {
     const int t = t0 + tl;
     if (t >= T) break;
-    int kt = k_per_token != nullptr ? k_per_token[t] : k_uniform;
-    if (kt < 1 || kt > k_max) {
-      if (lane == 0) flag(SEMMOE_DEVERR_K);
-      kt = kt < 1 ? 1 : k_max;
-    }
-    float v[kRouteMaxE / 32];
-#pragma unroll
-    for (int i = 0; i < kRouteMaxE / 32; ++i) {
-      float val = -INFINITY;
-      int e = lane + 32 * i;
-      if (i < nper && e < E) {
-        val = lg[tl * Epad + e];
-        if (!isfinite(val)) {
-          flag(SEMMOE_DEVERR_NONFINITE);
-          val = -INFINITY;
-        }
-      }
-      v[i] = val;
-    }
-    unsigned taken = 0;
-    for (int j = 0; j < kt; ++j) {
-      float bv = -INFINITY;
-      int be = 0x7fffffff;
-#pragma unroll
-      for (int i = 0; i < kRouteMaxE / 32; ++i) {
-        int e = lane + 32 * i;
-        if (i < nper && e < E && !((taken >> i) & 1u)) {
-          if (v[i] > bv || (v[i] == bv && e < be)) { bv = v[i]; be = e; }
-        }
-      }
-#pragma unroll
-      for (int off = 16; off > 0; off >>= 1) {
-        float ov = __shfl_xor_sync(0xffffffffu, bv, off);
-        int oe = __shfl_xor_sync(0xffffffffu, be, off);
-        if (ov > bv || (ov == bv && oe < be)) { bv = ov; be = oe; }
-      }
-      if (be >= E) {  // only when fewer than kt finite candidates exist
-        if (lane == 0) flag(SEMMOE_DEVERR_NONFINITE);
-        be = -1;
-      } else if ((be & 31) == lane) {
-        taken |= 1u << (be >> 5);
-      }
-      if (lane == 0) { my_v[j] = bv; my_e[j] = be; }
-    }
-    __syncwarp();
-    // gates: softmax over the selected logits, renormalised (fp32)
-    const float m = my_v[0];
-    float part = 0.f;
-    for (int j = lane; j < kt; j += 32) part += (my_e[j] >= 0) ? expf(my_v[j] - m) : 0.f;
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) part += __shfl_xor_sync(0xffffffffu, part, off);
-    const float inv_den = part;
-    for (int j = lane; j < k_max; j += 32) {
-      int e = -1;
-      float g = 0.f;
-      if (j < kt && my_e[j] >= 0) {
-        e = my_e[j];
-        g = expf(my_v[j] - m) / inv_den;
-      }
-      topk_idx[(size_t)t * k_max + j] = e;
-      topk_w[(size_t)t * k_max + j] = g;
-    }
-    __syncwarp();
+    warp_topk(lg + tl * Epad, 1, 0, nullptr, E, t, k_per_token, k_uniform, k_max, sel_v + warp * k_max,
+              sel_e + warp * k_max, topk_idx, topk_w);
   }
+}
+
+// Top-k of precomputed fp32 logits [T,E] (the sum of ks partial [T,E] slices):
+// one warp per token, 8 tokens per CTA,
+// so every token's (latency-bound) selection runs concurrently with the others.
+constexpr int kTopkWarps = 8;
+
+__global__ void __launch_bounds__(kTopkWarps * 32)
+topk_kernel(const float* __restrict__ logits, int ks, float* __restrict__ logits_out,
+            const int32_t* __restrict__ k_per_token, int k_uniform, int T, int E, int k_max,
+            int32_t* __restrict__ topk_idx, float* __restrict__ topk_w) {
+  extern __shared__ __align__(16) unsigned char smem_raw[];
+  float* sel_v = reinterpret_cast<float*>(smem_raw);
+  int* sel_e = reinterpret_cast<int*>(sel_v + kTopkWarps * k_max);
+  const int warp = threadIdx.x / 32;
+  const int t = blockIdx.x * kTopkWarps + warp;
+  if (t >= T) return;
+  warp_topk(logits + (size_t)t * E, ks, (size_t)T * E, logits_out != nullptr ? logits_out + (size_t)t * E : nullptr,
+            E, t, k_per_token, k_uniform, k_max, sel_v + warp * k_max, sel_e + warp * k_max, topk_idx, topk_w);
 }
 
 __global__ void affinity_lookup_kernel(const int32_t* __restrict__ ids, const int32_t* __restrict__ lut,
@@ -302,32 +332,42 @@ int route_take_errors(cudaStream_t s, int* bits) {
 // CUDA-core kernel that fuses the GEMM with the top-k.
 static bool route_on_tensor_cores(int x_dtype, int H) { return x_dtype == SEMMOE_BF16 && H % 8 == 0; }
 
-// Workspace: [fp32 logits T x E][three-part bf16 split of an fp32 router weight].
+// Workspace: [fp32 partial logits ks x T x E][three-part bf16 split of an fp32 router weight].
+static size_t route_partials_bytes(int T, int H, int E, int w_dtype) {
+  return align_up((size_t)route_tc_k_slices(T, H, E, w_dtype) * (T > 0 ? T : 1) * E * sizeof(float), 256);
+}
+
 size_t route_ws_bytes(int T, int H, int E, int x_dtype, int w_dtype) {
   if (!route_on_tensor_cores(x_dtype, H)) return 0;
-  return align_up((size_t)(T > 0 ? T : 1) * E * sizeof(float), 256) + route_tc_split_bytes(H, E, w_dtype);
+  return route_partials_bytes(T, H, E, w_dtype) + route_tc_split_bytes(H, E, w_dtype);
 }
 
 cudaError_t launch_route(const void* x, int x_dtype, const void* w, int w_dtype, const float* logits_in,
                          float* logits_out, const int32_t* kpt, int k_uniform, int T, int H, int E, int k_max,
                          int32_t* topk_idx, float* topk_w, void* ws, cudaStream_t s) {
   if (T == 0) return cudaSuccess;
+  int ks = 1;
   if (logits_in == nullptr && route_on_tensor_cores(x_dtype, H)) {
     unsigned char* w8 = static_cast<unsigned char*>(ws);
-    void* split = w8 + align_up((size_t)T * E * sizeof(float), 256);
-    if (route_tc_fuses_topk(E, k_max, w_dtype))  // GEMM, top-k and gates in one kernel
-      return launch_route_logits_tc(x, w, w_dtype, T, H, E, logits_out, split, kpt, k_uniform, k_max, topk_idx,
-                                    topk_w, s);
-    float* lg = logits_out != nullptr ? logits_out : reinterpret_cast<float*>(w8);
-    cudaError_t e = launch_route_logits_tc(x, w, w_dtype, T, H, E, lg, split, nullptr, 0, k_max, nullptr,
-                                           nullptr, s);
+    float* partials = reinterpret_cast<float*>(w8);
+    void* split = w8 + route_partials_bytes(T, H, E, w_dtype);
+    ks = route_tc_k_slices(T, H, E, w_dtype);
+    cudaError_t e = launch_route_logits_tc(x, w, w_dtype, T, H, E, partials, ks, split, s);
     if (e != cudaSuccess) return e;
-    logits_in = lg;
+    const int kb_all = (H + 63) / 64, per = (kb_all + ks - 1) / ks;
+    ks = (kb_all + per - 1) / per;  // the slices the launcher actually used
+    logits_in = partials;
+  } else if (logits_in != nullptr && logits_out == logits_in) {
     logits_out = nullptr;
   }
-  if (logits_in != nullptr)  // top-k of the given logits (x and w unused)
-    return launch_route_t<float, float>(nullptr, nullptr, logits_in, logits_out, kpt, k_uniform, T, H, E,
-                                        k_max, topk_idx, topk_w, s);
+  if (logits_in != nullptr) {  // top-k of the (summed) logits; x and w unused here
+    const size_t sm = (size_t)kTopkWarps * k_max * (sizeof(float) + sizeof(int));
+    topk_kernel<<<(T + kTopkWarps - 1) / kTopkWarps, kTopkWarps * 32, sm, s>>>(logits_in, ks, logits_out, kpt,
+                                                                               k_uniform, T, E, k_max, topk_idx,
+                                                                               topk_w);
+    count_launches(1);
+    return cudaGetLastError();
+  }
   if (x_dtype == SEMMOE_BF16 && w_dtype == SEMMOE_F32)
     return launch_route_t<__nv_bfloat16, float>(x, w, nullptr, logits_out, kpt, k_uniform, T, H, E, k_max,
                                                 topk_idx, topk_w, s);

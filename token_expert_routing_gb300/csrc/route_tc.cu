@@ -13,9 +13,10 @@
 //
 // One CTA per (128-token tile, pass of EC experts); warp 0 issues TMA, warp 1
 // allocates TMEM and issues the MMAs, warps 2..5 read the accumulator and write
-// fp32 logits.  When every expert fits one pass and k_max <= 16, the epilogue
-// also does the top-k and the gates (one token per thread), so the logits never
-// go through memory.  Waits are bounded as in the grouped-FFN kernel.
+// fp32 logits.  The operand ring has as many stages (up to 8) as fit 200 KB, so
+// a CTA keeps as many loads in flight as the tile size allows: the GEMM is
+// small and the ring depth is what hides HBM latency.  Waits are bounded as in
+// the grouped-FFN kernel.
 #include "common.cuh"
 #include "internal.h"
 #include "tc_common.cuh"
@@ -27,19 +28,21 @@ using namespace tc;
 
 __device__ int g_err;
 
-constexpr int BM = 128, BK = 64, UK = 16, STAGES = 4, THREADS = 192;
+constexpr int BM = 128, BK = 64, UK = 16, THREADS = 192;
+constexpr int MAX_STAGES = 8;
 constexpr int A_BYTES = BM * BK * 2;            // 16 KB
 constexpr int MAX_NB = 256;                     // MMA N limit
-constexpr int B_BYTES_MAX = MAX_NB * BK * 2;    // 32 KB
+constexpr size_t kStageBudget = 200 * 1024;     // operand ring
 constexpr uint32_t TMEM_COLS = 256;
+constexpr int kMaxKSlices = 8;
 
 struct Shared {
-  uint64_t full[STAGES], empty[STAGES], tfull, done;
+  uint64_t full[MAX_STAGES], empty[MAX_STAGES], tfull, done;
   uint32_t tmem_base;
   int abort_flag;
 };
 
-constexpr size_t kSmemBytes = 1024 + (size_t)STAGES * (A_BYTES + B_BYTES_MAX) + sizeof(Shared);
+constexpr size_t kSmemBytes = 1024 + kStageBudget + sizeof(Shared);
 
 // Experts per pass: S * EC <= 256 columns, EC a multiple of 16.
 inline int experts_per_pass(int E, int S) {
@@ -71,35 +74,28 @@ __global__ void split_router_kernel(const float* __restrict__ w, int E, int H, i
   }
 }
 
-// Outputs of the fused top-k (every field unused unless TOPK).
-struct TopkOut {
-  const int32_t* k_per_token;  // nullable: k_uniform then
-  int k_uniform, k_max;
-  int32_t* topk_idx;
-  float* topk_w;
-};
-
-constexpr int KREG = 16;  // largest k_max the fused top-k keeps in registers
-
-template <int S, bool TOPK>
+template <int S>
 __global__ void __launch_bounds__(THREADS, 1)
 route_tc_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_constant__ CUtensorMap map_w, int T, int H,
-                int E, int EC, float* __restrict__ logits, TopkOut tk) {
+                int E, int EC, int stages, int kb_per_slice, float* __restrict__ partials) {
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   const uint32_t pad = (1024u - (smem_u32(smem_raw) & 1023u)) & 1023u;
-  unsigned char* stage_a = smem_raw + pad;
-  unsigned char* stage_b = stage_a + STAGES * A_BYTES;
-  Shared& sh = *reinterpret_cast<Shared*>(stage_b + STAGES * B_BYTES_MAX);
+  unsigned char* ring = smem_raw + pad;  // stage s: A tile then B tile, stage_bytes apart
+  Shared& sh = *reinterpret_cast<Shared*>(ring + kStageBudget);
   volatile int* abort_flag = &sh.abort_flag;
 
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   const int NB = S * EC;
   const uint32_t b_bytes = (uint32_t)NB * BK * 2;
-  const int t0 = blockIdx.x * BM, pass = blockIdx.y;
-  const int kb_n = (H + BK - 1) / BK;
+  const uint32_t stage_bytes = A_BYTES + b_bytes;  // a multiple of 1024 (NB % 16 == 0)
+  const int t0 = blockIdx.x * BM, pass = blockIdx.y, slice = blockIdx.z;
+  const int kb_all = (H + BK - 1) / BK;
+  const int kb0 = slice * kb_per_slice;
+  const int kb_n = kb_all - kb0 < kb_per_slice ? kb_all - kb0 : kb_per_slice;  // >= 1 by construction
+  float* logits = partials + (size_t)slice * T * E;  // this K slice's partial sums
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < STAGES; ++s) {
+    for (int s = 0; s < stages; ++s) {
       mbar_init(&sh.full[s], 1);
       mbar_init(&sh.empty[s], 1);
     }
@@ -120,28 +116,29 @@ route_tc_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_constant
     if (lane == 0) {  // TMA producer
       int it = 0;
       for (int kb = 0; kb < kb_n; ++kb) {
-        const int s = kb % STAGES;
-        const uint32_t ph = (kb / STAGES) & 1;
+        const int s = kb % stages;
+        const uint32_t ph = (kb / stages) & 1;
         if (!mbar_wait(&sh.empty[s], ph ^ 1, abort_flag, &g_err)) break;
-        mbar_expect_tx(&sh.full[s], A_BYTES + b_bytes);
-        tma_load_2d(stage_a + s * A_BYTES, &map_x, &sh.full[s], kb * BK, t0);
-        tma_load_2d(stage_b + s * B_BYTES_MAX, &map_w, &sh.full[s], kb * BK, pass * NB);
+        unsigned char* st = ring + (size_t)s * stage_bytes;
+        mbar_expect_tx(&sh.full[s], stage_bytes);
+        tma_load_2d(st, &map_x, &sh.full[s], (kb0 + kb) * BK, t0);
+        tma_load_2d(st + A_BYTES, &map_w, &sh.full[s], (kb0 + kb) * BK, pass * NB);
         ++it;
       }
       if (*abort_flag)
-        for (int j = it > STAGES ? it - STAGES : 0; j < it; ++j)
-          mbar_drain(&sh.full[j % STAGES], (j / STAGES) & 1, &g_err);
+        for (int j = it > stages ? it - stages : 0; j < it; ++j)
+          mbar_drain(&sh.full[j % stages], (j / stages) & 1, &g_err);
     }
   } else if (warp == 1) {
     if (lane == 0) {  // MMA issuer
       const uint32_t idesc = idesc_bf16_f32(BM, NB);
       bool ok = true;
       for (int kb = 0; kb < kb_n; ++kb) {
-        const int s = kb % STAGES;
-        const uint32_t ph = (kb / STAGES) & 1;
+        const int s = kb % stages;
+        const uint32_t ph = (kb / stages) & 1;
         if (!mbar_wait(&sh.full[s], ph, abort_flag, &g_err)) { ok = false; break; }
         fence_after();
-        const uint32_t sa = smem_u32(stage_a + s * A_BYTES), sb = smem_u32(stage_b + s * B_BYTES_MAX);
+        const uint32_t sa = smem_u32(ring + (size_t)s * stage_bytes), sb = sa + A_BYTES;
 #pragma unroll
         for (int k = 0; k < BK / UK; ++k)
           mma_bf16(tmem, sw128_desc(sa + k * UK * 2), sw128_desc(sb + k * UK * 2), idesc, (kb | k) != 0);
@@ -159,15 +156,7 @@ route_tc_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_constant
     if (ok) {
       fence_after();
       const uint32_t trow = tmem + ((uint32_t)(q * 32) << 16);
-      float* lrow = logits != nullptr ? logits + (size_t)(t < T ? t : 0) * E : nullptr;
-      // Fused top-k (single pass, experts in ascending order): a register list
-      // sorted by logit descending; a new logit enters only if strictly larger
-      // than the last entry and bubbles past strictly smaller ones, so equal
-      // logits keep the lower expert index first.
-      float bv[TOPK ? KREG : 1];
-      int be[TOPK ? KREG : 1];
-#pragma unroll
-      for (int i = 0; i < (TOPK ? KREG : 1); ++i) { bv[i] = -INFINITY; be[i] = -1; }
+      float* lrow = logits + (size_t)(t < T ? t : 0) * E;
       for (int c = 0; c < EC; c += 16) {
         uint32_t v0[16], v1[16], v2[16];
         tmem_ld16(trow + c, v0);
@@ -183,49 +172,8 @@ route_tc_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_constant
             if (e < E) {
               float l = __uint_as_float(v0[i]);
               if (S == 3) l = (l + __uint_as_float(v1[i])) + __uint_as_float(v2[i]);
-              if (lrow != nullptr) lrow[e] = l;
-              if (TOPK) {
-                if (!isfinite(l)) {
-                  atomicOr(&g_err, SEMMOE_DEVERR_NONFINITE);
-                  l = -INFINITY;
-                }
-                if (l > bv[KREG - 1]) {
-                  bv[KREG - 1] = l;
-                  be[KREG - 1] = e;
-#pragma unroll
-                  for (int j = KREG - 1; j > 0; --j) {
-                    if (bv[j] > bv[j - 1]) {
-                      const float tv = bv[j]; bv[j] = bv[j - 1]; bv[j - 1] = tv;
-                      const int te = be[j]; be[j] = be[j - 1]; be[j - 1] = te;
-                    }
-                  }
-                }
-              }
+              lrow[e] = l;
             }
-          }
-        }
-      }
-      if (TOPK && t < T) {
-        int kt = tk.k_per_token != nullptr ? tk.k_per_token[t] : tk.k_uniform;
-        if (kt < 1 || kt > tk.k_max) {
-          atomicOr(&g_err, SEMMOE_DEVERR_K);
-          kt = kt < 1 ? 1 : tk.k_max;
-        }
-        // gates: softmax over the selected logits, renormalised (fp32)
-        const float m = bv[0];
-        float den = 0.f;
-#pragma unroll
-        for (int j = 0; j < KREG; ++j)
-          if (j < kt && be[j] >= 0) den += expf(bv[j] - m);
-        int32_t* irow = tk.topk_idx + (size_t)t * tk.k_max;
-        float* wrow = tk.topk_w + (size_t)t * tk.k_max;
-#pragma unroll
-        for (int j = 0; j < KREG; ++j) {
-          if (j < tk.k_max) {
-            const bool live = j < kt && be[j] >= 0;
-            if (j < kt && be[j] < 0) atomicOr(&g_err, SEMMOE_DEVERR_NONFINITE);
-            irow[j] = live ? be[j] : -1;
-            wrow[j] = live ? expf(bv[j] - m) / den : 0.f;
           }
         }
       }
@@ -252,22 +200,29 @@ size_t route_tc_split_bytes(int H, int E, int w_dtype) {
   return align_up((size_t)n_pass * 3 * EC * H * 2, 256);
 }
 
-// Whether the top-k can run in the router kernel's epilogue: every expert in
-// one pass and k_max within the register list.
-bool route_tc_fuses_topk(int E, int k_max, int w_dtype) {
-  const int S = w_dtype == SEMMOE_F32 ? 3 : 1;
-  return E <= experts_per_pass(E, S) && k_max <= KREG;
-}
-
-// x [T,H] bf16 (H % 8 == 0); w [E,H] fp32 or bf16; split: workspace of
-// route_tc_split_bytes() (fp32 weight only).  Writes logits [T,E] (nullable
-// when topk_idx is set) and, when topk_idx != nullptr (only if
-// route_tc_fuses_topk), the top-k indices and gates.
-cudaError_t launch_route_logits_tc(const void* x, const void* w, int w_dtype, int T, int H, int E, float* logits,
-                                   void* split, const int32_t* k_per_token, int k_uniform, int k_max,
-                                   int32_t* topk_idx, float* topk_w, cudaStream_t s) {
+// K slices of the router GEMM: enough (token tile, pass, slice) CTAs to fill
+// the GPU once, with at least 4 k-blocks of H per slice.
+int route_tc_k_slices(int T, int H, int E, int w_dtype) {
   const int S = w_dtype == SEMMOE_F32 ? 3 : 1;
   const int EC = experts_per_pass(E, S), n_pass = (E + EC - 1) / EC;
+  const long long ctas = (long long)((T + BM - 1) / BM) * n_pass;
+  const int kb_all = (H + BK - 1) / BK;
+  int ks = (int)(tc::sm_count() / (ctas > 0 ? ctas : 1));
+  if (ks > kb_all / 4) ks = kb_all / 4;
+  if (ks > kMaxKSlices) ks = kMaxKSlices;
+  return ks < 1 ? 1 : ks;
+}
+
+// x [T,H] bf16 (H % 8 == 0); w [E,H] fp32 or bf16; partials [ks][T][E] fp32
+// out (ks = route_tc_k_slices(); the logits are their sum in slice order);
+// split: workspace of route_tc_split_bytes() (fp32 weight only).
+cudaError_t launch_route_logits_tc(const void* x, const void* w, int w_dtype, int T, int H, int E, float* partials,
+                                   int ks, void* split, cudaStream_t s) {
+  const int S = w_dtype == SEMMOE_F32 ? 3 : 1;
+  const int EC = experts_per_pass(E, S), n_pass = (E + EC - 1) / EC;
+  const int kb_all = (H + BK - 1) / BK;
+  const int kb_per_slice = (kb_all + ks - 1) / ks;
+  ks = (kb_all + kb_per_slice - 1) / kb_per_slice;  // every slice non-empty
   const void* wb = w;
   int w_rows = E;
   if (S == 3) {
@@ -295,22 +250,22 @@ cudaError_t launch_route_logits_tc(const void* x, const void* w, int w_dtype, in
     const cuuint32_t box[2] = {BK, (cuuint32_t)(S * EC)};
     if (!make_map_bf16(&mw, wb, 2, dims, str, box)) return cudaErrorInvalidValue;
   }
-  const TopkOut tk{k_per_token, k_uniform, k_max, topk_idx, topk_w};
-  const bool topk = topk_idx != nullptr;
-  dim3 grid((T + BM - 1) / BM, n_pass);
+  const size_t stage_bytes = A_BYTES + (size_t)S * EC * BK * 2;
+  int stages = (int)(kStageBudget / stage_bytes);
+  if (stages > MAX_STAGES) stages = MAX_STAGES;
+  dim3 grid((T + BM - 1) / BM, n_pass, ks);
   cudaError_t e;
-#define SEMMOE_ROUTE_TC_LAUNCH(S_, K_)                                                   \
-  do {                                                                                   \
-    static std::atomic<unsigned long long> smem_set{0};                                  \
-    e = ensure_smem_limit(route_tc_kernel<S_, K_>, (int)kSmemBytes, smem_set);           \
-    if (e != cudaSuccess) return e;                                                      \
-    route_tc_kernel<S_, K_><<<grid, THREADS, kSmemBytes, s>>>(mx, mw, T, H, E, EC, logits, tk); \
-  } while (0)
-  if (S == 3 && topk) SEMMOE_ROUTE_TC_LAUNCH(3, true);
-  else if (S == 3) SEMMOE_ROUTE_TC_LAUNCH(3, false);
-  else if (topk) SEMMOE_ROUTE_TC_LAUNCH(1, true);
-  else SEMMOE_ROUTE_TC_LAUNCH(1, false);
-#undef SEMMOE_ROUTE_TC_LAUNCH
+  if (S == 3) {
+    static std::atomic<unsigned long long> smem_set{0};
+    e = ensure_smem_limit(route_tc_kernel<3>, (int)kSmemBytes, smem_set);
+    if (e != cudaSuccess) return e;
+    route_tc_kernel<3><<<grid, THREADS, kSmemBytes, s>>>(mx, mw, T, H, E, EC, stages, kb_per_slice, partials);
+  } else {
+    static std::atomic<unsigned long long> smem_set{0};
+    e = ensure_smem_limit(route_tc_kernel<1>, (int)kSmemBytes, smem_set);
+    if (e != cudaSuccess) return e;
+    route_tc_kernel<1><<<grid, THREADS, kSmemBytes, s>>>(mx, mw, T, H, E, EC, stages, kb_per_slice, partials);
+  }
   count_launches(1);
   return cudaGetLastError();
 }
