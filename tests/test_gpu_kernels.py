@@ -225,3 +225,25 @@ def test_route_tensor_core_per_token_budgets(E, k_max, wd):
     ref_idx, ref_w = oracle.topk_route(np_(lg), kpt, k_max)
     np.testing.assert_array_equal(np_(idx), ref_idx)
     np.testing.assert_allclose(np_(gw), ref_w, rtol=0, atol=GATE_ATOL)
+
+
+@pytest.mark.parametrize("P,E,H,I", [(1000, 8, 256, 160), (5000, 64, 512, 352)])
+def test_grouped_ffn_cluster_pair_matches_single_cta(P, E, H, I, monkeypatch):
+    """The cluster-of-2 grouped GEMM (weight tiles shared by TMA multicast)
+    returns exactly what the single-CTA kernel returns."""
+    rng = np.random.default_rng(P + E)
+    cnt = rng.multinomial(P, np.full(E, 1.0 / E))
+    off = torch.from_numpy(np.r_[0, np.cumsum(cnt)].astype(np.int32)).cuda()
+    pe = torch.from_numpy(rng.permutation(E).astype(np.int32)).cuda()
+    x = torch.from_numpy(rng.standard_normal((P, H)).astype(np.float32)).to(torch.bfloat16).cuda()
+    w13 = torch.from_numpy((rng.standard_normal((E, 2 * I, H)) / np.sqrt(H)).astype(np.float32)).to(torch.bfloat16).cuda()
+    w2 = torch.from_numpy((rng.standard_normal((E, H, I)) / np.sqrt(I)).astype(np.float32)).to(torch.bfloat16).cuda()
+    ws = torch.empty(abi().semmoe_grouped_ffn_workspace_size(P, I, 1), dtype=torch.uint8, device="cuda")
+    outs = []
+    for cl in ("1", "2"):
+        monkeypatch.setenv("SEMMOE_FFN_CLUSTER", cl)
+        y = torch.empty(P, H, dtype=torch.bfloat16, device="cuda")
+        abi().semmoe_grouped_ffn(x, off, pe, w13, w2, P, E, H, I, y, ws)
+        assert abi().semmoe_check_errors() == 0
+        outs.append(y.cpu())
+    assert torch.equal(outs[0], outs[1])

@@ -18,10 +18,19 @@
 // accumulator columns [0,128) hold x W1^T and [128,256) hold x W3^T for the
 // same 128 h-columns.
 //
+// A second variant runs clusters of two CTAs on two m-tiles of the same expert
+// and n-tile: each CTA loads half of the shared weight tile and multicasts it to
+// both (SEMMOE_FFN_CLUSTER=2).  It halves L2 reads of the weights but not the
+// shared-memory traffic per SM (TMA writes + MMA operand reads), which is what
+// bounds this single-SM M128xN256 tile, and the pair runs in lock-step; it
+// measured slower, so independent CTAs are the default.
+//
 // Every wait is bounded (%globaltimer); a wait that runs out sets the timeout
 // bit of the device error word and an abort flag, after which every role
 // stops, in-flight TMA loads and MMAs are drained (again with a bound), and
 // TMEM is freed before the CTA exits.
+#include <stdlib.h>
+
 #include "common.cuh"
 #include "internal.h"
 #include "tc_common.cuh"
@@ -65,21 +74,26 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   return *reinterpret_cast<uint32_t*>(&v);
 }
 
-// m-tile -> (group, first row, valid rows, expert), from the per-CTA tables.
-__device__ __forceinline__ void decode_mtile(const Shared& sh, int G, int mt, int& row0, int& rows, int& e) {
-  int lo = 0, hi = G - 1;  // largest g with tp[g] <= mt
+// Tile unit mu (CL consecutive m-tiles of one group, one per CTA of the
+// cluster) -> this CTA's (first row, valid rows, expert).  A CTA whose m-tile
+// lies past its group's end gets rows = 0 (it still takes part in the loads).
+template <int CL>
+__device__ __forceinline__ void decode_mtile(const Shared& sh, int G, int mu, int rank, int& row0, int& rows,
+                                             int& e) {
+  int lo = 0, hi = G - 1;  // largest g with tp[g] <= mu
   while (lo < hi) {
     const int mid = (lo + hi + 1) >> 1;
-    if (sh.tp[mid] <= mt) lo = mid;
+    if (sh.tp[mid] <= mu) lo = mid;
     else hi = mid - 1;
   }
-  row0 = sh.off[lo] + (mt - sh.tp[lo]) * BM;
+  row0 = sh.off[lo] + ((mu - sh.tp[lo]) * CL + rank) * BM;
   const int left = sh.off[lo + 1] - row0;
-  rows = left < BM ? left : BM;
+  rows = left <= 0 ? 0 : (left < BM ? left : BM);
+  if (left <= 0) row0 = sh.off[lo + 1];
   e = sh.pe[lo];
 }
 
-template <bool GLU>
+template <bool GLU, int CL>
 __global__ void __launch_bounds__(THREADS, 1)
 ffn_tc_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b,
               const int32_t* __restrict__ offsets, const int32_t* __restrict__ phys_to_expert, int G, int P,
@@ -96,7 +110,7 @@ ffn_tc_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(&sh.full[s], 1);
-      mbar_init(&sh.empty[s], 1);
+      mbar_init(&sh.empty[s], CL);  // released by the MMA of every CTA that reads this stage
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(&sh.tfull[a], 1);
@@ -124,7 +138,7 @@ ffn_tc_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__
       if (g < G) {
         const int lo = sh.off[g], hi = sh.off[g + 1], e = sh.pe[g];
         if (lo < 0 || hi < lo || hi > P || e < 0 || e >= E) atomicOr(&g_err, SEMMOE_DEVERR_PAIRS);
-        else c = (hi - lo + BM - 1) / BM;
+        else c = ((hi - lo + BM - 1) / BM + CL - 1) / CL;
       }
       cnt[i] = c;
       sum += c;
@@ -150,20 +164,24 @@ ffn_tc_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__
   fence_before();
   __syncthreads();
   fence_after();
+  if (CL > 1) cluster_sync_all();  // the peers' barriers exist before any multicast reaches them
 
   const uint32_t tmem = sh.tmem_base;
-  const int total = sh.total_mtiles * n_tiles;
+  const int total = sh.total_mtiles * n_tiles;  // tile units: (CL m-tiles, n-tile)
   const int kb_n = (K + BK - 1) / BK;
+  const int rank = CL > 1 ? (int)cluster_ctarank() : 0;
+  const int unit0 = blockIdx.x / CL, units = gridDim.x / CL;
+  constexpr uint16_t kAll = (uint16_t)((1u << CL) - 1);
 
   if (warp == 0) {
     if (lane == 0) {
       // ---------------- TMA producer ----------------
       uint32_t it = 0;
-      for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
+      for (int tile = unit0; tile < total; tile += units) {
         if (*abort_flag) break;
         const int mt = tile / n_tiles, nt = tile % n_tiles;
         int row0, rows, e;
-        decode_mtile(sh, G, mt, row0, rows, e);
+        decode_mtile<CL>(sh, G, mt, rank, row0, rows, e);
         bool ok = true;
         for (int kb = 0; kb < kb_n; ++kb) {
           const int s = it % STAGES;
@@ -171,12 +189,20 @@ ffn_tc_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__
           if (!mbar_wait(&sh.empty[s], ph ^ 1, abort_flag, &g_err)) { ok = false; break; }
           mbar_expect_tx(&sh.full[s], STAGE_BYTES);
           tma_load_2d(stage_a + s * A_BYTES, &map_a, &sh.full[s], kb * BK, row0);
-          if (GLU) {
-            unsigned char* b = stage_b + s * B_BYTES;
-            tma_load_4d(b, &map_b, &sh.full[s], kb * BK, nt * 128, 0, e);
-            tma_load_4d(b + B_BYTES / 2, &map_b, &sh.full[s], kb * BK, nt * 128, 1, e);
-          } else {
-            tma_load_3d(stage_b + s * B_BYTES, &map_b, &sh.full[s], kb * BK, nt * BN, e);
+          unsigned char* b = stage_b + s * B_BYTES;
+          if (CL == 1) {
+            if (GLU) {
+              tma_load_4d(b, &map_b, &sh.full[s], kb * BK, nt * 128, 0, e);
+              tma_load_4d(b + B_BYTES / 2, &map_b, &sh.full[s], kb * BK, nt * 128, 1, e);
+            } else {
+              tma_load_3d(b, &map_b, &sh.full[s], kb * BK, nt * BN, e);
+            }
+          } else {  // CTA `rank` loads half `rank` of the shared weight tile for both CTAs
+            if (GLU)
+              tma_load_4d_mc(b + rank * (B_BYTES / 2), &map_b, &sh.full[s], kb * BK, nt * 128, rank, e, kAll);
+            else
+              tma_load_3d_mc(b + rank * (B_BYTES / 2), &map_b, &sh.full[s], kb * BK, nt * BN + rank * 128, e,
+                             kAll);
           }
           ++it;
         }
@@ -191,7 +217,7 @@ ffn_tc_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__
     if (lane == 0) {
       // ---------------- MMA issuer ----------------
       uint32_t it = 0, acc_it = 0;
-      for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
+      for (int tile = unit0; tile < total; tile += units) {
         if (*abort_flag) break;
         const uint32_t a = acc_it & 1, aph = (acc_it >> 1) & 1;
         if (!mbar_wait(&sh.tempty[a], aph ^ 1, abort_flag, &g_err)) break;
@@ -207,7 +233,8 @@ ffn_tc_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__
 #pragma unroll
           for (int k = 0; k < BK / UK; ++k)
             mma_bf16(d, sw128_desc(sa + k * UK * 2), sw128_desc(sb + k * UK * 2), kIdesc, (kb | k) != 0);
-          commit(&sh.empty[s]);  // frees the stage once these MMAs have read it
+          if (CL == 1) commit(&sh.empty[s]);  // frees the stage once these MMAs have read it
+          else commit_mc(&sh.empty[s], kAll);  // in every CTA whose producer writes this stage
           ++it;
         }
         if (!ok) break;
@@ -222,10 +249,10 @@ ffn_tc_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__
     const int q = warp & 3;           // TMEM lane quarter this warp may access
     const int r = q * 32 + lane;      // tile row held by this thread
     uint32_t acc_it = 0;
-    for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
+    for (int tile = unit0; tile < total; tile += units) {
       const int mt = tile / n_tiles, nt = tile % n_tiles;
       int row0, rows, e;
-      decode_mtile(sh, G, mt, row0, rows, e);
+      decode_mtile<CL>(sh, G, mt, rank, row0, rows, e);
       const uint32_t a = acc_it & 1, aph = (acc_it >> 1) & 1;
       int ok = 1;
       if (lane == 0) ok = mbar_wait(&sh.tfull[a], aph, abort_flag, &g_err);
@@ -292,6 +319,7 @@ ffn_tc_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__
 
   fence_before();
   __syncthreads();
+  if (CL > 1) cluster_sync_all();  // no peer still multicasts into, or arrives on, this CTA
   if (warp == 1) {
     __syncwarp();
     fence_after();
@@ -302,17 +330,41 @@ ffn_tc_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__
 // ---------------------------------------------------------------------------
 // host side
 // ---------------------------------------------------------------------------
-template <bool GLU>
+template <bool GLU, int CL>
 cudaError_t launch_one(const CUtensorMap& ma, const CUtensorMap& mb, const int32_t* offsets, const int32_t* p2e,
                        int G, int P, int E, int N, int K, int n_tiles, __nv_bfloat16* out, cudaStream_t s) {
-  auto kern = ffn_tc_kernel<GLU>;
+  auto kern = ffn_tc_kernel<GLU, CL>;
   static std::atomic<unsigned long long> smem_set{0};
   cudaError_t e = ensure_smem_limit(kern, (int)kSmemBytes, smem_set);
   if (e != cudaSuccess) return e;
-  const long long max_tiles = ((long long)(P + BM - 1) / BM + G) * n_tiles;
-  int grid = sm_count();
-  if (max_tiles < grid) grid = (int)max_tiles;
-  kern<<<grid, THREADS, kSmemBytes, s>>>(ma, mb, offsets, p2e, G, P, E, N, K, n_tiles, out);
+  const long long max_units = ((long long)(P + BM - 1) / BM + G) * n_tiles;  // >= tile units of any grouping
+  if (CL == 1) {
+    int grid = sm_count();
+    if (max_units < grid) grid = (int)max_units;
+    kern<<<grid, THREADS, kSmemBytes, s>>>(ma, mb, offsets, p2e, G, P, E, N, K, n_tiles, out);
+  } else {
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = CL;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.blockDim = dim3(THREADS);
+    cfg.dynamicSmemBytes = kSmemBytes;
+    cfg.stream = s;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cfg.gridDim = dim3(sm_count() / CL * CL);
+    int clusters = 0;  // as many clusters as can be resident at once
+    e = cudaOccupancyMaxActiveClusters(&clusters, kern, &cfg);
+    if (e != cudaSuccess) return e;
+    if (clusters < 1) return cudaErrorInvalidConfiguration;
+    long long units = clusters;
+    if (max_units < units) units = max_units;
+    cfg.gridDim = dim3((unsigned)(units * CL));
+    e = cudaLaunchKernelEx(&cfg, kern, ma, mb, offsets, p2e, G, P, E, N, K, n_tiles, out);
+    if (e != cudaSuccess) return e;
+  }
   count_launches(1);
   return cudaGetLastError();
 }
@@ -321,11 +373,21 @@ cudaError_t launch_one(const CUtensorMap& ma, const CUtensorMap& mb, const int32
 
 int ffn_tc_take_errors(cudaStream_t s, int* bits) { return take_error_word(g_err, s, bits); }
 
+// CTAs per cluster of the grouped GEMM: 2 (the pair shares each weight tile
+// through TMA multicast) unless SEMMOE_FFN_CLUSTER=1 asks for independent CTAs.
+static int ffn_cluster_size() {
+  const char* v = getenv("SEMMOE_FFN_CLUSTER");
+  if (v != nullptr && v[0] == '1' && v[1] == 0) return 1;
+  if (v != nullptr && v[0] == '2' && v[1] == 0) return 2;
+  return 1;
+}
+
 // x [P,H], w13 [E,2I,H], w2 [E,H,I], h (workspace) [P,I], y [P,H]; all bf16.
 cudaError_t launch_ffn_tc(const void* x, const int32_t* offsets, const int32_t* p2e, const void* w13,
                           const void* w2, int P, int E, int H, int I, void* y, void* ws, cudaStream_t s) {
   if (P == 0) return cudaSuccess;
   const int G = offsets ? E : 1;
+  const int CL = ffn_cluster_size();
   const cuuint64_t es = 2;
   CUtensorMap ma1, mb1, ma2, mb2;
   {
@@ -349,14 +411,20 @@ cudaError_t launch_ffn_tc(const void* x, const int32_t* offsets, const int32_t* 
   {
     const cuuint64_t dims[3] = {(cuuint64_t)I, (cuuint64_t)H, (cuuint64_t)E};
     const cuuint64_t str[2] = {(cuuint64_t)I * es, (cuuint64_t)H * I * es};
-    const cuuint32_t box[3] = {BK, BN, 1};
+    const cuuint32_t box[3] = {BK, (cuuint32_t)(BN / CL), 1};  // a cluster CTA loads 1/CL of the tile
     if (!make_map_bf16(&mb2, w2, 3, dims, str, box)) return cudaErrorInvalidValue;
   }
   __nv_bfloat16* h = static_cast<__nv_bfloat16*>(ws);
-  cudaError_t e = launch_one<true>(ma1, mb1, offsets, p2e, G, P, E, I, H, (I + 127) / 128, h, s);
+  __nv_bfloat16* yb = static_cast<__nv_bfloat16*>(y);
+  cudaError_t e;
+  if (CL == 2) {
+    e = launch_one<true, 2>(ma1, mb1, offsets, p2e, G, P, E, I, H, (I + 127) / 128, h, s);
+    if (e != cudaSuccess) return e;
+    return launch_one<false, 2>(ma2, mb2, offsets, p2e, G, P, E, H, I, (H + BN - 1) / BN, yb, s);
+  }
+  e = launch_one<true, 1>(ma1, mb1, offsets, p2e, G, P, E, I, H, (I + 127) / 128, h, s);
   if (e != cudaSuccess) return e;
-  return launch_one<false>(ma2, mb2, offsets, p2e, G, P, E, H, I, (H + BN - 1) / BN, static_cast<__nv_bfloat16*>(y),
-                           s);
+  return launch_one<false, 1>(ma2, mb2, offsets, p2e, G, P, E, H, I, (H + BN - 1) / BN, yb, s);
 }
 
 }  // namespace semmoe
