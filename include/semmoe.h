@@ -157,7 +157,7 @@ int semmoe_affinity_lookup(const int32_t* token_ids, const int32_t* lut, int V, 
  * topk_idx    [device] [T,k_max] int32 (-1 = padding slot, skipped)
  * pred_rank   [device] [T] int32;  expert_rank [device] [E] int32 in [0,R)
  * counts      [device] [R,R] int32 out (overwritten);  remote [device] [R] int32 out
- * Limits: 1 <= R <= 64.
+ * Limits: 1 <= R <= 64, 1 <= E <= 256.
  */
 int semmoe_remote_count(const int32_t* topk_idx, const int32_t* pred_rank,
                         const int32_t* expert_rank, int T, int k_max, int E, int R,

@@ -227,10 +227,11 @@ def test_route_tensor_core_per_token_budgets(E, k_max, wd):
     np.testing.assert_allclose(np_(gw), ref_w, rtol=0, atol=GATE_ATOL)
 
 
-@pytest.mark.parametrize("P,E,H,I", [(1000, 8, 256, 160), (5000, 64, 512, 352)])
-def test_grouped_ffn_cluster_pair_matches_single_cta(P, E, H, I, monkeypatch):
-    """The cluster-of-2 grouped GEMM (weight tiles shared by TMA multicast)
-    returns exactly what the single-CTA kernel returns."""
+@pytest.mark.parametrize("P,E,H,I", [(1000, 8, 256, 160), (5000, 64, 512, 352), (3000, 16, 512, 640)])
+def test_grouped_ffn_forms_are_bit_identical(P, E, H, I, monkeypatch):
+    """Every form of the grouped GEMM -- independent CTAs, CTA pairs sharing
+    weight tiles by TMA multicast, 2-SM MMA pairs with one or two accumulator
+    buffers -- returns exactly the same bits."""
     rng = np.random.default_rng(P + E)
     cnt = rng.multinomial(P, np.full(E, 1.0 / E))
     off = torch.from_numpy(np.r_[0, np.cumsum(cnt)].astype(np.int32)).cuda()
@@ -240,10 +241,11 @@ def test_grouped_ffn_cluster_pair_matches_single_cta(P, E, H, I, monkeypatch):
     w2 = torch.from_numpy((rng.standard_normal((E, H, I)) / np.sqrt(I)).astype(np.float32)).to(torch.bfloat16).cuda()
     ws = torch.empty(abi().semmoe_grouped_ffn_workspace_size(P, I, 1), dtype=torch.uint8, device="cuda")
     outs = []
-    for cl in ("1", "2"):
-        monkeypatch.setenv("SEMMOE_FFN_CLUSTER", cl)
+    for mode in ("single", "multicast", "pair1", "pair"):
+        monkeypatch.setenv("SEMMOE_FFN_MODE", mode)
         y = torch.empty(P, H, dtype=torch.bfloat16, device="cuda")
         abi().semmoe_grouped_ffn(x, off, pe, w13, w2, P, E, H, I, y, ws)
         assert abi().semmoe_check_errors() == 0
         outs.append(y.cpu())
-    assert torch.equal(outs[0], outs[1])
+    for o in outs[1:]:
+        assert torch.equal(outs[0], o)

@@ -134,7 +134,8 @@ int semmoe_affinity_lookup(const int32_t* token_ids, const int32_t* lut, int V, 
 
 int semmoe_remote_count(const int32_t* topk_idx, const int32_t* pred_rank, const int32_t* expert_rank, int T,
                         int k_max, int E, int R, int32_t* counts, int32_t* remote, void* stream) {
-  REQUIRE(T >= 0 && k_max >= 1 && E >= 1, "semmoe_remote_count: bad sizes T=%d k_max=%d E=%d", T, k_max, E);
+  REQUIRE(T >= 0 && k_max >= 1 && E >= 1 && E <= 256, "semmoe_remote_count: bad sizes T=%d k_max=%d E=%d", T, k_max,
+          E);
   REQUIRE(R >= 1 && R <= 64, "semmoe_remote_count: R = %d outside [1, 64]", R);
   REQUIRE(counts && remote && expert_rank, "semmoe_remote_count: null pointer");
   REQUIRE(T == 0 || (topk_idx && pred_rank), "semmoe_remote_count: null topk_idx or pred_rank");

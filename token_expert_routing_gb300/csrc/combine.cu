@@ -143,7 +143,7 @@ cudaError_t launch_combine(const void* y_perm, const int32_t* pair_to_sorted, co
   const int cap = sm_count() * 16;
   if (blocks > cap) blocks = cap;
   if (dtype == SEMMOE_BF16)
-    combine_kernel<__nv_bfloat16, 2><<<blocks, kThreads, 0, s>>>(
+    combine_kernel<__nv_bfloat16, 4><<<blocks, kThreads, 0, s>>>(
         static_cast<const __nv_bfloat16*>(y_perm), pair_to_sorted, topk_w,
         static_cast<const __nv_bfloat16*>(y_shared), T, H, k_max, P, static_cast<__nv_bfloat16*>(out));
   else

@@ -18,18 +18,24 @@
 // accumulator columns [0,128) hold x W1^T and [128,256) hold x W3^T for the
 // same 128 h-columns.
 //
-// A second variant runs clusters of two CTAs on two m-tiles of the same expert
-// and n-tile: each CTA loads half of the shared weight tile and multicasts it to
-// both (SEMMOE_FFN_CLUSTER=2).  It halves L2 reads of the weights but not the
-// shared-memory traffic per SM (TMA writes + MMA operand reads), which is what
-// bounds this single-SM M128xN256 tile, and the pair runs in lock-step; it
-// measured slower, so independent CTAs are the default.
+// Forms of the same computation (all bit-identical):
+//  * independent CTAs (above): M128 x N256 per SM;
+//  * 2-SM pairs (ffn_pair_kernel, the default for I >= 512): a cluster of two
+//    CTAs runs tcgen05.mma.cta_group::2 with M = 256, each SM staging its own
+//    A rows and half of the weight tile, a third less shared-memory traffic per
+//    SM; pairs cover two m-tiles of one expert, so groups with an odd m-tile
+//    count leave one half idle, which costs more than it saves on short
+//    (I < 512) tiles;
+//  * multicast pairs (SEMMOE_FFN_MODE=multicast): independent MMAs, weight tile
+//    shared by TMA multicast; it halves L2 weight reads but not per-SM
+//    shared-memory traffic and measured slower.
 //
 // Every wait is bounded (%globaltimer); a wait that runs out sets the timeout
 // bit of the device error word and an abort flag, after which every role
 // stops, in-flight TMA loads and MMAs are drained (again with a bound), and
 // TMEM is freed before the CTA exits.
 #include <stdlib.h>
+#include <string.h>
 
 #include "common.cuh"
 #include "internal.h"
@@ -77,9 +83,8 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
 // Tile unit mu (CL consecutive m-tiles of one group, one per CTA of the
 // cluster) -> this CTA's (first row, valid rows, expert).  A CTA whose m-tile
 // lies past its group's end gets rows = 0 (it still takes part in the loads).
-template <int CL>
-__device__ __forceinline__ void decode_mtile(const Shared& sh, int G, int mu, int rank, int& row0, int& rows,
-                                             int& e) {
+template <int CL, typename SH>
+__device__ __forceinline__ void decode_mtile(const SH& sh, int G, int mu, int rank, int& row0, int& rows, int& e) {
   int lo = 0, hi = G - 1;  // largest g with tp[g] <= mu
   while (lo < hi) {
     const int mid = (lo + hi + 1) >> 1;
@@ -328,6 +333,242 @@ ffn_tc_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__
 }
 
 // ---------------------------------------------------------------------------
+// 2-SM variant (SEMMOE_FFN_MODE=pair): clusters of two CTAs on two SMs run
+// tcgen05.mma.cta_group::2 with M = 256.  Each CTA stages its own 128 A rows and
+// half of the 256-row weight tile (CTA 0 the gate / first half, CTA 1 the up /
+// second half); the pair's even CTA issues the MMAs, and each CTA's TMEM holds
+// the accumulator rows of its own A rows.  Per SM and k-block that is 32 KB of
+// TMA writes and 32 KB of MMA operand reads instead of 48 + 48 KB.
+// ---------------------------------------------------------------------------
+constexpr int P_STAGES = 6;
+constexpr int P_B_BYTES = 128 * BK * 2;             // half of the 256-row weight tile
+constexpr int P_STAGE_BYTES = A_BYTES + P_B_BYTES;  // 32 KB
+
+struct PairShared {
+  uint64_t full[P_STAGES], empty[P_STAGES], tfull[2], tempty[2], done;
+  uint32_t tmem_base;
+  int abort_flag;
+  int total_mtiles;
+  int off[MAX_GROUPS + 1];
+  int pe[MAX_GROUPS];
+  int tp[MAX_GROUPS + 1];
+};
+
+constexpr size_t kPairSmemBytes = 1024 + (size_t)P_STAGES * P_STAGE_BYTES + sizeof(PairShared);
+constexpr uint32_t kIdescPair = idesc_bf16_f32(2 * BM, BN);
+
+template <bool GLU, int NBUF>
+__global__ void __launch_bounds__(THREADS, 1)
+ffn_pair_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b,
+                const int32_t* __restrict__ offsets, const int32_t* __restrict__ phys_to_expert, int G, int P,
+                int E, int N, int K, int n_tiles, __nv_bfloat16* __restrict__ out) {
+  extern __shared__ __align__(1024) unsigned char smem_raw[];
+  const uint32_t pad = (1024u - (smem_u32(smem_raw) & 1023u)) & 1023u;
+  unsigned char* ring = smem_raw + pad;  // stage s: A [128 x 64] then B half [128 x 64]
+  PairShared& sh = *reinterpret_cast<PairShared*>(ring + P_STAGES * P_STAGE_BYTES);
+  volatile int* abort_flag = &sh.abort_flag;
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  const int rank = (int)cluster_ctarank();
+  const bool leader = rank == 0;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < P_STAGES; ++s) {
+      mbar_init(&sh.full[s], 1);   // the leader's arrive.expect_tx; both CTAs' bytes
+      mbar_init(&sh.empty[s], 1);  // the pair MMA's commit
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(&sh.tfull[a], 1);
+      mbar_init(&sh.tempty[a], 2 * 128);  // both CTAs' epilogue threads (leader's copy is used)
+    }
+    mbar_init(&sh.done, 1);
+    sh.abort_flag = 0;
+    mbar_init_fence();
+    prefetch_map(&map_a);
+    prefetch_map(&map_b);
+  }
+  for (int g = threadIdx.x; g <= G; g += THREADS) sh.off[g] = offsets ? offsets[g] : (g == 0 ? 0 : P);
+  for (int g = threadIdx.x; g < G; g += THREADS) sh.pe[g] = phys_to_expert ? phys_to_expert[g] : 0;
+  __syncthreads();
+  if (warp == 1) tmem_alloc_pair(&sh.tmem_base, NBUF * ACC_COLS);
+  if (warp == 0) {  // exclusive prefix of m-tile pairs per group, 8 groups per lane
+    int cnt[8], sum = 0;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const int g = lane * 8 + i;
+      int c = 0;
+      if (g < G) {
+        const int lo = sh.off[g], hi = sh.off[g + 1], e = sh.pe[g];
+        if (lo < 0 || hi < lo || hi > P || e < 0 || e >= E) atomicOr(&g_err, SEMMOE_DEVERR_PAIRS);
+        else c = ((hi - lo + BM - 1) / BM + 1) / 2;
+      }
+      cnt[i] = c;
+      sum += c;
+    }
+    int incl = sum;
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+      const int v = __shfl_up_sync(0xffffffffu, incl, d);
+      if (lane >= d) incl += v;
+    }
+    int run = incl - sum;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const int g = lane * 8 + i;
+      if (g < G) sh.tp[g] = run;
+      run += cnt[i];
+    }
+    if (lane == 31) {
+      sh.tp[G] = incl;
+      sh.total_mtiles = incl;
+    }
+  }
+  fence_before();
+  __syncthreads();
+  cluster_sync_all();  // the peer's barriers and TMEM exist before anything crosses the pair
+  fence_after();
+
+  const uint32_t tmem = sh.tmem_base;
+  const int total = sh.total_mtiles * n_tiles;
+  const int kb_n = (K + BK - 1) / BK;
+  const int unit0 = blockIdx.x / 2, units = gridDim.x / 2;
+
+  if (warp == 0) {
+    if (lane == 0) {  // TMA producer (both CTAs): own A rows + own half of B, counted on the leader's barrier
+      uint32_t it = 0;
+      for (int tile = unit0; tile < total; tile += units) {
+        if (*abort_flag) break;
+        const int mt = tile / n_tiles, nt = tile % n_tiles;
+        int row0, rows, e;
+        decode_mtile<2>(sh, G, mt, rank, row0, rows, e);
+        bool ok = true;
+        for (int kb = 0; kb < kb_n; ++kb) {
+          const int s = it % P_STAGES;
+          const uint32_t ph = (it / P_STAGES) & 1;
+          if (!mbar_wait(&sh.empty[s], ph ^ 1, abort_flag, &g_err)) { ok = false; break; }
+          if (leader) mbar_expect_tx(&sh.full[s], 2 * P_STAGE_BYTES);
+          const uint32_t fb = mapa_rank(&sh.full[s], 0);
+          unsigned char* st = ring + (size_t)s * P_STAGE_BYTES;
+          tma_load_2d_pair(st, &map_a, fb, kb * BK, row0);
+          if (GLU) tma_load_4d_pair(st + A_BYTES, &map_b, fb, kb * BK, nt * 128, rank, e);
+          else tma_load_3d_pair(st + A_BYTES, &map_b, fb, kb * BK, nt * BN + rank * 128, e);
+          ++it;
+        }
+        if (!ok) break;
+      }
+      if (*abort_flag && leader) {
+        for (uint32_t j = it > (uint32_t)P_STAGES ? it - P_STAGES : 0; j < it; ++j)
+          mbar_drain(&sh.full[j % P_STAGES], (j / P_STAGES) & 1, &g_err);
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0 && leader) {  // MMA issuer: the pair's even CTA only
+      uint32_t it = 0, acc_it = 0;
+      for (int tile = unit0; tile < total; tile += units) {
+        if (*abort_flag) break;
+        const uint32_t a = acc_it % NBUF, aph = (acc_it / NBUF) & 1;
+        if (!mbar_wait(&sh.tempty[a], aph ^ 1, abort_flag, &g_err)) break;
+        fence_after();
+        const uint32_t d = tmem + a * ACC_COLS;
+        bool ok = true;
+        for (int kb = 0; kb < kb_n; ++kb) {
+          const int s = it % P_STAGES;
+          const uint32_t ph = (it / P_STAGES) & 1;
+          if (!mbar_wait(&sh.full[s], ph, abort_flag, &g_err)) { ok = false; break; }
+          fence_after();
+          const uint32_t sa = smem_u32(ring + (size_t)s * P_STAGE_BYTES), sb = sa + A_BYTES;
+#pragma unroll
+          for (int k = 0; k < BK / UK; ++k)
+            mma_bf16_pair(d, sw128_desc(sa + k * UK * 2), sw128_desc(sb + k * UK * 2), kIdescPair, (kb | k) != 0);
+          commit_pair_mc(&sh.empty[s], 0x3);  // both CTAs may refill this stage
+          ++it;
+        }
+        if (!ok) break;
+        commit_pair_mc(&sh.tfull[a], 0x3);    // both CTAs' accumulator rows are ready
+        ++acc_it;
+      }
+      commit_pair_mc(&sh.done, 0x1);
+      mbar_drain(&sh.done, 0, &g_err);
+    }
+  } else {  // epilogue (both CTAs): this CTA's 128 rows of the 256-row tile
+    const int q = warp & 3, r = q * 32 + lane;
+    uint32_t acc_it = 0;
+    for (int tile = unit0; tile < total; tile += units) {
+      const int mt = tile / n_tiles, nt = tile % n_tiles;
+      int row0, rows, e;
+      decode_mtile<2>(sh, G, mt, rank, row0, rows, e);
+      const uint32_t a = acc_it % NBUF, aph = (acc_it / NBUF) & 1;
+      int ok = 1;
+      if (lane == 0) ok = mbar_wait(&sh.tfull[a], aph, abort_flag, &g_err);
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+      if (!ok) break;
+      fence_after();
+      const uint32_t t_row = tmem + ((uint32_t)(q * 32) << 16) + a * ACC_COLS;
+      const bool row_ok = r < rows;
+      __nv_bfloat16* orow = out + (size_t)(row0 + (row_ok ? r : 0)) * N;
+      if (GLU) {
+#pragma unroll 1
+        for (int c = 0; c < 128; c += 32) {
+          uint32_t gv[32], uv[32];
+          tmem_ld32(t_row + c, gv);
+          tmem_ld32(t_row + 128 + c, uv);
+          tmem_ld_wait();
+          const int col0 = nt * 128 + c;
+          if (row_ok) {
+#pragma unroll
+            for (int v = 0; v < 4; ++v) {
+              const int col = col0 + 8 * v;
+              if (col + 8 <= N) {
+                uint32_t w[4];
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                  const float g0 = __uint_as_float(gv[8 * v + 2 * i]), g1 = __uint_as_float(gv[8 * v + 2 * i + 1]);
+                  const float u0 = __uint_as_float(uv[8 * v + 2 * i]), u1 = __uint_as_float(uv[8 * v + 2 * i + 1]);
+                  w[i] = pack_bf16x2(__fdividef(g0, 1.0f + __expf(-g0)) * u0, __fdividef(g1, 1.0f + __expf(-g1)) * u1);
+                }
+                *reinterpret_cast<uint4*>(orow + col) = make_uint4(w[0], w[1], w[2], w[3]);
+              }
+            }
+          }
+        }
+      } else {
+#pragma unroll 1
+        for (int c = 0; c < BN; c += 32) {
+          uint32_t yv[32];
+          tmem_ld32(t_row + c, yv);
+          tmem_ld_wait();
+          const int col0 = nt * BN + c;
+          if (row_ok) {
+#pragma unroll
+            for (int v = 0; v < 4; ++v) {
+              const int col = col0 + 8 * v;
+              if (col + 8 <= N) {
+                uint32_t w[4];
+#pragma unroll
+                for (int i = 0; i < 4; ++i)
+                  w[i] = pack_bf16x2(__uint_as_float(yv[8 * v + 2 * i]), __uint_as_float(yv[8 * v + 2 * i + 1]));
+                *reinterpret_cast<uint4*>(orow + col) = make_uint4(w[0], w[1], w[2], w[3]);
+              }
+            }
+          }
+        }
+      }
+      fence_before();
+      mbar_arrive_cluster(mapa_rank(&sh.tempty[a], 0));  // the leader's MMA may reuse this buffer
+      ++acc_it;
+    }
+  }
+
+  fence_before();
+  __syncthreads();
+  cluster_sync_all();  // nothing crosses the pair any more
+  if (warp == 1) {
+    __syncwarp();
+    fence_after();
+    tmem_dealloc_pair(tmem, NBUF * ACC_COLS);
+  }
+}
+
+// ---------------------------------------------------------------------------
 // host side
 // ---------------------------------------------------------------------------
 template <bool GLU, int CL>
@@ -369,25 +610,65 @@ cudaError_t launch_one(const CUtensorMap& ma, const CUtensorMap& mb, const int32
   return cudaGetLastError();
 }
 
+template <bool GLU, int NBUF>
+cudaError_t launch_pair(const CUtensorMap& ma, const CUtensorMap& mb, const int32_t* offsets, const int32_t* p2e,
+                        int G, int P, int E, int N, int K, int n_tiles, __nv_bfloat16* out, cudaStream_t s) {
+  auto kern = ffn_pair_kernel<GLU, NBUF>;
+  static std::atomic<unsigned long long> smem_set{0};
+  cudaError_t e = ensure_smem_limit(kern, (int)kPairSmemBytes, smem_set);
+  if (e != cudaSuccess) return e;
+  const long long max_units = ((long long)(P + BM - 1) / BM + G) * n_tiles;
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.blockDim = dim3(THREADS);
+  cfg.dynamicSmemBytes = kPairSmemBytes;
+  cfg.stream = s;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  cfg.gridDim = dim3(sm_count() / 2 * 2);
+  int clusters = 0;
+  e = cudaOccupancyMaxActiveClusters(&clusters, kern, &cfg);
+  if (e != cudaSuccess) return e;
+  if (clusters < 1) return cudaErrorInvalidConfiguration;
+  long long units = clusters;
+  if (max_units < units) units = max_units;
+  cfg.gridDim = dim3((unsigned)(units * 2));
+  e = cudaLaunchKernelEx(&cfg, kern, ma, mb, offsets, p2e, G, P, E, N, K, n_tiles, out);
+  if (e != cudaSuccess) return e;
+  count_launches(1);
+  return cudaGetLastError();
+}
+
 }  // namespace
 
 int ffn_tc_take_errors(cudaStream_t s, int* bits) { return take_error_word(g_err, s, bits); }
 
-// CTAs per cluster of the grouped GEMM: 2 (the pair shares each weight tile
-// through TMA multicast) unless SEMMOE_FFN_CLUSTER=1 asks for independent CTAs.
-static int ffn_cluster_size() {
-  const char* v = getenv("SEMMOE_FFN_CLUSTER");
-  if (v != nullptr && v[0] == '1' && v[1] == 0) return 1;
-  if (v != nullptr && v[0] == '2' && v[1] == 0) return 2;
-  return 1;
+// Grouped-GEMM form: 0 = independent CTAs; 1 = pairs sharing weight tiles by
+// multicast; 2 / 3 = 2-SM MMA pairs with one / two accumulator buffers.
+// Default: 2-SM pairs when the expert intermediate is at least 512 (long
+// tiles), independent CTAs otherwise; SEMMOE_FFN_MODE=single|multicast|pair1|pair
+// overrides it.
+static int ffn_mode(int I) {
+  const char* v = getenv("SEMMOE_FFN_MODE");
+  if (v != nullptr) {
+    if (strcmp(v, "single") == 0) return 0;
+    if (strcmp(v, "multicast") == 0) return 1;
+    if (strcmp(v, "pair1") == 0) return 2;
+    if (strcmp(v, "pair") == 0) return 3;
+  }
+  return I >= 512 ? 3 : 0;
 }
 
-// x [P,H], w13 [E,2I,H], w2 [E,H,I], h (workspace) [P,I], y [P,H]; all bf16.
 cudaError_t launch_ffn_tc(const void* x, const int32_t* offsets, const int32_t* p2e, const void* w13,
                           const void* w2, int P, int E, int H, int I, void* y, void* ws, cudaStream_t s) {
   if (P == 0) return cudaSuccess;
   const int G = offsets ? E : 1;
-  const int CL = ffn_cluster_size();
+  const int mode = ffn_mode(I);
+  const int CL = mode == 0 ? 1 : 2;
   const cuuint64_t es = 2;
   CUtensorMap ma1, mb1, ma2, mb2;
   {
@@ -417,10 +698,20 @@ cudaError_t launch_ffn_tc(const void* x, const int32_t* offsets, const int32_t* 
   __nv_bfloat16* h = static_cast<__nv_bfloat16*>(ws);
   __nv_bfloat16* yb = static_cast<__nv_bfloat16*>(y);
   cudaError_t e;
-  if (CL == 2) {
+  if (mode == 1) {
     e = launch_one<true, 2>(ma1, mb1, offsets, p2e, G, P, E, I, H, (I + 127) / 128, h, s);
     if (e != cudaSuccess) return e;
     return launch_one<false, 2>(ma2, mb2, offsets, p2e, G, P, E, H, I, (H + BN - 1) / BN, yb, s);
+  }
+  if (mode == 2) {
+    e = launch_pair<true, 1>(ma1, mb1, offsets, p2e, G, P, E, I, H, (I + 127) / 128, h, s);
+    if (e != cudaSuccess) return e;
+    return launch_pair<false, 1>(ma2, mb2, offsets, p2e, G, P, E, H, I, (H + BN - 1) / BN, yb, s);
+  }
+  if (mode == 3) {
+    e = launch_pair<true, 2>(ma1, mb1, offsets, p2e, G, P, E, I, H, (I + 127) / 128, h, s);
+    if (e != cudaSuccess) return e;
+    return launch_pair<false, 2>(ma2, mb2, offsets, p2e, G, P, E, H, I, (H + BN - 1) / BN, yb, s);
   }
   e = launch_one<true, 1>(ma1, mb1, offsets, p2e, G, P, E, I, H, (I + 127) / 128, h, s);
   if (e != cudaSuccess) return e;

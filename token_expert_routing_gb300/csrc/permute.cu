@@ -62,6 +62,7 @@ __device__ void physical_positions(const int32_t* __restrict__ expert_rank, int 
   __syncthreads();
   for (int e = threadIdx.x; e < E; e += blockDim.x) {
     int re = rank_s[e], pos = 0;
+#pragma unroll 16
     for (int f = 0; f < E; ++f) {
       int rf = rank_s[f];
       pos += (rf < re) || (rf == re && f < e);
@@ -110,10 +111,16 @@ perm_scatter_kernel(const int32_t* __restrict__ topk_idx, const int32_t* __restr
   const int tid = threadIdx.x;
   if (tid < E) {
     int before = 0, tot = 0;
-    for (int c = 0; c < nchunks; ++c) {
-      const int v = hist[(size_t)c * E + tid];
-      before += c < (int)blockIdx.x ? v : 0;
-      tot += v;
+    constexpr int B = 8;  // chunks per batch: the batch's loads are all in flight together
+    for (int c0 = 0; c0 < nchunks; c0 += B) {
+      int v[B];
+#pragma unroll
+      for (int u = 0; u < B; ++u) v[u] = c0 + u < nchunks ? hist[(size_t)(c0 + u) * E + tid] : 0;
+#pragma unroll
+      for (int u = 0; u < B; ++u) {
+        before += c0 + u < (int)blockIdx.x ? v[u] : 0;
+        tot += v[u];
+      }
     }
     total[tid] = tot;
     run[tid] = before;
@@ -197,6 +204,7 @@ perm_gather_kernel(const unsigned char* __restrict__ x, const int32_t* __restric
       continue;
     }
     const uint4* src = reinterpret_cast<const uint4*>(x + (size_t)t * row_bytes);
+#pragma unroll 4
     for (int off = lane; off < row_bytes / 16; off += 32) dst[off] = src[off];
   }
 }

@@ -41,22 +41,23 @@ __host__ __device__ inline size_t route_smem_bytes(int E, int k_max) {
 // ascending), skipping experts already taken; then the gates, the softmax of
 // the selected logits renormalised over the selection (fp32).  my_v / my_e:
 // k_max floats / ints of scratch for this warp.
+template <int NPER>  // logits held per lane: E <= 32 * NPER
 __device__ void warp_topk(const float* row, int ks, size_t slice_stride, float* logits_out, int E, int t,
                           const int32_t* __restrict__ k_per_token, int k_uniform, int k_max, float* my_v, int* my_e,
                           int32_t* __restrict__ topk_idx, float* __restrict__ topk_w) {
   const int lane = threadIdx.x % 32;
-  const int nper = (E + 31) / 32;
+  const int nper = NPER;
   int kt = k_per_token != nullptr ? k_per_token[t] : k_uniform;
   if (kt < 1 || kt > k_max) {
     if (lane == 0) flag(SEMMOE_DEVERR_K);
     kt = kt < 1 ? 1 : k_max;
   }
-  float v[kRouteMaxE / 32];
+  float v[NPER];
 #pragma unroll
-  for (int i = 0; i < kRouteMaxE / 32; ++i) {
+  for (int i = 0; i < NPER; ++i) {
     float val = -INFINITY;
     const int e = lane + 32 * i;
-    if (i < nper && e < E) {
+    if (e < E) {
       val = row[e];
       for (int k = 1; k < ks; ++k) val += row[(size_t)k * slice_stride + e];  // K slices in order
       if (logits_out != nullptr) logits_out[e] = val;
@@ -72,9 +73,9 @@ __device__ void warp_topk(const float* row, int ks, size_t slice_stride, float* 
     float bv = -INFINITY;
     int be = 0x7fffffff;
 #pragma unroll
-    for (int i = 0; i < kRouteMaxE / 32; ++i) {
+    for (int i = 0; i < NPER; ++i) {
       const int e = lane + 32 * i;
-      if (i < nper && e < E && !((taken >> i) & 1u)) {
+      if (e < E && !((taken >> i) & 1u)) {
         if (v[i] > bv || (v[i] == bv && e < be)) { bv = v[i]; be = e; }
       }
     }
@@ -182,8 +183,8 @@ route_kernel(const TX* __restrict__ x, const TW* __restrict__ w, const float* __
   for (int tl = warp; tl < kRouteTok; tl += kWarps) {
     const int t = t0 + tl;
     if (t >= T) break;
-    warp_topk(lg + tl * Epad, 1, 0, nullptr, E, t, k_per_token, k_uniform, k_max, sel_v + warp * k_max,
-              sel_e + warp * k_max, topk_idx, topk_w);
+    warp_topk<kRouteMaxE / 32>(lg + tl * Epad, 1, 0, nullptr, E, t, k_per_token, k_uniform, k_max,
+                               sel_v + warp * k_max, sel_e + warp * k_max, topk_idx, topk_w);
   }
 }
 
@@ -192,6 +193,7 @@ route_kernel(const TX* __restrict__ x, const TW* __restrict__ w, const float* __
 // so every token's (latency-bound) selection runs concurrently with the others.
 constexpr int kTopkWarps = 8;
 
+template <int NPER>
 __global__ void __launch_bounds__(kTopkWarps * 32)
 topk_kernel(const float* __restrict__ logits, int ks, float* __restrict__ logits_out,
             const int32_t* __restrict__ k_per_token, int k_uniform, int T, int E, int k_max,
@@ -202,7 +204,7 @@ topk_kernel(const float* __restrict__ logits, int ks, float* __restrict__ logits
   const int warp = threadIdx.x / 32;
   const int t = blockIdx.x * kTopkWarps + warp;
   if (t >= T) return;
-  warp_topk(logits + (size_t)t * E, ks, (size_t)T * E, logits_out != nullptr ? logits_out + (size_t)t * E : nullptr,
+  warp_topk<NPER>(logits + (size_t)t * E, ks, (size_t)T * E, logits_out != nullptr ? logits_out + (size_t)t * E : nullptr,
             E, t, k_per_token, k_uniform, k_max, sel_v + warp * k_max, sel_e + warp * k_max, topk_idx, topk_w);
 }
 
@@ -258,30 +260,22 @@ remote_count_one_block_kernel(const int32_t* __restrict__ topk_idx, const int32_
                               const int32_t* __restrict__ expert_rank, int T, int k_max, int E, int R,
                               int32_t* __restrict__ counts, int32_t* __restrict__ remote) {
   __shared__ int c[kMaxR * kMaxR];
+  __shared__ int rank_s[kRouteMaxE];
   for (int i = threadIdx.x; i < R * R; i += kCountThreads) c[i] = 0;
+  for (int e = threadIdx.x; e < E; e += kCountThreads) rank_s[e] = expert_rank[e];
   __syncthreads();
-  const long long n = (long long)T * k_max;
-  constexpr int B = 8;  // pairs per thread per batch: all their loads are issued before any use
-  for (long long p0 = threadIdx.x; p0 < n; p0 += (long long)B * kCountThreads) {
-    int e[B], src[B], dst[B];
-#pragma unroll
-    for (int u = 0; u < B; ++u) {
-      const long long p = p0 + (long long)u * kCountThreads;
-      e[u] = p < n ? topk_idx[p] : -1;
-    }
-#pragma unroll
-    for (int u = 0; u < B; ++u) {
-      const long long p = p0 + (long long)u * kCountThreads;
-      const bool ok = e[u] >= 0 && e[u] < E;
-      src[u] = ok ? pred[p / k_max] : 0;
-      dst[u] = ok ? expert_rank[e[u]] : 0;
-    }
-#pragma unroll
-    for (int u = 0; u < B; ++u) {
-      if (e[u] < 0) continue;
-      if (e[u] >= E) { flag(SEMMOE_DEVERR_EXPERT); continue; }
-      if (src[u] < 0 || src[u] >= R || dst[u] < 0 || dst[u] >= R) { flag(SEMMOE_DEVERR_LUT); continue; }
-      atomicAdd(&c[src[u] * R + dst[u]], 1);
+  // One token per thread per pass; its source rank and all its slots are
+  // loaded before any is used, so the loads of a pass overlap.
+  for (int t = threadIdx.x; t < T; t += kCountThreads) {
+    const int src = pred[t];
+    const int32_t* slots = topk_idx + (size_t)t * k_max;
+    for (int j = 0; j < k_max; ++j) {
+      const int e = slots[j];
+      if (e < 0) continue;
+      if (e >= E) { flag(SEMMOE_DEVERR_EXPERT); continue; }
+      const int dst = rank_s[e];
+      if (src < 0 || src >= R || dst < 0 || dst >= R) { flag(SEMMOE_DEVERR_LUT); continue; }
+      atomicAdd(&c[src * R + dst], 1);
     }
   }
   __syncthreads();
@@ -362,9 +356,15 @@ cudaError_t launch_route(const void* x, int x_dtype, const void* w, int w_dtype,
   }
   if (logits_in != nullptr) {  // top-k of the (summed) logits; x and w unused here
     const size_t sm = (size_t)kTopkWarps * k_max * (sizeof(float) + sizeof(int));
-    topk_kernel<<<(T + kTopkWarps - 1) / kTopkWarps, kTopkWarps * 32, sm, s>>>(logits_in, ks, logits_out, kpt,
-                                                                               k_uniform, T, E, k_max, topk_idx,
-                                                                               topk_w);
+    const dim3 grid((T + kTopkWarps - 1) / kTopkWarps), block(kTopkWarps * 32);
+    if (E <= 32)
+      topk_kernel<1><<<grid, block, sm, s>>>(logits_in, ks, logits_out, kpt, k_uniform, T, E, k_max, topk_idx, topk_w);
+    else if (E <= 64)
+      topk_kernel<2><<<grid, block, sm, s>>>(logits_in, ks, logits_out, kpt, k_uniform, T, E, k_max, topk_idx, topk_w);
+    else if (E <= 128)
+      topk_kernel<4><<<grid, block, sm, s>>>(logits_in, ks, logits_out, kpt, k_uniform, T, E, k_max, topk_idx, topk_w);
+    else
+      topk_kernel<8><<<grid, block, sm, s>>>(logits_in, ks, logits_out, kpt, k_uniform, T, E, k_max, topk_idx, topk_w);
     count_launches(1);
     return cudaGetLastError();
   }
