@@ -37,3 +37,56 @@ def test_layer_full_size(name):
     d = wl.make_inputs(wl.CONFIGS[name])
     res, P = run_gpu(d)
     check_layer_sampled(d, res, P)
+
+
+def _layer(d):
+    from token_expert_routing_gb300 import MoELayer
+    s = d["spec"]
+    return MoELayer(d["w_router"], d["w13"], d["w2"], d["expert_rank"], d["lut"], s.R, s.k_max, d["ws13"], d["ws2"])
+
+
+@pytest.mark.parametrize("name", ["dsv2lite_decode_T64", "prism_subexpert_T8192"])
+def test_captured_graph_matches_eager(name):
+    """A CUDA-graph replay of the layer gives the eager forward's bits, also
+    after new inputs are written into the static buffers."""
+    import torch
+    from token_expert_routing_gb300 import CapturedLayer
+    spec = wl.CONFIGS[name]
+    if name.startswith("prism"):
+        spec = wl.scaled(name, T=1024, tokens_per_request=32)
+    d = wl.make_inputs(spec)
+    layer = _layer(d)
+    per_token = bool(spec.k_choices)
+    cap = CapturedLayer(layer, spec.T, None if per_token else spec.k,
+                        d["k_per_token"] if per_token else None)
+    for seed in (0, 1):
+        x = d["x"] if seed == 0 else d["x"].flip(0).contiguous()
+        ids = d["token_ids"] if seed == 0 else d["token_ids"].flip(0).contiguous()
+        cap.x.copy_(x)
+        cap.token_ids.copy_(ids)
+        got = cap.replay()
+        kpt = d["k_per_token"].cuda() if per_token else None
+        want = layer.forward(x.cuda(), ids.cuda(), kpt, None if per_token else spec.k,
+                             int(d["k_per_token"].sum()))
+        torch.cuda.synchronize()
+        for key in ("out", "topk_idx", "pair_to_sorted", "counts"):
+            assert torch.equal(getattr(got, key), getattr(want, key)), key
+
+
+def test_host_pipeline_matches_forward():
+    """The overlapped host-buffer path returns each call's own output."""
+    import torch
+    from token_expert_routing_gb300 import HostPipeline
+    spec = wl.scaled("dsv2lite_prefill_T4096", T=512, H=256, I=160, I_shared=320, V=3000)
+    d = wl.make_inputs(spec)
+    layer = _layer(d)
+    pipe = HostPipeline(layer)
+    xs = [d["x"], d["x"].flip(0).contiguous(), (d["x"] * 0.5).contiguous()]
+    outs = [torch.empty(spec.T, spec.H, dtype=d["x"].dtype).pin_memory() for _ in xs]
+    ids = d["token_ids"].pin_memory()
+    for x, o in zip(xs, outs):
+        pipe.submit(x.pin_memory(), ids, o, k=spec.k)
+    pipe.synchronize()
+    for x, o in zip(xs, outs):
+        want = layer.forward(x.cuda(), ids.cuda(), k=spec.k).out.cpu()
+        assert torch.equal(o, want)

@@ -649,10 +649,11 @@ int ffn_tc_take_errors(cudaStream_t s, int* bits) { return take_error_word(g_err
 
 // Grouped-GEMM form: 0 = independent CTAs; 1 = pairs sharing weight tiles by
 // multicast; 2 / 3 = 2-SM MMA pairs with one / two accumulator buffers.
-// Default: 2-SM pairs when the expert intermediate is at least 512 (long
-// tiles), independent CTAs otherwise; SEMMOE_FFN_MODE=single|multicast|pair1|pair
-// overrides it.
-static int ffn_mode(int I) {
+// Default: 2-SM pairs when tiles are long (I >= 512) and groups average at
+// least two m-tiles (P >= 256 G; a pair covers two m-tiles of one group, so
+// smaller groups leave half of it idle), independent CTAs otherwise;
+// SEMMOE_FFN_MODE=single|multicast|pair1|pair overrides it.
+static int ffn_mode(int I, int P, int G) {
   const char* v = getenv("SEMMOE_FFN_MODE");
   if (v != nullptr) {
     if (strcmp(v, "single") == 0) return 0;
@@ -660,14 +661,14 @@ static int ffn_mode(int I) {
     if (strcmp(v, "pair1") == 0) return 2;
     if (strcmp(v, "pair") == 0) return 3;
   }
-  return I >= 512 ? 3 : 0;
+  return (I >= 512 && (long long)P >= 2LL * BM * G) ? 3 : 0;
 }
 
 cudaError_t launch_ffn_tc(const void* x, const int32_t* offsets, const int32_t* p2e, const void* w13,
                           const void* w2, int P, int E, int H, int I, void* y, void* ws, cudaStream_t s) {
   if (P == 0) return cudaSuccess;
   const int G = offsets ? E : 1;
-  const int mode = ffn_mode(I);
+  const int mode = ffn_mode(I, P, G);
   const int CL = mode == 0 ? 1 : 2;
   const cuuint64_t es = 2;
   CUtensorMap ma1, mb1, ma2, mb2;

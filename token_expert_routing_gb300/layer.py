@@ -156,3 +156,103 @@ class MoELayer:
                 out_host = torch.empty(res.out.shape, dtype=res.out.dtype, pin_memory=True)
             out_host.copy_(res.out, non_blocking=True)
         return out_host
+
+
+class HostPipeline:
+    """Host-buffer layer calls with copies overlapped across calls.
+
+    Each ``submit`` copies that call's inputs host→device, runs the layer and
+    copies ``out`` back into the given host tensor, like ``MoELayer.forward_host``;
+    but uploads and readbacks run on their own stream, double-buffered, so the
+    upload of call i+1 and the readback of call i-1 overlap the compute of
+    call i.  Host tensors should be pinned.  ``synchronize()`` waits for all.
+    """
+
+    def __init__(self, layer: MoELayer, stream=None):
+        self.layer = layer
+        self.compute = torch.cuda.current_stream() if stream is None else stream
+        self.copy = torch.cuda.Stream(device=layer.device)
+        self._slot = 0
+        self._free = [None, None]      # event: slot's device inputs are no longer read
+        self._bufs = [None, None]
+
+    def _buffers(self, slot, x_host, ids_host, k_host):
+        b = self._bufs[slot]
+        if b is None or b["x"].shape != x_host.shape:
+            dev = self.layer.device
+            b = dict(x=torch.empty(x_host.shape, dtype=x_host.dtype, device=dev),
+                     ids=torch.empty(ids_host.shape, dtype=ids_host.dtype, device=dev),
+                     k=None if k_host is None else torch.empty(k_host.shape, dtype=k_host.dtype, device=dev))
+            self._bufs[slot] = b
+        return b
+
+    def submit(self, x_host, ids_host, out_host, k_host=None, k: Optional[int] = None):
+        slot = self._slot
+        self._slot ^= 1
+        b = self._buffers(slot, x_host, ids_host, k_host)
+        P = None if k_host is None else int(k_host.sum())
+        with torch.cuda.stream(self.copy):
+            if self._free[slot] is not None:
+                self.copy.wait_event(self._free[slot])   # the call two back has read these buffers
+            b["x"].copy_(x_host, non_blocking=True)
+            b["ids"].copy_(ids_host, non_blocking=True)
+            if k_host is not None:
+                b["k"].copy_(k_host, non_blocking=True)
+            uploaded = torch.cuda.Event()
+            uploaded.record(self.copy)
+        self.compute.wait_event(uploaded)
+        with torch.cuda.stream(self.compute):
+            res = self.layer.forward(b["x"], b["ids"], b["k"], k, P, stream=self.compute)
+            done = torch.cuda.Event()
+            done.record(self.compute)
+        self._free[slot] = done
+        with torch.cuda.stream(self.copy):
+            self.copy.wait_event(done)
+            res.out.record_stream(self.copy)
+            out_host.copy_(res.out, non_blocking=True)
+        return out_host
+
+    def synchronize(self):
+        self.copy.synchronize()
+        self.compute.synchronize()
+
+
+class CapturedLayer:
+    """One layer forward captured as a CUDA graph for a fixed batch shape.
+
+    MoE-Prism (ko) §2 B splits the block at the attention/MoE boundary and keeps
+    one graph of the MoE segment per routing budget k; this is that segment for
+    one (T, k) -- or one per-token budget vector -- with static buffers: write
+    the inputs into ``x`` / ``token_ids`` (and ``k_per_token``), ``replay()``,
+    read ``result.out``.  Replays launch every kernel of the forward with one
+    graph launch.
+    """
+
+    def __init__(self, layer: MoELayer, T: int, k: Optional[int] = None, k_per_token_host=None,
+                 warmup: int = 2):
+        if (k is None) == (k_per_token_host is None):
+            raise ValueError("give exactly one of k and k_per_token_host")
+        dev = layer.device
+        self.layer = layer
+        self.x = torch.zeros(T, layer.H, dtype=layer.dtype, device=dev)
+        self.token_ids = torch.zeros(T, dtype=torch.int32, device=dev)
+        self.k = k
+        self.k_per_token = None
+        self.P = None
+        if k_per_token_host is not None:
+            self.k_per_token = k_per_token_host.to(dev, torch.int32)
+            self.P = int(k_per_token_host.sum())
+        side = torch.cuda.Stream(device=dev)
+        side.wait_stream(torch.cuda.current_stream(dev))
+        with torch.cuda.stream(side):           # allocate workspaces and set kernel attributes
+            for _ in range(warmup):
+                layer.forward(self.x, self.token_ids, self.k_per_token, k, self.P, stream=side)
+        torch.cuda.current_stream(dev).wait_stream(side)
+        self.graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(self.graph):
+            self.result = layer.forward(self.x, self.token_ids, self.k_per_token, k, self.P,
+                                        stream=torch.cuda.current_stream(dev))
+
+    def replay(self) -> LayerOutput:
+        self.graph.replay()
+        return self.result
