@@ -45,7 +45,7 @@ def _peaks():
 
 
 class ClockSampler:
-    """nvidia-smi clock/throttle samples every 200 ms while the timed region runs."""
+    """nvidia-smi clock/throttle samples (every 20 ms requested) while the timed region runs."""
 
     QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
@@ -64,17 +64,17 @@ class ClockSampler:
             sel = str(self.dev)
         try:
             self.proc = subprocess.Popen(
-                ["nvidia-smi", f"--query-gpu={self.QUERY}", "--format=csv,noheader,nounits", "-lms", "200",
+                ["nvidia-smi", f"--query-gpu={self.QUERY}", "--format=csv,noheader,nounits", "-lms", "20",
                  "-i", sel], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except Exception:
             self.proc = None
-        time.sleep(0.3)
+        time.sleep(0.15)  # let the sampler start before the timed region
         return self
 
     def __exit__(self, *a):
         if self.proc is None:
             return
-        time.sleep(0.25)
+        time.sleep(0.05)
         self.proc.terminate()
         try:
             out, _ = self.proc.communicate(timeout=5)
@@ -268,7 +268,7 @@ def run_ours(args, world, rank, local):
     _barrier(world)
     torch.cuda.synchronize(dev)
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    with ClockSampler(local) as clocks:
+    with ClockSampler(local) as clocks_eager:
         h0 = time.perf_counter()
         start.record(stream)
         for i in range(args.steps):
@@ -300,16 +300,19 @@ def run_ours(args, world, rank, local):
         _barrier(world)
         torch.cuda.synchronize(dev)
         g0, g1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        g0.record()
-        for _ in range(args.steps):
-            cap.replay()
-        g1.record()
-        torch.cuda.synchronize(dev)
+        with ClockSampler(local) as clocks_graph:
+            g0.record()
+            for _ in range(args.steps):
+                cap.replay()
+            g1.record()
+            torch.cuda.synchronize(dev)
+        _barrier(world)
         g_ms = _max_over_ranks(world, g0.elapsed_time(g1))
         _abi.semmoe_check_errors()
         graph = {"value": spec.T * args.steps * world / (g_ms * 1e-3), "unit": "tokens/s",
                  "ms_per_step": g_ms / args.steps,
-                 "how": "CapturedLayer: the whole forward captured once as a CUDA graph, one replay per step"}
+                 "how": "CapturedLayer: the whole forward captured once as a CUDA graph, one replay per step",
+                 "clocks": clocks_graph.summary()}
         del cap
 
     # end to end through the public API: pinned host inputs in, host output back
@@ -377,7 +380,8 @@ def run_ours(args, world, rank, local):
 
     total_tokens = spec.T * args.steps * world
     eager = {"value": total_tokens / (ms_max * 1e-3), "unit": "tokens/s", "ms_per_step": ms_max / args.steps,
-             "how": "MoELayer.forward per step (one library call per step of the layer)"}
+             "how": "MoELayer.forward per step (one library call per step of the layer)",
+             "clocks": clocks_eager.summary()}
     best = graph if graph is not None and graph["ms_per_step"] < eager["ms_per_step"] else eager
     line = {
         "metric": METRIC, "value": best["value"], "unit": "tokens/s", "n_gpus": world,
@@ -392,7 +396,7 @@ def run_ours(args, world, rank, local):
         "roofline": roofline,
         "stages": stages,
         "cpu_baseline": cpu,
-        "clocks": clocks.summary(),
+        "clocks": best["clocks"],
         "local_activation_rate": None,
     }
     res = layer.forward(x, ids, kpt, k, P, stream=stream)
