@@ -31,3 +31,4 @@ from .moe import (  # noqa: F401
     remote_count, physical_order, permute, expert_ffn, grouped_ffn, shared_ffn, combine,
     moe_layer,
 )
+from .scheduling import dp_schedule, transition_lookup  # noqa: F401
