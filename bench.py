@@ -132,16 +132,21 @@ def _max_over_ranks(world, v: float) -> float:
     return float(t.item())
 
 
-def _flops_bytes(spec, P):
-    """Algorithmic flops and bytes of each step for one layer forward."""
+def _flops_bytes(spec, P, active_experts):
+    """Algorithmic flops and bytes of each step for one layer forward.
+
+    FFN bytes: the weights of every expert with at least one row, the rows in,
+    the intermediate h written and read back, the rows out."""
     s = 2 if spec.dtype == "bf16" else 4
     sr = 2 if spec.router_dtype == "bf16" else 4
     T, H, E, I, k = spec.T, spec.H, spec.E, spec.I, spec.k_max
+    Is = spec.I_shared
     return {
         "route": dict(flops=2 * T * H * E, bytes=T * H * s + E * H * sr + T * k * 8),
         "permute": dict(bytes=4 * T * k * 2 + 4 * P + 4 * T * k + T * H * s + P * H * s),
-        "grouped_ffn": dict(flops=6 * H * I * P),
-        "shared_ffn": dict(flops=6 * H * spec.I_shared * T),
+        "grouped_ffn": dict(flops=6 * H * I * P,
+                            bytes=active_experts * 3 * H * I * s + P * H * s + 2 * P * I * s + P * H * s),
+        "shared_ffn": dict(flops=6 * H * Is * T, bytes=3 * H * Is * s + 2 * T * H * s + 2 * T * Is * s),
         "combine": dict(bytes=P * H * s + 8 * T * k + T * H * s * (2 if spec.I_shared else 1)),
     }
 
@@ -236,6 +241,61 @@ def _config(spec):
             "router_dtype": spec.router_dtype,
             "l2": "inputs larger than L2: expert weights (>1 GB) are streamed every step",
             "parallelism": "replicas"}
+
+
+def _time_around_layer(args, spec, d, layer, dev, stream):
+    """Device time of the table-driven steps around the layer, on the same
+    workload: Attention-DP request scheduling and the next-layer transition
+    lookup (not part of the layer step above)."""
+    from token_expert_routing_gb300 import _abi
+    T, R, E, k_max = spec.T, spec.R, spec.E, spec.k_max
+    i32 = dict(dtype=torch.int32, device=dev)
+    pred = torch.empty(T, **i32)
+    _abi.semmoe_affinity_lookup(d["token_ids"].to(dev), layer.lut, layer.V, R, T, pred, stream)
+    off = d["req_offsets"].to(dev)
+    n = off.shape[0] - 1
+    bufs = [torch.empty(n, R, **i32), torch.empty(n, **i32), torch.empty(n, **i32), torch.empty(R + 1, **i32),
+            torch.empty(n, **i32), torch.empty(T, **i32), torch.empty(T, **i32), torch.empty(R + 1, **i32)]
+    res = layer.forward(d["x"].to(dev), d["token_ids"].to(dev),
+                        d["k_per_token"].to(dev) if spec.k_choices else None,
+                        None if spec.k_choices else spec.k, int(d["k_per_token"].sum()), stream=stream)
+    trans = d["trans"].to(dev)
+    kpt = d["k_per_token"].to(dev) if spec.k_choices else None
+    nxt = torch.empty(T, **i32)
+    calls = {
+        "dp_schedule": (lambda: _abi.semmoe_dp_schedule(pred, off, T, n, R, *bufs),
+                        4 * T + 4 * (n + 1) * 3 + 4 * n * R + 4 * n * 4 + 8 * T + 4 * T, f"{n} requests"),
+        "transition_lookup": (lambda: _abi.semmoe_transition_lookup(res.topk_idx, kpt, 0 if kpt is not None else
+                                                                   spec.k, trans, T, k_max, E, R, nxt),
+                              4 * T * k_max + (4 * T if kpt is not None else 0) + 4 * E * R + 4 * T,
+                              f"E={E} R={R} k_max={k_max}"),
+    }
+    out = {}
+    n_it = max(args.steps, 20)
+    for name, (fn, nbytes, what) in calls.items():
+        for _ in range(3):
+            fn()
+        torch.cuda.synchronize(dev)
+        # n_it calls captured as one CUDA graph, so the device time is not the
+        # host's per-call cost
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):            # calls go to the capture stream (current inside)
+            for _ in range(n_it):
+                fn()
+        g.replay()
+        torch.cuda.synchronize(dev)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        g.replay()
+        b.record()
+        torch.cuda.synchronize(dev)
+        us = a.elapsed_time(b) * 1e3 / n_it
+        out[name] = {"us": us, "algorithmic_bytes": nbytes, "gbs": nbytes / (us * 1e-6) / 1e9, "workload": what,
+                     "bound": "latency (a few small kernels over kilobytes)",
+                     "how": f"{n_it} calls in one CUDA graph, CUDA events around one replay"}
+        del g
+    _abi.semmoe_check_errors()
+    return out
 
 
 def run_ours(args, world, rank, local):
@@ -344,20 +404,42 @@ def run_ours(args, world, rank, local):
                       "overlapped with compute across steps; host wall clock from the first submit to the "
                       "last readback"}
 
+    around = None if args.no_around else _time_around_layer(args, spec, d, layer, dev, stream)
+
     if rank != 0:
         return
     peaks = _peaks()
-    fb = _flops_bytes(spec, P)
+    res = layer.forward(x, ids, kpt, k, P, stream=stream)
+    active = int((res.expert_counts > 0).sum())
+    counts = res.counts.cpu().numpy()
+    fb = _flops_bytes(spec, P, active)
     ffn_ms = stage_avg["grouped_ffn"]
-    achieved = fb["grouped_ffn"]["flops"] / (ffn_ms * 1e-3) / 1e12
-    roofline = {
-        "kernel": "semmoe_grouped_ffn (GEMM1+SwiGLU, GEMM2)",
-        "bound": "tensor", "achieved": achieved, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
-        "frac": achieved / peaks["bf16_tflops"], "traffic": _traffic("semmoe_grouped_ffn", spec.name),
-        "peak_source": f"{peaks['source']} bf16 burst (short timed region, SM clock at its maximum); "
-                       f"sustained figure {peaks['bf16_tflops_sustained']} TFLOP/s",
-        "frac_of_sustained": achieved / peaks["bf16_tflops_sustained"],
-    }
+    ffn = fb["grouped_ffn"]
+    # the FFN's bound: whichever of its flops at the tensor peak and its bytes at
+    # the HBM peak takes longer (weight streaming wins for small batches)
+    t_tc = ffn["flops"] / (peaks["bf16_tflops"] * 1e12)
+    t_hbm = ffn["bytes"] / (peaks["hbm_gbs"] * 1e9)
+    tflops = ffn["flops"] / (ffn_ms * 1e-3) / 1e12
+    gbs = ffn["bytes"] / (ffn_ms * 1e-3) / 1e9
+    if t_tc >= t_hbm:
+        roofline = {
+            "kernel": "semmoe_grouped_ffn (GEMM1+SwiGLU, GEMM2)",
+            "bound": "tensor", "achieved": tflops, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+            "frac": tflops / peaks["bf16_tflops"], "traffic": _traffic("semmoe_grouped_ffn", spec.name),
+            "peak_source": f"{peaks['source']} bf16 burst (short timed region, SM clock at its maximum); "
+                           f"sustained figure {peaks['bf16_tflops_sustained']} TFLOP/s",
+            "frac_of_sustained": tflops / peaks["bf16_tflops_sustained"],
+            "frac_hbm": gbs / peaks["hbm_gbs"],
+        }
+    else:
+        roofline = {
+            "kernel": "semmoe_grouped_ffn (GEMM1+SwiGLU, GEMM2)",
+            "bound": "hbm", "achieved": gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+            "frac": gbs / peaks["hbm_gbs"], "traffic": _traffic("semmoe_grouped_ffn", spec.name),
+            "peak_source": f"{peaks['source']} HBM copy bandwidth",
+            "algorithmic_bytes": ffn["bytes"], "active_experts": active,
+            "frac_tensor": tflops / peaks["bf16_tflops"],
+        }
     stages = {}
     for name, avg in stage_avg.items():
         ent = {"ms": avg}
@@ -397,11 +479,9 @@ def run_ours(args, world, rank, local):
         "stages": stages,
         "cpu_baseline": cpu,
         "clocks": best["clocks"],
-        "local_activation_rate": None,
+        "local_activation_rate": float(np.trace(counts) / counts.sum()),
+        "around_layer": around,
     }
-    res = layer.forward(x, ids, kpt, k, P, stream=stream)
-    counts = res.counts.cpu().numpy()
-    line["local_activation_rate"] = float(np.trace(counts) / counts.sum())
     print(json.dumps(line), flush=True)
 
 
@@ -418,6 +498,8 @@ def main():
                     help="tokens of the one-pass CPU oracle baseline (capped at T)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true", help="skip the end-to-end (host buffers) timing")
+    ap.add_argument("--no-around", action="store_true",
+                    help="skip timing the scheduling steps around the layer")
     ap.add_argument("--no-graph", action="store_true", help="skip the CUDA-graph replay timing")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)   # at least 3 untimed warm-up steps

@@ -17,6 +17,9 @@
  *   semmoe_grouped_ffn      per-expert SwiGLU FFN over the sorted rows
  *   semmoe_shared_ffn       dense SwiGLU of the shared experts (optional)
  *   semmoe_combine          un-permute and gate-weighted sum
+ * and, around the layer:
+ *   semmoe_dp_schedule      requests placed on data-parallel ranks by affinity
+ *   semmoe_transition_lookup next layer's rank predicted from this layer's experts
  *
  * Conventions (every call):
  *  - Pointers marked [device] are CUDA device pointers owned by the caller;
@@ -70,7 +73,9 @@ enum {
   SEMMOE_DEVERR_K = 8,           /* k_t outside [1, k_max] */
   SEMMOE_DEVERR_PAIRS = 16,      /* more live pairs than the P passed in, or a bad pair index */
   SEMMOE_DEVERR_TIMEOUT = 32,    /* a bounded in-kernel wait gave up */
-  SEMMOE_DEVERR_NONFINITE = 64   /* a non-finite router logit */
+  SEMMOE_DEVERR_NONFINITE = 64,  /* a non-finite router logit or transition score */
+  SEMMOE_DEVERR_OFFSETS = 128,   /* request offsets not non-decreasing from 0 to T */
+  SEMMOE_DEVERR_RANK = 256       /* a predicted or request rank outside [0, R) */
 };
 
 /* Message of the last failing call on this host thread ("" if none). */
@@ -271,6 +276,58 @@ int semmoe_shared_ffn(const void* x, const void* ws13, const void* ws2, int dtyp
 int semmoe_combine(const void* y_perm, const int32_t* pair_to_sorted, const float* topk_w,
                    const void* y_shared, int dtype, int T, int H, int k_max, int P,
                    void* out, void* stream);
+
+/*
+ * semmoe_dp_schedule -- online inter-request scheduling of Attention-DP: a
+ * request is batched onto the data-parallel rank its tokens have the most
+ * affinity with ([SP] ko §2.2 item 2, de §2 B, ja §2.2 B.1).
+ *
+ * Request r owns tokens [req_offsets[r], req_offsets[r+1]).  Its affinity to
+ * rank q is hist[r][q] = #{t in r : pred_rank[t] = q}; req_rank[r] = the q
+ * with the largest count, the lowest q among equal counts (an empty request
+ * goes to rank 0).  Requests are then ordered stably by req_rank, and rank q's
+ * batch is its requests' tokens laid end to end in that order.
+ *
+ * pred_rank        [device] [T] int32 in [0,R) (e.g. from semmoe_affinity_lookup)
+ * req_offsets      [device] [n_req+1] int32, non-decreasing, 0 .. T
+ * hist             [device] [n_req,R] int32 out
+ * req_rank         [device] [n_req] int32 out
+ * req_order        [device] [n_req] int32 out: request ids in scheduled order
+ * rank_req_offsets [device] [R+1] int32 out: req_order range of rank q
+ * req_tok_start    [device] [n_req] int32 out: first slot of request r in tok_order
+ * tok_order        [device] [T] int32 out: token ids in scheduled order
+ * tok_rank         [device] [T] int32 out: req_rank of the token's request (the
+ *                  source rank to pass to semmoe_remote_count)
+ * rank_tok_offsets [device] [R+1] int32 out: tok_order range of rank q
+ * Limits: 1 <= R <= 64; n_req >= 1 unless T == 0.  Offsets that are not
+ * non-decreasing from 0 to T set SEMMOE_DEVERR_OFFSETS (the ranges are clamped
+ * into [0,T] and writes past T are dropped); a pred_rank outside [0,R) counts
+ * as rank 0 and sets SEMMOE_DEVERR_RANK.
+ */
+int semmoe_dp_schedule(const int32_t* pred_rank, const int32_t* req_offsets, int T, int n_req, int R,
+                       int32_t* hist, int32_t* req_rank, int32_t* req_order, int32_t* rank_req_offsets,
+                       int32_t* req_tok_start, int32_t* tok_order, int32_t* tok_rank,
+                       int32_t* rank_tok_offsets, void* stream);
+
+/*
+ * semmoe_transition_lookup -- the rank a token is expected to need in the next
+ * layer, from the experts it chose in this one: the Markovian inter-layer
+ * dependency of [SP] ko §2.1 / de §2 A, held as a table from experts to devices
+ * ([SP] ja §2.3).
+ *   score[t][q] = sum_{j < k_t, topk_idx[t,j] >= 0} trans[topk_idx[t,j]][q],
+ * added in slot order in fp32; pred_next[t] = argmax_q score, lowest q on ties.
+ *
+ * topk_idx    [device] [T,k_max] int32 (-1 = padding slot, skipped)
+ * k_per_token [device] [T] int32 or NULL to use k_uniform for every token
+ * trans       [device] [E,R] fp32 transition weights (finite)
+ * pred_next   [device] [T] int32 out
+ * Limits: 1 <= R <= 64, E >= 1, 1 <= k_max.  Bad experts set
+ * SEMMOE_DEVERR_EXPERT (slot skipped), k_t outside [1,k_max] SEMMOE_DEVERR_K
+ * (clamped), a non-finite score SEMMOE_DEVERR_NONFINITE.
+ */
+int semmoe_transition_lookup(const int32_t* topk_idx, const int32_t* k_per_token, int k_uniform,
+                             const float* trans, int T, int k_max, int E, int R, int32_t* pred_next,
+                             void* stream);
 
 #ifdef __cplusplus
 }

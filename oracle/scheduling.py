@@ -19,18 +19,23 @@ from .moe import _i64
 
 
 def dp_schedule(pred_rank, req_offsets, R: int):
-    """Per-request rank histogram, the chosen rank, and the requests regrouped by rank.
+    """Requests placed on DP ranks by their tokens' predicted ranks.
 
     Readings taken: a request's affinity to rank r is the number of its tokens
     whose predicted rank is r; the request goes to the rank of largest affinity,
     ties (and empty requests) to the lowest rank; requests are then ordered
-    stably by their rank.  Returns hist [n_req, R], req_rank [n_req],
-    req_order [n_req] (request ids in scheduled order), req_pos [n_req] (its
-    inverse) and rank_offsets [R+1] (int64).
+    stably by their rank, and a rank's batch is its requests' tokens laid end
+    to end in that order.  Returns a dict of int64 arrays:
+      hist [n_req, R], req_rank [n_req], req_order [n_req] (request ids in
+      scheduled order), req_pos [n_req] (its inverse), rank_req_offsets [R+1],
+      req_tok_start [n_req] (where request r's first token lands in tok_order),
+      tok_order [T] (token ids in scheduled order), tok_rank [T] (the rank of
+      the token's request), rank_tok_offsets [R+1].
     """
     pred = _i64(pred_rank)
     off = _i64(req_offsets)
     n = off.shape[0] - 1
+    T = pred.shape[0]
     hist = np.zeros((n, R), dtype=np.int64)
     for r in range(n):
         hist[r] = np.bincount(pred[off[r]:off[r + 1]], minlength=R)[:R]
@@ -38,8 +43,26 @@ def dp_schedule(pred_rank, req_offsets, R: int):
     order = np.argsort(req_rank, kind="stable")
     pos = np.empty(n, dtype=np.int64)
     pos[order] = np.arange(n)
-    rank_offsets = np.concatenate([[0], np.cumsum(np.bincount(req_rank, minlength=R))])
-    return hist, req_rank.astype(np.int64), order.astype(np.int64), pos, rank_offsets
+    lens = np.diff(off)
+    rank_req_offsets = np.concatenate([[0], np.cumsum(np.bincount(req_rank, minlength=R))])
+    starts_sched = np.concatenate([[0], np.cumsum(lens[order])])[:-1]
+    req_tok_start = np.empty(n, dtype=np.int64)
+    req_tok_start[order] = starts_sched
+    tok_order = np.concatenate([np.arange(off[r], off[r + 1]) for r in order] or [np.zeros(0)]).astype(np.int64)
+    tok_rank = np.repeat(req_rank, lens).astype(np.int64)
+    rank_tok = np.zeros(R, dtype=np.int64)
+    np.add.at(rank_tok, req_rank, lens)
+    return {
+        "hist": hist,
+        "req_rank": req_rank.astype(np.int64),
+        "req_order": order.astype(np.int64),
+        "req_pos": pos,
+        "rank_req_offsets": rank_req_offsets.astype(np.int64),
+        "req_tok_start": req_tok_start,
+        "tok_order": tok_order,
+        "tok_rank": tok_rank,
+        "rank_tok_offsets": np.concatenate([[0], np.cumsum(rank_tok)]).astype(np.int64),
+    }
 
 
 def transition_lookup(topk_idx_prev, k_per_token, trans):

@@ -112,6 +112,25 @@ def test_remote_count_validation(lib):
     assert rc == 1 and "R" in _err(lib)
 
 
+def test_schedule_validation(lib):
+    p = ctypes.c_void_p(256)
+    # R outside [1, 64]
+    rc = lib.semmoe_dp_schedule(p, p, 8, 2, 65, p, p, p, p, p, p, p, p, None)
+    assert rc == 1 and "R = 65" in _err(lib)
+    # tokens but no request
+    rc = lib.semmoe_dp_schedule(p, p, 8, 0, 4, p, p, p, p, p, p, p, p, None)
+    assert rc == 1 and "no request" in _err(lib)
+    # null token output
+    rc = lib.semmoe_dp_schedule(p, p, 8, 2, 4, p, p, p, p, p, None, p, p, None)
+    assert rc == 1 and "null" in _err(lib)
+    rc = lib.semmoe_transition_lookup(p, None, 3, p, 8, 2, 16, 4, p, None)
+    assert rc == 1 and "k_uniform" in _err(lib)
+    rc = lib.semmoe_transition_lookup(p, None, 1, p, 8, 2, 16, 0, p, None)
+    assert rc == 1 and "R = 0" in _err(lib)
+    rc = lib.semmoe_transition_lookup(p, None, 1, None, 8, 2, 16, 4, p, None)
+    assert rc == 1 and "null" in _err(lib)
+
+
 def test_product_path_fails_loudly_without_library(monkeypatch):
     from token_expert_routing_gb300 import _abi
     monkeypatch.setattr(_abi, "LIB_PATH", "/nonexistent/libsemmoe.so")

@@ -9,12 +9,30 @@ def test_dp_schedule_hand_example():
     # 3 requests over R = 3 ranks: [0,0,1] -> rank 0; [2,1,2,1] -> tie 1/2 -> rank 1; [] -> rank 0
     pred = np.array([0, 0, 1, 2, 1, 2, 1])
     off = np.array([0, 3, 7, 7])
-    hist, rank, order, pos, ro = oracle.dp_schedule(pred, off, 3)
-    np.testing.assert_array_equal(hist, [[2, 1, 0], [0, 2, 2], [0, 0, 0]])
-    np.testing.assert_array_equal(rank, [0, 1, 0])
-    np.testing.assert_array_equal(order, [0, 2, 1])
-    np.testing.assert_array_equal(pos, [0, 2, 1])
-    np.testing.assert_array_equal(ro, [0, 2, 3, 3])
+    s = oracle.dp_schedule(pred, off, 3)
+    np.testing.assert_array_equal(s["hist"], [[2, 1, 0], [0, 2, 2], [0, 0, 0]])
+    np.testing.assert_array_equal(s["req_rank"], [0, 1, 0])
+    np.testing.assert_array_equal(s["req_order"], [0, 2, 1])
+    np.testing.assert_array_equal(s["req_pos"], [0, 2, 1])
+    np.testing.assert_array_equal(s["rank_req_offsets"], [0, 2, 3, 3])
+    # rank 0 batch: request 0 (tokens 0..2) then the empty request 2; rank 1: request 1
+    np.testing.assert_array_equal(s["req_tok_start"], [0, 3, 3])
+    np.testing.assert_array_equal(s["tok_order"], [0, 1, 2, 3, 4, 5, 6])
+    np.testing.assert_array_equal(s["tok_rank"], [0, 0, 0, 1, 1, 1, 1])
+    np.testing.assert_array_equal(s["rank_tok_offsets"], [0, 3, 7, 7])
+
+
+def test_dp_schedule_hand_example_reordered():
+    # requests: [1,1] -> 1, [0] -> 0, [1,0,1] -> 1, [0,0] -> 0  (R = 2)
+    pred = np.array([1, 1, 0, 1, 0, 1, 0, 0])
+    off = np.array([0, 2, 3, 6, 8])
+    s = oracle.dp_schedule(pred, off, 2)
+    np.testing.assert_array_equal(s["req_rank"], [1, 0, 1, 0])
+    np.testing.assert_array_equal(s["req_order"], [1, 3, 0, 2])
+    np.testing.assert_array_equal(s["req_tok_start"], [3, 0, 5, 1])
+    np.testing.assert_array_equal(s["tok_order"], [2, 6, 7, 0, 1, 3, 4, 5])
+    np.testing.assert_array_equal(s["tok_rank"], [1, 1, 0, 1, 1, 1, 0, 0])
+    np.testing.assert_array_equal(s["rank_tok_offsets"], [0, 3, 8])
 
 
 def test_dp_schedule_brute_force_and_invariants():
@@ -23,7 +41,8 @@ def test_dp_schedule_brute_force_and_invariants():
     lens = rng.integers(0, 30, size=60)
     off = np.concatenate([[0], np.cumsum(lens)])
     pred = rng.integers(0, R, size=off[-1])
-    hist, rank, order, pos, ro = oracle.dp_schedule(pred, off, R)
+    s = oracle.dp_schedule(pred, off, R)
+    hist, rank, order, pos, ro = s["hist"], s["req_rank"], s["req_order"], s["req_pos"], s["rank_req_offsets"]
     for r in range(60):
         h = [int(np.sum(pred[off[r]:off[r + 1]] == q)) for q in range(R)]
         assert list(hist[r]) == h
@@ -35,6 +54,18 @@ def test_dp_schedule_brute_force_and_invariants():
     assert (np.diff(order)[same] > 0).all()      # stable
     np.testing.assert_array_equal(pos[order], np.arange(60))
     np.testing.assert_array_equal(np.diff(ro), np.bincount(rank, minlength=R))
+    # token side: a permutation of 0..T-1; each rank's slice holds exactly the
+    # tokens of its requests, each request contiguous and in order
+    T = off[-1]
+    tok, rto = s["tok_order"], s["rank_tok_offsets"]
+    assert sorted(tok.tolist()) == list(range(T))
+    for q in range(R):
+        want = [t for r in order if rank[r] == q for t in range(off[r], off[r + 1])]
+        assert tok[rto[q]:rto[q + 1]].tolist() == want
+    for r in range(60):
+        st = s["req_tok_start"][r]
+        assert tok[st:st + lens[r]].tolist() == list(range(off[r], off[r + 1]))
+        assert (s["tok_rank"][off[r]:off[r + 1]] == rank[r]).all()
 
 
 def test_transition_lookup_brute_force():

@@ -18,6 +18,10 @@ LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libsemmoe.s
 SEMMOE_OK, SEMMOE_ERR_INVALID_ARG, SEMMOE_ERR_UNSUPPORTED, SEMMOE_ERR_CUDA, \
     SEMMOE_ERR_DEVICE_CHECK, SEMMOE_ERR_DEVICE_TIMEOUT = range(6)
 SEMMOE_F32, SEMMOE_BF16 = 0, 1
+# device error word bits (semmoe_check_errors)
+SEMMOE_DEVERR_EXPERT, SEMMOE_DEVERR_TOKEN_ID, SEMMOE_DEVERR_LUT, SEMMOE_DEVERR_K, SEMMOE_DEVERR_PAIRS, \
+    SEMMOE_DEVERR_TIMEOUT, SEMMOE_DEVERR_NONFINITE, SEMMOE_DEVERR_OFFSETS, SEMMOE_DEVERR_RANK = \
+    (1 << i for i in range(9))
 
 _DTYPE = {torch.float32: SEMMOE_F32, torch.bfloat16: SEMMOE_BF16}
 
@@ -43,13 +47,16 @@ SIGNATURES = {
     "semmoe_shared_ffn_workspace_size": (_sz, [_i, _i, _i]),
     "semmoe_shared_ffn": (_i, [_vp, _vp, _vp, _i, _i, _i, _i, _vp, _vp, _sz, _vp]),
     "semmoe_combine": (_i, [_vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _vp, _vp]),
+    "semmoe_dp_schedule": (_i, [_vp, _vp, _i, _i, _i, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp]),
+    "semmoe_transition_lookup": (_i, [_vp, _vp, _i, _vp, _i, _i, _i, _i, _vp, _vp]),
 }
 
 
 class SemMoEError(RuntimeError):
-    def __init__(self, code: int, msg: str):
+    def __init__(self, code: int, msg: str, bits: int = 0):
         super().__init__(f"[semmoe status {code}] {msg}")
         self.code = code
+        self.bits = bits   # device error word bits, for SEMMOE_ERR_DEVICE_CHECK / _TIMEOUT
 
 
 _lib = None
@@ -115,10 +122,12 @@ def semmoe_kernel_launches() -> int:
 
 
 def semmoe_check_errors(stream=None) -> int:
-    """Synchronise the stream and raise if a kernel flagged bad data; returns the bits."""
+    """Synchronise the stream and raise if a kernel flagged bad data (the
+    error's ``bits`` holds the device error word); returns the bits (0)."""
     bits = ctypes.c_int(0)
     rc = lib().semmoe_check_errors(_stream(stream), ctypes.byref(bits))
-    _check(rc)
+    if rc != SEMMOE_OK:
+        raise SemMoEError(rc, lib().semmoe_last_error().decode(), bits.value)
     return bits.value
 
 
@@ -167,7 +176,7 @@ def semmoe_permute_noalloc(topk_idx, expert_rank, x, T, H, E, R, k_max, P, exper
                            phys_to_expert, expert_counts, sorted_to_pair, pair_to_sorted, x_perm,
                            stream=None):
     """semmoe_permute without a workspace: for callers that cannot allocate
-    device memory (the scratch is a static 1 MiB array inside the library)."""
+    device memory (the scratch is a static 96 KiB array inside the library)."""
     d = dtype_code(x) if x is not None else SEMMOE_F32
     _check(lib().semmoe_permute_noalloc(_p(topk_idx), _p(expert_rank), _p(x), d, T, H, E, R, k_max, P,
                                         _p(expert_offsets), _p(rank_offsets), _p(phys_to_expert),
@@ -199,3 +208,15 @@ def semmoe_shared_ffn(x, ws13, ws2, T, H, I_s, y_shared, ws, stream=None):
 def semmoe_combine(y_perm, pair_to_sorted, topk_w, y_shared, T, H, k_max, P, out, stream=None):
     _check(lib().semmoe_combine(_p(y_perm), _p(pair_to_sorted), _p(topk_w), _p(y_shared),
                                 dtype_code(out), T, H, k_max, P, _p(out), _stream(stream)))
+
+
+def semmoe_dp_schedule(pred_rank, req_offsets, T, n_req, R, hist, req_rank, req_order, rank_req_offsets,
+                       req_tok_start, tok_order, tok_rank, rank_tok_offsets, stream=None):
+    _check(lib().semmoe_dp_schedule(_p(pred_rank), _p(req_offsets), T, n_req, R, _p(hist), _p(req_rank),
+                                    _p(req_order), _p(rank_req_offsets), _p(req_tok_start), _p(tok_order),
+                                    _p(tok_rank), _p(rank_tok_offsets), _stream(stream)))
+
+
+def semmoe_transition_lookup(topk_idx, k_per_token, k_uniform, trans, T, k_max, E, R, pred_next, stream=None):
+    _check(lib().semmoe_transition_lookup(_p(topk_idx), _p(k_per_token), k_uniform, _p(trans), T, k_max, E, R,
+                                          _p(pred_next), _stream(stream)))

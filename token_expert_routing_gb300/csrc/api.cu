@@ -77,7 +77,7 @@ int semmoe_check_errors(void* stream, int* bits) {
   if (e != cudaSuccess) return cuda_status(e, "semmoe_check_errors");
   int b = 0;
   if (route_take_errors(s, &b) || permute_take_errors(s, &b) || ffn_take_errors(s, &b) ||
-      combine_take_errors(s, &b))
+      combine_take_errors(s, &b) || schedule_take_errors(s, &b))
     return cuda_status(cudaGetLastError(), "semmoe_check_errors: reading the device error word");
   if (bits != nullptr) *bits = b;
   if (b & SEMMOE_DEVERR_TIMEOUT) return fail(SEMMOE_ERR_DEVICE_TIMEOUT, "a bounded in-kernel wait ran out (bits 0x%x)", b);
@@ -278,6 +278,41 @@ int semmoe_combine(const void* y_perm, const int32_t* pair_to_sorted, const floa
   return cuda_status(launch_combine(y_perm, pair_to_sorted, topk_w, y_shared, dtype, T, H, k_max, P, out,
                                     static_cast<cudaStream_t>(stream)),
                      "semmoe_combine");
+}
+
+int semmoe_dp_schedule(const int32_t* pred_rank, const int32_t* req_offsets, int T, int n_req, int R, int32_t* hist,
+                       int32_t* req_rank, int32_t* req_order, int32_t* rank_req_offsets, int32_t* req_tok_start,
+                       int32_t* tok_order, int32_t* tok_rank, int32_t* rank_tok_offsets, void* stream) {
+  REQUIRE(T >= 0 && n_req >= 0, "semmoe_dp_schedule: bad sizes T=%d n_req=%d", T, n_req);
+  REQUIRE(R >= 1 && R <= 64, "semmoe_dp_schedule: R = %d outside [1, 64]", R);
+  REQUIRE(n_req >= 1 || T == 0, "semmoe_dp_schedule: %d tokens but no request", T);
+  REQUIRE((long long)n_req * R < (1LL << 31), "semmoe_dp_schedule: n_req * R too large");
+  REQUIRE(req_offsets && rank_req_offsets && rank_tok_offsets, "semmoe_dp_schedule: null pointer");
+  REQUIRE(n_req == 0 || (hist && req_rank && req_order && req_tok_start), "semmoe_dp_schedule: null request output");
+  REQUIRE(T == 0 || (pred_rank && tok_order && tok_rank), "semmoe_dp_schedule: null token array");
+  CHECK_DEVICE("semmoe_dp_schedule");
+  return cuda_status(launch_dp_schedule(pred_rank, req_offsets, T, n_req, R, hist, req_rank, req_order,
+                                        rank_req_offsets, req_tok_start, tok_order, tok_rank, rank_tok_offsets,
+                                        static_cast<cudaStream_t>(stream)),
+                     "semmoe_dp_schedule");
+}
+
+int semmoe_transition_lookup(const int32_t* topk_idx, const int32_t* k_per_token, int k_uniform, const float* trans,
+                             int T, int k_max, int E, int R, int32_t* pred_next, void* stream) {
+  REQUIRE(T >= 0 && k_max >= 1 && E >= 1, "semmoe_transition_lookup: bad sizes T=%d k_max=%d E=%d", T, k_max, E);
+  REQUIRE(R >= 1 && R <= 64, "semmoe_transition_lookup: R = %d outside [1, 64]", R);
+  REQUIRE((long long)T * k_max < (1LL << 31) && (long long)E * R < (1LL << 31),
+          "semmoe_transition_lookup: T * k_max or E * R too large");
+  REQUIRE(k_per_token != nullptr || (k_uniform >= 1 && k_uniform <= k_max),
+          "semmoe_transition_lookup: k_uniform = %d outside [1, k_max = %d]", k_uniform, k_max);
+  if (T == 0) return SEMMOE_OK;
+  REQUIRE(topk_idx && trans && pred_next, "semmoe_transition_lookup: null pointer");
+  REQUIRE(aligned(trans, 4) && aligned(topk_idx, 4) && aligned(pred_next, 4) && aligned(k_per_token, 4),
+          "semmoe_transition_lookup: misaligned pointer");
+  CHECK_DEVICE("semmoe_transition_lookup");
+  return cuda_status(launch_transition_lookup(topk_idx, k_per_token, k_uniform, trans, T, k_max, E, R, pred_next,
+                                              static_cast<cudaStream_t>(stream)),
+                     "semmoe_transition_lookup");
 }
 
 }  // extern "C"

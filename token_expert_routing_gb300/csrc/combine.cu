@@ -125,12 +125,6 @@ combine_kernel(const T* __restrict__ y_perm, const int32_t* __restrict__ pair_to
   }
 }
 
-int sm_count() {
-  int dev = 0, n = 148;
-  if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
-  return n;
-}
-
 }  // namespace
 
 int combine_take_errors(cudaStream_t s, int* bits) { return take_error_word(g_err, s, bits); }

@@ -73,4 +73,11 @@ inline cudaError_t ensure_smem_limit(K kernel, int bytes, std::atomic<unsigned l
 }
 inline int ceil_div(int a, int b) { return (a + b - 1) / b; }
 
+// Streaming multiprocessors of the current device.
+inline int sm_count() {
+  int dev = 0, n = 152;
+  if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+  return n;
+}
+
 }  // namespace semmoe

@@ -15,6 +15,7 @@ int route_take_errors(cudaStream_t s, int* bits);
 int permute_take_errors(cudaStream_t s, int* bits);
 int ffn_take_errors(cudaStream_t s, int* bits);
 int combine_take_errors(cudaStream_t s, int* bits);
+int schedule_take_errors(cudaStream_t s, int* bits);
 
 size_t route_ws_bytes(int T, int H, int E, int x_dtype, int w_dtype);
 // Tensor-core router (route_tc.cu): fp32 logits of bf16 activations.
@@ -60,5 +61,13 @@ cudaError_t launch_ffn(const void* x, const int32_t* offsets, const int32_t* phy
 cudaError_t launch_combine(const void* y_perm, const int32_t* pair_to_sorted, const float* topk_w,
                            const void* y_shared, int dtype, int T, int H, int k_max, int P,
                            void* out, cudaStream_t s);
+
+cudaError_t launch_dp_schedule(const int32_t* pred, const int32_t* off, int T, int n_req, int R, int32_t* hist,
+                               int32_t* req_rank, int32_t* req_order, int32_t* rank_req_offsets,
+                               int32_t* req_tok_start, int32_t* tok_order, int32_t* tok_rank,
+                               int32_t* rank_tok_offsets, cudaStream_t s);
+
+cudaError_t launch_transition_lookup(const int32_t* topk_idx, const int32_t* kpt, int ku, const float* trans, int T,
+                                     int k_max, int E, int R, int32_t* pred_next, cudaStream_t s);
 
 }  // namespace semmoe

@@ -209,12 +209,6 @@ perm_gather_kernel(const unsigned char* __restrict__ x, const int32_t* __restric
   }
 }
 
-int sm_count() {
-  int dev = 0, n = 148;
-  if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
-  return n;
-}
-
 }  // namespace
 
 int permute_take_errors(cudaStream_t s, int* bits) { return take_error_word(g_err, s, bits); }

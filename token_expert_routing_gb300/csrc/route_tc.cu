@@ -207,7 +207,7 @@ int route_tc_k_slices(int T, int H, int E, int w_dtype) {
   const int EC = experts_per_pass(E, S), n_pass = (E + EC - 1) / EC;
   const long long ctas = (long long)((T + BM - 1) / BM) * n_pass;
   const int kb_all = (H + BK - 1) / BK;
-  int ks = (int)(tc::sm_count() / (ctas > 0 ? ctas : 1));
+  int ks = (int)(sm_count() / (ctas > 0 ? ctas : 1));
   if (ks > kb_all / 4) ks = kb_all / 4;
   if (ks > kMaxKSlices) ks = kMaxKSlices;
   return ks < 1 ? 1 : ks;

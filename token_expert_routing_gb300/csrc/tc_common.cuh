@@ -323,11 +323,5 @@ inline bool make_map_bf16(CUtensorMap* m, const void* base, int rank, const cuui
   return r == CUDA_SUCCESS;
 }
 
-inline int sm_count() {
-  int dev = 0, n = 148;
-  if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
-  return n;
-}
-
 }  // namespace tc
 }  // namespace semmoe

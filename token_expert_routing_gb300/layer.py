@@ -1,8 +1,9 @@
 """One affinity-aware MoE layer forward on one GPU, through the C ABI.
 
-``MoELayer.forward`` enqueues the six library calls on the current stream:
-route -> affinity lookup -> remote count -> permute -> grouped FFN (+ shared
-FFN) -> combine.  Torch only provides device memory and the stream; every
+``MoELayer.forward`` enqueues the library calls on the current stream:
+route -> affinity lookup (-> request scheduling) -> remote count -> permute ->
+grouped FFN (+ shared FFN) -> combine, plus the next-layer transition lookup
+when the layer holds a transition table.  Torch only provides device memory and the stream; every
 step runs in the library's kernels, and nothing synchronises the host.
 """
 from __future__ import annotations
@@ -33,6 +34,8 @@ class LayerOutput:
     x_perm: torch.Tensor
     y_perm: torch.Tensor
     y_shared: Optional[torch.Tensor]
+    schedule: Optional[dict] = None      # semmoe_dp_schedule outputs (when req_offsets is given)
+    pred_next: Optional[torch.Tensor] = None  # next-layer rank per token (when trans is held)
 
 
 class MoELayer:
@@ -40,17 +43,19 @@ class MoELayer:
 
     w_router [E,H] (fp32 or bf16), w13 [E,2I,H], w2 [E,H,I] (activation type),
     expert_rank [E] and lut [V] int32, R logical ranks, k_max the largest budget;
-    ws13 [2*I_s,H] / ws2 [H,I_s] optional shared experts.
+    ws13 [2*I_s,H] / ws2 [H,I_s] optional shared experts; trans [E,R] fp32 an
+    optional expert -> next-layer-rank transition table.
     """
 
     def __init__(self, w_router, w13, w2, expert_rank, lut, R: int, k_max: int, ws13=None, ws2=None,
-                 device="cuda"):
+                 trans=None, device="cuda"):
         dev = torch.device(device)
         c = lambda t: None if t is None else t.to(dev).contiguous()  # noqa: E731
         self.w_router, self.w13, self.w2 = c(w_router), c(w13), c(w2)
         self.expert_rank = c(expert_rank).to(torch.int32)
         self.lut = c(lut).to(torch.int32)
         self.ws13, self.ws2 = c(ws13), c(ws2)
+        self.trans = None if trans is None else c(trans).to(torch.float32)
         self.E, twoI, self.H = self.w13.shape
         self.I = twoI // 2
         self.I_s = 0 if ws13 is None else self.ws13.shape[0] // 2
@@ -67,11 +72,15 @@ class MoELayer:
         return buf
 
     def forward(self, x, token_ids, k_per_token=None, k: Optional[int] = None, P: Optional[int] = None,
-                logits_in=None, keep_logits: bool = False, stream=None, marks=None) -> LayerOutput:
+                logits_in=None, keep_logits: bool = False, stream=None, marks=None,
+                req_offsets=None) -> LayerOutput:
         """x [T,H] (activation type) and token_ids [T] int32 on the device.
 
         Budgets: ``k`` for every token, or ``k_per_token`` [T] int32 on the device
         together with ``P`` = its sum (known to the caller, so no host sync).
+        ``req_offsets`` [n_req+1] int32 on the device: the batch's requests; when
+        given, requests are scheduled onto ranks by affinity and each token's
+        source rank for the remote count is its request's rank.
         ``marks``: optional list; a CUDA event is recorded on the stream after
         each step and appended as (step name, event), for per-step timing.
         """
@@ -104,9 +113,26 @@ class MoELayer:
         mark("route")
         pred = torch.empty(T, **i32)
         abi.semmoe_affinity_lookup(token_ids, self.lut, self.V, R, T, pred, stream)
+        src = pred
+        sched = None
+        if req_offsets is not None:
+            n_req = req_offsets.shape[0] - 1
+            sched = dict(hist=torch.empty(max(n_req, 1), R, **i32), req_rank=torch.empty(max(n_req, 1), **i32),
+                         req_order=torch.empty(max(n_req, 1), **i32), rank_req_offsets=torch.empty(R + 1, **i32),
+                         req_tok_start=torch.empty(max(n_req, 1), **i32), tok_order=torch.empty(T, **i32),
+                         tok_rank=torch.empty(T, **i32), rank_tok_offsets=torch.empty(R + 1, **i32))
+            abi.semmoe_dp_schedule(pred, req_offsets, T, n_req, R, sched["hist"], sched["req_rank"],
+                                   sched["req_order"], sched["rank_req_offsets"], sched["req_tok_start"],
+                                   sched["tok_order"], sched["tok_rank"], sched["rank_tok_offsets"], stream)
+            src = sched["tok_rank"]
+        pred_next = None
+        if self.trans is not None:
+            pred_next = torch.empty(T, **i32)
+            abi.semmoe_transition_lookup(topk_idx, k_per_token, k or 0, self.trans, T, k_max, E, R, pred_next,
+                                         stream)
         counts = torch.empty(R, R, **i32)
         remote = torch.empty(R, **i32)
-        abi.semmoe_remote_count(topk_idx, pred, self.expert_rank, T, k_max, E, R, counts, remote, stream)
+        abi.semmoe_remote_count(topk_idx, src, self.expert_rank, T, k_max, E, R, counts, remote, stream)
         mark("lookup_count")
         expert_offsets = torch.empty(E + 1, **i32)
         rank_offsets = torch.empty(R + 1, **i32)
@@ -137,7 +163,7 @@ class MoELayer:
         mark("combine")
         return LayerOutput(out, logits, topk_idx, topk_w, pred, counts, remote, expert_offsets,
                            rank_offsets, phys_to_expert, expert_counts, sorted_to_pair[:P],
-                           pair_to_sorted, x_perm, y_perm, y_shared)
+                           pair_to_sorted, x_perm, y_perm, y_shared, sched, pred_next)
 
     def forward_host(self, x_host, ids_host, k_host=None, k: Optional[int] = None, out_host=None,
                      stream=None) -> torch.Tensor:
@@ -229,7 +255,7 @@ class CapturedLayer:
     """
 
     def __init__(self, layer: MoELayer, T: int, k: Optional[int] = None, k_per_token_host=None,
-                 warmup: int = 2):
+                 req_offsets_host=None, warmup: int = 2):
         if (k is None) == (k_per_token_host is None):
             raise ValueError("give exactly one of k and k_per_token_host")
         dev = layer.device
@@ -242,16 +268,18 @@ class CapturedLayer:
         if k_per_token_host is not None:
             self.k_per_token = k_per_token_host.to(dev, torch.int32)
             self.P = int(k_per_token_host.sum())
+        self.req_offsets = None if req_offsets_host is None else req_offsets_host.to(dev, torch.int32)
         side = torch.cuda.Stream(device=dev)
         side.wait_stream(torch.cuda.current_stream(dev))
         with torch.cuda.stream(side):           # allocate workspaces and set kernel attributes
             for _ in range(warmup):
-                layer.forward(self.x, self.token_ids, self.k_per_token, k, self.P, stream=side)
+                layer.forward(self.x, self.token_ids, self.k_per_token, k, self.P, stream=side,
+                              req_offsets=self.req_offsets)
         torch.cuda.current_stream(dev).wait_stream(side)
         self.graph = torch.cuda.CUDAGraph()
         with torch.cuda.graph(self.graph):
             self.result = layer.forward(self.x, self.token_ids, self.k_per_token, k, self.P,
-                                        stream=torch.cuda.current_stream(dev))
+                                        stream=torch.cuda.current_stream(dev), req_offsets=self.req_offsets)
 
     def replay(self) -> LayerOutput:
         self.graph.replay()

@@ -59,6 +59,7 @@ class LayerSpec:
     sub_split: int = 1          # sub-experts per parent expert (MoE-Prism)
     k_choices: tuple = ()       # per-request top-k budgets, request r gets k_choices[r % len]
     tokens_per_request: int = 1
+    req_len_mean: int = 0       # > 0: requests of lognormal length with this mean (prefill batches)
     seed: int = 1000
 
     @property
@@ -79,7 +80,7 @@ CONFIGS = {
     "dsv2lite_prefill_T4096": _spec(
         name="dsv2lite_prefill_T4096", T=4096, H=2048, E=64, I=1408, R=8, k=6,
         dtype="bf16", router_dtype="f32", I_shared=2816, V=102400, zipf_s=1.1,
-        bias=3.0, k_pref=6, placement="clustered", lut="affinity", seed=1001),
+        bias=3.0, k_pref=6, placement="clustered", lut="affinity", req_len_mean=512, seed=1001),
     # Decode-shaped variants of the same layer (one token per request).
     "dsv2lite_decode_T64": _spec(
         name="dsv2lite_decode_T64", T=64, H=2048, E=64, I=1408, R=8, k=6,
@@ -97,7 +98,7 @@ CONFIGS = {
     "qwen3_30b_a3b_T16384": _spec(
         name="qwen3_30b_a3b_T16384", T=16384, H=2048, E=128, I=768, R=8, k=8,
         dtype="bf16", router_dtype="bf16", V=151936, zipf_s=1.0, bias=2.5, k_pref=8,
-        placement="clustered", lut="affinity", seed=1003),
+        placement="clustered", lut="affinity", req_len_mean=1024, seed=1003),
     # MoE-Prism elastic layer: 64 experts x 4 sub-experts (I = 1408 / 4 = 352),
     # 32 requests of 256 tokens with budgets {12,16,20,24} in one batch.
     "prism_subexpert_T8192": _spec(
@@ -235,6 +236,51 @@ def _normal_f32(shape, scale: float, seed: int, tag: int) -> np.ndarray:
     return a.reshape(shape)
 
 
+def request_offsets(T: int, seed: int, mean_len: int = 0, fixed_len: int = 1,
+                    empty_every: int = 0) -> np.ndarray:
+    """Token offsets [n_req+1] (int32) of the requests in a batch of T tokens.
+
+    mean_len > 0: lengths drawn lognormal (sigma 0.8) with that mean, at least 1,
+    the last request cut at T (a prefill batch of prompts); otherwise every
+    request has ``fixed_len`` tokens (the last one the remainder).
+    empty_every > 0 inserts an empty request after every that many requests.
+    """
+    if mean_len > 0:
+        rng = np.random.Generator(np.random.PCG64(np.random.SeedSequence([seed, 1001])))
+        lens = []
+        total = 0
+        sigma = 0.8
+        mu = np.log(mean_len) - sigma * sigma / 2
+        while total < T:
+            n = int(max(1, round(rng.lognormal(mu, sigma))))
+            n = min(n, T - total)
+            lens.append(n)
+            total += n
+    else:
+        full, rest = divmod(T, fixed_len)
+        lens = [fixed_len] * full + ([rest] if rest else [])
+    if empty_every > 0:
+        out = []
+        for i, n in enumerate(lens):
+            out.append(n)
+            if (i + 1) % empty_every == 0:
+                out.append(0)
+        lens = out
+    return np.concatenate([[0], np.cumsum(lens, dtype=np.int64)]).astype(np.int32)
+
+
+def transition_table(E: int, R: int, seed: int, samples: int = 1000) -> np.ndarray:
+    """Expert -> next-layer-rank transition counts [E,R] (float32, integer-valued).
+
+    Row e is ``samples`` draws from a multinomial whose probabilities follow a
+    Dirichlet(0.3) law, so each expert leans to a few ranks, as a table profiled
+    from a skewed routing trace would.  Integer values keep fp32 sums exact.
+    """
+    rng = np.random.Generator(np.random.PCG64(np.random.SeedSequence([seed, 1002])))
+    probs = rng.dirichlet(np.full(R, 0.3), size=E)
+    return np.stack([rng.multinomial(samples, p) for p in probs]).astype(np.float32)
+
+
 def _to(a: np.ndarray, dtype: str) -> torch.Tensor:
     t = torch.from_numpy(np.ascontiguousarray(a, dtype=np.float32))
     return t.to(torch.bfloat16) if dtype == "bf16" else t
@@ -245,7 +291,8 @@ def make_inputs(spec: LayerSpec, with_weights: bool = True) -> dict:
 
     Returns x [T,H], w_router [E,H], w13 [E,2I,H] (rows 0..I-1 gate, I..2I-1 up),
     w2 [E,H,I], ws13 [2*I_shared,H] / ws2 [H,I_shared] (or None), token_ids [T],
-    lut [V], expert_rank [E], k_per_token [T] (all int32), and the spec.
+    lut [V], expert_rank [E], k_per_token [T], req_offsets [n_req+1] (all int32),
+    trans [E,R] (float32 next-layer transition counts), and the spec.
     """
     rng = np.random.Generator(np.random.PCG64(spec.seed))
     T, H, E, I, R = spec.T, spec.H, spec.E, spec.I, spec.R
@@ -300,6 +347,8 @@ def make_inputs(spec: LayerSpec, with_weights: bool = True) -> dict:
         lut=torch.from_numpy(lut),
         expert_rank=torch.from_numpy(expert_rank.astype(np.int32)),
         k_per_token=torch.from_numpy(kpt.astype(np.int32)),
+        req_offsets=torch.from_numpy(request_offsets(T, spec.seed, spec.req_len_mean, spec.tokens_per_request)),
+        trans=torch.from_numpy(transition_table(E, R, spec.seed)),
         w13=None, w2=None, ws13=None, ws2=None,
     )
     if with_weights:
