@@ -32,3 +32,4 @@ from .moe import (  # noqa: F401
     moe_layer,
 )
 from .scheduling import dp_schedule, transition_lookup  # noqa: F401
+from .prism import hier_route, split_expert_weights, sub_scores  # noqa: F401

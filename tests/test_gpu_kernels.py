@@ -149,6 +149,34 @@ def test_combine(dtype, shared):
     assert max_rel(np_(out), ref) < (1e-6 if dtype == "f32" else 8e-3)
 
 
+@pytest.mark.parametrize("dtype,T,H,E,k_max,shared", [
+    ("bf16", 1000, 2048, 64, 6, True),      # full 512-element passes, shared row first
+    ("bf16", 300, 2056, 64, 8, False),      # a ragged last pass
+    ("f32", 257, 1032, 32, 24, True),       # per-token budgets up to 24: padding in most rows
+    ("bf16", 129, 520, 64, 32, False),      # every lane holds a slot
+    ("bf16", 65, 264, 64, 33, True),        # budgets above 32: the slot read directly
+    ("f32", 3, 4, 8, 2, False),             # rows of 16 bytes
+])
+def test_combine_shapes(dtype, T, H, E, k_max, shared):
+    """Combine against the oracle on ragged widths and budgets, output
+    pre-filled so an unwritten element shows."""
+    rng = np.random.default_rng(T + H)
+    tdt = torch.bfloat16 if dtype == "bf16" else torch.float32
+    idx, k = _route_random(rng, T, E, k_max)
+    _, w = oracle.topk_route(rng.standard_normal((T, E)), k, k_max)
+    perm = oracle.permute(idx, k, np.arange(E) % 4, 4)
+    P = int(k.sum())
+    y = torch.from_numpy(rng.standard_normal((P, H)).astype(np.float32)).to(tdt).cuda()
+    ys = torch.from_numpy(rng.standard_normal((T, H)).astype(np.float32)).to(tdt).cuda() if shared else None
+    p2s = torch.from_numpy(perm["pair_to_sorted"].astype(np.int32)).cuda()
+    wd = torch.from_numpy(w.astype(np.float32)).cuda()
+    out = torch.full((T, H), 7.0, dtype=tdt, device="cuda")
+    abi().semmoe_combine(y, p2s, wd, ys, T, H, k_max, P, out)
+    assert abi().semmoe_check_errors() == 0
+    ref = oracle.combine(y.cpu(), perm["pair_to_sorted"], w, k, dtype, None if ys is None else ys.cpu())
+    assert max_rel(np_(out), ref) < (1e-6 if dtype == "f32" else 8e-3)
+
+
 def test_data_errors_are_reported_not_faulted():
     """A token id beyond the vocabulary and a table value beyond R are caught
     by the kernels' own bounds checks and reported after a sync."""

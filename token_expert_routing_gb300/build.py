@@ -23,6 +23,7 @@ LIB = os.path.join(PKG, "libsemmoe.so")
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC,-O2", "--expt-relaxed-constexpr",
+              "-Werror", "cross-execution-space-call",
               "-I" + INCLUDE, "-I" + CSRC] + ARCH
 
 

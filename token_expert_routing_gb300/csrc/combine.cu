@@ -2,7 +2,7 @@
 // Shuffled-Allgather, which brings the expert results back to the original
 // token order (Semantic Parallelism (de) §2 B, (ja) §2.2 B):
 //   out[t] = y_shared[t] + sum_{j<k_t} w[t,j] * y_perm[pair_to_sorted[t*k_max+j]]
-// summed in that order in fp32.  One warp per token row, 16-byte vectors.
+// summed in that order in fp32.
 #include "common.cuh"
 #include "internal.h"
 
@@ -25,11 +25,15 @@ template <> struct Vec16<float> {
   __device__ static void store(float* p, const float* v) {
     *reinterpret_cast<float4*>(p) = make_float4(v[0], v[1], v[2], v[3]);
   }
+  __device__ static void unpack(const uint4& a, float* v) {
+    v[0] = __uint_as_float(a.x); v[1] = __uint_as_float(a.y);
+    v[2] = __uint_as_float(a.z); v[3] = __uint_as_float(a.w);
+  }
 };
 template <> struct Vec16<__nv_bfloat16> {
   static constexpr int N = 8;
-  __device__ static void load(const __nv_bfloat16* p, float* v) {
-    uint4 a = *reinterpret_cast<const uint4*>(p);
+  __device__ static void load(const __nv_bfloat16* p, float* v) { unpack(*reinterpret_cast<const uint4*>(p), v); }
+  __device__ static void unpack(const uint4& a, float* v) {
     const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&a);
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
@@ -46,19 +50,27 @@ template <> struct Vec16<__nv_bfloat16> {
   }
 };
 
-// One warp per token.  The token's (sorted row, gate) pairs are held by lanes
-// 0..k_max-1 and broadcast with shuffles; every lane accumulates CH 16-byte
-// chunks per pass (chunks lane, lane+32, ...), so a pass keeps CH * k_t
-// independent gathers in flight per lane.
-template <typename T, int CH>
-__global__ void __launch_bounds__(kThreads)
+// One warp per (token, column pass): a pass covers 32 lanes x CH 16-byte
+// chunks of the row.  The token's (sorted row, gate) pairs sit in lanes
+// 0..k_max-1 and are broadcast with shuffles; the rows are fetched JB slots at
+// a time with every load of a batch issued before the first add (padding slots
+// load nothing and leave the sum untouched), so each lane keeps JB * CH
+// 16-byte loads in flight.  The sum runs y_shared first, then the slots in
+// order, with fmaf.
+template <typename T, int CH, int JB>
+__global__ void __launch_bounds__(kThreads, 3)
 combine_kernel(const T* __restrict__ y_perm, const int32_t* __restrict__ pair_to_sorted,
                const float* __restrict__ topk_w, const T* __restrict__ y_shared, int T_, int H, int k_max,
                int P, T* __restrict__ out) {
   using V = Vec16<T>;
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   const int kk = k_max < 32 ? k_max : 32;
-  for (int t = blockIdx.x * kWarps + warp; t < T_; t += gridDim.x * kWarps) {
+  const int pass_elems = 32 * V::N * CH;
+  const int n_pass = (H + pass_elems - 1) / pass_elems;
+  const long long units = (long long)T_ * n_pass;
+  for (long long u = (long long)blockIdx.x * kWarps + warp; u < units; u += (long long)gridDim.x * kWarps) {
+    const int t = (int)(u / n_pass);
+    const int base = (int)(u - (long long)t * n_pass) * pass_elems;
     const int32_t* q_row = pair_to_sorted + (size_t)t * k_max;
     const float* w_row = topk_w + (size_t)t * k_max;
     int q_l = -1;
@@ -68,59 +80,65 @@ combine_kernel(const T* __restrict__ y_perm, const int32_t* __restrict__ pair_to
       w_l = w_row[lane];
       if (q_l >= P) { flag(SEMMOE_DEVERR_PAIRS); q_l = -1; }
     }
-    for (int base = 0; base < H; base += 32 * V::N * CH) {
-      float acc[CH][V::N];
+    float acc[CH][V::N];
 #pragma unroll
-      for (int u = 0; u < CH; ++u) {
-        const int c = base + (u * 32 + lane) * V::N;
-        if (y_shared != nullptr && c < H) {
-          V::load(y_shared + (size_t)t * H + c, acc[u]);
-        } else {
+    for (int c = 0; c < CH; ++c) {
+      const int col = base + (c * 32 + lane) * V::N;
+      if (y_shared != nullptr && col < H) {
+        V::load(y_shared + (size_t)t * H + col, acc[c]);
+      } else {
 #pragma unroll
-          for (int i = 0; i < V::N; ++i) acc[u][i] = 0.f;
-        }
+        for (int i = 0; i < V::N; ++i) acc[c][i] = 0.f;
       }
-#pragma unroll 2
-      for (int j = 0; j < kk; ++j) {
-        const int q = __shfl_sync(0xffffffffu, q_l, j);
-        const float w = __shfl_sync(0xffffffffu, w_l, j);
-        if (q < 0) continue;
-        float v[CH][V::N];
+    }
+    for (int j0 = 0; j0 < kk; j0 += JB) {
+      uint4 raw[JB][CH];
+      float wj[JB];
+      bool ok[JB];
 #pragma unroll
-        for (int u = 0; u < CH; ++u) {
-          const int c = base + (u * 32 + lane) * V::N;
-          if (c < H) V::load(y_perm + (size_t)q * H + c, v[u]);
-        }
+      for (int b = 0; b < JB; ++b) {
+        const int q = __shfl_sync(0xffffffffu, q_l, (j0 + b) & 31);
+        wj[b] = __shfl_sync(0xffffffffu, w_l, (j0 + b) & 31);
+        ok[b] = j0 + b < kk && q >= 0;
 #pragma unroll
-        for (int u = 0; u < CH; ++u) {
-          const int c = base + (u * 32 + lane) * V::N;
-          if (c < H) {
-#pragma unroll
-            for (int i = 0; i < V::N; ++i) acc[u][i] = fmaf(w, v[u][i], acc[u][i]);
-          }
-        }
-      }
-      for (int j = 32; j < k_max; ++j) {  // budgets above 32 experts: read the slot directly
-        const int q = q_row[j];
-        if (q < 0) continue;
-        if (q >= P) { flag(SEMMOE_DEVERR_PAIRS); continue; }
-        const float w = w_row[j];
-#pragma unroll
-        for (int u = 0; u < CH; ++u) {
-          const int c = base + (u * 32 + lane) * V::N;
-          if (c < H) {
-            float v[V::N];
-            V::load(y_perm + (size_t)q * H + c, v);
-#pragma unroll
-            for (int i = 0; i < V::N; ++i) acc[u][i] = fmaf(w, v[i], acc[u][i]);
-          }
+        for (int c = 0; c < CH; ++c) {
+          const int col = base + (c * 32 + lane) * V::N;
+          raw[b][c] = (ok[b] && col < H) ? *reinterpret_cast<const uint4*>(y_perm + (size_t)q * H + col)
+                                          : make_uint4(0, 0, 0, 0);
         }
       }
 #pragma unroll
-      for (int u = 0; u < CH; ++u) {
-        const int c = base + (u * 32 + lane) * V::N;
-        if (c < H) V::store(out + (size_t)t * H + c, acc[u]);
+      for (int b = 0; b < JB; ++b) {
+        if (!ok[b]) continue;
+#pragma unroll
+        for (int c = 0; c < CH; ++c) {
+          float v[V::N];
+          V::unpack(raw[b][c], v);
+#pragma unroll
+          for (int i = 0; i < V::N; ++i) acc[c][i] = fmaf(wj[b], v[i], acc[c][i]);
+        }
       }
+    }
+    for (int j = 32; j < k_max; ++j) {  // budgets above 32 experts: read the slot directly
+      const int q = q_row[j];
+      if (q < 0) continue;
+      if (q >= P) { flag(SEMMOE_DEVERR_PAIRS); continue; }
+      const float w = w_row[j];
+#pragma unroll
+      for (int c = 0; c < CH; ++c) {
+        const int col = base + (c * 32 + lane) * V::N;
+        if (col < H) {
+          float v[V::N];
+          V::load(y_perm + (size_t)q * H + col, v);
+#pragma unroll
+          for (int i = 0; i < V::N; ++i) acc[c][i] = fmaf(w, v[i], acc[c][i]);
+        }
+      }
+    }
+#pragma unroll
+    for (int c = 0; c < CH; ++c) {
+      const int col = base + (c * 32 + lane) * V::N;
+      if (col < H) V::store(out + (size_t)t * H + col, acc[c]);
     }
   }
 }
@@ -133,17 +151,20 @@ cudaError_t launch_combine(const void* y_perm, const int32_t* pair_to_sorted, co
                            const void* y_shared, int dtype, int T, int H, int k_max, int P, void* out,
                            cudaStream_t s) {
   if (T == 0) return cudaSuccess;
-  int blocks = (T + kWarps - 1) / kWarps;
-  const int cap = sm_count() * 16;
+  constexpr int kCH = 2, kJB = 4;
+  const int vec = dtype == SEMMOE_BF16 ? 8 : 4;
+  const long long units = (long long)T * ((H + 32 * vec * kCH - 1) / (32 * vec * kCH));
+  long long blocks = (units + kWarps - 1) / kWarps;
+  const long long cap = 8LL * sm_count();
   if (blocks > cap) blocks = cap;
   if (dtype == SEMMOE_BF16)
-    combine_kernel<__nv_bfloat16, 4><<<blocks, kThreads, 0, s>>>(
+    combine_kernel<__nv_bfloat16, kCH, kJB><<<(int)blocks, kThreads, 0, s>>>(
         static_cast<const __nv_bfloat16*>(y_perm), pair_to_sorted, topk_w,
         static_cast<const __nv_bfloat16*>(y_shared), T, H, k_max, P, static_cast<__nv_bfloat16*>(out));
   else
-    combine_kernel<float, 2><<<blocks, kThreads, 0, s>>>(static_cast<const float*>(y_perm), pair_to_sorted, topk_w,
-                                                      static_cast<const float*>(y_shared), T, H, k_max, P,
-                                                      static_cast<float*>(out));
+    combine_kernel<float, kCH, kJB><<<(int)blocks, kThreads, 0, s>>>(
+        static_cast<const float*>(y_perm), pair_to_sorted, topk_w, static_cast<const float*>(y_shared), T, H,
+        k_max, P, static_cast<float*>(out));
   count_launches(1);
   return cudaGetLastError();
 }

@@ -56,7 +56,7 @@ inline int take_error_word(const Sym& sym, cudaStream_t s, int* bits) {
 // ---------------------------------------------------------------------------
 // host helpers
 // ---------------------------------------------------------------------------
-inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+__host__ __device__ inline constexpr size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
 // Raise `kernel`'s dynamic shared-memory limit to `bytes` once per device;
 // `done` is a per-call-site bit mask of devices already set.

@@ -107,25 +107,44 @@ perm_scatter_kernel(const int32_t* __restrict__ topk_idx, const int32_t* __restr
                     int32_t* __restrict__ sorted_to_pair, int32_t* __restrict__ pair_to_sorted) {
   __shared__ int rank_s[kMaxE], phys_s[kMaxE], run[kMaxE], total[kMaxE], scan[kThreads];
   __shared__ int wcnt[kWarps][kMaxE];
+  __shared__ int part_before[kThreads], part_tot[kThreads];
   physical_positions(expert_rank, E, R, rank_s, phys_s);
   const int tid = threadIdx.x;
-  if (tid < E) {
+  // G threads per bucket (G = kThreads / E) each sum every G-th chunk's count,
+  // eight loads in flight at a time; the G partial sums are added below.
+  const int G = kThreads / E;
+  if (tid < G * E) {
+    const int b = tid % E, g = tid / E;
     int before = 0, tot = 0;
-    constexpr int B = 8;  // chunks per batch: the batch's loads are all in flight together
-    for (int c0 = 0; c0 < nchunks; c0 += B) {
+    constexpr int B = 8;
+    for (int c0 = g; c0 < nchunks; c0 += B * G) {
       int v[B];
 #pragma unroll
-      for (int u = 0; u < B; ++u) v[u] = c0 + u < nchunks ? hist[(size_t)(c0 + u) * E + tid] : 0;
+      for (int u = 0; u < B; ++u) {
+        const int c = c0 + u * G;
+        v[u] = c < nchunks ? hist[(size_t)c * E + b] : 0;
+      }
 #pragma unroll
       for (int u = 0; u < B; ++u) {
-        before += c0 + u < (int)blockIdx.x ? v[u] : 0;
+        before += c0 + u * G < (int)blockIdx.x ? v[u] : 0;
         tot += v[u];
       }
+    }
+    part_before[tid] = before;
+    part_tot[tid] = tot;
+  }
+  __syncthreads();
+  if (tid < E) {
+    int before = 0, tot = 0;
+    for (int g = 0; g < G; ++g) {
+      before += part_before[g * E + tid];
+      tot += part_tot[g * E + tid];
     }
     total[tid] = tot;
     run[tid] = before;
     for (int w = 0; w < kWarps; ++w) wcnt[w][tid] = 0;
   }
+  __syncthreads();
   scan[tid] = tid < E ? total[tid] : 0;
   __syncthreads();
   for (int d = 1; d < kThreads; d <<= 1) {  // inclusive scan of the bucket totals

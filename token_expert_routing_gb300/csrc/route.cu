@@ -46,27 +46,46 @@ __device__ void warp_topk(const float* row, int ks, size_t slice_stride, float* 
                           const int32_t* __restrict__ k_per_token, int k_uniform, int k_max, float* my_v, int* my_e,
                           int32_t* __restrict__ topk_idx, float* __restrict__ topk_w) {
   const int lane = threadIdx.x % 32;
-  const int nper = NPER;
   int kt = k_per_token != nullptr ? k_per_token[t] : k_uniform;
   if (kt < 1 || kt > k_max) {
     if (lane == 0) flag(SEMMOE_DEVERR_K);
     kt = kt < 1 ? 1 : k_max;
   }
+  // Partial logits of the K slices, added in slice order; each batch of slices
+  // is loaded before any is added, so the loads are in flight together.
+  constexpr int SB = NPER <= 2 ? 8 : (NPER == 4 ? 4 : 2);
   float v[NPER];
 #pragma unroll
-  for (int i = 0; i < NPER; ++i) {
-    float val = -INFINITY;
-    const int e = lane + 32 * i;
-    if (e < E) {
-      val = row[e];
-      for (int k = 1; k < ks; ++k) val += row[(size_t)k * slice_stride + e];  // K slices in order
-      if (logits_out != nullptr) logits_out[e] = val;
-      if (!isfinite(val)) {
-        flag(SEMMOE_DEVERR_NONFINITE);
-        val = -INFINITY;
+  for (int i = 0; i < NPER; ++i) v[i] = 0.f;
+  for (int k0 = 0; k0 < ks; k0 += SB) {
+    float part[NPER][SB];
+#pragma unroll
+    for (int i = 0; i < NPER; ++i) {
+      const int e = lane + 32 * i;
+#pragma unroll
+      for (int u = 0; u < SB; ++u)
+        part[i][u] = (e < E && k0 + u < ks) ? row[(size_t)(k0 + u) * slice_stride + e] : 0.f;
+    }
+#pragma unroll
+    for (int i = 0; i < NPER; ++i) {
+#pragma unroll
+      for (int u = 0; u < SB; ++u) {
+        if (k0 + u < ks) v[i] = (k0 + u == 0) ? part[i][u] : v[i] + part[i][u];
       }
     }
-    v[i] = val;
+  }
+#pragma unroll
+  for (int i = 0; i < NPER; ++i) {
+    const int e = lane + 32 * i;
+    if (e < E) {
+      if (logits_out != nullptr) logits_out[e] = v[i];
+      if (!isfinite(v[i])) {
+        flag(SEMMOE_DEVERR_NONFINITE);
+        v[i] = -INFINITY;
+      }
+    } else {
+      v[i] = -INFINITY;
+    }
   }
   unsigned taken = 0;
   for (int j = 0; j < kt; ++j) {
@@ -228,73 +247,49 @@ __global__ void affinity_lookup_kernel(const int32_t* __restrict__ ids, const in
 
 constexpr int kMaxR = 64;
 
-__global__ void remote_count_kernel(const int32_t* __restrict__ topk_idx, const int32_t* __restrict__ pred,
-                                    const int32_t* __restrict__ expert_rank, int T, int k_max, int E,
-                                    int R, int32_t* __restrict__ counts) {
-  __shared__ int c[kMaxR * kMaxR];
-  for (int i = threadIdx.x; i < R * R; i += blockDim.x) c[i] = 0;
-  __syncthreads();
-  const long long n = (long long)T * k_max;
-  for (long long p = blockIdx.x * (long long)blockDim.x + threadIdx.x; p < n;
-       p += (long long)gridDim.x * blockDim.x) {
-    int e = topk_idx[p];
-    if (e < 0) continue;
-    if (e >= E) { flag(SEMMOE_DEVERR_EXPERT); continue; }
-    int src = pred[p / k_max];
-    int dst = expert_rank[e];
-    if (src < 0 || src >= R || dst < 0 || dst >= R) { flag(SEMMOE_DEVERR_LUT); continue; }
-    atomicAdd(&c[src * R + dst], 1);
-  }
-  __syncthreads();
-  for (int i = threadIdx.x; i < R * R; i += blockDim.x)
-    if (c[i]) atomicAdd(&counts[i], c[i]);
-}
-
-// One CTA does the whole count when the pair list is small enough: no memset,
-// no global atomics, and the per-source remote sums in the same launch.
-constexpr int kCountThreads = 1024;
-constexpr long long kOneBlockPairs = 1LL << 20;
+// Activations per (source rank, destination rank), one pair per thread per
+// pass: equal (src, dst) keys of a warp are merged with __match_any_sync before
+// the shared-memory add, and each CTA adds its non-zero counts -- and its
+// off-diagonal row sums, the remote activations -- to the zeroed outputs.
+constexpr int kCountThreads = 256;
 
 __global__ void __launch_bounds__(kCountThreads)
-remote_count_one_block_kernel(const int32_t* __restrict__ topk_idx, const int32_t* __restrict__ pred,
-                              const int32_t* __restrict__ expert_rank, int T, int k_max, int E, int R,
-                              int32_t* __restrict__ counts, int32_t* __restrict__ remote) {
+remote_count_kernel(const int32_t* __restrict__ topk_idx, const int32_t* __restrict__ pred,
+                    const int32_t* __restrict__ expert_rank, int T, int k_max, int E, int R,
+                    int32_t* __restrict__ counts, int32_t* __restrict__ remote) {
   __shared__ int c[kMaxR * kMaxR];
   __shared__ int rank_s[kRouteMaxE];
   for (int i = threadIdx.x; i < R * R; i += kCountThreads) c[i] = 0;
   for (int e = threadIdx.x; e < E; e += kCountThreads) rank_s[e] = expert_rank[e];
   __syncthreads();
-  // One token per thread per pass; its source rank and all its slots are
-  // loaded before any is used, so the loads of a pass overlap.
-  for (int t = threadIdx.x; t < T; t += kCountThreads) {
-    const int src = pred[t];
-    const int32_t* slots = topk_idx + (size_t)t * k_max;
-    for (int j = 0; j < k_max; ++j) {
-      const int e = slots[j];
-      if (e < 0) continue;
-      if (e >= E) { flag(SEMMOE_DEVERR_EXPERT); continue; }
-      const int dst = rank_s[e];
-      if (src < 0 || src >= R || dst < 0 || dst >= R) { flag(SEMMOE_DEVERR_LUT); continue; }
-      atomicAdd(&c[src * R + dst], 1);
+  const long long n = (long long)T * k_max;
+  const long long stride = (long long)gridDim.x * kCountThreads;
+  const long long first = (long long)blockIdx.x * kCountThreads;
+  for (long long p0 = first; p0 < n; p0 += stride) {  // uniform trip count within a warp
+    const long long p = p0 + threadIdx.x;
+    int key = -1;
+    if (p < n) {
+      const int e = topk_idx[p];
+      if (e >= E) {
+        flag(SEMMOE_DEVERR_EXPERT);
+      } else if (e >= 0) {
+        const int src = pred[p / k_max];
+        const int dst = rank_s[e];
+        if (src < 0 || src >= R || dst < 0 || dst >= R) flag(SEMMOE_DEVERR_LUT);
+        else key = src * R + dst;
+      }
     }
+    const unsigned peers = __match_any_sync(0xffffffffu, key);
+    if (key >= 0 && (peers & lanemask_lt()) == 0) atomicAdd(&c[key], __popc(peers));
   }
   __syncthreads();
-  for (int i = threadIdx.x; i < R * R; i += kCountThreads) counts[i] = c[i];
+  for (int i = threadIdx.x; i < R * R; i += kCountThreads)
+    if (c[i]) atomicAdd(&counts[i], c[i]);
   if (threadIdx.x < R) {
     int sum = 0;
     for (int d = 0; d < R; ++d) sum += d != (int)threadIdx.x ? c[threadIdx.x * R + d] : 0;
-    remote[threadIdx.x] = sum;
+    if (sum) atomicAdd(&remote[threadIdx.x], sum);
   }
-}
-
-__global__ void remote_finalize_kernel(const int32_t* __restrict__ counts, int R,
-                                       int32_t* __restrict__ remote) {
-  int src = threadIdx.x;
-  if (src >= R) return;
-  int s = 0;
-  for (int d = 0; d < R; ++d)
-    if (d != src) s += counts[src * R + d];
-  remote[src] = s;
 }
 
 template <typename TX, typename TW>
@@ -393,22 +388,16 @@ cudaError_t launch_affinity_lookup(const int32_t* ids, const int32_t* lut, int V
 
 cudaError_t launch_remote_count(const int32_t* topk_idx, const int32_t* pred, const int32_t* expert_rank, int T,
                                 int k_max, int E, int R, int32_t* counts, int32_t* remote, cudaStream_t s) {
-  long long n = (long long)T * k_max;
-  if (n <= kOneBlockPairs) {
-    remote_count_one_block_kernel<<<1, kCountThreads, 0, s>>>(topk_idx, pred, expert_rank, T, k_max, E, R, counts,
-                                                              remote);
-    count_launches(1);
-    return cudaGetLastError();
-  }
   cudaError_t e = cudaMemsetAsync(counts, 0, sizeof(int32_t) * R * R, s);
+  if (e == cudaSuccess) e = cudaMemsetAsync(remote, 0, sizeof(int32_t) * R, s);
   if (e != cudaSuccess) return e;
-  long long blocks = (n + 1023) / 1024;
-  if (blocks > 1024) blocks = 1024;
-  remote_count_kernel<<<(int)blocks, 256, 0, s>>>(topk_idx, pred, expert_rank, T, k_max, E, R, counts);
-  count_launches(1);
-  e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
-  remote_finalize_kernel<<<1, kMaxR, 0, s>>>(counts, R, remote);
+  const long long n = (long long)T * k_max;
+  if (n == 0) return cudaSuccess;
+  long long blocks = (n + kCountThreads - 1) / kCountThreads;
+  const long long cap = 4LL * sm_count();
+  if (blocks > cap) blocks = cap;
+  remote_count_kernel<<<(int)blocks, kCountThreads, 0, s>>>(topk_idx, pred, expert_rank, T, k_max, E, R, counts,
+                                                            remote);
   count_launches(1);
   return cudaGetLastError();
 }

@@ -31,7 +31,6 @@ __device__ int g_err;
 constexpr int BM = 128, BK = 64, UK = 16, THREADS = 192;
 constexpr int MAX_STAGES = 8;
 constexpr int A_BYTES = BM * BK * 2;            // 16 KB
-constexpr int MAX_NB = 256;                     // MMA N limit
 constexpr size_t kStageBudget = 200 * 1024;     // operand ring
 constexpr uint32_t TMEM_COLS = 256;
 constexpr int kMaxKSlices = 8;
