@@ -270,6 +270,21 @@ def _time_around_layer(args, spec, d, layer, dev, stream):
                               4 * T * k_max + (4 * T if kpt is not None else 0) + 4 * E * R + 4 * T,
                               f"E={E} R={R} k_max={k_max}"),
     }
+    if d.get("sub_logw") is not None:   # MoE-Prism layer: the hierarchical gate over the same tokens
+        Ep = d["w_router_parent"].shape[0]
+        wp = d["w_router_parent"].to(dev)
+        slw = d["sub_logw"].to(dev)
+        hidx = torch.empty(T, k_max, **i32)
+        hw = torch.empty(T, k_max, dtype=torch.float32, device=dev)
+        hws = torch.empty(max(_abi.semmoe_route_hier_workspace_size(T, spec.H, Ep, _abi.dtype_code(d["x"]),
+                                                                     _abi.dtype_code(wp)), 256),
+                          dtype=torch.uint8, device=dev)
+        xd = d["x"].to(dev)
+        calls["route_hier"] = (
+            lambda: _abi.semmoe_route_hier(xd, wp, None, None, slw, E // Ep, kpt, 0 if kpt is not None else spec.k,
+                                           T, spec.H, Ep, k_max, hidx, hw, hws),
+            T * spec.H * 2 + Ep * spec.H * (2 if spec.router_dtype == "bf16" else 4) + 4 * E + T * k_max * 8,
+            f"Ep={Ep} N={E // Ep} k_max={k_max} (parent router GEMM + hierarchical top-k)")
     out = {}
     n_it = max(args.steps, 20)
     for name, (fn, nbytes, what) in calls.items():

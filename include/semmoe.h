@@ -10,6 +10,7 @@
  * One forward is six steps, each one call below, all asynchronous on one
  * CUDA stream:
  *   semmoe_route            router GEMM, fp32 softmax, per-token top-k
+ *   semmoe_route_hier       the same over sub-experts, by hierarchical gating
  *   semmoe_affinity_lookup  token id -> predicted logical rank
  *   semmoe_remote_count     activations per (source rank, destination rank)
  *   semmoe_permute          stable sort of (token, expert) pairs by
@@ -133,6 +134,37 @@ int semmoe_route(const void* x, int x_dtype, const void* w_router, int w_dtype,
                  const int32_t* k_per_token, int k_uniform,
                  int T, int H, int E, int k_max,
                  int32_t* topk_idx, float* topk_w, void* ws, size_t ws_bytes, void* stream);
+
+/*
+ * semmoe_route_hier -- MoE-Prism's training-free hierarchical gating over
+ * sub-experts ([MP] §2 A: each of Ep parent experts is split into N
+ * sub-experts, disjoint sets of its intermediate neurons; the routing is
+ * rebuilt without training from co-activation statistics).
+ *
+ * The parent router gives l[t,e] = x[t] . Wp[e] (fp32, as semmoe_route).
+ * Sub-expert s = e*N + i scores  score[t,s] = l[t,e] + sub_logw[s]  (fp32 add;
+ * sub_logw = log of the sub-expert's profiled co-activation weight, so the
+ * order is that of p_e * a[e,i]).  The k_t best scores are taken, ties to the
+ * lower s, slot j holding the j-th; the gate of a taken sub-expert of parent e
+ * is p_e renormalised over the distinct parents taken:
+ *   w = exp(l_e - m) / sum_{e' in parents taken} exp(l_e' - m),  m = their max logit.
+ * A parent's sub-experts all carry its gate (their outputs add up to the
+ * parent's output), so taking every sub-expert of the top-m parents gives
+ * back the parent router's renormalised top-m.
+ *
+ * x, x_dtype, w_parent [Ep,H], w_dtype, logits_in / logits_out [T,Ep],
+ * k_per_token / k_uniform, T, H: as semmoe_route with E = Ep.
+ * sub_logw  [device] [Ep*N] fp32, finite
+ * topk_idx  [device] [T,k_max] int32 out: sub-expert ids (-1 = padding)
+ * topk_w    [device] [T,k_max] fp32 out (0 = padding)
+ * ws        [device] workspace of semmoe_route_hier_workspace_size() bytes
+ * Limits: 1 <= N, 1 <= Ep*N <= 256, 1 <= k_max <= Ep*N.
+ */
+size_t semmoe_route_hier_workspace_size(int T, int H, int Ep, int x_dtype, int w_dtype);
+int semmoe_route_hier(const void* x, int x_dtype, const void* w_parent, int w_dtype, const float* logits_in,
+                      float* logits_out, const float* sub_logw, int N, const int32_t* k_per_token, int k_uniform,
+                      int T, int H, int Ep, int k_max, int32_t* topk_idx, float* topk_w, void* ws,
+                      size_t ws_bytes, void* stream);
 
 /*
  * semmoe_affinity_lookup -- predicted logical rank of each token from its id.

@@ -35,6 +35,9 @@ SIGNATURES = {
     "semmoe_check_errors": (_i, [_vp, ctypes.POINTER(_i)]),
     "semmoe_route_workspace_size": (_sz, [_i, _i, _i, _i, _i]),
     "semmoe_route": (_i, [_vp, _i, _vp, _i, _vp, _vp, _vp, _i, _i, _i, _i, _i, _vp, _vp, _vp, _sz, _vp]),
+    "semmoe_route_hier_workspace_size": (_sz, [_i, _i, _i, _i, _i]),
+    "semmoe_route_hier": (_i, [_vp, _i, _vp, _i, _vp, _vp, _vp, _i, _vp, _i, _i, _i, _i, _i, _vp, _vp, _vp, _sz,
+                               _vp]),
     "semmoe_affinity_lookup": (_i, [_vp, _vp, _i, _i, _i, _vp, _vp]),
     "semmoe_remote_count": (_i, [_vp, _vp, _vp, _i, _i, _i, _i, _vp, _vp, _vp]),
     "semmoe_permute_workspace_size": (_sz, [_i, _i, _i]),
@@ -147,6 +150,24 @@ def semmoe_route(x, w_router, logits_in, logits_out, k_per_token, k_uniform, T, 
     _check(lib().semmoe_route(_p(x), xd, _p(w_router), wd, _p(logits_in), _p(logits_out),
                               _p(k_per_token), k_uniform, T, H, E, k_max, _p(topk_idx), _p(topk_w),
                               _p(ws), ws.numel() * ws.element_size(), _stream(stream)))
+
+
+def semmoe_route_hier_workspace_size(T, H, Ep, x_dtype: int, w_dtype: int) -> int:
+    return lib().semmoe_route_hier_workspace_size(T, H, Ep, x_dtype, w_dtype)
+
+
+def semmoe_route_hier(x, w_parent, logits_in, logits_out, sub_logw, N, k_per_token, k_uniform, T, H, Ep, k_max,
+                      topk_idx, topk_w, ws=None, stream=None):
+    """Hierarchical sub-expert routing.  ``ws`` defaults to a fresh workspace
+    of the size the library asks for."""
+    xd = dtype_code(x) if x is not None else SEMMOE_F32
+    wd = dtype_code(w_parent) if w_parent is not None else SEMMOE_F32
+    if ws is None:
+        n = semmoe_route_hier_workspace_size(T, max(H, 1), Ep, xd, wd)
+        ws = torch.empty(n, dtype=torch.uint8, device=topk_idx.device)
+    _check(lib().semmoe_route_hier(_p(x), xd, _p(w_parent), wd, _p(logits_in), _p(logits_out), _p(sub_logw), N,
+                                   _p(k_per_token), k_uniform, T, H, Ep, k_max, _p(topk_idx), _p(topk_w),
+                                   _p(ws), ws.numel() * ws.element_size(), _stream(stream)))
 
 
 def semmoe_affinity_lookup(token_ids, lut, V, R, T, pred_rank, stream=None):

@@ -121,6 +121,47 @@ int semmoe_route(const void* x, int x_dtype, const void* w_router, int w_dtype, 
                      "semmoe_route");
 }
 
+size_t semmoe_route_hier_workspace_size(int T, int H, int Ep, int x_dtype, int w_dtype) {
+  if (T < 0 || H < 1 || Ep < 1 || !valid_dtype(x_dtype) || !valid_dtype(w_dtype)) return 0;
+  const size_t b = route_hier_ws_bytes(T, H, Ep, x_dtype, w_dtype);
+  return b > 0 ? b : 256;
+}
+
+int semmoe_route_hier(const void* x, int x_dtype, const void* w_parent, int w_dtype, const float* logits_in,
+                      float* logits_out, const float* sub_logw, int N, const int32_t* k_per_token, int k_uniform,
+                      int T, int H, int Ep, int k_max, int32_t* topk_idx, float* topk_w, void* ws, size_t ws_bytes,
+                      void* stream) {
+  REQUIRE(T >= 0, "semmoe_route_hier: T = %d < 0", T);
+  REQUIRE(N >= 1 && Ep >= 1 && (long long)Ep * N <= 256, "semmoe_route_hier: Ep * N = %lld outside [1, 256]",
+          (long long)Ep * N);
+  const int E = Ep * N;
+  REQUIRE(k_max >= 1 && k_max <= E, "semmoe_route_hier: k_max = %d outside [1, Ep*N = %d]", k_max, E);
+  REQUIRE((long long)T * E < (1LL << 31), "semmoe_route_hier: T * Ep * N too large");
+  REQUIRE(k_per_token != nullptr || (k_uniform >= 1 && k_uniform <= k_max),
+          "semmoe_route_hier: k_uniform = %d outside [1, k_max = %d]", k_uniform, k_max);
+  if (T == 0) return SEMMOE_OK;
+  REQUIRE(topk_idx != nullptr && topk_w != nullptr && sub_logw != nullptr, "semmoe_route_hier: null pointer");
+  if (logits_in == nullptr) {
+    REQUIRE(x != nullptr && w_parent != nullptr, "semmoe_route_hier: null x or w_parent without logits_in");
+    REQUIRE(valid_dtype(x_dtype) && valid_dtype(w_dtype), "semmoe_route_hier: bad dtype (%d, %d)", x_dtype, w_dtype);
+    REQUIRE(H >= 1, "semmoe_route_hier: H = %d < 1", H);
+    REQUIRE(aligned(x, 16) && aligned(w_parent, 16), "semmoe_route_hier: x and w_parent must be 16-byte aligned");
+    const size_t need = route_hier_ws_bytes(T, H, Ep, x_dtype, w_dtype);
+    REQUIRE(need == 0 || (ws != nullptr && aligned(ws, 256) && ws_bytes >= need),
+            "semmoe_route_hier: workspace null, not 256-byte aligned or below %zu bytes", need);
+  } else {
+    REQUIRE(aligned(logits_in, 4), "semmoe_route_hier: misaligned logits_in");
+  }
+  REQUIRE(aligned(topk_idx, 4) && aligned(topk_w, 4) && aligned(logits_out, 4) && aligned(k_per_token, 4) &&
+              aligned(sub_logw, 4),
+          "semmoe_route_hier: misaligned pointer");
+  CHECK_DEVICE("semmoe_route_hier");
+  return cuda_status(launch_route_hier(x, x_dtype, w_parent, w_dtype, logits_in, logits_out, sub_logw, N,
+                                       k_per_token, k_uniform, T, H, Ep, k_max, topk_idx, topk_w, ws,
+                                       static_cast<cudaStream_t>(stream)),
+                     "semmoe_route_hier");
+}
+
 int semmoe_affinity_lookup(const int32_t* token_ids, const int32_t* lut, int V, int R, int T, int32_t* pred_rank,
                            void* stream) {
   REQUIRE(T >= 0 && V >= 1 && R >= 1, "semmoe_affinity_lookup: bad sizes T=%d V=%d R=%d", T, V, R);

@@ -29,6 +29,13 @@ cudaError_t launch_route(const void* x, int x_dtype, const void* w, int w_dtype,
                          int k_uniform, int T, int H, int E, int k_max, int32_t* topk_idx,
                          float* topk_w, void* ws, cudaStream_t s);
 
+// MoE-Prism hierarchical gating over Ep parents x N sub-experts.
+size_t route_hier_ws_bytes(int T, int H, int Ep, int x_dtype, int w_dtype);
+cudaError_t launch_route_hier(const void* x, int x_dtype, const void* w, int w_dtype, const float* logits_in,
+                              float* logits_out, const float* sub_logw, int N, const int32_t* kpt, int k_uniform,
+                              int T, int H, int Ep, int k_max, int32_t* topk_idx, float* topk_w, void* ws,
+                              cudaStream_t s);
+
 cudaError_t launch_affinity_lookup(const int32_t* token_ids, const int32_t* lut, int V, int R,
                                    int T, int32_t* pred, cudaStream_t s);
 

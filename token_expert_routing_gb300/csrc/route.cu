@@ -35,26 +35,27 @@ __host__ __device__ inline size_t route_smem_bytes(int E, int k_max) {
          (size_t)kWarps * k_max * (sizeof(float) + sizeof(int));
 }
 
-// One warp selects token t's experts from its E logits (shared or global
-// memory; the sum of `ks` partial rows slice_stride floats apart, added in
-// slice order, copied to logits_out when that is set): k_t rounds of a warp argmax over (logit descending, expert index
-// ascending), skipping experts already taken; then the gates, the softmax of
-// the selected logits renormalised over the selection (fp32).  my_v / my_e:
-// k_max floats / ints of scratch for this warp.
-template <int NPER>  // logits held per lane: E <= 32 * NPER
-__device__ void warp_topk(const float* row, int ks, size_t slice_stride, float* logits_out, int E, int t,
-                          const int32_t* __restrict__ k_per_token, int k_uniform, int k_max, float* my_v, int* my_e,
-                          int32_t* __restrict__ topk_idx, float* __restrict__ topk_w) {
-  const int lane = threadIdx.x % 32;
+// Token t's budget k_t, clamped into [1, k_max] (and flagged) when out of range.
+__device__ __forceinline__ int warp_budget(const int32_t* __restrict__ k_per_token, int k_uniform, int k_max,
+                                           int t) {
   int kt = k_per_token != nullptr ? k_per_token[t] : k_uniform;
   if (kt < 1 || kt > k_max) {
-    if (lane == 0) flag(SEMMOE_DEVERR_K);
+    if ((threadIdx.x & 31) == 0) flag(SEMMOE_DEVERR_K);
     kt = kt < 1 ? 1 : k_max;
   }
-  // Partial logits of the K slices, added in slice order; each batch of slices
-  // is loaded before any is added, so the loads are in flight together.
+  return kt;
+}
+
+// One warp loads a token's E logits into v (lane holds e = lane + 32 i): the
+// sum of `ks` partial rows slice_stride floats apart, added in slice order
+// (each batch of slices loaded before any is added, so the loads are in flight
+// together), copied to logits_out when that is set.  Entries past E and
+// non-finite logits (flagged) become -inf.
+template <int NPER>
+__device__ __forceinline__ void warp_load_logits(const float* row, int ks, size_t slice_stride, float* logits_out,
+                                                 int E, float (&v)[NPER]) {
+  const int lane = threadIdx.x % 32;
   constexpr int SB = NPER <= 2 ? 8 : (NPER == 4 ? 4 : 2);
-  float v[NPER];
 #pragma unroll
   for (int i = 0; i < NPER; ++i) v[i] = 0.f;
   for (int k0 = 0; k0 < ks; k0 += SB) {
@@ -87,6 +88,14 @@ __device__ void warp_topk(const float* row, int ks, size_t slice_stride, float* 
       v[i] = -INFINITY;
     }
   }
+}
+
+// k_t rounds of a warp argmax over (score descending, index ascending) of the
+// n scores in v, skipping those already taken.  Lane 0 writes the j-th pick to
+// my_v[j] / my_e[j] (-1 when fewer than k_t scores are finite, flagged).
+template <int NPER>
+__device__ __forceinline__ void warp_select(const float (&v)[NPER], int n, int kt, float* my_v, int* my_e) {
+  const int lane = threadIdx.x % 32;
   unsigned taken = 0;
   for (int j = 0; j < kt; ++j) {
     float bv = -INFINITY;
@@ -94,7 +103,7 @@ __device__ void warp_topk(const float* row, int ks, size_t slice_stride, float* 
 #pragma unroll
     for (int i = 0; i < NPER; ++i) {
       const int e = lane + 32 * i;
-      if (e < E && !((taken >> i) & 1u)) {
+      if (e < n && !((taken >> i) & 1u)) {
         if (v[i] > bv || (v[i] == bv && e < be)) { bv = v[i]; be = e; }
       }
     }
@@ -104,7 +113,7 @@ __device__ void warp_topk(const float* row, int ks, size_t slice_stride, float* 
       const int oe = __shfl_xor_sync(0xffffffffu, be, off);
       if (ov > bv || (ov == bv && oe < be)) { bv = ov; be = oe; }
     }
-    if (be >= E) {  // fewer than kt finite logits
+    if (be >= n) {  // fewer than kt finite scores
       if (lane == 0) flag(SEMMOE_DEVERR_NONFINITE);
       be = -1;
     } else if ((be & 31) == lane) {
@@ -113,6 +122,21 @@ __device__ void warp_topk(const float* row, int ks, size_t slice_stride, float* 
     if (lane == 0) { my_v[j] = bv; my_e[j] = be; }
   }
   __syncwarp();
+}
+
+// One warp routes token t: its logits (see warp_load_logits), k_t picks (see
+// warp_select), then the gates, the softmax of the selected logits
+// renormalised over the selection (fp32).  my_v / my_e: k_max floats / ints of
+// scratch for this warp.
+template <int NPER>  // logits held per lane: E <= 32 * NPER
+__device__ void warp_topk(const float* row, int ks, size_t slice_stride, float* logits_out, int E, int t,
+                          const int32_t* __restrict__ k_per_token, int k_uniform, int k_max, float* my_v, int* my_e,
+                          int32_t* __restrict__ topk_idx, float* __restrict__ topk_w) {
+  const int lane = threadIdx.x % 32;
+  const int kt = warp_budget(k_per_token, k_uniform, k_max, t);
+  float v[NPER];
+  warp_load_logits<NPER>(row, ks, slice_stride, logits_out, E, v);
+  warp_select<NPER>(v, E, kt, my_v, my_e);
   const float m = my_v[0];
   float den = 0.f;
   for (int j = lane; j < kt; j += 32) den += my_e[j] >= 0 ? expf(my_v[j] - m) : 0.f;
@@ -227,6 +251,75 @@ topk_kernel(const float* __restrict__ logits, int ks, float* __restrict__ logits
             E, t, k_per_token, k_uniform, k_max, sel_v + warp * k_max, sel_e + warp * k_max, topk_idx, topk_w);
 }
 
+// MoE-Prism's training-free hierarchical gating, one warp per token: the
+// parent logits (summed over K slices) go to shared memory; sub-expert s of
+// parent s / N scores l[s / N] + sub_logw[s] (fp32); the k_t best scores are
+// picked as in warp_select; each pick carries its parent's softmax weight
+// renormalised over the distinct parents picked.
+template <int NPER>  // sub-experts (and parents) held per lane: Ep * N <= 32 * NPER
+__global__ void __launch_bounds__(kTopkWarps * 32)
+hier_topk_kernel(const float* __restrict__ logits, int ks, float* __restrict__ logits_out,
+                 const float* __restrict__ sub_logw, int N, const int32_t* __restrict__ k_per_token, int k_uniform,
+                 int T, int Ep, int k_max, int32_t* __restrict__ topk_idx, float* __restrict__ topk_w) {
+  extern __shared__ __align__(16) unsigned char smem_raw[];
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  float* base = reinterpret_cast<float*>(smem_raw);
+  float* lg = base + warp * Ep;
+  float* sel_v = base + kTopkWarps * Ep + warp * k_max;
+  int* sel_e = reinterpret_cast<int*>(base + kTopkWarps * (Ep + k_max)) + warp * k_max;
+  const int t = blockIdx.x * kTopkWarps + warp;
+  if (t >= T) return;
+  const int E = Ep * N;
+  const int kt = warp_budget(k_per_token, k_uniform, k_max, t);
+  {
+    float v[NPER];
+    warp_load_logits<NPER>(logits + (size_t)t * Ep, ks, (size_t)T * Ep,
+                           logits_out != nullptr ? logits_out + (size_t)t * Ep : nullptr, Ep, v);
+#pragma unroll
+    for (int i = 0; i < NPER; ++i)
+      if (lane + 32 * i < Ep) lg[lane + 32 * i] = v[i];
+  }
+  __syncwarp();
+  float sc[NPER];
+#pragma unroll
+  for (int i = 0; i < NPER; ++i) {
+    const int sx = lane + 32 * i;
+    sc[i] = -INFINITY;
+    if (sx < E) {
+      const float v = __fadd_rn(lg[sx / N], sub_logw[sx]);
+      if (isfinite(v)) sc[i] = v;
+      else flag(SEMMOE_DEVERR_NONFINITE);
+    }
+  }
+  warp_select<NPER>(sc, E, kt, sel_v, sel_e);
+  float m = -INFINITY;
+  for (int j = lane; j < kt; j += 32)
+    if (sel_e[j] >= 0) m = fmaxf(m, lg[sel_e[j] / N]);
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
+  float den = 0.f;
+  for (int j = lane; j < kt; j += 32) {
+    const int sx = sel_e[j];
+    if (sx < 0) continue;
+    const int pe = sx / N;
+    bool first = true;  // the parent's first pick counts once in the denominator
+    for (int i = 0; i < j && first; ++i) first = !(sel_e[i] >= 0 && sel_e[i] / N == pe);
+    if (first) den += expf(lg[pe] - m);
+  }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) den += __shfl_xor_sync(0xffffffffu, den, off);
+  for (int j = lane; j < k_max; j += 32) {
+    int sx = -1;
+    float g = 0.f;
+    if (j < kt && sel_e[j] >= 0) {
+      sx = sel_e[j];
+      g = expf(lg[sx / N] - m) / den;
+    }
+    topk_idx[(size_t)t * k_max + j] = sx;
+    topk_w[(size_t)t * k_max + j] = g;
+  }
+}
+
 __global__ void affinity_lookup_kernel(const int32_t* __restrict__ ids, const int32_t* __restrict__ lut,
                                        int V, int R, int T, int32_t* __restrict__ pred) {
   for (int t = blockIdx.x * blockDim.x + threadIdx.x; t < T; t += gridDim.x * blockDim.x) {
@@ -331,21 +424,30 @@ size_t route_ws_bytes(int T, int H, int E, int x_dtype, int w_dtype) {
   return route_partials_bytes(T, H, E, w_dtype) + route_tc_split_bytes(H, E, w_dtype);
 }
 
+// Tensor-core logits into the workspace: fp32 partial sums over *ks K slices,
+// laid out [ks][T][E].
+static cudaError_t route_partials_tc(const void* x, const void* w, int w_dtype, int T, int H, int E, void* ws,
+                                     const float** partials, int* ks, cudaStream_t s) {
+  unsigned char* w8 = static_cast<unsigned char*>(ws);
+  float* p = reinterpret_cast<float*>(w8);
+  void* split = w8 + route_partials_bytes(T, H, E, w_dtype);
+  int k = route_tc_k_slices(T, H, E, w_dtype);
+  cudaError_t e = launch_route_logits_tc(x, w, w_dtype, T, H, E, p, k, split, s);
+  if (e != cudaSuccess) return e;
+  const int kb_all = (H + 63) / 64, per = (kb_all + k - 1) / k;
+  *ks = (kb_all + per - 1) / per;  // the slices the launcher actually used
+  *partials = p;
+  return cudaSuccess;
+}
+
 cudaError_t launch_route(const void* x, int x_dtype, const void* w, int w_dtype, const float* logits_in,
                          float* logits_out, const int32_t* kpt, int k_uniform, int T, int H, int E, int k_max,
                          int32_t* topk_idx, float* topk_w, void* ws, cudaStream_t s) {
   if (T == 0) return cudaSuccess;
   int ks = 1;
   if (logits_in == nullptr && route_on_tensor_cores(x_dtype, H)) {
-    unsigned char* w8 = static_cast<unsigned char*>(ws);
-    float* partials = reinterpret_cast<float*>(w8);
-    void* split = w8 + route_partials_bytes(T, H, E, w_dtype);
-    ks = route_tc_k_slices(T, H, E, w_dtype);
-    cudaError_t e = launch_route_logits_tc(x, w, w_dtype, T, H, E, partials, ks, split, s);
+    cudaError_t e = route_partials_tc(x, w, w_dtype, T, H, E, ws, &logits_in, &ks, s);
     if (e != cudaSuccess) return e;
-    const int kb_all = (H + 63) / 64, per = (kb_all + ks - 1) / ks;
-    ks = (kb_all + per - 1) / per;  // the slices the launcher actually used
-    logits_in = partials;
   } else if (logits_in != nullptr && logits_out == logits_in) {
     logits_out = nullptr;
   }
@@ -374,6 +476,63 @@ cudaError_t launch_route(const void* x, int x_dtype, const void* w, int w_dtype,
                                         topk_w, s);
   return launch_route_t<float, __nv_bfloat16>(x, w, nullptr, logits_out, kpt, k_uniform, T, H, E, k_max,
                                               topk_idx, topk_w, s);
+}
+
+size_t route_hier_ws_bytes(int T, int H, int Ep, int x_dtype, int w_dtype) {
+  if (route_on_tensor_cores(x_dtype, H)) return route_ws_bytes(T, H, Ep, x_dtype, w_dtype);
+  // CUDA-core logits [T][Ep] plus the (unused) one-expert picks of that kernel
+  const size_t t = T > 0 ? T : 1;
+  return align_up(t * Ep * sizeof(float), 256) + 2 * align_up(t * sizeof(float), 256);
+}
+
+cudaError_t launch_route_hier(const void* x, int x_dtype, const void* w, int w_dtype, const float* logits_in,
+                              float* logits_out, const float* sub_logw, int N, const int32_t* kpt, int k_uniform,
+                              int T, int H, int Ep, int k_max, int32_t* topk_idx, float* topk_w, void* ws,
+                              cudaStream_t s) {
+  if (T == 0) return cudaSuccess;
+  int ks = 1;
+  if (logits_in == nullptr) {
+    if (route_on_tensor_cores(x_dtype, H)) {
+      cudaError_t e = route_partials_tc(x, w, w_dtype, T, H, Ep, ws, &logits_in, &ks, s);
+      if (e != cudaSuccess) return e;
+    } else {
+      unsigned char* w8 = static_cast<unsigned char*>(ws);
+      float* lg = reinterpret_cast<float*>(w8);
+      unsigned char* rest = w8 + align_up((size_t)T * Ep * sizeof(float), 256);
+      int32_t* idx1 = reinterpret_cast<int32_t*>(rest);
+      float* w1 = reinterpret_cast<float*>(rest + align_up((size_t)T * sizeof(float), 256));
+      cudaError_t e;
+      if (x_dtype == SEMMOE_BF16 && w_dtype == SEMMOE_F32)
+        e = launch_route_t<__nv_bfloat16, float>(x, w, nullptr, lg, nullptr, 1, T, H, Ep, 1, idx1, w1, s);
+      else if (x_dtype == SEMMOE_BF16)
+        e = launch_route_t<__nv_bfloat16, __nv_bfloat16>(x, w, nullptr, lg, nullptr, 1, T, H, Ep, 1, idx1, w1, s);
+      else if (w_dtype == SEMMOE_F32)
+        e = launch_route_t<float, float>(x, w, nullptr, lg, nullptr, 1, T, H, Ep, 1, idx1, w1, s);
+      else
+        e = launch_route_t<float, __nv_bfloat16>(x, w, nullptr, lg, nullptr, 1, T, H, Ep, 1, idx1, w1, s);
+      if (e != cudaSuccess) return e;
+      logits_in = lg;
+    }
+  } else if (logits_out == logits_in) {
+    logits_out = nullptr;
+  }
+  const int E = Ep * N;
+  const size_t sm = (size_t)kTopkWarps * (Ep + 2 * k_max) * sizeof(float);
+  const dim3 grid((T + kTopkWarps - 1) / kTopkWarps), block(kTopkWarps * 32);
+  if (E <= 32)
+    hier_topk_kernel<1><<<grid, block, sm, s>>>(logits_in, ks, logits_out, sub_logw, N, kpt, k_uniform, T, Ep,
+                                                k_max, topk_idx, topk_w);
+  else if (E <= 64)
+    hier_topk_kernel<2><<<grid, block, sm, s>>>(logits_in, ks, logits_out, sub_logw, N, kpt, k_uniform, T, Ep,
+                                                k_max, topk_idx, topk_w);
+  else if (E <= 128)
+    hier_topk_kernel<4><<<grid, block, sm, s>>>(logits_in, ks, logits_out, sub_logw, N, kpt, k_uniform, T, Ep,
+                                                k_max, topk_idx, topk_w);
+  else
+    hier_topk_kernel<8><<<grid, block, sm, s>>>(logits_in, ks, logits_out, sub_logw, N, kpt, k_uniform, T, Ep,
+                                                k_max, topk_idx, topk_w);
+  count_launches(1);
+  return cudaGetLastError();
 }
 
 cudaError_t launch_affinity_lookup(const int32_t* ids, const int32_t* lut, int V, int R, int T, int32_t* pred,

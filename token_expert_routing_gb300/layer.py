@@ -44,11 +44,13 @@ class MoELayer:
     w_router [E,H] (fp32 or bf16), w13 [E,2I,H], w2 [E,H,I] (activation type),
     expert_rank [E] and lut [V] int32, R logical ranks, k_max the largest budget;
     ws13 [2*I_s,H] / ws2 [H,I_s] optional shared experts; trans [E,R] fp32 an
-    optional expert -> next-layer-rank transition table.
+    optional expert -> next-layer-rank transition table.  With ``sub_logw``
+    [E] fp32 the layer routes by MoE-Prism's hierarchical gating: w_router is
+    then the parent router [Ep,H] and each parent owns N = E / Ep sub-experts.
     """
 
     def __init__(self, w_router, w13, w2, expert_rank, lut, R: int, k_max: int, ws13=None, ws2=None,
-                 trans=None, device="cuda"):
+                 trans=None, sub_logw=None, device="cuda"):
         dev = torch.device(device)
         c = lambda t: None if t is None else t.to(dev).contiguous()  # noqa: E731
         self.w_router, self.w13, self.w2 = c(w_router), c(w13), c(w2)
@@ -56,10 +58,14 @@ class MoELayer:
         self.lut = c(lut).to(torch.int32)
         self.ws13, self.ws2 = c(ws13), c(ws2)
         self.trans = None if trans is None else c(trans).to(torch.float32)
+        self.sub_logw = None if sub_logw is None else c(sub_logw).to(torch.float32)
         self.E, twoI, self.H = self.w13.shape
         self.I = twoI // 2
         self.I_s = 0 if ws13 is None else self.ws13.shape[0] // 2
         self.R, self.k_max, self.V = R, k_max, self.lut.shape[0]
+        self.Ep = self.w_router.shape[0]          # router rows: experts, or parents (hierarchical)
+        if self.sub_logw is not None and (self.E % self.Ep or self.sub_logw.numel() != self.E):
+            raise ValueError("hierarchical gating needs E = Ep * N and sub_logw of E values")
         self.dtype = self.w13.dtype
         self.device = dev
         self._ws = {}
@@ -103,13 +109,20 @@ class MoELayer:
         elif P is None:
             raise ValueError("k_per_token needs P = sum(k_per_token)")
         i32 = dict(dtype=torch.int32, device=dev)
-        logits = torch.empty(T, E, dtype=torch.float32, device=dev) if keep_logits else None
+        Ep = self.Ep
+        logits = torch.empty(T, Ep, dtype=torch.float32, device=dev) if keep_logits else None
         topk_idx = torch.empty(T, k_max, **i32)
         topk_w = torch.empty(T, k_max, dtype=torch.float32, device=dev)
-        ws = self._workspace("route", abi.semmoe_route_workspace_size(
-            T, H, E, abi.dtype_code(x), abi.dtype_code(self.w_router)))
-        abi.semmoe_route(x, self.w_router, logits_in, logits, k_per_token, k or 0, T, H, E, k_max,
-                         topk_idx, topk_w, ws, stream)
+        if self.sub_logw is None:
+            ws = self._workspace("route", abi.semmoe_route_workspace_size(
+                T, H, E, abi.dtype_code(x), abi.dtype_code(self.w_router)))
+            abi.semmoe_route(x, self.w_router, logits_in, logits, k_per_token, k or 0, T, H, E, k_max,
+                             topk_idx, topk_w, ws, stream)
+        else:
+            ws = self._workspace("route", abi.semmoe_route_hier_workspace_size(
+                T, H, Ep, abi.dtype_code(x), abi.dtype_code(self.w_router)))
+            abi.semmoe_route_hier(x, self.w_router, logits_in, logits, self.sub_logw, E // Ep, k_per_token,
+                                  k or 0, T, H, Ep, k_max, topk_idx, topk_w, ws, stream)
         mark("route")
         pred = torch.empty(T, **i32)
         abi.semmoe_affinity_lookup(token_ids, self.lut, self.V, R, T, pred, stream)

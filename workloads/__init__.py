@@ -292,7 +292,8 @@ def make_inputs(spec: LayerSpec, with_weights: bool = True) -> dict:
     Returns x [T,H], w_router [E,H], w13 [E,2I,H] (rows 0..I-1 gate, I..2I-1 up),
     w2 [E,H,I], ws13 [2*I_shared,H] / ws2 [H,I_shared] (or None), token_ids [T],
     lut [V], expert_rank [E], k_per_token [T], req_offsets [n_req+1] (all int32),
-    trans [E,R] (float32 next-layer transition counts), and the spec.
+    trans [E,R] (float32 next-layer transition counts), for MoE-Prism layers
+    w_router_parent [E/N,H] and sub_logw [E] (float32; else None), and the spec.
     """
     rng = np.random.Generator(np.random.PCG64(spec.seed))
     T, H, E, I, R = spec.T, spec.H, spec.E, spec.I, spec.R
@@ -333,6 +334,16 @@ def make_inputs(spec: LayerSpec, with_weights: bool = True) -> dict:
         g -= (g @ w_router.T) @ w_router
         x = target @ w_router + g
 
+    # MoE-Prism layers: the parent router (row e = the sum of its sub-experts'
+    # rows / sqrt(N), so its logits carry the parents' affinity bias) and the
+    # sub-experts' co-activation weights a[e, i] ~ Dirichlet(2) over i, as logs.
+    N = spec.sub_split
+    w_router_parent = sub_logw = None
+    if N > 1:
+        w_router_parent = w_router.reshape(parents, N, H).sum(axis=1) / np.sqrt(N)
+        crng = np.random.Generator(np.random.PCG64(np.random.SeedSequence([spec.seed, 1003])))
+        sub_logw = np.log(crng.dirichlet(np.full(N, 2.0), size=parents)).reshape(-1).astype(np.float32)
+
     if spec.k_choices:
         req = np.arange(T) // spec.tokens_per_request
         kpt = np.asarray(spec.k_choices, dtype=np.int32)[req % len(spec.k_choices)]
@@ -349,6 +360,8 @@ def make_inputs(spec: LayerSpec, with_weights: bool = True) -> dict:
         k_per_token=torch.from_numpy(kpt.astype(np.int32)),
         req_offsets=torch.from_numpy(request_offsets(T, spec.seed, spec.req_len_mean, spec.tokens_per_request)),
         trans=torch.from_numpy(transition_table(E, R, spec.seed)),
+        w_router_parent=None if w_router_parent is None else _to(w_router_parent, spec.router_dtype),
+        sub_logw=None if sub_logw is None else torch.from_numpy(sub_logw),
         w13=None, w2=None, ws13=None, ws2=None,
     )
     if with_weights:
