@@ -255,13 +255,21 @@ def test_route_tensor_core_per_token_budgets(E, k_max, wd):
     np.testing.assert_allclose(np_(gw), ref_w, rtol=0, atol=GATE_ATOL)
 
 
-@pytest.mark.parametrize("P,E,H,I", [(1000, 8, 256, 160), (5000, 64, 512, 352), (3000, 16, 512, 640)])
+SPLIT_COUNTS = [0, 1, 127, 128, 129, 255, 256, 257, 384, 511, 512, 640, 1000, 3, 900, 2048]
+
+
+@pytest.mark.parametrize("P,E,H,I", [(1000, 8, 256, 160), (5000, 64, 512, 352), (3000, 16, 512, 640),
+                                     (sum(SPLIT_COUNTS), 16, 256, 576), (30000, 64, 512, 704)])
 def test_grouped_ffn_forms_are_bit_identical(P, E, H, I, monkeypatch):
     """Every form of the grouped GEMM -- independent CTAs, CTA pairs sharing
     weight tiles by TMA multicast, 2-SM MMA pairs with one or two accumulator
-    buffers -- returns exactly the same bits."""
+    buffers -- returns exactly the same bits; one case pins group sizes around
+    the 128- and 256-row boundaries (empty groups, 1, 127..129, 255..257 rows)."""
     rng = np.random.default_rng(P + E)
-    cnt = rng.multinomial(P, np.full(E, 1.0 / E))
+    if P == sum(SPLIT_COUNTS) and E == len(SPLIT_COUNTS):
+        cnt = np.array(SPLIT_COUNTS)
+    else:
+        cnt = rng.multinomial(P, np.full(E, 1.0 / E))
     off = torch.from_numpy(np.r_[0, np.cumsum(cnt)].astype(np.int32)).cuda()
     pe = torch.from_numpy(rng.permutation(E).astype(np.int32)).cuda()
     x = torch.from_numpy(rng.standard_normal((P, H)).astype(np.float32)).to(torch.bfloat16).cuda()
