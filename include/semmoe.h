@@ -16,6 +16,7 @@
  *   semmoe_permute          stable sort of (token, expert) pairs by
  *                           (destination rank, expert) + row gather
  *   semmoe_grouped_ffn      per-expert SwiGLU FFN over the sorted rows
+ *   semmoe_grouped_ffn_gather  the same, reading x through the permutation
  *   semmoe_shared_ffn       dense SwiGLU of the shared experts (optional)
  *   semmoe_combine          un-permute and gate-weighted sum
  * and, around the layer:
@@ -281,6 +282,25 @@ int semmoe_grouped_ffn(const void* x_perm, const int32_t* expert_offsets,
                        const int32_t* phys_to_expert, const void* w13, const void* w2,
                        int dtype, int P, int E, int H, int I,
                        void* y_perm, void* ws, size_t ws_bytes, void* stream);
+
+/*
+ * semmoe_grouped_ffn_gather -- semmoe_grouped_ffn reading the expert inputs
+ * straight from the unpermuted activations: sorted row q of GEMM1 is
+ * x[sorted_to_pair[q] / k_max] (the row semmoe_permute would have gathered into
+ * x_perm[q]), fetched by TMA row gathers, so the permute can run on index
+ * tables only (x = x_perm = NULL) and no x_perm is written or read back.  The
+ * on-device shuffle fused into the expert GEMM ([SP] ko §2.2, de §2 B).
+ * Results are bit-identical to semmoe_permute + semmoe_grouped_ffn.
+ *
+ * x              [device] [T,H] dtype (16-byte aligned)
+ * sorted_to_pair [device] [P] int32, from semmoe_permute (a bad pair id reads
+ *                row 0 and sets SEMMOE_DEVERR_PAIRS)
+ * other arguments, workspace and limits as semmoe_grouped_ffn.
+ */
+int semmoe_grouped_ffn_gather(const void* x, const int32_t* sorted_to_pair, int k_max, int T,
+                              const int32_t* expert_offsets, const int32_t* phys_to_expert, const void* w13,
+                              const void* w2, int dtype, int P, int E, int H, int I, void* y_perm, void* ws,
+                              size_t ws_bytes, void* stream);
 
 /*
  * semmoe_shared_ffn -- the shared experts (applied to every token with gate 1,

@@ -285,3 +285,46 @@ def test_grouped_ffn_forms_are_bit_identical(P, E, H, I, monkeypatch):
         outs.append(y.cpu())
     for o in outs[1:]:
         assert torch.equal(outs[0], o)
+
+
+@pytest.mark.parametrize("dtype,T,E,k_max,H,I", [("bf16", 1000, 16, 4, 256, 640), ("bf16", 3001, 64, 6, 512, 1408),
+                                                 ("bf16", 257, 8, 8, 128, 160), ("f32", 300, 8, 3, 64, 96)])
+def test_grouped_ffn_gather_matches_permuted(dtype, T, E, k_max, H, I, monkeypatch):
+    """GEMM1 reading x through sorted_to_pair (row gathers) gives exactly the
+    bits of the permute's x_perm followed by the grouped FFN, in every form of
+    the grouped GEMM; per-token budgets leave padding slots, so sorted rows map
+    to tokens irregularly."""
+    rng = np.random.default_rng(T + I)
+    tdt = torch.bfloat16 if dtype == "bf16" else torch.float32
+    idx, k = _route_random(rng, T, E, k_max)
+    er = (np.arange(E) % 4).astype(np.int32)
+    P = int(k.sum())
+    x = torch.from_numpy(rng.standard_normal((T, H)).astype(np.float32)).to(tdt).cuda()
+    w13 = torch.from_numpy((rng.standard_normal((E, 2 * I, H)) / np.sqrt(H)).astype(np.float32)).to(tdt).cuda()
+    w2 = torch.from_numpy((rng.standard_normal((E, H, I)) / np.sqrt(I)).astype(np.float32)).to(tdt).cuda()
+    eo, ro = torch.empty(E + 1, **i32), torch.empty(5, **i32)
+    p2e, ec = torch.empty(E, **i32), torch.empty(E, **i32)
+    s2p, p2s = torch.empty(P, **i32), torch.empty(T * k_max, **i32)
+    xp = torch.empty(P, H, dtype=tdt, device="cuda")
+    ws = torch.empty(abi().semmoe_permute_workspace_size(T, k_max, E), dtype=torch.uint8, device="cuda")
+    abi().semmoe_permute(torch.from_numpy(idx).cuda(), torch.from_numpy(er).cuda(), x, T, H, E, 4, k_max, P, eo, ro,
+                         p2e, ec, s2p, p2s, xp, ws)
+    fws = torch.empty(abi().semmoe_grouped_ffn_workspace_size(P, I, 1 if dtype == "bf16" else 0), dtype=torch.uint8,
+                      device="cuda")
+    modes = ("single", "multicast", "pair1", "pair") if dtype == "bf16" else ("default",)
+    for mode in modes:
+        monkeypatch.setenv("SEMMOE_FFN_MODE", mode)
+        y0 = torch.full((P, H), 3.0, dtype=tdt, device="cuda")
+        y1 = torch.full((P, H), 5.0, dtype=tdt, device="cuda")
+        abi().semmoe_grouped_ffn(xp, eo, p2e, w13, w2, P, E, H, I, y0, fws)
+        abi().semmoe_grouped_ffn_gather(x, s2p, k_max, T, eo, p2e, w13, w2, P, E, H, I, y1, fws)
+        assert abi().semmoe_check_errors() == 0
+        assert torch.equal(y0.cpu(), y1.cpu()), mode
+    if dtype == "bf16":  # the CUDA-core path gathers the same way
+        monkeypatch.setenv("SEMMOE_FFN_IMPL", "simt")
+        y0 = torch.empty(P, H, dtype=tdt, device="cuda")
+        y1 = torch.empty(P, H, dtype=tdt, device="cuda")
+        abi().semmoe_grouped_ffn(xp, eo, p2e, w13, w2, P, E, H, I, y0, fws)
+        abi().semmoe_grouped_ffn_gather(x, s2p, k_max, T, eo, p2e, w13, w2, P, E, H, I, y1, fws)
+        assert abi().semmoe_check_errors() == 0
+        assert torch.equal(y0.cpu(), y1.cpu())

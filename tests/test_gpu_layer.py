@@ -21,10 +21,14 @@ SMALL = [
 ]
 
 
+@pytest.mark.parametrize("fused_gather", [True, False], ids=["gather", "x_perm"])
 @pytest.mark.parametrize("name,over", SMALL, ids=[f"{n}-{i}" for i, (n, _) in enumerate(SMALL)])
-def test_layer_small(name, over):
+def test_layer_small(name, over, fused_gather):
+    """Both ways into the expert GEMM: GEMM1 gathering x rows, and the permute
+    writing x_perm (compared with the oracle's permuted rows)."""
     d = wl.make_inputs(wl.scaled(name, **over))
-    res, P = run_gpu(d)
+    res, P = run_gpu(d, fused_gather=fused_gather)
+    assert (res.x_perm is None) == fused_gather
     check_layer_full(d, res, P)
 
 

@@ -47,6 +47,8 @@ SIGNATURES = {
                                     _vp, _vp, _vp]),
     "semmoe_grouped_ffn_workspace_size": (_sz, [_i, _i, _i]),
     "semmoe_grouped_ffn": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _vp, _vp, _sz, _vp]),
+    "semmoe_grouped_ffn_gather": (_i, [_vp, _vp, _i, _i, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _vp, _vp, _sz,
+                                       _vp]),
     "semmoe_shared_ffn_workspace_size": (_sz, [_i, _i, _i]),
     "semmoe_shared_ffn": (_i, [_vp, _vp, _vp, _i, _i, _i, _i, _vp, _vp, _sz, _vp]),
     "semmoe_combine": (_i, [_vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _vp, _vp]),
@@ -214,6 +216,13 @@ def semmoe_grouped_ffn(x_perm, expert_offsets, phys_to_expert, w13, w2, P, E, H,
     _check(lib().semmoe_grouped_ffn(_p(x_perm), _p(expert_offsets), _p(phys_to_expert), _p(w13),
                                     _p(w2), dtype_code(w13), P, E, H, I, _p(y_perm), _p(ws),
                                     ws.numel() * ws.element_size(), _stream(stream)))
+
+
+def semmoe_grouped_ffn_gather(x, sorted_to_pair, k_max, T, expert_offsets, phys_to_expert, w13, w2, P, E, H, I,
+                              y_perm, ws, stream=None):
+    _check(lib().semmoe_grouped_ffn_gather(_p(x), _p(sorted_to_pair), k_max, T, _p(expert_offsets),
+                                           _p(phys_to_expert), _p(w13), _p(w2), dtype_code(w13), P, E, H, I,
+                                           _p(y_perm), _p(ws), ws.numel() * ws.element_size(), _stream(stream)))
 
 
 def semmoe_shared_ffn_workspace_size(T, I_s, dtype: int) -> int:

@@ -285,8 +285,27 @@ int semmoe_grouped_ffn(const void* x_perm, const int32_t* expert_offsets, const 
   if (P == 0) return SEMMOE_OK;
   CHECK_DEVICE("semmoe_grouped_ffn");
   return cuda_status(launch_ffn(x_perm, expert_offsets, phys_to_expert, w13, w2, dtype, P, E, H, I, y_perm, ws,
-                                static_cast<cudaStream_t>(stream)),
+                                nullptr, 1, 0, static_cast<cudaStream_t>(stream)),
                      "semmoe_grouped_ffn");
+}
+
+int semmoe_grouped_ffn_gather(const void* x, const int32_t* sorted_to_pair, int k_max, int T,
+                              const int32_t* expert_offsets, const int32_t* phys_to_expert, const void* w13,
+                              const void* w2, int dtype, int P, int E, int H, int I, void* y_perm, void* ws,
+                              size_t ws_bytes, void* stream) {
+  REQUIRE(E >= 1 && E <= 256, "semmoe_grouped_ffn_gather: E = %d outside [1, 256]", E);
+  REQUIRE(T >= 0 && k_max >= 1 && (long long)T * k_max < (1LL << 31),
+          "semmoe_grouped_ffn_gather: bad sizes T=%d k_max=%d", T, k_max);
+  REQUIRE(P <= (long long)T * k_max, "semmoe_grouped_ffn_gather: P = %d > T * k_max", P);
+  REQUIRE(expert_offsets && phys_to_expert, "semmoe_grouped_ffn_gather: null offsets");
+  REQUIRE(P == 0 || sorted_to_pair, "semmoe_grouped_ffn_gather: null sorted_to_pair");
+  int rc = check_ffn_args("semmoe_grouped_ffn_gather", x, w13, w2, dtype, P, H, I, y_perm, ws, ws_bytes);
+  if (rc != SEMMOE_OK) return rc;
+  if (P == 0) return SEMMOE_OK;
+  CHECK_DEVICE("semmoe_grouped_ffn_gather");
+  return cuda_status(launch_ffn(x, expert_offsets, phys_to_expert, w13, w2, dtype, P, E, H, I, y_perm, ws,
+                                sorted_to_pair, k_max, T, static_cast<cudaStream_t>(stream)),
+                     "semmoe_grouped_ffn_gather");
 }
 
 size_t semmoe_shared_ffn_workspace_size(int T, int I_s, int dtype) {
@@ -300,7 +319,7 @@ int semmoe_shared_ffn(const void* x, const void* ws13, const void* ws2, int dtyp
   if (rc != SEMMOE_OK) return rc;
   if (T == 0) return SEMMOE_OK;
   CHECK_DEVICE("semmoe_shared_ffn");
-  return cuda_status(launch_ffn(x, nullptr, nullptr, ws13, ws2, dtype, T, 1, H, I_s, y_shared, ws,
+  return cuda_status(launch_ffn(x, nullptr, nullptr, ws13, ws2, dtype, T, 1, H, I_s, y_shared, ws, nullptr, 1, 0,
                                 static_cast<cudaStream_t>(stream)),
                      "semmoe_shared_ffn");
 }

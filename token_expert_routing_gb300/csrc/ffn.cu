@@ -11,9 +11,10 @@ namespace semmoe {
 
 cudaError_t launch_ffn_simt(const void* x, const int32_t* offsets, const int32_t* p2e, const void* w13,
                             const void* w2, int dtype, int P, int E, int H, int I, void* y, void* ws,
-                            cudaStream_t s);
+                            const int32_t* gather, int gather_div, int T_x, cudaStream_t s);
 cudaError_t launch_ffn_tc(const void* x, const int32_t* offsets, const int32_t* p2e, const void* w13,
-                          const void* w2, int P, int E, int H, int I, void* y, void* ws, cudaStream_t s);
+                          const void* w2, int P, int E, int H, int I, void* y, void* ws, const int32_t* gather,
+                          int gather_div, int T_x, cudaStream_t s);
 int ffn_simt_take_errors(cudaStream_t s, int* bits);
 int ffn_tc_take_errors(cudaStream_t s, int* bits);
 
@@ -35,9 +36,10 @@ static bool force_simt() {
 
 cudaError_t launch_ffn(const void* x, const int32_t* offsets, const int32_t* p2e, const void* w13,
                        const void* w2, int dtype, int P, int E, int H, int I, void* y, void* ws,
-                       cudaStream_t s) {
-  if (dtype == SEMMOE_BF16 && !force_simt()) return launch_ffn_tc(x, offsets, p2e, w13, w2, P, E, H, I, y, ws, s);
-  return launch_ffn_simt(x, offsets, p2e, w13, w2, dtype, P, E, H, I, y, ws, s);
+                       const int32_t* gather, int gather_div, int T_x, cudaStream_t s) {
+  if (dtype == SEMMOE_BF16 && !force_simt())
+    return launch_ffn_tc(x, offsets, p2e, w13, w2, P, E, H, I, y, ws, gather, gather_div, T_x, s);
+  return launch_ffn_simt(x, offsets, p2e, w13, w2, dtype, P, E, H, I, y, ws, gather, gather_div, T_x, s);
 }
 
 }  // namespace semmoe

@@ -24,12 +24,14 @@ template <typename T, bool GLU>
 __global__ void __launch_bounds__(kThreads)
 ffn_simt_kernel(const T* __restrict__ A, const int32_t* __restrict__ offsets,
                 const int32_t* __restrict__ phys_to_expert, int n_groups, int P, const T* __restrict__ W,
-                long long w_stride, int N, int K, int glu_off, int E, T* __restrict__ C) {
+                long long w_stride, int N, int K, int glu_off, int E, const int32_t* __restrict__ gather,
+                int gather_div, int gather_rows, T* __restrict__ C) {
   __shared__ float As[BK][BM];
   __shared__ float Bg[BK][BN];
   __shared__ float Bu[GLU ? BK : 1][GLU ? BN : 1];
   __shared__ int scan[kThreads];
   __shared__ GroupTile gt_s;
+  __shared__ int src_row[BM];  // A row of each tile row (sorted row, or gathered x row)
 
   const GroupTile gt =
       group_tile_block(offsets, phys_to_expert, n_groups, P, E, BM, blockIdx.x, scan, &gt_s, &g_err);
@@ -38,12 +40,28 @@ ffn_simt_kernel(const T* __restrict__ A, const int32_t* __restrict__ offsets,
   const int n0 = blockIdx.y * BN;
   const T* We = W + (long long)e * w_stride;
   const int tx = threadIdx.x % 16, ty = threadIdx.x / 16;
+  for (int m = threadIdx.x; m < BM; m += kThreads) {
+    int r = row0 + m;
+    if (gather != nullptr) {
+      r = 0;
+      if (m < rows) {
+        const int p = gather[row0 + m];
+        r = p >= 0 ? p / gather_div : -1;
+        if (r < 0 || r >= gather_rows) {
+          atomicOr(&g_err, SEMMOE_DEVERR_PAIRS);
+          r = 0;
+        }
+      }
+    }
+    src_row[m] = r;
+  }
+  __syncthreads();
 
   float acc[4][4] = {}, accu[4][4] = {};
   for (int k0 = 0; k0 < K; k0 += BK) {
     for (int i = threadIdx.x; i < BM * BK; i += kThreads) {
       int m = i / BK, k = i % BK;
-      As[k][m] = (m < rows && k0 + k < K) ? to_f32(A[(long long)(row0 + m) * K + k0 + k]) : 0.f;
+      As[k][m] = (m < rows && k0 + k < K) ? to_f32(A[(long long)src_row[m] * K + k0 + k]) : 0.f;
     }
     for (int i = threadIdx.x; i < BN * BK; i += kThreads) {
       int n = i / BK, k = i % BK;
@@ -88,19 +106,22 @@ ffn_simt_kernel(const T* __restrict__ A, const int32_t* __restrict__ offsets,
 
 template <typename T>
 cudaError_t run_simt(const void* x, const int32_t* offsets, const int32_t* p2e, const void* w13, const void* w2,
-                     int P, int E, int H, int I, void* y, void* ws, cudaStream_t s) {
+                     int P, int E, int H, int I, void* y, void* ws, const int32_t* gather, int gather_div, int T_x,
+                     cudaStream_t s) {
   const int n_groups = offsets ? E : 1;
   const int max_mtiles = (P + BM - 1) / BM + n_groups;
   T* h = static_cast<T*>(ws);
   dim3 g1(max_mtiles, (I + BN - 1) / BN);
   ffn_simt_kernel<T, true><<<g1, kThreads, 0, s>>>(static_cast<const T*>(x), offsets, p2e, n_groups, P,
-                                                   static_cast<const T*>(w13), 2LL * I * H, I, H, I, E, h);
+                                                   static_cast<const T*>(w13), 2LL * I * H, I, H, I, E, gather,
+                                                   gather_div, T_x, h);
   count_launches(1);
   cudaError_t err = cudaGetLastError();
   if (err != cudaSuccess) return err;
   dim3 g2(max_mtiles, (H + BN - 1) / BN);
   ffn_simt_kernel<T, false><<<g2, kThreads, 0, s>>>(h, offsets, p2e, n_groups, P, static_cast<const T*>(w2),
-                                                    (long long)H * I, H, I, 0, E, static_cast<T*>(y));
+                                                    (long long)H * I, H, I, 0, E, nullptr, 1, 0,
+                                                    static_cast<T*>(y));
   count_launches(1);
   return cudaGetLastError();
 }
@@ -111,10 +132,11 @@ int ffn_simt_take_errors(cudaStream_t s, int* bits) { return take_error_word(g_e
 
 cudaError_t launch_ffn_simt(const void* x, const int32_t* offsets, const int32_t* p2e, const void* w13,
                             const void* w2, int dtype, int P, int E, int H, int I, void* y, void* ws,
-                            cudaStream_t s) {
+                            const int32_t* gather, int gather_div, int T_x, cudaStream_t s) {
   if (P == 0) return cudaSuccess;
-  if (dtype == SEMMOE_BF16) return run_simt<__nv_bfloat16>(x, offsets, p2e, w13, w2, P, E, H, I, y, ws, s);
-  return run_simt<float>(x, offsets, p2e, w13, w2, P, E, H, I, y, ws, s);
+  if (dtype == SEMMOE_BF16)
+    return run_simt<__nv_bfloat16>(x, offsets, p2e, w13, w2, P, E, H, I, y, ws, gather, gather_div, T_x, s);
+  return run_simt<float>(x, offsets, p2e, w13, w2, P, E, H, I, y, ws, gather, gather_div, T_x, s);
 }
 
 }  // namespace semmoe

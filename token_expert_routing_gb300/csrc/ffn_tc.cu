@@ -98,11 +98,34 @@ __device__ __forceinline__ void decode_mtile(const SH& sh, int G, int mu, int ra
   e = sh.pe[lo];
 }
 
+// Row gather of the A operand (GEMM1 reading x directly instead of x_perm):
+// lane l of the producer warp fetches tile rows 4l .. 4l+3; sorted row q reads
+// x row gather[q] / gather_div (the token of pair q).  Rows past P, and bad pair
+// ids (flagged), read row 0: their results are never stored.
+__device__ __forceinline__ void gather_sources(const int32_t* __restrict__ gather, int gather_div, int gather_rows,
+                                               int P, int row0, int lane, int (&src)[4]) {
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int q = row0 + 4 * lane + i;
+    int r = 0;
+    if (q < P) {
+      const int p = gather[q];
+      r = p >= 0 ? p / gather_div : -1;
+      if (r < 0 || r >= gather_rows) {
+        atomicOr(&g_err, SEMMOE_DEVERR_PAIRS);
+        r = 0;
+      }
+    }
+    src[i] = r;
+  }
+}
+
 template <bool GLU, int CL>
 __global__ void __launch_bounds__(THREADS, 1)
 ffn_tc_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b,
               const int32_t* __restrict__ offsets, const int32_t* __restrict__ phys_to_expert, int G, int P,
-              int E, int N, int K, int n_tiles, __nv_bfloat16* __restrict__ out) {
+              int E, int N, int K, int n_tiles, const int32_t* __restrict__ gather, int gather_div, int gather_rows,
+              __nv_bfloat16* __restrict__ out) {
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   const uint32_t pad = (1024u - (smem_u32(smem_raw) & 1023u)) & 1023u;
   unsigned char* stage_a = smem_raw + pad;                 // STAGES x [128 x 64] bf16
@@ -179,21 +202,31 @@ ffn_tc_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__
   constexpr uint16_t kAll = (uint16_t)((1u << CL) - 1);
 
   if (warp == 0) {
-    if (lane == 0) {
-      // ---------------- TMA producer ----------------
-      uint32_t it = 0;
-      for (int tile = unit0; tile < total; tile += units) {
-        if (*abort_flag) break;
-        const int mt = tile / n_tiles, nt = tile % n_tiles;
-        int row0, rows, e;
-        decode_mtile<CL>(sh, G, mt, rank, row0, rows, e);
-        bool ok = true;
-        for (int kb = 0; kb < kb_n; ++kb) {
-          const int s = it % STAGES;
-          const uint32_t ph = (it / STAGES) & 1;
-          if (!mbar_wait(&sh.empty[s], ph ^ 1, abort_flag, &g_err)) { ok = false; break; }
+    // ---------------- TMA producer (warp 0; lane 0 unless A rows are gathered) ----------------
+    uint32_t it = 0;
+    for (int tile = unit0; tile < total; tile += units) {
+      if (*abort_flag) break;
+      const int mt = tile / n_tiles, nt = tile % n_tiles;
+      int row0, rows, e;
+      decode_mtile<CL>(sh, G, mt, rank, row0, rows, e);
+      int src[4] = {0, 0, 0, 0};
+      if (gather != nullptr) gather_sources(gather, gather_div, gather_rows, P, row0, lane, src);
+      bool ok = true;
+      for (int kb = 0; kb < kb_n; ++kb) {
+        const int s = it % STAGES;
+        const uint32_t ph = (it / STAGES) & 1;
+        int good = 1;
+        if (lane == 0) good = mbar_wait(&sh.empty[s], ph ^ 1, abort_flag, &g_err);
+        if (!__shfl_sync(0xffffffffu, good, 0)) { ok = false; break; }
+        if (gather != nullptr) {
+          if (lane == 0) mbar_expect_tx(&sh.full[s], STAGE_BYTES);
+          tma_gather4(stage_a + s * A_BYTES + lane * 4 * (BK * 2), &map_a, &sh.full[s], kb * BK, src[0], src[1],
+                      src[2], src[3]);
+        } else if (lane == 0) {
           mbar_expect_tx(&sh.full[s], STAGE_BYTES);
           tma_load_2d(stage_a + s * A_BYTES, &map_a, &sh.full[s], kb * BK, row0);
+        }
+        if (lane == 0) {
           unsigned char* b = stage_b + s * B_BYTES;
           if (CL == 1) {
             if (GLU) {
@@ -209,14 +242,14 @@ ffn_tc_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__
               tma_load_3d_mc(b + rank * (B_BYTES / 2), &map_b, &sh.full[s], kb * BK, nt * BN + rank * 128, e,
                              kAll);
           }
-          ++it;
         }
-        if (!ok) break;
+        ++it;
       }
-      if (*abort_flag) {  // no TMA write may still be landing when the CTA exits
-        for (uint32_t j = it > (uint32_t)STAGES ? it - STAGES : 0; j < it; ++j)
-          mbar_drain(&sh.full[j % STAGES], (j / STAGES) & 1, &g_err);
-      }
+      if (!ok) break;
+    }
+    if (lane == 0 && *abort_flag) {  // no TMA write may still be landing when the CTA exits
+      for (uint32_t j = it > (uint32_t)STAGES ? it - STAGES : 0; j < it; ++j)
+        mbar_drain(&sh.full[j % STAGES], (j / STAGES) & 1, &g_err);
     }
   } else if (warp == 1) {
     if (lane == 0) {
@@ -361,7 +394,8 @@ template <bool GLU, int NBUF>
 __global__ void __launch_bounds__(THREADS, 1)
 ffn_pair_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b,
                 const int32_t* __restrict__ offsets, const int32_t* __restrict__ phys_to_expert, int G, int P,
-                int E, int N, int K, int n_tiles, __nv_bfloat16* __restrict__ out) {
+                int E, int N, int K, int n_tiles, const int32_t* __restrict__ gather, int gather_div, int gather_rows,
+                __nv_bfloat16* __restrict__ out) {
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   const uint32_t pad = (1024u - (smem_u32(smem_raw) & 1023u)) & 1023u;
   unsigned char* ring = smem_raw + pad;  // stage s: A [128 x 64] then B half [128 x 64]
@@ -432,33 +466,40 @@ ffn_pair_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant
   const int kb_n = (K + BK - 1) / BK;
   const int unit0 = blockIdx.x / 2, units = gridDim.x / 2;
 
-  if (warp == 0) {
-    if (lane == 0) {  // TMA producer (both CTAs): own A rows + own half of B, counted on the leader's barrier
-      uint32_t it = 0;
-      for (int tile = unit0; tile < total; tile += units) {
-        if (*abort_flag) break;
-        const int mt = tile / n_tiles, nt = tile % n_tiles;
-        int row0, rows, e;
-        decode_mtile<2>(sh, G, mt, rank, row0, rows, e);
-        bool ok = true;
-        for (int kb = 0; kb < kb_n; ++kb) {
-          const int s = it % P_STAGES;
-          const uint32_t ph = (it / P_STAGES) & 1;
-          if (!mbar_wait(&sh.empty[s], ph ^ 1, abort_flag, &g_err)) { ok = false; break; }
-          if (leader) mbar_expect_tx(&sh.full[s], 2 * P_STAGE_BYTES);
-          const uint32_t fb = mapa_rank(&sh.full[s], 0);
-          unsigned char* st = ring + (size_t)s * P_STAGE_BYTES;
+  if (warp == 0) {  // TMA producer (both CTAs): own A rows + own half of B, counted on the leader's barrier
+    uint32_t it = 0;
+    for (int tile = unit0; tile < total; tile += units) {
+      if (*abort_flag) break;
+      const int mt = tile / n_tiles, nt = tile % n_tiles;
+      int row0, rows, e;
+      decode_mtile<2>(sh, G, mt, rank, row0, rows, e);
+      int src[4] = {0, 0, 0, 0};
+      if (gather != nullptr) gather_sources(gather, gather_div, gather_rows, P, row0, lane, src);
+      bool ok = true;
+      for (int kb = 0; kb < kb_n; ++kb) {
+        const int s = it % P_STAGES;
+        const uint32_t ph = (it / P_STAGES) & 1;
+        int good = 1;
+        if (lane == 0) good = mbar_wait(&sh.empty[s], ph ^ 1, abort_flag, &g_err);
+        if (!__shfl_sync(0xffffffffu, good, 0)) { ok = false; break; }
+        if (lane == 0 && leader) mbar_expect_tx(&sh.full[s], 2 * P_STAGE_BYTES);
+        const uint32_t fb = mapa_rank(&sh.full[s], 0);
+        unsigned char* st = ring + (size_t)s * P_STAGE_BYTES;
+        if (gather != nullptr)
+          tma_gather4_pair(st + lane * 4 * (BK * 2), &map_a, fb, kb * BK, src[0], src[1], src[2], src[3]);
+        else if (lane == 0)
           tma_load_2d_pair(st, &map_a, fb, kb * BK, row0);
+        if (lane == 0) {
           if (GLU) tma_load_4d_pair(st + A_BYTES, &map_b, fb, kb * BK, nt * 128, rank, e);
           else tma_load_3d_pair(st + A_BYTES, &map_b, fb, kb * BK, nt * BN + rank * 128, e);
-          ++it;
         }
-        if (!ok) break;
+        ++it;
       }
-      if (*abort_flag && leader) {
-        for (uint32_t j = it > (uint32_t)P_STAGES ? it - P_STAGES : 0; j < it; ++j)
-          mbar_drain(&sh.full[j % P_STAGES], (j / P_STAGES) & 1, &g_err);
-      }
+      if (!ok) break;
+    }
+    if (lane == 0 && *abort_flag && leader) {
+      for (uint32_t j = it > (uint32_t)P_STAGES ? it - P_STAGES : 0; j < it; ++j)
+        mbar_drain(&sh.full[j % P_STAGES], (j / P_STAGES) & 1, &g_err);
     }
   } else if (warp == 1) {
     if (lane == 0 && leader) {  // MMA issuer: the pair's even CTA only
@@ -571,9 +612,17 @@ ffn_pair_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant
 // ---------------------------------------------------------------------------
 // host side
 // ---------------------------------------------------------------------------
+// gather != nullptr: the A operand's sorted row q is x row gather[q] / gather_div
+// (ma then maps x with one-row boxes).
+struct Gather {
+  const int32_t* rows = nullptr;
+  int div = 1, n = 0;
+};
+
 template <bool GLU, int CL>
 cudaError_t launch_one(const CUtensorMap& ma, const CUtensorMap& mb, const int32_t* offsets, const int32_t* p2e,
-                       int G, int P, int E, int N, int K, int n_tiles, __nv_bfloat16* out, cudaStream_t s) {
+                       int G, int P, int E, int N, int K, int n_tiles, Gather ga, __nv_bfloat16* out,
+                       cudaStream_t s) {
   auto kern = ffn_tc_kernel<GLU, CL>;
   static std::atomic<unsigned long long> smem_set{0};
   cudaError_t e = ensure_smem_limit(kern, (int)kSmemBytes, smem_set);
@@ -582,7 +631,8 @@ cudaError_t launch_one(const CUtensorMap& ma, const CUtensorMap& mb, const int32
   if (CL == 1) {
     int grid = sm_count();
     if (max_units < grid) grid = (int)max_units;
-    kern<<<grid, THREADS, kSmemBytes, s>>>(ma, mb, offsets, p2e, G, P, E, N, K, n_tiles, out);
+    kern<<<grid, THREADS, kSmemBytes, s>>>(ma, mb, offsets, p2e, G, P, E, N, K, n_tiles, ga.rows, ga.div, ga.n,
+                                           out);
   } else {
     cudaLaunchConfig_t cfg = {};
     cudaLaunchAttribute attr[1];
@@ -603,7 +653,7 @@ cudaError_t launch_one(const CUtensorMap& ma, const CUtensorMap& mb, const int32
     long long units = clusters;
     if (max_units < units) units = max_units;
     cfg.gridDim = dim3((unsigned)(units * CL));
-    e = cudaLaunchKernelEx(&cfg, kern, ma, mb, offsets, p2e, G, P, E, N, K, n_tiles, out);
+    e = cudaLaunchKernelEx(&cfg, kern, ma, mb, offsets, p2e, G, P, E, N, K, n_tiles, ga.rows, ga.div, ga.n, out);
     if (e != cudaSuccess) return e;
   }
   count_launches(1);
@@ -612,7 +662,8 @@ cudaError_t launch_one(const CUtensorMap& ma, const CUtensorMap& mb, const int32
 
 template <bool GLU, int NBUF>
 cudaError_t launch_pair(const CUtensorMap& ma, const CUtensorMap& mb, const int32_t* offsets, const int32_t* p2e,
-                        int G, int P, int E, int N, int K, int n_tiles, __nv_bfloat16* out, cudaStream_t s) {
+                        int G, int P, int E, int N, int K, int n_tiles, Gather ga, __nv_bfloat16* out,
+                        cudaStream_t s) {
   auto kern = ffn_pair_kernel<GLU, NBUF>;
   static std::atomic<unsigned long long> smem_set{0};
   cudaError_t e = ensure_smem_limit(kern, (int)kPairSmemBytes, smem_set);
@@ -637,7 +688,7 @@ cudaError_t launch_pair(const CUtensorMap& ma, const CUtensorMap& mb, const int3
   long long units = clusters;
   if (max_units < units) units = max_units;
   cfg.gridDim = dim3((unsigned)(units * 2));
-  e = cudaLaunchKernelEx(&cfg, kern, ma, mb, offsets, p2e, G, P, E, N, K, n_tiles, out);
+  e = cudaLaunchKernelEx(&cfg, kern, ma, mb, offsets, p2e, G, P, E, N, K, n_tiles, ga.rows, ga.div, ga.n, out);
   if (e != cudaSuccess) return e;
   count_launches(1);
   return cudaGetLastError();
@@ -664,15 +715,27 @@ static int ffn_mode(int I, int P, int G) {
   return (I >= 512 && (long long)P >= 2LL * BM * G) ? 3 : 0;
 }
 
+// gather_rows != nullptr: x is the unpermuted [T_x, H] activation and sorted row
+// q of GEMM1 reads x row gather_rows[q] / gather_div.
 cudaError_t launch_ffn_tc(const void* x, const int32_t* offsets, const int32_t* p2e, const void* w13,
-                          const void* w2, int P, int E, int H, int I, void* y, void* ws, cudaStream_t s) {
+                          const void* w2, int P, int E, int H, int I, void* y, void* ws, const int32_t* gather_rows,
+                          int gather_div, int T_x, cudaStream_t s) {
   if (P == 0) return cudaSuccess;
   const int G = offsets ? E : 1;
   const int mode = ffn_mode(I, P, G);
   const int CL = mode == 0 ? 1 : 2;
   const cuuint64_t es = 2;
   CUtensorMap ma1, mb1, ma2, mb2;
-  {
+  Gather ga;
+  if (gather_rows != nullptr) {  // x rows fetched by row gathers: one-row boxes
+    ga.rows = gather_rows;
+    ga.div = gather_div;
+    ga.n = T_x;
+    const cuuint64_t dims[2] = {(cuuint64_t)H, (cuuint64_t)T_x};
+    const cuuint64_t str[1] = {(cuuint64_t)H * es};
+    const cuuint32_t box[2] = {BK, 1};
+    if (!make_map_bf16(&ma1, x, 2, dims, str, box)) return cudaErrorInvalidValue;
+  } else {
     const cuuint64_t dims[2] = {(cuuint64_t)H, (cuuint64_t)P};
     const cuuint64_t str[1] = {(cuuint64_t)H * es};
     const cuuint32_t box[2] = {BK, BM};
@@ -700,23 +763,23 @@ cudaError_t launch_ffn_tc(const void* x, const int32_t* offsets, const int32_t* 
   __nv_bfloat16* yb = static_cast<__nv_bfloat16*>(y);
   cudaError_t e;
   if (mode == 1) {
-    e = launch_one<true, 2>(ma1, mb1, offsets, p2e, G, P, E, I, H, (I + 127) / 128, h, s);
+    e = launch_one<true, 2>(ma1, mb1, offsets, p2e, G, P, E, I, H, (I + 127) / 128, ga, h, s);
     if (e != cudaSuccess) return e;
-    return launch_one<false, 2>(ma2, mb2, offsets, p2e, G, P, E, H, I, (H + BN - 1) / BN, yb, s);
+    return launch_one<false, 2>(ma2, mb2, offsets, p2e, G, P, E, H, I, (H + BN - 1) / BN, Gather(), yb, s);
   }
   if (mode == 2) {
-    e = launch_pair<true, 1>(ma1, mb1, offsets, p2e, G, P, E, I, H, (I + 127) / 128, h, s);
+    e = launch_pair<true, 1>(ma1, mb1, offsets, p2e, G, P, E, I, H, (I + 127) / 128, ga, h, s);
     if (e != cudaSuccess) return e;
-    return launch_pair<false, 1>(ma2, mb2, offsets, p2e, G, P, E, H, I, (H + BN - 1) / BN, yb, s);
+    return launch_pair<false, 1>(ma2, mb2, offsets, p2e, G, P, E, H, I, (H + BN - 1) / BN, Gather(), yb, s);
   }
   if (mode == 3) {
-    e = launch_pair<true, 2>(ma1, mb1, offsets, p2e, G, P, E, I, H, (I + 127) / 128, h, s);
+    e = launch_pair<true, 2>(ma1, mb1, offsets, p2e, G, P, E, I, H, (I + 127) / 128, ga, h, s);
     if (e != cudaSuccess) return e;
-    return launch_pair<false, 2>(ma2, mb2, offsets, p2e, G, P, E, H, I, (H + BN - 1) / BN, yb, s);
+    return launch_pair<false, 2>(ma2, mb2, offsets, p2e, G, P, E, H, I, (H + BN - 1) / BN, Gather(), yb, s);
   }
-  e = launch_one<true, 1>(ma1, mb1, offsets, p2e, G, P, E, I, H, (I + 127) / 128, h, s);
+  e = launch_one<true, 1>(ma1, mb1, offsets, p2e, G, P, E, I, H, (I + 127) / 128, ga, h, s);
   if (e != cudaSuccess) return e;
-  return launch_one<false, 1>(ma2, mb2, offsets, p2e, G, P, E, H, I, (H + BN - 1) / BN, yb, s);
+  return launch_one<false, 1>(ma2, mb2, offsets, p2e, G, P, E, H, I, (H + BN - 1) / BN, Gather(), yb, s);
 }
 
 }  // namespace semmoe

@@ -31,7 +31,7 @@ class LayerOutput:
     expert_counts: torch.Tensor
     sorted_to_pair: torch.Tensor
     pair_to_sorted: torch.Tensor
-    x_perm: torch.Tensor
+    x_perm: Optional[torch.Tensor]   # None when GEMM1 gathers x through the permutation
     y_perm: torch.Tensor
     y_shared: Optional[torch.Tensor]
     schedule: Optional[dict] = None      # semmoe_dp_schedule outputs (when req_offsets is given)
@@ -50,7 +50,7 @@ class MoELayer:
     """
 
     def __init__(self, w_router, w13, w2, expert_rank, lut, R: int, k_max: int, ws13=None, ws2=None,
-                 trans=None, sub_logw=None, device="cuda"):
+                 trans=None, sub_logw=None, fused_gather: bool = False, device="cuda"):
         dev = torch.device(device)
         c = lambda t: None if t is None else t.to(dev).contiguous()  # noqa: E731
         self.w_router, self.w13, self.w2 = c(w_router), c(w13), c(w2)
@@ -59,6 +59,10 @@ class MoELayer:
         self.ws13, self.ws2 = c(ws13), c(ws2)
         self.trans = None if trans is None else c(trans).to(torch.float32)
         self.sub_logw = None if sub_logw is None else c(sub_logw).to(torch.float32)
+        # fused_gather: GEMM1 reads x through the permutation by TMA row gathers
+        # and no x_perm is written; bit-identical, but slower on this hardware
+        # (32 four-row gathers per A tile and k-block), so off by default
+        self.fused_gather = fused_gather
         self.E, twoI, self.H = self.w13.shape
         self.I = twoI // 2
         self.I_s = 0 if ws13 is None else self.ws13.shape[0] // 2
@@ -153,17 +157,21 @@ class MoELayer:
         expert_counts = torch.empty(E, **i32)
         sorted_to_pair = torch.empty(max(P, 1), **i32)
         pair_to_sorted = torch.empty(T * k_max, **i32)
-        x_perm = torch.empty(P, H, dtype=x.dtype, device=dev)
+        x_perm = None if self.fused_gather else torch.empty(P, H, dtype=x.dtype, device=dev)
         ws = self._workspace("permute", abi.semmoe_permute_workspace_size(T, k_max, E))
-        abi.semmoe_permute(topk_idx, self.expert_rank, x, T, H, E, R, k_max, P, expert_offsets,
-                           rank_offsets, phys_to_expert, expert_counts, sorted_to_pair, pair_to_sorted,
-                           x_perm, ws, stream)
+        abi.semmoe_permute(topk_idx, self.expert_rank, None if self.fused_gather else x, T, H, E, R, k_max, P,
+                           expert_offsets, rank_offsets, phys_to_expert, expert_counts, sorted_to_pair,
+                           pair_to_sorted, x_perm, ws, stream)
         mark("permute")
         y_perm = torch.empty(P, H, dtype=x.dtype, device=dev)
         dcode = abi.dtype_code(self.w13)
         ws = self._workspace("ffn", abi.semmoe_grouped_ffn_workspace_size(P, I, dcode))
-        abi.semmoe_grouped_ffn(x_perm, expert_offsets, phys_to_expert, self.w13, self.w2, P, E, H, I,
-                               y_perm, ws, stream)
+        if self.fused_gather:
+            abi.semmoe_grouped_ffn_gather(x, sorted_to_pair, k_max, T, expert_offsets, phys_to_expert, self.w13,
+                                          self.w2, P, E, H, I, y_perm, ws, stream)
+        else:
+            abi.semmoe_grouped_ffn(x_perm, expert_offsets, phys_to_expert, self.w13, self.w2, P, E, H, I,
+                                   y_perm, ws, stream)
         mark("grouped_ffn")
         y_shared = None
         if self.ws13 is not None:
