@@ -66,6 +66,9 @@ enum {
 };
 
 enum { SEMMOE_F32 = 0, SEMMOE_BF16 = 1 };
+/* Router-weight type only: an fp32 router weight already split into three
+ * bf16 parts by semmoe_route_split_weight() (bf16 activations, H % 8 == 0). */
+enum { SEMMOE_F32_SPLIT = 2 };
 
 /* Device error word bits reported through semmoe_check_errors(). */
 enum {
@@ -135,6 +138,20 @@ int semmoe_route(const void* x, int x_dtype, const void* w_router, int w_dtype,
                  const int32_t* k_per_token, int k_uniform,
                  int T, int H, int E, int k_max,
                  int32_t* topk_idx, float* topk_w, void* ws, size_t ws_bytes, void* stream);
+
+/*
+ * semmoe_route_split_weight -- the form of an fp32 router weight that the
+ * tensor-core router multiplies: each value split exactly into three bf16
+ * parts (hi + mid + lo), stacked per pass of experts.  semmoe_route and
+ * semmoe_route_hier do this split on every call for w_dtype = SEMMOE_F32; a
+ * caller whose router weight does not change passes the split once made, with
+ * w_dtype = SEMMOE_F32_SPLIT, and saves that work.  Same results, bit for bit.
+ *
+ * w      [device] [E,H] fp32;  split [device] semmoe_route_split_size(H, E)
+ *        bytes out (256-byte aligned).  Limits: H % 8 == 0, 1 <= E <= 256.
+ */
+size_t semmoe_route_split_size(int H, int E);
+int semmoe_route_split_weight(const float* w, int H, int E, void* split, void* stream);
 
 /*
  * semmoe_route_hier -- MoE-Prism's training-free hierarchical gating over

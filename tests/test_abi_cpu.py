@@ -131,6 +131,17 @@ def test_schedule_validation(lib):
     assert rc == 1 and "null" in _err(lib)
 
 
+def test_router_split_validation(lib):
+    p = ctypes.c_void_p(256)
+    assert lib.semmoe_route_split_size(2048, 64) > 0
+    assert lib.semmoe_route_split_size(2047, 64) == 0
+    rc = lib.semmoe_route_split_weight(p, 100, 8, p, None)
+    assert rc == 1 and "multiple of 8" in _err(lib)
+    # a pre-split weight needs bf16 activations
+    rc = lib.semmoe_route(p, 0, p, 2, None, None, None, 2, 16, 64, 8, 2, p, p, p, 1 << 20, None)
+    assert rc == 1 and "dtype" in _err(lib)
+
+
 def test_product_path_fails_loudly_without_library(monkeypatch):
     from token_expert_routing_gb300 import _abi
     monkeypatch.setattr(_abi, "LIB_PATH", "/nonexistent/libsemmoe.so")

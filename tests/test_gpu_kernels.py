@@ -328,3 +328,26 @@ def test_grouped_ffn_gather_matches_permuted(dtype, T, E, k_max, H, I, monkeypat
         abi().semmoe_grouped_ffn_gather(x, s2p, k_max, T, eo, p2e, w13, w2, P, E, H, I, y1, fws)
         assert abi().semmoe_check_errors() == 0
         assert torch.equal(y0.cpu(), y1.cpu())
+
+
+@pytest.mark.parametrize("T,H,E", [(4096, 2048, 64), (300, 512, 256), (77, 200, 7)])
+def test_route_with_presplit_weight_is_identical(T, H, E):
+    """An fp32 router weight split once (semmoe_route_split_weight) and passed
+    as SEMMOE_F32_SPLIT routes exactly as the weight split on every call."""
+    rng = np.random.default_rng(T + E)
+    x = torch.from_numpy((rng.standard_normal((T, H)) / np.sqrt(H)).astype(np.float32)).to(torch.bfloat16).cuda()
+    wr = torch.from_numpy((rng.standard_normal((E, H)) / np.sqrt(H)).astype(np.float32)).cuda()
+    k_max = min(6, E)
+    outs = []
+    split = torch.empty(abi().semmoe_route_split_size(H, E), dtype=torch.uint8, device="cuda")
+    abi().semmoe_route_split_weight(wr, H, E, split)
+    for w, wd in ((wr, None), (split, abi().SEMMOE_F32_SPLIT)):
+        idx = torch.empty(T, k_max, **i32)
+        gw = torch.empty(T, k_max, dtype=torch.float32, device="cuda")
+        lg = torch.empty(T, E, dtype=torch.float32, device="cuda")
+        abi().semmoe_route(x, w, None, lg, None, k_max, T, H, E, k_max, idx, gw, w_dtype=wd)
+        assert abi().semmoe_check_errors() == 0
+        outs.append((lg.cpu(), idx.cpu(), gw.cpu()))
+    for a, b in zip(*outs):
+        assert torch.equal(a, b)
+    assert max_rel(np_(outs[0][0]), oracle.router_logits(x, wr)) < LOGIT_TOL

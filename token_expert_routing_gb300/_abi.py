@@ -18,6 +18,7 @@ LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libsemmoe.s
 SEMMOE_OK, SEMMOE_ERR_INVALID_ARG, SEMMOE_ERR_UNSUPPORTED, SEMMOE_ERR_CUDA, \
     SEMMOE_ERR_DEVICE_CHECK, SEMMOE_ERR_DEVICE_TIMEOUT = range(6)
 SEMMOE_F32, SEMMOE_BF16 = 0, 1
+SEMMOE_F32_SPLIT = 2   # router weight only: the output of semmoe_route_split_weight
 # device error word bits (semmoe_check_errors)
 SEMMOE_DEVERR_EXPERT, SEMMOE_DEVERR_TOKEN_ID, SEMMOE_DEVERR_LUT, SEMMOE_DEVERR_K, SEMMOE_DEVERR_PAIRS, \
     SEMMOE_DEVERR_TIMEOUT, SEMMOE_DEVERR_NONFINITE, SEMMOE_DEVERR_OFFSETS, SEMMOE_DEVERR_RANK = \
@@ -35,6 +36,8 @@ SIGNATURES = {
     "semmoe_check_errors": (_i, [_vp, ctypes.POINTER(_i)]),
     "semmoe_route_workspace_size": (_sz, [_i, _i, _i, _i, _i]),
     "semmoe_route": (_i, [_vp, _i, _vp, _i, _vp, _vp, _vp, _i, _i, _i, _i, _i, _vp, _vp, _vp, _sz, _vp]),
+    "semmoe_route_split_size": (_sz, [_i, _i]),
+    "semmoe_route_split_weight": (_i, [_vp, _i, _i, _vp, _vp]),
     "semmoe_route_hier_workspace_size": (_sz, [_i, _i, _i, _i, _i]),
     "semmoe_route_hier": (_i, [_vp, _i, _vp, _i, _vp, _vp, _vp, _i, _vp, _i, _i, _i, _i, _i, _vp, _vp, _vp, _sz,
                                _vp]),
@@ -141,11 +144,12 @@ def semmoe_route_workspace_size(T, H, E, x_dtype: int, w_dtype: int) -> int:
 
 
 def semmoe_route(x, w_router, logits_in, logits_out, k_per_token, k_uniform, T, H, E, k_max,
-                 topk_idx, topk_w, ws=None, stream=None):
+                 topk_idx, topk_w, ws=None, stream=None, w_dtype=None):
     """Router GEMM + top-k.  ``ws`` defaults to a fresh workspace of the size
-    the library asks for (pass one to avoid the allocation)."""
+    the library asks for (pass one to avoid the allocation); ``w_dtype`` =
+    SEMMOE_F32_SPLIT when w_router holds the output of semmoe_route_split_weight."""
     xd = dtype_code(x) if x is not None else SEMMOE_F32
-    wd = dtype_code(w_router) if w_router is not None else SEMMOE_F32
+    wd = w_dtype if w_dtype is not None else (dtype_code(w_router) if w_router is not None else SEMMOE_F32)
     if ws is None:
         n = semmoe_route_workspace_size(T, max(H, 1), E, xd, wd)
         ws = torch.empty(n, dtype=torch.uint8, device=topk_idx.device)
@@ -154,16 +158,24 @@ def semmoe_route(x, w_router, logits_in, logits_out, k_per_token, k_uniform, T, 
                               _p(ws), ws.numel() * ws.element_size(), _stream(stream)))
 
 
+def semmoe_route_split_size(H, E) -> int:
+    return lib().semmoe_route_split_size(H, E)
+
+
+def semmoe_route_split_weight(w, H, E, split, stream=None):
+    _check(lib().semmoe_route_split_weight(_p(w), H, E, _p(split), _stream(stream)))
+
+
 def semmoe_route_hier_workspace_size(T, H, Ep, x_dtype: int, w_dtype: int) -> int:
     return lib().semmoe_route_hier_workspace_size(T, H, Ep, x_dtype, w_dtype)
 
 
 def semmoe_route_hier(x, w_parent, logits_in, logits_out, sub_logw, N, k_per_token, k_uniform, T, H, Ep, k_max,
-                      topk_idx, topk_w, ws=None, stream=None):
+                      topk_idx, topk_w, ws=None, stream=None, w_dtype=None):
     """Hierarchical sub-expert routing.  ``ws`` defaults to a fresh workspace
-    of the size the library asks for."""
+    of the size the library asks for; ``w_dtype`` as in semmoe_route."""
     xd = dtype_code(x) if x is not None else SEMMOE_F32
-    wd = dtype_code(w_parent) if w_parent is not None else SEMMOE_F32
+    wd = w_dtype if w_dtype is not None else (dtype_code(w_parent) if w_parent is not None else SEMMOE_F32)
     if ws is None:
         n = semmoe_route_hier_workspace_size(T, max(H, 1), Ep, xd, wd)
         ws = torch.empty(n, dtype=torch.uint8, device=topk_idx.device)

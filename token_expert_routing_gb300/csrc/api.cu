@@ -30,6 +30,11 @@ int cuda_status(cudaError_t e, const char* where) {
 
 bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 bool valid_dtype(int d) { return d == SEMMOE_F32 || d == SEMMOE_BF16; }
+// Router weights may also come as the split of an fp32 weight, for bf16
+// activations with 16-byte rows (the tensor-core router).
+bool valid_router_dtype(int w, int x, int H) {
+  return valid_dtype(w) || (w == SEMMOE_F32_SPLIT && x == SEMMOE_BF16 && H % 8 == 0);
+}
 size_t elem_size(int d) { return d == SEMMOE_BF16 ? 2 : 4; }
 
 // The kernels are built for sm_103a only.
@@ -86,7 +91,7 @@ int semmoe_check_errors(void* stream, int* bits) {
 }
 
 size_t semmoe_route_workspace_size(int T, int H, int E, int x_dtype, int w_dtype) {
-  if (T < 0 || H < 1 || E < 1 || !valid_dtype(x_dtype) || !valid_dtype(w_dtype)) return 0;
+  if (T < 0 || H < 1 || E < 1 || !valid_dtype(x_dtype) || !valid_router_dtype(w_dtype, x_dtype, H)) return 0;
   const size_t b = route_ws_bytes(T, H, E, x_dtype, w_dtype);
   return b > 0 ? b : 256;
 }
@@ -104,7 +109,8 @@ int semmoe_route(const void* x, int x_dtype, const void* w_router, int w_dtype, 
   REQUIRE(topk_idx != nullptr && topk_w != nullptr, "semmoe_route: null output pointer");
   if (logits_in == nullptr) {
     REQUIRE(x != nullptr && w_router != nullptr, "semmoe_route: null x or w_router without logits_in");
-    REQUIRE(valid_dtype(x_dtype) && valid_dtype(w_dtype), "semmoe_route: bad dtype (%d, %d)", x_dtype, w_dtype);
+    REQUIRE(valid_dtype(x_dtype) && valid_router_dtype(w_dtype, x_dtype, H), "semmoe_route: bad dtype (%d, %d)",
+            x_dtype, w_dtype);
     REQUIRE(H >= 1, "semmoe_route: H = %d < 1", H);
     REQUIRE(aligned(x, 16) && aligned(w_router, 16), "semmoe_route: x and w_router must be 16-byte aligned");
     const size_t need = route_ws_bytes(T, H, E, x_dtype, w_dtype);
@@ -121,8 +127,23 @@ int semmoe_route(const void* x, int x_dtype, const void* w_router, int w_dtype, 
                      "semmoe_route");
 }
 
+size_t semmoe_route_split_size(int H, int E) {
+  if (H < 8 || H % 8 != 0 || E < 1 || E > 256) return 0;
+  return route_split_size(H, E);
+}
+
+int semmoe_route_split_weight(const float* w, int H, int E, void* split, void* stream) {
+  REQUIRE(H >= 8 && H % 8 == 0, "semmoe_route_split_weight: H = %d must be a positive multiple of 8", H);
+  REQUIRE(E >= 1 && E <= 256, "semmoe_route_split_weight: E = %d outside [1, 256]", E);
+  REQUIRE(w != nullptr && split != nullptr, "semmoe_route_split_weight: null pointer");
+  REQUIRE(aligned(w, 4) && aligned(split, 256), "semmoe_route_split_weight: misaligned pointer");
+  CHECK_DEVICE("semmoe_route_split_weight");
+  return cuda_status(launch_route_split(w, H, E, split, static_cast<cudaStream_t>(stream)),
+                     "semmoe_route_split_weight");
+}
+
 size_t semmoe_route_hier_workspace_size(int T, int H, int Ep, int x_dtype, int w_dtype) {
-  if (T < 0 || H < 1 || Ep < 1 || !valid_dtype(x_dtype) || !valid_dtype(w_dtype)) return 0;
+  if (T < 0 || H < 1 || Ep < 1 || !valid_dtype(x_dtype) || !valid_router_dtype(w_dtype, x_dtype, H)) return 0;
   const size_t b = route_hier_ws_bytes(T, H, Ep, x_dtype, w_dtype);
   return b > 0 ? b : 256;
 }
@@ -143,7 +164,8 @@ int semmoe_route_hier(const void* x, int x_dtype, const void* w_parent, int w_dt
   REQUIRE(topk_idx != nullptr && topk_w != nullptr && sub_logw != nullptr, "semmoe_route_hier: null pointer");
   if (logits_in == nullptr) {
     REQUIRE(x != nullptr && w_parent != nullptr, "semmoe_route_hier: null x or w_parent without logits_in");
-    REQUIRE(valid_dtype(x_dtype) && valid_dtype(w_dtype), "semmoe_route_hier: bad dtype (%d, %d)", x_dtype, w_dtype);
+    REQUIRE(valid_dtype(x_dtype) && valid_router_dtype(w_dtype, x_dtype, H), "semmoe_route_hier: bad dtype (%d, %d)",
+            x_dtype, w_dtype);
     REQUIRE(H >= 1, "semmoe_route_hier: H = %d < 1", H);
     REQUIRE(aligned(x, 16) && aligned(w_parent, 16), "semmoe_route_hier: x and w_parent must be 16-byte aligned");
     const size_t need = route_hier_ws_bytes(T, H, Ep, x_dtype, w_dtype);

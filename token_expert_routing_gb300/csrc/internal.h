@@ -21,6 +21,8 @@ size_t route_ws_bytes(int T, int H, int E, int x_dtype, int w_dtype);
 // Tensor-core router (route_tc.cu): fp32 logits of bf16 activations.
 int route_tc_take_errors(cudaStream_t s, int* bits);
 size_t route_tc_split_bytes(int H, int E, int w_dtype);
+size_t route_split_size(int H, int E);
+cudaError_t launch_route_split(const float* w, int H, int E, void* split, cudaStream_t s);
 int route_tc_k_slices(int T, int H, int E, int w_dtype);
 cudaError_t launch_route_logits_tc(const void* x, const void* w, int w_dtype, int T, int H, int E, float* partials,
                                    int ks, void* split, cudaStream_t s);

@@ -192,9 +192,14 @@ route_tc_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_constant
 
 int route_tc_take_errors(cudaStream_t s, int* bits) { return take_error_word(g_err, s, bits); }
 
-// Workspace of the tensor-core router: the three-part split of an fp32 weight.
+// Workspace of the tensor-core router: the three-part split of an fp32 weight
+// (none when the caller passes the split already made).
 size_t route_tc_split_bytes(int H, int E, int w_dtype) {
   if (w_dtype != SEMMOE_F32) return 0;
+  return route_split_size(H, E);
+}
+
+size_t route_split_size(int H, int E) {
   const int EC = experts_per_pass(E, 3), n_pass = (E + EC - 1) / EC;
   return align_up((size_t)n_pass * 3 * EC * H * 2, 256);
 }
@@ -202,7 +207,7 @@ size_t route_tc_split_bytes(int H, int E, int w_dtype) {
 // K slices of the router GEMM: enough (token tile, pass, slice) CTAs to fill
 // the GPU once, with at least 4 k-blocks of H per slice.
 int route_tc_k_slices(int T, int H, int E, int w_dtype) {
-  const int S = w_dtype == SEMMOE_F32 ? 3 : 1;
+  const int S = w_dtype == SEMMOE_BF16 ? 1 : 3;
   const int EC = experts_per_pass(E, S), n_pass = (E + EC - 1) / EC;
   const long long ctas = (long long)((T + BM - 1) / BM) * n_pass;
   const int kb_all = (H + BK - 1) / BK;
@@ -212,12 +217,23 @@ int route_tc_k_slices(int T, int H, int E, int w_dtype) {
   return ks < 1 ? 1 : ks;
 }
 
-// x [T,H] bf16 (H % 8 == 0); w [E,H] fp32 or bf16; partials [ks][T][E] fp32
-// out (ks = route_tc_k_slices(); the logits are their sum in slice order);
-// split: workspace of route_tc_split_bytes() (fp32 weight only).
+cudaError_t launch_route_split(const float* w, int H, int E, void* split, cudaStream_t s) {
+  const int EC = experts_per_pass(E, 3), n_pass = (E + EC - 1) / EC;
+  const long long total = (long long)n_pass * 3 * EC * H;
+  long long blocks = (total + 255) / 256;
+  if (blocks > 4096) blocks = 4096;
+  split_router_kernel<<<(int)blocks, 256, 0, s>>>(w, E, H, EC, n_pass, static_cast<__nv_bfloat16*>(split));
+  count_launches(1);
+  return cudaGetLastError();
+}
+
+// x [T,H] bf16 (H % 8 == 0); w [E,H] fp32 or bf16, or the split of an fp32
+// weight (SEMMOE_F32_SPLIT); partials [ks][T][E] fp32 out (ks =
+// route_tc_k_slices(); the logits are their sum in slice order); split:
+// workspace of route_tc_split_bytes() (fp32 weight only).
 cudaError_t launch_route_logits_tc(const void* x, const void* w, int w_dtype, int T, int H, int E, float* partials,
                                    int ks, void* split, cudaStream_t s) {
-  const int S = w_dtype == SEMMOE_F32 ? 3 : 1;
+  const int S = w_dtype == SEMMOE_BF16 ? 1 : 3;
   const int EC = experts_per_pass(E, S), n_pass = (E + EC - 1) / EC;
   const int kb_all = (H + BK - 1) / BK;
   const int kb_per_slice = (kb_all + ks - 1) / ks;
@@ -225,15 +241,11 @@ cudaError_t launch_route_logits_tc(const void* x, const void* w, int w_dtype, in
   const void* wb = w;
   int w_rows = E;
   if (S == 3) {
-    const long long total = (long long)n_pass * 3 * EC * H;
-    long long blocks = (total + 255) / 256;
-    if (blocks > 4096) blocks = 4096;
-    split_router_kernel<<<(int)blocks, 256, 0, s>>>(static_cast<const float*>(w), E, H, EC, n_pass,
-                                                    static_cast<__nv_bfloat16*>(split));
-    count_launches(1);
-    cudaError_t e = cudaGetLastError();
-    if (e != cudaSuccess) return e;
-    wb = split;
+    if (w_dtype == SEMMOE_F32) {
+      cudaError_t e = launch_route_split(static_cast<const float*>(w), H, E, split, s);
+      if (e != cudaSuccess) return e;
+      wb = split;
+    }
     w_rows = n_pass * 3 * EC;
   }
   CUtensorMap mx, mw;

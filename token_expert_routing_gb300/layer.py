@@ -73,6 +73,21 @@ class MoELayer:
         self.dtype = self.w13.dtype
         self.device = dev
         self._ws = {}
+        # An fp32 router weight meeting bf16 activations is split into its three
+        # bf16 parts once here instead of on every call.
+        self.w_route, self.w_route_dtype = self.w_router, abi.dtype_code(self.w_router)
+        if self.w_router.dtype == torch.float32 and self.dtype == torch.bfloat16 and self.H % 8 == 0:
+            n = abi.semmoe_route_split_size(self.H, self.Ep)
+            self.w_route = torch.empty(n, dtype=torch.uint8, device=dev)
+            abi.semmoe_route_split_weight(self.w_router, self.H, self.Ep, self.w_route)
+            self.w_route_dtype = abi.SEMMOE_F32_SPLIT
+
+    def _router_weight(self, x):
+        """The router weight to pass with x, and its type code (the pre-split
+        fp32 weight when x is bf16)."""
+        if self.w_route_dtype == abi.SEMMOE_F32_SPLIT and x.dtype != torch.bfloat16:
+            return self.w_router, abi.dtype_code(self.w_router)
+        return self.w_route, self.w_route_dtype
 
     def _workspace(self, key, nbytes):
         buf = self._ws.get(key)
@@ -118,15 +133,15 @@ class MoELayer:
         topk_idx = torch.empty(T, k_max, **i32)
         topk_w = torch.empty(T, k_max, dtype=torch.float32, device=dev)
         if self.sub_logw is None:
-            ws = self._workspace("route", abi.semmoe_route_workspace_size(
-                T, H, E, abi.dtype_code(x), abi.dtype_code(self.w_router)))
-            abi.semmoe_route(x, self.w_router, logits_in, logits, k_per_token, k or 0, T, H, E, k_max,
-                             topk_idx, topk_w, ws, stream)
+            wr, wd = self._router_weight(x)
+            ws = self._workspace("route", abi.semmoe_route_workspace_size(T, H, E, abi.dtype_code(x), wd))
+            abi.semmoe_route(x, wr, logits_in, logits, k_per_token, k or 0, T, H, E, k_max,
+                             topk_idx, topk_w, ws, stream, w_dtype=wd)
         else:
-            ws = self._workspace("route", abi.semmoe_route_hier_workspace_size(
-                T, H, Ep, abi.dtype_code(x), abi.dtype_code(self.w_router)))
-            abi.semmoe_route_hier(x, self.w_router, logits_in, logits, self.sub_logw, E // Ep, k_per_token,
-                                  k or 0, T, H, Ep, k_max, topk_idx, topk_w, ws, stream)
+            wr, wd = self._router_weight(x)
+            ws = self._workspace("route", abi.semmoe_route_hier_workspace_size(T, H, Ep, abi.dtype_code(x), wd))
+            abi.semmoe_route_hier(x, wr, logits_in, logits, self.sub_logw, E // Ep, k_per_token,
+                                  k or 0, T, H, Ep, k_max, topk_idx, topk_w, ws, stream, w_dtype=wd)
         mark("route")
         pred = torch.empty(T, **i32)
         abi.semmoe_affinity_lookup(token_ids, self.lut, self.V, R, T, pred, stream)
