@@ -50,7 +50,8 @@ class MoELayer:
     """
 
     def __init__(self, w_router, w13, w2, expert_rank, lut, R: int, k_max: int, ws13=None, ws2=None,
-                 trans=None, sub_logw=None, fused_gather: bool = False, device="cuda"):
+                 trans=None, sub_logw=None, fused_gather: bool = False, overlap: bool = True,
+                 overlap_shared: bool = True, device="cuda"):
         dev = torch.device(device)
         c = lambda t: None if t is None else t.to(dev).contiguous()  # noqa: E731
         self.w_router, self.w13, self.w2 = c(w_router), c(w13), c(w2)
@@ -63,6 +64,12 @@ class MoELayer:
         # and no x_perm is written; bit-identical, but slower on this hardware
         # (32 four-row gathers per A tile and k-block), so off by default
         self.fused_gather = fused_gather
+        # overlap: the lookup, scheduling and counting steps (nothing later in
+        # the layer reads them) run on a second stream beside the permute and
+        # the FFN; overlap_shared: the shared experts' FFN runs there too,
+        # beside the routed FFN
+        self.overlap, self.overlap_shared = overlap, overlap_shared
+        self._side = None
         self.E, twoI, self.H = self.w13.shape
         self.I = twoI // 2
         self.I_s = 0 if ws13 is None else self.ws13.shape[0] // 2
@@ -96,9 +103,14 @@ class MoELayer:
             self._ws[key] = buf
         return buf
 
+    def _side_stream(self):
+        if self._side is None:
+            self._side = torch.cuda.Stream(device=self.device)
+        return self._side
+
     def forward(self, x, token_ids, k_per_token=None, k: Optional[int] = None, P: Optional[int] = None,
                 logits_in=None, keep_logits: bool = False, stream=None, marks=None,
-                req_offsets=None) -> LayerOutput:
+                req_offsets=None, side_marks=None) -> LayerOutput:
         """x [T,H] (activation type) and token_ids [T] int32 on the device.
 
         Budgets: ``k`` for every token, or ``k_per_token`` [T] int32 on the device
@@ -107,15 +119,37 @@ class MoELayer:
         given, requests are scheduled onto ranks by affinity and each token's
         source rank for the remote count is its request's rank.
         ``marks``: optional list; a CUDA event is recorded on the stream after
-        each step and appended as (step name, event), for per-step timing.
+        each step and appended as (step name, event), for per-step timing;
+        ``side_marks`` gets (step name, start event, end event) for the steps
+        run on the second stream.  Every step has finished on ``stream`` when
+        the work enqueued by this call has.
         """
         s = torch.cuda.current_stream() if stream is None else stream
+        side = self._side_stream() if (self.overlap or self.overlap_shared) else None
 
         def mark(name):
             if marks is not None:
                 ev = torch.cuda.Event(enable_timing=True)
                 ev.record(s)
                 marks.append((name, ev))
+
+        forked = []
+
+        def fork():
+            ev = torch.cuda.Event()
+            ev.record(s)
+            side.wait_event(ev)
+            forked.append(ev)
+
+        def join():
+            ev = torch.cuda.Event()
+            ev.record(side)
+            s.wait_event(ev)
+
+        def side_event():
+            ev = torch.cuda.Event(enable_timing=True)
+            ev.record(side)
+            return ev
 
         mark("start")
         T = x.shape[0]
@@ -143,8 +177,13 @@ class MoELayer:
             abi.semmoe_route_hier(x, wr, logits_in, logits, self.sub_logw, E // Ep, k_per_token,
                                   k or 0, T, H, Ep, k_max, topk_idx, topk_w, ws, stream, w_dtype=wd)
         mark("route")
+        ts = s
+        if self.overlap:  # lookup .. counts on the second stream
+            fork()
+            ts = side
+            ev0 = side_event() if side_marks is not None else None
         pred = torch.empty(T, **i32)
-        abi.semmoe_affinity_lookup(token_ids, self.lut, self.V, R, T, pred, stream)
+        abi.semmoe_affinity_lookup(token_ids, self.lut, self.V, R, T, pred, ts)
         src = pred
         sched = None
         if req_offsets is not None:
@@ -155,17 +194,21 @@ class MoELayer:
                          tok_rank=torch.empty(T, **i32), rank_tok_offsets=torch.empty(R + 1, **i32))
             abi.semmoe_dp_schedule(pred, req_offsets, T, n_req, R, sched["hist"], sched["req_rank"],
                                    sched["req_order"], sched["rank_req_offsets"], sched["req_tok_start"],
-                                   sched["tok_order"], sched["tok_rank"], sched["rank_tok_offsets"], stream)
+                                   sched["tok_order"], sched["tok_rank"], sched["rank_tok_offsets"], ts)
             src = sched["tok_rank"]
         pred_next = None
         if self.trans is not None:
             pred_next = torch.empty(T, **i32)
             abi.semmoe_transition_lookup(topk_idx, k_per_token, k or 0, self.trans, T, k_max, E, R, pred_next,
-                                         stream)
+                                         ts)
         counts = torch.empty(R, R, **i32)
         remote = torch.empty(R, **i32)
-        abi.semmoe_remote_count(topk_idx, src, self.expert_rank, T, k_max, E, R, counts, remote, stream)
-        mark("lookup_count")
+        abi.semmoe_remote_count(topk_idx, src, self.expert_rank, T, k_max, E, R, counts, remote, ts)
+        if self.overlap:
+            if side_marks is not None:
+                side_marks.append(("lookup_count", ev0, side_event()))
+        else:
+            mark("lookup_count")
         expert_offsets = torch.empty(E + 1, **i32)
         rank_offsets = torch.empty(R + 1, **i32)
         phys_to_expert = torch.empty(E, **i32)
@@ -180,6 +223,16 @@ class MoELayer:
         mark("permute")
         y_perm = torch.empty(P, H, dtype=x.dtype, device=dev)
         dcode = abi.dtype_code(self.w13)
+        y_shared = None
+        shared_side = self.ws13 is not None and self.overlap_shared
+        if shared_side:  # the shared experts beside the routed FFN
+            y_shared = torch.empty(T, H, dtype=x.dtype, device=dev)
+            wss = self._workspace("shared", abi.semmoe_shared_ffn_workspace_size(T, self.I_s, dcode))
+            fork()
+            ev1 = side_event() if side_marks is not None else None
+            abi.semmoe_shared_ffn(x, self.ws13, self.ws2, T, H, self.I_s, y_shared, wss, side)
+            if side_marks is not None:
+                side_marks.append(("shared_ffn", ev1, side_event()))
         ws = self._workspace("ffn", abi.semmoe_grouped_ffn_workspace_size(P, I, dcode))
         if self.fused_gather:
             abi.semmoe_grouped_ffn_gather(x, sorted_to_pair, k_max, T, expert_offsets, phys_to_expert, self.w13,
@@ -188,12 +241,13 @@ class MoELayer:
             abi.semmoe_grouped_ffn(x_perm, expert_offsets, phys_to_expert, self.w13, self.w2, P, E, H, I,
                                    y_perm, ws, stream)
         mark("grouped_ffn")
-        y_shared = None
-        if self.ws13 is not None:
+        if self.ws13 is not None and not shared_side:
             y_shared = torch.empty(T, H, dtype=x.dtype, device=dev)
             ws = self._workspace("shared", abi.semmoe_shared_ffn_workspace_size(T, self.I_s, dcode))
             abi.semmoe_shared_ffn(x, self.ws13, self.ws2, T, H, self.I_s, y_shared, ws, stream)
             mark("shared_ffn")
+        if forked:
+            join()  # the second stream's steps are done before the combine (and the call's end)
         out = torch.empty(T, H, dtype=x.dtype, device=dev)
         abi.semmoe_combine(y_perm, pair_to_sorted, topk_w, y_shared, T, H, k_max, P, out, stream)
         mark("combine")
