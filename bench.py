@@ -320,8 +320,13 @@ def run_ours(args, world, rank, local):
     torch.cuda.set_device(dev)
     spec = wl.CONFIGS[args.config]
     d = wl.make_inputs(spec)
+    # the layer as a user runs it (its steps spread over two streams), and the
+    # same layer with every step on one stream, whose per-step events give the
+    # stage times and the roofline of each kernel alone
     layer = MoELayer(d["w_router"], d["w13"], d["w2"], d["expert_rank"], d["lut"], spec.R, spec.k_max,
                      d["ws13"], d["ws2"], device=dev)
+    serial = MoELayer(d["w_router"], d["w13"], d["w2"], d["expert_rank"], d["lut"], spec.R, spec.k_max,
+                      d["ws13"], d["ws2"], overlap=False, overlap_shared=False, device=dev)
     x = d["x"].to(dev)
     ids = d["token_ids"].to(dev)
     per_token = bool(spec.k_choices)
@@ -331,7 +336,7 @@ def run_ours(args, world, rank, local):
     stream = torch.cuda.current_stream(dev)
 
     def step(marks=None, side_marks=None):
-        return layer.forward(x, ids, kpt, k, P, stream=stream, marks=marks, side_marks=side_marks)
+        return serial.forward(x, ids, kpt, k, P, stream=stream, marks=marks, side_marks=side_marks)
 
     for _ in range(args.warmup):
         step()
@@ -390,38 +395,53 @@ def run_ours(args, world, rank, local):
         _abi.semmoe_check_errors()
         graph = {"value": spec.T * args.steps * world / (g_ms * 1e-3), "unit": "tokens/s",
                  "ms_per_step": g_ms / args.steps,
-                 "how": "CapturedLayer: the whole forward captured once as a CUDA graph, one replay per step",
+                 "how": "CapturedLayer: the whole forward (steps on two streams: bookkeeping and the shared "
+                        "experts beside the permute and routed FFN) captured once as a CUDA graph, one replay "
+                        "per step",
                  "clocks": clocks_graph.summary()}
         del cap
 
-    # end to end through the public API: pinned host inputs in, host output back
-    e2e = None
+    # end to end through the public API: pinned host inputs in, host output back,
+    # every step (GraphPipeline: one graph replay per step; HostPipeline: eager)
+    e2e = e2e_eager = None
     if not args.no_e2e:
+        from token_expert_routing_gb300 import GraphPipeline, HostPipeline
         x_h = d["x"].pin_memory()
         ids_h = d["token_ids"].pin_memory()
         k_h = d["k_per_token"].pin_memory() if per_token else None
-        out_h = torch.empty(spec.T, spec.H, dtype=d["x"].dtype).pin_memory()
-        from token_expert_routing_gb300 import HostPipeline
-        pipe = HostPipeline(layer, stream=stream)
         outs = [torch.empty(spec.T, spec.H, dtype=d["x"].dtype).pin_memory() for _ in range(2)]
-        for i in range(args.warmup):
-            pipe.submit(x_h, ids_h, outs[i % 2], k_h, k)
-        pipe.synchronize()
-        _barrier(world)
-        torch.cuda.synchronize(dev)
-        t0 = time.perf_counter()           # wall clock: the copies run on their own stream
-        for i in range(args.steps):
-            pipe.submit(x_h, ids_h, outs[i % 2], k_h, k)
-        pipe.synchronize()
-        e2e_ms = _max_over_ranks(world, (time.perf_counter() - t0) * 1e3)
-        out_h = outs[0]
         h2d = x_h.numel() * x_h.element_size() + ids_h.numel() * 4 + (k_h.numel() * 4 if per_token else 0)
-        d2h = out_h.numel() * out_h.element_size()
-        e2e = {"value": spec.T * args.steps * world / (e2e_ms * 1e-3), "unit": "tokens/s",
-               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-               "how": "HostPipeline.submit per step (pinned inputs in, output back), uploads and readbacks "
-                      "overlapped with compute across steps; host wall clock from the first submit to the "
-                      "last readback"}
+        d2h = outs[0].numel() * outs[0].element_size()
+
+        def run_pipe(submit, sync):
+            for i in range(args.warmup):
+                submit(i)
+            sync()
+            _barrier(world)
+            torch.cuda.synchronize(dev)
+            t0 = time.perf_counter()           # wall clock: the copies run on their own stream
+            for i in range(args.steps):
+                submit(i)
+            sync()
+            return _max_over_ranks(world, (time.perf_counter() - t0) * 1e3)
+
+        pipe = HostPipeline(layer, stream=stream)
+        ms_e = run_pipe(lambda i: pipe.submit(x_h, ids_h, outs[i % 2], k_h, k), pipe.synchronize)
+        e2e_eager = {"value": spec.T * args.steps * world / (ms_e * 1e-3), "unit": "tokens/s",
+                     "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                     "how": "HostPipeline.submit per step: eager forward, uploads and readbacks on a copy stream "
+                            "overlapped with compute; host wall clock"}
+        e2e = e2e_eager
+        if not args.no_graph:
+            gp = GraphPipeline(layer, spec.T, None if per_token else spec.k, d["k_per_token"] if per_token else None,
+                               stream=stream)
+            ms_g = run_pipe(lambda i: gp.submit(x_h, ids_h, outs[i % 2]), gp.synchronize)
+            e2e = {"value": spec.T * args.steps * world / (ms_g * 1e-3), "unit": "tokens/s",
+                   "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                   "how": "GraphPipeline.submit per step (pinned inputs in, output back): one graph replay per "
+                          "step, uploads and readbacks on a copy stream overlapped with compute across steps; "
+                          "host wall clock from the first submit to the last readback"}
+            del gp
 
     around = None if args.no_around else _time_around_layer(args, spec, d, layer, dev, stream)
 
@@ -481,7 +501,8 @@ def run_ours(args, world, rank, local):
 
     total_tokens = spec.T * args.steps * world
     eager = {"value": total_tokens / (ms_max * 1e-3), "unit": "tokens/s", "ms_per_step": ms_max / args.steps,
-             "how": "MoELayer.forward per step (one library call per step of the layer)",
+             "how": "MoELayer.forward per step, its steps serialised on one stream (one library call per step "
+                    "of the layer; per-step events give the stages and the roofline)",
              "clocks": clocks_eager.summary()}
     best = graph if graph is not None and graph["ms_per_step"] < eager["ms_per_step"] else eager
     line = {
@@ -491,6 +512,7 @@ def run_ours(args, world, rank, local):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": spec.dtype,
         "data": "synthetic", "config": _config(spec),
         "e2e": e2e,
+        "e2e_eager": e2e_eager,
         "graph": graph,
         "gpu_launches": launches,
         "host_enqueue_ms_per_step": host_ms,

@@ -94,3 +94,32 @@ def test_host_pipeline_matches_forward():
     for x, o in zip(xs, outs):
         want = layer.forward(x.cuda(), ids.cuda(), k=spec.k).out.cpu()
         assert torch.equal(o, want)
+
+
+@pytest.mark.parametrize("name,over", [("dsv2lite_prefill_T4096", dict(T=512, H=256, I=160, I_shared=320, V=3000)),
+                                       ("prism_subexpert_T8192", dict(T=512, H=256, I=40, V=3000,
+                                                                      tokens_per_request=64))])
+def test_graph_pipeline_matches_forward(name, over):
+    """Host-buffer calls through the two captured graphs return each call's
+    own output (five calls, so both slots are reused), equal to the eager
+    forward; per-token budgets included."""
+    import torch
+    from token_expert_routing_gb300 import GraphPipeline
+    spec = wl.scaled(name, **over)
+    d = wl.make_inputs(spec)
+    layer = _layer(d)
+    per_token = bool(spec.k_choices)
+    gp = GraphPipeline(layer, spec.T, None if per_token else spec.k, d["k_per_token"] if per_token else None)
+    gen = torch.Generator().manual_seed(5)
+    xs = [(d["x"].float() * (0.5 + i) + 0.1 * torch.randn(d["x"].shape, generator=gen)).to(d["x"].dtype)
+          for i in range(5)]
+    idss = [d["token_ids"].roll(i) for i in range(5)]
+    outs = [torch.empty(spec.T, spec.H, dtype=d["x"].dtype).pin_memory() for _ in xs]
+    for x, ids, o in zip(xs, idss, outs):
+        gp.submit(x.pin_memory(), ids.pin_memory(), o)
+    gp.synchronize()
+    kpt = d["k_per_token"].cuda() if per_token else None
+    P = int(d["k_per_token"].sum())
+    for x, ids, o in zip(xs, idss, outs):
+        want = layer.forward(x.cuda(), ids.cuda(), kpt, None if per_token else spec.k, P).out.cpu()
+        assert torch.equal(o, want)

@@ -10,6 +10,6 @@ the library sources (``csrc/``), its build script, the ctypes binding
 """
 from . import _abi  # noqa: F401
 from ._abi import SemMoEError  # noqa: F401
-from .layer import CapturedLayer, HostPipeline, LayerOutput, MoELayer  # noqa: F401
+from .layer import CapturedLayer, GraphPipeline, HostPipeline, LayerOutput, MoELayer  # noqa: F401
 
-__all__ = ["MoELayer", "LayerOutput", "HostPipeline", "CapturedLayer", "SemMoEError"]
+__all__ = ["MoELayer", "LayerOutput", "HostPipeline", "GraphPipeline", "CapturedLayer", "SemMoEError"]

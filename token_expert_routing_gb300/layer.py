@@ -374,3 +374,48 @@ class CapturedLayer:
     def replay(self) -> LayerOutput:
         self.graph.replay()
         return self.result
+
+
+class GraphPipeline:
+    """Host-buffer calls of one batch shape through captured graphs.
+
+    Like ``HostPipeline`` (pinned inputs uploaded and outputs read back on a
+    copy stream, overlapped with the compute of neighbouring calls), but each
+    call's compute is one replay of a ``CapturedLayer``: two of them, one per
+    double-buffer slot, so call i+1's upload lands in the other graph's static
+    inputs while call i runs.  The batch shape and budgets are fixed at
+    construction.  ``synchronize()`` waits for all submitted calls.
+    """
+
+    def __init__(self, layer: MoELayer, T: int, k: Optional[int] = None, k_per_token_host=None, stream=None):
+        self.compute = torch.cuda.current_stream() if stream is None else stream
+        self.copy = torch.cuda.Stream(device=layer.device)
+        self.slots = [CapturedLayer(layer, T, k, k_per_token_host) for _ in range(2)]
+        self._done = [None, None]      # event: the slot's last replay has finished
+        self._slot = 0
+
+    def submit(self, x_host, ids_host, out_host):
+        slot = self._slot
+        self._slot ^= 1
+        cap = self.slots[slot]
+        with torch.cuda.stream(self.copy):
+            if self._done[slot] is not None:
+                self.copy.wait_event(self._done[slot])  # the call two back no longer reads its inputs
+            cap.x.copy_(x_host, non_blocking=True)
+            cap.token_ids.copy_(ids_host, non_blocking=True)
+            uploaded = torch.cuda.Event()
+            uploaded.record(self.copy)
+        self.compute.wait_event(uploaded)
+        with torch.cuda.stream(self.compute):
+            cap.replay()
+            done = torch.cuda.Event()
+            done.record(self.compute)
+        self._done[slot] = done
+        with torch.cuda.stream(self.copy):
+            self.copy.wait_event(done)
+            out_host.copy_(cap.result.out, non_blocking=True)  # before the slot's next upload, on this stream
+        return out_host
+
+    def synchronize(self):
+        self.copy.synchronize()
+        self.compute.synchronize()
