@@ -10,8 +10,8 @@
 //                    starting positions, ranks its pairs stably within the
 //                    chunk (warp match + per-warp bucket counts) and writes
 //                    both maps; CTA 0 writes the bucket and rank tables
-// then perm_gather copies x rows into sorted order (one warp per row,
-// 16-byte vectors).
+// then perm_copy writes each x row to its tokens' sorted rows (one warp per
+// token, 16-byte vectors).
 #include <mutex>
 
 #include "common.cuh"
@@ -208,23 +208,56 @@ perm_scatter_kernel(const int32_t* __restrict__ topk_idx, const int32_t* __restr
   }
 }
 
-// x_perm[q, :] = x[sorted_to_pair[q] / k_max, :], one warp per sorted row.
+// x_perm[pair_to_sorted[t * k_max + j], :] = x[t, :] for every live slot j of
+// token t: one warp per token reads its row once, in segments of up to 4 KB
+// held in registers, and writes each segment to the token's k_t sorted rows.
+// (Walking the sorted rows instead re-reads each x row k_t times, far apart
+// in time, and the row writes push those reads out of L2.)
+constexpr int kSegVec = 8;  // 16-byte vectors per lane per segment: 32 x 8 x 16 B = 4 KB
+
 __global__ void __launch_bounds__(kThreads)
-perm_gather_kernel(const unsigned char* __restrict__ x, const int32_t* __restrict__ sorted_to_pair, int P,
-                   int T, int k_max, int row_bytes, unsigned char* __restrict__ x_perm) {
+perm_copy_kernel(const unsigned char* __restrict__ x, const int32_t* __restrict__ pair_to_sorted, int T, int k_max,
+                 int P, int row_bytes, unsigned char* __restrict__ x_perm) {
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-  for (int q = blockIdx.x * kWarps + warp; q < P; q += gridDim.x * kWarps) {
-    const int p = sorted_to_pair[q];
-    const int t = p / k_max;
-    uint4* dst = reinterpret_cast<uint4*>(x_perm + (size_t)q * row_bytes);
-    if (p < 0 || t >= T) {
-      if (lane == 0) flag(SEMMOE_DEVERR_PAIRS);
-      for (int off = lane; off < row_bytes / 16; off += 32) dst[off] = make_uint4(0, 0, 0, 0);
-      continue;
+  const int n16 = row_bytes / 16;
+  const int kk = k_max < 32 ? k_max : 32;
+  for (int t = blockIdx.x * kWarps + warp; t < T; t += gridDim.x * kWarps) {
+    const int32_t* slots = pair_to_sorted + (size_t)t * k_max;
+    int q_l = -1;
+    if (lane < kk) {
+      q_l = slots[lane];
+      if (q_l >= P) { flag(SEMMOE_DEVERR_PAIRS); q_l = -1; }
     }
     const uint4* src = reinterpret_cast<const uint4*>(x + (size_t)t * row_bytes);
-#pragma unroll 4
-    for (int off = lane; off < row_bytes / 16; off += 32) dst[off] = src[off];
+    for (int seg = 0; seg < n16; seg += 32 * kSegVec) {
+      uint4 v[kSegVec];
+#pragma unroll
+      for (int u = 0; u < kSegVec; ++u) {
+        const int c = seg + u * 32 + lane;
+        if (c < n16) v[u] = src[c];
+      }
+      for (int j = 0; j < kk; ++j) {
+        const int q = __shfl_sync(0xffffffffu, q_l, j);
+        if (q < 0) continue;
+        uint4* dst = reinterpret_cast<uint4*>(x_perm + (size_t)q * row_bytes);
+#pragma unroll
+        for (int u = 0; u < kSegVec; ++u) {
+          const int c = seg + u * 32 + lane;
+          if (c < n16) dst[c] = v[u];
+        }
+      }
+      for (int j = 32; j < k_max; ++j) {  // budgets above 32 experts: read the slot directly
+        const int q = slots[j];
+        if (q < 0) continue;
+        if (q >= P) { if (lane == 0) flag(SEMMOE_DEVERR_PAIRS); continue; }
+        uint4* dst = reinterpret_cast<uint4*>(x_perm + (size_t)q * row_bytes);
+#pragma unroll
+        for (int u = 0; u < kSegVec; ++u) {
+          const int c = seg + u * 32 + lane;
+          if (c < n16) dst[c] = v[u];
+        }
+      }
+    }
   }
 }
 
@@ -258,11 +291,11 @@ cudaError_t launch_permute(const int32_t* topk_idx, const int32_t* expert_rank, 
   count_launches(1);
   if (x != nullptr && x_perm != nullptr && P > 0) {
     const int row_bytes = H * (dtype == SEMMOE_BF16 ? 2 : 4);
-    int blocks = (P + kWarps - 1) / kWarps;
+    int blocks = (T + kWarps - 1) / kWarps;
     const int cap = sm_count() * 16;
     if (blocks > cap) blocks = cap;
-    perm_gather_kernel<<<blocks, kThreads, 0, s>>>(static_cast<const unsigned char*>(x), sorted_to_pair, P, T,
-                                                   k_max, row_bytes, static_cast<unsigned char*>(x_perm));
+    perm_copy_kernel<<<blocks, kThreads, 0, s>>>(static_cast<const unsigned char*>(x), pair_to_sorted, T, k_max, P,
+                                                 row_bytes, static_cast<unsigned char*>(x_perm));
     count_launches(1);
   }
   return cudaGetLastError();
