@@ -204,6 +204,7 @@ ffn_tc_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__
   if (warp == 0) {
     // ---------------- TMA producer (warp 0; lane 0 unless A rows are gathered) ----------------
     uint32_t it = 0;
+    if (gather != nullptr || lane == 0)  // without row gathers lane 0 alone: 1% faster than the warp
     for (int tile = unit0; tile < total; tile += units) {
       if (*abort_flag) break;
       const int mt = tile / n_tiles, nt = tile % n_tiles;
@@ -217,7 +218,7 @@ ffn_tc_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__
         const uint32_t ph = (it / STAGES) & 1;
         int good = 1;
         if (lane == 0) good = mbar_wait(&sh.empty[s], ph ^ 1, abort_flag, &g_err);
-        if (!__shfl_sync(0xffffffffu, good, 0)) { ok = false; break; }
+        if (gather != nullptr ? !__shfl_sync(0xffffffffu, good, 0) : !good) { ok = false; break; }
         if (gather != nullptr) {
           if (lane == 0) mbar_expect_tx(&sh.full[s], STAGE_BYTES);
           tma_gather4(stage_a + s * A_BYTES + lane * 4 * (BK * 2), &map_a, &sh.full[s], kb * BK, src[0], src[1],
@@ -468,6 +469,7 @@ ffn_pair_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant
 
   if (warp == 0) {  // TMA producer (both CTAs): own A rows + own half of B, counted on the leader's barrier
     uint32_t it = 0;
+    if (gather != nullptr || lane == 0)  // without row gathers lane 0 alone: 1% faster than the warp
     for (int tile = unit0; tile < total; tile += units) {
       if (*abort_flag) break;
       const int mt = tile / n_tiles, nt = tile % n_tiles;
@@ -481,7 +483,7 @@ ffn_pair_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant
         const uint32_t ph = (it / P_STAGES) & 1;
         int good = 1;
         if (lane == 0) good = mbar_wait(&sh.empty[s], ph ^ 1, abort_flag, &g_err);
-        if (!__shfl_sync(0xffffffffu, good, 0)) { ok = false; break; }
+        if (gather != nullptr ? !__shfl_sync(0xffffffffu, good, 0) : !good) { ok = false; break; }
         if (lane == 0 && leader) mbar_expect_tx(&sh.full[s], 2 * P_STAGE_BYTES);
         const uint32_t fb = mapa_rank(&sh.full[s], 0);
         unsigned char* st = ring + (size_t)s * P_STAGE_BYTES;
