@@ -279,15 +279,18 @@ class HostPipeline:
 
     Each ``submit`` copies that call's inputs host→device, runs the layer and
     copies ``out`` back into the given host tensor, like ``MoELayer.forward_host``;
-    but uploads and readbacks run on their own stream, double-buffered, so the
-    upload of call i+1 and the readback of call i-1 overlap the compute of
-    call i.  Host tensors should be pinned.  ``synchronize()`` waits for all.
+    but uploads and readbacks run on streams of their own (one each, so a
+    readback waiting for its call never holds up the next upload),
+    double-buffered, so the upload of call i+1 and the readback of call i-1
+    overlap the compute of call i.  Host tensors should be pinned.
+    ``synchronize()`` waits for all.
     """
 
     def __init__(self, layer: MoELayer, stream=None):
         self.layer = layer
         self.compute = torch.cuda.current_stream() if stream is None else stream
-        self.copy = torch.cuda.Stream(device=layer.device)
+        self.copy = torch.cuda.Stream(device=layer.device)     # uploads
+        self.down = torch.cuda.Stream(device=layer.device)     # readbacks
         self._slot = 0
         self._free = [None, None]      # event: slot's device inputs are no longer read
         self._bufs = [None, None]
@@ -322,14 +325,15 @@ class HostPipeline:
             done = torch.cuda.Event()
             done.record(self.compute)
         self._free[slot] = done
-        with torch.cuda.stream(self.copy):
-            self.copy.wait_event(done)
-            res.out.record_stream(self.copy)
+        with torch.cuda.stream(self.down):
+            self.down.wait_event(done)
+            res.out.record_stream(self.down)
             out_host.copy_(res.out, non_blocking=True)
         return out_host
 
     def synchronize(self):
         self.copy.synchronize()
+        self.down.synchronize()
         self.compute.synchronize()
 
 
@@ -389,9 +393,11 @@ class GraphPipeline:
 
     def __init__(self, layer: MoELayer, T: int, k: Optional[int] = None, k_per_token_host=None, stream=None):
         self.compute = torch.cuda.current_stream() if stream is None else stream
-        self.copy = torch.cuda.Stream(device=layer.device)
+        self.copy = torch.cuda.Stream(device=layer.device)     # uploads
+        self.down = torch.cuda.Stream(device=layer.device)     # readbacks
         self.slots = [CapturedLayer(layer, T, k, k_per_token_host) for _ in range(2)]
         self._done = [None, None]      # event: the slot's last replay has finished
+        self._read = [None, None]      # event: the slot's output has been read back
         self._slot = 0
 
     def submit(self, x_host, ids_host, out_host):
@@ -406,16 +412,22 @@ class GraphPipeline:
             uploaded = torch.cuda.Event()
             uploaded.record(self.copy)
         self.compute.wait_event(uploaded)
+        if self._read[slot] is not None:
+            self.compute.wait_event(self._read[slot])  # the call two back's output has been read back
         with torch.cuda.stream(self.compute):
             cap.replay()
             done = torch.cuda.Event()
             done.record(self.compute)
         self._done[slot] = done
-        with torch.cuda.stream(self.copy):
-            self.copy.wait_event(done)
-            out_host.copy_(cap.result.out, non_blocking=True)  # before the slot's next upload, on this stream
+        with torch.cuda.stream(self.down):
+            self.down.wait_event(done)
+            out_host.copy_(cap.result.out, non_blocking=True)
+            read = torch.cuda.Event()
+            read.record(self.down)
+        self._read[slot] = read
         return out_host
 
     def synchronize(self):
         self.copy.synchronize()
+        self.down.synchronize()
         self.compute.synchronize()
