@@ -55,9 +55,10 @@ template <> struct Vec16<__nv_bfloat16> {
 // 0..k_max-1 and are broadcast with shuffles; the rows are fetched JB slots at
 // a time with every load of a batch issued before the first add (padding slots
 // load nothing and leave the sum untouched), so each lane keeps JB * CH
-// 16-byte loads in flight.  CH = 2, JB = 2 at four CTAs per SM measured best
-// (against CH = 2, JB = 4 at three and CH = 4, JB = 4 at two): 64% / 84% / 81% of
-// the HBM copy bandwidth on the DeepSeek / Qwen3 / MoE-Prism shapes.  The sum runs y_shared first, then the slots in
+// 16-byte loads in flight.  CH = 2, JB = 3 at four CTAs per SM measured best of
+// the forms tried (CH x JB x CTAs per SM: 2x2x4, 1x4x4, 1x6x4, 2x3x4, 1x8x3,
+// 2x4x3, 4x4x2): 67% / 89% / 86% of the HBM copy bandwidth on the DeepSeek /
+// Qwen3 / MoE-Prism shapes.  The sum runs y_shared first, then the slots in
 // order, with fmaf.
 template <typename T, int CH, int JB>
 __global__ void __launch_bounds__(kThreads, 4)
@@ -153,7 +154,7 @@ cudaError_t launch_combine(const void* y_perm, const int32_t* pair_to_sorted, co
                            const void* y_shared, int dtype, int T, int H, int k_max, int P, void* out,
                            cudaStream_t s) {
   if (T == 0) return cudaSuccess;
-  constexpr int kCH = 2, kJB = 2;
+  constexpr int kCH = 2, kJB = 3;
   const int vec = dtype == SEMMOE_BF16 ? 8 : 4;
   const long long units = (long long)T * ((H + 32 * vec * kCH - 1) / (32 * vec * kCH));
   long long blocks = (units + kWarps - 1) / kWarps;
