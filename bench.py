@@ -371,6 +371,7 @@ def run_ours(args, world, rank, local):
         for name, a, b in side:
             stage_ms.setdefault(name, []).append(a.elapsed_time(b))
     stage_avg = {n: sum(v) / len(v) for n, v in stage_ms.items()}
+    per_step = sorted(m[0][1].elapsed_time(m[-1][1]) for m in all_marks)  # each eager step, first to last mark
 
     # the same forward as one CUDA-graph replay per step (static buffers)
     graph = None
@@ -384,12 +385,16 @@ def run_ours(args, world, rank, local):
         _barrier(world)
         torch.cuda.synchronize(dev)
         g0, g1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        rep_ev = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps + 1)]
         with ClockSampler(local) as clocks_graph:
             g0.record()
-            for _ in range(args.steps):
+            rep_ev[0].record()
+            for i in range(args.steps):
                 cap.replay()
+                rep_ev[i + 1].record()
             g1.record()
             torch.cuda.synchronize(dev)
+        per_replay = sorted(a.elapsed_time(b) for a, b in zip(rep_ev[:-1], rep_ev[1:]))
         _barrier(world)
         g_ms = _max_over_ranks(world, g0.elapsed_time(g1))
         _abi.semmoe_check_errors()
@@ -398,6 +403,7 @@ def run_ours(args, world, rank, local):
                  "how": "CapturedLayer: the whole forward (steps on two streams: bookkeeping and the shared "
                         "experts beside the permute and routed FFN) captured once as a CUDA graph, one replay "
                         "per step",
+                 "ms_median": per_replay[len(per_replay) // 2], "ms_min": per_replay[0], "ms_max": per_replay[-1],
                  "clocks": clocks_graph.summary()}
         del cap
 
@@ -501,6 +507,7 @@ def run_ours(args, world, rank, local):
 
     total_tokens = spec.T * args.steps * world
     eager = {"value": total_tokens / (ms_max * 1e-3), "unit": "tokens/s", "ms_per_step": ms_max / args.steps,
+             "ms_median": per_step[len(per_step) // 2], "ms_min": per_step[0], "ms_max": per_step[-1],
              "how": "MoELayer.forward per step, its steps serialised on one stream (one library call per step "
                     "of the layer; per-step events give the stages and the roofline)",
              "clocks": clocks_eager.summary()}
