@@ -398,6 +398,16 @@ int semmoe_transition_lookup(const int32_t* topk_idx, const int32_t* k_per_token
                              const float* trans, int T, int k_max, int E, int R, int32_t* pred_next,
                              void* stream);
 
+/*
+ * semmoe_selftest_bounded_wait -- exercises the failure path of the kernels'
+ * waits (not part of the layer; the pages have no counterpart).  It launches
+ * one CTA whose mbarrier wait can never complete; like every wait in the
+ * tensor-core kernels, it gives up after its 2 s bound and sets
+ * SEMMOE_DEVERR_TIMEOUT, so the next semmoe_check_errors() on the stream
+ * returns SEMMOE_ERR_DEVICE_TIMEOUT and the CUDA context stays usable.
+ */
+int semmoe_selftest_bounded_wait(void* stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -351,3 +351,19 @@ def test_route_with_presplit_weight_is_identical(T, H, E):
     for a, b in zip(*outs):
         assert torch.equal(a, b)
     assert max_rel(np_(outs[0][0]), oracle.router_logits(x, wr)) < LOGIT_TOL
+
+
+def test_bounded_wait_reports_timeout_and_context_survives():
+    """A wait that nothing can complete gives up after its bound: the host
+    reads SEMMOE_ERR_DEVICE_TIMEOUT with the timeout bit, the error word is
+    cleared, and the GPU goes on working."""
+    import time
+    t0 = time.perf_counter()
+    abi().semmoe_selftest_bounded_wait()
+    with pytest.raises(abi().SemMoEError) as ei:
+        abi().semmoe_check_errors()
+    assert ei.value.code == abi().SEMMOE_ERR_DEVICE_TIMEOUT
+    assert ei.value.bits & abi().SEMMOE_DEVERR_TIMEOUT
+    assert 0.1 < time.perf_counter() - t0 < 60
+    assert abi().semmoe_check_errors() == 0
+    test_combine("f32", True)  # the context still runs kernels

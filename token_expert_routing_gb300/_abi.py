@@ -55,6 +55,7 @@ SIGNATURES = {
     "semmoe_shared_ffn_workspace_size": (_sz, [_i, _i, _i]),
     "semmoe_shared_ffn": (_i, [_vp, _vp, _vp, _i, _i, _i, _i, _vp, _vp, _sz, _vp]),
     "semmoe_combine": (_i, [_vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _vp, _vp]),
+    "semmoe_selftest_bounded_wait": (_i, [_vp]),
     "semmoe_dp_schedule": (_i, [_vp, _vp, _i, _i, _i, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp]),
     "semmoe_transition_lookup": (_i, [_vp, _vp, _i, _vp, _i, _i, _i, _i, _vp, _vp]),
 }
@@ -262,3 +263,9 @@ def semmoe_dp_schedule(pred_rank, req_offsets, T, n_req, R, hist, req_rank, req_
 def semmoe_transition_lookup(topk_idx, k_per_token, k_uniform, trans, T, k_max, E, R, pred_next, stream=None):
     _check(lib().semmoe_transition_lookup(_p(topk_idx), _p(k_per_token), k_uniform, _p(trans), T, k_max, E, R,
                                           _p(pred_next), _stream(stream)))
+
+
+def semmoe_selftest_bounded_wait(stream=None):
+    """Launch the wait that can never complete (it gives up after 2 s and sets
+    the timeout bit); see include/semmoe.h."""
+    _check(lib().semmoe_selftest_bounded_wait(_stream(stream)))

@@ -82,7 +82,7 @@ int semmoe_check_errors(void* stream, int* bits) {
   if (e != cudaSuccess) return cuda_status(e, "semmoe_check_errors");
   int b = 0;
   if (route_take_errors(s, &b) || permute_take_errors(s, &b) || ffn_take_errors(s, &b) ||
-      combine_take_errors(s, &b) || schedule_take_errors(s, &b))
+      combine_take_errors(s, &b) || schedule_take_errors(s, &b) || selftest_take_errors(s, &b))
     return cuda_status(cudaGetLastError(), "semmoe_check_errors: reading the device error word");
   if (bits != nullptr) *bits = b;
   if (b & SEMMOE_DEVERR_TIMEOUT) return fail(SEMMOE_ERR_DEVICE_TIMEOUT, "a bounded in-kernel wait ran out (bits 0x%x)", b);
@@ -395,6 +395,11 @@ int semmoe_transition_lookup(const int32_t* topk_idx, const int32_t* k_per_token
   return cuda_status(launch_transition_lookup(topk_idx, k_per_token, k_uniform, trans, T, k_max, E, R, pred_next,
                                               static_cast<cudaStream_t>(stream)),
                      "semmoe_transition_lookup");
+}
+
+int semmoe_selftest_bounded_wait(void* stream) {
+  CHECK_DEVICE("semmoe_selftest_bounded_wait");
+  return cuda_status(launch_selftest_bounded_wait(static_cast<cudaStream_t>(stream)), "semmoe_selftest_bounded_wait");
 }
 
 }  // extern "C"

@@ -11,6 +11,9 @@ namespace semmoe {
 namespace tc {
 
 constexpr uint64_t kWaitNs = 2000000000ull;  // bound on any single wait: 2 s
+// Second bound, on polls, in case the global timer were ever to stand still
+// (a poll takes 0.1-1 us, so this is far beyond the time bound).
+constexpr uint32_t kWaitPolls = 1u << 26;
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -51,10 +54,10 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
 __device__ inline bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag, int* err) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
-  while (true) {
+  for (uint32_t polls = 0;; ++polls) {
     if (mbar_try_wait(bar, parity)) return true;
     if (*abort_flag) return false;
-    if (globaltimer_ns() - t0 > kWaitNs) {
+    if (globaltimer_ns() - t0 > kWaitNs || polls > kWaitPolls) {
       atomicOr(err, SEMMOE_DEVERR_TIMEOUT);
       *abort_flag = 1;
       return false;
@@ -65,8 +68,8 @@ __device__ inline bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* a
 // Teardown wait: ignores the abort flag, still bounded.
 __device__ inline void mbar_drain(uint64_t* bar, uint32_t parity, int* err) {
   const uint64_t t0 = globaltimer_ns();
-  while (!mbar_try_wait(bar, parity)) {
-    if (globaltimer_ns() - t0 > kWaitNs) {
+  for (uint32_t polls = 0; !mbar_try_wait(bar, parity); ++polls) {
+    if (globaltimer_ns() - t0 > kWaitNs || polls > kWaitPolls) {
       atomicOr(err, SEMMOE_DEVERR_TIMEOUT);
       return;
     }
