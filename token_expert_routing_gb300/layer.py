@@ -51,7 +51,7 @@ class MoELayer:
 
     def __init__(self, w_router, w13, w2, expert_rank, lut, R: int, k_max: int, ws13=None, ws2=None,
                  trans=None, sub_logw=None, fused_gather: bool = False, overlap: bool = True,
-                 overlap_shared: bool = True, device="cuda"):
+                 overlap_shared: bool = True, shared_at: str = "start", device="cuda"):
         dev = torch.device(device)
         c = lambda t: None if t is None else t.to(dev).contiguous()  # noqa: E731
         self.w_router, self.w13, self.w2 = c(w_router), c(w13), c(w2)
@@ -66,9 +66,13 @@ class MoELayer:
         self.fused_gather = fused_gather
         # overlap: the lookup, scheduling and counting steps (nothing later in
         # the layer reads them) run on a second stream beside the permute and
-        # the FFN; overlap_shared: the shared experts' FFN runs there too,
-        # beside the routed FFN
+        # the FFN; overlap_shared: the shared experts' FFN runs there too, from
+        # the start of the forward (shared_at="start": it fills the SMs the
+        # router and permute leave idle) or from the end of the permute
         self.overlap, self.overlap_shared = overlap, overlap_shared
+        if shared_at not in ("start", "permute"):
+            raise ValueError("shared_at is 'start' or 'permute'")
+        self.shared_at = shared_at  # where the shared experts' FFN forks off: before the router, or after the permute
         self._side = None
         self.E, twoI, self.H = self.w13.shape
         self.I = twoI // 2
@@ -155,6 +159,22 @@ class MoELayer:
         T = x.shape[0]
         H, E, I, R, k_max = self.H, self.E, self.I, self.R, self.k_max
         dev = self.device
+        dcode = abi.dtype_code(self.w13)
+        y_shared = None
+        shared_side = self.ws13 is not None and self.overlap_shared
+
+        def shared_on_side():
+            nonlocal y_shared
+            y_shared = torch.empty(T, H, dtype=x.dtype, device=dev)
+            wss = self._workspace("shared", abi.semmoe_shared_ffn_workspace_size(T, self.I_s, dcode))
+            fork()
+            ev1 = side_event() if side_marks is not None else None
+            abi.semmoe_shared_ffn(x, self.ws13, self.ws2, T, H, self.I_s, y_shared, wss, side)
+            if side_marks is not None:
+                side_marks.append(("shared_ffn", ev1, side_event()))
+
+        if shared_side and self.shared_at == "start":
+            shared_on_side()
         if k_per_token is None:
             if k is None:
                 raise ValueError("give k or k_per_token")
@@ -222,17 +242,8 @@ class MoELayer:
                            pair_to_sorted, x_perm, ws, stream)
         mark("permute")
         y_perm = torch.empty(P, H, dtype=x.dtype, device=dev)
-        dcode = abi.dtype_code(self.w13)
-        y_shared = None
-        shared_side = self.ws13 is not None and self.overlap_shared
-        if shared_side:  # the shared experts beside the routed FFN
-            y_shared = torch.empty(T, H, dtype=x.dtype, device=dev)
-            wss = self._workspace("shared", abi.semmoe_shared_ffn_workspace_size(T, self.I_s, dcode))
-            fork()
-            ev1 = side_event() if side_marks is not None else None
-            abi.semmoe_shared_ffn(x, self.ws13, self.ws2, T, H, self.I_s, y_shared, wss, side)
-            if side_marks is not None:
-                side_marks.append(("shared_ffn", ev1, side_event()))
+        if shared_side and self.shared_at == "permute":  # the shared experts beside the routed FFN
+            shared_on_side()
         ws = self._workspace("ffn", abi.semmoe_grouped_ffn_workspace_size(P, I, dcode))
         if self.fused_gather:
             abi.semmoe_grouped_ffn_gather(x, sorted_to_pair, k_max, T, expert_offsets, phys_to_expert, self.w13,
