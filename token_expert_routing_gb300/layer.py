@@ -68,10 +68,11 @@ class MoELayer:
         # the layer reads them) run on a second stream beside the permute and
         # the FFN; overlap_shared: the shared experts' FFN runs there too, from
         # the start of the forward (shared_at="start": it fills the SMs the
-        # router and permute leave idle) or from the end of the permute
+        # router and permute leave idle), after the router ("route", measured
+        # the same) or after the permute ("permute", 4-7% slower)
         self.overlap, self.overlap_shared = overlap, overlap_shared
-        if shared_at not in ("start", "permute"):
-            raise ValueError("shared_at is 'start' or 'permute'")
+        if shared_at not in ("start", "route", "permute"):
+            raise ValueError("shared_at is 'start', 'route' or 'permute'")
         self.shared_at = shared_at  # where the shared experts' FFN forks off: before the router, or after the permute
         self._side = None
         self.E, twoI, self.H = self.w13.shape
@@ -197,6 +198,8 @@ class MoELayer:
             abi.semmoe_route_hier(x, wr, logits_in, logits, self.sub_logw, E // Ep, k_per_token,
                                   k or 0, T, H, Ep, k_max, topk_idx, topk_w, ws, stream, w_dtype=wd)
         mark("route")
+        if shared_side and self.shared_at == "route":
+            shared_on_side()
         ts = s
         if self.overlap:  # lookup .. counts on the second stream
             fork()
