@@ -71,13 +71,57 @@ struct Shared {
   int tp[MAX_GROUPS + 1];
 };
 
-constexpr size_t kSmemBytes = 1024 + (size_t)STAGES * STAGE_BYTES + sizeof(Shared);
+// Output staging of the epilogue: per epilogue warp two 2 KB buffers (32 rows x
+// 32 bf16 columns each), written back by TMA stores.
+constexpr int OUT_STAGE_BYTES = 4 * 2 * 2048;
+
+constexpr size_t kSmemBytes = 1024 + (size_t)STAGES * STAGE_BYTES + OUT_STAGE_BYTES + sizeof(Shared);
 
 constexpr uint32_t kIdesc = idesc_bf16_f32(BM, BN);
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
   return *reinterpret_cast<uint32_t*>(&v);
+}
+
+// Epilogue output of one 32-column chunk of an epilogue warp's 32 tile rows
+// (lane = row; w = the row's 32 bf16 values, packed in pairs).  A warp whose 32
+// rows all hold data stages the chunk in shared memory (64-byte swizzle: 16-byte
+// piece v of row r at piece v ^ ((r >> 1) & 3)) and writes it with one TMA store,
+// alternating between its two buffers; the warp at a group's end (some rows past
+// it) writes its valid rows directly, so no store reaches another group's rows.
+struct ChunkOut {
+  const CUtensorMap* map;  // [rows, N] bf16, box {32 columns, 32 rows}, 64-byte swizzle
+  unsigned char* stage;    // this warp's two 2 KB buffers
+  uint32_t n;              // chunks stored through the buffers so far
+};
+
+__device__ __forceinline__ void emit_chunk(ChunkOut& co, const uint32_t (&w)[16], bool full, bool row_ok,
+                                           __nv_bfloat16* orow, int col0, int N, int wrow0, int lane) {
+  if (col0 >= N) return;
+  if (full) {
+    unsigned char* buf = co.stage + (co.n & 1) * 2048;
+    if (co.n >= 2 && lane == 0) bulk_wait_read<1>();  // this buffer's previous store has read it
+    __syncwarp();
+#pragma unroll
+    for (int v = 0; v < 4; ++v)
+      *reinterpret_cast<uint4*>(buf + lane * 64 + ((v ^ ((lane >> 1) & 3)) << 4)) =
+          make_uint4(w[4 * v], w[4 * v + 1], w[4 * v + 2], w[4 * v + 3]);
+    fence_async_smem();
+    __syncwarp();
+    if (lane == 0) {
+      tma_store_2d(co.map, buf, col0, wrow0);
+      bulk_commit();
+    }
+    ++co.n;
+  } else if (row_ok) {
+#pragma unroll
+    for (int v = 0; v < 4; ++v) {
+      const int col = col0 + 8 * v;
+      if (col + 8 <= N)
+        *reinterpret_cast<uint4*>(orow + col) = make_uint4(w[4 * v], w[4 * v + 1], w[4 * v + 2], w[4 * v + 3]);
+    }
+  }
 }
 
 // Tile unit mu (CL consecutive m-tiles of one group, one per CTA of the
@@ -123,6 +167,7 @@ __device__ __forceinline__ void gather_sources(const int32_t* __restrict__ gathe
 template <bool GLU, int CL>
 __global__ void __launch_bounds__(THREADS, 1)
 ffn_tc_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b,
+              const __grid_constant__ CUtensorMap map_out,
               const int32_t* __restrict__ offsets, const int32_t* __restrict__ phys_to_expert, int G, int P,
               int E, int N, int K, int n_tiles, const int32_t* __restrict__ gather, int gather_div, int gather_rows,
               __nv_bfloat16* __restrict__ out) {
@@ -130,7 +175,8 @@ ffn_tc_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__
   const uint32_t pad = (1024u - (smem_u32(smem_raw) & 1023u)) & 1023u;
   unsigned char* stage_a = smem_raw + pad;                 // STAGES x [128 x 64] bf16
   unsigned char* stage_b = stage_a + STAGES * A_BYTES;     // STAGES x [256 x 64] bf16
-  Shared& sh = *reinterpret_cast<Shared*>(stage_a + STAGES * STAGE_BYTES);
+  unsigned char* out_stage = stage_a + STAGES * STAGE_BYTES;  // OUT_STAGE_BYTES, 1024-aligned
+  Shared& sh = *reinterpret_cast<Shared*>(out_stage + OUT_STAGE_BYTES);
   volatile int* abort_flag = &sh.abort_flag;
 
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
@@ -149,6 +195,7 @@ ffn_tc_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__
     mbar_init_fence();
     prefetch_map(&map_a);
     prefetch_map(&map_b);
+    prefetch_map(&map_out);
   }
   for (int g = threadIdx.x; g <= G; g += THREADS) sh.off[g] = offsets ? offsets[g] : (g == 0 ? 0 : P);
   for (int g = threadIdx.x; g < G; g += THREADS) sh.pe[g] = phys_to_expert ? phys_to_expert[g] : 0;
@@ -288,6 +335,7 @@ ffn_tc_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__
     const int q = warp & 3;           // TMEM lane quarter this warp may access
     const int r = q * 32 + lane;      // tile row held by this thread
     uint32_t acc_it = 0;
+    ChunkOut co{&map_out, out_stage + q * 4096, 0};
     for (int tile = unit0; tile < total; tile += units) {
       const int mt = tile / n_tiles, nt = tile % n_tiles;
       int row0, rows, e;
@@ -301,59 +349,38 @@ ffn_tc_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__
       const uint32_t t_row = tmem + ((uint32_t)(q * 32) << 16) + a * ACC_COLS;
       const bool row_ok = r < rows;
       __nv_bfloat16* orow = out + (size_t)(row0 + (row_ok ? r : 0)) * N;
+      const bool full = q * 32 + 32 <= rows;  // all 32 rows of this warp lie in the group
       if (GLU) {
 #pragma unroll 1
         for (int c = 0; c < 128; c += 32) {
-          uint32_t gv[32], uv[32];
+          uint32_t gv[32], uv[32], w[16];
           tmem_ld32(t_row + c, gv);
           tmem_ld32(t_row + 128 + c, uv);
           tmem_ld_wait();
-          const int col0 = nt * 128 + c;
-          if (row_ok) {
 #pragma unroll
-            for (int v = 0; v < 4; ++v) {
-              const int col = col0 + 8 * v;
-              if (col + 8 <= N) {
-                uint32_t w[4];
-#pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                  const float g0 = __uint_as_float(gv[8 * v + 2 * i]), g1 = __uint_as_float(gv[8 * v + 2 * i + 1]);
-                  const float u0 = __uint_as_float(uv[8 * v + 2 * i]), u1 = __uint_as_float(uv[8 * v + 2 * i + 1]);
-                  const float h0 = __fdividef(g0, 1.0f + __expf(-g0)) * u0;
-                  const float h1 = __fdividef(g1, 1.0f + __expf(-g1)) * u1;
-                  w[i] = pack_bf16x2(h0, h1);
-                }
-                *reinterpret_cast<uint4*>(orow + col) = make_uint4(w[0], w[1], w[2], w[3]);
-              }
-            }
+          for (int i = 0; i < 16; ++i) {
+            const float g0 = __uint_as_float(gv[2 * i]), g1 = __uint_as_float(gv[2 * i + 1]);
+            const float u0 = __uint_as_float(uv[2 * i]), u1 = __uint_as_float(uv[2 * i + 1]);
+            w[i] = pack_bf16x2(__fdividef(g0, 1.0f + __expf(-g0)) * u0, __fdividef(g1, 1.0f + __expf(-g1)) * u1);
           }
+          emit_chunk(co, w, full, row_ok, orow, nt * 128 + c, N, row0 + q * 32, lane);
         }
       } else {
 #pragma unroll 1
         for (int c = 0; c < BN; c += 32) {
-          uint32_t yv[32];
+          uint32_t yv[32], w[16];
           tmem_ld32(t_row + c, yv);
           tmem_ld_wait();
-          const int col0 = nt * BN + c;
-          if (row_ok) {
 #pragma unroll
-            for (int v = 0; v < 4; ++v) {
-              const int col = col0 + 8 * v;
-              if (col + 8 <= N) {
-                uint32_t w[4];
-#pragma unroll
-                for (int i = 0; i < 4; ++i)
-                  w[i] = pack_bf16x2(__uint_as_float(yv[8 * v + 2 * i]), __uint_as_float(yv[8 * v + 2 * i + 1]));
-                *reinterpret_cast<uint4*>(orow + col) = make_uint4(w[0], w[1], w[2], w[3]);
-              }
-            }
-          }
+          for (int i = 0; i < 16; ++i) w[i] = pack_bf16x2(__uint_as_float(yv[2 * i]), __uint_as_float(yv[2 * i + 1]));
+          emit_chunk(co, w, full, row_ok, orow, nt * BN + c, N, row0 + q * 32, lane);
         }
       }
       fence_before();
       mbar_arrive(&sh.tempty[a]);
       ++acc_it;
     }
+    if (lane == 0) bulk_wait_all();  // this warp's output stores are complete
   }
 
   fence_before();
@@ -388,19 +415,21 @@ struct PairShared {
   int tp[MAX_GROUPS + 1];
 };
 
-constexpr size_t kPairSmemBytes = 1024 + (size_t)P_STAGES * P_STAGE_BYTES + sizeof(PairShared);
+constexpr size_t kPairSmemBytes = 1024 + (size_t)P_STAGES * P_STAGE_BYTES + OUT_STAGE_BYTES + sizeof(PairShared);
 constexpr uint32_t kIdescPair = idesc_bf16_f32(2 * BM, BN);
 
 template <bool GLU, int NBUF>
 __global__ void __launch_bounds__(THREADS, 1)
 ffn_pair_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b,
+                const __grid_constant__ CUtensorMap map_out,
                 const int32_t* __restrict__ offsets, const int32_t* __restrict__ phys_to_expert, int G, int P,
                 int E, int N, int K, int n_tiles, const int32_t* __restrict__ gather, int gather_div, int gather_rows,
                 __nv_bfloat16* __restrict__ out) {
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   const uint32_t pad = (1024u - (smem_u32(smem_raw) & 1023u)) & 1023u;
   unsigned char* ring = smem_raw + pad;  // stage s: A [128 x 64] then B half [128 x 64]
-  PairShared& sh = *reinterpret_cast<PairShared*>(ring + P_STAGES * P_STAGE_BYTES);
+  unsigned char* out_stage = ring + P_STAGES * P_STAGE_BYTES;  // OUT_STAGE_BYTES, 1024-aligned
+  PairShared& sh = *reinterpret_cast<PairShared*>(out_stage + OUT_STAGE_BYTES);
   volatile int* abort_flag = &sh.abort_flag;
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   const int rank = (int)cluster_ctarank();
@@ -420,6 +449,7 @@ ffn_pair_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant
     mbar_init_fence();
     prefetch_map(&map_a);
     prefetch_map(&map_b);
+    prefetch_map(&map_out);
   }
   for (int g = threadIdx.x; g <= G; g += THREADS) sh.off[g] = offsets ? offsets[g] : (g == 0 ? 0 : P);
   for (int g = threadIdx.x; g < G; g += THREADS) sh.pe[g] = phys_to_expert ? phys_to_expert[g] : 0;
@@ -535,6 +565,7 @@ ffn_pair_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant
   } else {  // epilogue (both CTAs): this CTA's 128 rows of the 256-row tile
     const int q = warp & 3, r = q * 32 + lane;
     uint32_t acc_it = 0;
+    ChunkOut co{&map_out, out_stage + q * 4096, 0};
     for (int tile = unit0; tile < total; tile += units) {
       const int mt = tile / n_tiles, nt = tile % n_tiles;
       int row0, rows, e;
@@ -548,57 +579,38 @@ ffn_pair_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant
       const uint32_t t_row = tmem + ((uint32_t)(q * 32) << 16) + a * ACC_COLS;
       const bool row_ok = r < rows;
       __nv_bfloat16* orow = out + (size_t)(row0 + (row_ok ? r : 0)) * N;
+      const bool full = q * 32 + 32 <= rows;  // all 32 rows of this warp lie in the group
       if (GLU) {
 #pragma unroll 1
         for (int c = 0; c < 128; c += 32) {
-          uint32_t gv[32], uv[32];
+          uint32_t gv[32], uv[32], w[16];
           tmem_ld32(t_row + c, gv);
           tmem_ld32(t_row + 128 + c, uv);
           tmem_ld_wait();
-          const int col0 = nt * 128 + c;
-          if (row_ok) {
 #pragma unroll
-            for (int v = 0; v < 4; ++v) {
-              const int col = col0 + 8 * v;
-              if (col + 8 <= N) {
-                uint32_t w[4];
-#pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                  const float g0 = __uint_as_float(gv[8 * v + 2 * i]), g1 = __uint_as_float(gv[8 * v + 2 * i + 1]);
-                  const float u0 = __uint_as_float(uv[8 * v + 2 * i]), u1 = __uint_as_float(uv[8 * v + 2 * i + 1]);
-                  w[i] = pack_bf16x2(__fdividef(g0, 1.0f + __expf(-g0)) * u0, __fdividef(g1, 1.0f + __expf(-g1)) * u1);
-                }
-                *reinterpret_cast<uint4*>(orow + col) = make_uint4(w[0], w[1], w[2], w[3]);
-              }
-            }
+          for (int i = 0; i < 16; ++i) {
+            const float g0 = __uint_as_float(gv[2 * i]), g1 = __uint_as_float(gv[2 * i + 1]);
+            const float u0 = __uint_as_float(uv[2 * i]), u1 = __uint_as_float(uv[2 * i + 1]);
+            w[i] = pack_bf16x2(__fdividef(g0, 1.0f + __expf(-g0)) * u0, __fdividef(g1, 1.0f + __expf(-g1)) * u1);
           }
+          emit_chunk(co, w, full, row_ok, orow, nt * 128 + c, N, row0 + q * 32, lane);
         }
       } else {
 #pragma unroll 1
         for (int c = 0; c < BN; c += 32) {
-          uint32_t yv[32];
+          uint32_t yv[32], w[16];
           tmem_ld32(t_row + c, yv);
           tmem_ld_wait();
-          const int col0 = nt * BN + c;
-          if (row_ok) {
 #pragma unroll
-            for (int v = 0; v < 4; ++v) {
-              const int col = col0 + 8 * v;
-              if (col + 8 <= N) {
-                uint32_t w[4];
-#pragma unroll
-                for (int i = 0; i < 4; ++i)
-                  w[i] = pack_bf16x2(__uint_as_float(yv[8 * v + 2 * i]), __uint_as_float(yv[8 * v + 2 * i + 1]));
-                *reinterpret_cast<uint4*>(orow + col) = make_uint4(w[0], w[1], w[2], w[3]);
-              }
-            }
-          }
+          for (int i = 0; i < 16; ++i) w[i] = pack_bf16x2(__uint_as_float(yv[2 * i]), __uint_as_float(yv[2 * i + 1]));
+          emit_chunk(co, w, full, row_ok, orow, nt * BN + c, N, row0 + q * 32, lane);
         }
       }
       fence_before();
       mbar_arrive_cluster(mapa_rank(&sh.tempty[a], 0));  // the leader's MMA may reuse this buffer
       ++acc_it;
     }
+    if (lane == 0) bulk_wait_all();  // this warp's output stores are complete
   }
 
   fence_before();
@@ -622,7 +634,8 @@ struct Gather {
 };
 
 template <bool GLU, int CL>
-cudaError_t launch_one(const CUtensorMap& ma, const CUtensorMap& mb, const int32_t* offsets, const int32_t* p2e,
+cudaError_t launch_one(const CUtensorMap& ma, const CUtensorMap& mb, const CUtensorMap& mo, const int32_t* offsets,
+                       const int32_t* p2e,
                        int G, int P, int E, int N, int K, int n_tiles, Gather ga, __nv_bfloat16* out,
                        cudaStream_t s) {
   auto kern = ffn_tc_kernel<GLU, CL>;
@@ -633,7 +646,7 @@ cudaError_t launch_one(const CUtensorMap& ma, const CUtensorMap& mb, const int32
   if (CL == 1) {
     int grid = sm_count();
     if (max_units < grid) grid = (int)max_units;
-    kern<<<grid, THREADS, kSmemBytes, s>>>(ma, mb, offsets, p2e, G, P, E, N, K, n_tiles, ga.rows, ga.div, ga.n,
+    kern<<<grid, THREADS, kSmemBytes, s>>>(ma, mb, mo, offsets, p2e, G, P, E, N, K, n_tiles, ga.rows, ga.div, ga.n,
                                            out);
   } else {
     cudaLaunchConfig_t cfg = {};
@@ -655,7 +668,7 @@ cudaError_t launch_one(const CUtensorMap& ma, const CUtensorMap& mb, const int32
     long long units = clusters;
     if (max_units < units) units = max_units;
     cfg.gridDim = dim3((unsigned)(units * CL));
-    e = cudaLaunchKernelEx(&cfg, kern, ma, mb, offsets, p2e, G, P, E, N, K, n_tiles, ga.rows, ga.div, ga.n, out);
+    e = cudaLaunchKernelEx(&cfg, kern, ma, mb, mo, offsets, p2e, G, P, E, N, K, n_tiles, ga.rows, ga.div, ga.n, out);
     if (e != cudaSuccess) return e;
   }
   count_launches(1);
@@ -663,7 +676,8 @@ cudaError_t launch_one(const CUtensorMap& ma, const CUtensorMap& mb, const int32
 }
 
 template <bool GLU, int NBUF>
-cudaError_t launch_pair(const CUtensorMap& ma, const CUtensorMap& mb, const int32_t* offsets, const int32_t* p2e,
+cudaError_t launch_pair(const CUtensorMap& ma, const CUtensorMap& mb, const CUtensorMap& mo, const int32_t* offsets,
+                        const int32_t* p2e,
                         int G, int P, int E, int N, int K, int n_tiles, Gather ga, __nv_bfloat16* out,
                         cudaStream_t s) {
   auto kern = ffn_pair_kernel<GLU, NBUF>;
@@ -690,7 +704,7 @@ cudaError_t launch_pair(const CUtensorMap& ma, const CUtensorMap& mb, const int3
   long long units = clusters;
   if (max_units < units) units = max_units;
   cfg.gridDim = dim3((unsigned)(units * 2));
-  e = cudaLaunchKernelEx(&cfg, kern, ma, mb, offsets, p2e, G, P, E, N, K, n_tiles, ga.rows, ga.div, ga.n, out);
+  e = cudaLaunchKernelEx(&cfg, kern, ma, mb, mo, offsets, p2e, G, P, E, N, K, n_tiles, ga.rows, ga.div, ga.n, out);
   if (e != cudaSuccess) return e;
   count_launches(1);
   return cudaGetLastError();
@@ -761,27 +775,42 @@ cudaError_t launch_ffn_tc(const void* x, const int32_t* offsets, const int32_t* 
     const cuuint32_t box[3] = {BK, (cuuint32_t)(BN / CL), 1};  // a cluster CTA loads 1/CL of the tile
     if (!make_map_bf16(&mb2, w2, 3, dims, str, box)) return cudaErrorInvalidValue;
   }
+  // outputs h [P, I] and y [P, H], written by the epilogue's TMA stores in
+  // boxes of 32 rows x 32 columns (64-byte rows, 64-byte swizzle)
+  CUtensorMap mo1, mo2;
+  {
+    const cuuint64_t dims[2] = {(cuuint64_t)I, (cuuint64_t)P};
+    const cuuint64_t str[1] = {(cuuint64_t)I * es};
+    const cuuint32_t box[2] = {32, 32};
+    if (!make_map_bf16(&mo1, ws, 2, dims, str, box, CU_TENSOR_MAP_SWIZZLE_64B)) return cudaErrorInvalidValue;
+  }
+  {
+    const cuuint64_t dims[2] = {(cuuint64_t)H, (cuuint64_t)P};
+    const cuuint64_t str[1] = {(cuuint64_t)H * es};
+    const cuuint32_t box[2] = {32, 32};
+    if (!make_map_bf16(&mo2, y, 2, dims, str, box, CU_TENSOR_MAP_SWIZZLE_64B)) return cudaErrorInvalidValue;
+  }
   __nv_bfloat16* h = static_cast<__nv_bfloat16*>(ws);
   __nv_bfloat16* yb = static_cast<__nv_bfloat16*>(y);
   cudaError_t e;
   if (mode == 1) {
-    e = launch_one<true, 2>(ma1, mb1, offsets, p2e, G, P, E, I, H, (I + 127) / 128, ga, h, s);
+    e = launch_one<true, 2>(ma1, mb1, mo1, offsets, p2e, G, P, E, I, H, (I + 127) / 128, ga, h, s);
     if (e != cudaSuccess) return e;
-    return launch_one<false, 2>(ma2, mb2, offsets, p2e, G, P, E, H, I, (H + BN - 1) / BN, Gather(), yb, s);
+    return launch_one<false, 2>(ma2, mb2, mo2, offsets, p2e, G, P, E, H, I, (H + BN - 1) / BN, Gather(), yb, s);
   }
   if (mode == 2) {
-    e = launch_pair<true, 1>(ma1, mb1, offsets, p2e, G, P, E, I, H, (I + 127) / 128, ga, h, s);
+    e = launch_pair<true, 1>(ma1, mb1, mo1, offsets, p2e, G, P, E, I, H, (I + 127) / 128, ga, h, s);
     if (e != cudaSuccess) return e;
-    return launch_pair<false, 1>(ma2, mb2, offsets, p2e, G, P, E, H, I, (H + BN - 1) / BN, Gather(), yb, s);
+    return launch_pair<false, 1>(ma2, mb2, mo2, offsets, p2e, G, P, E, H, I, (H + BN - 1) / BN, Gather(), yb, s);
   }
   if (mode == 3) {
-    e = launch_pair<true, 2>(ma1, mb1, offsets, p2e, G, P, E, I, H, (I + 127) / 128, ga, h, s);
+    e = launch_pair<true, 2>(ma1, mb1, mo1, offsets, p2e, G, P, E, I, H, (I + 127) / 128, ga, h, s);
     if (e != cudaSuccess) return e;
-    return launch_pair<false, 2>(ma2, mb2, offsets, p2e, G, P, E, H, I, (H + BN - 1) / BN, Gather(), yb, s);
+    return launch_pair<false, 2>(ma2, mb2, mo2, offsets, p2e, G, P, E, H, I, (H + BN - 1) / BN, Gather(), yb, s);
   }
-  e = launch_one<true, 1>(ma1, mb1, offsets, p2e, G, P, E, I, H, (I + 127) / 128, ga, h, s);
+  e = launch_one<true, 1>(ma1, mb1, mo1, offsets, p2e, G, P, E, I, H, (I + 127) / 128, ga, h, s);
   if (e != cudaSuccess) return e;
-  return launch_one<false, 1>(ma2, mb2, offsets, p2e, G, P, E, H, I, (H + BN - 1) / BN, Gather(), yb, s);
+  return launch_one<false, 1>(ma2, mb2, mo2, offsets, p2e, G, P, E, H, I, (H + BN - 1) / BN, Gather(), yb, s);
 }
 
 }  // namespace semmoe

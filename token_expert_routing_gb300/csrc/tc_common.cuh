@@ -171,6 +171,25 @@ __device__ __forceinline__ void tma_gather4_pair(void* dst, const CUtensorMap* m
       : "memory");
 }
 
+// TMA store of a 2-D box from this CTA's shared memory (bulk async-group
+// completion: commit with bulk_commit, wait with bulk_wait_read / bulk_wait_all
+// from the same thread).
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, const void* src, int c0, int c1) {
+  asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%2, %3}], [%1];" ::"l"(
+                   reinterpret_cast<uint64_t>(map)),
+               "r"(smem_u32(src)), "r"(c0), "r"(c1)
+               : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+// At most N of this thread's committed bulk groups still reading shared memory.
+template <int N>
+__device__ __forceinline__ void bulk_wait_read() {
+  asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
+}
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+// Generic-proxy writes to shared memory made visible to the async proxy (TMA).
+__device__ __forceinline__ void fence_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+
 // shared::cluster address of this CTA's shared variable `p` in CTA `rank`.
 __device__ __forceinline__ uint32_t mapa_rank(const void* p, uint32_t rank) {
   uint32_t r;
@@ -336,12 +355,13 @@ inline PFN_cuTensorMapEncodeTiled_v12000 encoder() {
 
 // bf16 tensor map with 128-byte swizzle; dims/strides innermost first, strides in bytes.
 inline bool make_map_bf16(CUtensorMap* m, const void* base, int rank, const cuuint64_t* dims,
-                          const cuuint64_t* strides, const cuuint32_t* box) {
+                          const cuuint64_t* strides, const cuuint32_t* box,
+                          CUtensorMapSwizzle swizzle = CU_TENSOR_MAP_SWIZZLE_128B) {
   auto enc = encoder();
   if (enc == nullptr) return false;
   cuuint32_t estr[5] = {1, 1, 1, 1, 1};
   CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank, const_cast<void*>(base), dims, strides, box, estr,
-                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
 }
