@@ -71,8 +71,8 @@ struct Shared {
   int tp[MAX_GROUPS + 1];
 };
 
-// Output staging of the epilogue: per epilogue warp two 2 KB buffers (32 rows x
-// 32 bf16 columns each), written back by TMA stores.
+// Output staging of the epilogue: per epilogue warp one 4 KB buffer (two boxes of
+// 32 rows x 32 bf16 columns), written back by TMA stores.
 constexpr int OUT_STAGE_BYTES = 4 * 2 * 2048;
 
 constexpr size_t kSmemBytes = 1024 + (size_t)STAGES * STAGE_BYTES + OUT_STAGE_BYTES + sizeof(Shared);
@@ -84,45 +84,55 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   return *reinterpret_cast<uint32_t*>(&v);
 }
 
-// Epilogue output of one 32-column chunk of an epilogue warp's 32 tile rows
-// (lane = row; w = the row's 32 bf16 values, packed in pairs).  A warp whose 32
-// rows all hold data stages the chunk in shared memory (64-byte swizzle: 16-byte
-// piece v of row r at piece v ^ ((r >> 1) & 3)) and writes it with one TMA store,
-// alternating between its two buffers; the warp at a group's end (some rows past
-// it) writes its valid rows directly, so no store reaches another group's rows.
+// silu(g) * u on raw fp32 accumulator words
+__device__ __forceinline__ float swiglu(uint32_t gw, uint32_t uw) {
+  const float g = __uint_as_float(gw), u = __uint_as_float(uw);
+  return __fdividef(g, 1.0f + __expf(-g)) * u;
+}
+
+// Epilogue output of one 64-column chunk of an epilogue warp's 32 tile rows
+// (lane = row; w = the row's 64 bf16 values, packed in pairs).  A warp whose 32
+// rows all hold data stages the chunk in shared memory as two 32 x 32 boxes
+// (64-byte rows, 64-byte swizzle: 16-byte piece v of row r sits at piece
+// v ^ ((r >> 1) & 3)) and writes them with TMA stores; the warp at a group's end
+// (some rows past it) writes its valid rows directly, so no store reaches another
+// group's rows.  Columns past N are clipped by the store / skipped.
 struct ChunkOut {
   const CUtensorMap* map;  // [rows, N] bf16, box {32 columns, 32 rows}, 64-byte swizzle
-  unsigned char* stage;    // this warp's two 2 KB buffers
-  uint32_t n;              // chunks stored through the buffers so far
+  unsigned char* stage;    // this warp's 4 KB staging buffer
+  uint32_t n;              // chunks stored through the buffer so far
 };
 
-__device__ __forceinline__ void emit_chunk(ChunkOut& co, const uint32_t (&w)[16], bool full, bool row_ok,
+__device__ __forceinline__ void emit_chunk(ChunkOut& co, const uint32_t (&w)[32], bool full, bool row_ok,
                                            __nv_bfloat16* orow, int col0, int N, int wrow0, int lane) {
   if (col0 >= N) return;
   if (full) {
-    unsigned char* buf = co.stage + (co.n & 1) * 2048;
-    if (co.n >= 2 && lane == 0) bulk_wait_read<1>();  // this buffer's previous store has read it
+    if (co.n > 0 && lane == 0) bulk_wait_read<0>();  // the previous chunk's stores have read the buffer
     __syncwarp();
 #pragma unroll
-    for (int v = 0; v < 4; ++v)
-      *reinterpret_cast<uint4*>(buf + lane * 64 + ((v ^ ((lane >> 1) & 3)) << 4)) =
-          make_uint4(w[4 * v], w[4 * v + 1], w[4 * v + 2], w[4 * v + 3]);
+    for (int h = 0; h < 2; ++h)
+#pragma unroll
+      for (int v = 0; v < 4; ++v)
+        *reinterpret_cast<uint4*>(co.stage + h * 2048 + lane * 64 + ((v ^ ((lane >> 1) & 3)) << 4)) =
+            make_uint4(w[16 * h + 4 * v], w[16 * h + 4 * v + 1], w[16 * h + 4 * v + 2], w[16 * h + 4 * v + 3]);
     fence_async_smem();
     __syncwarp();
     if (lane == 0) {
-      tma_store_2d(co.map, buf, col0, wrow0);
+      tma_store_2d(co.map, co.stage, col0, wrow0);
+      if (col0 + 32 < N) tma_store_2d(co.map, co.stage + 2048, col0 + 32, wrow0);
       bulk_commit();
     }
     ++co.n;
   } else if (row_ok) {
 #pragma unroll
-    for (int v = 0; v < 4; ++v) {
+    for (int v = 0; v < 8; ++v) {
       const int col = col0 + 8 * v;
       if (col + 8 <= N)
         *reinterpret_cast<uint4*>(orow + col) = make_uint4(w[4 * v], w[4 * v + 1], w[4 * v + 2], w[4 * v + 3]);
     }
   }
 }
+
 
 // Tile unit mu (CL consecutive m-tiles of one group, one per CTA of the
 // cluster) -> this CTA's (first row, valid rows, expert).  A CTA whose m-tile
@@ -350,29 +360,34 @@ ffn_tc_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__
       const bool row_ok = r < rows;
       __nv_bfloat16* orow = out + (size_t)(row0 + (row_ok ? r : 0)) * N;
       const bool full = q * 32 + 32 <= rows;  // all 32 rows of this warp lie in the group
-      if (GLU) {
+      if (GLU) {  // accumulator columns [0, 128) gate, [128, 256) up; 128 output columns
 #pragma unroll 1
-        for (int c = 0; c < 128; c += 32) {
-          uint32_t gv[32], uv[32], w[16];
-          tmem_ld32(t_row + c, gv);
-          tmem_ld32(t_row + 128 + c, uv);
+        for (int c = 0; c < 128; c += 64) {
+          uint32_t g0[32], g1[32], u0[32], u1[32], w[32];
+          tmem_ld32(t_row + c, g0);
+          tmem_ld32(t_row + c + 32, g1);
+          tmem_ld32(t_row + 128 + c, u0);
+          tmem_ld32(t_row + 128 + c + 32, u1);
           tmem_ld_wait();
 #pragma unroll
           for (int i = 0; i < 16; ++i) {
-            const float g0 = __uint_as_float(gv[2 * i]), g1 = __uint_as_float(gv[2 * i + 1]);
-            const float u0 = __uint_as_float(uv[2 * i]), u1 = __uint_as_float(uv[2 * i + 1]);
-            w[i] = pack_bf16x2(__fdividef(g0, 1.0f + __expf(-g0)) * u0, __fdividef(g1, 1.0f + __expf(-g1)) * u1);
+            w[i] = pack_bf16x2(swiglu(g0[2 * i], u0[2 * i]), swiglu(g0[2 * i + 1], u0[2 * i + 1]));
+            w[16 + i] = pack_bf16x2(swiglu(g1[2 * i], u1[2 * i]), swiglu(g1[2 * i + 1], u1[2 * i + 1]));
           }
           emit_chunk(co, w, full, row_ok, orow, nt * 128 + c, N, row0 + q * 32, lane);
         }
       } else {
 #pragma unroll 1
-        for (int c = 0; c < BN; c += 32) {
-          uint32_t yv[32], w[16];
-          tmem_ld32(t_row + c, yv);
+        for (int c = 0; c < BN; c += 64) {
+          uint32_t y0[32], y1[32], w[32];
+          tmem_ld32(t_row + c, y0);
+          tmem_ld32(t_row + c + 32, y1);
           tmem_ld_wait();
 #pragma unroll
-          for (int i = 0; i < 16; ++i) w[i] = pack_bf16x2(__uint_as_float(yv[2 * i]), __uint_as_float(yv[2 * i + 1]));
+          for (int i = 0; i < 16; ++i) {
+            w[i] = pack_bf16x2(__uint_as_float(y0[2 * i]), __uint_as_float(y0[2 * i + 1]));
+            w[16 + i] = pack_bf16x2(__uint_as_float(y1[2 * i]), __uint_as_float(y1[2 * i + 1]));
+          }
           emit_chunk(co, w, full, row_ok, orow, nt * BN + c, N, row0 + q * 32, lane);
         }
       }
@@ -580,29 +595,34 @@ ffn_pair_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant
       const bool row_ok = r < rows;
       __nv_bfloat16* orow = out + (size_t)(row0 + (row_ok ? r : 0)) * N;
       const bool full = q * 32 + 32 <= rows;  // all 32 rows of this warp lie in the group
-      if (GLU) {
+      if (GLU) {  // accumulator columns [0, 128) gate, [128, 256) up; 128 output columns
 #pragma unroll 1
-        for (int c = 0; c < 128; c += 32) {
-          uint32_t gv[32], uv[32], w[16];
-          tmem_ld32(t_row + c, gv);
-          tmem_ld32(t_row + 128 + c, uv);
+        for (int c = 0; c < 128; c += 64) {
+          uint32_t g0[32], g1[32], u0[32], u1[32], w[32];
+          tmem_ld32(t_row + c, g0);
+          tmem_ld32(t_row + c + 32, g1);
+          tmem_ld32(t_row + 128 + c, u0);
+          tmem_ld32(t_row + 128 + c + 32, u1);
           tmem_ld_wait();
 #pragma unroll
           for (int i = 0; i < 16; ++i) {
-            const float g0 = __uint_as_float(gv[2 * i]), g1 = __uint_as_float(gv[2 * i + 1]);
-            const float u0 = __uint_as_float(uv[2 * i]), u1 = __uint_as_float(uv[2 * i + 1]);
-            w[i] = pack_bf16x2(__fdividef(g0, 1.0f + __expf(-g0)) * u0, __fdividef(g1, 1.0f + __expf(-g1)) * u1);
+            w[i] = pack_bf16x2(swiglu(g0[2 * i], u0[2 * i]), swiglu(g0[2 * i + 1], u0[2 * i + 1]));
+            w[16 + i] = pack_bf16x2(swiglu(g1[2 * i], u1[2 * i]), swiglu(g1[2 * i + 1], u1[2 * i + 1]));
           }
           emit_chunk(co, w, full, row_ok, orow, nt * 128 + c, N, row0 + q * 32, lane);
         }
       } else {
 #pragma unroll 1
-        for (int c = 0; c < BN; c += 32) {
-          uint32_t yv[32], w[16];
-          tmem_ld32(t_row + c, yv);
+        for (int c = 0; c < BN; c += 64) {
+          uint32_t y0[32], y1[32], w[32];
+          tmem_ld32(t_row + c, y0);
+          tmem_ld32(t_row + c + 32, y1);
           tmem_ld_wait();
 #pragma unroll
-          for (int i = 0; i < 16; ++i) w[i] = pack_bf16x2(__uint_as_float(yv[2 * i]), __uint_as_float(yv[2 * i + 1]));
+          for (int i = 0; i < 16; ++i) {
+            w[i] = pack_bf16x2(__uint_as_float(y0[2 * i]), __uint_as_float(y0[2 * i + 1]));
+            w[16 + i] = pack_bf16x2(__uint_as_float(y1[2 * i]), __uint_as_float(y1[2 * i + 1]));
+          }
           emit_chunk(co, w, full, row_ok, orow, nt * BN + c, N, row0 + q * 32, lane);
         }
       }
