@@ -288,12 +288,14 @@ def test_grouped_ffn_forms_are_bit_identical(P, E, H, I, monkeypatch):
 
 
 @pytest.mark.parametrize("dtype,T,E,k_max,H,I", [("bf16", 1000, 16, 4, 256, 640), ("bf16", 3001, 64, 6, 512, 1408),
-                                                 ("bf16", 257, 8, 8, 128, 160), ("f32", 300, 8, 3, 64, 96)])
+                                                 ("bf16", 257, 8, 8, 128, 160), ("bf16", 700, 8, 4, 200, 96),
+                                                 ("f32", 300, 8, 3, 64, 96)])
 def test_grouped_ffn_gather_matches_permuted(dtype, T, E, k_max, H, I, monkeypatch):
     """GEMM1 reading x through sorted_to_pair (row gathers) gives exactly the
     bits of the permute's x_perm followed by the grouped FFN, in every form of
     the grouped GEMM; per-token budgets leave padding slots, so sorted rows map
-    to tokens irregularly."""
+    to tokens irregularly; H = 200 leaves a partial last k-block (zero-filled
+    columns) and a partial last output tile."""
     rng = np.random.default_rng(T + I)
     tdt = torch.bfloat16 if dtype == "bf16" else torch.float32
     idx, k = _route_random(rng, T, E, k_max)
