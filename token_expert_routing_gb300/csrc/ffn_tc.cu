@@ -514,6 +514,9 @@ ffn_pair_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant
 
   if (warp == 0) {  // TMA producer (both CTAs): own A rows + own half of B, counted on the leader's barrier
     uint32_t it = 0;
+    int s = 0;          // stage of k-block `it` ...
+    uint32_t ph = 0;    // ... and the parity of its use
+    const uint32_t fb0 = mapa_rank(&sh.full[0], 0);  // the leader's barriers, 8 bytes apart
     if (gather != nullptr || lane == 0)  // without row gathers lane 0 alone: 1% faster than the warp
     for (int tile = unit0; tile < total; tile += units) {
       if (*abort_flag) break;
@@ -524,13 +527,11 @@ ffn_pair_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant
       if (gather != nullptr) gather_sources(gather, gather_div, gather_rows, P, row0, lane, src);
       bool ok = true;
       for (int kb = 0; kb < kb_n; ++kb) {
-        const int s = it % P_STAGES;
-        const uint32_t ph = (it / P_STAGES) & 1;
         int good = 1;
         if (lane == 0) good = mbar_wait(&sh.empty[s], ph ^ 1, abort_flag, &g_err);
         if (gather != nullptr ? !__shfl_sync(0xffffffffu, good, 0) : !good) { ok = false; break; }
         if (lane == 0 && leader) mbar_expect_tx(&sh.full[s], 2 * P_STAGE_BYTES);
-        const uint32_t fb = mapa_rank(&sh.full[s], 0);
+        const uint32_t fb = fb0 + 8u * s;
         unsigned char* st = ring + (size_t)s * P_STAGE_BYTES;
         if (gather != nullptr)
           tma_gather4_pair(st + lane * 4 * (BK * 2), &map_a, fb, kb * BK, src[0], src[1], src[2], src[3]);
@@ -541,6 +542,10 @@ ffn_pair_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant
           else tma_load_3d_pair(st + A_BYTES, &map_b, fb, kb * BK, nt * BN + rank * 128, e);
         }
         ++it;
+        if (++s == P_STAGES) {
+          s = 0;
+          ph ^= 1;
+        }
       }
       if (!ok) break;
     }
@@ -550,7 +555,8 @@ ffn_pair_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant
     }
   } else if (warp == 1) {
     if (lane == 0 && leader) {  // MMA issuer: the pair's even CTA only
-      uint32_t it = 0, acc_it = 0;
+      uint32_t acc_it = 0, ph = 0;
+      int s = 0;
       for (int tile = unit0; tile < total; tile += units) {
         if (*abort_flag) break;
         const uint32_t a = acc_it % NBUF, aph = (acc_it / NBUF) & 1;
@@ -559,8 +565,6 @@ ffn_pair_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant
         const uint32_t d = tmem + a * ACC_COLS;
         bool ok = true;
         for (int kb = 0; kb < kb_n; ++kb) {
-          const int s = it % P_STAGES;
-          const uint32_t ph = (it / P_STAGES) & 1;
           if (!mbar_wait(&sh.full[s], ph, abort_flag, &g_err)) { ok = false; break; }
           fence_after();
           const uint32_t sa = smem_u32(ring + (size_t)s * P_STAGE_BYTES), sb = sa + A_BYTES;
@@ -568,7 +572,10 @@ ffn_pair_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant
           for (int k = 0; k < BK / UK; ++k)
             mma_bf16_pair(d, sw128_desc(sa + k * UK * 2), sw128_desc(sb + k * UK * 2), kIdescPair, (kb | k) != 0);
           commit_pair_mc(&sh.empty[s], 0x3);  // both CTAs may refill this stage
-          ++it;
+          if (++s == P_STAGES) {
+            s = 0;
+            ph ^= 1;
+          }
         }
         if (!ok) break;
         commit_pair_mc(&sh.tfull[a], 0x3);    // both CTAs' accumulator rows are ready
