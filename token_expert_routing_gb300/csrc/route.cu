@@ -92,34 +92,41 @@ __device__ __forceinline__ void warp_load_logits(const float* row, int ks, size_
 
 // k_t rounds of a warp argmax over (score descending, index ascending) of the
 // n scores in v, skipping those already taken.  Lane 0 writes the j-th pick to
-// my_v[j] / my_e[j] (-1 when fewer than k_t scores are finite, flagged).
+// my_v[j] / my_e[j] (-1 when fewer than k_t scores are left, flagged).
+// Each score becomes an order-preserving 32-bit key (-0.0 counted as +0.0; key 0
+// marks padding and taken scores, below every float including -inf), so a round
+// is two warp reductions: the largest key, then the lowest index holding it.
 template <int NPER>
 __device__ __forceinline__ void warp_select(const float (&v)[NPER], int n, int kt, float* my_v, int* my_e) {
   const int lane = threadIdx.x % 32;
-  unsigned taken = 0;
+  uint32_t key[NPER];
+#pragma unroll
+  for (int i = 0; i < NPER; ++i) {
+    const uint32_t b = __float_as_uint(__fadd_rn(v[i], 0.0f));  // -0.0 -> +0.0
+    key[i] = lane + 32 * i < n ? ((b & 0x80000000u) ? ~b : (b | 0x80000000u)) : 0u;
+  }
   for (int j = 0; j < kt; ++j) {
-    float bv = -INFINITY;
-    int be = 0x7fffffff;
+    uint32_t m = key[0];
 #pragma unroll
-    for (int i = 0; i < NPER; ++i) {
-      const int e = lane + 32 * i;
-      if (e < n && !((taken >> i) & 1u)) {
-        if (v[i] > bv || (v[i] == bv && e < be)) { bv = v[i]; be = e; }
-      }
-    }
+    for (int i = 1; i < NPER; ++i) m = max(m, key[i]);
+    m = __reduce_max_sync(0xffffffffu, m);
+    int be = -1;
+    if (m != 0u) {
+      uint32_t mine = 0xffffffffu;  // this lane's lowest index whose key is m
 #pragma unroll
-    for (int off = 16; off > 0; off >>= 1) {
-      const float ov = __shfl_xor_sync(0xffffffffu, bv, off);
-      const int oe = __shfl_xor_sync(0xffffffffu, be, off);
-      if (ov > bv || (ov == bv && oe < be)) { bv = ov; be = oe; }
+      for (int i = NPER - 1; i >= 0; --i)
+        if (key[i] == m) mine = (uint32_t)(lane + 32 * i);
+      be = (int)__reduce_min_sync(0xffffffffu, mine);
+#pragma unroll
+      for (int i = 0; i < NPER; ++i)
+        if (be == lane + 32 * i) key[i] = 0u;
+    } else if (lane == 0) {
+      flag(SEMMOE_DEVERR_NONFINITE);  // fewer than kt scores
     }
-    if (be >= n) {  // fewer than kt finite scores
-      if (lane == 0) flag(SEMMOE_DEVERR_NONFINITE);
-      be = -1;
-    } else if ((be & 31) == lane) {
-      taken |= 1u << (be >> 5);
+    if (lane == 0) {
+      my_v[j] = be >= 0 ? __uint_as_float((m & 0x80000000u) ? (m ^ 0x80000000u) : ~m) : -INFINITY;
+      my_e[j] = be;
     }
-    if (lane == 0) { my_v[j] = bv; my_e[j] = be; }
   }
   __syncwarp();
 }

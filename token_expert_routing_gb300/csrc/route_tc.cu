@@ -147,15 +147,20 @@ route_tc_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_constant
       commit(&sh.done);
       mbar_drain(&sh.done, 0, &g_err);
     }
-  } else {  // epilogue: one token row per thread
-    const int q = warp & 3, r = q * 32 + lane, t = t0 + r;
+  } else {  // epilogue: thread = one token row of the accumulator
+    const int q = warp & 3;
     int ok = 1;
     if (lane == 0) ok = mbar_wait(&sh.tfull, 0, abort_flag, &g_err);
     ok = __shfl_sync(0xffffffffu, ok, 0);
     if (ok) {
       fence_after();
       const uint32_t trow = tmem + ((uint32_t)(q * 32) << 16);
-      float* lrow = logits + (size_t)(t < T ? t : 0) * E;
+      // The warp's 32 rows x 16 columns pass through 2 KB of the operand ring
+      // (every MMA has read it once tfull has fired): lane l stores its row's
+      // four 16-byte pieces at piece p ^ ((l >> 1) & 3) of its 64-byte row, then
+      // each store instruction writes two rows' 64-byte segments.
+      float* stg = reinterpret_cast<float*>(ring) + q * 32 * 16;
+      const int sw = (lane >> 1) & 3;
       for (int c = 0; c < EC; c += 16) {
         uint32_t v0[16], v1[16], v2[16];
         tmem_ld16(trow + c, v0);
@@ -164,17 +169,25 @@ route_tc_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_constant
           tmem_ld16(trow + 2 * EC + c, v2);
         }
         tmem_ld_wait();
-        if (t < T) {
+        float l[16];
 #pragma unroll
-          for (int i = 0; i < 16; ++i) {
-            const int e = pass * EC + c + i;
-            if (e < E) {
-              float l = __uint_as_float(v0[i]);
-              if (S == 3) l = (l + __uint_as_float(v1[i])) + __uint_as_float(v2[i]);
-              lrow[e] = l;
-            }
-          }
+        for (int i = 0; i < 16; ++i) {
+          l[i] = __uint_as_float(v0[i]);
+          if (S == 3) l[i] = (l[i] + __uint_as_float(v1[i])) + __uint_as_float(v2[i]);
         }
+#pragma unroll
+        for (int p = 0; p < 4; ++p)
+          *reinterpret_cast<float4*>(stg + lane * 16 + ((p ^ sw) << 2)) =
+              make_float4(l[4 * p], l[4 * p + 1], l[4 * p + 2], l[4 * p + 3]);
+        __syncwarp();
+        const int col = lane & 15, e = pass * EC + c + col;
+#pragma unroll 4
+        for (int rr = 0; rr < 32; rr += 2) {
+          const int row = rr + (lane >> 4), t = t0 + q * 32 + row;
+          const float val = stg[row * 16 + ((((col >> 2) ^ ((row >> 1) & 3))) << 2) + (col & 3)];
+          if (t < T && e < E) logits[(size_t)t * E + e] = val;
+        }
+        __syncwarp();
       }
     }
   }
