@@ -35,6 +35,7 @@ constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
 constexpr int kMaxE = 256;
 constexpr int kTargetChunks = 96;  // enough CTAs to cover the GPU, few enough to scan cheaply
+constexpr int kPre = 8;            // pair ids loaded ahead per thread (rounds of a chunk)
 static_assert(kTargetChunks * kMaxE * 4 <= kNoAllocScratchBytes, "no-alloc scratch too small");
 
 // Pairs per CTA: a multiple of kThreads (one "round" each) giving about
@@ -81,13 +82,20 @@ perm_hist_kernel(const int32_t* __restrict__ topk_idx, const int32_t* __restrict
   __syncthreads();
   const int chunk = rounds * kThreads;
   const long long base = (long long)blockIdx.x * chunk;
-  for (int i = threadIdx.x; i < chunk; i += kThreads) {
-    long long p = base + i;
-    if (p >= n_pairs) break;
-    int e = topk_idx[p];
-    if (e < 0) continue;
-    if (e >= E) { flag(SEMMOE_DEVERR_EXPERT); continue; }
-    atomicAdd(&h[phys_s[e]], 1);
+  for (int i0 = 0; i0 < chunk; i0 += kPre * kThreads) {  // kPre loads in flight per thread
+    int ev[kPre];
+#pragma unroll
+    for (int u = 0; u < kPre; ++u) {
+      const int i = i0 + u * kThreads + threadIdx.x;
+      ev[u] = (i < chunk && base + i < n_pairs) ? topk_idx[base + i] : -1;
+    }
+#pragma unroll
+    for (int u = 0; u < kPre; ++u) {
+      const int e = ev[u];
+      if (e < 0) continue;
+      if (e >= E) { flag(SEMMOE_DEVERR_EXPERT); continue; }
+      atomicAdd(&h[phys_s[e]], 1);
+    }
   }
   __syncthreads();
   for (int b = threadIdx.x; b < E; b += kThreads) hist[(size_t)blockIdx.x * E + b] = h[b];
@@ -175,12 +183,23 @@ perm_scatter_kernel(const int32_t* __restrict__ topk_idx, const int32_t* __restr
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   (void)lane;
   const long long base = (long long)blockIdx.x * rounds * kThreads;
+  int ev[kPre];  // the pair ids of rounds r0 .. r0 + kPre - 1, loaded together
   for (int r = 0; r < rounds; ++r) {
     if (base + (long long)r * kThreads >= n_pairs) break;  // uniform across the CTA
+    if (r % kPre == 0) {
+#pragma unroll
+      for (int u = 0; u < kPre; ++u) {
+        const long long pu = base + (long long)(r + u) * kThreads + threadIdx.x;
+        ev[u] = (r + u < rounds && pu < n_pairs) ? topk_idx[pu] : -1;
+      }
+    }
     const long long p = base + (long long)r * kThreads + threadIdx.x;
     int key = E;  // E = "no bucket" (padding slot or past the end)
     if (p < n_pairs) {
-      int e = topk_idx[p];
+      int e = 0;
+#pragma unroll
+      for (int u = 0; u < kPre; ++u)
+        if (u == r % kPre) e = ev[u];  // register select, no local-memory indexing
       if (e >= E) flag(SEMMOE_DEVERR_EXPERT);
       else if (e >= 0) key = phys_s[e];
     }

@@ -31,7 +31,9 @@ __device__ int g_err;
 constexpr int BM = 128, BK = 64, UK = 16, THREADS = 192;
 constexpr int MAX_STAGES = 8;
 constexpr int A_BYTES = BM * BK * 2;            // 16 KB
-constexpr size_t kStageBudget = 200 * 1024;     // operand ring
+// Operand ring per CTA: 200 KB when the grid fits one CTA per SM, 100 KB (two
+// CTAs per SM, each one's epilogue beside the other's loads) when it is larger.
+__host__ __device__ constexpr size_t stage_budget(int cps) { return cps == 1 ? 200 * 1024 : 100 * 1024; }
 constexpr uint32_t TMEM_COLS = 256;
 constexpr int kMaxKSlices = 8;
 
@@ -41,7 +43,7 @@ struct Shared {
   int abort_flag;
 };
 
-constexpr size_t kSmemBytes = 1024 + kStageBudget + sizeof(Shared);
+__host__ __device__ constexpr size_t smem_bytes(int cps) { return 1024 + stage_budget(cps) + sizeof(Shared); }
 
 // Experts per pass: S * EC <= 256 columns, EC a multiple of 16.
 inline int experts_per_pass(int E, int S) {
@@ -73,14 +75,14 @@ __global__ void split_router_kernel(const float* __restrict__ w, int E, int H, i
   }
 }
 
-template <int S>
-__global__ void __launch_bounds__(THREADS, 1)
+template <int S, int CPS>  // CPS: resident CTAs per SM the ring is sized for
+__global__ void __launch_bounds__(THREADS, CPS)
 route_tc_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_constant__ CUtensorMap map_w, int T, int H,
                 int E, int EC, int stages, int kb_per_slice, float* __restrict__ partials) {
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   const uint32_t pad = (1024u - (smem_u32(smem_raw) & 1023u)) & 1023u;
   unsigned char* ring = smem_raw + pad;  // stage s: A tile then B tile, stage_bytes apart
-  Shared& sh = *reinterpret_cast<Shared*>(ring + kStageBudget);
+  Shared& sh = *reinterpret_cast<Shared*>(ring + stage_budget(CPS));
   volatile int* abort_flag = &sh.abort_flag;
 
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
@@ -240,6 +242,17 @@ cudaError_t launch_route_split(const float* w, int H, int E, void* split, cudaSt
   return cudaGetLastError();
 }
 
+template <int S, int CPS>
+static cudaError_t launch_k(dim3 grid, const CUtensorMap& mx, const CUtensorMap& mw, int T, int H, int E, int EC,
+                            int stages, int kb_per_slice, float* partials, cudaStream_t s) {
+  static std::atomic<unsigned long long> smem_set{0};
+  cudaError_t e = ensure_smem_limit(route_tc_kernel<S, CPS>, (int)smem_bytes(CPS), smem_set);
+  if (e != cudaSuccess) return e;
+  route_tc_kernel<S, CPS><<<grid, THREADS, smem_bytes(CPS), s>>>(mx, mw, T, H, E, EC, stages, kb_per_slice,
+                                                                 partials);
+  return cudaSuccess;
+}
+
 // x [T,H] bf16 (H % 8 == 0); w [E,H] fp32 or bf16, or the split of an fp32
 // weight (SEMMOE_F32_SPLIT); partials [ks][T][E] fp32 out (ks =
 // route_tc_k_slices(); the logits are their sum in slice order); split:
@@ -275,21 +288,16 @@ cudaError_t launch_route_logits_tc(const void* x, const void* w, int w_dtype, in
     if (!make_map_bf16(&mw, wb, 2, dims, str, box)) return cudaErrorInvalidValue;
   }
   const size_t stage_bytes = A_BYTES + (size_t)S * EC * BK * 2;
-  int stages = (int)(kStageBudget / stage_bytes);
-  if (stages > MAX_STAGES) stages = MAX_STAGES;
   dim3 grid((T + BM - 1) / BM, n_pass, ks);
+  const int cps = (long long)grid.x * grid.y * grid.z > sm_count() ? 2 : 1;
+  int stages = (int)(stage_budget(cps) / stage_bytes);
+  if (stages > MAX_STAGES) stages = MAX_STAGES;
   cudaError_t e;
-  if (S == 3) {
-    static std::atomic<unsigned long long> smem_set{0};
-    e = ensure_smem_limit(route_tc_kernel<3>, (int)kSmemBytes, smem_set);
-    if (e != cudaSuccess) return e;
-    route_tc_kernel<3><<<grid, THREADS, kSmemBytes, s>>>(mx, mw, T, H, E, EC, stages, kb_per_slice, partials);
-  } else {
-    static std::atomic<unsigned long long> smem_set{0};
-    e = ensure_smem_limit(route_tc_kernel<1>, (int)kSmemBytes, smem_set);
-    if (e != cudaSuccess) return e;
-    route_tc_kernel<1><<<grid, THREADS, kSmemBytes, s>>>(mx, mw, T, H, E, EC, stages, kb_per_slice, partials);
-  }
+  if (S == 3 && cps == 1) e = launch_k<3, 1>(grid, mx, mw, T, H, E, EC, stages, kb_per_slice, partials, s);
+  else if (S == 3) e = launch_k<3, 2>(grid, mx, mw, T, H, E, EC, stages, kb_per_slice, partials, s);
+  else if (cps == 1) e = launch_k<1, 1>(grid, mx, mw, T, H, E, EC, stages, kb_per_slice, partials, s);
+  else e = launch_k<1, 2>(grid, mx, mw, T, H, E, EC, stages, kb_per_slice, partials, s);
+  if (e != cudaSuccess) return e;
   count_launches(1);
   return cudaGetLastError();
 }
