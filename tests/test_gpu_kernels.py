@@ -234,9 +234,9 @@ def test_remote_count_large_pair_list():
                                         (256, 16, torch.bfloat16), (256, 24, torch.float32),
                                         (128, 8, torch.bfloat16)])
 def test_route_tensor_core_per_token_budgets(E, k_max, wd):
-    """bf16 activations: the tensor-core router, with the top-k fused into its
-    epilogue when every expert fits one pass and k_max <= 16, else a separate
-    top-k kernel; per-token budgets and ties from duplicated router rows."""
+    """bf16 activations: the tensor-core router (split over K when the token
+    tiles alone leave SMs idle) and the warp-per-token top-k; per-token budgets
+    and ties from duplicated router rows."""
     rng = np.random.default_rng(E * 31 + k_max)
     T, H = 515, 256
     x = torch.from_numpy(rng.standard_normal((T, H)).astype(np.float32) / np.sqrt(H)).to(torch.bfloat16)
@@ -251,6 +251,26 @@ def test_route_tensor_core_per_token_budgets(E, k_max, wd):
     assert abi().semmoe_check_errors() == 0
     assert max_rel(np_(lg), oracle.router_logits(x, wr)) < LOGIT_TOL
     ref_idx, ref_w = oracle.topk_route(np_(lg), kpt, k_max)
+    np.testing.assert_array_equal(np_(idx), ref_idx)
+    np.testing.assert_allclose(np_(gw), ref_w, rtol=0, atol=GATE_ATOL)
+
+
+@pytest.mark.parametrize("wd", [torch.bfloat16, torch.float32])
+def test_route_tensor_core_grid_beyond_one_wave(wd):
+    """More token tiles than SMs: the router GEMM runs two resident CTAs per SM
+    with the smaller operand ring; logits within tolerance, picks bit-exact."""
+    rng = np.random.default_rng(77)
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    T, H, E, k_max = (sms + 3) * 128 + 77, 256, 64, 6
+    x = torch.from_numpy(rng.standard_normal((T, H)).astype(np.float32) / np.sqrt(H)).to(torch.bfloat16)
+    wr = torch.from_numpy(rng.standard_normal((E, H)).astype(np.float32) / np.sqrt(H)).to(wd)
+    idx = torch.empty(T, k_max, **i32)
+    gw = torch.empty(T, k_max, dtype=torch.float32, device="cuda")
+    lg = torch.empty(T, E, dtype=torch.float32, device="cuda")
+    abi().semmoe_route(x.cuda(), wr.cuda(), None, lg, None, k_max, T, H, E, k_max, idx, gw)
+    assert abi().semmoe_check_errors() == 0
+    assert max_rel(np_(lg), oracle.router_logits(x, wr)) < LOGIT_TOL
+    ref_idx, ref_w = oracle.topk_route(np_(lg), np.full(T, k_max), k_max)
     np.testing.assert_array_equal(np_(idx), ref_idx)
     np.testing.assert_allclose(np_(gw), ref_w, rtol=0, atol=GATE_ATOL)
 

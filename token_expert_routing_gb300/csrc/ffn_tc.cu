@@ -11,7 +11,9 @@
 // Warp roles (192 threads):
 //   warp 0      TMA producer: A tile [128 x 64] + B tile [256 x 64] per stage
 //   warp 1      allocates TMEM; one thread issues tcgen05.mma (M128 N256 K16)
-//   warps 2..5  epilogue: tcgen05.ld the accumulator, SwiGLU / convert, store
+//   warps 2..5  epilogue: tcgen05.ld the accumulator, SwiGLU / convert, stage
+//               32 x 64 bf16 blocks in shared memory and write them with TMA
+//               stores (a warp whose rows cross its group's end stores directly)
 // Pipelines: a 4-stage smem ring (full/empty mbarriers) and a 2-deep TMEM
 // accumulator ring (tfull/tempty), so the epilogue of tile i overlaps the MMAs
 // of tile i+1.  GEMM1's B tile is 128 gate rows + the 128 matching up rows, so
@@ -30,7 +32,7 @@
 //    shared by TMA multicast; it halves L2 weight reads but not per-SM
 //    shared-memory traffic and measured slower.
 //
-// Every wait is bounded (%globaltimer); a wait that runs out sets the timeout
+// Every wait is bounded (%globaltimer and a poll count); a wait that runs out sets the timeout
 // bit of the device error word and an abort flag, after which every role
 // stops, in-flight TMA loads and MMAs are drained (again with a bound), and
 // TMEM is freed before the CTA exits.
