@@ -173,10 +173,10 @@ perm_scatter_kernel(const int32_t* __restrict__ topk_idx, const int32_t* __restr
       expert_offsets[E] = sum;
       if (sum != P) flag(SEMMOE_DEVERR_PAIRS);
     }
-    if (tid <= R) {
-      int nb = 0;  // buckets of ranks below r = tid
-      for (int e = 0; e < E; ++e) nb += rank_s[e] < tid;
-      rank_offsets[tid] = nb == 0 ? 0 : scan[nb - 1];
+    for (int r = tid; r <= R; r += kThreads) {  // R + 1 entries (R may be 256)
+      int nb = 0;  // buckets of ranks below r
+      for (int e = 0; e < E; ++e) nb += rank_s[e] < r;
+      rank_offsets[r] = nb == 0 ? 0 : scan[nb - 1];
     }
   }
   __syncthreads();
