@@ -104,6 +104,12 @@ def test_ffn_and_combine_validation(lib):
     # H * 2 bytes not a multiple of 16
     rc = lib.semmoe_combine(p, p, p, None, 1, 4, 12, 2, 8, p, None)
     assert rc == 1
+    # no rows: empty activations (null pointers) are fine, nothing is launched
+    assert lib.semmoe_grouped_ffn(None, p, p, p, p, 1, 0, 4, 128, 128, None, p, 1 << 30, None) == 0
+    assert lib.semmoe_shared_ffn(None, p, p, 1, 0, 128, 256, None, p, 1 << 30, None) == 0
+    # rows but no activations
+    rc = lib.semmoe_grouped_ffn(None, p, p, p, p, 1, 64, 4, 128, 128, p, p, 1 << 30, None)
+    assert rc == 1 and "null" in _err(lib)
 
 
 def test_remote_count_validation(lib):

@@ -392,3 +392,38 @@ def test_bounded_wait_reports_timeout_and_context_survives():
     assert 0.1 < time.perf_counter() - t0 < 60
     assert abi().semmoe_check_errors() == 0
     test_combine("f32", True)  # the context still runs kernels
+
+
+def test_empty_batch_through_every_step():
+    """T = 0 (and so P = 0) through the router, lookup, remote count, permute,
+    grouped FFN and combine: every call succeeds, the tables come out as the
+    oracle gives them for an empty batch (physical order, zero offsets and
+    counts), and nothing else is written."""
+    E, R, k_max, H, I = 8, 4, 3, 64, 96
+    er = (np.arange(E) % R).astype(np.int32)
+    ref = oracle.permute(np.zeros((0, k_max), np.int32), np.zeros(0, np.int32), er, R)
+    e0 = lambda *shape, dt=torch.int32: torch.empty(*shape, dtype=dt, device="cuda")  # noqa: E731
+    x = e0(0, H, dt=torch.bfloat16)
+    idx, w = e0(0, k_max), e0(0, k_max, dt=torch.float32)
+    abi().semmoe_route(x, torch.randn(E, H, device="cuda"), None, None, None, 2, 0, H, E, k_max, idx, w)
+    pred = e0(0)
+    abi().semmoe_affinity_lookup(e0(0), torch.zeros(10, dtype=torch.int32, device="cuda"), 10, R, 0, pred)
+    counts = torch.full((R, R), 7, dtype=torch.int32, device="cuda")
+    remote = torch.full((R,), 7, dtype=torch.int32, device="cuda")
+    abi().semmoe_remote_count(idx, pred, torch.from_numpy(er).cuda(), 0, k_max, E, R, counts, remote)
+    eo, ro = torch.full((E + 1,), -5, **i32), torch.full((R + 1,), -5, **i32)
+    p2e, ec = torch.full((E,), -5, **i32), torch.full((E,), -5, **i32)
+    ws = torch.empty(abi().semmoe_permute_workspace_size(0, k_max, E), dtype=torch.uint8, device="cuda")
+    abi().semmoe_permute(idx, torch.from_numpy(er).cuda(), x, 0, H, E, R, k_max, 0, eo, ro, p2e, ec, e0(1), e0(0),
+                         e0(0, H, dt=torch.bfloat16), ws)
+    fws = torch.empty(abi().semmoe_grouped_ffn_workspace_size(0, I, 1), dtype=torch.uint8, device="cuda")
+    w13 = torch.randn(E, 2 * I, H, device="cuda").to(torch.bfloat16)
+    w2 = torch.randn(E, H, I, device="cuda").to(torch.bfloat16)
+    y = e0(0, H, dt=torch.bfloat16)
+    abi().semmoe_grouped_ffn(e0(0, H, dt=torch.bfloat16), eo, p2e, w13, w2, 0, E, H, I, y, fws)
+    out = e0(0, H, dt=torch.bfloat16)
+    abi().semmoe_combine(y, e0(0), w, None, 0, H, k_max, 0, out)
+    assert abi().semmoe_check_errors() == 0
+    for key, got in (("expert_offsets", eo), ("rank_offsets", ro), ("phys_to_expert", p2e), ("expert_counts", ec)):
+        np.testing.assert_array_equal(np_(got), ref[key], err_msg=key)
+    assert int(counts.sum()) == 0 and int(remote.sum()) == 0

@@ -123,3 +123,15 @@ def test_graph_pipeline_matches_forward(name, over):
     for x, ids, o in zip(xs, idss, outs):
         want = layer.forward(x.cuda(), ids.cuda(), kpt, None if per_token else spec.k, P).out.cpu()
         assert torch.equal(o, want)
+
+
+def test_layer_empty_batch():
+    """A forward over no tokens returns an empty output and flags nothing."""
+    from token_expert_routing_gb300 import MoELayer, _abi
+    d = wl.make_inputs(wl.scaled("dsv2lite_prefill_T4096", T=64, H=256, I=160, I_shared=320, V=3000))
+    s = d["spec"]
+    layer = MoELayer(d["w_router"], d["w13"], d["w2"], d["expert_rank"], d["lut"], s.R, s.k_max, d["ws13"], d["ws2"])
+    x = d["x"][:0].cuda()
+    res = layer.forward(x, d["token_ids"][:0].cuda(), None, s.k, 0)
+    assert _abi.semmoe_check_errors() == 0
+    assert tuple(res.out.shape) == (0, s.H)

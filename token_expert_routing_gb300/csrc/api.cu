@@ -288,7 +288,7 @@ static int check_ffn_args(const char* fn, const void* x, const void* w13, const 
   REQUIRE(P >= 0 && H >= 8 && I >= 8 && H % 8 == 0 && I % 8 == 0, "%s: need P >= 0 and H, I multiples of 8 (P=%d H=%d I=%d)",
           fn, P, H, I);
   REQUIRE((long long)P * (H > I ? H : I) < (1LL << 40), "%s: P too large", fn);
-  REQUIRE(x && w13 && w2 && y, "%s: null pointer", fn);
+  REQUIRE(w13 && w2 && (P == 0 || (x && y)), "%s: null pointer", fn);  // no rows: x and y may be empty
   REQUIRE(aligned(x, 16) && aligned(w13, 16) && aligned(w2, 16) && aligned(y, 16), "%s: pointers must be 16-byte aligned",
           fn);
   REQUIRE(ws != nullptr && aligned(ws, 256), "%s: workspace null or not 256-byte aligned", fn);
