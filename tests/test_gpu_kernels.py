@@ -81,6 +81,7 @@ def _route_random(rng, T, E, k_max, skew=None, per_token=True):
     (700, 256, 8, 24, None, 16, "mod"),
     (300, 12, 3, 12, None, 16, "mod"),         # k = E
     (300, 256, 256, 4, None, 8, "mod"),        # R = 256: a rank per expert, 257 rank offsets
+    (2000, 256, 64, 8, None, 16, "random"),    # R = 64: the remote counter's largest table
 ])
 def test_permute_and_counts(T, E, R, k_max, skew, H, placement):
     rng = np.random.default_rng(T * 7 + E)
@@ -427,3 +428,34 @@ def test_empty_batch_through_every_step():
     for key, got in (("expert_offsets", eo), ("rank_offsets", ro), ("phys_to_expert", p2e), ("expert_counts", ec)):
         np.testing.assert_array_equal(np_(got), ref[key], err_msg=key)
     assert int(counts.sum()) == 0 and int(remote.sum()) == 0
+
+
+def test_permute_flags_bad_expert_and_pair_count():
+    """An expert id past E is skipped (its slot maps to -1) and flagged; a P
+    that disagrees with the live pairs is flagged; the other pairs are placed
+    exactly as the oracle places them without the bad one."""
+    rng = np.random.default_rng(91)
+    T, E, R, k_max = 100, 8, 4, 2
+    idx, k = _route_random(rng, T, E, k_max)
+    er = (np.arange(E) % R).astype(np.int32)
+    good = idx.copy()
+    good[7, 1] = -1                        # the oracle's view: that slot is padding
+    bad = idx.copy()
+    bad[7, 1] = E + 3
+    k_good = (good >= 0).sum(axis=1)
+    P = int(k_good.sum())                  # live pairs without the bad one
+    ref = oracle.permute(good, k_good, er, R)
+    eo, ro = torch.empty(E + 1, **i32), torch.empty(R + 1, **i32)
+    p2e, ec = torch.empty(E, **i32), torch.empty(E, **i32)
+    s2p, p2s = torch.empty(P + 1, **i32), torch.empty(T * k_max, **i32)
+    ws = torch.empty(abi().semmoe_permute_workspace_size(T, k_max, E), dtype=torch.uint8, device="cuda")
+    abi().semmoe_permute(torch.from_numpy(bad).cuda(), torch.from_numpy(er).cuda(), None, T, 0, E, R, k_max, P + 1,
+                         eo, ro, p2e, ec, s2p, p2s, None, ws)
+    with pytest.raises(abi().SemMoEError) as ei:
+        abi().semmoe_check_errors()
+    assert ei.value.bits & abi().SEMMOE_DEVERR_EXPERT
+    assert ei.value.bits & abi().SEMMOE_DEVERR_PAIRS   # P + 1 passed, P pairs live
+    assert int(p2s[7 * k_max + 1]) == -1
+    np.testing.assert_array_equal(np_(p2s), ref["pair_to_sorted"])
+    np.testing.assert_array_equal(np_(s2p[:P]), ref["sorted_to_pair"])
+    np.testing.assert_array_equal(np_(eo), ref["expert_offsets"])
