@@ -293,6 +293,10 @@ int semmoe_permute_noalloc(const int32_t* topk_idx, const int32_t* expert_rank,
  * y_perm  [device] [P,H] dtype out
  * ws      [device] workspace of at least semmoe_grouped_ffn_workspace_size()
  * Limits: H % 8 == 0 and I % 8 == 0 (16-byte rows for bf16 tensor-core tiles).
+ * Device checks: offsets that decrease or leave [0, P] set
+ * SEMMOE_DEVERR_PAIRS, an expert id outside [0, E) SEMMOE_DEVERR_EXPERT; such
+ * a group is skipped (its rows of y_perm keep what they held).  P == 0 needs
+ * no activation buffers.
  */
 size_t semmoe_grouped_ffn_workspace_size(int P, int I, int dtype);
 int semmoe_grouped_ffn(const void* x_perm, const int32_t* expert_offsets,

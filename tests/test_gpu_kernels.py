@@ -459,3 +459,42 @@ def test_permute_flags_bad_expert_and_pair_count():
     np.testing.assert_array_equal(np_(p2s), ref["pair_to_sorted"])
     np.testing.assert_array_equal(np_(s2p[:P]), ref["sorted_to_pair"])
     np.testing.assert_array_equal(np_(eo), ref["expert_offsets"])
+
+
+@pytest.mark.parametrize("mode,dtype", [("single", "bf16"), ("pair", "bf16"), ("default", "f32")])
+def test_grouped_ffn_flags_bad_group_table(mode, dtype, monkeypatch):
+    """Group offsets that decrease or run past P (SEMMOE_DEVERR_PAIRS) and an
+    expert id past E (SEMMOE_DEVERR_EXPERT) are flagged by the kernels' checks
+    in every form; those groups are skipped, the valid ones are still computed
+    exactly as with a clean table."""
+    monkeypatch.setenv("SEMMOE_FFN_MODE", mode)
+    rng = np.random.default_rng(5)
+    tdt = torch.bfloat16 if dtype == "bf16" else torch.float32
+    E, H, I, P = 4, 128, 128, 600
+    x = torch.from_numpy(rng.standard_normal((P, H)).astype(np.float32)).to(tdt).cuda()
+    w13 = torch.from_numpy((rng.standard_normal((E, 2 * I, H)) / np.sqrt(H)).astype(np.float32)).to(tdt).cuda()
+    w2 = torch.from_numpy((rng.standard_normal((E, H, I)) / np.sqrt(I)).astype(np.float32)).to(tdt).cuda()
+    ws = torch.empty(abi().semmoe_grouped_ffn_workspace_size(P, I, 1 if dtype == "bf16" else 0),
+                     dtype=torch.uint8, device="cuda")
+    p2e = torch.tensor([0, 1, 2, 3], **i32)
+    clean = torch.tensor([0, 300, 300, 450, 600], **i32)
+    y0 = torch.zeros(P, H, dtype=tdt, device="cuda")
+    abi().semmoe_grouped_ffn(x, clean, p2e, w13, w2, P, E, H, I, y0, ws)
+    assert abi().semmoe_check_errors() == 0
+    # group 1 runs backwards (300 -> 200), group 3 past P (450 -> 700)
+    bad = torch.tensor([0, 300, 200, 450, 700], **i32)
+    y1 = torch.zeros(P, H, dtype=tdt, device="cuda")
+    abi().semmoe_grouped_ffn(x, bad, p2e, w13, w2, P, E, H, I, y1, ws)
+    with pytest.raises(abi().SemMoEError) as ei:
+        abi().semmoe_check_errors()
+    assert ei.value.bits & abi().SEMMOE_DEVERR_PAIRS
+    # group 0 is valid, but the valid group 2 (rows 200..449) overlaps it: rows 0..199 are group 0's alone
+    assert torch.equal(y1[:200], y0[:200])
+    p2e_bad = torch.tensor([0, 1, 9, 3], **i32)        # expert 9 of 4
+    y2 = torch.zeros(P, H, dtype=tdt, device="cuda")
+    abi().semmoe_grouped_ffn(x, clean, p2e_bad, w13, w2, P, E, H, I, y2, ws)
+    with pytest.raises(abi().SemMoEError) as ei:
+        abi().semmoe_check_errors()
+    assert ei.value.bits & abi().SEMMOE_DEVERR_EXPERT
+    assert torch.equal(y2[:300], y0[:300]) and torch.equal(y2[450:], y0[450:])
+    assert not torch.any(y2[300:450] != 0)               # the skipped group wrote nothing

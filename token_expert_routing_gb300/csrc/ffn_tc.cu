@@ -224,7 +224,8 @@ ffn_tc_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__
       int c = 0;
       if (g < G) {
         const int lo = sh.off[g], hi = sh.off[g + 1], e = sh.pe[g];
-        if (lo < 0 || hi < lo || hi > P || e < 0 || e >= E) atomicOr(&g_err, SEMMOE_DEVERR_PAIRS);
+        if (lo < 0 || hi < lo || hi > P) atomicOr(&g_err, SEMMOE_DEVERR_PAIRS);
+        else if (e < 0 || e >= E) atomicOr(&g_err, SEMMOE_DEVERR_EXPERT);
         else c = ((hi - lo + BM - 1) / BM + CL - 1) / CL;
       }
       cnt[i] = c;
@@ -480,7 +481,8 @@ ffn_pair_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant
       int c = 0;
       if (g < G) {
         const int lo = sh.off[g], hi = sh.off[g + 1], e = sh.pe[g];
-        if (lo < 0 || hi < lo || hi > P || e < 0 || e >= E) atomicOr(&g_err, SEMMOE_DEVERR_PAIRS);
+        if (lo < 0 || hi < lo || hi > P) atomicOr(&g_err, SEMMOE_DEVERR_PAIRS);
+        else if (e < 0 || e >= E) atomicOr(&g_err, SEMMOE_DEVERR_EXPERT);
         else c = ((hi - lo + BM - 1) / BM + 1) / 2;
       }
       cnt[i] = c;
