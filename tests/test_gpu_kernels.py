@@ -19,14 +19,17 @@ def abi():
     return _abi
 
 
-def route_logits_in(logits, k, k_max):
+def route_logits_in(logits, k, k_max, expect_clean=True):
     T, E = logits.shape
     li = torch.as_tensor(logits, dtype=torch.float32).cuda()
     kpt = torch.as_tensor(k, dtype=torch.int32).cuda()
     idx = torch.empty(T, k_max, **i32)
     w = torch.empty(T, k_max, dtype=torch.float32, device="cuda")
     abi().semmoe_route(None, None, li, None, kpt, 0, T, 0, E, k_max, idx, w)
-    assert abi().semmoe_check_errors() == 0
+    if expect_clean:
+        assert abi().semmoe_check_errors() == 0
+    else:
+        torch.cuda.synchronize()
     return np_(idx), np_(w)
 
 
@@ -498,3 +501,46 @@ def test_grouped_ffn_flags_bad_group_table(mode, dtype, monkeypatch):
     assert ei.value.bits & abi().SEMMOE_DEVERR_EXPERT
     assert torch.equal(y2[:300], y0[:300]) and torch.equal(y2[450:], y0[450:])
     assert not torch.any(y2[300:450] != 0)               # the skipped group wrote nothing
+
+
+def test_route_nonfinite_logits_are_skipped_and_flagged():
+    """NaN and ±inf logits count as -inf (never picked while finite ones are
+    left) and set SEMMOE_DEVERR_NONFINITE; the picks and gates equal the
+    oracle's on the logits with those entries set to -inf."""
+    rng = np.random.default_rng(17)
+    T, E, k_max = 200, 16, 4
+    lg = rng.standard_normal((T, E)).astype(np.float32)
+    lg[3, 5], lg[10, 0], lg[11, 2], lg[12, 7] = np.nan, np.inf, -np.inf, np.nan
+    k = rng.integers(1, k_max + 1, size=T).astype(np.int32)
+    idx, w = route_logits_in(lg, k, k_max, expect_clean=False)
+    with pytest.raises(abi().SemMoEError) as ei:
+        abi().semmoe_check_errors()
+    assert ei.value.bits & abi().SEMMOE_DEVERR_NONFINITE
+    clean = np.where(np.isfinite(lg), lg, np.float32(-np.inf)).astype(np.float32)
+    ref_idx, ref_w = oracle.topk_route(clean, k, k_max)
+    np.testing.assert_array_equal(idx, ref_idx)
+    np.testing.assert_allclose(w, ref_w, rtol=0, atol=GATE_ATOL)
+
+
+def test_combine_skips_and_flags_a_slot_past_P():
+    """A pair_to_sorted entry >= P is skipped and flagged; the token's sum runs
+    over its other slots, exactly as the oracle's with that slot as padding."""
+    rng = np.random.default_rng(23)
+    T, E, k_max, H = 50, 8, 3, 64
+    idx, k = _route_random(rng, T, E, k_max)
+    _, w = oracle.topk_route(rng.standard_normal((T, E)), k, k_max)
+    perm = oracle.permute(idx, k, np.arange(E) % 4, 4)
+    P = int(k.sum())
+    y = torch.from_numpy(rng.standard_normal((P, H)).astype(np.float32)).cuda()
+    p2s = perm["pair_to_sorted"].astype(np.int32).copy()
+    p2s[4] = P + 10                        # token 1, slot 1 (k_max = 3)
+    out = torch.full((T, H), 9.0, device="cuda")
+    abi().semmoe_combine(y, torch.from_numpy(p2s).cuda(), torch.from_numpy(w.astype(np.float32)).cuda(), None,
+                         T, H, k_max, P, out)
+    with pytest.raises(abi().SemMoEError) as ei:
+        abi().semmoe_check_errors()
+    assert ei.value.bits & abi().SEMMOE_DEVERR_PAIRS
+    w_ref = w.copy()
+    w_ref[1, 1] = 0.0                      # the skipped slot contributes nothing
+    ref = oracle.combine(np_(y), perm["pair_to_sorted"], w_ref, k, "f32")
+    assert max_rel(np_(out), ref) < 1e-6
