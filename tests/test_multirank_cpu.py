@@ -45,3 +45,24 @@ def test_single_rank_needs_no_process_group(monkeypatch):
         monkeypatch.delenv(k, raising=False)
     assert bench._dist() == (1, 0, 0)
     assert bench._max_over_ranks(1, 3.5) == 3.5
+
+
+def test_reference_arm_under_two_ranks_prints_once():
+    """`bench.py --impl reference` launched as two ranks (gloo on the CPU):
+    rank 0 times the oracle and prints the one JSON line, the other rank exits
+    0 without work."""
+    import json
+    import subprocess
+    import sys
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1", "--nproc-per-node", "2",
+           "--master-addr", "127.0.0.1", "--master-port", str(_free_port()), "bench.py", "--impl", "reference",
+           "--gpus", "2", "--config", "tiny_fp32_T256_E8", "--steps", "1", "--warmup", "3", "--ref-tokens", "16"]
+    env = dict(os.environ, CUDA_VISIBLE_DEVICES="")
+    r = subprocess.run(cmd, cwd=root, env=env, capture_output=True, text=True, timeout=300)
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [ln for ln in r.stdout.splitlines() if ln.startswith("{")]
+    assert len(lines) == 1, r.stdout
+    line = json.loads(lines[0])
+    assert line["impl"] == "reference" and line["n_gpus"] == 2 and line["value"] > 0
+    assert line["cpu_baseline"]["kind"] == "oracle" and line["e2e"]["h2d_bytes_per_step"] == 0
