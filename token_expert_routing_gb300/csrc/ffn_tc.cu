@@ -745,21 +745,42 @@ cudaError_t launch_pair(const CUtensorMap& ma, const CUtensorMap& mb, const CUte
 
 int ffn_tc_take_errors(cudaStream_t s, int* bits) { return take_error_word(g_err, s, bits); }
 
-// Grouped-GEMM form: 0 = independent CTAs; 1 = pairs sharing weight tiles by
-// multicast; 2 / 3 = 2-SM MMA pairs with one / two accumulator buffers.
-// Default: 2-SM pairs when tiles are long (I >= 512) and groups average at
-// least two m-tiles (P >= 256 G; a pair covers two m-tiles of one group, so
-// smaller groups leave half of it idle), independent CTAs otherwise;
-// SEMMOE_FFN_MODE=single|multicast|pair1|pair overrides it.
-static int ffn_mode(int I, int P, int G) {
+// Grouped-GEMM form, chosen per GEMM: 0 = independent CTAs; 1 = pairs sharing
+// weight tiles by multicast; 2 / 3 = 2-SM MMA pairs with one / two accumulator
+// buffers.  A pair covers two m-tiles of one group, so short groups leave half
+// of it idle.  Defaults: GEMM1 (K = H) in 2-SM pairs when the groups average at
+// least 512 rows (P >= 512 G), GEMM2 (K = I) when I >= 512 and they average at
+// least 256 (P >= 256 G), independent CTAs otherwise (measured per GEMM on the
+// DeepSeek, Qwen3 and MoE-Prism shapes).  SEMMOE_FFN_MODE=single|multicast|
+// pair1|pair sets both.
+static void ffn_modes(int I, int P, int G, int* m1, int* m2) {
   const char* v = getenv("SEMMOE_FFN_MODE");
   if (v != nullptr) {
-    if (strcmp(v, "single") == 0) return 0;
-    if (strcmp(v, "multicast") == 0) return 1;
-    if (strcmp(v, "pair1") == 0) return 2;
-    if (strcmp(v, "pair") == 0) return 3;
+    int m = -1;
+    if (strcmp(v, "single") == 0) m = 0;
+    if (strcmp(v, "multicast") == 0) m = 1;
+    if (strcmp(v, "pair1") == 0) m = 2;
+    if (strcmp(v, "pair") == 0) m = 3;
+    if (m >= 0) {
+      *m1 = *m2 = m;
+      return;
+    }
   }
-  return (I >= 512 && (long long)P >= 2LL * BM * G) ? 3 : 0;
+  *m1 = (long long)P >= 4LL * BM * G ? 3 : 0;
+  *m2 = (I >= 512 && (long long)P >= 2LL * BM * G) ? 3 : 0;
+}
+
+// One GEMM of the FFN in form `mode`.
+template <bool GLU>
+static cudaError_t launch_gemm(int mode, const CUtensorMap& ma, const CUtensorMap& mb, const CUtensorMap& mo,
+                               const int32_t* offsets, const int32_t* p2e, int G, int P, int E, int N, int K,
+                               int n_tiles, Gather ga, __nv_bfloat16* out, cudaStream_t s) {
+  switch (mode) {
+    case 1: return launch_one<GLU, 2>(ma, mb, mo, offsets, p2e, G, P, E, N, K, n_tiles, ga, out, s);
+    case 2: return launch_pair<GLU, 1>(ma, mb, mo, offsets, p2e, G, P, E, N, K, n_tiles, ga, out, s);
+    case 3: return launch_pair<GLU, 2>(ma, mb, mo, offsets, p2e, G, P, E, N, K, n_tiles, ga, out, s);
+    default: return launch_one<GLU, 1>(ma, mb, mo, offsets, p2e, G, P, E, N, K, n_tiles, ga, out, s);
+  }
 }
 
 // gather_rows != nullptr: x is the unpermuted [T_x, H] activation and sorted row
@@ -769,8 +790,9 @@ cudaError_t launch_ffn_tc(const void* x, const int32_t* offsets, const int32_t* 
                           int gather_div, int T_x, cudaStream_t s) {
   if (P == 0) return cudaSuccess;
   const int G = offsets ? E : 1;
-  const int mode = ffn_mode(I, P, G);
-  const int CL = mode == 0 ? 1 : 2;
+  int mode1 = 0, mode2 = 0;
+  ffn_modes(I, P, G, &mode1, &mode2);
+  const int CL = mode2 == 0 ? 1 : 2;  // CTAs sharing GEMM2's weight tile
   const cuuint64_t es = 2;
   CUtensorMap ma1, mb1, ma2, mb2;
   Gather ga;
@@ -823,25 +845,9 @@ cudaError_t launch_ffn_tc(const void* x, const int32_t* offsets, const int32_t* 
   }
   __nv_bfloat16* h = static_cast<__nv_bfloat16*>(ws);
   __nv_bfloat16* yb = static_cast<__nv_bfloat16*>(y);
-  cudaError_t e;
-  if (mode == 1) {
-    e = launch_one<true, 2>(ma1, mb1, mo1, offsets, p2e, G, P, E, I, H, (I + 127) / 128, ga, h, s);
-    if (e != cudaSuccess) return e;
-    return launch_one<false, 2>(ma2, mb2, mo2, offsets, p2e, G, P, E, H, I, (H + BN - 1) / BN, Gather(), yb, s);
-  }
-  if (mode == 2) {
-    e = launch_pair<true, 1>(ma1, mb1, mo1, offsets, p2e, G, P, E, I, H, (I + 127) / 128, ga, h, s);
-    if (e != cudaSuccess) return e;
-    return launch_pair<false, 1>(ma2, mb2, mo2, offsets, p2e, G, P, E, H, I, (H + BN - 1) / BN, Gather(), yb, s);
-  }
-  if (mode == 3) {
-    e = launch_pair<true, 2>(ma1, mb1, mo1, offsets, p2e, G, P, E, I, H, (I + 127) / 128, ga, h, s);
-    if (e != cudaSuccess) return e;
-    return launch_pair<false, 2>(ma2, mb2, mo2, offsets, p2e, G, P, E, H, I, (H + BN - 1) / BN, Gather(), yb, s);
-  }
-  e = launch_one<true, 1>(ma1, mb1, mo1, offsets, p2e, G, P, E, I, H, (I + 127) / 128, ga, h, s);
+  cudaError_t e = launch_gemm<true>(mode1, ma1, mb1, mo1, offsets, p2e, G, P, E, I, H, (I + 127) / 128, ga, h, s);
   if (e != cudaSuccess) return e;
-  return launch_one<false, 1>(ma2, mb2, mo2, offsets, p2e, G, P, E, H, I, (H + BN - 1) / BN, Gather(), yb, s);
+  return launch_gemm<false>(mode2, ma2, mb2, mo2, offsets, p2e, G, P, E, H, I, (H + BN - 1) / BN, Gather(), yb, s);
 }
 
 }  // namespace semmoe
