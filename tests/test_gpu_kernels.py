@@ -544,3 +544,30 @@ def test_combine_skips_and_flags_a_slot_past_P():
     w_ref[1, 1] = 0.0                      # the skipped slot contributes nothing
     ref = oracle.combine(np_(y), perm["pair_to_sorted"], w_ref, k, "f32")
     assert max_rel(np_(out), ref) < 1e-6
+
+
+@pytest.mark.parametrize("P,E,I", [(5000, 8, 352),    # groups of ~625 rows, I < 512: GEMM1 in pairs, GEMM2 single
+                                   (4000, 10, 640)])  # groups of ~400 rows, I >= 512: GEMM1 single, GEMM2 in pairs
+def test_grouped_ffn_mixed_default_forms_match_single(P, E, I, monkeypatch):
+    """The default per-GEMM form choice mixes the 2-SM and single-CTA forms
+    within one call; the result is bit-identical to both GEMMs single-CTA."""
+    rng = np.random.default_rng(P + I)
+    H = 256
+    cuts = np.sort(rng.integers(0, P, size=E - 1))
+    eo = torch.from_numpy(np.concatenate([[0], cuts, [P]]).astype(np.int32)).cuda()
+    p2e = torch.from_numpy(rng.permutation(E).astype(np.int32)).cuda()
+    x = torch.from_numpy(rng.standard_normal((P, H)).astype(np.float32)).to(torch.bfloat16).cuda()
+    w13 = torch.from_numpy((rng.standard_normal((E, 2 * I, H)) / np.sqrt(H)).astype(np.float32)).to(torch.bfloat16).cuda()
+    w2 = torch.from_numpy((rng.standard_normal((E, H, I)) / np.sqrt(I)).astype(np.float32)).to(torch.bfloat16).cuda()
+    ws = torch.empty(abi().semmoe_grouped_ffn_workspace_size(P, I, 1), dtype=torch.uint8, device="cuda")
+    outs = []
+    for mode in (None, "single"):
+        if mode is None:
+            monkeypatch.delenv("SEMMOE_FFN_MODE", raising=False)
+        else:
+            monkeypatch.setenv("SEMMOE_FFN_MODE", mode)
+        y = torch.full((P, H), 7.0, dtype=torch.bfloat16, device="cuda")
+        abi().semmoe_grouped_ffn(x, eo, p2e, w13, w2, P, E, H, I, y, ws)
+        assert abi().semmoe_check_errors() == 0
+        outs.append(y.cpu())
+    assert torch.equal(outs[0], outs[1])
