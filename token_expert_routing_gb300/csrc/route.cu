@@ -91,13 +91,19 @@ __device__ __forceinline__ void warp_load_logits(const float* row, int ks, size_
 }
 
 // k_t rounds of a warp argmax over (score descending, index ascending) of the
-// n scores in v, skipping those already taken.  Lane 0 writes the j-th pick to
-// my_v[j] / my_e[j] (-1 when fewer than k_t scores are left, flagged).
-// Each score becomes an order-preserving 32-bit key (-0.0 counted as +0.0; key 0
-// marks padding and taken scores, below every float including -inf), so a round
-// is two warp reductions: the largest key, then the lowest index holding it.
+// n scores in v.  Lane 0 writes the j-th pick to my_v[j] / my_e[j] (-1 when
+// fewer than k_t scores are left, flagged).  Each score becomes an
+// order-preserving 32-bit key (-0.0 counted as +0.0; key 0 marks padding,
+// below every float including -inf).  Two forms with the same picks: rescanning
+// the lane's keys every round (cheaper for 2-4 scores per lane), or sorting them
+// once (13% faster than rescanning at 8 per lane, E = 256, k <= 24; 3-6% slower
+// at 2-4).
+
+// Few scores per lane (NPER <= 4): each round rescans the lane's keys -- two
+// warp reductions (the largest key, then the lowest index holding it), and the
+// picked score's key becomes 0 (taken).
 template <int NPER>
-__device__ __forceinline__ void warp_select(const float (&v)[NPER], int n, int kt, float* my_v, int* my_e) {
+__device__ __forceinline__ void warp_select_rescan(const float (&v)[NPER], int n, int kt, float* my_v, int* my_e) {
   const int lane = threadIdx.x % 32;
   uint32_t key[NPER];
 #pragma unroll
@@ -129,6 +135,60 @@ __device__ __forceinline__ void warp_select(const float (&v)[NPER], int n, int k
     }
   }
   __syncwarp();
+}
+
+// Many scores per lane (NPER >= 8): each score's key is packed with its inverted
+// index into a 64-bit word that orders (score descending, index ascending).
+// Each lane sorts its NPER words once; a round is then two warp reductions over
+// the lanes' heads (the largest key, then the lowest index holding it) and the
+// winning lane drops its head.  A head with the round's key is its lane's
+// lowest index with that key, so the lowest index among heads is the lowest
+// overall.
+template <int NPER>
+__device__ __forceinline__ void warp_select_sorted(const float (&v)[NPER], int n, int kt, float* my_v, int* my_e) {
+  const int lane = threadIdx.x % 32;
+  unsigned long long c[NPER];
+#pragma unroll
+  for (int i = 0; i < NPER; ++i) {
+    const uint32_t b = __float_as_uint(__fadd_rn(v[i], 0.0f));  // -0.0 -> +0.0
+    const uint32_t key = lane + 32 * i < n ? ((b & 0x80000000u) ? ~b : (b | 0x80000000u)) : 0u;
+    c[i] = key == 0u ? 0ull : ((unsigned long long)key << 32) | (uint32_t)~(uint32_t)(lane + 32 * i);
+  }
+#pragma unroll
+  for (int i = 1; i < NPER; ++i)  // insertion network: c[0] >= c[1] >= ...
+#pragma unroll
+    for (int j = i; j > 0; --j) {
+      const unsigned long long a = c[j - 1], d = c[j];
+      c[j - 1] = a > d ? a : d;
+      c[j] = a > d ? d : a;
+    }
+  for (int j = 0; j < kt; ++j) {
+    const uint32_t hk = (uint32_t)(c[0] >> 32);
+    const uint32_t m = __reduce_max_sync(0xffffffffu, hk);
+    int be = -1;
+    if (m != 0u) {
+      const uint32_t mine = hk == m ? ~(uint32_t)c[0] : 0xffffffffu;  // the head's index
+      be = (int)__reduce_min_sync(0xffffffffu, mine);
+      if (mine == (uint32_t)be) {  // this lane's head is the pick: drop it
+#pragma unroll
+        for (int i = 0; i + 1 < NPER; ++i) c[i] = c[i + 1];
+        c[NPER - 1] = 0ull;
+      }
+    } else if (lane == 0) {
+      flag(SEMMOE_DEVERR_NONFINITE);  // fewer than kt scores
+    }
+    if (lane == 0) {
+      my_v[j] = be >= 0 ? __uint_as_float((m & 0x80000000u) ? (m ^ 0x80000000u) : ~m) : -INFINITY;
+      my_e[j] = be;
+    }
+  }
+  __syncwarp();
+}
+
+template <int NPER>
+__device__ __forceinline__ void warp_select(const float (&v)[NPER], int n, int kt, float* my_v, int* my_e) {
+  if constexpr (NPER >= 8) warp_select_sorted<NPER>(v, n, kt, my_v, my_e);
+  else warp_select_rescan<NPER>(v, n, kt, my_v, my_e);
 }
 
 // One warp routes token t: its logits (see warp_load_logits), k_t picks (see
