@@ -340,9 +340,18 @@ def test_grouped_ffn_gather_matches_permuted(dtype, T, E, k_max, H, I, monkeypat
                          p2e, ec, s2p, p2s, xp, ws)
     fws = torch.empty(abi().semmoe_grouped_ffn_workspace_size(P, I, 1 if dtype == "bf16" else 0), dtype=torch.uint8,
                       device="cuda")
-    modes = ("single", "multicast", "pair1", "pair") if dtype == "bf16" else ("default",)
+    modes = ("single", "single/tma-gather", "multicast", "pair1", "pair", "default") if dtype == "bf16" else ("default",)
     for mode in modes:
-        monkeypatch.setenv("SEMMOE_FFN_MODE", mode)
+        # single: gathering warps feed GEMM1; single/tma-gather: TMA four-row gathers;
+        # default: the gathered GEMM1's own form choice
+        if mode == "default":
+            monkeypatch.delenv("SEMMOE_FFN_MODE", raising=False)
+        else:
+            monkeypatch.setenv("SEMMOE_FFN_MODE", mode.split("/")[0])
+        if mode.endswith("tma-gather"):
+            monkeypatch.setenv("SEMMOE_GATHER_WARPS", "0")
+        else:
+            monkeypatch.delenv("SEMMOE_GATHER_WARPS", raising=False)
         y0 = torch.full((P, H), 3.0, dtype=tdt, device="cuda")
         y1 = torch.full((P, H), 5.0, dtype=tdt, device="cuda")
         abi().semmoe_grouped_ffn(xp, eo, p2e, w13, w2, P, E, H, I, y0, fws)
@@ -501,6 +510,46 @@ def test_grouped_ffn_flags_bad_group_table(mode, dtype, monkeypatch):
     assert ei.value.bits & abi().SEMMOE_DEVERR_EXPERT
     assert torch.equal(y2[:300], y0[:300]) and torch.equal(y2[450:], y0[450:])
     assert not torch.any(y2[300:450] != 0)               # the skipped group wrote nothing
+
+
+@pytest.mark.parametrize("producer", ["gather-warps", "tma-gather", "pair"])
+def test_grouped_ffn_gather_flags_bad_pair_id(producer, monkeypatch):
+    """A sorted_to_pair entry naming no token (negative, or a token past T)
+    sets SEMMOE_DEVERR_PAIRS in every gathering producer; that row reads token
+    0 instead, and every other row keeps the bits of the clean call."""
+    monkeypatch.setenv("SEMMOE_FFN_MODE", "pair" if producer == "pair" else "single")
+    if producer == "tma-gather":
+        monkeypatch.setenv("SEMMOE_GATHER_WARPS", "0")
+    rng = np.random.default_rng(23)
+    E, H, I, T, k_max = 4, 256, 128, 300, 2
+    P = T * k_max
+    x = torch.from_numpy(rng.standard_normal((T, H)).astype(np.float32)).to(torch.bfloat16).cuda()
+    w13 = torch.from_numpy((rng.standard_normal((E, 2 * I, H)) / np.sqrt(H)).astype(np.float32)).to(torch.bfloat16).cuda()
+    w2 = torch.from_numpy((rng.standard_normal((E, H, I)) / np.sqrt(I)).astype(np.float32)).to(torch.bfloat16).cuda()
+    ws = torch.empty(abi().semmoe_grouped_ffn_workspace_size(P, I, 1), dtype=torch.uint8, device="cuda")
+    eo = torch.tensor([0, 150, 300, 450, 600], **i32)
+    p2e = torch.tensor([0, 1, 2, 3], **i32)
+    s2p = torch.from_numpy(rng.permutation(P).astype(np.int32)).cuda()
+    y0 = torch.zeros(P, H, dtype=torch.bfloat16, device="cuda")
+    abi().semmoe_grouped_ffn_gather(x, s2p, k_max, T, eo, p2e, w13, w2, P, E, H, I, y0, ws)
+    assert abi().semmoe_check_errors() == 0
+    bad = s2p.clone()
+    bad[7], bad[301] = -5, T * k_max + 9               # no token; token T + 4 of T
+    y1 = torch.zeros(P, H, dtype=torch.bfloat16, device="cuda")
+    abi().semmoe_grouped_ffn_gather(x, bad, k_max, T, eo, p2e, w13, w2, P, E, H, I, y1, ws)
+    with pytest.raises(abi().SemMoEError) as ei:
+        abi().semmoe_check_errors()
+    assert ei.value.bits & abi().SEMMOE_DEVERR_PAIRS
+    keep = torch.ones(P, dtype=torch.bool)
+    keep[[7, 301]] = False
+    assert torch.equal(y1.cpu()[keep], y0.cpu()[keep])
+    # the flagged rows read token 0: the same bits as a clean map sending them to pair 0
+    ref_map = s2p.clone()
+    ref_map[7], ref_map[301] = 0, 0
+    y2 = torch.zeros(P, H, dtype=torch.bfloat16, device="cuda")
+    abi().semmoe_grouped_ffn_gather(x, ref_map, k_max, T, eo, p2e, w13, w2, P, E, H, I, y2, ws)
+    assert abi().semmoe_check_errors() == 0
+    assert torch.equal(y1.cpu(), y2.cpu())
 
 
 def test_route_nonfinite_logits_are_skipped_and_flagged():

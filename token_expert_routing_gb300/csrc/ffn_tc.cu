@@ -14,6 +14,9 @@
 //   warps 2..5  epilogue: tcgen05.ld the accumulator, SwiGLU / convert, stage
 //               32 x 64 bf16 blocks in shared memory and write them with TMA
 //               stores (a warp whose rows cross its group's end stores directly)
+//   warps 6..13 (GEMM1 gathering x rows, single-CTA form only): the A rows,
+//               fetched with 16-byte loads and stored in the swizzled layout;
+//               warp 0 then loads only the weight tile
 // Pipelines: a 4-stage smem ring (full/empty mbarriers) and a 2-deep TMEM
 // accumulator ring (tfull/tempty), so the epilogue of tile i overlaps the MMAs
 // of tile i+1.  GEMM1's B tile is 128 gate rows + the 128 matching up rows, so
@@ -176,13 +179,22 @@ __device__ __forceinline__ void gather_sources(const int32_t* __restrict__ gathe
   }
 }
 
-template <bool GLU, int CL>
-__global__ void __launch_bounds__(THREADS, 1)
+// GW > 0: GW more warps gather the A rows (x row gather[q] / gather_div) with
+// 16-byte loads into registers and shared-memory stores in the swizzled layout,
+// each lane then fencing for the async proxy and arriving on the stage barrier.
+// Against one warp issuing TMA four-row gathers this took the routed FFN from
+// 855 to 543 us (DeepSeek shape), 2148 to 1388 us (Qwen3), 1350 to 814 us
+// (MoE-Prism); tiled loads of a permuted copy still take 361 / 846 / 579 us.
+constexpr int GATHER_WARPS = 8;
+constexpr int RPL = 4;  // 16-byte pieces per lane per k-block: 8 warps x 32 lanes x 4 = 128 rows x 128 B
+template <bool GLU, int CL, int GW = 0>
+__global__ void __launch_bounds__(THREADS + 32 * GW, 1)
 ffn_tc_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b,
               const __grid_constant__ CUtensorMap map_out,
               const int32_t* __restrict__ offsets, const int32_t* __restrict__ phys_to_expert, int G, int P,
               int E, int N, int K, int n_tiles, const int32_t* __restrict__ gather, int gather_div, int gather_rows,
-              __nv_bfloat16* __restrict__ out) {
+              __nv_bfloat16* __restrict__ out, const __nv_bfloat16* __restrict__ gx) {
+  static_assert(GW == 0 || GW * 32 * RPL * 16 == BM * BK * 2, "gather warps cover one A stage");
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   const uint32_t pad = (1024u - (smem_u32(smem_raw) & 1023u)) & 1023u;
   unsigned char* stage_a = smem_raw + pad;                 // STAGES x [128 x 64] bf16
@@ -195,7 +207,7 @@ ffn_tc_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
-      mbar_init(&sh.full[s], 1);
+      mbar_init(&sh.full[s], 1 + 32 * GW);
       mbar_init(&sh.empty[s], CL);  // released by the MMA of every CTA that reads this stage
     }
     for (int a = 0; a < 2; ++a) {
@@ -209,8 +221,8 @@ ffn_tc_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__
     prefetch_map(&map_b);
     prefetch_map(&map_out);
   }
-  for (int g = threadIdx.x; g <= G; g += THREADS) sh.off[g] = offsets ? offsets[g] : (g == 0 ? 0 : P);
-  for (int g = threadIdx.x; g < G; g += THREADS) sh.pe[g] = phys_to_expert ? phys_to_expert[g] : 0;
+  for (int g = threadIdx.x; g <= G; g += blockDim.x) sh.off[g] = offsets ? offsets[g] : (g == 0 ? 0 : P);
+  for (int g = threadIdx.x; g < G; g += blockDim.x) sh.pe[g] = phys_to_expert ? phys_to_expert[g] : 0;
   __syncthreads();
 
   if (warp == 1) {  // whole warp: allocate all 512 TMEM columns
@@ -264,22 +276,25 @@ ffn_tc_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__
   if (warp == 0) {
     // ---------------- TMA producer (warp 0; lane 0 unless A rows are gathered) ----------------
     uint32_t it = 0;
-    if (gather != nullptr || lane == 0)  // without row gathers lane 0 alone: 1% faster than the warp
+    const int32_t* tg = GW > 0 ? nullptr : gather;  // TMA row gathers only without gathering warps
+    if (tg != nullptr || lane == 0)  // without row gathers lane 0 alone: 1% faster than the warp
     for (int tile = unit0; tile < total; tile += units) {
       if (*abort_flag) break;
       const int mt = tile / n_tiles, nt = tile % n_tiles;
       int row0, rows, e;
       decode_mtile<CL>(sh, G, mt, rank, row0, rows, e);
       int src[4] = {0, 0, 0, 0};
-      if (gather != nullptr) gather_sources(gather, gather_div, gather_rows, P, row0, lane, src);
+      if (tg != nullptr) gather_sources(tg, gather_div, gather_rows, P, row0, lane, src);
       bool ok = true;
       for (int kb = 0; kb < kb_n; ++kb) {
         const int s = it % STAGES;
         const uint32_t ph = (it / STAGES) & 1;
         int good = 1;
         if (lane == 0) good = mbar_wait(&sh.empty[s], ph ^ 1, abort_flag, &g_err);
-        if (gather != nullptr ? !__shfl_sync(0xffffffffu, good, 0) : !good) { ok = false; break; }
-        if (gather != nullptr) {
+        if (tg != nullptr ? !__shfl_sync(0xffffffffu, good, 0) : !good) { ok = false; break; }
+        if (GW > 0) {
+          mbar_expect_tx(&sh.full[s], B_BYTES);
+        } else if (tg != nullptr) {
           if (lane == 0) mbar_expect_tx(&sh.full[s], STAGE_BYTES);
           tma_gather4(stage_a + s * A_BYTES + lane * 4 * (BK * 2), &map_a, &sh.full[s], kb * BK, src[0], src[1],
                       src[2], src[3]);
@@ -343,7 +358,7 @@ ffn_tc_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__
       commit(&sh.done);          // every MMA issued above has completed ...
       mbar_drain(&sh.done, 0, &g_err);      // ... before TMEM can be released
     }
-  } else {
+  } else if (warp < 6) {
     // ---------------- epilogue (warps 2..5) ----------------
     const int q = warp & 3;           // TMEM lane quarter this warp may access
     const int r = q * 32 + lane;      // tile row held by this thread
@@ -399,6 +414,76 @@ ffn_tc_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__
       ++acc_it;
     }
     if (lane == 0) bulk_wait_all();  // this warp's output stores are complete
+  } else if (GW > 0) {
+    // ---------------- row-gathering warps (6 .. 5 + GW) ----------------
+    // Lane l copies 16-byte piece l & 7 of rows gw * 16 + 4 j + (l >> 3), j < RPL,
+    // into the layout a 128-byte-swizzled TMA load of the [128 x 64] box writes
+    // (piece c of row r at piece c ^ (r & 7)).  The loads of the next k-block are
+    // in flight while this one waits for its stage.
+    const int gw = warp - 6, c = lane & 7;
+    const __nv_bfloat16* cur[RPL];
+    const __nv_bfloat16* nxt[RPL];
+    uint4 vc[RPL], vn[RPL];
+    auto sources = [&](int t, const __nv_bfloat16* (&p)[RPL]) {
+      int row0, rows, e;
+      decode_mtile<1>(sh, G, t / n_tiles, 0, row0, rows, e);
+#pragma unroll
+      for (int j = 0; j < RPL; ++j) {
+        const int q = row0 + gw * (BM / GW) + 4 * j + (lane >> 3);
+        int r = 0;
+        if (q < P) {
+          const int pid = gather[q];
+          r = pid >= 0 ? pid / gather_div : -1;
+          if (r < 0 || r >= gather_rows) {
+            atomicOr(&g_err, SEMMOE_DEVERR_PAIRS);
+            r = 0;
+          }
+        }
+        p[j] = gx + (size_t)r * K;
+      }
+    };
+    auto fetch = [&](const __nv_bfloat16* const (&p)[RPL], int kb, uint4 (&v)[RPL]) {
+      const int col = kb * BK + c * 8;
+#pragma unroll
+      for (int j = 0; j < RPL; ++j)
+        v[j] = col < K ? __ldg(reinterpret_cast<const uint4*>(p[j] + col)) : make_uint4(0, 0, 0, 0);
+    };
+    int tile = unit0, kb = 0;
+    if (tile < total) {
+      sources(tile, cur);
+      fetch(cur, 0, vc);
+    }
+    uint32_t it = 0;
+    while (tile < total) {
+      int ntile = tile, nkb = kb + 1;
+#pragma unroll
+      for (int j = 0; j < RPL; ++j) nxt[j] = cur[j];
+      if (nkb == kb_n) {
+        nkb = 0;
+        ntile += units;
+        if (ntile < total) sources(ntile, nxt);
+      }
+      if (ntile < total) fetch(nxt, nkb, vn);
+      const int s = it % STAGES;
+      const uint32_t ph = (it / STAGES) & 1;
+      if (!mbar_wait(&sh.empty[s], ph ^ 1, abort_flag, &g_err)) break;
+      unsigned char* a = stage_a + s * A_BYTES;
+#pragma unroll
+      for (int j = 0; j < RPL; ++j) {
+        const int r = gw * (BM / GW) + 4 * j + (lane >> 3);
+        *reinterpret_cast<uint4*>(a + r * 128 + ((c ^ (r & 7)) << 4)) = vc[j];
+      }
+      fence_async_smem();
+      mbar_arrive(&sh.full[s]);
+      ++it;
+      tile = ntile;
+      kb = nkb;
+#pragma unroll
+      for (int j = 0; j < RPL; ++j) {
+        cur[j] = nxt[j];
+        vc[j] = vn[j];
+      }
+    }
   }
 
   fence_before();
@@ -662,14 +747,15 @@ ffn_pair_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant
 struct Gather {
   const int32_t* rows = nullptr;
   int div = 1, n = 0;
+  const __nv_bfloat16* x = nullptr;
 };
 
-template <bool GLU, int CL>
+template <bool GLU, int CL, int GW = 0>
 cudaError_t launch_one(const CUtensorMap& ma, const CUtensorMap& mb, const CUtensorMap& mo, const int32_t* offsets,
                        const int32_t* p2e,
                        int G, int P, int E, int N, int K, int n_tiles, Gather ga, __nv_bfloat16* out,
                        cudaStream_t s) {
-  auto kern = ffn_tc_kernel<GLU, CL>;
+  auto kern = ffn_tc_kernel<GLU, CL, GW>;
   static std::atomic<unsigned long long> smem_set{0};
   cudaError_t e = ensure_smem_limit(kern, (int)kSmemBytes, smem_set);
   if (e != cudaSuccess) return e;
@@ -677,8 +763,8 @@ cudaError_t launch_one(const CUtensorMap& ma, const CUtensorMap& mb, const CUten
   if (CL == 1) {
     int grid = sm_count();
     if (max_units < grid) grid = (int)max_units;
-    kern<<<grid, THREADS, kSmemBytes, s>>>(ma, mb, mo, offsets, p2e, G, P, E, N, K, n_tiles, ga.rows, ga.div, ga.n,
-                                           out);
+    kern<<<grid, THREADS + 32 * GW, kSmemBytes, s>>>(ma, mb, mo, offsets, p2e, G, P, E, N, K, n_tiles, ga.rows,
+                                                     ga.div, ga.n, out, ga.x);
   } else {
     cudaLaunchConfig_t cfg = {};
     cudaLaunchAttribute attr[1];
@@ -699,7 +785,8 @@ cudaError_t launch_one(const CUtensorMap& ma, const CUtensorMap& mb, const CUten
     long long units = clusters;
     if (max_units < units) units = max_units;
     cfg.gridDim = dim3((unsigned)(units * CL));
-    e = cudaLaunchKernelEx(&cfg, kern, ma, mb, mo, offsets, p2e, G, P, E, N, K, n_tiles, ga.rows, ga.div, ga.n, out);
+    e = cudaLaunchKernelEx(&cfg, kern, ma, mb, mo, offsets, p2e, G, P, E, N, K, n_tiles, ga.rows, ga.div, ga.n, out,
+                           ga.x);
     if (e != cudaSuccess) return e;
   }
   count_launches(1);
@@ -751,9 +838,11 @@ int ffn_tc_take_errors(cudaStream_t s, int* bits) { return take_error_word(g_err
 // of it idle.  Defaults: GEMM1 (K = H) in 2-SM pairs when the groups average at
 // least 512 rows (P >= 512 G), GEMM2 (K = I) when I >= 512 and they average at
 // least 256 (P >= 256 G), independent CTAs otherwise (measured per GEMM on the
-// DeepSeek, Qwen3 and MoE-Prism shapes).  SEMMOE_FFN_MODE=single|multicast|
-// pair1|pair sets both.
-static void ffn_modes(int I, int P, int G, int* m1, int* m2) {
+// DeepSeek, Qwen3 and MoE-Prism shapes).  A GEMM1 that gathers its rows runs
+// in the single-CTA form, where gathering warps feed it (1.6x faster than the
+// pairs' TMA row gathers).  SEMMOE_FFN_MODE=single|multicast|pair1|pair sets
+// both.
+static void ffn_modes(int I, int P, int G, bool gathered, int* m1, int* m2) {
   const char* v = getenv("SEMMOE_FFN_MODE");
   if (v != nullptr) {
     int m = -1;
@@ -766,7 +855,7 @@ static void ffn_modes(int I, int P, int G, int* m1, int* m2) {
       return;
     }
   }
-  *m1 = (long long)P >= 4LL * BM * G ? 3 : 0;
+  *m1 = !gathered && (long long)P >= 4LL * BM * G ? 3 : 0;
   *m2 = (I >= 512 && (long long)P >= 2LL * BM * G) ? 3 : 0;
 }
 
@@ -779,7 +868,13 @@ static cudaError_t launch_gemm(int mode, const CUtensorMap& ma, const CUtensorMa
     case 1: return launch_one<GLU, 2>(ma, mb, mo, offsets, p2e, G, P, E, N, K, n_tiles, ga, out, s);
     case 2: return launch_pair<GLU, 1>(ma, mb, mo, offsets, p2e, G, P, E, N, K, n_tiles, ga, out, s);
     case 3: return launch_pair<GLU, 2>(ma, mb, mo, offsets, p2e, G, P, E, N, K, n_tiles, ga, out, s);
-    default: return launch_one<GLU, 1>(ma, mb, mo, offsets, p2e, G, P, E, N, K, n_tiles, ga, out, s);
+    default:
+      if constexpr (GLU) {  // gathered rows: gathering warps unless SEMMOE_GATHER_WARPS=0 (TMA row gathers)
+        const char* gwv = getenv("SEMMOE_GATHER_WARPS");
+        if (ga.rows != nullptr && !(gwv != nullptr && atoi(gwv) == 0))
+          return launch_one<GLU, 1, GATHER_WARPS>(ma, mb, mo, offsets, p2e, G, P, E, N, K, n_tiles, ga, out, s);
+      }
+      return launch_one<GLU, 1>(ma, mb, mo, offsets, p2e, G, P, E, N, K, n_tiles, ga, out, s);
   }
 }
 
@@ -791,7 +886,7 @@ cudaError_t launch_ffn_tc(const void* x, const int32_t* offsets, const int32_t* 
   if (P == 0) return cudaSuccess;
   const int G = offsets ? E : 1;
   int mode1 = 0, mode2 = 0;
-  ffn_modes(I, P, G, &mode1, &mode2);
+  ffn_modes(I, P, G, gather_rows != nullptr, &mode1, &mode2);
   const int CL = mode2 == 0 ? 1 : 2;  // CTAs sharing GEMM2's weight tile
   const cuuint64_t es = 2;
   CUtensorMap ma1, mb1, ma2, mb2;
@@ -800,6 +895,7 @@ cudaError_t launch_ffn_tc(const void* x, const int32_t* offsets, const int32_t* 
     ga.rows = gather_rows;
     ga.div = gather_div;
     ga.n = T_x;
+    ga.x = static_cast<const __nv_bfloat16*>(x);
     const cuuint64_t dims[2] = {(cuuint64_t)H, (cuuint64_t)T_x};
     const cuuint64_t str[1] = {(cuuint64_t)H * es};
     const cuuint32_t box[2] = {BK, 1};
