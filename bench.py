@@ -132,20 +132,23 @@ def _max_over_ranks(world, v: float) -> float:
     return float(t.item())
 
 
-def _flops_bytes(spec, P, active_experts):
+def _flops_bytes(spec, P, active_experts, fused_gather=False):
     """Algorithmic flops and bytes of each step for one layer forward.
 
     FFN bytes: the weights of every expert with at least one row, the rows in,
-    the intermediate h written and read back, the rows out."""
+    the intermediate h written and read back, the rows out.  With the permute
+    fused into GEMM1 (fused_gather) the permute writes index tables only and
+    GEMM1's rows in are the T token rows of x, each read once."""
     s = 2 if spec.dtype == "bf16" else 4
     sr = 2 if spec.router_dtype == "bf16" else 4
     T, H, E, I, k = spec.T, spec.H, spec.E, spec.I, spec.k_max
     Is = spec.I_shared
     return {
         "route": dict(flops=2 * T * H * E, bytes=T * H * s + E * H * sr + T * k * 8),
-        "permute": dict(bytes=4 * T * k * 2 + 4 * P + 4 * T * k + T * H * s + P * H * s),
+        "permute": dict(bytes=4 * T * k * 2 + 4 * P + 4 * T * k + (0 if fused_gather else T * H * s + P * H * s)),
         "grouped_ffn": dict(flops=6 * H * I * P,
-                            bytes=active_experts * 3 * H * I * s + P * H * s + 2 * P * I * s + P * H * s),
+                            bytes=active_experts * 3 * H * I * s + (T if fused_gather else P) * H * s
+                            + 2 * P * I * s + P * H * s),
         "shared_ffn": dict(flops=6 * H * Is * T, bytes=3 * H * Is * s + 2 * T * H * s + 2 * T * Is * s),
         "combine": dict(bytes=P * H * s + 8 * T * k + T * H * s * (2 if spec.I_shared else 1)),
     }
@@ -457,9 +460,10 @@ def run_ours(args, world, rank, local):
     res = layer.forward(x, ids, kpt, k, P, stream=stream)
     active = int((res.expert_counts > 0).sum())
     counts = res.counts.cpu().numpy()
-    fb = _flops_bytes(spec, P, active)
+    fb = _flops_bytes(spec, P, active, serial.fused_gather)
     ffn_ms = stage_avg["grouped_ffn"]
     ffn = fb["grouped_ffn"]
+    ffn_call = "semmoe_grouped_ffn_gather" if serial.fused_gather else "semmoe_grouped_ffn"
     # the FFN's bound: whichever of its flops at the tensor peak and its bytes at
     # the HBM peak takes longer (weight streaming wins for small batches)
     t_tc = ffn["flops"] / (peaks["bf16_tflops"] * 1e12)
@@ -468,9 +472,9 @@ def run_ours(args, world, rank, local):
     gbs = ffn["bytes"] / (ffn_ms * 1e-3) / 1e9
     if t_tc >= t_hbm:
         roofline = {
-            "kernel": "semmoe_grouped_ffn (GEMM1+SwiGLU, GEMM2)",
+            "kernel": ffn_call + " (GEMM1+SwiGLU, GEMM2)",
             "bound": "tensor", "achieved": tflops, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
-            "frac": tflops / peaks["bf16_tflops"], "traffic": _traffic("semmoe_grouped_ffn", spec.name),
+            "frac": tflops / peaks["bf16_tflops"], "traffic": _traffic(ffn_call, spec.name),
             "peak_source": f"{peaks['source']} bf16 burst (short timed region, SM clock at its maximum); "
                            f"sustained figure {peaks['bf16_tflops_sustained']} TFLOP/s",
             "frac_of_sustained": tflops / peaks["bf16_tflops_sustained"],
@@ -478,9 +482,9 @@ def run_ours(args, world, rank, local):
         }
     else:
         roofline = {
-            "kernel": "semmoe_grouped_ffn (GEMM1+SwiGLU, GEMM2)",
+            "kernel": ffn_call + " (GEMM1+SwiGLU, GEMM2)",
             "bound": "hbm", "achieved": gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
-            "frac": gbs / peaks["hbm_gbs"], "traffic": _traffic("semmoe_grouped_ffn", spec.name),
+            "frac": gbs / peaks["hbm_gbs"], "traffic": _traffic(ffn_call, spec.name),
             "peak_source": f"{peaks['source']} HBM copy bandwidth",
             "algorithmic_bytes": ffn["bytes"], "active_experts": active,
             "frac_tensor": tflops / peaks["bf16_tflops"],

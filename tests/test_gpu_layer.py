@@ -43,10 +43,42 @@ def test_layer_full_size(name):
     check_layer_sampled(d, res, P)
 
 
+def test_layer_full_size_fused_gather():
+    """The MoE-Prism layer at full size through the path its layer takes by
+    default (GEMM1 gathering x rows, no x_perm), on the same sampled checks."""
+    d = wl.make_inputs(wl.CONFIGS["prism_subexpert_T8192"])
+    res, P = run_gpu(d, fused_gather=True)
+    assert res.x_perm is None
+    check_layer_sampled(d, res, P)
+
+
 def _layer(d):
     from token_expert_routing_gb300 import MoELayer
     s = d["spec"]
     return MoELayer(d["w_router"], d["w13"], d["w2"], d["expert_rank"], d["lut"], s.R, s.k_max, d["ws13"], d["ws2"])
+
+
+@pytest.mark.parametrize("name,over,fused", [
+    ("prism_subexpert_T8192", dict(T=256, H=256, V=3000, tokens_per_request=64), True),        # I = 352
+    ("prism_subexpert_T8192", dict(T=256, H=256, I=384, V=3000, tokens_per_request=64), True),
+    ("prism_subexpert_T8192", dict(T=256, H=256, I=392, V=3000, tokens_per_request=64), False),
+    ("qwen3_30b_a3b_T16384", dict(T=256, H=256, V=3000), False),                                # I = 768
+    ("tiny_fp32_T256_E8", {}, False),                                                           # fp32 experts
+])
+def test_layer_fused_gather_default(name, over, fused):
+    """Left unset, the permute is fused into GEMM1 exactly for bf16 experts with
+    I <= 384 (each x row gathered for at most 3 GEMM1 output tiles), and the
+    forward then writes no x_perm."""
+    import torch
+    d = wl.make_inputs(wl.scaled(name, **over))
+    layer = _layer(d)
+    assert layer.fused_gather == fused
+    s = d["spec"]
+    kpt = d["k_per_token"].cuda() if s.k_choices else None
+    res = layer.forward(d["x"].cuda(), d["token_ids"].cuda(), kpt, None if s.k_choices else s.k,
+                        int(d["k_per_token"].sum()))
+    torch.cuda.synchronize()
+    assert (res.x_perm is None) == fused
 
 
 @pytest.mark.parametrize("name", ["dsv2lite_decode_T64", "prism_subexpert_T8192"])

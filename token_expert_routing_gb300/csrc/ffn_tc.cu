@@ -182,10 +182,14 @@ __device__ __forceinline__ void gather_sources(const int32_t* __restrict__ gathe
 // GW > 0: GW more warps gather the A rows (x row gather[q] / gather_div) with
 // 16-byte loads into registers and shared-memory stores in the swizzled layout,
 // each lane then fencing for the async proxy and arriving on the stage barrier.
-// Against one warp issuing TMA four-row gathers this took the routed FFN from
-// 855 to 543 us (DeepSeek shape), 2148 to 1388 us (Qwen3), 1350 to 814 us
-// (MoE-Prism); tiled loads of a permuted copy still take 361 / 846 / 579 us.
+// Each warp keeps the loads of GATHER_DEPTH k-blocks in flight.  Routed FFN,
+// single-CTA form: one warp issuing TMA four-row gathers 855 / 2148 / 1350 us
+// (DeepSeek / Qwen3 / MoE-Prism shapes); 8 warps 2 deep 543 / 1388 / 814; 3 deep
+// 451 / 1129 / 686; 4 deep 426 / 1060 / 650; 5 deep 414 / 1032 / 635; 6 and 7
+// deep spill registers and lose (460 / 1152 / 700 at 6).  Tiled loads of a
+// permuted copy take 346-354 / 789-832 / 554-570 us in the default forms.
 constexpr int GATHER_WARPS = 8;
+constexpr int GATHER_DEPTH = 5;
 constexpr int RPL = 4;  // 16-byte pieces per lane per k-block: 8 warps x 32 lanes x 4 = 128 rows x 128 B
 template <bool GLU, int CL, int GW = 0>
 __global__ void __launch_bounds__(THREADS + 32 * GW, 1)
@@ -418,12 +422,11 @@ ffn_tc_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__
     // ---------------- row-gathering warps (6 .. 5 + GW) ----------------
     // Lane l copies 16-byte piece l & 7 of rows gw * 16 + 4 j + (l >> 3), j < RPL,
     // into the layout a 128-byte-swizzled TMA load of the [128 x 64] box writes
-    // (piece c of row r at piece c ^ (r & 7)).  The loads of the next k-block are
-    // in flight while this one waits for its stage.
+    // (piece c of row r at piece c ^ (r & 7)).  The loads of the next
+    // GATHER_DEPTH - 1 k-blocks are in flight (registers v, a ring indexed by the
+    // k-block count) while this one waits for its stage.
     const int gw = warp - 6, c = lane & 7;
     const __nv_bfloat16* cur[RPL];
-    const __nv_bfloat16* nxt[RPL];
-    uint4 vc[RPL], vn[RPL];
     auto sources = [&](int t, const __nv_bfloat16* (&p)[RPL]) {
       int row0, rows, e;
       decode_mtile<1>(sh, G, t / n_tiles, 0, row0, rows, e);
@@ -448,40 +451,40 @@ ffn_tc_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__
       for (int j = 0; j < RPL; ++j)
         v[j] = col < K ? __ldg(reinterpret_cast<const uint4*>(p[j] + col)) : make_uint4(0, 0, 0, 0);
     };
-    int tile = unit0, kb = 0;
-    if (tile < total) {
-      sources(tile, cur);
-      fetch(cur, 0, vc);
-    }
-    uint32_t it = 0;
-    while (tile < total) {
-      int ntile = tile, nkb = kb + 1;
-#pragma unroll
-      for (int j = 0; j < RPL; ++j) nxt[j] = cur[j];
-      if (nkb == kb_n) {
-        nkb = 0;
-        ntile += units;
-        if (ntile < total) sources(ntile, nxt);
+    constexpr int D = GATHER_DEPTH;  // k-blocks of loads in flight per warp
+    uint4 v[D][RPL];
+    const int my_tiles = unit0 < total ? (total - unit0 + units - 1) / units : 0;
+    const int npos = my_tiles * kb_n;
+    int ltile = unit0, lkb = 0;  // position of the next k-block to load
+    auto load_next = [&](uint4 (&dst)[RPL]) {
+      if (lkb == 0) sources(ltile, cur);
+      fetch(cur, lkb, dst);
+      if (++lkb == kb_n) {
+        lkb = 0;
+        ltile += units;
       }
-      if (ntile < total) fetch(nxt, nkb, vn);
-      const int s = it % STAGES;
-      const uint32_t ph = (it / STAGES) & 1;
-      if (!mbar_wait(&sh.empty[s], ph ^ 1, abort_flag, &g_err)) break;
-      unsigned char* a = stage_a + s * A_BYTES;
+    };
 #pragma unroll
-      for (int j = 0; j < RPL; ++j) {
-        const int r = gw * (BM / GW) + 4 * j + (lane >> 3);
-        *reinterpret_cast<uint4*>(a + r * 128 + ((c ^ (r & 7)) << 4)) = vc[j];
-      }
-      fence_async_smem();
-      mbar_arrive(&sh.full[s]);
-      ++it;
-      tile = ntile;
-      kb = nkb;
+    for (int u = 0; u < D - 1; ++u)
+      if (u < npos) load_next(v[u]);
+    bool ok = true;
+    for (int base = 0; ok && base < npos; base += D) {
 #pragma unroll
-      for (int j = 0; j < RPL; ++j) {
-        cur[j] = nxt[j];
-        vc[j] = vn[j];
+      for (int u = 0; u < D; ++u) {
+        const int it = base + u;
+        if (it >= npos) break;
+        if (it + D - 1 < npos) load_next(v[(u + D - 1) % D]);
+        const int s = it % STAGES;
+        const uint32_t ph = (it / STAGES) & 1;
+        if (!mbar_wait(&sh.empty[s], ph ^ 1, abort_flag, &g_err)) { ok = false; break; }
+        unsigned char* a = stage_a + s * A_BYTES;
+#pragma unroll
+        for (int j = 0; j < RPL; ++j) {
+          const int r = gw * (BM / GW) + 4 * j + (lane >> 3);
+          *reinterpret_cast<uint4*>(a + r * 128 + ((c ^ (r & 7)) << 4)) = v[u][j];
+        }
+        fence_async_smem();
+        mbar_arrive(&sh.full[s]);
       }
     }
   }

@@ -50,7 +50,7 @@ class MoELayer:
     """
 
     def __init__(self, w_router, w13, w2, expert_rank, lut, R: int, k_max: int, ws13=None, ws2=None,
-                 trans=None, sub_logw=None, fused_gather: bool = False, overlap: bool = True,
+                 trans=None, sub_logw=None, fused_gather: Optional[bool] = None, overlap: bool = True,
                  overlap_shared: bool = True, shared_at: str = "start", device="cuda"):
         dev = torch.device(device)
         c = lambda t: None if t is None else t.to(dev).contiguous()  # noqa: E731
@@ -60,10 +60,6 @@ class MoELayer:
         self.ws13, self.ws2 = c(ws13), c(ws2)
         self.trans = None if trans is None else c(trans).to(torch.float32)
         self.sub_logw = None if sub_logw is None else c(sub_logw).to(torch.float32)
-        # fused_gather: GEMM1 reads x through the permutation by TMA row gathers
-        # and no x_perm is written; bit-identical, but slower on this hardware
-        # (32 four-row gathers per A tile and k-block), so off by default
-        self.fused_gather = fused_gather
         # overlap: the lookup, scheduling and counting steps (nothing later in
         # the layer reads them) run on a second stream beside the permute and
         # the FFN; overlap_shared: the shared experts' FFN runs there too, from
@@ -77,6 +73,16 @@ class MoELayer:
         self._side = None
         self.E, twoI, self.H = self.w13.shape
         self.I = twoI // 2
+        # fused_gather: GEMM1 gathers its rows of x through the permutation and
+        # no x_perm is written (bit-identical).  Each row is gathered once per
+        # GEMM1 output tile of 128 h columns, while the copy it replaces is
+        # written once, so it pays off only for narrow experts.  None = on for
+        # bf16 experts with I <= 384 (at most 3 tiles).  Measured, one-stream
+        # layer: MoE-Prism (I 352) 815 against 852 us; Qwen3 (I 768) 1188
+        # against 1086; DeepSeek (I 1408) 569 against 523.
+        if fused_gather is None:
+            fused_gather = self.I <= 384 and self.w13.dtype == torch.bfloat16
+        self.fused_gather = bool(fused_gather)
         self.I_s = 0 if ws13 is None else self.ws13.shape[0] // 2
         self.R, self.k_max, self.V = R, k_max, self.lut.shape[0]
         self.Ep = self.w_router.shape[0]          # router rows: experts, or parents (hierarchical)
