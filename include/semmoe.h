@@ -308,8 +308,11 @@ int semmoe_grouped_ffn(const void* x_perm, const int32_t* expert_offsets,
  * semmoe_grouped_ffn_gather -- semmoe_grouped_ffn reading the expert inputs
  * straight from the unpermuted activations: sorted row q of GEMM1 is
  * x[sorted_to_pair[q] / k_max] (the row semmoe_permute would have gathered into
- * x_perm[q]), fetched by TMA row gathers, so the permute can run on index
- * tables only (x = x_perm = NULL) and no x_perm is written or read back.  The
+ * x_perm[q]), fetched into GEMM1's staged tiles by gathering warps (TMA row
+ * gathers in the 2-SM form), so the permute can run on index tables only
+ * (x = x_perm = NULL) and no x_perm is written or read back.  Each row is
+ * fetched once per 128 columns of h, so this pays off for narrow experts only
+ * (measured faster for I = 352, slower for I = 768 and 1408).  The
  * on-device shuffle fused into the expert GEMM ([SP] ko §2.2, de §2 B).
  * Results are bit-identical to semmoe_permute + semmoe_grouped_ffn.
  *
