@@ -420,7 +420,7 @@ ffn_tc_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__
     if (lane == 0) bulk_wait_all();  // this warp's output stores are complete
   } else if (GW > 0) {
     // ---------------- row-gathering warps (6 .. 5 + GW) ----------------
-    // Lane l copies 16-byte piece l & 7 of rows gw * 16 + 4 j + (l >> 3), j < RPL,
+    // Lane l copies 16-byte piece l & 7 of rows gw * (128 / GW) + 4 j + (l >> 3), j < RPL,
     // into the layout a 128-byte-swizzled TMA load of the [128 x 64] box writes
     // (piece c of row r at piece c ^ (r & 7)).  The loads of the next
     // GATHER_DEPTH - 1 k-blocks are in flight (registers v, a ring indexed by the
@@ -842,9 +842,10 @@ int ffn_tc_take_errors(cudaStream_t s, int* bits) { return take_error_word(g_err
 // least 512 rows (P >= 512 G), GEMM2 (K = I) when I >= 512 and they average at
 // least 256 (P >= 256 G), independent CTAs otherwise (measured per GEMM on the
 // DeepSeek, Qwen3 and MoE-Prism shapes).  A GEMM1 that gathers its rows runs
-// in the single-CTA form, where gathering warps feed it (1.6x faster than the
-// pairs' TMA row gathers).  SEMMOE_FFN_MODE=single|multicast|pair1|pair sets
-// both.
+// in the single-CTA form, where gathering warps feed it (2.1x faster than TMA
+// row gathers from the producer warp at the DeepSeek shape; gathering warps in
+// the 2-SM form measured twice as slow as in the single-CTA form).
+// SEMMOE_FFN_MODE=single|multicast|pair1|pair sets both.
 static void ffn_modes(int I, int P, int G, bool gathered, int* m1, int* m2) {
   const char* v = getenv("SEMMOE_FFN_MODE");
   if (v != nullptr) {
