@@ -38,6 +38,18 @@ class LayerOutput:
     pred_next: Optional[torch.Tensor] = None  # next-layer rank per token (when trans is held)
 
 
+def fuse_gather_default(I: int, dtype) -> bool:
+    """Whether a layer fuses the permute's row gather into GEMM1 by default.
+
+    Each x row is gathered once per GEMM1 output tile of 128 h columns, while
+    the copy it replaces is written once, so fusing pays off only for narrow
+    experts: on for bf16 experts with I <= 384 (at most 3 tiles).  Measured,
+    one-stream layer on GB300: MoE-Prism (I 352) 815 against 852 us; Qwen3
+    (I 768) 1188 against 1086; DeepSeek (I 1408) 569 against 523.  fp32
+    experts take the CUDA-core path, where no tile count applies."""
+    return I <= 384 and dtype == torch.bfloat16
+
+
 class MoELayer:
     """Weights and tables of one MoE layer, resident on a CUDA device.
 
@@ -74,14 +86,9 @@ class MoELayer:
         self.E, twoI, self.H = self.w13.shape
         self.I = twoI // 2
         # fused_gather: GEMM1 gathers its rows of x through the permutation and
-        # no x_perm is written (bit-identical).  Each row is gathered once per
-        # GEMM1 output tile of 128 h columns, while the copy it replaces is
-        # written once, so it pays off only for narrow experts.  None = on for
-        # bf16 experts with I <= 384 (at most 3 tiles).  Measured, one-stream
-        # layer: MoE-Prism (I 352) 815 against 852 us; Qwen3 (I 768) 1188
-        # against 1086; DeepSeek (I 1408) 569 against 523.
+        # no x_perm is written (bit-identical); None = fuse_gather_default
         if fused_gather is None:
-            fused_gather = self.I <= 384 and self.w13.dtype == torch.bfloat16
+            fused_gather = fuse_gather_default(self.I, self.w13.dtype)
         self.fused_gather = bool(fused_gather)
         self.I_s = 0 if ws13 is None else self.ws13.shape[0] // 2
         self.R, self.k_max, self.V = R, k_max, self.lut.shape[0]
