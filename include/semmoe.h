@@ -265,9 +265,10 @@ int semmoe_permute(const int32_t* topk_idx, const int32_t* expert_rank,
  * SEMMOE_ERR_INVALID_ARG before anything runs.  The call makes no cudaMalloc,
  * cudaFree or other allocating call.
  *
- * The first call on each device looks up the array's device address (once,
- * with that device current) and caches it; make that first call before any
- * stream capture.  All calls share the one array and it keeps the last call's
+ * The first call in each CUDA context (normally: on each device) looks up the
+ * array's device address with that context current and caches it under the
+ * context's unique ID, so a context made after cudaDeviceReset looks it up
+ * afresh; make that first call before any stream capture.  All calls share the one array and it keeps the last call's
  * contents (the kernels overwrite whatever they read), so two calls that
  * overlap on the GPU -- on different streams, or from different threads --
  * race on it; order them on one stream.
@@ -325,6 +326,45 @@ int semmoe_grouped_ffn_gather(const void* x, const int32_t* sorted_to_pair, int 
                               const int32_t* expert_offsets, const int32_t* phys_to_expert, const void* w13,
                               const void* w2, int dtype, int P, int E, int H, int I, void* y_perm, void* ws,
                               size_t ws_bytes, void* stream);
+
+/*
+ * semmoe_grouped_ffn_form -- semmoe_grouped_ffn (sorted_to_pair == NULL) or
+ * semmoe_grouped_ffn_gather (sorted_to_pair set) with the kernel form of each
+ * GEMM pinned by the caller instead of chosen from the shapes.  The pages have
+ * no counterpart: it exists so that tests can run every form of the same
+ * computation and check that they agree bit for bit.  The two production
+ * calls above are this call with SEMMOE_FORM_DEFAULT for both GEMMs.
+ *
+ * form1 (GEMM1 + SwiGLU) and form2 (GEMM2), one of
+ *   SEMMOE_FORM_DEFAULT            chosen from P, E, I and dtype (what the
+ *                                  production calls run)
+ *   SEMMOE_FORM_SINGLE             one CTA per SM, M128 x N256 tiles (GEMM1
+ *                                  with gathered rows: gathering warps)
+ *   SEMMOE_FORM_PAIR1              2-SM pairs (tcgen05 cta_group::2, M256 x
+ *                                  N256), one accumulator buffer
+ *   SEMMOE_FORM_PAIR               2-SM pairs, two accumulator buffers
+ *   SEMMOE_FORM_SINGLE_TMA_GATHER  GEMM1 with gathered rows only: one CTA per
+ *                                  SM, rows fetched by TMA four-row gathers
+ *   SEMMOE_FORM_CUDA_CORE          both GEMMs on CUDA cores (form1 and form2
+ *                                  both this value)
+ * bf16 accepts all of them; fp32 only SEMMOE_FORM_DEFAULT or
+ * SEMMOE_FORM_CUDA_CORE (it always runs on CUDA cores).  Any other combination
+ * returns SEMMOE_ERR_INVALID_ARG.  Arguments, workspace, limits and device
+ * checks as semmoe_grouped_ffn / semmoe_grouped_ffn_gather (x is x_perm when
+ * sorted_to_pair is NULL; k_max and T are then ignored).
+ */
+enum {
+  SEMMOE_FORM_DEFAULT = 0,
+  SEMMOE_FORM_SINGLE = 1,
+  SEMMOE_FORM_PAIR1 = 2,
+  SEMMOE_FORM_PAIR = 3,
+  SEMMOE_FORM_SINGLE_TMA_GATHER = 4,
+  SEMMOE_FORM_CUDA_CORE = 5
+};
+int semmoe_grouped_ffn_form(const void* x, const int32_t* sorted_to_pair, int k_max, int T,
+                            const int32_t* expert_offsets, const int32_t* phys_to_expert, const void* w13,
+                            const void* w2, int dtype, int P, int E, int H, int I, void* y_perm, void* ws,
+                            size_t ws_bytes, int form1, int form2, void* stream);
 
 /*
  * semmoe_shared_ffn -- the shared experts (applied to every token with gate 1,

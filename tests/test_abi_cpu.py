@@ -154,3 +154,23 @@ def test_product_path_fails_loudly_without_library(monkeypatch):
     monkeypatch.setattr(_abi, "_lib", None)
     with pytest.raises(RuntimeError, match="missing"):
         _abi.lib()
+
+
+def test_ffn_form_validation(lib):
+    from token_expert_routing_gb300 import _abi as a
+    p = ctypes.c_void_p(1 << 12)
+
+    def call(f1, f2, s2p=None, dtype=1):
+        return lib.semmoe_grouped_ffn_form(p, s2p, 2, 64, p, p, p, p, dtype, 64, 4, 128, 128, p, p, 1 << 30, f1, f2,
+                                           None)
+    # forms outside the enum, or the CUDA-core form in one GEMM only
+    assert call(9, 0) == 1 and "form" in _err(lib)
+    assert call(a.SEMMOE_FORM_CUDA_CORE, a.SEMMOE_FORM_SINGLE) == 1
+    # four-row TMA gathers exist only for a GEMM1 that gathers its rows
+    assert call(a.SEMMOE_FORM_SINGLE_TMA_GATHER, a.SEMMOE_FORM_SINGLE) == 1 and "gathered" in _err(lib)
+    assert call(a.SEMMOE_FORM_SINGLE, a.SEMMOE_FORM_SINGLE_TMA_GATHER, s2p=p) == 1
+    # fp32 runs on CUDA cores only
+    assert call(a.SEMMOE_FORM_PAIR, a.SEMMOE_FORM_PAIR, dtype=0) == 1 and "fp32" in _err(lib)
+    # no rows: nothing is launched, for any valid form pair
+    assert lib.semmoe_grouped_ffn_form(None, None, 1, 0, p, p, p, p, 1, 0, 4, 128, 128, None, p, 1 << 30,
+                                       a.SEMMOE_FORM_PAIR, a.SEMMOE_FORM_SINGLE, None) == 0

@@ -7,7 +7,7 @@ import pytest
 import torch
 
 import oracle
-from parity_utils import GATE_ATOL, LOGIT_TOL, max_rel, np_
+from parity_utils import GATE_ATOL, LOGIT_TOL, TOL, max_rel, np_
 
 pytestmark = pytest.mark.gpu
 
@@ -287,11 +287,12 @@ SPLIT_COUNTS = [0, 1, 127, 128, 129, 255, 256, 257, 384, 511, 512, 640, 1000, 3,
 
 @pytest.mark.parametrize("P,E,H,I", [(1000, 8, 256, 160), (5000, 64, 512, 352), (3000, 16, 512, 640),
                                      (sum(SPLIT_COUNTS), 16, 256, 576), (30000, 64, 512, 704)])
-def test_grouped_ffn_forms_are_bit_identical(P, E, H, I, monkeypatch):
-    """Every form of the grouped GEMM -- independent CTAs, CTA pairs sharing
-    weight tiles by TMA multicast, 2-SM MMA pairs with one or two accumulator
-    buffers -- returns exactly the same bits; one case pins group sizes around
-    the 128- and 256-row boundaries (empty groups, 1, 127..129, 255..257 rows)."""
+def test_grouped_ffn_forms_are_bit_identical(P, E, H, I):
+    """Every form of the grouped GEMM -- independent CTAs, 2-SM MMA pairs with
+    one or two accumulator buffers, and the shape-chosen default -- returns
+    exactly the same bits, and those bits match the oracle's grouped FFN row by
+    row within the bf16 tolerance; one case pins group sizes around the 128-
+    and 256-row boundaries (empty groups, 1, 127..129, 255..257 rows)."""
     rng = np.random.default_rng(P + E)
     if P == sum(SPLIT_COUNTS) and E == len(SPLIT_COUNTS):
         cnt = np.array(SPLIT_COUNTS)
@@ -304,20 +305,30 @@ def test_grouped_ffn_forms_are_bit_identical(P, E, H, I, monkeypatch):
     w2 = torch.from_numpy((rng.standard_normal((E, H, I)) / np.sqrt(I)).astype(np.float32)).to(torch.bfloat16).cuda()
     ws = torch.empty(abi().semmoe_grouped_ffn_workspace_size(P, I, 1), dtype=torch.uint8, device="cuda")
     outs = []
-    for mode in ("single", "multicast", "pair1", "pair"):
-        monkeypatch.setenv("SEMMOE_FFN_MODE", mode)
+    a = abi()
+    for form in (a.SEMMOE_FORM_SINGLE, a.SEMMOE_FORM_PAIR1, a.SEMMOE_FORM_PAIR, a.SEMMOE_FORM_DEFAULT):
         y = torch.empty(P, H, dtype=torch.bfloat16, device="cuda")
-        abi().semmoe_grouped_ffn(x, off, pe, w13, w2, P, E, H, I, y, ws)
-        assert abi().semmoe_check_errors() == 0
+        a.semmoe_grouped_ffn_form(x, None, 1, 0, off, pe, w13, w2, P, E, H, I, y, ws, form, form)
+        assert a.semmoe_check_errors() == 0
         outs.append(y.cpu())
     for o in outs[1:]:
         assert torch.equal(outs[0], o)
+    ref = oracle.grouped_ffn(x.cpu(), off.cpu(), pe.cpu(), w13.cpu().to(torch.float64).numpy(),
+                             w2.cpu().to(torch.float64).numpy(), "bf16")
+    got = outs[0].to(torch.float64).numpy()
+    assert max_rel(got, ref) < TOL["bf16"]
+    # every group's last row (the ragged tail of its last tile) on its own
+    offs = off.cpu().numpy()
+    for b in range(E):
+        lo, hi = int(offs[b]), int(offs[b + 1])
+        if hi > lo:
+            assert max_rel(got[hi - 1], ref[hi - 1]) < TOL["bf16"], b
 
 
 @pytest.mark.parametrize("dtype,T,E,k_max,H,I", [("bf16", 1000, 16, 4, 256, 640), ("bf16", 3001, 64, 6, 512, 1408),
                                                  ("bf16", 257, 8, 8, 128, 160), ("bf16", 700, 8, 4, 200, 96),
                                                  ("f32", 300, 8, 3, 64, 96)])
-def test_grouped_ffn_gather_matches_permuted(dtype, T, E, k_max, H, I, monkeypatch):
+def test_grouped_ffn_gather_matches_permuted(dtype, T, E, k_max, H, I):
     """GEMM1 reading x through sorted_to_pair (row gathers) gives exactly the
     bits of the permute's x_perm followed by the grouped FFN, in every form of
     the grouped GEMM; per-token budgets leave padding slots, so sorted rows map
@@ -340,31 +351,34 @@ def test_grouped_ffn_gather_matches_permuted(dtype, T, E, k_max, H, I, monkeypat
                          p2e, ec, s2p, p2s, xp, ws)
     fws = torch.empty(abi().semmoe_grouped_ffn_workspace_size(P, I, 1 if dtype == "bf16" else 0), dtype=torch.uint8,
                       device="cuda")
-    modes = ("single", "single/tma-gather", "multicast", "pair1", "pair", "default") if dtype == "bf16" else ("default",)
-    for mode in modes:
-        # single: gathering warps feed GEMM1; single/tma-gather: TMA four-row gathers;
-        # default: the gathered GEMM1's own form choice
-        if mode == "default":
-            monkeypatch.delenv("SEMMOE_FFN_MODE", raising=False)
-        else:
-            monkeypatch.setenv("SEMMOE_FFN_MODE", mode.split("/")[0])
-        if mode.endswith("tma-gather"):
-            monkeypatch.setenv("SEMMOE_GATHER_WARPS", "0")
-        else:
-            monkeypatch.delenv("SEMMOE_GATHER_WARPS", raising=False)
+    a = abi()
+    # (GEMM1 form of the x_perm call, GEMM1 form of the gathered call, GEMM2 form): single = gathering
+    # warps feed the gathered GEMM1; single/TMA gather = the producer's four-row gathers
+    forms = [(a.SEMMOE_FORM_SINGLE, a.SEMMOE_FORM_SINGLE, a.SEMMOE_FORM_SINGLE),
+             (a.SEMMOE_FORM_SINGLE, a.SEMMOE_FORM_SINGLE_TMA_GATHER, a.SEMMOE_FORM_SINGLE),
+             (a.SEMMOE_FORM_PAIR1, a.SEMMOE_FORM_PAIR1, a.SEMMOE_FORM_PAIR1),
+             (a.SEMMOE_FORM_PAIR, a.SEMMOE_FORM_PAIR, a.SEMMOE_FORM_PAIR)] if dtype == "bf16" else []
+    for f_plain, f_gather, f2 in forms:
         y0 = torch.full((P, H), 3.0, dtype=tdt, device="cuda")
         y1 = torch.full((P, H), 5.0, dtype=tdt, device="cuda")
-        abi().semmoe_grouped_ffn(xp, eo, p2e, w13, w2, P, E, H, I, y0, fws)
-        abi().semmoe_grouped_ffn_gather(x, s2p, k_max, T, eo, p2e, w13, w2, P, E, H, I, y1, fws)
-        assert abi().semmoe_check_errors() == 0
-        assert torch.equal(y0.cpu(), y1.cpu()), mode
+        a.semmoe_grouped_ffn_form(xp, None, 1, 0, eo, p2e, w13, w2, P, E, H, I, y0, fws, f_plain, f2)
+        a.semmoe_grouped_ffn_form(x, s2p, k_max, T, eo, p2e, w13, w2, P, E, H, I, y1, fws, f_gather, f2)
+        assert a.semmoe_check_errors() == 0
+        assert torch.equal(y0.cpu(), y1.cpu()), (f_plain, f_gather, f2)
+    # the production calls, each with its own shape-chosen forms
+    y0 = torch.full((P, H), 3.0, dtype=tdt, device="cuda")
+    y1 = torch.full((P, H), 5.0, dtype=tdt, device="cuda")
+    a.semmoe_grouped_ffn(xp, eo, p2e, w13, w2, P, E, H, I, y0, fws)
+    a.semmoe_grouped_ffn_gather(x, s2p, k_max, T, eo, p2e, w13, w2, P, E, H, I, y1, fws)
+    assert a.semmoe_check_errors() == 0
+    assert torch.equal(y0.cpu(), y1.cpu())
     if dtype == "bf16":  # the CUDA-core path gathers the same way
-        monkeypatch.setenv("SEMMOE_FFN_IMPL", "simt")
+        cc = a.SEMMOE_FORM_CUDA_CORE
         y0 = torch.empty(P, H, dtype=tdt, device="cuda")
         y1 = torch.empty(P, H, dtype=tdt, device="cuda")
-        abi().semmoe_grouped_ffn(xp, eo, p2e, w13, w2, P, E, H, I, y0, fws)
-        abi().semmoe_grouped_ffn_gather(x, s2p, k_max, T, eo, p2e, w13, w2, P, E, H, I, y1, fws)
-        assert abi().semmoe_check_errors() == 0
+        a.semmoe_grouped_ffn_form(xp, None, 1, 0, eo, p2e, w13, w2, P, E, H, I, y0, fws, cc, cc)
+        a.semmoe_grouped_ffn_form(x, s2p, k_max, T, eo, p2e, w13, w2, P, E, H, I, y1, fws, cc, cc)
+        assert a.semmoe_check_errors() == 0
         assert torch.equal(y0.cpu(), y1.cpu())
 
 
@@ -474,12 +488,16 @@ def test_permute_flags_bad_expert_and_pair_count():
 
 
 @pytest.mark.parametrize("mode,dtype", [("single", "bf16"), ("pair", "bf16"), ("default", "f32")])
-def test_grouped_ffn_flags_bad_group_table(mode, dtype, monkeypatch):
+def test_grouped_ffn_flags_bad_group_table(mode, dtype):
     """Group offsets that decrease or run past P (SEMMOE_DEVERR_PAIRS) and an
     expert id past E (SEMMOE_DEVERR_EXPERT) are flagged by the kernels' checks
     in every form; those groups are skipped, the valid ones are still computed
     exactly as with a clean table."""
-    monkeypatch.setenv("SEMMOE_FFN_MODE", mode)
+    a = abi()
+    form = {"single": a.SEMMOE_FORM_SINGLE, "pair": a.SEMMOE_FORM_PAIR, "default": a.SEMMOE_FORM_DEFAULT}[mode]
+
+    def ffn(xx, off, pe, y):
+        a.semmoe_grouped_ffn_form(xx, None, 1, 0, off, pe, w13, w2, P, E, H, I, y, ws, form, form)
     rng = np.random.default_rng(5)
     tdt = torch.bfloat16 if dtype == "bf16" else torch.float32
     E, H, I, P = 4, 128, 128, 600
@@ -491,12 +509,12 @@ def test_grouped_ffn_flags_bad_group_table(mode, dtype, monkeypatch):
     p2e = torch.tensor([0, 1, 2, 3], **i32)
     clean = torch.tensor([0, 300, 300, 450, 600], **i32)
     y0 = torch.zeros(P, H, dtype=tdt, device="cuda")
-    abi().semmoe_grouped_ffn(x, clean, p2e, w13, w2, P, E, H, I, y0, ws)
+    ffn(x, clean, p2e, y0)
     assert abi().semmoe_check_errors() == 0
     # group 1 runs backwards (300 -> 200), group 3 past P (450 -> 700)
     bad = torch.tensor([0, 300, 200, 450, 700], **i32)
     y1 = torch.zeros(P, H, dtype=tdt, device="cuda")
-    abi().semmoe_grouped_ffn(x, bad, p2e, w13, w2, P, E, H, I, y1, ws)
+    ffn(x, bad, p2e, y1)
     with pytest.raises(abi().SemMoEError) as ei:
         abi().semmoe_check_errors()
     assert ei.value.bits & abi().SEMMOE_DEVERR_PAIRS
@@ -504,7 +522,7 @@ def test_grouped_ffn_flags_bad_group_table(mode, dtype, monkeypatch):
     assert torch.equal(y1[:200], y0[:200])
     p2e_bad = torch.tensor([0, 1, 9, 3], **i32)        # expert 9 of 4
     y2 = torch.zeros(P, H, dtype=tdt, device="cuda")
-    abi().semmoe_grouped_ffn(x, clean, p2e_bad, w13, w2, P, E, H, I, y2, ws)
+    ffn(x, clean, p2e_bad, y2)
     with pytest.raises(abi().SemMoEError) as ei:
         abi().semmoe_check_errors()
     assert ei.value.bits & abi().SEMMOE_DEVERR_EXPERT
@@ -513,13 +531,14 @@ def test_grouped_ffn_flags_bad_group_table(mode, dtype, monkeypatch):
 
 
 @pytest.mark.parametrize("producer", ["gather-warps", "tma-gather", "pair"])
-def test_grouped_ffn_gather_flags_bad_pair_id(producer, monkeypatch):
+def test_grouped_ffn_gather_flags_bad_pair_id(producer):
     """A sorted_to_pair entry naming no token (negative, or a token past T)
     sets SEMMOE_DEVERR_PAIRS in every gathering producer; that row reads token
     0 instead, and every other row keeps the bits of the clean call."""
-    monkeypatch.setenv("SEMMOE_FFN_MODE", "pair" if producer == "pair" else "single")
-    if producer == "tma-gather":
-        monkeypatch.setenv("SEMMOE_GATHER_WARPS", "0")
+    a = abi()
+    f1, f2 = {"gather-warps": (a.SEMMOE_FORM_SINGLE, a.SEMMOE_FORM_SINGLE),
+              "tma-gather": (a.SEMMOE_FORM_SINGLE_TMA_GATHER, a.SEMMOE_FORM_SINGLE),
+              "pair": (a.SEMMOE_FORM_PAIR, a.SEMMOE_FORM_PAIR)}[producer]
     rng = np.random.default_rng(23)
     E, H, I, T, k_max = 4, 256, 128, 300, 2
     P = T * k_max
@@ -531,12 +550,12 @@ def test_grouped_ffn_gather_flags_bad_pair_id(producer, monkeypatch):
     p2e = torch.tensor([0, 1, 2, 3], **i32)
     s2p = torch.from_numpy(rng.permutation(P).astype(np.int32)).cuda()
     y0 = torch.zeros(P, H, dtype=torch.bfloat16, device="cuda")
-    abi().semmoe_grouped_ffn_gather(x, s2p, k_max, T, eo, p2e, w13, w2, P, E, H, I, y0, ws)
+    a.semmoe_grouped_ffn_form(x, s2p, k_max, T, eo, p2e, w13, w2, P, E, H, I, y0, ws, f1, f2)
     assert abi().semmoe_check_errors() == 0
     bad = s2p.clone()
     bad[7], bad[301] = -5, T * k_max + 9               # no token; token T + 4 of T
     y1 = torch.zeros(P, H, dtype=torch.bfloat16, device="cuda")
-    abi().semmoe_grouped_ffn_gather(x, bad, k_max, T, eo, p2e, w13, w2, P, E, H, I, y1, ws)
+    a.semmoe_grouped_ffn_form(x, bad, k_max, T, eo, p2e, w13, w2, P, E, H, I, y1, ws, f1, f2)
     with pytest.raises(abi().SemMoEError) as ei:
         abi().semmoe_check_errors()
     assert ei.value.bits & abi().SEMMOE_DEVERR_PAIRS
@@ -547,7 +566,7 @@ def test_grouped_ffn_gather_flags_bad_pair_id(producer, monkeypatch):
     ref_map = s2p.clone()
     ref_map[7], ref_map[301] = 0, 0
     y2 = torch.zeros(P, H, dtype=torch.bfloat16, device="cuda")
-    abi().semmoe_grouped_ffn_gather(x, ref_map, k_max, T, eo, p2e, w13, w2, P, E, H, I, y2, ws)
+    a.semmoe_grouped_ffn_form(x, ref_map, k_max, T, eo, p2e, w13, w2, P, E, H, I, y2, ws, f1, f2)
     assert abi().semmoe_check_errors() == 0
     assert torch.equal(y1.cpu(), y2.cpu())
 
@@ -597,7 +616,7 @@ def test_combine_skips_and_flags_a_slot_past_P():
 
 @pytest.mark.parametrize("P,E,I", [(5000, 8, 352),    # groups of ~625 rows, I < 512: GEMM1 in pairs, GEMM2 single
                                    (4000, 10, 640)])  # groups of ~400 rows, I >= 512: GEMM1 single, GEMM2 in pairs
-def test_grouped_ffn_mixed_default_forms_match_single(P, E, I, monkeypatch):
+def test_grouped_ffn_mixed_default_forms_match_single(P, E, I):
     """The default per-GEMM form choice mixes the 2-SM and single-CTA forms
     within one call; the result is bit-identical to both GEMMs single-CTA."""
     rng = np.random.default_rng(P + I)
@@ -610,13 +629,16 @@ def test_grouped_ffn_mixed_default_forms_match_single(P, E, I, monkeypatch):
     w2 = torch.from_numpy((rng.standard_normal((E, H, I)) / np.sqrt(I)).astype(np.float32)).to(torch.bfloat16).cuda()
     ws = torch.empty(abi().semmoe_grouped_ffn_workspace_size(P, I, 1), dtype=torch.uint8, device="cuda")
     outs = []
-    for mode in (None, "single"):
-        if mode is None:
-            monkeypatch.delenv("SEMMOE_FFN_MODE", raising=False)
-        else:
-            monkeypatch.setenv("SEMMOE_FFN_MODE", mode)
+    a = abi()
+    for form in (None, a.SEMMOE_FORM_SINGLE):
         y = torch.full((P, H), 7.0, dtype=torch.bfloat16, device="cuda")
-        abi().semmoe_grouped_ffn(x, eo, p2e, w13, w2, P, E, H, I, y, ws)
-        assert abi().semmoe_check_errors() == 0
+        if form is None:
+            a.semmoe_grouped_ffn(x, eo, p2e, w13, w2, P, E, H, I, y, ws)
+        else:
+            a.semmoe_grouped_ffn_form(x, None, 1, 0, eo, p2e, w13, w2, P, E, H, I, y, ws, form, form)
+        assert a.semmoe_check_errors() == 0
         outs.append(y.cpu())
     assert torch.equal(outs[0], outs[1])
+    ref = oracle.grouped_ffn(x.cpu(), eo.cpu(), p2e.cpu(), w13.cpu().to(torch.float64).numpy(),
+                             w2.cpu().to(torch.float64).numpy(), "bf16")
+    assert max_rel(outs[0].to(torch.float64).numpy(), ref) < TOL["bf16"]

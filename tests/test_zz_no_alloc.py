@@ -38,7 +38,7 @@ def _routing(rng, T, E, k_max):
     order = np.argsort(-l, axis=1, kind="stable")[:, :k_max]
     k = rng.integers(1, k_max + 1, size=T)
     idx = np.where(np.arange(k_max)[None, :] < k[:, None], order, -1)
-    return idx.astype(np.int32), int(k.sum())
+    return idx.astype(np.int32), k
 
 
 def _run(fn_name, idx, er, x, T, H, E, R, k_max, P):
@@ -63,12 +63,20 @@ def _run(fn_name, idx, er, x, T, H, E, R, k_max, P):
 
 @pytest.mark.gpu
 def test_noalloc_matches_workspace_permute_on_two_calls():
+    """Two calls in a row, the second with other routing: each equals the
+    workspace-taking permute bit for bit, and the oracle's permutation."""
+    import oracle
     rng = np.random.default_rng(2024)
     for T, E, R, k_max, H in ((4096, 64, 8, 6, 256), (3001, 256, 8, 24, 64)):
-        idx, P = _routing(rng, T, E, k_max)
+        idx, k = _routing(rng, T, E, k_max)
+        P = int(k.sum())
         er = rng.permutation(np.arange(E) % R).astype(np.int32)
         x = torch.from_numpy(rng.standard_normal((T, H)).astype(np.float32)).to(torch.bfloat16).cuda()
         want = _run("semmoe_permute", idx, er, x, T, H, E, R, k_max, P)
         got = _run("semmoe_permute_noalloc", idx, er, x, T, H, E, R, k_max, P)
         for key in want:
             assert torch.equal(got[key], want[key]), (T, E, key)
+        ref = oracle.permute(idx, k, er, R, x.cpu())
+        for key in ref:
+            g = got[key].to(torch.float64) if key == "x_perm" else got[key]
+            assert np.array_equal(g.numpy(), ref[key]), (T, E, key)

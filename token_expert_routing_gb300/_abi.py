@@ -19,6 +19,9 @@ SEMMOE_OK, SEMMOE_ERR_INVALID_ARG, SEMMOE_ERR_UNSUPPORTED, SEMMOE_ERR_CUDA, \
     SEMMOE_ERR_DEVICE_CHECK, SEMMOE_ERR_DEVICE_TIMEOUT = range(6)
 SEMMOE_F32, SEMMOE_BF16 = 0, 1
 SEMMOE_F32_SPLIT = 2   # router weight only: the output of semmoe_route_split_weight
+# grouped-FFN kernel forms (semmoe_grouped_ffn_form)
+SEMMOE_FORM_DEFAULT, SEMMOE_FORM_SINGLE, SEMMOE_FORM_PAIR1, SEMMOE_FORM_PAIR, SEMMOE_FORM_SINGLE_TMA_GATHER, \
+    SEMMOE_FORM_CUDA_CORE = range(6)
 # device error word bits (semmoe_check_errors)
 SEMMOE_DEVERR_EXPERT, SEMMOE_DEVERR_TOKEN_ID, SEMMOE_DEVERR_LUT, SEMMOE_DEVERR_K, SEMMOE_DEVERR_PAIRS, \
     SEMMOE_DEVERR_TIMEOUT, SEMMOE_DEVERR_NONFINITE, SEMMOE_DEVERR_OFFSETS, SEMMOE_DEVERR_RANK = \
@@ -52,6 +55,8 @@ SIGNATURES = {
     "semmoe_grouped_ffn": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _vp, _vp, _sz, _vp]),
     "semmoe_grouped_ffn_gather": (_i, [_vp, _vp, _i, _i, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _vp, _vp, _sz,
                                        _vp]),
+    "semmoe_grouped_ffn_form": (_i, [_vp, _vp, _i, _i, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _vp, _vp, _sz,
+                                     _i, _i, _vp]),
     "semmoe_shared_ffn_workspace_size": (_sz, [_i, _i, _i]),
     "semmoe_shared_ffn": (_i, [_vp, _vp, _vp, _i, _i, _i, _i, _vp, _vp, _sz, _vp]),
     "semmoe_combine": (_i, [_vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _vp, _vp]),
@@ -236,6 +241,14 @@ def semmoe_grouped_ffn_gather(x, sorted_to_pair, k_max, T, expert_offsets, phys_
     _check(lib().semmoe_grouped_ffn_gather(_p(x), _p(sorted_to_pair), k_max, T, _p(expert_offsets),
                                            _p(phys_to_expert), _p(w13), _p(w2), dtype_code(w13), P, E, H, I,
                                            _p(y_perm), _p(ws), ws.numel() * ws.element_size(), _stream(stream)))
+
+
+def semmoe_grouped_ffn_form(x, sorted_to_pair, k_max, T, expert_offsets, phys_to_expert, w13, w2, P, E, H, I,
+                            y_perm, ws, form1, form2, stream=None):
+    _check(lib().semmoe_grouped_ffn_form(_p(x), _p(sorted_to_pair), k_max, T, _p(expert_offsets),
+                                         _p(phys_to_expert), _p(w13), _p(w2), dtype_code(w13), P, E, H, I,
+                                         _p(y_perm), _p(ws), ws.numel() * ws.element_size(), form1, form2,
+                                         _stream(stream)))
 
 
 def semmoe_shared_ffn_workspace_size(T, I_s, dtype: int) -> int:

@@ -330,6 +330,36 @@ int semmoe_grouped_ffn_gather(const void* x, const int32_t* sorted_to_pair, int 
                      "semmoe_grouped_ffn_gather");
 }
 
+int semmoe_grouped_ffn_form(const void* x, const int32_t* sorted_to_pair, int k_max, int T,
+                            const int32_t* expert_offsets, const int32_t* phys_to_expert, const void* w13,
+                            const void* w2, int dtype, int P, int E, int H, int I, void* y_perm, void* ws,
+                            size_t ws_bytes, int form1, int form2, void* stream) {
+  const char* fn = "semmoe_grouped_ffn_form";
+  REQUIRE(E >= 1 && E <= 256, "%s: E = %d outside [1, 256]", fn, E);
+  REQUIRE(expert_offsets && phys_to_expert, "%s: null offsets", fn);
+  const bool gathered = sorted_to_pair != nullptr;
+  if (gathered) {
+    REQUIRE(T >= 0 && k_max >= 1 && (long long)T * k_max < (1LL << 31), "%s: bad sizes T=%d k_max=%d", fn, T, k_max);
+    REQUIRE(P <= (long long)T * k_max, "%s: P = %d > T * k_max", fn, P);
+  }
+  const bool cc1 = form1 == SEMMOE_FORM_CUDA_CORE, cc2 = form2 == SEMMOE_FORM_CUDA_CORE;
+  REQUIRE(form1 >= SEMMOE_FORM_DEFAULT && form1 <= SEMMOE_FORM_CUDA_CORE && form2 >= SEMMOE_FORM_DEFAULT &&
+              form2 <= SEMMOE_FORM_CUDA_CORE && cc1 == cc2,
+          "%s: bad form pair (%d, %d)", fn, form1, form2);
+  REQUIRE(form2 != SEMMOE_FORM_SINGLE_TMA_GATHER && (form1 != SEMMOE_FORM_SINGLE_TMA_GATHER || gathered),
+          "%s: SEMMOE_FORM_SINGLE_TMA_GATHER applies to a GEMM1 with gathered rows only", fn);
+  REQUIRE(dtype != SEMMOE_F32 || ((form1 == SEMMOE_FORM_DEFAULT || cc1) && (form2 == SEMMOE_FORM_DEFAULT || cc2)),
+          "%s: fp32 runs on CUDA cores only (form SEMMOE_FORM_DEFAULT or SEMMOE_FORM_CUDA_CORE)", fn);
+  int rc = check_ffn_args(fn, x, w13, w2, dtype, P, H, I, y_perm, ws, ws_bytes);
+  if (rc != SEMMOE_OK) return rc;
+  if (P == 0) return SEMMOE_OK;
+  CHECK_DEVICE(fn);
+  return cuda_status(launch_ffn(x, expert_offsets, phys_to_expert, w13, w2, dtype, P, E, H, I, y_perm, ws,
+                                sorted_to_pair, gathered ? k_max : 1, gathered ? T : 0,
+                                static_cast<cudaStream_t>(stream), form1, form2),
+                     fn);
+}
+
 size_t semmoe_shared_ffn_workspace_size(int T, int I_s, int dtype) {
   if (T < 0 || I_s < 1 || !valid_dtype(dtype)) return 0;
   return ffn_ws_bytes(T, I_s, dtype);

@@ -1,9 +1,7 @@
 // Grouped-FFN dispatch: bf16 runs on the tensor cores (ffn_tc.cu); fp32 runs
-// on CUDA cores (ffn_simt.cu).  Setting SEMMOE_FFN_IMPL=simt in the
-// environment runs bf16 on the CUDA-core kernel as well (a slow cross-check).
-#include <stdlib.h>
-#include <string.h>
-
+// on CUDA cores (ffn_simt.cu).  The kernel depends only on the dtype and, for
+// the tensor-core forms, on the shapes, unless the caller pins a form
+// (semmoe_grouped_ffn_form, for tests that compare the forms bit for bit).
 #include "common.cuh"
 #include "internal.h"
 
@@ -14,7 +12,7 @@ cudaError_t launch_ffn_simt(const void* x, const int32_t* offsets, const int32_t
                             const int32_t* gather, int gather_div, int T_x, cudaStream_t s);
 cudaError_t launch_ffn_tc(const void* x, const int32_t* offsets, const int32_t* p2e, const void* w13,
                           const void* w2, int P, int E, int H, int I, void* y, void* ws, const int32_t* gather,
-                          int gather_div, int T_x, cudaStream_t s);
+                          int gather_div, int T_x, int form1, int form2, cudaStream_t s);
 int ffn_simt_take_errors(cudaStream_t s, int* bits);
 int ffn_tc_take_errors(cudaStream_t s, int* bits);
 
@@ -29,16 +27,11 @@ size_t ffn_ws_bytes(int P, int I, int dtype) {
   return align_up((size_t)(P > 0 ? P : 1) * I * es, 256);
 }
 
-static bool force_simt() {
-  const char* v = getenv("SEMMOE_FFN_IMPL");
-  return v != nullptr && strcmp(v, "simt") == 0;
-}
-
 cudaError_t launch_ffn(const void* x, const int32_t* offsets, const int32_t* p2e, const void* w13,
                        const void* w2, int dtype, int P, int E, int H, int I, void* y, void* ws,
-                       const int32_t* gather, int gather_div, int T_x, cudaStream_t s) {
-  if (dtype == SEMMOE_BF16 && !force_simt())
-    return launch_ffn_tc(x, offsets, p2e, w13, w2, P, E, H, I, y, ws, gather, gather_div, T_x, s);
+                       const int32_t* gather, int gather_div, int T_x, cudaStream_t s, int form1, int form2) {
+  if (dtype == SEMMOE_BF16 && form1 != SEMMOE_FORM_CUDA_CORE)
+    return launch_ffn_tc(x, offsets, p2e, w13, w2, P, E, H, I, y, ws, gather, gather_div, T_x, form1, form2, s);
   return launch_ffn_simt(x, offsets, p2e, w13, w2, dtype, P, E, H, I, y, ws, gather, gather_div, T_x, s);
 }
 

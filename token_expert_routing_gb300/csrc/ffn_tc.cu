@@ -30,18 +30,12 @@
 //    A rows and half of the weight tile, a third less shared-memory traffic per
 //    SM; pairs cover two m-tiles of one expert, so groups with an odd m-tile
 //    count leave one half idle, which costs more than it saves on short
-//    (I < 512) tiles;
-//  * multicast pairs (SEMMOE_FFN_MODE=multicast): independent MMAs, weight tile
-//    shared by TMA multicast; it halves L2 weight reads but not per-SM
-//    shared-memory traffic and measured slower.
+//    (I < 512) tiles.
 //
 // Every wait is bounded (%globaltimer and a poll count); a wait that runs out sets the timeout
 // bit of the device error word and an abort flag, after which every role
 // stops, in-flight TMA loads and MMAs are drained (again with a bound), and
 // TMEM is freed before the CTA exits.
-#include <stdlib.h>
-#include <string.h>
-
 #include "common.cuh"
 #include "internal.h"
 #include "tc_common.cuh"
@@ -139,8 +133,9 @@ __device__ __forceinline__ void emit_chunk(ChunkOut& co, const uint32_t (&w)[32]
 }
 
 
-// Tile unit mu (CL consecutive m-tiles of one group, one per CTA of the
-// cluster) -> this CTA's (first row, valid rows, expert).  A CTA whose m-tile
+// Tile unit mu (CL consecutive m-tiles of one group: CL = 1 for independent
+// CTAs, 2 for a 2-SM pair, one m-tile per CTA) -> this CTA's (first row, valid
+// rows, expert).  A CTA whose m-tile
 // lies past its group's end gets rows = 0 (it still takes part in the loads).
 template <int CL, typename SH>
 __device__ __forceinline__ void decode_mtile(const SH& sh, int G, int mu, int rank, int& row0, int& rows, int& e) {
@@ -191,7 +186,7 @@ __device__ __forceinline__ void gather_sources(const int32_t* __restrict__ gathe
 constexpr int GATHER_WARPS = 8;
 constexpr int GATHER_DEPTH = 5;
 constexpr int RPL = 4;  // 16-byte pieces per lane per k-block: 8 warps x 32 lanes x 4 = 128 rows x 128 B
-template <bool GLU, int CL, int GW = 0>
+template <bool GLU, int GW = 0>
 __global__ void __launch_bounds__(THREADS + 32 * GW, 1)
 ffn_tc_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b,
               const __grid_constant__ CUtensorMap map_out,
@@ -212,7 +207,7 @@ ffn_tc_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(&sh.full[s], 1 + 32 * GW);
-      mbar_init(&sh.empty[s], CL);  // released by the MMA of every CTA that reads this stage
+      mbar_init(&sh.empty[s], 1);  // released by the MMA's commit
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(&sh.tfull[a], 1);
@@ -242,7 +237,7 @@ ffn_tc_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__
         const int lo = sh.off[g], hi = sh.off[g + 1], e = sh.pe[g];
         if (lo < 0 || hi < lo || hi > P) atomicOr(&g_err, SEMMOE_DEVERR_PAIRS);
         else if (e < 0 || e >= E) atomicOr(&g_err, SEMMOE_DEVERR_EXPERT);
-        else c = ((hi - lo + BM - 1) / BM + CL - 1) / CL;
+        else c = (hi - lo + BM - 1) / BM;
       }
       cnt[i] = c;
       sum += c;
@@ -268,14 +263,11 @@ ffn_tc_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__
   fence_before();
   __syncthreads();
   fence_after();
-  if (CL > 1) cluster_sync_all();  // the peers' barriers exist before any multicast reaches them
 
   const uint32_t tmem = sh.tmem_base;
-  const int total = sh.total_mtiles * n_tiles;  // tile units: (CL m-tiles, n-tile)
+  const int total = sh.total_mtiles * n_tiles;  // tile units: (m-tile, n-tile)
   const int kb_n = (K + BK - 1) / BK;
-  const int rank = CL > 1 ? (int)cluster_ctarank() : 0;
-  const int unit0 = blockIdx.x / CL, units = gridDim.x / CL;
-  constexpr uint16_t kAll = (uint16_t)((1u << CL) - 1);
+  const int unit0 = blockIdx.x, units = gridDim.x;
 
   if (warp == 0) {
     // ---------------- TMA producer (warp 0; lane 0 unless A rows are gathered) ----------------
@@ -286,7 +278,7 @@ ffn_tc_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__
       if (*abort_flag) break;
       const int mt = tile / n_tiles, nt = tile % n_tiles;
       int row0, rows, e;
-      decode_mtile<CL>(sh, G, mt, rank, row0, rows, e);
+      decode_mtile<1>(sh, G, mt, 0, row0, rows, e);
       int src[4] = {0, 0, 0, 0};
       if (tg != nullptr) gather_sources(tg, gather_div, gather_rows, P, row0, lane, src);
       bool ok = true;
@@ -308,19 +300,11 @@ ffn_tc_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__
         }
         if (lane == 0) {
           unsigned char* b = stage_b + s * B_BYTES;
-          if (CL == 1) {
-            if (GLU) {
-              tma_load_4d(b, &map_b, &sh.full[s], kb * BK, nt * 128, 0, e);
-              tma_load_4d(b + B_BYTES / 2, &map_b, &sh.full[s], kb * BK, nt * 128, 1, e);
-            } else {
-              tma_load_3d(b, &map_b, &sh.full[s], kb * BK, nt * BN, e);
-            }
-          } else {  // CTA `rank` loads half `rank` of the shared weight tile for both CTAs
-            if (GLU)
-              tma_load_4d_mc(b + rank * (B_BYTES / 2), &map_b, &sh.full[s], kb * BK, nt * 128, rank, e, kAll);
-            else
-              tma_load_3d_mc(b + rank * (B_BYTES / 2), &map_b, &sh.full[s], kb * BK, nt * BN + rank * 128, e,
-                             kAll);
+          if (GLU) {
+            tma_load_4d(b, &map_b, &sh.full[s], kb * BK, nt * 128, 0, e);
+            tma_load_4d(b + B_BYTES / 2, &map_b, &sh.full[s], kb * BK, nt * 128, 1, e);
+          } else {
+            tma_load_3d(b, &map_b, &sh.full[s], kb * BK, nt * BN, e);
           }
         }
         ++it;
@@ -351,8 +335,7 @@ ffn_tc_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__
 #pragma unroll
           for (int k = 0; k < BK / UK; ++k)
             mma_bf16(d, sw128_desc(sa + k * UK * 2), sw128_desc(sb + k * UK * 2), kIdesc, (kb | k) != 0);
-          if (CL == 1) commit(&sh.empty[s]);  // frees the stage once these MMAs have read it
-          else commit_mc(&sh.empty[s], kAll);  // in every CTA whose producer writes this stage
+          commit(&sh.empty[s]);  // frees the stage once these MMAs have read it
           ++it;
         }
         if (!ok) break;
@@ -371,7 +354,7 @@ ffn_tc_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__
     for (int tile = unit0; tile < total; tile += units) {
       const int mt = tile / n_tiles, nt = tile % n_tiles;
       int row0, rows, e;
-      decode_mtile<CL>(sh, G, mt, rank, row0, rows, e);
+      decode_mtile<1>(sh, G, mt, 0, row0, rows, e);
       const uint32_t a = acc_it & 1, aph = (acc_it >> 1) & 1;
       int ok = 1;
       if (lane == 0) ok = mbar_wait(&sh.tfull[a], aph, abort_flag, &g_err);
@@ -491,7 +474,6 @@ ffn_tc_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__
 
   fence_before();
   __syncthreads();
-  if (CL > 1) cluster_sync_all();  // no peer still multicasts into, or arrives on, this CTA
   if (warp == 1) {
     __syncwarp();
     fence_after();
@@ -500,7 +482,7 @@ ffn_tc_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__
 }
 
 // ---------------------------------------------------------------------------
-// 2-SM variant (SEMMOE_FFN_MODE=pair): clusters of two CTAs on two SMs run
+// 2-SM variant: clusters of two CTAs on two SMs run
 // tcgen05.mma.cta_group::2 with M = 256.  Each CTA stages its own 128 A rows and
 // half of the 256-row weight tile (CTA 0 the gate / first half, CTA 1 the up /
 // second half); the pair's even CTA issues the MMAs, and each CTA's TMEM holds
@@ -753,45 +735,20 @@ struct Gather {
   const __nv_bfloat16* x = nullptr;
 };
 
-template <bool GLU, int CL, int GW = 0>
+template <bool GLU, int GW = 0>
 cudaError_t launch_one(const CUtensorMap& ma, const CUtensorMap& mb, const CUtensorMap& mo, const int32_t* offsets,
                        const int32_t* p2e,
                        int G, int P, int E, int N, int K, int n_tiles, Gather ga, __nv_bfloat16* out,
                        cudaStream_t s) {
-  auto kern = ffn_tc_kernel<GLU, CL, GW>;
+  auto kern = ffn_tc_kernel<GLU, GW>;
   static std::atomic<unsigned long long> smem_set{0};
   cudaError_t e = ensure_smem_limit(kern, (int)kSmemBytes, smem_set);
   if (e != cudaSuccess) return e;
   const long long max_units = ((long long)(P + BM - 1) / BM + G) * n_tiles;  // >= tile units of any grouping
-  if (CL == 1) {
-    int grid = sm_count();
-    if (max_units < grid) grid = (int)max_units;
-    kern<<<grid, THREADS + 32 * GW, kSmemBytes, s>>>(ma, mb, mo, offsets, p2e, G, P, E, N, K, n_tiles, ga.rows,
-                                                     ga.div, ga.n, out, ga.x);
-  } else {
-    cudaLaunchConfig_t cfg = {};
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = CL;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.blockDim = dim3(THREADS);
-    cfg.dynamicSmemBytes = kSmemBytes;
-    cfg.stream = s;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    cfg.gridDim = dim3(sm_count() / CL * CL);
-    int clusters = 0;  // as many clusters as can be resident at once
-    e = cudaOccupancyMaxActiveClusters(&clusters, kern, &cfg);
-    if (e != cudaSuccess) return e;
-    if (clusters < 1) return cudaErrorInvalidConfiguration;
-    long long units = clusters;
-    if (max_units < units) units = max_units;
-    cfg.gridDim = dim3((unsigned)(units * CL));
-    e = cudaLaunchKernelEx(&cfg, kern, ma, mb, mo, offsets, p2e, G, P, E, N, K, n_tiles, ga.rows, ga.div, ga.n, out,
-                           ga.x);
-    if (e != cudaSuccess) return e;
-  }
+  int grid = sm_count();
+  if (max_units < grid) grid = (int)max_units;
+  kern<<<grid, THREADS + 32 * GW, kSmemBytes, s>>>(ma, mb, mo, offsets, p2e, G, P, E, N, K, n_tiles, ga.rows, ga.div,
+                                                   ga.n, out, ga.x);
   count_launches(1);
   return cudaGetLastError();
 }
@@ -835,50 +792,37 @@ cudaError_t launch_pair(const CUtensorMap& ma, const CUtensorMap& mb, const CUte
 
 int ffn_tc_take_errors(cudaStream_t s, int* bits) { return take_error_word(g_err, s, bits); }
 
-// Grouped-GEMM form, chosen per GEMM: 0 = independent CTAs; 1 = pairs sharing
-// weight tiles by multicast; 2 / 3 = 2-SM MMA pairs with one / two accumulator
-// buffers.  A pair covers two m-tiles of one group, so short groups leave half
-// of it idle.  Defaults: GEMM1 (K = H) in 2-SM pairs when the groups average at
-// least 512 rows (P >= 512 G), GEMM2 (K = I) when I >= 512 and they average at
-// least 256 (P >= 256 G), independent CTAs otherwise (measured per GEMM on the
-// DeepSeek, Qwen3 and MoE-Prism shapes).  A GEMM1 that gathers its rows runs
-// in the single-CTA form, where gathering warps feed it (2.1x faster than TMA
-// row gathers from the producer warp at the DeepSeek shape; gathering warps in
-// the 2-SM form measured twice as slow as in the single-CTA form).
-// SEMMOE_FFN_MODE=single|multicast|pair1|pair sets both.
-static void ffn_modes(int I, int P, int G, bool gathered, int* m1, int* m2) {
-  const char* v = getenv("SEMMOE_FFN_MODE");
-  if (v != nullptr) {
-    int m = -1;
-    if (strcmp(v, "single") == 0) m = 0;
-    if (strcmp(v, "multicast") == 0) m = 1;
-    if (strcmp(v, "pair1") == 0) m = 2;
-    if (strcmp(v, "pair") == 0) m = 3;
-    if (m >= 0) {
-      *m1 = *m2 = m;
-      return;
-    }
-  }
-  *m1 = !gathered && (long long)P >= 4LL * BM * G ? 3 : 0;
-  *m2 = (I >= 512 && (long long)P >= 2LL * BM * G) ? 3 : 0;
+// Grouped-GEMM form of one GEMM (SEMMOE_FORM_*).  The default picks, from the
+// shapes alone: GEMM1 (K = H) in 2-SM pairs when the groups average at least
+// 512 rows (P >= 512 G), GEMM2 (K = I) when I >= 512 and they average at least
+// 256 (P >= 256 G), independent CTAs otherwise (measured per GEMM on the
+// DeepSeek, Qwen3 and MoE-Prism shapes).  A pair covers two m-tiles of one
+// group, so short groups leave half of it idle.  A GEMM1 that gathers its rows
+// runs in the single-CTA form, where gathering warps feed it (2.1x faster than
+// TMA row gathers from the producer warp at the DeepSeek shape; gathering warps
+// in the 2-SM form measured twice as slow as in the single-CTA form).
+static int resolve_form(int form, bool glu, int I, int P, int G, bool gathered) {
+  if (form != SEMMOE_FORM_DEFAULT) return form;
+  if (glu) return !gathered && (long long)P >= 4LL * BM * G ? SEMMOE_FORM_PAIR : SEMMOE_FORM_SINGLE;
+  return (I >= 512 && (long long)P >= 2LL * BM * G) ? SEMMOE_FORM_PAIR : SEMMOE_FORM_SINGLE;
 }
 
-// One GEMM of the FFN in form `mode`.
+// One GEMM of the FFN in a resolved form.
 template <bool GLU>
-static cudaError_t launch_gemm(int mode, const CUtensorMap& ma, const CUtensorMap& mb, const CUtensorMap& mo,
+static cudaError_t launch_gemm(int form, const CUtensorMap& ma, const CUtensorMap& mb, const CUtensorMap& mo,
                                const int32_t* offsets, const int32_t* p2e, int G, int P, int E, int N, int K,
                                int n_tiles, Gather ga, __nv_bfloat16* out, cudaStream_t s) {
-  switch (mode) {
-    case 1: return launch_one<GLU, 2>(ma, mb, mo, offsets, p2e, G, P, E, N, K, n_tiles, ga, out, s);
-    case 2: return launch_pair<GLU, 1>(ma, mb, mo, offsets, p2e, G, P, E, N, K, n_tiles, ga, out, s);
-    case 3: return launch_pair<GLU, 2>(ma, mb, mo, offsets, p2e, G, P, E, N, K, n_tiles, ga, out, s);
+  switch (form) {
+    case SEMMOE_FORM_PAIR1: return launch_pair<GLU, 1>(ma, mb, mo, offsets, p2e, G, P, E, N, K, n_tiles, ga, out, s);
+    case SEMMOE_FORM_PAIR: return launch_pair<GLU, 2>(ma, mb, mo, offsets, p2e, G, P, E, N, K, n_tiles, ga, out, s);
+    case SEMMOE_FORM_SINGLE_TMA_GATHER:  // gathered rows by TMA four-row gathers from the producer warp
+      return launch_one<GLU>(ma, mb, mo, offsets, p2e, G, P, E, N, K, n_tiles, ga, out, s);
     default:
-      if constexpr (GLU) {  // gathered rows: gathering warps unless SEMMOE_GATHER_WARPS=0 (TMA row gathers)
-        const char* gwv = getenv("SEMMOE_GATHER_WARPS");
-        if (ga.rows != nullptr && !(gwv != nullptr && atoi(gwv) == 0))
-          return launch_one<GLU, 1, GATHER_WARPS>(ma, mb, mo, offsets, p2e, G, P, E, N, K, n_tiles, ga, out, s);
+      if constexpr (GLU) {
+        if (ga.rows != nullptr)  // gathered rows: gathering warps
+          return launch_one<GLU, GATHER_WARPS>(ma, mb, mo, offsets, p2e, G, P, E, N, K, n_tiles, ga, out, s);
       }
-      return launch_one<GLU, 1>(ma, mb, mo, offsets, p2e, G, P, E, N, K, n_tiles, ga, out, s);
+      return launch_one<GLU>(ma, mb, mo, offsets, p2e, G, P, E, N, K, n_tiles, ga, out, s);
   }
 }
 
@@ -886,12 +830,12 @@ static cudaError_t launch_gemm(int mode, const CUtensorMap& ma, const CUtensorMa
 // q of GEMM1 reads x row gather_rows[q] / gather_div.
 cudaError_t launch_ffn_tc(const void* x, const int32_t* offsets, const int32_t* p2e, const void* w13,
                           const void* w2, int P, int E, int H, int I, void* y, void* ws, const int32_t* gather_rows,
-                          int gather_div, int T_x, cudaStream_t s) {
+                          int gather_div, int T_x, int form1, int form2, cudaStream_t s) {
   if (P == 0) return cudaSuccess;
   const int G = offsets ? E : 1;
-  int mode1 = 0, mode2 = 0;
-  ffn_modes(I, P, G, gather_rows != nullptr, &mode1, &mode2);
-  const int CL = mode2 == 0 ? 1 : 2;  // CTAs sharing GEMM2's weight tile
+  const int mode1 = resolve_form(form1, true, I, P, G, gather_rows != nullptr);
+  const int mode2 = resolve_form(form2, false, I, P, G, false);
+  const int CL = mode2 == SEMMOE_FORM_SINGLE ? 1 : 2;  // CTAs of a pair each load half of GEMM2's weight tile
   const cuuint64_t es = 2;
   CUtensorMap ma1, mb1, ma2, mb2;
   Gather ga;
@@ -925,7 +869,7 @@ cudaError_t launch_ffn_tc(const void* x, const int32_t* offsets, const int32_t* 
   {
     const cuuint64_t dims[3] = {(cuuint64_t)I, (cuuint64_t)H, (cuuint64_t)E};
     const cuuint64_t str[2] = {(cuuint64_t)I * es, (cuuint64_t)H * I * es};
-    const cuuint32_t box[3] = {BK, (cuuint32_t)(BN / CL), 1};  // a cluster CTA loads 1/CL of the tile
+    const cuuint32_t box[3] = {BK, (cuuint32_t)(BN / CL), 1};  // a pair CTA loads half of the tile
     if (!make_map_bf16(&mb2, w2, 3, dims, str, box)) return cudaErrorInvalidValue;
   }
   // outputs h [P, I] and y [P, H], written by the epilogue's TMA stores in

@@ -5,6 +5,8 @@
 #include <stddef.h>
 #include <stdint.h>
 
+#include "semmoe.h"
+
 namespace semmoe {
 
 // Adds n to the library-wide count of kernel launches (see semmoe_kernel_launches).
@@ -67,9 +69,12 @@ size_t ffn_ws_bytes(int P, int I, int dtype);
 // offsets == nullptr: one group of rows [0, P) using expert 0 of w13/w2.
 // gather != nullptr: x is [T_x, H] unpermuted and GEMM1's sorted row q reads x
 // row gather[q] / gather_div; otherwise x holds the P sorted rows.
+// form1 / form2: SEMMOE_FORM_* of GEMM1 / GEMM2 (SEMMOE_FORM_DEFAULT: chosen from
+// the shapes; SEMMOE_FORM_CUDA_CORE in form1 runs both GEMMs on CUDA cores).
 cudaError_t launch_ffn(const void* x, const int32_t* offsets, const int32_t* phys_to_expert,
                        const void* w13, const void* w2, int dtype, int P, int E, int H, int I,
-                       void* y, void* ws, const int32_t* gather, int gather_div, int T_x, cudaStream_t s);
+                       void* y, void* ws, const int32_t* gather, int gather_div, int T_x, cudaStream_t s,
+                       int form1 = SEMMOE_FORM_DEFAULT, int form2 = SEMMOE_FORM_DEFAULT);
 
 cudaError_t launch_combine(const void* y_perm, const int32_t* pair_to_sorted, const float* topk_w,
                            const void* y_shared, int dtype, int T, int H, int k_max, int P,

@@ -12,6 +12,8 @@
 //                    both maps; CTA 0 writes the bucket and rank tables
 // then perm_copy writes each x row to its tokens' sorted rows (one warp per
 // token, 16-byte vectors).
+#include <cuda.h>
+
 #include <mutex>
 
 #include "common.cuh"
@@ -322,24 +324,61 @@ cudaError_t launch_permute(const int32_t* topk_idx, const int32_t* expert_rank, 
 
 size_t permute_noalloc_max_scratch() { return kNoAllocScratchBytes; }
 
-// Device address of g_noalloc_scratch on the current device.  In host code the
-// array's name is only a host-side stand-in, so the address is looked up once
-// per device (with that device current) and cached.
+// Device address of g_noalloc_scratch in the current CUDA context.  In host
+// code the array's name is only a host-side stand-in, so the address is looked
+// up with cudaGetSymbolAddress, with the context current, and cached.  The
+// cache is keyed on the context's unique ID (cuCtxGetId), not on the device
+// number: after cudaDeviceReset, or in another context on the same device, the
+// library's module is loaded again and the array has another address, while a
+// context's ID is never reused within the process.
+// The two driver calls, fetched through the runtime (the library links no
+// driver library, so it still loads on hosts without one).
+template <typename F>
+static F driver_fn(const char* name, int version) {
+  void* p = nullptr;
+  cudaDriverEntryPointQueryResult q;
+  if (cudaGetDriverEntryPointByVersion(name, &p, version, cudaEnableDefault, &q) != cudaSuccess ||
+      q != cudaDriverEntryPointSuccess)
+    return nullptr;
+  return reinterpret_cast<F>(p);
+}
+
 static cudaError_t noalloc_scratch_address(void** out) {
+  using CtxGetCurrent = CUresult (*)(CUcontext*);
+  using CtxGetId = CUresult (*)(CUcontext, unsigned long long*);
+  static const CtxGetCurrent ctx_get_current = driver_fn<CtxGetCurrent>("cuCtxGetCurrent", 4000);
+  static const CtxGetId ctx_get_id = driver_fn<CtxGetId>("cuCtxGetId", 12000);
+  if (ctx_get_current == nullptr || ctx_get_id == nullptr) return cudaErrorNotSupported;
+  struct Entry {
+    unsigned long long ctx_id;
+    void* addr;
+  };
+  constexpr int kSlots = 16;
   static std::mutex mu;
-  static void* addr[64] = {};
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return e;
-  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-  std::lock_guard<std::mutex> lock(mu);
-  if (addr[dev] == nullptr) {
+  static Entry cache[kSlots] = {};
+  static int next_slot = 0;
+  CUcontext ctx = nullptr;
+  if (ctx_get_current(&ctx) != CUDA_SUCCESS) return cudaErrorInitializationError;
+  if (ctx == nullptr) {  // the runtime has not made a context current on this thread yet: let it
     void* p = nullptr;
-    e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+    cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
     if (e != cudaSuccess) return e;
-    addr[dev] = p;
+    if (ctx_get_current(&ctx) != CUDA_SUCCESS || ctx == nullptr) return cudaErrorInitializationError;
   }
-  *out = addr[dev];
+  unsigned long long id = 0;
+  if (ctx_get_id(ctx, &id) != CUDA_SUCCESS) return cudaErrorInitializationError;
+  std::lock_guard<std::mutex> lock(mu);
+  for (const Entry& en : cache)
+    if (en.addr != nullptr && en.ctx_id == id) {
+      *out = en.addr;
+      return cudaSuccess;
+    }
+  void* p = nullptr;
+  cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+  if (e != cudaSuccess) return e;
+  cache[next_slot] = Entry{id, p};  // oldest entry replaced once all slots are used
+  next_slot = (next_slot + 1) % kSlots;
+  *out = p;
   return cudaSuccess;
 }
 
