@@ -209,6 +209,89 @@ def _cores():
         return os.cpu_count()
 
 
+def _cpu_model() -> str:
+    """The host CPU's model name (lscpu, else /proc/cpuinfo, else platform)."""
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for ln in out.splitlines():
+            if ln.strip().lower().startswith("model name"):
+                return ln.split(":", 1)[1].strip()
+    except Exception:
+        pass
+    try:
+        with open("/proc/cpuinfo") as f:
+            for ln in f:
+                if ln.lower().startswith(("model name", "cpu model")):
+                    return ln.split(":", 1)[1].strip()
+    except Exception:
+        pass
+    import platform
+    return platform.processor() or platform.machine()
+
+
+def _blas_threads():
+    """Threads numpy's BLAS runs with: asked of the loaded OpenBLAS itself,
+    else the thread environment variables, else the usable cores."""
+    import ctypes
+    try:
+        with open("/proc/self/maps") as f:
+            paths = sorted({ln.split()[-1] for ln in f if "openblas" in ln.lower() and ".so" in ln})
+        for path in paths:
+            lib = ctypes.CDLL(path)
+            for sym in ("scipy_openblas_get_num_threads64_", "openblas_get_num_threads64_",
+                        "openblas_get_num_threads"):
+                fn = getattr(lib, sym, None)
+                if fn is not None:
+                    fn.restype = ctypes.c_int
+                    return int(fn()), f"{os.path.basename(path)} {sym}()"
+    except Exception:
+        pass
+    for var in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS"):
+        if os.environ.get(var, "").isdigit():
+            return int(os.environ[var]), var
+    return _cores(), "usable cores (BLAS default)"
+
+
+def _cpu_desc(value, sample):
+    threads, how = _blas_threads()
+    return {"value": value, "unit": "tokens/s", "cores": threads, "kind": "oracle", "sample": sample,
+            "cpu_model": _cpu_model(), "host_cores": _cores(), "threads_from": how}
+
+
+#: workloads the oracle is also timed on with one thread (tiny layer, decode)
+SINGLE_THREAD_CONFIGS = ("tiny_fp32_T256_E8", "dsv2lite_decode_T64")
+
+
+def oracle_single_thread():
+    """Oracle tokens/s on the tiny and decode workloads with one BLAS thread.
+    Runs in a child process started with the thread variables set to 1 (numpy
+    reads them once, at import)."""
+    out = {}
+    for name in SINGLE_THREAD_CONFIGS:
+        spec = wl.CONFIGS[name]
+        d = wl.make_inputs(spec)
+        rate, dt = cpu_oracle_rate(d, spec.T)
+        out[name] = {"value": rate, "unit": "tokens/s", "s": dt, "tokens": spec.T}
+    threads, how = _blas_threads()
+    out["threads"] = threads
+    out["threads_from"] = how
+    return out
+
+
+def _single_thread_baseline():
+    env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1",
+               CUDA_VISIBLE_DEVICES="")
+    try:
+        r = subprocess.run([sys.executable, os.path.abspath(__file__), "--oracle-single-thread"],
+                           capture_output=True, text=True, timeout=600, env=env)
+        for ln in r.stdout.splitlines()[::-1]:
+            if ln.startswith("{"):
+                return json.loads(ln)
+        return {"error": (r.stderr or r.stdout)[-300:]}
+    except Exception as e:  # reported, never fatal to the benchmark line
+        return {"error": repr(e)[:300]}
+
+
 def run_reference(args, world, rank):
     """The oracle as the reference arm: each step is a bounded sample of the workload."""
     if rank != 0:
@@ -231,8 +314,7 @@ def run_reference(args, world, rank):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1000 * total / args.steps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic", "config": _config(spec),
-        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": _cores(), "kind": "oracle",
-                         "sample": sample},
+        "cpu_baseline": _cpu_desc(value, sample),
         "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
@@ -316,56 +398,47 @@ def _time_around_layer(args, spec, d, layer, dev, stream):
     return out
 
 
-def run_ours(args, world, rank, local):
-    from token_expert_routing_gb300 import MoELayer, _abi
-
-    dev = torch.device("cuda", local)
-    torch.cuda.set_device(dev)
-    spec = wl.CONFIGS[args.config]
-    d = wl.make_inputs(spec)
-    # the layer as a user runs it (its steps spread over two streams), and the
-    # same layer with every step on one stream, whose per-step events give the
-    # stage times and the roofline of each kernel alone
+def _build_layers(spec, d, dev):
+    """The layer as a user runs it (its steps spread over two streams), and the
+    same layer with every step on one stream, whose per-step events give the
+    stage times and the roofline of each kernel alone."""
+    from token_expert_routing_gb300 import MoELayer
     layer = MoELayer(d["w_router"], d["w13"], d["w2"], d["expert_rank"], d["lut"], spec.R, spec.k_max,
                      d["ws13"], d["ws2"], device=dev)
     serial = MoELayer(d["w_router"], d["w13"], d["w2"], d["expert_rank"], d["lut"], spec.R, spec.k_max,
                       d["ws13"], d["ws2"], overlap=False, overlap_shared=False, device=dev)
-    x = d["x"].to(dev)
-    ids = d["token_ids"].to(dev)
-    per_token = bool(spec.k_choices)
-    kpt = d["k_per_token"].to(dev) if per_token else None
-    k = None if per_token else spec.k
-    P = int(d["k_per_token"].sum())
-    stream = torch.cuda.current_stream(dev)
+    return layer, serial
+
+
+def _time_eager(serial, inp, steps, warmup, world, dev, stream, local):
+    """K one-stream forwards, inputs resident in HBM; per-step events give the stages."""
+    from token_expert_routing_gb300 import _abi
+    x, ids, kpt, k, P = inp
 
     def step(marks=None, side_marks=None):
         return serial.forward(x, ids, kpt, k, P, stream=stream, marks=marks, side_marks=side_marks)
 
-    for _ in range(args.warmup):
+    for _ in range(warmup):
         step()
     _abi.semmoe_check_errors()
-
-    # device-timed region: K whole-layer steps, inputs resident in HBM
-    all_marks = [[] for _ in range(args.steps)]
-    all_side = [[] for _ in range(args.steps)]
+    all_marks = [[] for _ in range(steps)]
+    all_side = [[] for _ in range(steps)]
     launches0 = _abi.semmoe_kernel_launches()
     _barrier(world)
     torch.cuda.synchronize(dev)
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    with ClockSampler(local) as clocks_eager:
+    with ClockSampler(local) as clocks:
         h0 = time.perf_counter()
         start.record(stream)
-        for i in range(args.steps):
+        for i in range(steps):
             step(all_marks[i], all_side[i])
         end.record(stream)
-        host_ms = (time.perf_counter() - h0) * 1e3 / args.steps   # enqueue cost per step
+        host_ms = (time.perf_counter() - h0) * 1e3 / steps   # enqueue cost per step
         torch.cuda.synchronize(dev)
     _barrier(world)
     launches = _abi.semmoe_kernel_launches() - launches0
     _abi.semmoe_check_errors()
-    ms = start.elapsed_time(end)
-    ms_max = _max_over_ranks(world, ms)
-
+    ms_max = _max_over_ranks(world, start.elapsed_time(end))
     stage_ms = {}
     for marks in all_marks:
         for (_, a), (name, b) in zip(marks[:-1], marks[1:]):
@@ -374,41 +447,147 @@ def run_ours(args, world, rank, local):
         for name, a, b in side:
             stage_ms.setdefault(name, []).append(a.elapsed_time(b))
     stage_avg = {n: sum(v) / len(v) for n, v in stage_ms.items()}
-    per_step = sorted(m[0][1].elapsed_time(m[-1][1]) for m in all_marks)  # each eager step, first to last mark
+    per_step = sorted(m[0][1].elapsed_time(m[-1][1]) for m in all_marks)  # each step, first to last mark
+    return dict(ms_max=ms_max, stage_avg=stage_avg, per_step=per_step, launches=launches, host_ms=host_ms,
+                clocks=clocks.summary())
 
-    # the same forward as one CUDA-graph replay per step (static buffers)
-    graph = None
-    if not args.no_graph:
-        from token_expert_routing_gb300 import CapturedLayer
-        cap = CapturedLayer(layer, spec.T, None if per_token else spec.k, d["k_per_token"] if per_token else None)
-        cap.x.copy_(x)
-        cap.token_ids.copy_(ids)
-        for _ in range(args.warmup):
+
+def _time_graph(layer, spec, d, inp, steps, warmup, world, dev, local):
+    """The same forward as one CUDA-graph replay per step (static buffers)."""
+    from token_expert_routing_gb300 import CapturedLayer, _abi
+    x, ids, _, _, _ = inp
+    per_token = bool(spec.k_choices)
+    cap = CapturedLayer(layer, spec.T, None if per_token else spec.k, d["k_per_token"] if per_token else None)
+    cap.x.copy_(x)
+    cap.token_ids.copy_(ids)
+    for _ in range(warmup):
+        cap.replay()
+    _barrier(world)
+    torch.cuda.synchronize(dev)
+    g0, g1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    rep_ev = [torch.cuda.Event(enable_timing=True) for _ in range(steps + 1)]
+    with ClockSampler(local) as clocks_graph:
+        g0.record()
+        rep_ev[0].record()
+        for i in range(steps):
             cap.replay()
-        _barrier(world)
+            rep_ev[i + 1].record()
+        g1.record()
         torch.cuda.synchronize(dev)
-        g0, g1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        rep_ev = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps + 1)]
-        with ClockSampler(local) as clocks_graph:
-            g0.record()
-            rep_ev[0].record()
-            for i in range(args.steps):
-                cap.replay()
-                rep_ev[i + 1].record()
-            g1.record()
-            torch.cuda.synchronize(dev)
-        per_replay = sorted(a.elapsed_time(b) for a, b in zip(rep_ev[:-1], rep_ev[1:]))
-        _barrier(world)
-        g_ms = _max_over_ranks(world, g0.elapsed_time(g1))
-        _abi.semmoe_check_errors()
-        graph = {"value": spec.T * args.steps * world / (g_ms * 1e-3), "unit": "tokens/s",
-                 "ms_per_step": g_ms / args.steps,
-                 "how": "CapturedLayer: the whole forward (steps on two streams: bookkeeping and the shared "
-                        "experts beside the permute and routed FFN) captured once as a CUDA graph, one replay "
-                        "per step",
-                 "ms_median": per_replay[len(per_replay) // 2], "ms_min": per_replay[0], "ms_max": per_replay[-1],
-                 "clocks": clocks_graph.summary()}
-        del cap
+    per_replay = sorted(a.elapsed_time(b) for a, b in zip(rep_ev[:-1], rep_ev[1:]))
+    _barrier(world)
+    g_ms = _max_over_ranks(world, g0.elapsed_time(g1))
+    _abi.semmoe_check_errors()
+    del cap
+    return {"value": spec.T * steps * world / (g_ms * 1e-3), "unit": "tokens/s",
+            "ms_per_step": g_ms / steps,
+            "how": "CapturedLayer: the whole forward (steps on two streams: bookkeeping and the shared "
+                   "experts beside the permute and routed FFN) captured once as a CUDA graph, one replay "
+                   "per step",
+            "ms_median": per_replay[len(per_replay) // 2], "ms_min": per_replay[0], "ms_max": per_replay[-1],
+            "clocks": clocks_graph.summary()}
+
+
+def _roofline_and_stages(spec, P, active, fused_gather, stage_avg, peaks):
+    """The grouped FFN's roofline object and every stage's fraction of its bound."""
+    fb = _flops_bytes(spec, P, active, fused_gather)
+    ffn_ms = stage_avg["grouped_ffn"]
+    ffn = fb["grouped_ffn"]
+    ffn_call = "semmoe_grouped_ffn_gather" if fused_gather else "semmoe_grouped_ffn"
+    # the FFN's bound: whichever of its flops at the tensor peak and its bytes at
+    # the HBM peak takes longer (weight streaming wins for small batches)
+    t_tc = ffn["flops"] / (peaks["bf16_tflops"] * 1e12)
+    t_hbm = ffn["bytes"] / (peaks["hbm_gbs"] * 1e9)
+    tflops = ffn["flops"] / (ffn_ms * 1e-3) / 1e12
+    gbs = ffn["bytes"] / (ffn_ms * 1e-3) / 1e9
+    if t_tc >= t_hbm:
+        roofline = {
+            "kernel": ffn_call + " (GEMM1+SwiGLU, GEMM2)",
+            "bound": "tensor", "achieved": tflops, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+            "frac": tflops / peaks["bf16_tflops"], "traffic": _traffic(ffn_call, spec.name),
+            "peak_source": f"{peaks['source']} bf16 burst (short timed region, SM clock at its maximum); "
+                           f"sustained figure {peaks['bf16_tflops_sustained']} TFLOP/s",
+            "frac_of_sustained": tflops / peaks["bf16_tflops_sustained"],
+            "frac_hbm": gbs / peaks["hbm_gbs"],
+            "algorithmic_flops": ffn["flops"], "ms": ffn_ms,
+        }
+    else:
+        roofline = {
+            "kernel": ffn_call + " (GEMM1+SwiGLU, GEMM2)",
+            "bound": "hbm", "achieved": gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+            "frac": gbs / peaks["hbm_gbs"], "traffic": _traffic(ffn_call, spec.name),
+            "peak_source": f"{peaks['source']} HBM copy bandwidth",
+            "algorithmic_bytes": ffn["bytes"], "active_experts": active,
+            "frac_tensor": tflops / peaks["bf16_tflops"], "ms": ffn_ms,
+        }
+    stages = {}
+    for name, avg in stage_avg.items():
+        ent = {"ms": avg}
+        f = fb.get(name, {})
+        if "flops" in f:
+            ent["tflops"] = f["flops"] / (avg * 1e-3) / 1e12
+            ent["frac_tensor"] = ent["tflops"] / peaks["bf16_tflops"]
+        if "bytes" in f:
+            ent["gbs"] = f["bytes"] / (avg * 1e-3) / 1e9
+            ent["frac_hbm"] = ent["gbs"] / peaks["hbm_gbs"]
+        stages[name] = ent
+    return roofline, stages
+
+
+def _inputs_on(spec, d, dev):
+    per_token = bool(spec.k_choices)
+    return (d["x"].to(dev), d["token_ids"].to(dev), d["k_per_token"].to(dev) if per_token else None,
+            None if per_token else spec.k, int(d["k_per_token"].sum()))
+
+
+def _other_workloads(args, world, dev, stream, local, peaks):
+    """The other large workloads, timed the same way with fewer steps: their
+    graph-replay throughput, FFN roofline and the permute / combine / route
+    fractions of HBM (the survey's HBM targets apply on each)."""
+    out = {}
+    for name in [n for n in args.also.split(",") if n and n != args.config]:
+        spec = wl.CONFIGS[name]
+        d = wl.make_inputs(spec)
+        layer, serial = _build_layers(spec, d, dev)
+        inp = _inputs_on(spec, d, dev)
+        steps = max(3, args.also_steps)
+        ev = _time_eager(serial, inp, steps, args.warmup, world, dev, stream, local)
+        gr = None if args.no_graph else _time_graph(layer, spec, d, inp, steps, args.warmup, world, dev, local)
+        res = layer.forward(*inp[:4], inp[4], stream=stream)
+        active = int((res.expert_counts > 0).sum())
+        roof, stages = _roofline_and_stages(spec, inp[4], active, serial.fused_gather, ev["stage_avg"], peaks)
+        eager_value = spec.T * steps * world / (ev["ms_max"] * 1e-3)
+        best = gr if gr is not None and gr["ms_per_step"] < ev["ms_max"] / steps else None
+        out[name] = {
+            "value": best["value"] if best else eager_value, "unit": "tokens/s",
+            "ms_per_step": best["ms_per_step"] if best else ev["ms_max"] / steps,
+            "timed_path": "graph replay" if best else "eager, one stream", "steps": steps,
+            "eager_ms_per_step": ev["ms_max"] / steps,
+            "roofline": {k: roof[k] for k in ("bound", "achieved", "peak", "unit", "frac", "ms")},
+            "stages": {k: {kk: round(vv, 5) for kk, vv in v.items()} for k, v in stages.items()},
+            "clocks": (best or ev)["clocks"],
+        }
+        del layer, serial, res, d
+        torch.cuda.empty_cache()
+    return out
+
+
+def run_ours(args, world, rank, local):
+    from token_expert_routing_gb300 import _abi
+
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    spec = wl.CONFIGS[args.config]
+    d = wl.make_inputs(spec)
+    layer, serial = _build_layers(spec, d, dev)
+    inp = _inputs_on(spec, d, dev)
+    x, ids, kpt, k, P = inp
+    per_token = bool(spec.k_choices)
+    stream = torch.cuda.current_stream(dev)
+
+    ev = _time_eager(serial, inp, args.steps, args.warmup, world, dev, stream, local)
+    ms_max, stage_avg, per_step = ev["ms_max"], ev["stage_avg"], ev["per_step"]
+    graph = None if args.no_graph else _time_graph(layer, spec, d, inp, args.steps, args.warmup, world, dev, local)
 
     # end to end through the public API: pinned host inputs in, host output back,
     # every step (GraphPipeline: one graph replay per step; HostPipeline: eager)
@@ -454,67 +633,29 @@ def run_ours(args, world, rank, local):
 
     around = None if args.no_around else _time_around_layer(args, spec, d, layer, dev, stream)
 
+    peaks = _peaks()
+    others = None if args.no_also else _other_workloads(args, world, dev, stream, local, peaks)
+
     if rank != 0:
         return
-    peaks = _peaks()
     res = layer.forward(x, ids, kpt, k, P, stream=stream)
     active = int((res.expert_counts > 0).sum())
     counts = res.counts.cpu().numpy()
-    fb = _flops_bytes(spec, P, active, serial.fused_gather)
-    ffn_ms = stage_avg["grouped_ffn"]
-    ffn = fb["grouped_ffn"]
-    ffn_call = "semmoe_grouped_ffn_gather" if serial.fused_gather else "semmoe_grouped_ffn"
-    # the FFN's bound: whichever of its flops at the tensor peak and its bytes at
-    # the HBM peak takes longer (weight streaming wins for small batches)
-    t_tc = ffn["flops"] / (peaks["bf16_tflops"] * 1e12)
-    t_hbm = ffn["bytes"] / (peaks["hbm_gbs"] * 1e9)
-    tflops = ffn["flops"] / (ffn_ms * 1e-3) / 1e12
-    gbs = ffn["bytes"] / (ffn_ms * 1e-3) / 1e9
-    if t_tc >= t_hbm:
-        roofline = {
-            "kernel": ffn_call + " (GEMM1+SwiGLU, GEMM2)",
-            "bound": "tensor", "achieved": tflops, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
-            "frac": tflops / peaks["bf16_tflops"], "traffic": _traffic(ffn_call, spec.name),
-            "peak_source": f"{peaks['source']} bf16 burst (short timed region, SM clock at its maximum); "
-                           f"sustained figure {peaks['bf16_tflops_sustained']} TFLOP/s",
-            "frac_of_sustained": tflops / peaks["bf16_tflops_sustained"],
-            "frac_hbm": gbs / peaks["hbm_gbs"],
-        }
-    else:
-        roofline = {
-            "kernel": ffn_call + " (GEMM1+SwiGLU, GEMM2)",
-            "bound": "hbm", "achieved": gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
-            "frac": gbs / peaks["hbm_gbs"], "traffic": _traffic(ffn_call, spec.name),
-            "peak_source": f"{peaks['source']} HBM copy bandwidth",
-            "algorithmic_bytes": ffn["bytes"], "active_experts": active,
-            "frac_tensor": tflops / peaks["bf16_tflops"],
-        }
-    stages = {}
-    for name, avg in stage_avg.items():
-        ent = {"ms": avg}
-        f = fb.get(name, {})
-        if "flops" in f:
-            ent["tflops"] = f["flops"] / (avg * 1e-3) / 1e12
-            ent["frac_tensor"] = ent["tflops"] / peaks["bf16_tflops"]
-        if "bytes" in f:
-            ent["gbs"] = f["bytes"] / (avg * 1e-3) / 1e9
-            ent["frac_hbm"] = ent["gbs"] / peaks["hbm_gbs"]
-        stages[name] = ent
-
+    roofline, stages = _roofline_and_stages(spec, P, active, serial.fused_gather, stage_avg, peaks)
     cpu = None
     if not args.no_cpu_baseline:
         n_cpu = min(args.cpu_tokens, spec.T)
         rate, dt = cpu_oracle_rate(d, n_cpu)
-        cpu = {"value": rate, "unit": "tokens/s", "cores": _cores(), "kind": "oracle",
-               "sample": f"first {n_cpu} of {spec.T} tokens of {spec.name}, one pass "
-                         f"({dt:.1f} s, float64 numpy oracle)"}
+        cpu = _cpu_desc(rate, f"first {n_cpu} of {spec.T} tokens of {spec.name}, one pass "
+                              f"({dt:.1f} s, float64 numpy oracle)")
+        cpu["single_thread"] = _single_thread_baseline()
 
     total_tokens = spec.T * args.steps * world
     eager = {"value": total_tokens / (ms_max * 1e-3), "unit": "tokens/s", "ms_per_step": ms_max / args.steps,
              "ms_median": per_step[len(per_step) // 2], "ms_min": per_step[0], "ms_max": per_step[-1],
              "how": "MoELayer.forward per step, its steps serialised on one stream (one library call per step "
                     "of the layer; per-step events give the stages and the roofline)",
-             "clocks": clocks_eager.summary()}
+             "clocks": ev["clocks"]}
     best = graph if graph is not None and graph["ms_per_step"] < eager["ms_per_step"] else eager
     line = {
         "metric": METRIC, "value": best["value"], "unit": "tokens/s", "n_gpus": world,
@@ -525,14 +666,15 @@ def run_ours(args, world, rank, local):
         "e2e": e2e,
         "e2e_eager": e2e_eager,
         "graph": graph,
-        "gpu_launches": launches,
-        "host_enqueue_ms_per_step": host_ms,
+        "gpu_launches": ev["launches"],
+        "host_enqueue_ms_per_step": ev["host_ms"],
         "roofline": roofline,
         "stages": stages,
         "cpu_baseline": cpu,
         "clocks": best["clocks"],
         "local_activation_rate": float(np.trace(counts) / counts.sum()),
         "around_layer": around,
+        "other_workloads": others,
     }
     print(json.dumps(line), flush=True)
 
@@ -553,7 +695,15 @@ def main():
     ap.add_argument("--no-around", action="store_true",
                     help="skip timing the scheduling steps around the layer")
     ap.add_argument("--no-graph", action="store_true", help="skip the CUDA-graph replay timing")
+    ap.add_argument("--also", default="dsv2lite_prefill_T4096,prism_subexpert_T8192",
+                    help="other workloads timed in the same run (comma-separated; reported under other_workloads)")
+    ap.add_argument("--also-steps", type=int, default=10)
+    ap.add_argument("--no-also", action="store_true", help="time the --config workload only")
+    ap.add_argument("--oracle-single-thread", action="store_true", help=argparse.SUPPRESS)
     args = ap.parse_args()
+    if args.oracle_single_thread:   # child process of the CPU baseline: one BLAS thread
+        print(json.dumps(oracle_single_thread()), flush=True)
+        return
     args.warmup = max(args.warmup, 3)   # at least 3 untimed warm-up steps
     world, rank, local = _dist()
     try:

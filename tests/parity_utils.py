@@ -98,7 +98,8 @@ def check_layer_full(d, res, P):
 def check_layer_sampled(d, res, P, n_tokens=96, seed=0):
     """Full-size check: every integer output in full; the FFN, shared FFN and
     combined output on a seeded sample of tokens (each recomputed by the
-    oracle row by row from the GPU-independent routing)."""
+    oracle row by row from the GPU-independent routing), and the FFN output
+    of the last sorted row of every expert group."""
     spec = d["spec"]
     idx, w, perm = check_routing(d, res, P)
     k = d["k_per_token"].numpy()
@@ -121,6 +122,15 @@ def check_layer_sampled(d, res, P, n_tokens=96, seed=0):
         _, y = oracle.expert_ffn(xs, d["w13"][e], d["w2"][e], spec.dtype)
         ref_y[rows] = y
     assert max_rel(gpu_y, ref_y) < TOL[spec.dtype]
+    # the last sorted row of every expert group: the ragged tail of its last tile
+    off, pe, s2p = perm["expert_offsets"], perm["phys_to_expert"], perm["sorted_to_pair"]
+    tails = [(int(off[b + 1]) - 1, int(pe[b])) for b in range(pe.shape[0]) if off[b + 1] > off[b]]
+    gpu_tail = np_(res.y_perm[torch.as_tensor([q for q, _ in tails], device=res.y_perm.device)])
+    ref_tail = np.zeros_like(gpu_tail)
+    for i, (q, e) in enumerate(tails):
+        t = int(s2p[q]) // spec.k_max
+        _, ref_tail[i:i + 1] = oracle.expert_ffn(x[t:t + 1], d["w13"][e], d["w2"][e], spec.dtype)
+    assert max_rel(gpu_tail, ref_tail) < TOL[spec.dtype]
     acc = np.zeros((len(toks), spec.H))
     if d["ws13"] is not None:
         ys = oracle.shared_ffn(x[torch.as_tensor(toks)], d["ws13"], d["ws2"], spec.dtype)

@@ -87,6 +87,33 @@ def _tie_logits(rng, T, E):
     return l
 
 
+def test_router_logits_golden():
+    """Router logits against values worked by hand (tests/golden/router_logits.json):
+    integer inputs (every product and sum exact), a case where the exact sum
+    rounded once to fp32 differs from fp32 accumulation, and the fp32 storage
+    point itself.  A dropped term, a transposed weight or a sum accumulated in
+    fp32 fails one of them."""
+    with open(os.path.join(GOLDEN, "router_logits.json")) as f:
+        g = json.load(f)
+    for name in ("integer_case", "one_rounding_case", "storage_case"):
+        c = g[name]
+        got = oracle.router_logits(np.array(c["x"], dtype=np.float64), np.array(c["w_router"], dtype=np.float64))
+        want = np.array(c["logits"], dtype=np.float64)
+        assert got.shape == want.shape, name
+        assert np.array_equal(got, want), (name, got, want)
+    # the rounding case really separates the two readings
+    c = g["one_rounding_case"]
+    acc = np.float32(0)
+    for a, b in zip(c["x"][0], c["w_router"][0]):
+        acc = np.float32(acc + np.float32(a) * np.float32(b))
+    assert float(acc) == 1.0 != c["logits"][0][0]
+    # not symmetric in x and Wr: transposing the weight gives another result
+    c = g["integer_case"]
+    wt = np.array(c["w_router"], dtype=np.float64).T
+    assert not np.array_equal(oracle.router_logits(np.array(c["x"], dtype=np.float64), wt),
+                              np.array(c["logits"], dtype=np.float64))
+
+
 @pytest.mark.parametrize("E", [1, 2, 3, 8])
 def test_topk_brute_force(E):
     rng = np.random.default_rng(E)
