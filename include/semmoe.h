@@ -70,6 +70,9 @@ enum { SEMMOE_F32 = 0, SEMMOE_BF16 = 1 };
  * bf16 parts by semmoe_route_split_weight() (bf16 activations, H % 8 == 0). */
 enum { SEMMOE_F32_SPLIT = 2 };
 
+/* Tokens per chunk of the pair count table (semmoe_pair_counts_size). */
+enum { SEMMOE_PAIR_COUNT_CHUNK = 128 };
+
 /* Device error word bits reported through semmoe_check_errors(). */
 enum {
   SEMMOE_DEVERR_EXPERT = 1,      /* expert index outside [0, E) */
@@ -123,6 +126,12 @@ int semmoe_check_errors(void* stream, int* bits);
  * k_uniform  budget of every token when k_per_token is NULL (1..k_max).
  * topk_idx   [device] [T,k_max] int32 out: slot j < k_t = expert, else -1.
  * topk_w     [device] [T,k_max] fp32 out: gates, 0 in padding slots.
+ * pair_counts[device] NULL, or semmoe_pair_counts_size(T, E) bytes (16-byte
+ *            aligned) out: the count table of the picks, for semmoe_permute
+ *            (which then skips its own counting pass).  Layout [E][S] int32,
+ *            S = semmoe_pair_counts_stride(T): entry [e][c] = live pairs of
+ *            expert e among the tokens [128c, 128c + 128); entries c >= the
+ *            number of chunks are 0.  Zeroed and filled by this call.
  * ws         [device] workspace of semmoe_route_workspace_size() bytes (may be
  *            NULL when that size is 256, i.e. the CUDA-core path).
  * Limits: 1 <= k_max <= E <= 256; T >= 0 (T = 0 enqueues nothing).
@@ -137,7 +146,14 @@ int semmoe_route(const void* x, int x_dtype, const void* w_router, int w_dtype,
                  const float* logits_in, float* logits_out,
                  const int32_t* k_per_token, int k_uniform,
                  int T, int H, int E, int k_max,
-                 int32_t* topk_idx, float* topk_w, void* ws, size_t ws_bytes, void* stream);
+                 int32_t* topk_idx, float* topk_w, int32_t* pair_counts,
+                 void* ws, size_t ws_bytes, void* stream);
+
+/* Bytes and row stride (entries) of the pair count table of T tokens and E
+ * experts: E rows of semmoe_pair_counts_stride(T) int32 entries, one per
+ * 128-token chunk, rounded up to a multiple of 4. */
+size_t semmoe_pair_counts_size(int T, int E);
+int semmoe_pair_counts_stride(int T);
 
 /*
  * semmoe_route_split_weight -- the form of an fp32 router weight that the
@@ -175,14 +191,16 @@ int semmoe_route_split_weight(const float* w, int H, int E, void* split, void* s
  * sub_logw  [device] [Ep*N] fp32, finite
  * topk_idx  [device] [T,k_max] int32 out: sub-expert ids (-1 = padding)
  * topk_w    [device] [T,k_max] fp32 out (0 = padding)
+ * pair_counts [device] NULL or the count table of the picks, as semmoe_route
+ *           with E = Ep*N sub-experts
  * ws        [device] workspace of semmoe_route_hier_workspace_size() bytes
  * Limits: 1 <= N, 1 <= Ep*N <= 256, 1 <= k_max <= Ep*N.
  */
 size_t semmoe_route_hier_workspace_size(int T, int H, int Ep, int x_dtype, int w_dtype);
 int semmoe_route_hier(const void* x, int x_dtype, const void* w_parent, int w_dtype, const float* logits_in,
                       float* logits_out, const float* sub_logw, int N, const int32_t* k_per_token, int k_uniform,
-                      int T, int H, int Ep, int k_max, int32_t* topk_idx, float* topk_w, void* ws,
-                      size_t ws_bytes, void* stream);
+                      int T, int H, int Ep, int k_max, int32_t* topk_idx, float* topk_w,
+                      int32_t* pair_counts, void* ws, size_t ws_bytes, void* stream);
 
 /*
  * semmoe_affinity_lookup -- predicted logical rank of each token from its id.
@@ -239,15 +257,26 @@ int semmoe_remote_count(const int32_t* topk_idx, const int32_t* pred_rank,
  * pair_to_sorted [device] [T*k_max] int32 out: sorted row of pair p, -1 for padding
  * x_perm         [device] [P,H] dtype out (x_perm[q] = x[sorted_to_pair[q] / k_max]),
  *                or NULL when x is NULL
+ * pair_counts    [device] NULL, or the count table that semmoe_route /
+ *                semmoe_route_hier wrote for these same topk_idx: the permute
+ *                then starts from it instead of counting the pairs itself (one
+ *                kernel instead of two).  A table that does not match topk_idx
+ *                gives wrong maps (rows past P are dropped and flagged
+ *                SEMMOE_DEVERR_PAIRS, never written out of bounds).  Used while
+ *                T <= 131072 (1024 chunks); larger batches count for themselves.
  * ws, ws_bytes   [device] workspace of at least semmoe_permute_workspace_size()
  * Limits: 1 <= E <= 256, 1 <= R <= E, 1 <= k_max <= E.
+ *
+ * Kernels: each CTA takes a run of tokens, derives its first row in every
+ * bucket from the count table, ranks its own pairs stably, writes both maps
+ * and copies its tokens' rows -- one pass, no CTA waiting on another.
  */
 size_t semmoe_permute_workspace_size(int T, int k_max, int E);
 int semmoe_permute(const int32_t* topk_idx, const int32_t* expert_rank,
                    const void* x, int dtype, int T, int H, int E, int R, int k_max, int P,
                    int32_t* expert_offsets, int32_t* rank_offsets, int32_t* phys_to_expert,
                    int32_t* expert_counts, int32_t* sorted_to_pair, int32_t* pair_to_sorted,
-                   void* x_perm, void* ws, size_t ws_bytes, void* stream);
+                   void* x_perm, const int32_t* pair_counts, void* ws, size_t ws_bytes, void* stream);
 
 /*
  * semmoe_permute_noalloc -- semmoe_permute for callers that cannot allocate
@@ -257,8 +286,9 @@ int semmoe_permute(const int32_t* topk_idx, const int32_t* expert_rank,
  * allocation hook, or a latency-critical serving loop that forbids cudaMalloc
  * after start-up because it can synchronise the whole device.
  *
- * Same arguments, outputs and errors as semmoe_permute, minus the workspace:
- * the scratch (per-chunk bucket counts: at most 96 chunks * E * 4 bytes) lives
+ * Same arguments, outputs and errors as semmoe_permute, minus the workspace
+ * and the count table (it always counts for itself): the scratch (that count
+ * table: at most 96 chunks * E * 4 bytes) lives
  * in a static 96 KiB device array compiled into the library, which every GPU
  * that loads the library holds until the process exits.  That covers every
  * E <= 256; sizes beyond it (E > 256, T*k_max >= 2^31) are rejected with

@@ -50,40 +50,40 @@ def _err(lib):
 
 def test_route_validation(lib):
     # E outside [1, 256]
-    rc = lib.semmoe_route(None, 1, None, 0, None, None, None, 2, 16, 64, 0, 2, None, None, None, 0, None)
+    rc = lib.semmoe_route(None, 1, None, 0, None, None, None, 2, 16, 64, 0, 2, None, None, None, None, 0, None)
     assert rc == 1 and "E" in _err(lib)
-    rc = lib.semmoe_route(None, 1, None, 0, None, None, None, 2, 16, 64, 300, 2, None, None, None, 0, None)
+    rc = lib.semmoe_route(None, 1, None, 0, None, None, None, 2, 16, 64, 300, 2, None, None, None, None, 0, None)
     assert rc == 1
     # k_max > E
-    rc = lib.semmoe_route(None, 1, None, 0, None, None, None, 2, 16, 64, 8, 9, None, None, None, 0, None)
+    rc = lib.semmoe_route(None, 1, None, 0, None, None, None, 2, 16, 64, 8, 9, None, None, None, None, 0, None)
     assert rc == 1 and "k_max" in _err(lib)
     # k_uniform outside [1, k_max]
-    rc = lib.semmoe_route(None, 1, None, 0, None, None, None, 0, 16, 64, 8, 2, None, None, None, 0, None)
+    rc = lib.semmoe_route(None, 1, None, 0, None, None, None, 0, 16, 64, 8, 2, None, None, None, None, 0, None)
     assert rc == 1 and "k_uniform" in _err(lib)
     # null outputs
-    rc = lib.semmoe_route(None, 1, None, 0, None, None, None, 2, 16, 64, 8, 2, None, None, None, 0, None)
+    rc = lib.semmoe_route(None, 1, None, 0, None, None, None, 2, 16, 64, 8, 2, None, None, None, None, 0, None)
     assert rc == 1 and "null" in _err(lib)
     # T = 0 is a no-op
-    assert lib.semmoe_route(None, 1, None, 0, None, None, None, 2, 0, 64, 8, 2, None, None, None, 0, None) == 0
+    assert lib.semmoe_route(None, 1, None, 0, None, None, None, 2, 0, 64, 8, 2, None, None, None, None, 0, None) == 0
 
 
 def test_permute_validation(lib):
     p = ctypes.c_void_p(256)
     # P larger than T * k_max
-    rc = lib.semmoe_permute(p, p, None, 1, 4, 8, 8, 2, 2, 9, p, p, p, p, p, p, None, p, 1 << 20, None)
+    rc = lib.semmoe_permute(p, p, None, 1, 4, 8, 8, 2, 2, 9, p, p, p, p, p, p, None, None, p, 1 << 20, None)
     assert rc == 1 and "P" in _err(lib)
     # undersized workspace
-    rc = lib.semmoe_permute(p, p, None, 1, 4, 8, 8, 2, 2, 8, p, p, p, p, p, p, None, p, 4, None)
+    rc = lib.semmoe_permute(p, p, None, 1, 4, 8, 8, 2, 2, 8, p, p, p, p, p, p, None, None, p, 4, None)
     assert rc == 1 and "workspace" in _err(lib)
     # misaligned workspace
-    rc = lib.semmoe_permute(p, p, None, 1, 4, 8, 8, 2, 2, 8, p, p, p, p, p, p, None,
+    rc = lib.semmoe_permute(p, p, None, 1, 4, 8, 8, 2, 2, 8, p, p, p, p, p, p, None, None,
                             ctypes.c_void_p(260), 1 << 20, None)
     assert rc == 1
     # x without x_perm
-    rc = lib.semmoe_permute(p, p, p, 1, 4, 8, 8, 2, 2, 8, p, p, p, p, p, p, None, p, 1 << 20, None)
+    rc = lib.semmoe_permute(p, p, p, 1, 4, 8, 8, 2, 2, 8, p, p, p, p, p, p, None, None, p, 1 << 20, None)
     assert rc == 1 and "x_perm" in _err(lib)
     # R > E
-    rc = lib.semmoe_permute(p, p, None, 1, 4, 8, 4, 5, 2, 8, p, p, p, p, p, p, None, p, 1 << 20, None)
+    rc = lib.semmoe_permute(p, p, None, 1, 4, 8, 4, 5, 2, 8, p, p, p, p, p, p, None, None, p, 1 << 20, None)
     assert rc == 1
 
 
@@ -144,7 +144,7 @@ def test_router_split_validation(lib):
     rc = lib.semmoe_route_split_weight(p, 100, 8, p, None)
     assert rc == 1 and "multiple of 8" in _err(lib)
     # a pre-split weight needs bf16 activations
-    rc = lib.semmoe_route(p, 0, p, 2, None, None, None, 2, 16, 64, 8, 2, p, p, p, 1 << 20, None)
+    rc = lib.semmoe_route(p, 0, p, 2, None, None, None, 2, 16, 64, 8, 2, p, p, None, p, 1 << 20, None)
     assert rc == 1 and "dtype" in _err(lib)
 
 

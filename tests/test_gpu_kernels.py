@@ -642,3 +642,79 @@ def test_grouped_ffn_mixed_default_forms_match_single(P, E, I):
     ref = oracle.grouped_ffn(x.cpu(), eo.cpu(), p2e.cpu(), w13.cpu().to(torch.float64).numpy(),
                              w2.cpu().to(torch.float64).numpy(), "bf16")
     assert max_rel(outs[0].to(torch.float64).numpy(), ref) < TOL["bf16"]
+
+
+def _chunk_histogram(idx, k, E, stride):
+    """Expected count table: live pairs of expert e among the tokens of 128-token chunk c."""
+    T, k_max = idx.shape
+    live = np.arange(k_max)[None, :] < np.asarray(k)[:, None]
+    tok = np.broadcast_to(np.arange(T)[:, None], (T, k_max))[live]
+    cnt = np.zeros((E, stride), dtype=np.int64)
+    np.add.at(cnt, (idx[live], tok // 128), 1)
+    return cnt
+
+
+@pytest.mark.parametrize("T,E,R,k_max,per_token,H", [(1, 8, 4, 2, False, 16), (70, 3, 2, 2, True, 8),
+                                                    (300, 8, 4, 2, True, 64), (4096, 64, 8, 6, False, 128),
+                                                    (5000, 256, 8, 24, True, 16), (16384, 128, 8, 8, False, 32),
+                                                    (131200, 4, 2, 2, True, 8)])
+def test_route_pair_counts_and_counted_permute(T, E, R, k_max, per_token, H):
+    """The router's count table equals the per-chunk histogram of its picks
+    (entries past the last chunk are 0), and the permute started from it
+    returns exactly the oracle's maps and rows -- as does the permute that counts
+    the pairs itself.  T = 131200 has more than 1024 chunks, where the permute
+    ignores the table and counts for itself."""
+    a = abi()
+    rng = np.random.default_rng(T + E)
+    logits = (rng.integers(-6, 7, size=(T, E)) * 0.25).astype(np.float32)     # many exact ties
+    k = rng.integers(1, k_max + 1, size=T).astype(np.int32) if per_token else np.full(T, k_max, np.int32)
+    li = torch.from_numpy(logits).cuda()
+    idx = torch.empty(T, k_max, **i32)
+    w = torch.empty(T, k_max, dtype=torch.float32, device="cuda")
+    stride = a.semmoe_pair_counts_stride(T)
+    assert a.semmoe_pair_counts_size(T, E) == E * stride * 4 and stride % 4 == 0
+    counts = torch.full((E * stride,), -3, **i32)                               # stale contents are overwritten
+    kpt = torch.from_numpy(k).cuda() if per_token else None
+    a.semmoe_route(None, None, li, None, kpt, 0 if per_token else k_max, T, 0, E, k_max, idx, w,
+                   pair_counts=counts)
+    assert a.semmoe_check_errors() == 0
+    ref_idx, _ = oracle.topk_route(logits, k, k_max)
+    np.testing.assert_array_equal(np_(idx), ref_idx)
+    np.testing.assert_array_equal(np_(counts).reshape(E, stride), _chunk_histogram(ref_idx, k, E, stride))
+    er = rng.permutation(np.arange(E) % R).astype(np.int32)
+    P = int(k.sum())
+    x = torch.from_numpy(rng.standard_normal((T, H)).astype(np.float32)).to(torch.bfloat16).cuda()
+    ref = oracle.permute(ref_idx, k, er, R, x.cpu())
+    ws = torch.empty(a.semmoe_permute_workspace_size(T, k_max, E), dtype=torch.uint8, device="cuda")
+    for pc in (counts, None):
+        outs = dict(expert_offsets=torch.empty(E + 1, **i32), rank_offsets=torch.empty(R + 1, **i32),
+                    phys_to_expert=torch.empty(E, **i32), expert_counts=torch.empty(E, **i32),
+                    sorted_to_pair=torch.full((P,), -9, **i32), pair_to_sorted=torch.full((T * k_max,), -9, **i32),
+                    x_perm=torch.zeros(P, H, dtype=torch.bfloat16, device="cuda"))
+        a.semmoe_permute(idx, torch.from_numpy(er).cuda(), x, T, H, E, R, k_max, P, outs["expert_offsets"],
+                         outs["rank_offsets"], outs["phys_to_expert"], outs["expert_counts"], outs["sorted_to_pair"],
+                         outs["pair_to_sorted"], outs["x_perm"], ws, pair_counts=pc)
+        assert a.semmoe_check_errors() == 0
+        for key, v in ref.items():
+            np.testing.assert_array_equal(np_(outs[key]), v, err_msg=f"{key} (counts {'given' if pc is not None else 'own'})")
+
+
+def test_hier_route_pair_counts():
+    """The hierarchical router counts its sub-expert picks the same way."""
+    a = abi()
+    rng = np.random.default_rng(77)
+    T, Ep, N, k_max = 1000, 16, 4, 12
+    l = rng.standard_normal((T, Ep)).astype(np.float32)
+    logw = np.log(rng.dirichlet(np.full(N, 2.0), size=Ep)).astype(np.float32).ravel()
+    k = rng.integers(1, k_max + 1, size=T).astype(np.int32)
+    E = Ep * N
+    idx = torch.empty(T, k_max, **i32)
+    w = torch.empty(T, k_max, dtype=torch.float32, device="cuda")
+    stride = a.semmoe_pair_counts_stride(T)
+    counts = torch.full((E * stride,), 5, **i32)
+    a.semmoe_route_hier(None, None, torch.from_numpy(l).cuda(), None, torch.from_numpy(logw).cuda(), N,
+                        torch.from_numpy(k).cuda(), 0, T, 0, Ep, k_max, idx, w, pair_counts=counts)
+    assert a.semmoe_check_errors() == 0
+    ref_idx, _ = oracle.hier_route(l, logw, N, k, k_max)
+    np.testing.assert_array_equal(np_(idx), ref_idx)
+    np.testing.assert_array_equal(np_(counts).reshape(E, stride), _chunk_histogram(ref_idx, k, E, stride))

@@ -38,17 +38,19 @@ SIGNATURES = {
     "semmoe_kernel_launches": (ctypes.c_ulonglong, []),
     "semmoe_check_errors": (_i, [_vp, ctypes.POINTER(_i)]),
     "semmoe_route_workspace_size": (_sz, [_i, _i, _i, _i, _i]),
-    "semmoe_route": (_i, [_vp, _i, _vp, _i, _vp, _vp, _vp, _i, _i, _i, _i, _i, _vp, _vp, _vp, _sz, _vp]),
+    "semmoe_route": (_i, [_vp, _i, _vp, _i, _vp, _vp, _vp, _i, _i, _i, _i, _i, _vp, _vp, _vp, _vp, _sz, _vp]),
+    "semmoe_pair_counts_size": (_sz, [_i, _i]),
+    "semmoe_pair_counts_stride": (_i, [_i]),
     "semmoe_route_split_size": (_sz, [_i, _i]),
     "semmoe_route_split_weight": (_i, [_vp, _i, _i, _vp, _vp]),
     "semmoe_route_hier_workspace_size": (_sz, [_i, _i, _i, _i, _i]),
-    "semmoe_route_hier": (_i, [_vp, _i, _vp, _i, _vp, _vp, _vp, _i, _vp, _i, _i, _i, _i, _i, _vp, _vp, _vp, _sz,
-                               _vp]),
+    "semmoe_route_hier": (_i, [_vp, _i, _vp, _i, _vp, _vp, _vp, _i, _vp, _i, _i, _i, _i, _i, _vp, _vp, _vp, _vp,
+                               _sz, _vp]),
     "semmoe_affinity_lookup": (_i, [_vp, _vp, _i, _i, _i, _vp, _vp]),
     "semmoe_remote_count": (_i, [_vp, _vp, _vp, _i, _i, _i, _i, _vp, _vp, _vp]),
     "semmoe_permute_workspace_size": (_sz, [_i, _i, _i]),
     "semmoe_permute": (_i, [_vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _i, _vp, _vp, _vp, _vp, _vp, _vp,
-                            _vp, _vp, _sz, _vp]),
+                            _vp, _vp, _vp, _sz, _vp]),
     "semmoe_permute_noalloc": (_i, [_vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _i, _vp, _vp, _vp, _vp, _vp,
                                     _vp, _vp, _vp]),
     "semmoe_grouped_ffn_workspace_size": (_sz, [_i, _i, _i]),
@@ -149,11 +151,21 @@ def semmoe_route_workspace_size(T, H, E, x_dtype: int, w_dtype: int) -> int:
     return lib().semmoe_route_workspace_size(T, H, E, x_dtype, w_dtype)
 
 
+def semmoe_pair_counts_size(T, E) -> int:
+    return lib().semmoe_pair_counts_size(T, E)
+
+
+def semmoe_pair_counts_stride(T) -> int:
+    return lib().semmoe_pair_counts_stride(T)
+
+
 def semmoe_route(x, w_router, logits_in, logits_out, k_per_token, k_uniform, T, H, E, k_max,
-                 topk_idx, topk_w, ws=None, stream=None, w_dtype=None):
+                 topk_idx, topk_w, ws=None, stream=None, w_dtype=None, pair_counts=None):
     """Router GEMM + top-k.  ``ws`` defaults to a fresh workspace of the size
     the library asks for (pass one to avoid the allocation); ``w_dtype`` =
-    SEMMOE_F32_SPLIT when w_router holds the output of semmoe_route_split_weight."""
+    SEMMOE_F32_SPLIT when w_router holds the output of semmoe_route_split_weight;
+    ``pair_counts`` (semmoe_pair_counts_size bytes) receives the count table of
+    the picks for semmoe_permute."""
     xd = dtype_code(x) if x is not None else SEMMOE_F32
     wd = w_dtype if w_dtype is not None else (dtype_code(w_router) if w_router is not None else SEMMOE_F32)
     if ws is None:
@@ -161,7 +173,7 @@ def semmoe_route(x, w_router, logits_in, logits_out, k_per_token, k_uniform, T, 
         ws = torch.empty(n, dtype=torch.uint8, device=topk_idx.device)
     _check(lib().semmoe_route(_p(x), xd, _p(w_router), wd, _p(logits_in), _p(logits_out),
                               _p(k_per_token), k_uniform, T, H, E, k_max, _p(topk_idx), _p(topk_w),
-                              _p(ws), ws.numel() * ws.element_size(), _stream(stream)))
+                              _p(pair_counts), _p(ws), ws.numel() * ws.element_size(), _stream(stream)))
 
 
 def semmoe_route_split_size(H, E) -> int:
@@ -177,9 +189,10 @@ def semmoe_route_hier_workspace_size(T, H, Ep, x_dtype: int, w_dtype: int) -> in
 
 
 def semmoe_route_hier(x, w_parent, logits_in, logits_out, sub_logw, N, k_per_token, k_uniform, T, H, Ep, k_max,
-                      topk_idx, topk_w, ws=None, stream=None, w_dtype=None):
+                      topk_idx, topk_w, ws=None, stream=None, w_dtype=None, pair_counts=None):
     """Hierarchical sub-expert routing.  ``ws`` defaults to a fresh workspace
-    of the size the library asks for; ``w_dtype`` as in semmoe_route."""
+    of the size the library asks for; ``w_dtype`` and ``pair_counts`` as in
+    semmoe_route."""
     xd = dtype_code(x) if x is not None else SEMMOE_F32
     wd = w_dtype if w_dtype is not None else (dtype_code(w_parent) if w_parent is not None else SEMMOE_F32)
     if ws is None:
@@ -187,7 +200,7 @@ def semmoe_route_hier(x, w_parent, logits_in, logits_out, sub_logw, N, k_per_tok
         ws = torch.empty(n, dtype=torch.uint8, device=topk_idx.device)
     _check(lib().semmoe_route_hier(_p(x), xd, _p(w_parent), wd, _p(logits_in), _p(logits_out), _p(sub_logw), N,
                                    _p(k_per_token), k_uniform, T, H, Ep, k_max, _p(topk_idx), _p(topk_w),
-                                   _p(ws), ws.numel() * ws.element_size(), _stream(stream)))
+                                   _p(pair_counts), _p(ws), ws.numel() * ws.element_size(), _stream(stream)))
 
 
 def semmoe_affinity_lookup(token_ids, lut, V, R, T, pred_rank, stream=None):
@@ -205,12 +218,14 @@ def semmoe_permute_workspace_size(T, k_max, E) -> int:
 
 def semmoe_permute(topk_idx, expert_rank, x, T, H, E, R, k_max, P, expert_offsets, rank_offsets,
                    phys_to_expert, expert_counts, sorted_to_pair, pair_to_sorted, x_perm, ws,
-                   stream=None):
+                   stream=None, pair_counts=None):
+    """``pair_counts``: the router's count table for these topk_idx, or None
+    (the permute then counts the pairs itself)."""
     d = dtype_code(x) if x is not None else SEMMOE_F32
     _check(lib().semmoe_permute(_p(topk_idx), _p(expert_rank), _p(x), d, T, H, E, R, k_max, P,
                                 _p(expert_offsets), _p(rank_offsets), _p(phys_to_expert),
                                 _p(expert_counts), _p(sorted_to_pair), _p(pair_to_sorted), _p(x_perm),
-                                _p(ws), ws.numel() * ws.element_size(), _stream(stream)))
+                                _p(pair_counts), _p(ws), ws.numel() * ws.element_size(), _stream(stream)))
 
 
 def semmoe_permute_noalloc(topk_idx, expert_rank, x, T, H, E, R, k_max, P, expert_offsets, rank_offsets,

@@ -96,9 +96,16 @@ size_t semmoe_route_workspace_size(int T, int H, int E, int x_dtype, int w_dtype
   return b > 0 ? b : 256;
 }
 
+size_t semmoe_pair_counts_size(int T, int E) {
+  if (T < 0 || E < 1) return 0;
+  return pair_counts_bytes(T, E);
+}
+
+int semmoe_pair_counts_stride(int T) { return T < 0 ? 0 : pair_counts_stride(T); }
+
 int semmoe_route(const void* x, int x_dtype, const void* w_router, int w_dtype, const float* logits_in,
                  float* logits_out, const int32_t* k_per_token, int k_uniform, int T, int H, int E, int k_max,
-                 int32_t* topk_idx, float* topk_w, void* ws, size_t ws_bytes, void* stream) {
+                 int32_t* topk_idx, float* topk_w, int32_t* pair_counts, void* ws, size_t ws_bytes, void* stream) {
   REQUIRE(T >= 0, "semmoe_route: T = %d < 0", T);
   REQUIRE(E >= 1 && E <= 256, "semmoe_route: E = %d outside [1, 256]", E);
   REQUIRE(k_max >= 1 && k_max <= E, "semmoe_route: k_max = %d outside [1, E = %d]", k_max, E);
@@ -119,11 +126,12 @@ int semmoe_route(const void* x, int x_dtype, const void* w_router, int w_dtype, 
   } else {
     REQUIRE(aligned(logits_in, 4), "semmoe_route: misaligned logits_in");
   }
-  REQUIRE(aligned(topk_idx, 4) && aligned(topk_w, 4) && aligned(logits_out, 4) && aligned(k_per_token, 4),
+  REQUIRE(aligned(topk_idx, 4) && aligned(topk_w, 4) && aligned(logits_out, 4) && aligned(k_per_token, 4) &&
+              aligned(pair_counts, 16),
           "semmoe_route: misaligned output or k_per_token");
   CHECK_DEVICE("semmoe_route");
   return cuda_status(launch_route(x, x_dtype, w_router, w_dtype, logits_in, logits_out, k_per_token, k_uniform, T,
-                                  H, E, k_max, topk_idx, topk_w, ws, static_cast<cudaStream_t>(stream)),
+                                  H, E, k_max, topk_idx, topk_w, pair_counts, ws, static_cast<cudaStream_t>(stream)),
                      "semmoe_route");
 }
 
@@ -150,8 +158,8 @@ size_t semmoe_route_hier_workspace_size(int T, int H, int Ep, int x_dtype, int w
 
 int semmoe_route_hier(const void* x, int x_dtype, const void* w_parent, int w_dtype, const float* logits_in,
                       float* logits_out, const float* sub_logw, int N, const int32_t* k_per_token, int k_uniform,
-                      int T, int H, int Ep, int k_max, int32_t* topk_idx, float* topk_w, void* ws, size_t ws_bytes,
-                      void* stream) {
+                      int T, int H, int Ep, int k_max, int32_t* topk_idx, float* topk_w, int32_t* pair_counts,
+                      void* ws, size_t ws_bytes, void* stream) {
   REQUIRE(T >= 0, "semmoe_route_hier: T = %d < 0", T);
   REQUIRE(N >= 1 && Ep >= 1 && (long long)Ep * N <= 256, "semmoe_route_hier: Ep * N = %lld outside [1, 256]",
           (long long)Ep * N);
@@ -175,11 +183,11 @@ int semmoe_route_hier(const void* x, int x_dtype, const void* w_parent, int w_dt
     REQUIRE(aligned(logits_in, 4), "semmoe_route_hier: misaligned logits_in");
   }
   REQUIRE(aligned(topk_idx, 4) && aligned(topk_w, 4) && aligned(logits_out, 4) && aligned(k_per_token, 4) &&
-              aligned(sub_logw, 4),
+              aligned(sub_logw, 4) && aligned(pair_counts, 16),
           "semmoe_route_hier: misaligned pointer");
   CHECK_DEVICE("semmoe_route_hier");
   return cuda_status(launch_route_hier(x, x_dtype, w_parent, w_dtype, logits_in, logits_out, sub_logw, N,
-                                       k_per_token, k_uniform, T, H, Ep, k_max, topk_idx, topk_w, ws,
+                                       k_per_token, k_uniform, T, H, Ep, k_max, topk_idx, topk_w, pair_counts, ws,
                                        static_cast<cudaStream_t>(stream)),
                      "semmoe_route_hier");
 }
@@ -217,7 +225,8 @@ size_t semmoe_permute_workspace_size(int T, int k_max, int E) {
 int semmoe_permute(const int32_t* topk_idx, const int32_t* expert_rank, const void* x, int dtype, int T, int H,
                    int E, int R, int k_max, int P, int32_t* expert_offsets, int32_t* rank_offsets,
                    int32_t* phys_to_expert, int32_t* expert_counts, int32_t* sorted_to_pair,
-                   int32_t* pair_to_sorted, void* x_perm, void* ws, size_t ws_bytes, void* stream) {
+                   int32_t* pair_to_sorted, void* x_perm, const int32_t* pair_counts, void* ws, size_t ws_bytes,
+                   void* stream) {
   REQUIRE(T >= 0, "semmoe_permute: T = %d < 0", T);
   REQUIRE(E >= 1 && E <= 256, "semmoe_permute: E = %d outside [1, 256]", E);
   REQUIRE(R >= 1 && R <= E, "semmoe_permute: R = %d outside [1, E]", R);
@@ -237,10 +246,11 @@ int semmoe_permute(const int32_t* topk_idx, const int32_t* expert_rank, const vo
   REQUIRE(ws != nullptr && aligned(ws, 256), "semmoe_permute: workspace null or not 256-byte aligned");
   REQUIRE(ws_bytes >= permute_ws_bytes(T, k_max, E), "semmoe_permute: workspace %zu < %zu bytes", ws_bytes,
           permute_ws_bytes(T, k_max, E));
+  REQUIRE(aligned(pair_counts, 16), "semmoe_permute: pair_counts not 16-byte aligned");
   CHECK_DEVICE("semmoe_permute");
   return cuda_status(launch_permute(topk_idx, expert_rank, x, dtype, T, H, E, R, k_max, P, expert_offsets,
                                     rank_offsets, phys_to_expert, expert_counts, sorted_to_pair, pair_to_sorted,
-                                    x_perm, ws, static_cast<cudaStream_t>(stream)),
+                                    x_perm, pair_counts, ws, static_cast<cudaStream_t>(stream)),
                      "semmoe_permute");
 }
 

@@ -30,17 +30,19 @@ cudaError_t launch_route_split(const float* w, int H, int E, void* split, cudaSt
 int route_tc_k_slices(int T, int H, int E, int w_dtype);
 cudaError_t launch_route_logits_tc(const void* x, const void* w, int w_dtype, int T, int H, int E, float* partials,
                                    int ks, void* split, cudaStream_t s);
+// pair_counts (nullable): zeroed here, then the live picks are counted into it
+// (layout of pair_counts_bytes).
 cudaError_t launch_route(const void* x, int x_dtype, const void* w, int w_dtype,
                          const float* logits_in, float* logits_out, const int32_t* k_per_token,
                          int k_uniform, int T, int H, int E, int k_max, int32_t* topk_idx,
-                         float* topk_w, void* ws, cudaStream_t s);
+                         float* topk_w, int32_t* pair_counts, void* ws, cudaStream_t s);
 
 // MoE-Prism hierarchical gating over Ep parents x N sub-experts.
 size_t route_hier_ws_bytes(int T, int H, int Ep, int x_dtype, int w_dtype);
 cudaError_t launch_route_hier(const void* x, int x_dtype, const void* w, int w_dtype, const float* logits_in,
                               float* logits_out, const float* sub_logw, int N, const int32_t* kpt, int k_uniform,
-                              int T, int H, int Ep, int k_max, int32_t* topk_idx, float* topk_w, void* ws,
-                              cudaStream_t s);
+                              int T, int H, int Ep, int k_max, int32_t* topk_idx, float* topk_w,
+                              int32_t* pair_counts, void* ws, cudaStream_t s);
 
 cudaError_t launch_affinity_lookup(const int32_t* token_ids, const int32_t* lut, int V, int R,
                                    int T, int32_t* pred, cudaStream_t s);
@@ -50,12 +52,16 @@ cudaError_t launch_remote_count(const int32_t* topk_idx, const int32_t* pred,
                                 int32_t* counts, int32_t* remote, cudaStream_t s);
 
 size_t permute_ws_bytes(int T, int k_max, int E);
+// The pair count table [E][pair_counts_stride(T)] of 128-token chunks
+// (SEMMOE_PAIR_COUNT_CHUNK) that the router can write for the permute.
+size_t pair_counts_bytes(int T, int E);
+int pair_counts_stride(int T);
 cudaError_t launch_permute(const int32_t* topk_idx, const int32_t* expert_rank, const void* x,
                            int dtype, int T, int H, int E, int R, int k_max, int P,
                            int32_t* expert_offsets, int32_t* rank_offsets,
                            int32_t* phys_to_expert, int32_t* expert_counts,
                            int32_t* sorted_to_pair, int32_t* pair_to_sorted, void* x_perm,
-                           void* ws, cudaStream_t s);
+                           const int32_t* pair_counts, void* ws, cudaStream_t s);
 
 // semmoe_permute with its scratch in a static device array (no allocation).
 size_t permute_noalloc_max_scratch();

@@ -4,14 +4,14 @@
 // (de) §2 B, (ja) §2.2 B).  The rank-major expert order is the physical
 // layout that (ja) §2.2 A obtains by shuffling the gate matrix's columns.
 //
-// Two passes over the pair ids, neither waiting on another CTA:
-//   1. perm_hist:    each CTA counts its chunk of pairs per physical bucket
-//   2. perm_scatter: each CTA scans the [chunk][bucket] counts for its own
-//                    starting positions, ranks its pairs stably within the
-//                    chunk (warp match + per-warp bucket counts) and writes
-//                    both maps; CTA 0 writes the bucket and rank tables
-// then perm_copy writes each x row to its tokens' sorted rows (one warp per
-// token, 16-byte vectors).
+// The sort starts from a count table, counts[e][c] = live pairs of expert e
+// among the tokens of chunk c: the router writes it as it picks the experts
+// (128-token chunks, semmoe_route's pair_counts), or, when the caller has none,
+// perm_count_kernel makes it (one CTA per chunk).  perm_rank_copy_kernel then
+// does the rest in one pass: each CTA derives its first row in every bucket
+// from the table, ranks its own tokens' pairs stably (warp match + per-warp
+// bucket counts), writes both maps, and copies its tokens' x rows to their
+// sorted rows (one warp per token, 16-byte vectors).
 #include <cuda.h>
 
 #include <mutex>
@@ -19,11 +19,11 @@
 #include "common.cuh"
 #include "internal.h"
 
-// Scratch of semmoe_permute_noalloc: the per-chunk bucket counts live in this
-// file-scope device array instead of a caller workspace.  Every GPU that loads
-// the library holds it until the process exits.
-// The permute splits the pairs into at most 96 chunks, so it needs at most
-// 96 * E * 4 bytes of scratch: 96 KiB covers every E up to the 256 it accepts.
+// Scratch of semmoe_permute_noalloc: the count table lives in this file-scope
+// device array instead of a caller workspace.  Every GPU that loads the library
+// holds it until the process exits.  The table the permute makes itself has at
+// most 96 chunks, so it needs at most 96 * E * 4 bytes of scratch: 96 KiB
+// covers every E up to the 256 it accepts.
 static constexpr size_t kNoAllocScratchBytes = 96u * 256u * 4u;  // 96 KiB
 static __device__ __align__(256) int32_t g_noalloc_scratch[kNoAllocScratchBytes / sizeof(int32_t)];
 
@@ -33,22 +33,24 @@ namespace {
 __device__ int g_err;
 __device__ __forceinline__ void flag(int bit) { atomicOr(&g_err, bit); }
 
-constexpr int kThreads = 256;
-constexpr int kWarps = kThreads / 32;
 constexpr int kMaxE = 256;
-constexpr int kTargetChunks = 96;  // enough CTAs to cover the GPU, few enough to scan cheaply
-constexpr int kPre = 8;            // pair ids loaded ahead per thread (rounds of a chunk)
-static_assert(kTargetChunks * kMaxE * 4 <= kNoAllocScratchBytes, "no-alloc scratch too small");
+constexpr int kHistThreads = 256;
+constexpr int kThreads = 512;               // the ranking + copy kernel
+constexpr int kWarps = kThreads / 32;
+constexpr int kPre = 8;                     // loads in flight per thread in the counting loops
+constexpr int kMaxInternalChunks = 96;      // chunks of the count table the permute makes itself
+static_assert(kMaxInternalChunks * kMaxE * 4 <= kNoAllocScratchBytes, "no-alloc scratch too small");
 
-// Pairs per CTA: a multiple of kThreads (one "round" each) giving about
-// kTargetChunks chunks.
-inline int rounds_per_chunk(long long n_pairs) {
-  const long long r = (n_pairs + (long long)kTargetChunks * kThreads - 1) / ((long long)kTargetChunks * kThreads);
-  return r < 1 ? 1 : (int)r;
-}
-inline int n_chunks(long long n_pairs) {
-  const long long chunk = (long long)rounds_per_chunk(n_pairs) * kThreads;
-  return (int)((n_pairs + chunk - 1) / chunk);
+// Row stride of a [E][chunks] count table: chunks rounded up to a multiple of 4,
+// so that each expert's row starts 16-byte aligned.
+inline int padded_chunks(int nc) { return (nc + 3) / 4 * 4; }
+
+// Tokens per chunk of the count table the permute makes itself (when the caller
+// passes none): SEMMOE_PAIR_COUNT_CHUNK, or more so that there are at most 96
+// chunks (the table then fits the no-alloc scratch for every E <= 256).
+inline int internal_chunk_tokens(int T) {
+  const int c = (T + kMaxInternalChunks - 1) / kMaxInternalChunks;
+  return c > SEMMOE_PAIR_COUNT_CHUNK ? c : SEMMOE_PAIR_COUNT_CHUNK;
 }
 
 // phys_s[e] = position of expert e in the (expert_rank[e], e) order.
@@ -75,96 +77,181 @@ __device__ void physical_positions(const int32_t* __restrict__ expert_rank, int 
   __syncthreads();
 }
 
-__global__ void __launch_bounds__(kThreads)
-perm_hist_kernel(const int32_t* __restrict__ topk_idx, const int32_t* __restrict__ expert_rank,
-                 long long n_pairs, int rounds, int E, int R, int32_t* __restrict__ hist) {
-  __shared__ int rank_s[kMaxE], phys_s[kMaxE], h[kMaxE];
-  physical_positions(expert_rank, E, R, rank_s, phys_s);
-  for (int b = threadIdx.x; b < E; b += kThreads) h[b] = 0;
+// Count table of the pairs: counts[e * ncp + c] = live pairs of expert e among
+// the tokens [c * chunk, (c + 1) * chunk).  One CTA per chunk; every entry of its
+// column is written (no zeroing needed).
+__global__ void __launch_bounds__(kHistThreads)
+perm_count_kernel(const int32_t* __restrict__ topk_idx, int T, int k_max, int E, int chunk, int ncp,
+                  int32_t* __restrict__ counts) {
+  __shared__ int h[kMaxE];
+  for (int e = threadIdx.x; e < E; e += kHistThreads) h[e] = 0;
   __syncthreads();
-  const int chunk = rounds * kThreads;
-  const long long base = (long long)blockIdx.x * chunk;
-  for (int i0 = 0; i0 < chunk; i0 += kPre * kThreads) {  // kPre loads in flight per thread
+  const long long p0 = (long long)blockIdx.x * chunk * k_max;
+  const long long p1 = min((long long)T, (long long)(blockIdx.x + 1) * chunk) * k_max;
+  for (long long i0 = p0; i0 < p1; i0 += (long long)kPre * kHistThreads) {
     int ev[kPre];
 #pragma unroll
     for (int u = 0; u < kPre; ++u) {
-      const int i = i0 + u * kThreads + threadIdx.x;
-      ev[u] = (i < chunk && base + i < n_pairs) ? topk_idx[base + i] : -1;
+      const long long i = i0 + (long long)u * kHistThreads + threadIdx.x;
+      ev[u] = i < p1 ? topk_idx[i] : -1;
     }
 #pragma unroll
     for (int u = 0; u < kPre; ++u) {
       const int e = ev[u];
       if (e < 0) continue;
       if (e >= E) { flag(SEMMOE_DEVERR_EXPERT); continue; }
-      atomicAdd(&h[phys_s[e]], 1);
+      atomicAdd(&h[e], 1);
     }
   }
   __syncthreads();
-  for (int b = threadIdx.x; b < E; b += kThreads) hist[(size_t)blockIdx.x * E + b] = h[b];
+  for (int e = threadIdx.x; e < E; e += kHistThreads) counts[(size_t)e * ncp + blockIdx.x] = h[e];
 }
 
-// Each CTA ranks the pairs of its chunk.  Its starting position in every bucket
-// is derived from the per-chunk histograms of pass 1: it sums, per bucket, the
-// counts of all chunks (totals) and of the chunks before its own, and scans the
-// totals over buckets.  CTA 0 also writes the bucket / rank tables.  Nothing
-// waits on another CTA: every CTA recomputes the (small) scan for itself.
-__global__ void __launch_bounds__(kThreads)
-perm_scatter_kernel(const int32_t* __restrict__ topk_idx, const int32_t* __restrict__ expert_rank,
-                    long long n_pairs, int rounds, int nchunks, int E, int R, int P,
-                    const int32_t* __restrict__ hist,
-                    int32_t* __restrict__ expert_offsets, int32_t* __restrict__ rank_offsets,
-                    int32_t* __restrict__ phys_to_expert, int32_t* __restrict__ expert_counts,
-                    int32_t* __restrict__ sorted_to_pair, int32_t* __restrict__ pair_to_sorted) {
-  __shared__ int rank_s[kMaxE], phys_s[kMaxE], run[kMaxE], total[kMaxE], scan[kThreads];
-  __shared__ int wcnt[kWarps][kMaxE];
-  __shared__ int part_before[kThreads], part_tot[kThreads];
-  physical_positions(expert_rank, E, R, rank_s, phys_s);
-  const int tid = threadIdx.x;
-  // G threads per bucket (G = kThreads / E) each sum every G-th chunk's count,
-  // eight loads in flight at a time; the G partial sums are added below.
-  const int G = kThreads / E;
-  if (tid < G * E) {
-    const int b = tid % E, g = tid / E;
-    int before = 0, tot = 0;
-    constexpr int B = 8;
-    for (int c0 = g; c0 < nchunks; c0 += B * G) {
-      int v[B];
+// One warp writes token t's activation row x[t] to its live slots' sorted rows
+// pair_to_sorted[t * k_max + j]: the row is read once, in segments of up to
+// 4 KB held in registers, and each segment is written to the k_t rows.
+// (Walking the sorted rows instead re-reads each x row k_t times, far apart in
+// time, and the row writes push those reads out of L2.)
+constexpr int kSegVec = 8;  // 16-byte vectors per lane per segment: 32 x 8 x 16 B = 4 KB
+
+__device__ __forceinline__ void copy_token_row(const unsigned char* __restrict__ x, const int32_t* slots, int t,
+                                               int k_max, int P, int row_bytes, unsigned char* __restrict__ x_perm) {
+  const int lane = threadIdx.x % 32;
+  const int n16 = row_bytes / 16;
+  const int kk = k_max < 32 ? k_max : 32;
+  int q_l = -1;
+  if (lane < kk) {
+    q_l = slots[lane];
+    if (q_l >= P) { flag(SEMMOE_DEVERR_PAIRS); q_l = -1; }
+  }
+  const uint4* src = reinterpret_cast<const uint4*>(x + (size_t)t * row_bytes);
+  for (int seg = 0; seg < n16; seg += 32 * kSegVec) {
+    uint4 v[kSegVec];
 #pragma unroll
-      for (int u = 0; u < B; ++u) {
-        const int c = c0 + u * G;
-        v[u] = c < nchunks ? hist[(size_t)c * E + b] : 0;
-      }
+    for (int u = 0; u < kSegVec; ++u) {
+      const int c = seg + u * 32 + lane;
+      if (c < n16) v[u] = src[c];
+    }
+    for (int j = 0; j < kk; ++j) {
+      const int q = __shfl_sync(0xffffffffu, q_l, j);
+      if (q < 0) continue;
+      uint4* dst = reinterpret_cast<uint4*>(x_perm + (size_t)q * row_bytes);
 #pragma unroll
-      for (int u = 0; u < B; ++u) {
-        before += c0 + u * G < (int)blockIdx.x ? v[u] : 0;
-        tot += v[u];
+      for (int u = 0; u < kSegVec; ++u) {
+        const int c = seg + u * 32 + lane;
+        if (c < n16) dst[c] = v[u];
       }
     }
-    part_before[tid] = before;
+    for (int j = 32; j < k_max; ++j) {  // budgets above 32 experts: read the slot directly
+      const int q = slots[j];
+      if (q < 0) continue;
+      if (q >= P) { if (lane == 0) flag(SEMMOE_DEVERR_PAIRS); continue; }
+      uint4* dst = reinterpret_cast<uint4*>(x_perm + (size_t)q * row_bytes);
+#pragma unroll
+      for (int u = 0; u < kSegVec; ++u) {
+        const int c = seg + u * 32 + lane;
+        if (c < n16) dst[c] = v[u];
+      }
+    }
+  }
+}
+
+// The stable counting sort and the row gather in one pass.  CTA b takes the
+// tokens [t0, t1) = [b * tpc, (b + 1) * tpc) and
+//  1. derives, per expert, the rows of all tokens (totals) and of the tokens
+//     before t0 from the count table: whole chunks before t0's chunk from the
+//     table, the part of t0's own chunk before t0 by counting those pairs;
+//  2. scans the totals in physical order (bucket starts; CTA 0 writes the
+//     bucket and rank tables), so its first row in bucket b is
+//     start[b] + (rows of b before t0);
+//  3. ranks its own pairs in pair order, a round of kThreads pairs at a time
+//     (warp match + per-warp bucket counts), and writes both maps;
+//  4. copies each of its tokens' x rows to the token's sorted rows.
+// No CTA waits on another: each recomputes the (small) prefix for itself.
+__global__ void __launch_bounds__(kThreads)
+perm_rank_copy_kernel(const int32_t* __restrict__ topk_idx, const int32_t* __restrict__ expert_rank,
+                      const int32_t* __restrict__ counts, int nc, int ncp, int chunk, int T, int k_max, int E, int R,
+                      int P, int tpc, int32_t* __restrict__ expert_offsets, int32_t* __restrict__ rank_offsets,
+                      int32_t* __restrict__ phys_to_expert, int32_t* __restrict__ expert_counts,
+                      int32_t* __restrict__ sorted_to_pair, int32_t* pair_to_sorted,
+                      const unsigned char* __restrict__ x, int row_bytes, unsigned char* __restrict__ x_perm) {
+  __shared__ int rank_s[kMaxE], phys_s[kMaxE], run[kMaxE], total[kMaxE], sub[kMaxE], bef_s[kMaxE], scan[kMaxE];
+  __shared__ int part_tot[kThreads], part_bef[kThreads];
+  __shared__ int wcnt[kWarps][kMaxE];
+  const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
+  const int t0 = min(T, (int)blockIdx.x * tpc), t1 = min(T, t0 + tpc);
+  const int c0 = t0 / chunk;  // the chunk holding t0
+  for (int i = tid; i < E; i += kThreads) sub[i] = 0;
+  for (int i = tid; i < kWarps * kMaxE; i += kThreads) (&wcnt[0][0])[i] = 0;
+  physical_positions(expert_rank, E, R, rank_s, phys_s);
+
+  // 1a. G threads per expert each sum a strided part of its row of the table
+  //     (16-byte loads; rows are ncp >= nc entries, zero-padded or unread past nc)
+  const int G = kThreads / E;  // >= 2 (E <= 256)
+  if (tid < G * E) {
+    const int e = tid % E, g = tid / E;
+    const int4* row = reinterpret_cast<const int4*>(counts + (size_t)e * ncp);
+    int tot = 0, bef = 0;
+    for (int v0 = g; v0 * 4 < nc; v0 += kPre * G) {
+      int4 v[kPre];
+#pragma unroll
+      for (int u = 0; u < kPre; ++u) {
+        const int vi = v0 + u * G;
+        v[u] = vi * 4 < nc ? row[vi] : make_int4(0, 0, 0, 0);
+      }
+#pragma unroll
+      for (int u = 0; u < kPre; ++u) {
+        const int c = (v0 + u * G) * 4;
+        const int a[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          if (c + i < nc) {
+            tot += a[i];
+            if (c + i < c0) bef += a[i];
+          }
+        }
+      }
+    }
     part_tot[tid] = tot;
+    part_bef[tid] = bef;
+  }
+  // 1b. pairs of t0's chunk before t0
+  {
+    const long long p0 = (long long)c0 * chunk * k_max, p1 = (long long)t0 * k_max;
+    for (long long i0 = p0; i0 < p1; i0 += (long long)kPre * kThreads) {
+      int ev[kPre];
+#pragma unroll
+      for (int u = 0; u < kPre; ++u) {
+        const long long i = i0 + (long long)u * kThreads + tid;
+        ev[u] = i < p1 ? topk_idx[i] : -1;
+      }
+#pragma unroll
+      for (int u = 0; u < kPre; ++u)
+        if (ev[u] >= 0 && ev[u] < E) atomicAdd(&sub[ev[u]], 1);
+    }
   }
   __syncthreads();
   if (tid < E) {
-    int before = 0, tot = 0;
+    int tot = 0, bef = 0;
     for (int g = 0; g < G; ++g) {
-      before += part_before[g * E + tid];
       tot += part_tot[g * E + tid];
+      bef += part_bef[g * E + tid];
     }
-    total[tid] = tot;
-    run[tid] = before;
-    for (int w = 0; w < kWarps; ++w) wcnt[w][tid] = 0;
+    total[phys_s[tid]] = tot;               // indexed by physical bucket from here on
+    bef_s[tid] = bef + sub[tid];            // rows of expert tid before t0
   }
   __syncthreads();
-  scan[tid] = tid < E ? total[tid] : 0;
+  // 2. inclusive scan of the bucket totals (Hillis-Steele over E <= 256 entries)
+  if (tid < E) scan[tid] = total[tid];
   __syncthreads();
-  for (int d = 1; d < kThreads; d <<= 1) {  // inclusive scan of the bucket totals
-    const int v = tid >= d ? scan[tid - d] : 0;
+  for (int d = 1; d < E; d <<= 1) {
+    const int v = (tid < E && tid >= d) ? scan[tid - d] : 0;
     __syncthreads();
-    scan[tid] += v;
+    if (tid < E) scan[tid] += v;
     __syncthreads();
   }
-  const int sum = scan[kThreads - 1];
-  if (tid < E) run[tid] += scan[tid] - total[tid];  // bucket start + rows of earlier chunks
+  const int sum = E > 0 ? scan[E - 1] : 0;
+  if (tid < E) run[phys_s[tid]] = scan[phys_s[tid]] - total[phys_s[tid]] + bef_s[tid];
   if (blockIdx.x == 0) {
     if (tid < E) {
       expert_offsets[tid] = scan[tid] - total[tid];
@@ -182,26 +269,14 @@ perm_scatter_kernel(const int32_t* __restrict__ topk_idx, const int32_t* __restr
     }
   }
   __syncthreads();
-  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-  (void)lane;
-  const long long base = (long long)blockIdx.x * rounds * kThreads;
-  int ev[kPre];  // the pair ids of rounds r0 .. r0 + kPre - 1, loaded together
-  for (int r = 0; r < rounds; ++r) {
-    if (base + (long long)r * kThreads >= n_pairs) break;  // uniform across the CTA
-    if (r % kPre == 0) {
-#pragma unroll
-      for (int u = 0; u < kPre; ++u) {
-        const long long pu = base + (long long)(r + u) * kThreads + threadIdx.x;
-        ev[u] = (r + u < rounds && pu < n_pairs) ? topk_idx[pu] : -1;
-      }
-    }
-    const long long p = base + (long long)r * kThreads + threadIdx.x;
+
+  // 3. stable ranking of the pairs [t0 * k_max, t1 * k_max), kThreads per round
+  const long long pe = (long long)t1 * k_max;
+  for (long long base = (long long)t0 * k_max; base < pe; base += kThreads) {
+    const long long p = base + tid;
     int key = E;  // E = "no bucket" (padding slot or past the end)
-    if (p < n_pairs) {
-      int e = 0;
-#pragma unroll
-      for (int u = 0; u < kPre; ++u)
-        if (u == r % kPre) e = ev[u];  // register select, no local-memory indexing
+    if (p < pe) {
+      const int e = topk_idx[p];
       if (e >= E) flag(SEMMOE_DEVERR_EXPERT);
       else if (e >= 0) key = phys_s[e];
     }
@@ -209,128 +284,91 @@ perm_scatter_kernel(const int32_t* __restrict__ topk_idx, const int32_t* __restr
     const int rank_in_warp = __popc(peers & lanemask_lt());
     if (key < E && rank_in_warp == 0) wcnt[warp][key] = __popc(peers);
     __syncthreads();
-    if (p < n_pairs) {
+    if (p < pe) {
       int pos = -1;
       if (key < E) {
         pos = run[key] + rank_in_warp;
         for (int w = 0; w < warp; ++w) pos += wcnt[w][key];
-        if (pos >= P) { flag(SEMMOE_DEVERR_PAIRS); pos = -1; }
+        if (pos < 0 || pos >= P) { flag(SEMMOE_DEVERR_PAIRS); pos = -1; }
         else sorted_to_pair[pos] = (int32_t)p;
       }
       pair_to_sorted[p] = pos;
     }
     __syncthreads();
-    for (int b = threadIdx.x; b < E; b += kThreads) {
+    for (int b = tid; b < E; b += kThreads) {
       int s2 = 0;
       for (int w = 0; w < kWarps; ++w) { s2 += wcnt[w][b]; wcnt[w][b] = 0; }
       run[b] += s2;
     }
     __syncthreads();
   }
-}
 
-// x_perm[pair_to_sorted[t * k_max + j], :] = x[t, :] for every live slot j of
-// token t: one warp per token reads its row once, in segments of up to 4 KB
-// held in registers, and writes each segment to the token's k_t sorted rows.
-// (Walking the sorted rows instead re-reads each x row k_t times, far apart
-// in time, and the row writes push those reads out of L2.)
-constexpr int kSegVec = 8;  // 16-byte vectors per lane per segment: 32 x 8 x 16 B = 4 KB
-
-__global__ void __launch_bounds__(kThreads)
-perm_copy_kernel(const unsigned char* __restrict__ x, const int32_t* __restrict__ pair_to_sorted, int T, int k_max,
-                 int P, int row_bytes, unsigned char* __restrict__ x_perm) {
-  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-  const int n16 = row_bytes / 16;
-  const int kk = k_max < 32 ? k_max : 32;
-  for (int t = blockIdx.x * kWarps + warp; t < T; t += gridDim.x * kWarps) {
-    const int32_t* slots = pair_to_sorted + (size_t)t * k_max;
-    int q_l = -1;
-    if (lane < kk) {
-      q_l = slots[lane];
-      if (q_l >= P) { flag(SEMMOE_DEVERR_PAIRS); q_l = -1; }
-    }
-    const uint4* src = reinterpret_cast<const uint4*>(x + (size_t)t * row_bytes);
-    for (int seg = 0; seg < n16; seg += 32 * kSegVec) {
-      uint4 v[kSegVec];
-#pragma unroll
-      for (int u = 0; u < kSegVec; ++u) {
-        const int c = seg + u * 32 + lane;
-        if (c < n16) v[u] = src[c];
-      }
-      for (int j = 0; j < kk; ++j) {
-        const int q = __shfl_sync(0xffffffffu, q_l, j);
-        if (q < 0) continue;
-        uint4* dst = reinterpret_cast<uint4*>(x_perm + (size_t)q * row_bytes);
-#pragma unroll
-        for (int u = 0; u < kSegVec; ++u) {
-          const int c = seg + u * 32 + lane;
-          if (c < n16) dst[c] = v[u];
-        }
-      }
-      for (int j = 32; j < k_max; ++j) {  // budgets above 32 experts: read the slot directly
-        const int q = slots[j];
-        if (q < 0) continue;
-        if (q >= P) { if (lane == 0) flag(SEMMOE_DEVERR_PAIRS); continue; }
-        uint4* dst = reinterpret_cast<uint4*>(x_perm + (size_t)q * row_bytes);
-#pragma unroll
-        for (int u = 0; u < kSegVec; ++u) {
-          const int c = seg + u * 32 + lane;
-          if (c < n16) dst[c] = v[u];
-        }
-      }
-    }
-  }
+  // 4. the rows (this CTA's own pair_to_sorted entries, written above)
+  if (x != nullptr && P > 0)
+    for (int t = t0 + warp; t < t1; t += kWarps)
+      copy_token_row(x, pair_to_sorted + (size_t)t * k_max, t, k_max, P, row_bytes, x_perm);
+  (void)lane;
 }
 
 }  // namespace
 
 int permute_take_errors(cudaStream_t s, int* bits) { return take_error_word(g_err, s, bits); }
 
+// Scratch of the permute: the count table it makes itself when the caller
+// passes none.
 size_t permute_ws_bytes(int T, int k_max, int E) {
-  long long n = (long long)T * k_max;
-  int nc = n_chunks(n > 0 ? n : 1);
-  return align_up((size_t)nc * E * sizeof(int32_t), 256);
+  (void)k_max;
+  const int chunk = internal_chunk_tokens(T > 0 ? T : 1);
+  const int nc = (T + chunk - 1) / chunk;
+  return align_up((size_t)E * padded_chunks(nc > 0 ? nc : 1) * sizeof(int32_t), 256);
+}
+
+size_t pair_counts_bytes(int T, int E) {
+  const int nc = (T + SEMMOE_PAIR_COUNT_CHUNK - 1) / SEMMOE_PAIR_COUNT_CHUNK;
+  return (size_t)E * padded_chunks(nc > 0 ? nc : 1) * sizeof(int32_t);
+}
+
+int pair_counts_stride(int T) {
+  return padded_chunks((T + SEMMOE_PAIR_COUNT_CHUNK - 1) / SEMMOE_PAIR_COUNT_CHUNK);
 }
 
 cudaError_t launch_permute(const int32_t* topk_idx, const int32_t* expert_rank, const void* x, int dtype, int T,
                            int H, int E, int R, int k_max, int P, int32_t* expert_offsets,
                            int32_t* rank_offsets, int32_t* phys_to_expert, int32_t* expert_counts,
-                           int32_t* sorted_to_pair, int32_t* pair_to_sorted, void* x_perm, void* ws,
-                           cudaStream_t s) {
-  const long long n_pairs = (long long)T * k_max;
-  const int nc = n_chunks(n_pairs > 0 ? n_pairs : 1);
-  int32_t* hist = static_cast<int32_t*>(ws);
-  if (n_pairs > 0) {
-    perm_hist_kernel<<<nc, kThreads, 0, s>>>(topk_idx, expert_rank, n_pairs, rounds_per_chunk(n_pairs), E, R,
-                                             hist);
-    count_launches(1);
+                           int32_t* sorted_to_pair, int32_t* pair_to_sorted, void* x_perm,
+                           const int32_t* pair_counts, void* ws, cudaStream_t s) {
+  // The count table: the caller's (128-token chunks, from the router) while it
+  // has at most 1024 chunks, else one made here (at most 96 chunks).
+  int chunk = SEMMOE_PAIR_COUNT_CHUNK;
+  int nc = (T + chunk - 1) / chunk;
+  const int32_t* counts = pair_counts;
+  if (counts == nullptr || nc > 1024) {
+    chunk = internal_chunk_tokens(T > 0 ? T : 1);
+    nc = (T + chunk - 1) / chunk;
+    int32_t* own = static_cast<int32_t*>(ws);
+    if (nc > 0) {
+      perm_count_kernel<<<nc, kHistThreads, 0, s>>>(topk_idx, T, k_max, E, chunk, padded_chunks(nc), own);
+      count_launches(1);
+    }
+    counts = own;
   }
-  perm_scatter_kernel<<<n_pairs > 0 ? nc : 1, kThreads, 0, s>>>(
-      topk_idx, expert_rank, n_pairs, rounds_per_chunk(n_pairs), n_pairs > 0 ? nc : 0, E, R, P, hist,
-      expert_offsets, rank_offsets,
-      phys_to_expert, expert_counts, sorted_to_pair, pair_to_sorted);
+  // tokens per CTA: about two CTAs per SM
+  const int target = 2 * sm_count();
+  int tpc = (T + target - 1) / target;
+  if (tpc < 1) tpc = 1;
+  const int grid = T > 0 ? (T + tpc - 1) / tpc : 1;
+  const int row_bytes = H * (dtype == SEMMOE_BF16 ? 2 : 4);
+  perm_rank_copy_kernel<<<grid, kThreads, 0, s>>>(
+      topk_idx, expert_rank, counts, nc, padded_chunks(nc), chunk, T, k_max, E, R, P, tpc, expert_offsets,
+      rank_offsets, phys_to_expert, expert_counts, sorted_to_pair, pair_to_sorted,
+      x_perm != nullptr ? static_cast<const unsigned char*>(x) : nullptr, row_bytes,
+      static_cast<unsigned char*>(x_perm));
   count_launches(1);
-  if (x != nullptr && x_perm != nullptr && P > 0) {
-    const int row_bytes = H * (dtype == SEMMOE_BF16 ? 2 : 4);
-    int blocks = (T + kWarps - 1) / kWarps;
-    const int cap = sm_count() * 16;
-    if (blocks > cap) blocks = cap;
-    perm_copy_kernel<<<blocks, kThreads, 0, s>>>(static_cast<const unsigned char*>(x), pair_to_sorted, T, k_max, P,
-                                                 row_bytes, static_cast<unsigned char*>(x_perm));
-    count_launches(1);
-  }
   return cudaGetLastError();
 }
 
 size_t permute_noalloc_max_scratch() { return kNoAllocScratchBytes; }
 
-// Device address of g_noalloc_scratch in the current CUDA context.  In host
-// code the array's name is only a host-side stand-in, so the address is looked
-// up with cudaGetSymbolAddress, with the context current, and cached.  The
-// cache is keyed on the context's unique ID (cuCtxGetId), not on the device
-// number: after cudaDeviceReset, or in another context on the same device, the
-// library's module is loaded again and the array has another address, while a
-// context's ID is never reused within the process.
 // The two driver calls, fetched through the runtime (the library links no
 // driver library, so it still loads on hosts without one).
 template <typename F>
@@ -343,6 +381,13 @@ static F driver_fn(const char* name, int version) {
   return reinterpret_cast<F>(p);
 }
 
+// Device address of g_noalloc_scratch in the current CUDA context.  In host
+// code the array's name is only a host-side stand-in, so the address is looked
+// up with cudaGetSymbolAddress, with the context current, and cached.  The
+// cache is keyed on the context's unique ID (cuCtxGetId), not on the device
+// number: after cudaDeviceReset, or in another context on the same device, the
+// library's module is loaded again and the array has another address, while a
+// context's ID is never reused within the process.
 static cudaError_t noalloc_scratch_address(void** out) {
   using CtxGetCurrent = CUresult (*)(CUcontext*);
   using CtxGetId = CUresult (*)(CUcontext, unsigned long long*);
@@ -389,10 +434,10 @@ cudaError_t launch_permute_noalloc(const int32_t* topk_idx, const int32_t* exper
   void* scratch = nullptr;
   cudaError_t e = noalloc_scratch_address(&scratch);
   if (e != cudaSuccess) return e;
-  // The kernels write every scratch entry before they read it, so stale contents of an
-  // earlier call never leak into this one.
+  // The count kernel writes every table entry the ranking kernel adds up before
+  // that kernel runs, so stale contents of an earlier call never leak into this one.
   return launch_permute(topk_idx, expert_rank, x, dtype, T, H, E, R, k_max, P, expert_offsets, rank_offsets,
-                        phys_to_expert, expert_counts, sorted_to_pair, pair_to_sorted, x_perm, scratch, s);
+                        phys_to_expert, expert_counts, sorted_to_pair, pair_to_sorted, x_perm, nullptr, scratch, s);
 }
 
 }  // namespace semmoe

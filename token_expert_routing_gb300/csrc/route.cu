@@ -17,6 +17,17 @@ __device__ int g_err;  // SEMMOE_DEVERR_* bits seen by this file's kernels
 
 __device__ __forceinline__ void flag(int bit) { atomicOr(&g_err, bit); }
 
+// Optional count table of the picks for the permute: counts[e * stride + c] =
+// live pairs of expert e among the tokens of 128-token chunk c (zeroed before
+// the kernel; one atomic add per pick).
+struct PairCounts {
+  int32_t* p = nullptr;
+  int stride = 0;
+};
+__device__ __forceinline__ void count_pick(const PairCounts& pc, int e, int t) {
+  if (pc.p != nullptr) atomicAdd(pc.p + (size_t)e * pc.stride + t / SEMMOE_PAIR_COUNT_CHUNK, 1);
+}
+
 constexpr int kRouteThreads = 256;
 constexpr int kRouteTok = 32;   // tokens per block
 constexpr int kRouteEC = 64;    // experts per GEMM chunk
@@ -198,7 +209,7 @@ __device__ __forceinline__ void warp_select(const float (&v)[NPER], int n, int k
 template <int NPER>  // logits held per lane: E <= 32 * NPER
 __device__ void warp_topk(const float* row, int ks, size_t slice_stride, float* logits_out, int E, int t,
                           const int32_t* __restrict__ k_per_token, int k_uniform, int k_max, float* my_v, int* my_e,
-                          int32_t* __restrict__ topk_idx, float* __restrict__ topk_w) {
+                          int32_t* __restrict__ topk_idx, float* __restrict__ topk_w, const PairCounts& pc) {
   const int lane = threadIdx.x % 32;
   const int kt = warp_budget(k_per_token, k_uniform, k_max, t);
   float v[NPER];
@@ -215,6 +226,7 @@ __device__ void warp_topk(const float* row, int ks, size_t slice_stride, float* 
     if (j < kt && my_e[j] >= 0) {
       e = my_e[j];
       g = expf(my_v[j] - m) / den;
+      count_pick(pc, e, t);
     }
     topk_idx[(size_t)t * k_max + j] = e;
     topk_w[(size_t)t * k_max + j] = g;
@@ -227,7 +239,7 @@ __global__ void __launch_bounds__(kRouteThreads)
 route_kernel(const TX* __restrict__ x, const TW* __restrict__ w, const float* __restrict__ logits_in,
              float* __restrict__ logits_out, const int32_t* __restrict__ k_per_token, int k_uniform,
              int T, int H, int E, int k_max, int32_t* __restrict__ topk_idx,
-             float* __restrict__ topk_w) {
+             float* __restrict__ topk_w, PairCounts pc) {
   extern __shared__ __align__(16) unsigned char smem_raw[];
   const int Epad = (E + 31) / 32 * 32;
   float* lg = reinterpret_cast<float*>(smem_raw);
@@ -294,7 +306,7 @@ route_kernel(const TX* __restrict__ x, const TW* __restrict__ w, const float* __
     const int t = t0 + tl;
     if (t >= T) break;
     warp_topk<kRouteMaxE / 32>(lg + tl * Epad, 1, 0, nullptr, E, t, k_per_token, k_uniform, k_max,
-                               sel_v + warp * k_max, sel_e + warp * k_max, topk_idx, topk_w);
+                               sel_v + warp * k_max, sel_e + warp * k_max, topk_idx, topk_w, pc);
   }
 }
 
@@ -307,7 +319,7 @@ template <int NPER>
 __global__ void __launch_bounds__(kTopkWarps * 32)
 topk_kernel(const float* __restrict__ logits, int ks, float* __restrict__ logits_out,
             const int32_t* __restrict__ k_per_token, int k_uniform, int T, int E, int k_max,
-            int32_t* __restrict__ topk_idx, float* __restrict__ topk_w) {
+            int32_t* __restrict__ topk_idx, float* __restrict__ topk_w, PairCounts pc) {
   extern __shared__ __align__(16) unsigned char smem_raw[];
   float* sel_v = reinterpret_cast<float*>(smem_raw);
   int* sel_e = reinterpret_cast<int*>(sel_v + kTopkWarps * k_max);
@@ -315,7 +327,7 @@ topk_kernel(const float* __restrict__ logits, int ks, float* __restrict__ logits
   const int t = blockIdx.x * kTopkWarps + warp;
   if (t >= T) return;
   warp_topk<NPER>(logits + (size_t)t * E, ks, (size_t)T * E, logits_out != nullptr ? logits_out + (size_t)t * E : nullptr,
-            E, t, k_per_token, k_uniform, k_max, sel_v + warp * k_max, sel_e + warp * k_max, topk_idx, topk_w);
+            E, t, k_per_token, k_uniform, k_max, sel_v + warp * k_max, sel_e + warp * k_max, topk_idx, topk_w, pc);
 }
 
 // MoE-Prism's training-free hierarchical gating, one warp per token: the
@@ -327,7 +339,8 @@ template <int NPER>  // sub-experts (and parents) held per lane: Ep * N <= 32 * 
 __global__ void __launch_bounds__(kTopkWarps * 32)
 hier_topk_kernel(const float* __restrict__ logits, int ks, float* __restrict__ logits_out,
                  const float* __restrict__ sub_logw, int N, const int32_t* __restrict__ k_per_token, int k_uniform,
-                 int T, int Ep, int k_max, int32_t* __restrict__ topk_idx, float* __restrict__ topk_w) {
+                 int T, int Ep, int k_max, int32_t* __restrict__ topk_idx, float* __restrict__ topk_w,
+                 PairCounts pc) {
   extern __shared__ __align__(16) unsigned char smem_raw[];
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   float* base = reinterpret_cast<float*>(smem_raw);
@@ -381,6 +394,7 @@ hier_topk_kernel(const float* __restrict__ logits, int ks, float* __restrict__ l
     if (j < kt && sel_e[j] >= 0) {
       sx = sel_e[j];
       g = expf(lg[sx / N] - m) / den;
+      count_pick(pc, sx, t);
     }
     topk_idx[(size_t)t * k_max + j] = sx;
     topk_w[(size_t)t * k_max + j] = g;
@@ -455,7 +469,7 @@ remote_count_kernel(const int32_t* __restrict__ topk_idx, const int32_t* __restr
 template <typename TX, typename TW>
 cudaError_t launch_route_t(const void* x, const void* w, const float* li, float* lo, const int32_t* kpt,
                            int ku, int T, int H, int E, int k_max, int32_t* idx, float* wt,
-                           cudaStream_t s) {
+                           cudaStream_t s, PairCounts pc = PairCounts()) {
   size_t sm = route_smem_bytes(E, k_max);
   auto kern = route_kernel<TX, TW>;
   if (sm > 48 * 1024) {  // raise the limit once to the largest layout (E = k_max = 256)
@@ -465,7 +479,7 @@ cudaError_t launch_route_t(const void* x, const void* w, const float* li, float*
   }
   dim3 grid((T + kRouteTok - 1) / kRouteTok);
   kern<<<grid, kRouteThreads, sm, s>>>(static_cast<const TX*>(x), static_cast<const TW*>(w), li, lo, kpt,
-                                       ku, T, H, E, k_max, idx, wt);
+                                       ku, T, H, E, k_max, idx, wt, pc);
   count_launches(1);
   return cudaGetLastError();
 }
@@ -507,10 +521,21 @@ static cudaError_t route_partials_tc(const void* x, const void* w, int w_dtype, 
   return cudaSuccess;
 }
 
+// The count table for the permute, zeroed on the stream (the top-k kernels add to it).
+static cudaError_t pair_counts_begin(int32_t* counts, int T, int E, PairCounts* pc, cudaStream_t s) {
+  if (counts == nullptr) return cudaSuccess;
+  pc->p = counts;
+  pc->stride = pair_counts_stride(T);
+  return cudaMemsetAsync(counts, 0, pair_counts_bytes(T, E), s);
+}
+
 cudaError_t launch_route(const void* x, int x_dtype, const void* w, int w_dtype, const float* logits_in,
                          float* logits_out, const int32_t* kpt, int k_uniform, int T, int H, int E, int k_max,
-                         int32_t* topk_idx, float* topk_w, void* ws, cudaStream_t s) {
+                         int32_t* topk_idx, float* topk_w, int32_t* pair_counts, void* ws, cudaStream_t s) {
   if (T == 0) return cudaSuccess;
+  PairCounts pc;
+  cudaError_t ec = pair_counts_begin(pair_counts, T, E, &pc, s);
+  if (ec != cudaSuccess) return ec;
   int ks = 1;
   if (logits_in == nullptr && route_on_tensor_cores(x_dtype, H)) {
     cudaError_t e = route_partials_tc(x, w, w_dtype, T, H, E, ws, &logits_in, &ks, s);
@@ -522,27 +547,31 @@ cudaError_t launch_route(const void* x, int x_dtype, const void* w, int w_dtype,
     const size_t sm = (size_t)kTopkWarps * k_max * (sizeof(float) + sizeof(int));
     const dim3 grid((T + kTopkWarps - 1) / kTopkWarps), block(kTopkWarps * 32);
     if (E <= 32)
-      topk_kernel<1><<<grid, block, sm, s>>>(logits_in, ks, logits_out, kpt, k_uniform, T, E, k_max, topk_idx, topk_w);
+      topk_kernel<1><<<grid, block, sm, s>>>(logits_in, ks, logits_out, kpt, k_uniform, T, E, k_max, topk_idx, topk_w,
+                                               pc);
     else if (E <= 64)
-      topk_kernel<2><<<grid, block, sm, s>>>(logits_in, ks, logits_out, kpt, k_uniform, T, E, k_max, topk_idx, topk_w);
+      topk_kernel<2><<<grid, block, sm, s>>>(logits_in, ks, logits_out, kpt, k_uniform, T, E, k_max, topk_idx, topk_w,
+                                               pc);
     else if (E <= 128)
-      topk_kernel<4><<<grid, block, sm, s>>>(logits_in, ks, logits_out, kpt, k_uniform, T, E, k_max, topk_idx, topk_w);
+      topk_kernel<4><<<grid, block, sm, s>>>(logits_in, ks, logits_out, kpt, k_uniform, T, E, k_max, topk_idx, topk_w,
+                                               pc);
     else
-      topk_kernel<8><<<grid, block, sm, s>>>(logits_in, ks, logits_out, kpt, k_uniform, T, E, k_max, topk_idx, topk_w);
+      topk_kernel<8><<<grid, block, sm, s>>>(logits_in, ks, logits_out, kpt, k_uniform, T, E, k_max, topk_idx, topk_w,
+                                               pc);
     count_launches(1);
     return cudaGetLastError();
   }
   if (x_dtype == SEMMOE_BF16 && w_dtype == SEMMOE_F32)
     return launch_route_t<__nv_bfloat16, float>(x, w, nullptr, logits_out, kpt, k_uniform, T, H, E, k_max,
-                                                topk_idx, topk_w, s);
+                                                topk_idx, topk_w, s, pc);
   if (x_dtype == SEMMOE_BF16 && w_dtype == SEMMOE_BF16)
     return launch_route_t<__nv_bfloat16, __nv_bfloat16>(x, w, nullptr, logits_out, kpt, k_uniform, T, H, E,
-                                                        k_max, topk_idx, topk_w, s);
+                                                        k_max, topk_idx, topk_w, s, pc);
   if (x_dtype == SEMMOE_F32 && w_dtype == SEMMOE_F32)
     return launch_route_t<float, float>(x, w, nullptr, logits_out, kpt, k_uniform, T, H, E, k_max, topk_idx,
-                                        topk_w, s);
+                                        topk_w, s, pc);
   return launch_route_t<float, __nv_bfloat16>(x, w, nullptr, logits_out, kpt, k_uniform, T, H, E, k_max,
-                                              topk_idx, topk_w, s);
+                                              topk_idx, topk_w, s, pc);
 }
 
 size_t route_hier_ws_bytes(int T, int H, int Ep, int x_dtype, int w_dtype) {
@@ -554,8 +583,8 @@ size_t route_hier_ws_bytes(int T, int H, int Ep, int x_dtype, int w_dtype) {
 
 cudaError_t launch_route_hier(const void* x, int x_dtype, const void* w, int w_dtype, const float* logits_in,
                               float* logits_out, const float* sub_logw, int N, const int32_t* kpt, int k_uniform,
-                              int T, int H, int Ep, int k_max, int32_t* topk_idx, float* topk_w, void* ws,
-                              cudaStream_t s) {
+                              int T, int H, int Ep, int k_max, int32_t* topk_idx, float* topk_w,
+                              int32_t* pair_counts, void* ws, cudaStream_t s) {
   if (T == 0) return cudaSuccess;
   int ks = 1;
   if (logits_in == nullptr) {
@@ -584,20 +613,23 @@ cudaError_t launch_route_hier(const void* x, int x_dtype, const void* w, int w_d
     logits_out = nullptr;
   }
   const int E = Ep * N;
+  PairCounts pc;
+  cudaError_t ec = pair_counts_begin(pair_counts, T, E, &pc, s);
+  if (ec != cudaSuccess) return ec;
   const size_t sm = (size_t)kTopkWarps * (Ep + 2 * k_max) * sizeof(float);
   const dim3 grid((T + kTopkWarps - 1) / kTopkWarps), block(kTopkWarps * 32);
   if (E <= 32)
     hier_topk_kernel<1><<<grid, block, sm, s>>>(logits_in, ks, logits_out, sub_logw, N, kpt, k_uniform, T, Ep,
-                                                k_max, topk_idx, topk_w);
+                                                k_max, topk_idx, topk_w, pc);
   else if (E <= 64)
     hier_topk_kernel<2><<<grid, block, sm, s>>>(logits_in, ks, logits_out, sub_logw, N, kpt, k_uniform, T, Ep,
-                                                k_max, topk_idx, topk_w);
+                                                k_max, topk_idx, topk_w, pc);
   else if (E <= 128)
     hier_topk_kernel<4><<<grid, block, sm, s>>>(logits_in, ks, logits_out, sub_logw, N, kpt, k_uniform, T, Ep,
-                                                k_max, topk_idx, topk_w);
+                                                k_max, topk_idx, topk_w, pc);
   else
     hier_topk_kernel<8><<<grid, block, sm, s>>>(logits_in, ks, logits_out, sub_logw, N, kpt, k_uniform, T, Ep,
-                                                k_max, topk_idx, topk_w);
+                                                k_max, topk_idx, topk_w, pc);
   count_launches(1);
   return cudaGetLastError();
 }

@@ -200,16 +200,19 @@ class MoELayer:
         logits = torch.empty(T, Ep, dtype=torch.float32, device=dev) if keep_logits else None
         topk_idx = torch.empty(T, k_max, **i32)
         topk_w = torch.empty(T, k_max, dtype=torch.float32, device=dev)
+        # the router counts its picks per 128-token chunk; the permute starts from that table
+        pair_counts = torch.empty(max(abi.semmoe_pair_counts_size(T, E) // 4, 4), **i32)
         if self.sub_logw is None:
             wr, wd = self._router_weight(x)
             ws = self._workspace("route", abi.semmoe_route_workspace_size(T, H, E, abi.dtype_code(x), wd))
             abi.semmoe_route(x, wr, logits_in, logits, k_per_token, k or 0, T, H, E, k_max,
-                             topk_idx, topk_w, ws, stream, w_dtype=wd)
+                             topk_idx, topk_w, ws, stream, w_dtype=wd, pair_counts=pair_counts)
         else:
             wr, wd = self._router_weight(x)
             ws = self._workspace("route", abi.semmoe_route_hier_workspace_size(T, H, Ep, abi.dtype_code(x), wd))
             abi.semmoe_route_hier(x, wr, logits_in, logits, self.sub_logw, E // Ep, k_per_token,
-                                  k or 0, T, H, Ep, k_max, topk_idx, topk_w, ws, stream, w_dtype=wd)
+                                  k or 0, T, H, Ep, k_max, topk_idx, topk_w, ws, stream, w_dtype=wd,
+                                  pair_counts=pair_counts)
         mark("route")
         if shared_side and self.shared_at == "route":
             shared_on_side()
@@ -255,7 +258,7 @@ class MoELayer:
         ws = self._workspace("permute", abi.semmoe_permute_workspace_size(T, k_max, E))
         abi.semmoe_permute(topk_idx, self.expert_rank, None if self.fused_gather else x, T, H, E, R, k_max, P,
                            expert_offsets, rank_offsets, phys_to_expert, expert_counts, sorted_to_pair,
-                           pair_to_sorted, x_perm, ws, stream)
+                           pair_to_sorted, x_perm, ws, stream, pair_counts=pair_counts)
         mark("permute")
         y_perm = torch.empty(P, H, dtype=x.dtype, device=dev)
         if shared_side and self.shared_at == "permute":  # the shared experts beside the routed FFN
