@@ -718,3 +718,35 @@ def test_hier_route_pair_counts():
     ref_idx, _ = oracle.hier_route(l, logw, N, k, k_max)
     np.testing.assert_array_equal(np_(idx), ref_idx)
     np.testing.assert_array_equal(np_(counts).reshape(E, stride), _chunk_histogram(ref_idx, k, E, stride))
+
+
+@pytest.mark.parametrize("T,H,E,k_max,wd,per_token", [
+    (77, 256, 8, 1, "bf16", False), (1000, 512, 64, 6, "bf16", True), (16384 + 45, 2048, 128, 8, "bf16", False),
+    (20485, 256, 256, 24, "bf16", True), (300, 200, 7, 3, "f32", True), (4096, 2048, 64, 6, "f32", False),
+    (130, 128, 64, 32, "bf16", True)])
+def test_router_with_top_k_in_the_gemm_epilogue(T, H, E, k_max, wd, per_token):
+    """The one-kernel router (tensor-core GEMM, top-k in the epilogue, one
+    thread per token): logits within the logit tolerance of the oracle, picks
+    bit-exact against the oracle's top-k of the GPU's own logits, gates within
+    the gate tolerance, and the count table equal to the per-chunk histogram of
+    the picks.  Covers a ragged last tile, per-token budgets, a grid beyond one
+    CTA per SM (T = 20485), k_max = 32 and fp32 weights split into bf16 parts."""
+    a = abi()
+    rng = np.random.default_rng(T + E + k_max)
+    x = torch.from_numpy((rng.standard_normal((T, H)) / np.sqrt(H)).astype(np.float32)).to(torch.bfloat16)
+    wdt = torch.bfloat16 if wd == "bf16" else torch.float32
+    wr = torch.from_numpy(rng.standard_normal((E, H)).astype(np.float32)).to(wdt)
+    k = rng.integers(1, k_max + 1, size=T).astype(np.int32) if per_token else np.full(T, k_max, np.int32)
+    idx = torch.empty(T, k_max, **i32)
+    gw = torch.empty(T, k_max, dtype=torch.float32, device="cuda")
+    lg = torch.empty(T, E, dtype=torch.float32, device="cuda")
+    stride = a.semmoe_pair_counts_stride(T)
+    counts = torch.full((E * stride,), -1, **i32)
+    a.semmoe_route(x.cuda(), wr.cuda(), None, lg, torch.from_numpy(k).cuda() if per_token else None,
+                   0 if per_token else k_max, T, H, E, k_max, idx, gw, pair_counts=counts)
+    assert a.semmoe_check_errors() == 0
+    assert max_rel(np_(lg), oracle.router_logits(x, wr)) < LOGIT_TOL
+    ref_idx, ref_w = oracle.topk_route(np_(lg), k, k_max)
+    np.testing.assert_array_equal(np_(idx), ref_idx)
+    np.testing.assert_allclose(np_(gw), ref_w, rtol=0, atol=GATE_ATOL)
+    np.testing.assert_array_equal(np_(counts).reshape(E, stride), _chunk_histogram(ref_idx, k, E, stride))

@@ -30,6 +30,13 @@ cudaError_t launch_route_split(const float* w, int H, int E, void* split, cudaSt
 int route_tc_k_slices(int T, int H, int E, int w_dtype);
 cudaError_t launch_route_logits_tc(const void* x, const void* w, int w_dtype, int T, int H, int E, float* partials,
                                    int ks, void* split, cudaStream_t s);
+// The router GEMM and the top-k in one tensor-core kernel (route_tc.cu), for
+// routers whose experts fit one MMA (route_topk_tc_ok); writes the count table
+// (counts, row stride count_stride) in full when counts is not null.
+bool route_topk_tc_ok(int E, int k_max, int w_dtype);
+cudaError_t launch_route_topk_tc(const void* x, const void* w, int w_dtype, int T, int H, int E, int k_max,
+                                 float* logits_out, const int32_t* kpt, int k_uniform, int32_t* topk_idx,
+                                 float* topk_w, int32_t* counts, int count_stride, void* split, cudaStream_t s);
 // pair_counts (nullable): zeroed here, then the live picks are counted into it
 // (layout of pair_counts_bytes).
 cudaError_t launch_route(const void* x, int x_dtype, const void* w, int w_dtype,

@@ -203,6 +203,241 @@ route_tc_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_constant
   }
 }
 
+
+// ---------------------------------------------------------------------------
+// Router GEMM and top-k in one kernel (E16 * S <= 256 accumulator columns,
+// k_max <= KM): one CTA per 128-token tile reads the whole contraction over H
+// (no K slices, no logits in memory), and each epilogue thread owns one token
+// row of the accumulator: it adds the weight parts' columns into logits, keeps
+// the KM best as (key, index) in a sorted register list, then writes the k_t
+// picks, their gates and the tile's pair counts.  The k-blocks are visited
+// from a per-tile starting block (tile index mod the block count), so the
+// tiles do not all read the same weight lines at the same moment.
+// ---------------------------------------------------------------------------
+
+// Order-preserving 32-bit key of an fp32 score: larger key = larger score; -0.0
+// counts as +0.0; 0 is below every float (an empty list slot).
+__device__ __forceinline__ uint32_t score_key(float v) {
+  const uint32_t b = __float_as_uint(__fadd_rn(v, 0.0f));
+  return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+}
+__device__ __forceinline__ float key_score(uint32_t k) {
+  return __uint_as_float((k & 0x80000000u) ? (k ^ 0x80000000u) : ~k);
+}
+
+// Insert (key, e) into keys/ids, sorted by key descending; entries scanned in
+// increasing e, so among equal keys the earlier (lower) index stays ahead.
+template <int KM>
+__device__ __forceinline__ void list_insert(uint32_t (&keys)[KM], int (&ids)[KM], uint32_t key, int e) {
+  if (!(key > keys[KM - 1])) return;
+  bool placed = false;
+#pragma unroll
+  for (int i = KM - 1; i > 0; --i) {
+    const bool up = key > keys[i - 1];
+    const uint32_t nk = placed ? keys[i] : (up ? keys[i - 1] : key);
+    const int ne = placed ? ids[i] : (up ? ids[i - 1] : e);
+    keys[i] = nk;
+    ids[i] = ne;
+    placed = placed || !up;
+  }
+  if (!placed) {
+    keys[0] = key;
+    ids[0] = e;
+  }
+}
+
+template <int S, int KM, int CPS>
+__global__ void __launch_bounds__(THREADS, CPS)
+route_topk_tc_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_constant__ CUtensorMap map_w, int T,
+                     int H, int E, int E16, int stages, float* __restrict__ logits_out,
+                     const int32_t* __restrict__ k_per_token, int k_uniform, int k_max,
+                     int32_t* __restrict__ topk_idx, float* __restrict__ topk_w, int32_t* __restrict__ counts,
+                     int count_stride) {
+  extern __shared__ __align__(1024) unsigned char smem_raw[];
+  const uint32_t pad = (1024u - (smem_u32(smem_raw) & 1023u)) & 1023u;
+  unsigned char* ring = smem_raw + pad;
+  Shared& sh = *reinterpret_cast<Shared*>(ring + stage_budget(CPS));
+  __shared__ int hist[256];
+  volatile int* abort_flag = &sh.abort_flag;
+
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  const int NB = S * E16;
+  const uint32_t b_bytes = (uint32_t)NB * BK * 2;
+  const uint32_t stage_bytes = A_BYTES + b_bytes;
+  const int t0 = blockIdx.x * BM;
+  const int kb_all = (H + BK - 1) / BK;
+  const int kb_first = (int)(blockIdx.x % (unsigned)kb_all);
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < stages; ++s) {
+      mbar_init(&sh.full[s], 1);
+      mbar_init(&sh.empty[s], 1);
+    }
+    mbar_init(&sh.tfull, 1);
+    mbar_init(&sh.done, 1);
+    sh.abort_flag = 0;
+    mbar_init_fence();
+    prefetch_map(&map_x);
+    prefetch_map(&map_w);
+  }
+  for (int e = threadIdx.x; e < 256; e += THREADS) hist[e] = 0;
+  if (warp == 1) tmem_alloc(&sh.tmem_base, TMEM_COLS);
+  fence_before();
+  __syncthreads();
+  fence_after();
+  const uint32_t tmem = sh.tmem_base;
+
+  if (warp == 0) {
+    if (lane == 0) {  // TMA producer
+      int it = 0;
+      for (int i = 0; i < kb_all; ++i) {
+        const int kb = kb_first + i < kb_all ? kb_first + i : kb_first + i - kb_all;
+        const int s = i % stages;
+        const uint32_t ph = (i / stages) & 1;
+        if (!mbar_wait(&sh.empty[s], ph ^ 1, abort_flag, &g_err)) break;
+        unsigned char* st = ring + (size_t)s * stage_bytes;
+        mbar_expect_tx(&sh.full[s], stage_bytes);
+        tma_load_2d(st, &map_x, &sh.full[s], kb * BK, t0);
+        tma_load_2d(st + A_BYTES, &map_w, &sh.full[s], kb * BK, 0);
+        ++it;
+      }
+      if (*abort_flag)
+        for (int j = it > stages ? it - stages : 0; j < it; ++j)
+          mbar_drain(&sh.full[j % stages], (j / stages) & 1, &g_err);
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {  // MMA issuer
+      const uint32_t idesc = idesc_bf16_f32(BM, NB);
+      bool ok = true;
+      for (int i = 0; i < kb_all; ++i) {
+        const int s = i % stages;
+        const uint32_t ph = (i / stages) & 1;
+        if (!mbar_wait(&sh.full[s], ph, abort_flag, &g_err)) { ok = false; break; }
+        fence_after();
+        const uint32_t sa = smem_u32(ring + (size_t)s * stage_bytes), sb = sa + A_BYTES;
+#pragma unroll
+        for (int k = 0; k < BK / UK; ++k)
+          mma_bf16(tmem, sw128_desc(sa + k * UK * 2), sw128_desc(sb + k * UK * 2), idesc, (i | k) != 0);
+        commit(&sh.empty[s]);
+      }
+      if (ok) commit(&sh.tfull);
+      commit(&sh.done);
+      mbar_drain(&sh.done, 0, &g_err);
+    }
+  } else {  // epilogue: thread = token row t of the tile
+    const int q = warp & 3;
+    const int t = t0 + q * 32 + lane;
+    int ok = 1;
+    if (lane == 0) ok = mbar_wait(&sh.tfull, 0, abort_flag, &g_err);
+    ok = __shfl_sync(0xffffffffu, ok, 0);
+    if (ok) {
+      fence_after();
+      const uint32_t trow = tmem + ((uint32_t)(q * 32) << 16);
+      uint32_t keys[KM];
+      int ids[KM];
+#pragma unroll
+      for (int j = 0; j < KM; ++j) {
+        keys[j] = 0u;
+        ids[j] = -1;
+      }
+      bool nonfinite = false;
+      for (int c = 0; c < E16; c += 16) {
+        uint32_t v0[16], v1[16], v2[16];
+        tmem_ld16(trow + c, v0);
+        if (S == 3) {
+          tmem_ld16(trow + E16 + c, v1);
+          tmem_ld16(trow + 2 * E16 + c, v2);
+        }
+        tmem_ld_wait();
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          const int e = c + i;
+          if (e < E) {
+            float l = __uint_as_float(v0[i]);
+            if (S == 3) l = (l + __uint_as_float(v1[i])) + __uint_as_float(v2[i]);
+            if (logits_out != nullptr && t < T) logits_out[(size_t)t * E + e] = l;
+            if (!isfinite(l)) {
+              nonfinite = true;
+              l = -INFINITY;
+            }
+            list_insert<KM>(keys, ids, score_key(l), e);
+          }
+        }
+      }
+      if (t < T) {
+        if (nonfinite) atomicOr(&g_err, SEMMOE_DEVERR_NONFINITE);
+        int kt = k_per_token != nullptr ? k_per_token[t] : k_uniform;
+        if (kt < 1 || kt > k_max) {
+          atomicOr(&g_err, SEMMOE_DEVERR_K);
+          kt = kt < 1 ? 1 : k_max;
+        }
+        const float m = key_score(keys[0]);
+        float den = 0.f;
+#pragma unroll
+        for (int j = 0; j < KM; ++j)
+          if (j < kt && ids[j] >= 0) den += expf(key_score(keys[j]) - m);
+#pragma unroll
+        for (int j = 0; j < KM; ++j) {
+          if (j < k_max) {
+            int e = -1;
+            float g = 0.f;
+            if (j < kt) {
+              if (ids[j] >= 0) {
+                e = ids[j];
+                g = expf(key_score(keys[j]) - m) / den;
+                atomicAdd(&hist[e], 1);
+              } else {
+                atomicOr(&g_err, SEMMOE_DEVERR_NONFINITE);  // fewer than k_t scores
+              }
+            }
+            topk_idx[(size_t)t * k_max + j] = e;
+            topk_w[(size_t)t * k_max + j] = g;
+          }
+        }
+      }
+    }
+    // the tile's pair counts (the tile is chunk blockIdx.x of the count table)
+    asm volatile("bar.sync 1, 128;" ::: "memory");
+    if (counts != nullptr) {
+      const int et = threadIdx.x - 64;
+      for (int e = et; e < E; e += 128) counts[(size_t)e * count_stride + blockIdx.x] = hist[e];
+      if (blockIdx.x == 0) {  // entries past the last chunk are 0
+        const int nchunk = (int)gridDim.x;
+        for (int i = et; i < E * (count_stride - nchunk); i += 128)
+          counts[(size_t)(i / (count_stride - nchunk)) * count_stride + nchunk + i % (count_stride - nchunk)] = 0;
+      }
+    }
+  }
+
+  fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    __syncwarp();
+    fence_after();
+    tmem_dealloc(tmem, TMEM_COLS);
+  }
+}
+
+template <int S, int KM, int CPS>
+static cudaError_t launch_topk_k(int grid, const CUtensorMap& mx, const CUtensorMap& mw, int T, int H, int E, int E16,
+                                 int stages, float* logits_out, const int32_t* kpt, int k_uniform, int k_max,
+                                 int32_t* topk_idx, float* topk_w, int32_t* counts, int count_stride, cudaStream_t s) {
+  static std::atomic<unsigned long long> smem_set{0};
+  cudaError_t e = ensure_smem_limit(route_topk_tc_kernel<S, KM, CPS>, (int)smem_bytes(CPS), smem_set);
+  if (e != cudaSuccess) return e;
+  route_topk_tc_kernel<S, KM, CPS><<<grid, THREADS, smem_bytes(CPS), s>>>(
+      mx, mw, T, H, E, E16, stages, logits_out, kpt, k_uniform, k_max, topk_idx, topk_w, counts, count_stride);
+  return cudaSuccess;
+}
+
+template <int S, int KM>
+static cudaError_t launch_topk_km(int grid, int cps, const CUtensorMap& mx, const CUtensorMap& mw, int T, int H, int E,
+                                  int E16, int stages, float* lo, const int32_t* kpt, int ku, int k_max, int32_t* idx,
+                                  float* w, int32_t* counts, int cs, cudaStream_t s) {
+  if (cps == 1) return launch_topk_k<S, KM, 1>(grid, mx, mw, T, H, E, E16, stages, lo, kpt, ku, k_max, idx, w, counts, cs, s);
+  return launch_topk_k<S, KM, 2>(grid, mx, mw, T, H, E, E16, stages, lo, kpt, ku, k_max, idx, w, counts, cs, s);
+}
+
 }  // namespace
 
 int route_tc_take_errors(cudaStream_t s, int* bits) { return take_error_word(g_err, s, bits); }
@@ -297,6 +532,62 @@ cudaError_t launch_route_logits_tc(const void* x, const void* w, int w_dtype, in
   else if (S == 3) e = launch_k<3, 2>(grid, mx, mw, T, H, E, EC, stages, kb_per_slice, partials, s);
   else if (cps == 1) e = launch_k<1, 1>(grid, mx, mw, T, H, E, EC, stages, kb_per_slice, partials, s);
   else e = launch_k<1, 2>(grid, mx, mw, T, H, E, EC, stages, kb_per_slice, partials, s);
+  if (e != cudaSuccess) return e;
+  count_launches(1);
+  return cudaGetLastError();
+}
+
+// The one-kernel router applies when every expert's accumulator columns fit one
+// MMA (S parts x E rounded up to 16 <= 256; an fp32 weight's split holds up to 64
+// experts in one pass) and k_max <= 32.
+bool route_topk_tc_ok(int E, int k_max, int w_dtype) {
+  const int S = w_dtype == SEMMOE_BF16 ? 1 : 3;
+  const int E16 = (E + 15) / 16 * 16;
+  if (S == 3 && E16 > 64) return false;
+  return S * E16 <= 256 && k_max <= 32;
+}
+
+cudaError_t launch_route_topk_tc(const void* x, const void* w, int w_dtype, int T, int H, int E, int k_max,
+                                 float* logits_out, const int32_t* kpt, int k_uniform, int32_t* topk_idx,
+                                 float* topk_w, int32_t* counts, int count_stride, void* split, cudaStream_t s) {
+  const int S = w_dtype == SEMMOE_BF16 ? 1 : 3;
+  const int E16 = (E + 15) / 16 * 16;
+  const void* wb = w;
+  int w_rows = E;
+  if (S == 3) {
+    if (w_dtype == SEMMOE_F32) {  // one pass: the split's EC is E16 when E16 <= 64
+      cudaError_t e = launch_route_split(static_cast<const float*>(w), H, E, split, s);
+      if (e != cudaSuccess) return e;
+      wb = split;
+    }
+    w_rows = 3 * E16;
+  }
+  CUtensorMap mx, mw;
+  {
+    const cuuint64_t dims[2] = {(cuuint64_t)H, (cuuint64_t)T};
+    const cuuint64_t str[1] = {(cuuint64_t)H * 2};
+    const cuuint32_t box[2] = {BK, BM};
+    if (!make_map_bf16(&mx, x, 2, dims, str, box)) return cudaErrorInvalidValue;
+  }
+  {
+    const cuuint64_t dims[2] = {(cuuint64_t)H, (cuuint64_t)w_rows};
+    const cuuint64_t str[1] = {(cuuint64_t)H * 2};
+    const cuuint32_t box[2] = {BK, (cuuint32_t)(S * E16)};
+    if (!make_map_bf16(&mw, wb, 2, dims, str, box)) return cudaErrorInvalidValue;
+  }
+  const int grid = (T + BM - 1) / BM;
+  const int cps = grid > sm_count() ? 2 : 1;
+  const size_t stage_bytes = A_BYTES + (size_t)S * E16 * BK * 2;
+  int stages = (int)(stage_budget(cps) / stage_bytes);
+  if (stages > MAX_STAGES) stages = MAX_STAGES;
+  cudaError_t e;
+  const int km = k_max <= 8 ? 8 : (k_max <= 16 ? 16 : 32);
+  if (S == 1 && km == 8) e = launch_topk_km<1, 8>(grid, cps, mx, mw, T, H, E, E16, stages, logits_out, kpt, k_uniform, k_max, topk_idx, topk_w, counts, count_stride, s);
+  else if (S == 1 && km == 16) e = launch_topk_km<1, 16>(grid, cps, mx, mw, T, H, E, E16, stages, logits_out, kpt, k_uniform, k_max, topk_idx, topk_w, counts, count_stride, s);
+  else if (S == 1) e = launch_topk_km<1, 32>(grid, cps, mx, mw, T, H, E, E16, stages, logits_out, kpt, k_uniform, k_max, topk_idx, topk_w, counts, count_stride, s);
+  else if (km == 8) e = launch_topk_km<3, 8>(grid, cps, mx, mw, T, H, E, E16, stages, logits_out, kpt, k_uniform, k_max, topk_idx, topk_w, counts, count_stride, s);
+  else if (km == 16) e = launch_topk_km<3, 16>(grid, cps, mx, mw, T, H, E, E16, stages, logits_out, kpt, k_uniform, k_max, topk_idx, topk_w, counts, count_stride, s);
+  else e = launch_topk_km<3, 32>(grid, cps, mx, mw, T, H, E, E16, stages, logits_out, kpt, k_uniform, k_max, topk_idx, topk_w, counts, count_stride, s);
   if (e != cudaSuccess) return e;
   count_launches(1);
   return cudaGetLastError();
