@@ -207,12 +207,16 @@ route_tc_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_constant
 // ---------------------------------------------------------------------------
 // Router GEMM and top-k in one kernel (E16 * S <= 256 accumulator columns,
 // k_max <= KM): one CTA per 128-token tile reads the whole contraction over H
-// (no K slices, no logits in memory), and each epilogue thread owns one token
-// row of the accumulator: it adds the weight parts' columns into logits, keeps
-// the KM best as (key, index) in a sorted register list, then writes the k_t
-// picks, their gates and the tile's pair counts.  The k-blocks are visited
-// from a per-tile starting block (tile index mod the block count), so the
-// tiles do not all read the same weight lines at the same moment.
+// (no K slices, no logits in memory).  The epilogue has G groups of four warps;
+// a thread of group g owns one token row of the accumulator and the g-th of G
+// contiguous column ranges: it adds the weight parts' columns into logits and
+// keeps the KM best as (key, index) in a sorted register list.  Groups 1..G-1
+// leave their lists in shared memory; group 0 merges them in column order
+// (so equal scores keep the lower expert first) and writes the k_t picks,
+// their gates and the tile's pair counts.  (With one group the selection ran
+// about 10K dependent instructions per warp and set the kernel's time.)  The
+// k-blocks are visited from a per-tile starting block (tile index mod the
+// block count), so the tiles do not all read the same weight lines at once.
 // ---------------------------------------------------------------------------
 
 // Order-preserving 32-bit key of an fp32 score: larger key = larger score; -0.0
@@ -246,8 +250,8 @@ __device__ __forceinline__ void list_insert(uint32_t (&keys)[KM], int (&ids)[KM]
   }
 }
 
-template <int S, int KM, int CPS>
-__global__ void __launch_bounds__(THREADS, CPS)
+template <int S, int KM, int CPS, int G>
+__global__ void __launch_bounds__(64 + 128 * G, CPS)
 route_topk_tc_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_constant__ CUtensorMap map_w, int T,
                      int H, int E, int E16, int stages, float* __restrict__ logits_out,
                      const int32_t* __restrict__ k_per_token, int k_uniform, int k_max,
@@ -280,7 +284,7 @@ route_topk_tc_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_con
     prefetch_map(&map_x);
     prefetch_map(&map_w);
   }
-  for (int e = threadIdx.x; e < 256; e += THREADS) hist[e] = 0;
+  for (int e = threadIdx.x; e < 256; e += blockDim.x) hist[e] = 0;
   if (warp == 1) tmem_alloc(&sh.tmem_base, TMEM_COLS);
   fence_before();
   __syncthreads();
@@ -324,24 +328,31 @@ route_topk_tc_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_con
       commit(&sh.done);
       mbar_drain(&sh.done, 0, &g_err);
     }
-  } else {  // epilogue: thread = token row t of the tile
-    const int q = warp & 3;
-    const int t = t0 + q * 32 + lane;
+  } else {  // epilogue: thread = token row t of the tile, column range g
+    const int q = warp & 3;            // TMEM lane quarter of this warp
+    const int g = (warp - 2) / 4;      // column group
+    const int r = q * 32 + lane;       // tile row
+    const int t = t0 + r;
+    const int nch = E16 / 16;
+    const int c_lo = (g * nch / G) * 16, c_hi = ((g + 1) * nch / G) * 16;
+    // groups 1..G-1 hand their lists over in the (by then idle) operand ring
+    uint32_t* mkeys = reinterpret_cast<uint32_t*>(ring);
+    int* mids = reinterpret_cast<int*>(ring + (size_t)(G > 1 ? G - 1 : 1) * BM * KM * 4);
+    uint32_t keys[KM];
+    int ids[KM];
+#pragma unroll
+    for (int j = 0; j < KM; ++j) {
+      keys[j] = 0u;
+      ids[j] = -1;
+    }
+    bool nonfinite = false;
     int ok = 1;
     if (lane == 0) ok = mbar_wait(&sh.tfull, 0, abort_flag, &g_err);
     ok = __shfl_sync(0xffffffffu, ok, 0);
     if (ok) {
       fence_after();
       const uint32_t trow = tmem + ((uint32_t)(q * 32) << 16);
-      uint32_t keys[KM];
-      int ids[KM];
-#pragma unroll
-      for (int j = 0; j < KM; ++j) {
-        keys[j] = 0u;
-        ids[j] = -1;
-      }
-      bool nonfinite = false;
-      for (int c = 0; c < E16; c += 16) {
+      for (int c = c_lo; c < c_hi; c += 16) {
         uint32_t v0[16], v1[16], v2[16];
         tmem_ld16(trow + c, v0);
         if (S == 3) {
@@ -364,8 +375,27 @@ route_topk_tc_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_con
           }
         }
       }
-      if (t < T) {
-        if (nonfinite) atomicOr(&g_err, SEMMOE_DEVERR_NONFINITE);
+      if (G > 1 && g > 0) {
+#pragma unroll
+        for (int j = 0; j < KM; ++j) {
+          mkeys[((size_t)(g - 1) * BM + r) * KM + j] = keys[j];
+          mids[((size_t)(g - 1) * BM + r) * KM + j] = ids[j];
+        }
+      }
+    }
+    if (nonfinite && t < T) atomicOr(&g_err, SEMMOE_DEVERR_NONFINITE);
+    if (G > 1) asm volatile("bar.sync 1, %0;" ::"r"(128 * G) : "memory");
+    if (g == 0) {
+      if (ok) {
+        for (int h = 1; h < G; ++h) {  // later column ranges: equal keys stay behind
+          for (int j = 0; j < KM; ++j) {
+            const uint32_t k2 = mkeys[((size_t)(h - 1) * BM + r) * KM + j];
+            if (!(k2 > keys[KM - 1])) break;  // the rest of that sorted list is no better
+            list_insert<KM>(keys, ids, k2, mids[((size_t)(h - 1) * BM + r) * KM + j]);
+          }
+        }
+      }
+      if (ok && t < T) {
         int kt = k_per_token != nullptr ? k_per_token[t] : k_uniform;
         if (kt < 1 || kt > k_max) {
           atomicOr(&g_err, SEMMOE_DEVERR_K);
@@ -380,31 +410,30 @@ route_topk_tc_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_con
         for (int j = 0; j < KM; ++j) {
           if (j < k_max) {
             int e = -1;
-            float g = 0.f;
+            float gw = 0.f;
             if (j < kt) {
               if (ids[j] >= 0) {
                 e = ids[j];
-                g = expf(key_score(keys[j]) - m) / den;
+                gw = expf(key_score(keys[j]) - m) / den;
                 atomicAdd(&hist[e], 1);
               } else {
                 atomicOr(&g_err, SEMMOE_DEVERR_NONFINITE);  // fewer than k_t scores
               }
             }
             topk_idx[(size_t)t * k_max + j] = e;
-            topk_w[(size_t)t * k_max + j] = g;
+            topk_w[(size_t)t * k_max + j] = gw;
           }
         }
       }
-    }
-    // the tile's pair counts (the tile is chunk blockIdx.x of the count table)
-    asm volatile("bar.sync 1, 128;" ::: "memory");
-    if (counts != nullptr) {
-      const int et = threadIdx.x - 64;
-      for (int e = et; e < E; e += 128) counts[(size_t)e * count_stride + blockIdx.x] = hist[e];
-      if (blockIdx.x == 0) {  // entries past the last chunk are 0
-        const int nchunk = (int)gridDim.x;
-        for (int i = et; i < E * (count_stride - nchunk); i += 128)
-          counts[(size_t)(i / (count_stride - nchunk)) * count_stride + nchunk + i % (count_stride - nchunk)] = 0;
+      // the tile's pair counts (the tile is chunk blockIdx.x of the count table)
+      asm volatile("bar.sync 2, 128;" ::: "memory");
+      if (counts != nullptr) {
+        const int et = threadIdx.x - 64;  // group 0 is threads 64 .. 191
+        for (int e = et; e < E; e += 128) counts[(size_t)e * count_stride + blockIdx.x] = hist[e];
+        if (blockIdx.x == 0) {  // entries past the last chunk are 0
+          const int nchunk = (int)gridDim.x, padn = count_stride - nchunk;
+          for (int i = et; i < E * padn; i += 128) counts[(size_t)(i / padn) * count_stride + nchunk + i % padn] = 0;
+        }
       }
     }
   }
@@ -418,14 +447,17 @@ route_topk_tc_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_con
   }
 }
 
+// Epilogue column groups: four with one CTA per SM and k_max <= 16 (the lists'
+// registers allow it), else fewer.
 template <int S, int KM, int CPS>
 static cudaError_t launch_topk_k(int grid, const CUtensorMap& mx, const CUtensorMap& mw, int T, int H, int E, int E16,
                                  int stages, float* logits_out, const int32_t* kpt, int k_uniform, int k_max,
                                  int32_t* topk_idx, float* topk_w, int32_t* counts, int count_stride, cudaStream_t s) {
+  constexpr int G = CPS == 1 ? (KM <= 16 ? 4 : 2) : 1;
   static std::atomic<unsigned long long> smem_set{0};
-  cudaError_t e = ensure_smem_limit(route_topk_tc_kernel<S, KM, CPS>, (int)smem_bytes(CPS), smem_set);
+  cudaError_t e = ensure_smem_limit(route_topk_tc_kernel<S, KM, CPS, G>, (int)smem_bytes(CPS), smem_set);
   if (e != cudaSuccess) return e;
-  route_topk_tc_kernel<S, KM, CPS><<<grid, THREADS, smem_bytes(CPS), s>>>(
+  route_topk_tc_kernel<S, KM, CPS, G><<<grid, 64 + 128 * G, smem_bytes(CPS), s>>>(
       mx, mw, T, H, E, E16, stages, logits_out, kpt, k_uniform, k_max, topk_idx, topk_w, counts, count_stride);
   return cudaSuccess;
 }
