@@ -269,7 +269,8 @@ int semmoe_remote_count(const int32_t* topk_idx, const int32_t* pred_rank,
  *
  * Kernels: each CTA takes a run of tokens, derives its first row in every
  * bucket from the count table, ranks its own pairs stably, writes both maps
- * and copies its tokens' rows -- one pass, no CTA waiting on another.
+ * and copies its tokens' rows (copies of 256 MB and more run as a second
+ * kernel) -- no CTA waiting on another.
  */
 size_t semmoe_permute_workspace_size(int T, int k_max, int E);
 int semmoe_permute(const int32_t* topk_idx, const int32_t* expert_rank,

@@ -753,3 +753,33 @@ def test_router_with_top_k_in_the_gemm_epilogue(T, H, E, k_max, wd, per_token):
     np.testing.assert_array_equal(np_(idx), ref_idx)
     np.testing.assert_allclose(np_(gw), ref_w, rtol=0, atol=GATE_ATOL)
     np.testing.assert_array_equal(np_(counts).reshape(E, stride), _chunk_histogram(ref_idx, k, E, stride))
+
+
+@pytest.mark.parametrize("T,E,k_max,H,fused_copy", [(3000, 64, 6, 2048, True), (16384, 128, 8, 1024, False)])
+def test_permute_copy_inside_and_as_its_own_kernel(T, E, k_max, H, fused_copy):
+    """The rows are copied inside the ranking kernel below 256 MB of rows and by
+    a copy kernel of its own above; both give the oracle's index tables and
+    x_perm[q] = x[sorted_to_pair[q] / k_max] exactly (the rows checked on the
+    GPU against a plain gather through the oracle-equal map)."""
+    a = abi()
+    rng = np.random.default_rng(T)
+    P = T * k_max
+    assert (P * H * 2 >= 256 << 20) == (not fused_copy)
+    idx, k = _route_random(rng, T, E, k_max, per_token=False)
+    R = 8
+    er = rng.permutation(np.arange(E) % R).astype(np.int32)
+    x = torch.randn(T, H, device="cuda").to(torch.bfloat16)
+    o = dict(expert_offsets=torch.empty(E + 1, **i32), rank_offsets=torch.empty(R + 1, **i32),
+             phys_to_expert=torch.empty(E, **i32), expert_counts=torch.empty(E, **i32),
+             sorted_to_pair=torch.empty(P, **i32), pair_to_sorted=torch.empty(T * k_max, **i32),
+             x_perm=torch.zeros(P, H, dtype=torch.bfloat16, device="cuda"))
+    ws = torch.empty(a.semmoe_permute_workspace_size(T, k_max, E), dtype=torch.uint8, device="cuda")
+    a.semmoe_permute(torch.from_numpy(idx).cuda(), torch.from_numpy(er).cuda(), x, T, H, E, R, k_max, P,
+                     o["expert_offsets"], o["rank_offsets"], o["phys_to_expert"], o["expert_counts"],
+                     o["sorted_to_pair"], o["pair_to_sorted"], o["x_perm"], ws)
+    assert a.semmoe_check_errors() == 0
+    ref = oracle.permute(idx, k, er, R)
+    for key, v in ref.items():
+        np.testing.assert_array_equal(np_(o[key]), v, err_msg=key)
+    want = x.index_select(0, (o["sorted_to_pair"] // k_max).long())
+    assert torch.equal(o["x_perm"], want)

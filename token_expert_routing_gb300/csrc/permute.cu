@@ -8,10 +8,12 @@
 // among the tokens of chunk c: the router writes it as it picks the experts
 // (128-token chunks, semmoe_route's pair_counts), or, when the caller has none,
 // perm_count_kernel makes it (one CTA per chunk).  perm_rank_copy_kernel then
-// does the rest in one pass: each CTA derives its first row in every bucket
-// from the table, ranks its own tokens' pairs stably (warp match + per-warp
-// bucket counts), writes both maps, and copies its tokens' x rows to their
-// sorted rows (one warp per token, 16-byte vectors).
+// does the rest: each CTA derives its first row in every bucket from the table,
+// ranks its own tokens' pairs stably (warp match + per-warp bucket counts),
+// writes both maps, and copies its tokens' x rows to their sorted rows (bulk
+// copies through shared memory) -- or, for copies of 256 MB and more,
+// perm_copy_kernel does the copy as a kernel of its own (one warp per token,
+// 16-byte vectors, more warps per SM).
 #include <cuda.h>
 
 #include <mutex>
@@ -108,13 +110,71 @@ perm_count_kernel(const int32_t* __restrict__ topk_idx, int T, int k_max, int E,
   for (int e = threadIdx.x; e < E; e += kHistThreads) counts[(size_t)e * ncp + blockIdx.x] = h[e];
 }
 
-// Row gather: each warp owns a 4 KB shared-memory slot.  For each of its
-// tokens, lane 0 bulk-loads the row (a segment of up to 4 KB at a time) into the
-// slot and bulk-stores it to the token's k_t sorted rows, so the row is read
-// from HBM once and every byte moves by the copy engine, not through registers
-// (a register-staged warp copy stalled on the memory-instruction queues at 40%
-// warp occupancy: 111 us against 104 us for this form at the Qwen3 shape).
+// Row gather inside the ranking kernel: each warp owns a 4 KB shared-memory
+// slot.  For each of its tokens, lane 0 bulk-loads the row (a segment of up to
+// 4 KB at a time) into the slot and bulk-stores it to the token's k_t sorted
+// rows, so the row is read from HBM once and moves by the copy engine.
 constexpr int kSlotBytes = 4096;
+
+// One warp writes token t's activation row x[t] to its live slots' sorted rows
+// pair_to_sorted[t * k_max + j]: the row is read once, in segments of up to
+// 4 KB held in registers, and each segment is written to the k_t rows.
+// (Walking the sorted rows instead re-reads each x row k_t times, far apart in
+// time, and the row writes push those reads out of L2.)
+constexpr int kSegVec = 8;  // 16-byte vectors per lane per segment: 32 x 8 x 16 B = 4 KB
+
+__device__ __forceinline__ void copy_token_row(const unsigned char* __restrict__ x, const int32_t* slots, int t,
+                                               int k_max, int P, int row_bytes, unsigned char* __restrict__ x_perm) {
+  const int lane = threadIdx.x % 32;
+  const int n16 = row_bytes / 16;
+  const int kk = k_max < 32 ? k_max : 32;
+  int q_l = -1;
+  if (lane < kk) {
+    q_l = slots[lane];
+    if (q_l >= P) { flag(SEMMOE_DEVERR_PAIRS); q_l = -1; }
+  }
+  const uint4* src = reinterpret_cast<const uint4*>(x + (size_t)t * row_bytes);
+  for (int seg = 0; seg < n16; seg += 32 * kSegVec) {
+    uint4 v[kSegVec];
+#pragma unroll
+    for (int u = 0; u < kSegVec; ++u) {
+      const int c = seg + u * 32 + lane;
+      if (c < n16) v[u] = src[c];
+    }
+    for (int j = 0; j < kk; ++j) {
+      const int q = __shfl_sync(0xffffffffu, q_l, j);
+      if (q < 0) continue;
+      uint4* dst = reinterpret_cast<uint4*>(x_perm + (size_t)q * row_bytes);
+#pragma unroll
+      for (int u = 0; u < kSegVec; ++u) {
+        const int c = seg + u * 32 + lane;
+        if (c < n16) dst[c] = v[u];
+      }
+    }
+    for (int j = 32; j < k_max; ++j) {  // budgets above 32 experts: read the slot directly
+      const int q = slots[j];
+      if (q < 0) continue;
+      if (q >= P) { if (lane == 0) flag(SEMMOE_DEVERR_PAIRS); continue; }
+      uint4* dst = reinterpret_cast<uint4*>(x_perm + (size_t)q * row_bytes);
+#pragma unroll
+      for (int u = 0; u < kSegVec; ++u) {
+        const int c = seg + u * 32 + lane;
+        if (c < n16) dst[c] = v[u];
+      }
+    }
+  }
+}
+
+
+// The row gather as a kernel of its own (large copies): one warp per token,
+// 256-thread CTAs, up to 16 per SM.
+__global__ void __launch_bounds__(kHistThreads)
+perm_copy_kernel(const unsigned char* __restrict__ x, const int32_t* __restrict__ pair_to_sorted, int T, int k_max,
+                 int P, int row_bytes, unsigned char* __restrict__ x_perm) {
+  const int warp = threadIdx.x / 32;
+  for (int t = blockIdx.x * 8 + warp; t < T; t += gridDim.x * 8)
+    copy_token_row(x, pair_to_sorted + (size_t)t * k_max, t, k_max, P, row_bytes, x_perm);
+}
 
 // The stable counting sort and the row gather in one pass.  CTA b takes the
 // tokens [t0, t1) = [b * tpc, (b + 1) * tpc) and
@@ -368,7 +428,14 @@ cudaError_t launch_permute(const int32_t* topk_idx, const int32_t* expert_rank, 
   if (tpc < 1) tpc = 1;
   const int grid = T > 0 ? (T + tpc - 1) / tpc : 1;
   const int row_bytes = H * (dtype == SEMMOE_BF16 ? 2 : 4);
-  const bool copy = x != nullptr && x_perm != nullptr;
+  // Where the rows are copied: inside the ranking kernel for copies under
+  // 256 MB, by a copy kernel of its own (more warps per SM) above that.
+  // Measured per call with L2 flushed: DeepSeek prefill (101 MB) 29.3 us inside
+  // against 35.5 us separate; Qwen3 (537 MB) 119.4 against 114.3; MoE-Prism
+  // (604 MB) 136.8 against 128.7.
+  const bool any_copy = x != nullptr && x_perm != nullptr && P > 0;
+  const bool separate = any_copy && (long long)P * row_bytes >= (256LL << 20);
+  const bool copy = any_copy && !separate;
   const size_t dyn = copy ? (size_t)kWarps * kSlotBytes : 0;
   static std::atomic<unsigned long long> smem_set{0};
   cudaError_t e = ensure_smem_limit(perm_rank_copy_kernel, (int)(kWarps * kSlotBytes), smem_set);
@@ -376,9 +443,16 @@ cudaError_t launch_permute(const int32_t* topk_idx, const int32_t* expert_rank, 
   perm_rank_copy_kernel<<<grid, kThreads, dyn, s>>>(
       topk_idx, expert_rank, counts, nc, padded_chunks(nc), chunk, T, k_max, E, R, P, tpc, expert_offsets,
       rank_offsets, phys_to_expert, expert_counts, sorted_to_pair, pair_to_sorted,
-      x_perm != nullptr ? static_cast<const unsigned char*>(x) : nullptr, row_bytes,
-      static_cast<unsigned char*>(x_perm));
+      copy ? static_cast<const unsigned char*>(x) : nullptr, row_bytes, static_cast<unsigned char*>(x_perm));
   count_launches(1);
+  if (separate) {
+    int blocks = (T + 7) / 8;
+    const int cap = sm_count() * 16;
+    if (blocks > cap) blocks = cap;
+    perm_copy_kernel<<<blocks, kHistThreads, 0, s>>>(static_cast<const unsigned char*>(x), pair_to_sorted, T, k_max,
+                                                     P, row_bytes, static_cast<unsigned char*>(x_perm));
+    count_launches(1);
+  }
   return cudaGetLastError();
 }
 
