@@ -398,6 +398,48 @@ int semmoe_grouped_ffn_form(const void* x, const int32_t* sorted_to_pair, int k_
                             size_t ws_bytes, int form1, int form2, void* stream);
 
 /*
+ * semmoe_grouped_ffn_combine -- semmoe_grouped_ffn with the combine folded
+ * into GEMM2: the on-device Shuffled-Allgather ([SP] de §2 B, ja §2.2 B)
+ * returning each expert row to its token's position as GEMM2 produces it, so
+ * no y_perm is written or read back.  The expert rows add into their token's
+ * row the way MoE-Prism's sub-expert outputs add into their parent's ([MP]
+ * §2 A).  semmoe_combine_finish then adds the shared experts and rounds:
+ *
+ *   acc[t] = sum_{j<k_t} topk_w[t,j] * y_j   (fp32; y_j = GEMM2 row of pair t*k_max+j)
+ *   out[t] = y_shared[t] + acc[t]            (semmoe_combine_finish, rounded to bf16)
+ *
+ * This call zeroes acc, runs GEMM1 and then GEMM2, whose epilogue multiplies
+ * each fp32 row by its gate and adds it into acc (float4 atomic adds).
+ * Differences from semmoe_grouped_ffn + semmoe_combine: y is not rounded to
+ * bf16 before the weighted sum, and the sum's order depends on scheduling, so
+ * results are not bit-reproducible from run to run (they stay within the bf16
+ * tolerance of the layer's definition).
+ *
+ * x              [device] x_perm [P,H] (x_rows_are_tokens = 0), or the token rows
+ *                x [T,H] gathered through sorted_to_pair (x_rows_are_tokens = 1,
+ *                as semmoe_grouped_ffn_gather)
+ * sorted_to_pair [device] [P] int32 (from semmoe_permute); a pair naming no
+ *                token sets SEMMOE_DEVERR_PAIRS and its row is dropped
+ * topk_w         [device] [T,k_max] fp32 gates, indexed by pair id
+ * acc            [device] [T,H] fp32 out (16-byte aligned)
+ * ws             [device] workspace of semmoe_grouped_ffn_workspace_size(P, I, dtype)
+ * dtype must be SEMMOE_BF16 (tensor cores), else SEMMOE_ERR_UNSUPPORTED.
+ * Other arguments, limits and device checks as semmoe_grouped_ffn.
+ */
+int semmoe_grouped_ffn_combine(const void* x, int x_rows_are_tokens, const int32_t* sorted_to_pair, int k_max,
+                               int T, const int32_t* expert_offsets, const int32_t* phys_to_expert,
+                               const void* w13, const void* w2, const float* topk_w, int dtype, int P, int E,
+                               int H, int I, float* acc, void* ws, size_t ws_bytes, void* stream);
+
+/*
+ * semmoe_combine_finish -- out = y_shared + acc, rounded to dtype (bf16 only):
+ * the last step after semmoe_grouped_ffn_combine.
+ * acc [device] [T,H] fp32; y_shared [device] [T,H] or NULL; out [device] [T,H].
+ * H % 8 == 0; pointers 16-byte aligned.
+ */
+int semmoe_combine_finish(const float* acc, const void* y_shared, int dtype, int T, int H, void* out, void* stream);
+
+/*
  * semmoe_shared_ffn -- the shared experts (applied to every token with gate 1,
  * their weights concatenated along the intermediate dimension I_s):
  *   y_shared = (silu(x Ws1^T) * (x Ws3^T)) Ws2^T.

@@ -34,14 +34,15 @@ def np_(t) -> np.ndarray:
     return t.numpy()
 
 
-def run_gpu(d, logits_in=None, fused_gather=False):
+def run_gpu(d, logits_in=None, fused_gather=False, fused_combine=False):
     """One layer forward of inputs ``d`` (from workloads.make_inputs) on cuda:0;
     fused_gather=True lets GEMM1 gather x rows instead of the permute writing
-    x_perm."""
+    x_perm; fused_combine=True lets GEMM2 add its rows into the token order
+    instead of writing y_perm."""
     from token_expert_routing_gb300 import MoELayer, _abi
     spec = d["spec"]
     layer = MoELayer(d["w_router"], d["w13"], d["w2"], d["expert_rank"], d["lut"], spec.R, spec.k_max,
-                     d["ws13"], d["ws2"], fused_gather=fused_gather)
+                     d["ws13"], d["ws2"], fused_gather=fused_gather, fused_combine=fused_combine)
     x = d["x"].cuda()
     ids = d["token_ids"].cuda()
     P = int(d["k_per_token"].sum())
@@ -86,7 +87,8 @@ def check_layer_full(d, res, P):
         np.testing.assert_array_equal(np_(res.x_perm), x_perm)
     y_perm = oracle.grouped_ffn(x_perm, perm["expert_offsets"], perm["phys_to_expert"], d["w13"], d["w2"],
                                 spec.dtype)
-    assert max_rel(np_(res.y_perm), y_perm) < TOL[spec.dtype]
+    if res.y_perm is not None:
+        assert max_rel(np_(res.y_perm), y_perm) < TOL[spec.dtype]
     y_shared = None
     if d["ws13"] is not None:
         y_shared = oracle.shared_ffn(d["x"], d["ws13"], d["ws2"], spec.dtype)
@@ -111,26 +113,18 @@ def check_layer_sampled(d, res, P, n_tokens=96, seed=0):
     p2s = perm["pair_to_sorted"]
     pairs = [(n, int(t), j, int(idx[t, j]), int(p2s[t * spec.k_max + j]))
              for n, t in enumerate(toks) for j in range(int(k[t]))]
-    qs = torch.as_tensor([q for *_, q in pairs], device=res.y_perm.device)
-    gpu_y = np_(res.y_perm[qs])
+    qs = torch.as_tensor([q for *_, q in pairs], device=res.out.device)
     if res.x_perm is not None:
         np.testing.assert_array_equal(np_(res.x_perm[qs]), np_(x[torch.as_tensor([t for _, t, *_ in pairs])]))
-    ref_y = np.zeros_like(gpu_y)
+    ref_y = np.zeros((len(pairs), spec.H))
     for e in sorted({e for *_, e, _ in pairs}):          # one oracle call per expert
         rows = [i for i, pr in enumerate(pairs) if pr[3] == e]
         xs = x[torch.as_tensor([pairs[i][1] for i in rows])]
         _, y = oracle.expert_ffn(xs, d["w13"][e], d["w2"][e], spec.dtype)
         ref_y[rows] = y
-    assert max_rel(gpu_y, ref_y) < TOL[spec.dtype]
-    # the last sorted row of every expert group: the ragged tail of its last tile
-    off, pe, s2p = perm["expert_offsets"], perm["phys_to_expert"], perm["sorted_to_pair"]
-    tails = [(int(off[b + 1]) - 1, int(pe[b])) for b in range(pe.shape[0]) if off[b + 1] > off[b]]
-    gpu_tail = np_(res.y_perm[torch.as_tensor([q for q, _ in tails], device=res.y_perm.device)])
-    ref_tail = np.zeros_like(gpu_tail)
-    for i, (q, e) in enumerate(tails):
-        t = int(s2p[q]) // spec.k_max
-        _, ref_tail[i:i + 1] = oracle.expert_ffn(x[t:t + 1], d["w13"][e], d["w2"][e], spec.dtype)
-    assert max_rel(gpu_tail, ref_tail) < TOL[spec.dtype]
+    if res.y_perm is not None:       # GEMM2 wrote y_perm (else it added its rows into the output)
+        assert max_rel(np_(res.y_perm[qs]), ref_y) < TOL[spec.dtype]
+        check_group_tails(d, res, perm)
     acc = np.zeros((len(toks), spec.H))
     if d["ws13"] is not None:
         ys = oracle.shared_ffn(x[torch.as_tensor(toks)], d["ws13"], d["ws2"], spec.dtype)
@@ -140,3 +134,18 @@ def check_layer_sampled(d, res, P, n_tokens=96, seed=0):
     for i, (n, t, j, e, q) in enumerate(pairs):            # combine in slot order
         acc[n] += w[t, j] * ref_y[i]
     assert max_rel(gpu_out, oracle.round_to(acc, spec.dtype)) < TOL[spec.dtype]
+
+
+def check_group_tails(d, res, perm):
+    """The FFN output of the last sorted row of every expert group (the ragged
+    tail of its last tile), recomputed by the oracle row by row."""
+    spec = d["spec"]
+    x = d["x"]
+    off, pe, s2p = perm["expert_offsets"], perm["phys_to_expert"], perm["sorted_to_pair"]
+    tails = [(int(off[b + 1]) - 1, int(pe[b])) for b in range(pe.shape[0]) if off[b + 1] > off[b]]
+    gpu_tail = np_(res.y_perm[torch.as_tensor([q for q, _ in tails], device=res.y_perm.device)])
+    ref_tail = np.zeros_like(gpu_tail)
+    for i, (q, e) in enumerate(tails):
+        t = int(s2p[q]) // spec.k_max
+        _, ref_tail[i:i + 1] = oracle.expert_ffn(x[t:t + 1], d["w13"][e], d["w2"][e], spec.dtype)
+    assert max_rel(gpu_tail, ref_tail) < TOL[spec.dtype]

@@ -783,3 +783,83 @@ def test_permute_copy_inside_and_as_its_own_kernel(T, E, k_max, H, fused_copy):
         np.testing.assert_array_equal(np_(o[key]), v, err_msg=key)
     want = x.index_select(0, (o["sorted_to_pair"] // k_max).long())
     assert torch.equal(o["x_perm"], want)
+
+
+@pytest.mark.parametrize("T,E,k_max,H,I,gathered,shared", [
+    (500, 16, 4, 256, 640, False, True),      # groups of ~125 rows: GEMM2 in single CTAs
+    (8000, 16, 4, 256, 640, True, False),     # groups of ~2000 rows, I >= 512: GEMM2 in 2-SM pairs
+    (700, 8, 4, 200, 96, True, True),         # H = 200: a partial last k-block and output tile
+    (3000, 64, 6, 512, 352, False, False)])
+def test_grouped_ffn_with_folded_combine_matches_oracle(T, E, k_max, H, I, gathered, shared):
+    """semmoe_grouped_ffn_combine + semmoe_combine_finish (GEMM2 adding its
+    gate-weighted rows into the token order) against the oracle's grouped FFN
+    followed by its combine, within the bf16 tolerance; per-token budgets leave
+    padding slots; rows from x_perm or gathered from x."""
+    a = abi()
+    rng = np.random.default_rng(T + I)
+    idx, k = _route_random(rng, T, E, k_max)
+    _, w = oracle.topk_route(rng.standard_normal((T, E)), k, k_max)   # some gates (values only matter)
+    er = (np.arange(E) % 4).astype(np.int32)
+    P = int(k.sum())
+    x = torch.from_numpy(rng.standard_normal((T, H)).astype(np.float32)).to(torch.bfloat16).cuda()
+    w13 = torch.from_numpy((rng.standard_normal((E, 2 * I, H)) / np.sqrt(H)).astype(np.float32)).to(torch.bfloat16).cuda()
+    w2 = torch.from_numpy((rng.standard_normal((E, H, I)) / np.sqrt(I)).astype(np.float32)).to(torch.bfloat16).cuda()
+    ys = torch.from_numpy(rng.standard_normal((T, H)).astype(np.float32)).to(torch.bfloat16).cuda() if shared else None
+    eo, ro = torch.empty(E + 1, **i32), torch.empty(5, **i32)
+    p2e, ec = torch.empty(E, **i32), torch.empty(E, **i32)
+    s2p, p2s = torch.empty(P, **i32), torch.empty(T * k_max, **i32)
+    xp = torch.empty(P, H, dtype=torch.bfloat16, device="cuda")
+    ws = torch.empty(a.semmoe_permute_workspace_size(T, k_max, E), dtype=torch.uint8, device="cuda")
+    a.semmoe_permute(torch.from_numpy(idx).cuda(), torch.from_numpy(er).cuda(), x, T, H, E, 4, k_max, P, eo, ro,
+                     p2e, ec, s2p, p2s, xp, ws)
+    fws = torch.empty(a.semmoe_grouped_ffn_workspace_size(P, I, 1), dtype=torch.uint8, device="cuda")
+    acc = torch.full((T, H), 123.0, dtype=torch.float32, device="cuda")       # zeroed by the call
+    out = torch.empty(T, H, dtype=torch.bfloat16, device="cuda")
+    tw = torch.from_numpy(w.astype(np.float32)).cuda()
+    a.semmoe_grouped_ffn_combine(x if gathered else xp, gathered, s2p, k_max, T, eo, p2e, w13, w2, tw, P, E, H, I,
+                                 acc, fws)
+    a.semmoe_combine_finish(acc, ys, T, H, out)
+    assert a.semmoe_check_errors() == 0
+    perm = oracle.permute(idx, k, er, 4, x.cpu())
+    y_ref = oracle.grouped_ffn(perm["x_perm"], perm["expert_offsets"], perm["phys_to_expert"],
+                               w13.cpu().to(torch.float64).numpy(), w2.cpu().to(torch.float64).numpy(), "bf16")
+    ref = oracle.combine(y_ref, perm["pair_to_sorted"], w, k, "bf16", None if ys is None else np_(ys))
+    assert max_rel(np_(out), ref) < TOL["bf16"]
+
+
+def test_folded_combine_flags_a_bad_pair_and_drops_its_row():
+    """A sorted_to_pair entry naming no token sets SEMMOE_DEVERR_PAIRS; its row
+    is left out of the sums and every token's output is otherwise the oracle's
+    with that pair's slot counted as padding."""
+    a = abi()
+    rng = np.random.default_rng(31)
+    T, E, k_max, H, I = 300, 4, 2, 128, 128
+    P = T * k_max
+    x = torch.from_numpy(rng.standard_normal((T, H)).astype(np.float32)).to(torch.bfloat16).cuda()
+    w13 = torch.from_numpy((rng.standard_normal((E, 2 * I, H)) / np.sqrt(H)).astype(np.float32)).to(torch.bfloat16).cuda()
+    w2 = torch.from_numpy((rng.standard_normal((E, H, I)) / np.sqrt(I)).astype(np.float32)).to(torch.bfloat16).cuda()
+    eo = torch.tensor([0, 150, 300, 450, 600], **i32)
+    p2e = torch.tensor([0, 1, 2, 3], **i32)
+    s2p_np = rng.permutation(P).astype(np.int32)
+    bad_q = 17
+    dropped = int(s2p_np[bad_q])
+    s2p_np[bad_q] = -3
+    w = rng.random((T, k_max)).astype(np.float32)
+    fws = torch.empty(a.semmoe_grouped_ffn_workspace_size(P, I, 1), dtype=torch.uint8, device="cuda")
+    acc = torch.empty(T, H, dtype=torch.float32, device="cuda")
+    out = torch.empty(T, H, dtype=torch.bfloat16, device="cuda")
+    a.semmoe_grouped_ffn_combine(x, True, torch.from_numpy(s2p_np).cuda(), k_max, T, eo, p2e, w13, w2,
+                                 torch.from_numpy(w).cuda(), P, E, H, I, acc, fws)
+    a.semmoe_combine_finish(acc, None, T, H, out)
+    with pytest.raises(a.SemMoEError) as ei:
+        a.semmoe_check_errors()
+    assert ei.value.bits & a.SEMMOE_DEVERR_PAIRS
+    # oracle: the sorted rows' pairs, with the bad row's pair dropped
+    x_perm = np_(x)[np.where(s2p_np >= 0, s2p_np, 0) // k_max]
+    y_ref = oracle.grouped_ffn(x_perm, eo.cpu(), p2e.cpu(), w13.cpu().to(torch.float64).numpy(),
+                               w2.cpu().to(torch.float64).numpy(), "bf16")
+    p2s = np.full(T * k_max, -1, dtype=np.int64)
+    p2s[s2p_np[s2p_np >= 0]] = np.nonzero(s2p_np >= 0)[0]
+    assert p2s[dropped] == -1
+    ref = oracle.combine(y_ref, p2s, w.astype(np.float64), np.full(T, k_max), "bf16")
+    assert max_rel(np_(out), ref) < TOL["bf16"]

@@ -167,3 +167,26 @@ def test_layer_empty_batch():
     res = layer.forward(x, d["token_ids"][:0].cuda(), None, s.k, 0)
     assert _abi.semmoe_check_errors() == 0
     assert tuple(res.out.shape) == (0, s.H)
+
+
+FOLDED = [s for s in SMALL if not s[0].startswith("tiny_fp32")]   # bf16 experts
+
+
+@pytest.mark.parametrize("fused_gather", [True, False], ids=["gather", "x_perm"])
+@pytest.mark.parametrize("name,over", FOLDED, ids=[f"{n}-{i}" for i, (n, _) in enumerate(FOLDED)])
+def test_layer_small_folded_combine(name, over, fused_gather):
+    """The layer with GEMM2 adding its gate-weighted rows straight into the
+    token order (no y_perm), against the oracle in full: every integer output
+    bit-exact, the output within the bf16 tolerance."""
+    d = wl.make_inputs(wl.scaled(name, **over))
+    res, P = run_gpu(d, fused_gather=fused_gather, fused_combine=True)
+    assert res.y_perm is None
+    check_layer_full(d, res, P)
+
+
+@pytest.mark.parametrize("name", ["qwen3_30b_a3b_T16384", "prism_subexpert_T8192", "dsv2lite_prefill_T4096"])
+def test_layer_full_size_folded_combine(name):
+    """The full-size layers with the combine folded into GEMM2, on the sampled checks."""
+    d = wl.make_inputs(wl.CONFIGS[name])
+    res, P = run_gpu(d, fused_gather=name.startswith("prism"), fused_combine=True)
+    check_layer_sampled(d, res, P)

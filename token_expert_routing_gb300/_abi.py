@@ -59,6 +59,9 @@ SIGNATURES = {
                                        _vp]),
     "semmoe_grouped_ffn_form": (_i, [_vp, _vp, _i, _i, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _vp, _vp, _sz,
                                      _i, _i, _vp]),
+    "semmoe_grouped_ffn_combine": (_i, [_vp, _i, _vp, _i, _i, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _vp,
+                                        _vp, _sz, _vp]),
+    "semmoe_combine_finish": (_i, [_vp, _vp, _i, _i, _i, _vp, _vp]),
     "semmoe_shared_ffn_workspace_size": (_sz, [_i, _i, _i]),
     "semmoe_shared_ffn": (_i, [_vp, _vp, _vp, _i, _i, _i, _i, _vp, _vp, _sz, _vp]),
     "semmoe_combine": (_i, [_vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _vp, _vp]),
@@ -264,6 +267,18 @@ def semmoe_grouped_ffn_form(x, sorted_to_pair, k_max, T, expert_offsets, phys_to
                                          _p(phys_to_expert), _p(w13), _p(w2), dtype_code(w13), P, E, H, I,
                                          _p(y_perm), _p(ws), ws.numel() * ws.element_size(), form1, form2,
                                          _stream(stream)))
+
+
+def semmoe_grouped_ffn_combine(x, x_rows_are_tokens, sorted_to_pair, k_max, T, expert_offsets, phys_to_expert, w13,
+                               w2, topk_w, P, E, H, I, acc, ws, stream=None):
+    _check(lib().semmoe_grouped_ffn_combine(_p(x), int(bool(x_rows_are_tokens)), _p(sorted_to_pair), k_max, T,
+                                            _p(expert_offsets), _p(phys_to_expert), _p(w13), _p(w2), _p(topk_w),
+                                            dtype_code(w13), P, E, H, I, _p(acc), _p(ws),
+                                            ws.numel() * ws.element_size(), _stream(stream)))
+
+
+def semmoe_combine_finish(acc, y_shared, T, H, out, stream=None):
+    _check(lib().semmoe_combine_finish(_p(acc), _p(y_shared), dtype_code(out), T, H, _p(out), _stream(stream)))
 
 
 def semmoe_shared_ffn_workspace_size(T, I_s, dtype: int) -> int:

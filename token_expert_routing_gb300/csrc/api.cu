@@ -370,6 +370,41 @@ int semmoe_grouped_ffn_form(const void* x, const int32_t* sorted_to_pair, int k_
                      fn);
 }
 
+int semmoe_grouped_ffn_combine(const void* x, int x_rows_are_tokens, const int32_t* sorted_to_pair, int k_max, int T,
+                               const int32_t* expert_offsets, const int32_t* phys_to_expert, const void* w13,
+                               const void* w2, const float* topk_w, int dtype, int P, int E, int H, int I, float* acc,
+                               void* ws, size_t ws_bytes, void* stream) {
+  const char* fn = "semmoe_grouped_ffn_combine";
+  REQUIRE(E >= 1 && E <= 256, "%s: E = %d outside [1, 256]", fn, E);
+  REQUIRE(T >= 0 && k_max >= 1 && (long long)T * k_max < (1LL << 31), "%s: bad sizes T=%d k_max=%d", fn, T, k_max);
+  REQUIRE(P >= 0 && P <= (long long)T * k_max, "%s: P = %d outside [0, T * k_max]", fn, P);
+  REQUIRE(H >= 8 && I >= 8 && H % 8 == 0 && I % 8 == 0, "%s: need H, I multiples of 8 (H=%d I=%d)", fn, H, I);
+  if (dtype != SEMMOE_BF16) return fail(SEMMOE_ERR_UNSUPPORTED, "%s: bf16 activations and experts only", fn);
+  if (T == 0) return SEMMOE_OK;
+  REQUIRE(expert_offsets && phys_to_expert && w13 && w2 && topk_w && acc, "%s: null pointer", fn);
+  REQUIRE(P == 0 || (x && sorted_to_pair), "%s: null x or sorted_to_pair", fn);
+  REQUIRE(aligned(x, 16) && aligned(w13, 16) && aligned(w2, 16) && aligned(acc, 16) && aligned(topk_w, 4),
+          "%s: misaligned pointer", fn);
+  REQUIRE(ws != nullptr && aligned(ws, 256) && ws_bytes >= ffn_ws_bytes(P, I, dtype),
+          "%s: workspace null, not 256-byte aligned or below %zu bytes", fn, ffn_ws_bytes(P, I, dtype));
+  CHECK_DEVICE(fn);
+  return cuda_status(launch_ffn_combine(x, x_rows_are_tokens != 0, sorted_to_pair, k_max, T, expert_offsets,
+                                        phys_to_expert, w13, w2, topk_w, P, E, H, I, acc, ws,
+                                        static_cast<cudaStream_t>(stream)),
+                     fn);
+}
+
+int semmoe_combine_finish(const float* acc, const void* y_shared, int dtype, int T, int H, void* out, void* stream) {
+  const char* fn = "semmoe_combine_finish";
+  REQUIRE(T >= 0 && H >= 8 && H % 8 == 0, "%s: bad sizes T=%d H=%d", fn, T, H);
+  if (dtype != SEMMOE_BF16) return fail(SEMMOE_ERR_UNSUPPORTED, "%s: bf16 output only", fn);
+  if (T == 0) return SEMMOE_OK;
+  REQUIRE(acc && out, "%s: null pointer", fn);
+  REQUIRE(aligned(acc, 16) && aligned(y_shared, 16) && aligned(out, 16), "%s: misaligned pointer", fn);
+  CHECK_DEVICE(fn);
+  return cuda_status(launch_combine_finish(acc, y_shared, T, H, out, static_cast<cudaStream_t>(stream)), fn);
+}
+
 size_t semmoe_shared_ffn_workspace_size(int T, int I_s, int dtype) {
   if (T < 0 || I_s < 1 || !valid_dtype(dtype)) return 0;
   return ffn_ws_bytes(T, I_s, dtype);

@@ -146,7 +146,42 @@ combine_kernel(const T* __restrict__ y_perm, const int32_t* __restrict__ pair_to
   }
 }
 
+// out[t] = y_shared[t] + acc[t] in bf16 (y_shared may be null): the last step of
+// the combine folded into GEMM2.  Eight elements per thread.
+__global__ void __launch_bounds__(kThreads)
+combine_finish_kernel(const float4* __restrict__ acc, const uint4* __restrict__ y_shared, long long n8,
+                      uint4* __restrict__ out) {
+  for (long long i = blockIdx.x * (long long)kThreads + threadIdx.x; i < n8; i += (long long)gridDim.x * kThreads) {
+    const float4 a = acc[2 * i], b = acc[2 * i + 1];
+    float v[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+    if (y_shared != nullptr) {
+      float sv[8];
+      Vec16<__nv_bfloat16>::unpack(y_shared[i], sv);
+#pragma unroll
+      for (int k = 0; k < 8; ++k) v[k] = sv[k] + v[k];
+    }
+    uint4 o;
+    __nv_bfloat162* h = reinterpret_cast<__nv_bfloat162*>(&o);
+#pragma unroll
+    for (int k = 0; k < 4; ++k) h[k] = __floats2bfloat162_rn(v[2 * k], v[2 * k + 1]);
+    out[i] = o;
+  }
+}
+
 }  // namespace
+
+cudaError_t launch_combine_finish(const float* acc, const void* y_shared, int T, int H, void* out, cudaStream_t s) {
+  const long long n8 = (long long)T * H / 8;
+  if (n8 == 0) return cudaSuccess;
+  long long blocks = (n8 + kThreads - 1) / kThreads;
+  const long long cap = 8LL * sm_count();
+  if (blocks > cap) blocks = cap;
+  combine_finish_kernel<<<(int)blocks, kThreads, 0, s>>>(reinterpret_cast<const float4*>(acc),
+                                                         static_cast<const uint4*>(y_shared), n8,
+                                                         static_cast<uint4*>(out));
+  count_launches(1);
+  return cudaGetLastError();
+}
 
 int combine_take_errors(cudaStream_t s, int* bits) { return take_error_word(g_err, s, bits); }
 

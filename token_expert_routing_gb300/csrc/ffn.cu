@@ -12,7 +12,9 @@ cudaError_t launch_ffn_simt(const void* x, const int32_t* offsets, const int32_t
                             const int32_t* gather, int gather_div, int T_x, cudaStream_t s);
 cudaError_t launch_ffn_tc(const void* x, const int32_t* offsets, const int32_t* p2e, const void* w13,
                           const void* w2, int P, int E, int H, int I, void* y, void* ws, const int32_t* gather,
-                          int gather_div, int T_x, int form1, int form2, cudaStream_t s);
+                          int gather_div, int T_x, int form1, int form2, cudaStream_t s,
+                          const int32_t* sorted_to_pair = nullptr, const float* topk_w = nullptr, int k_max = 1,
+                          int T_acc = 0, float* acc = nullptr);
 int ffn_simt_take_errors(cudaStream_t s, int* bits);
 int ffn_tc_take_errors(cudaStream_t s, int* bits);
 
@@ -33,6 +35,16 @@ cudaError_t launch_ffn(const void* x, const int32_t* offsets, const int32_t* p2e
   if (dtype == SEMMOE_BF16 && form1 != SEMMOE_FORM_CUDA_CORE)
     return launch_ffn_tc(x, offsets, p2e, w13, w2, P, E, H, I, y, ws, gather, gather_div, T_x, form1, form2, s);
   return launch_ffn_simt(x, offsets, p2e, w13, w2, dtype, P, E, H, I, y, ws, gather, gather_div, T_x, s);
+}
+
+cudaError_t launch_ffn_combine(const void* x, bool gathered, const int32_t* sorted_to_pair, int k_max, int T,
+                               const int32_t* offsets, const int32_t* p2e, const void* w13, const void* w2,
+                               const float* topk_w, int P, int E, int H, int I, float* acc, void* ws,
+                               cudaStream_t s) {
+  cudaError_t e = cudaMemsetAsync(acc, 0, (size_t)T * H * sizeof(float), s);
+  if (e != cudaSuccess || P == 0) return e;
+  return launch_ffn_tc(x, offsets, p2e, w13, w2, P, E, H, I, nullptr, ws, gathered ? sorted_to_pair : nullptr, k_max,
+                       T, SEMMOE_FORM_DEFAULT, SEMMOE_FORM_DEFAULT, s, sorted_to_pair, topk_w, k_max, T, acc);
 }
 
 }  // namespace semmoe

@@ -132,6 +132,56 @@ __device__ __forceinline__ void emit_chunk(ChunkOut& co, const uint32_t (&w)[32]
   }
 }
 
+// GEMM2 adding its rows into the token-order output instead of storing y_perm
+// (the combine folded into the epilogue): sorted row q is pair p =
+// pairs[q] of token p / div, weighted by gates[p], and added into acc [T, N]
+// fp32.  Each epilogue warp transposes its 32 rows x 32 columns through its
+// staging buffer (16-byte piece v of row r at piece v ^ (r & 7)) so that
+// eight lanes cover one row's 128 bytes: the adds are float4 atomics, four
+// rows per instruction.  Scattered per-row atomics measured half the rate.
+struct Scatter {
+  const int32_t* pairs = nullptr;  // sorted_to_pair [P]
+  const float* gates = nullptr;    // topk_w [T * div], by pair id
+  int div = 1;                     // k_max
+  int T = 0;
+  float* acc = nullptr;            // [T, N] fp32, zeroed before GEMM2
+};
+
+// The token (or -1) and gate of sorted row q.
+__device__ __forceinline__ void scatter_row(const Scatter& sc, int q, bool row_ok, int& t, float& g) {
+  t = -1;
+  g = 0.f;
+  if (!row_ok) return;
+  const int p = sc.pairs[q];
+  const int tt = p >= 0 ? p / sc.div : -1;
+  if (tt < 0 || tt >= sc.T) {
+    atomicOr(&g_err, SEMMOE_DEVERR_PAIRS);
+    return;
+  }
+  t = tt;
+  g = sc.gates[p];
+}
+
+// Half a 64-column chunk (32 accumulator words of the thread's row) weighted by
+// g and added into acc rows of the warp's 32 tokens.
+__device__ __forceinline__ void scatter_half(const Scatter& sc, unsigned char* stage, const uint32_t (&y)[32], int t,
+                                             float g, int col0, int N, int lane) {
+#pragma unroll
+  for (int v = 0; v < 8; ++v)
+    *reinterpret_cast<float4*>(stage + lane * 128 + ((v ^ (lane & 7)) << 4)) =
+        make_float4(g * __uint_as_float(y[4 * v]), g * __uint_as_float(y[4 * v + 1]),
+                    g * __uint_as_float(y[4 * v + 2]), g * __uint_as_float(y[4 * v + 3]));
+  __syncwarp();
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const int rr = i * 4 + (lane >> 3), v = lane & 7;
+    const float4 val = *reinterpret_cast<const float4*>(stage + rr * 128 + ((v ^ (rr & 7)) << 4));
+    const int tr = __shfl_sync(0xffffffffu, t, rr);
+    const int col = col0 + 4 * v;
+    if (tr >= 0 && col < N) atomicAdd(reinterpret_cast<float4*>(sc.acc + (size_t)tr * N + col), val);
+  }
+  __syncwarp();
+}
 
 // Tile unit mu (CL consecutive m-tiles of one group: CL = 1 for independent
 // CTAs, 2 for a 2-SM pair, one m-tile per CTA) -> this CTA's (first row, valid
@@ -186,13 +236,13 @@ __device__ __forceinline__ void gather_sources(const int32_t* __restrict__ gathe
 constexpr int GATHER_WARPS = 8;
 constexpr int GATHER_DEPTH = 5;
 constexpr int RPL = 4;  // 16-byte pieces per lane per k-block: 8 warps x 32 lanes x 4 = 128 rows x 128 B
-template <bool GLU, int GW = 0>
+template <bool GLU, int GW = 0, bool SC = false>
 __global__ void __launch_bounds__(THREADS + 32 * GW, 1)
 ffn_tc_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b,
               const __grid_constant__ CUtensorMap map_out,
               const int32_t* __restrict__ offsets, const int32_t* __restrict__ phys_to_expert, int G, int P,
               int E, int N, int K, int n_tiles, const int32_t* __restrict__ gather, int gather_div, int gather_rows,
-              __nv_bfloat16* __restrict__ out, const __nv_bfloat16* __restrict__ gx) {
+              __nv_bfloat16* __restrict__ out, const __nv_bfloat16* __restrict__ gx, Scatter sc) {
   static_assert(GW == 0 || GW * 32 * RPL * 16 == BM * BK * 2, "gather warps cover one A stage");
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   const uint32_t pad = (1024u - (smem_u32(smem_raw) & 1023u)) & 1023u;
@@ -381,6 +431,20 @@ ffn_tc_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__
           }
           emit_chunk(co, w, full, row_ok, orow, nt * 128 + c, N, row0 + q * 32, lane);
         }
+      } else if (SC) {  // rows weighted and added into the token-order output
+        int st;
+        float sg;
+        scatter_row(sc, row0 + (row_ok ? r : 0), row_ok, st, sg);
+#pragma unroll 1
+        for (int c = 0; c < BN; c += 64) {
+          if (nt * BN + c >= N) break;
+          uint32_t y0[32], y1[32];
+          tmem_ld32(t_row + c, y0);
+          tmem_ld32(t_row + c + 32, y1);
+          tmem_ld_wait();
+          scatter_half(sc, co.stage, y0, st, sg, nt * BN + c, N, lane);
+          scatter_half(sc, co.stage, y1, st, sg, nt * BN + c + 32, N, lane);
+        }
       } else {
 #pragma unroll 1
         for (int c = 0; c < BN; c += 64) {
@@ -506,13 +570,13 @@ struct PairShared {
 constexpr size_t kPairSmemBytes = 1024 + (size_t)P_STAGES * P_STAGE_BYTES + OUT_STAGE_BYTES + sizeof(PairShared);
 constexpr uint32_t kIdescPair = idesc_bf16_f32(2 * BM, BN);
 
-template <bool GLU, int NBUF>
+template <bool GLU, int NBUF, bool SC = false>
 __global__ void __launch_bounds__(THREADS, 1)
 ffn_pair_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b,
                 const __grid_constant__ CUtensorMap map_out,
                 const int32_t* __restrict__ offsets, const int32_t* __restrict__ phys_to_expert, int G, int P,
                 int E, int N, int K, int n_tiles, const int32_t* __restrict__ gather, int gather_div, int gather_rows,
-                __nv_bfloat16* __restrict__ out) {
+                __nv_bfloat16* __restrict__ out, Scatter sc) {
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   const uint32_t pad = (1024u - (smem_u32(smem_raw) & 1023u)) & 1023u;
   unsigned char* ring = smem_raw + pad;  // stage s: A [128 x 64] then B half [128 x 64]
@@ -692,6 +756,20 @@ ffn_pair_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant
           }
           emit_chunk(co, w, full, row_ok, orow, nt * 128 + c, N, row0 + q * 32, lane);
         }
+      } else if (SC) {  // rows weighted and added into the token-order output
+        int st;
+        float sg;
+        scatter_row(sc, row0 + (row_ok ? r : 0), row_ok, st, sg);
+#pragma unroll 1
+        for (int c = 0; c < BN; c += 64) {
+          if (nt * BN + c >= N) break;
+          uint32_t y0[32], y1[32];
+          tmem_ld32(t_row + c, y0);
+          tmem_ld32(t_row + c + 32, y1);
+          tmem_ld_wait();
+          scatter_half(sc, co.stage, y0, st, sg, nt * BN + c, N, lane);
+          scatter_half(sc, co.stage, y1, st, sg, nt * BN + c + 32, N, lane);
+        }
       } else {
 #pragma unroll 1
         for (int c = 0; c < BN; c += 64) {
@@ -735,12 +813,12 @@ struct Gather {
   const __nv_bfloat16* x = nullptr;
 };
 
-template <bool GLU, int GW = 0>
+template <bool GLU, int GW = 0, bool SC = false>
 cudaError_t launch_one(const CUtensorMap& ma, const CUtensorMap& mb, const CUtensorMap& mo, const int32_t* offsets,
                        const int32_t* p2e,
                        int G, int P, int E, int N, int K, int n_tiles, Gather ga, __nv_bfloat16* out,
-                       cudaStream_t s) {
-  auto kern = ffn_tc_kernel<GLU, GW>;
+                       cudaStream_t s, Scatter sc = Scatter()) {
+  auto kern = ffn_tc_kernel<GLU, GW, SC>;
   static std::atomic<unsigned long long> smem_set{0};
   cudaError_t e = ensure_smem_limit(kern, (int)kSmemBytes, smem_set);
   if (e != cudaSuccess) return e;
@@ -748,17 +826,17 @@ cudaError_t launch_one(const CUtensorMap& ma, const CUtensorMap& mb, const CUten
   int grid = sm_count();
   if (max_units < grid) grid = (int)max_units;
   kern<<<grid, THREADS + 32 * GW, kSmemBytes, s>>>(ma, mb, mo, offsets, p2e, G, P, E, N, K, n_tiles, ga.rows, ga.div,
-                                                   ga.n, out, ga.x);
+                                                   ga.n, out, ga.x, sc);
   count_launches(1);
   return cudaGetLastError();
 }
 
-template <bool GLU, int NBUF>
+template <bool GLU, int NBUF, bool SC = false>
 cudaError_t launch_pair(const CUtensorMap& ma, const CUtensorMap& mb, const CUtensorMap& mo, const int32_t* offsets,
                         const int32_t* p2e,
                         int G, int P, int E, int N, int K, int n_tiles, Gather ga, __nv_bfloat16* out,
-                        cudaStream_t s) {
-  auto kern = ffn_pair_kernel<GLU, NBUF>;
+                        cudaStream_t s, Scatter sc = Scatter()) {
+  auto kern = ffn_pair_kernel<GLU, NBUF, SC>;
   static std::atomic<unsigned long long> smem_set{0};
   cudaError_t e = ensure_smem_limit(kern, (int)kPairSmemBytes, smem_set);
   if (e != cudaSuccess) return e;
@@ -782,7 +860,8 @@ cudaError_t launch_pair(const CUtensorMap& ma, const CUtensorMap& mb, const CUte
   long long units = clusters;
   if (max_units < units) units = max_units;
   cfg.gridDim = dim3((unsigned)(units * 2));
-  e = cudaLaunchKernelEx(&cfg, kern, ma, mb, mo, offsets, p2e, G, P, E, N, K, n_tiles, ga.rows, ga.div, ga.n, out);
+  e = cudaLaunchKernelEx(&cfg, kern, ma, mb, mo, offsets, p2e, G, P, E, N, K, n_tiles, ga.rows, ga.div, ga.n, out,
+                         sc);
   if (e != cudaSuccess) return e;
   count_launches(1);
   return cudaGetLastError();
@@ -811,7 +890,17 @@ static int resolve_form(int form, bool glu, int I, int P, int G, bool gathered) 
 template <bool GLU>
 static cudaError_t launch_gemm(int form, const CUtensorMap& ma, const CUtensorMap& mb, const CUtensorMap& mo,
                                const int32_t* offsets, const int32_t* p2e, int G, int P, int E, int N, int K,
-                               int n_tiles, Gather ga, __nv_bfloat16* out, cudaStream_t s) {
+                               int n_tiles, Gather ga, __nv_bfloat16* out, cudaStream_t s,
+                               const Scatter* sc = nullptr) {
+  if constexpr (!GLU) {
+    if (sc != nullptr) {  // GEMM2 adding its rows into the token-order output
+      if (form == SEMMOE_FORM_PAIR1)
+        return launch_pair<false, 1, true>(ma, mb, mo, offsets, p2e, G, P, E, N, K, n_tiles, ga, out, s, *sc);
+      if (form == SEMMOE_FORM_PAIR)
+        return launch_pair<false, 2, true>(ma, mb, mo, offsets, p2e, G, P, E, N, K, n_tiles, ga, out, s, *sc);
+      return launch_one<false, 0, true>(ma, mb, mo, offsets, p2e, G, P, E, N, K, n_tiles, ga, out, s, *sc);
+    }
+  }
   switch (form) {
     case SEMMOE_FORM_PAIR1: return launch_pair<GLU, 1>(ma, mb, mo, offsets, p2e, G, P, E, N, K, n_tiles, ga, out, s);
     case SEMMOE_FORM_PAIR: return launch_pair<GLU, 2>(ma, mb, mo, offsets, p2e, G, P, E, N, K, n_tiles, ga, out, s);
@@ -828,9 +917,13 @@ static cudaError_t launch_gemm(int form, const CUtensorMap& ma, const CUtensorMa
 
 // gather_rows != nullptr: x is the unpermuted [T_x, H] activation and sorted row
 // q of GEMM1 reads x row gather_rows[q] / gather_div.
+// acc != nullptr: GEMM2 adds each row, weighted by topk_w[sorted_to_pair[q]],
+// into acc [T_acc, H] fp32 (row of token sorted_to_pair[q] / k_max) instead of
+// writing y.
 cudaError_t launch_ffn_tc(const void* x, const int32_t* offsets, const int32_t* p2e, const void* w13,
                           const void* w2, int P, int E, int H, int I, void* y, void* ws, const int32_t* gather_rows,
-                          int gather_div, int T_x, int form1, int form2, cudaStream_t s) {
+                          int gather_div, int T_x, int form1, int form2, cudaStream_t s, const int32_t* sorted_to_pair,
+                          const float* topk_w, int k_max, int T_acc, float* acc) {
   if (P == 0) return cudaSuccess;
   const int G = offsets ? E : 1;
   const int mode1 = resolve_form(form1, true, I, P, G, gather_rows != nullptr);
@@ -881,17 +974,26 @@ cudaError_t launch_ffn_tc(const void* x, const int32_t* offsets, const int32_t* 
     const cuuint32_t box[2] = {32, 32};
     if (!make_map_bf16(&mo1, ws, 2, dims, str, box, CU_TENSOR_MAP_SWIZZLE_64B)) return cudaErrorInvalidValue;
   }
-  {
+  if (acc == nullptr) {
     const cuuint64_t dims[2] = {(cuuint64_t)H, (cuuint64_t)P};
     const cuuint64_t str[1] = {(cuuint64_t)H * es};
     const cuuint32_t box[2] = {32, 32};
     if (!make_map_bf16(&mo2, y, 2, dims, str, box, CU_TENSOR_MAP_SWIZZLE_64B)) return cudaErrorInvalidValue;
+  } else {
+    mo2 = mo1;  // no y: GEMM2 adds into acc (the map is not used)
   }
+  Scatter sc;
+  sc.pairs = sorted_to_pair;
+  sc.gates = topk_w;
+  sc.div = k_max;
+  sc.T = T_acc;
+  sc.acc = acc;
   __nv_bfloat16* h = static_cast<__nv_bfloat16*>(ws);
   __nv_bfloat16* yb = static_cast<__nv_bfloat16*>(y);
   cudaError_t e = launch_gemm<true>(mode1, ma1, mb1, mo1, offsets, p2e, G, P, E, I, H, (I + 127) / 128, ga, h, s);
   if (e != cudaSuccess) return e;
-  return launch_gemm<false>(mode2, ma2, mb2, mo2, offsets, p2e, G, P, E, H, I, (H + BN - 1) / BN, Gather(), yb, s);
+  return launch_gemm<false>(mode2, ma2, mb2, mo2, offsets, p2e, G, P, E, H, I, (H + BN - 1) / BN, Gather(), yb, s,
+                            acc != nullptr ? &sc : nullptr);
 }
 
 }  // namespace semmoe

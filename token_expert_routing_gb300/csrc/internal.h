@@ -89,6 +89,15 @@ cudaError_t launch_ffn(const void* x, const int32_t* offsets, const int32_t* phy
                        void* y, void* ws, const int32_t* gather, int gather_div, int T_x, cudaStream_t s,
                        int form1 = SEMMOE_FORM_DEFAULT, int form2 = SEMMOE_FORM_DEFAULT);
 
+// The combine folded into GEMM2 (bf16): acc [T, H] fp32 zeroed, then the grouped
+// FFN whose GEMM2 adds its gate-weighted rows into acc; launch_combine_finish
+// then writes out = y_shared + acc.
+cudaError_t launch_ffn_combine(const void* x, bool gathered, const int32_t* sorted_to_pair, int k_max, int T,
+                               const int32_t* offsets, const int32_t* p2e, const void* w13, const void* w2,
+                               const float* topk_w, int P, int E, int H, int I, float* acc, void* ws,
+                               cudaStream_t s);
+cudaError_t launch_combine_finish(const float* acc, const void* y_shared, int T, int H, void* out, cudaStream_t s);
+
 cudaError_t launch_combine(const void* y_perm, const int32_t* pair_to_sorted, const float* topk_w,
                            const void* y_shared, int dtype, int T, int H, int k_max, int P,
                            void* out, cudaStream_t s);

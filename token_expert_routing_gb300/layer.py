@@ -32,10 +32,17 @@ class LayerOutput:
     sorted_to_pair: torch.Tensor
     pair_to_sorted: torch.Tensor
     x_perm: Optional[torch.Tensor]   # None when GEMM1 gathers x through the permutation
-    y_perm: torch.Tensor
+    y_perm: Optional[torch.Tensor]   # None when GEMM2 adds its rows into the token order (fused_combine)
     y_shared: Optional[torch.Tensor]
     schedule: Optional[dict] = None      # semmoe_dp_schedule outputs (when req_offsets is given)
     pred_next: Optional[torch.Tensor] = None  # next-layer rank per token (when trans is held)
+
+
+def fuse_combine_default(I: int, dtype, shared: bool) -> bool:
+    """Whether a layer folds the combine into GEMM2 by default (semmoe_grouped_ffn_combine).
+
+    Off for now: the default is set from measurements of the whole layer."""
+    return False
 
 
 def fuse_gather_default(I: int, dtype) -> bool:
@@ -62,7 +69,8 @@ class MoELayer:
     """
 
     def __init__(self, w_router, w13, w2, expert_rank, lut, R: int, k_max: int, ws13=None, ws2=None,
-                 trans=None, sub_logw=None, fused_gather: Optional[bool] = None, overlap: bool = True,
+                 trans=None, sub_logw=None, fused_gather: Optional[bool] = None,
+                 fused_combine: Optional[bool] = None, overlap: bool = True,
                  overlap_shared: bool = True, shared_at: str = "start", device="cuda"):
         dev = torch.device(device)
         c = lambda t: None if t is None else t.to(dev).contiguous()  # noqa: E731
@@ -90,6 +98,13 @@ class MoELayer:
         if fused_gather is None:
             fused_gather = fuse_gather_default(self.I, self.w13.dtype)
         self.fused_gather = bool(fused_gather)
+        # fused_combine: GEMM2 adds its gate-weighted rows into an fp32 token-order
+        # accumulator (no y_perm); bf16 experts only; None = fuse_combine_default
+        if fused_combine is None:
+            fused_combine = fuse_combine_default(self.I, self.w13.dtype, ws13 is not None)
+        if fused_combine and self.w13.dtype != torch.bfloat16:
+            raise ValueError("fused_combine needs bf16 experts")
+        self.fused_combine = bool(fused_combine)
         self.I_s = 0 if ws13 is None else self.ws13.shape[0] // 2
         self.R, self.k_max, self.V = R, k_max, self.lut.shape[0]
         self.Ep = self.w_router.shape[0]          # router rows: experts, or parents (hierarchical)
@@ -260,11 +275,16 @@ class MoELayer:
                            expert_offsets, rank_offsets, phys_to_expert, expert_counts, sorted_to_pair,
                            pair_to_sorted, x_perm, ws, stream, pair_counts=pair_counts)
         mark("permute")
-        y_perm = torch.empty(P, H, dtype=x.dtype, device=dev)
+        y_perm = None if self.fused_combine else torch.empty(P, H, dtype=x.dtype, device=dev)
+        acc = torch.empty(T, H, dtype=torch.float32, device=dev) if self.fused_combine else None
         if shared_side and self.shared_at == "permute":  # the shared experts beside the routed FFN
             shared_on_side()
         ws = self._workspace("ffn", abi.semmoe_grouped_ffn_workspace_size(P, I, dcode))
-        if self.fused_gather:
+        if self.fused_combine:  # GEMM2 adds its rows into the token order
+            abi.semmoe_grouped_ffn_combine(x if self.fused_gather else x_perm, self.fused_gather, sorted_to_pair,
+                                           k_max, T, expert_offsets, phys_to_expert, self.w13, self.w2, topk_w,
+                                           P, E, H, I, acc, ws, stream)
+        elif self.fused_gather:
             abi.semmoe_grouped_ffn_gather(x, sorted_to_pair, k_max, T, expert_offsets, phys_to_expert, self.w13,
                                           self.w2, P, E, H, I, y_perm, ws, stream)
         else:
@@ -279,7 +299,10 @@ class MoELayer:
         if forked:
             join()  # the second stream's steps are done before the combine (and the call's end)
         out = torch.empty(T, H, dtype=x.dtype, device=dev)
-        abi.semmoe_combine(y_perm, pair_to_sorted, topk_w, y_shared, T, H, k_max, P, out, stream)
+        if self.fused_combine:
+            abi.semmoe_combine_finish(acc, y_shared, T, H, out, stream)
+        else:
+            abi.semmoe_combine(y_perm, pair_to_sorted, topk_w, y_shared, T, H, k_max, P, out, stream)
         mark("combine")
         return LayerOutput(out, logits, topk_idx, topk_w, pred, counts, remote, expert_offsets,
                            rank_offsets, phys_to_expert, expert_counts, sorted_to_pair[:P],
