@@ -861,5 +861,7 @@ def test_folded_combine_flags_a_bad_pair_and_drops_its_row():
     p2s = np.full(T * k_max, -1, dtype=np.int64)
     p2s[s2p_np[s2p_np >= 0]] = np.nonzero(s2p_np >= 0)[0]
     assert p2s[dropped] == -1
-    ref = oracle.combine(y_ref, p2s, w.astype(np.float64), np.full(T, k_max), "bf16")
+    w_ref = w.astype(np.float64)
+    w_ref[dropped // k_max, dropped % k_max] = 0.0      # the dropped pair contributes nothing
+    ref = oracle.combine(y_ref, p2s, w_ref, np.full(T, k_max), "bf16")
     assert max_rel(np_(out), ref) < TOL["bf16"]
