@@ -41,7 +41,12 @@ class LayerOutput:
 def fuse_combine_default(I: int, dtype, shared: bool) -> bool:
     """Whether a layer folds the combine into GEMM2 by default (semmoe_grouped_ffn_combine).
 
-    Off for now: the default is set from measurements of the whole layer."""
+    Off for every shape: the float4 atomic adds in GEMM2's epilogue (about 6 TB/s
+    of fp32 payload at best) slow GEMM2 by more than the y_perm round trip and
+    the combine kernel cost.  Measured on GB300, whole layer in graph replay,
+    unfolded against folded: Qwen3 (I 768) 1044 against 1160 us; MoE-Prism
+    (I 352) 821 against 909; DeepSeek prefill 498 against 502; DeepSeek decode
+    T = 512 234 against 236."""
     return False
 
 
