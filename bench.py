@@ -452,6 +452,43 @@ def _time_eager(serial, inp, steps, warmup, world, dev, stream, local):
                 clocks=clocks.summary())
 
 
+def _time_stages_graph(serial, inp, steps, warmup, dev):
+    """Per-step device times of the one-stream forward captured as one CUDA
+    graph: events between its steps are captured as event nodes, so every
+    replay times each step without the gaps of separate launches from the host.
+    Returns {step: mean ms} over the replays, or None if this torch cannot
+    capture timing events."""
+    x, ids, kpt, k, P = inp
+    try:
+        torch.cuda.Event(enable_timing=True, external=True)
+    except TypeError:
+        return None
+    side = torch.cuda.Stream(device=dev)
+    side.wait_stream(torch.cuda.current_stream(dev))
+    with torch.cuda.stream(side):            # workspaces and kernel attributes before capture
+        for _ in range(2):
+            serial.forward(x, ids, kpt, k, P, stream=side)
+    torch.cuda.current_stream(dev).wait_stream(side)
+    torch.cuda.synchronize(dev)
+    marks = []
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        serial.forward(x, ids, kpt, k, P, stream=torch.cuda.current_stream(dev), marks=marks, mark_external=True)
+    for _ in range(warmup):
+        g.replay()
+    torch.cuda.synchronize(dev)
+    stage_ms = {}
+    for _ in range(steps):
+        g.replay()
+        torch.cuda.synchronize(dev)
+        for (_, a), (name, b) in zip(marks[:-1], marks[1:]):
+            stage_ms.setdefault(name, []).append(a.elapsed_time(b))
+    from token_expert_routing_gb300 import _abi
+    _abi.semmoe_check_errors()
+    del g
+    return {n: sum(v) / len(v) for n, v in stage_ms.items()}
+
+
 def _time_graph(layer, spec, d, inp, steps, warmup, world, dev, local):
     """The same forward as one CUDA-graph replay per step (static buffers)."""
     from token_expert_routing_gb300 import CapturedLayer, _abi
@@ -553,9 +590,10 @@ def _other_workloads(args, world, dev, stream, local, peaks):
         steps = max(3, args.also_steps)
         ev = _time_eager(serial, inp, steps, args.warmup, world, dev, stream, local)
         gr = None if args.no_graph else _time_graph(layer, spec, d, inp, steps, args.warmup, world, dev, local)
+        gst = None if args.no_graph else _time_stages_graph(serial, inp, steps, args.warmup, dev)
         res = layer.forward(*inp[:4], inp[4], stream=stream)
         active = int((res.expert_counts > 0).sum())
-        roof, stages = _roofline_and_stages(spec, inp[4], active, serial.fused_gather, ev["stage_avg"], peaks)
+        roof, stages = _roofline_and_stages(spec, inp[4], active, serial.fused_gather, gst or ev["stage_avg"], peaks)
         eager_value = spec.T * steps * world / (ev["ms_max"] * 1e-3)
         best = gr if gr is not None and gr["ms_per_step"] < ev["ms_max"] / steps else None
         out[name] = {
@@ -565,6 +603,7 @@ def _other_workloads(args, world, dev, stream, local, peaks):
             "eager_ms_per_step": ev["ms_max"] / steps,
             "roofline": {k: roof[k] for k in ("bound", "achieved", "peak", "unit", "frac", "ms")},
             "stages": {k: {kk: round(vv, 5) for kk, vv in v.items()} for k, v in stages.items()},
+            "stages_timed_in": "one-stream graph replay" if gst else "eager one-stream forwards",
             "clocks": (best or ev)["clocks"],
         }
         del layer, serial, res, d
@@ -588,6 +627,7 @@ def run_ours(args, world, rank, local):
     ev = _time_eager(serial, inp, args.steps, args.warmup, world, dev, stream, local)
     ms_max, stage_avg, per_step = ev["ms_max"], ev["stage_avg"], ev["per_step"]
     graph = None if args.no_graph else _time_graph(layer, spec, d, inp, args.steps, args.warmup, world, dev, local)
+    graph_stages = None if args.no_graph else _time_stages_graph(serial, inp, args.steps, args.warmup, dev)
 
     # end to end through the public API: pinned host inputs in, host output back,
     # every step (GraphPipeline: one graph replay per step; HostPipeline: eager)
@@ -641,7 +681,11 @@ def run_ours(args, world, rank, local):
     res = layer.forward(x, ids, kpt, k, P, stream=stream)
     active = int((res.expert_counts > 0).sum())
     counts = res.counts.cpu().numpy()
-    roofline, stages = _roofline_and_stages(spec, P, active, serial.fused_gather, stage_avg, peaks)
+    roofline, stages = _roofline_and_stages(spec, P, active, serial.fused_gather, graph_stages or stage_avg, peaks)
+    _, stages_eager = _roofline_and_stages(spec, P, active, serial.fused_gather, stage_avg, peaks)
+    roofline["timed_in"] = ("the one-stream forward captured as a CUDA graph, events between its steps (one "
+                            "replay per step, mean over the replays)" if graph_stages else
+                            "eager one-stream forwards, events between the steps")
     cpu = None
     if not args.no_cpu_baseline:
         n_cpu = min(args.cpu_tokens, spec.T)
@@ -670,6 +714,7 @@ def run_ours(args, world, rank, local):
         "host_enqueue_ms_per_step": ev["host_ms"],
         "roofline": roofline,
         "stages": stages,
+        "stages_eager": stages_eager,
         "cpu_baseline": cpu,
         "clocks": best["clocks"],
         "local_activation_rate": float(np.trace(counts) / counts.sum()),

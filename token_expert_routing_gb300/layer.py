@@ -148,7 +148,7 @@ class MoELayer:
 
     def forward(self, x, token_ids, k_per_token=None, k: Optional[int] = None, P: Optional[int] = None,
                 logits_in=None, keep_logits: bool = False, stream=None, marks=None,
-                req_offsets=None, side_marks=None) -> LayerOutput:
+                req_offsets=None, side_marks=None, mark_external: bool = False) -> LayerOutput:
         """x [T,H] (activation type) and token_ids [T] int32 on the device.
 
         Budgets: ``k`` for every token, or ``k_per_token`` [T] int32 on the device
@@ -159,15 +159,18 @@ class MoELayer:
         ``marks``: optional list; a CUDA event is recorded on the stream after
         each step and appended as (step name, event), for per-step timing;
         ``side_marks`` gets (step name, start event, end event) for the steps
-        run on the second stream.  Every step has finished on ``stream`` when
-        the work enqueued by this call has.
+        run on the second stream.  ``mark_external``: the marks' events are
+        recorded as event nodes when the forward is captured in a CUDA graph
+        (so each replay times its steps).  Every step has finished on ``stream``
+        when the work enqueued by this call has.
         """
         s = torch.cuda.current_stream() if stream is None else stream
         side = self._side_stream() if (self.overlap or self.overlap_shared) else None
 
         def mark(name):
             if marks is not None:
-                ev = torch.cuda.Event(enable_timing=True)
+                ev = torch.cuda.Event(enable_timing=True, external=True) if mark_external else \
+                    torch.cuda.Event(enable_timing=True)
                 ev.record(s)
                 marks.append((name, ev))
 
