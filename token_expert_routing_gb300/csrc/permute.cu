@@ -56,30 +56,6 @@ inline int internal_chunk_tokens(int T) {
   return c > SEMMOE_PAIR_COUNT_CHUNK ? c : SEMMOE_PAIR_COUNT_CHUNK;
 }
 
-// phys_s[e] = position of expert e in the (expert_rank[e], e) order.
-__device__ void physical_positions(const int32_t* __restrict__ expert_rank, int E, int R, int* rank_s,
-                                   int* phys_s) {
-  for (int e = threadIdx.x; e < E; e += blockDim.x) {
-    int r = expert_rank[e];
-    if (r < 0 || r >= R) {
-      flag(SEMMOE_DEVERR_LUT);
-      r = r < 0 ? 0 : R - 1;
-    }
-    rank_s[e] = r;
-  }
-  __syncthreads();
-  for (int e = threadIdx.x; e < E; e += blockDim.x) {
-    int re = rank_s[e], pos = 0;
-#pragma unroll 16
-    for (int f = 0; f < E; ++f) {
-      int rf = rank_s[f];
-      pos += (rf < re) || (rf == re && f < e);
-    }
-    phys_s[e] = pos;
-  }
-  __syncthreads();
-}
-
 // Count table of the pairs: counts[e * ncp + c] = live pairs of expert e among
 // the tokens [c * chunk, (c + 1) * chunk).  One CTA per chunk; every entry of its
 // column is written (no zeroing needed).
@@ -212,52 +188,110 @@ perm_rank_copy_kernel(const int32_t* __restrict__ topk_idx, const int32_t* __res
   const int c0 = t0 / chunk;  // the chunk holding t0
   for (int i = tid; i < E; i += kThreads) sub[i] = 0;
   for (int i = tid; i < kWarps * kMaxE; i += kThreads) (&wcnt[0][0])[i] = 0;
-  physical_positions(expert_rank, E, R, rank_s, phys_s);
+  __syncthreads();
 
-  // 1a. G threads per expert each sum a strided part of its row of the table
-  //     (16-byte loads; rows are ncp >= nc entries, zero-padded or unread past nc)
-  const int G = kThreads / E;  // >= 2 (E <= 256)
-  if (tid < G * E) {
-    const int e = tid % E, g = tid / E;
-    const int4* row = reinterpret_cast<const int4*>(counts + (size_t)e * ncp);
-    int tot = 0, bef = 0;
-    for (int v0 = g; v0 * 4 < nc; v0 += kPre * G) {
-      int4 v[kPre];
+  // Every load that depends on nothing computed here is issued first, so that
+  // their latencies overlap: the first row each warp copies (the row does not
+  // depend on the ranking, only its destinations do), this thread's share of
+  // the count table, the pairs of t0's chunk before t0, and the CTA's own pairs
+  // of the first ranking round.
+  const bool copy = x != nullptr && P > 0;
+  unsigned char* slot = slots_smem + (size_t)warp * kSlotBytes;
+  uint64_t* bar = &cbar[warp];
+  if (copy && lane == 0 && t0 + warp < t1) {
+    const uint32_t bytes = (uint32_t)(row_bytes < kSlotBytes ? row_bytes : kSlotBytes);
+    tc::mbar_expect_tx(bar, bytes);
+    tc::bulk_load_1d(slot, x + (size_t)(t0 + warp) * row_bytes, bytes, bar);
+  }
+  const int G = kThreads / E;  // threads per expert for the table (>= 2: E <= 256)
+  const int ge = tid % E, gg = tid / E;
+  const int4* crow = reinterpret_cast<const int4*>(counts + (size_t)ge * ncp);
+  int4 cv[kPre];  // first batch of this thread's table vectors: vector gg + u * G of expert ge
 #pragma unroll
-      for (int u = 0; u < kPre; ++u) {
-        const int vi = v0 + u * G;
-        v[u] = vi * 4 < nc ? row[vi] : make_int4(0, 0, 0, 0);
+  for (int u = 0; u < kPre; ++u) {
+    const int vi = gg + u * G;
+    cv[u] = (tid < G * E && vi * 4 < nc) ? crow[vi] : make_int4(0, 0, 0, 0);
+  }
+  const long long sp0 = (long long)c0 * chunk * k_max, sp1 = (long long)t0 * k_max;
+  int sv[kPre];  // first batch of the pairs before t0 in its chunk
+#pragma unroll
+  for (int u = 0; u < kPre; ++u) {
+    const long long i = sp0 + (long long)u * kThreads + tid;
+    sv[u] = i < sp1 ? topk_idx[i] : -1;
+  }
+  const long long pb = (long long)t0 * k_max, pe = (long long)t1 * k_max;
+  const int e_first = pb + tid < pe ? topk_idx[pb + tid] : -1;  // first ranking round
+
+  // Physical position of each expert: M threads per expert split the E compares.
+  {
+    int M = kThreads / E;
+    M = M >= 32 ? 32 : (M >= 16 ? 16 : (M >= 8 ? 8 : (M >= 4 ? 4 : 2)));
+    for (int e = tid; e < E; e += kThreads) {
+      int r = expert_rank[e];
+      if (r < 0 || r >= R) {
+        flag(SEMMOE_DEVERR_LUT);
+        r = r < 0 ? 0 : R - 1;
       }
-#pragma unroll
-      for (int u = 0; u < kPre; ++u) {
-        const int c = (v0 + u * G) * 4;
-        const int a[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          if (c + i < nc) {
-            tot += a[i];
-            if (c + i < c0) bef += a[i];
-          }
-        }
+      rank_s[e] = r;
+    }
+    __syncthreads();
+    const int e = tid / M, m = tid % M;  // M divides 32: the M threads of an expert share a warp
+    int pos = 0;
+    if (e < E) {
+      const int re = rank_s[e];
+      for (int f = m; f < E; f += M) {
+        const int rf = rank_s[f];
+        pos += (rf < re) || (rf == re && f < e);
       }
     }
-    part_tot[tid] = tot;
-    part_bef[tid] = bef;
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1)
+      if (d < M) pos += __shfl_xor_sync(0xffffffffu, pos, d);
+    if (e < E && m == 0) phys_s[e] = pos;
+  }
+
+  // 1a. the table: totals and the chunks before c0, per expert
+  {
+    int tot = 0, bef = 0;
+    auto add = [&](const int4& v, int c) {
+      const int a4[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+        if (c + i < nc) {
+          tot += a4[i];
+          if (c + i < c0) bef += a4[i];
+        }
+    };
+#pragma unroll
+    for (int u = 0; u < kPre; ++u) add(cv[u], (gg + u * G) * 4);
+    if (tid < G * E)
+      for (int v0 = gg + kPre * G; v0 * 4 < nc; v0 += kPre * G) {  // tables of more than 8 G vectors
+#pragma unroll
+        for (int u = 0; u < kPre; ++u) {
+          const int vi = v0 + u * G;
+          cv[u] = vi * 4 < nc ? crow[vi] : make_int4(0, 0, 0, 0);
+        }
+#pragma unroll
+        for (int u = 0; u < kPre; ++u) add(cv[u], (v0 + u * G) * 4);
+      }
+    if (tid < G * E) {
+      part_tot[tid] = tot;
+      part_bef[tid] = bef;
+    }
   }
   // 1b. pairs of t0's chunk before t0
-  {
-    const long long p0 = (long long)c0 * chunk * k_max, p1 = (long long)t0 * k_max;
-    for (long long i0 = p0; i0 < p1; i0 += (long long)kPre * kThreads) {
-      int ev[kPre];
 #pragma unroll
-      for (int u = 0; u < kPre; ++u) {
-        const long long i = i0 + (long long)u * kThreads + tid;
-        ev[u] = i < p1 ? topk_idx[i] : -1;
-      }
+  for (int u = 0; u < kPre; ++u)
+    if (sv[u] >= 0 && sv[u] < E) atomicAdd(&sub[sv[u]], 1);
+  for (long long i0 = sp0 + (long long)kPre * kThreads; i0 < sp1; i0 += (long long)kPre * kThreads) {
 #pragma unroll
-      for (int u = 0; u < kPre; ++u)
-        if (ev[u] >= 0 && ev[u] < E) atomicAdd(&sub[ev[u]], 1);
+    for (int u = 0; u < kPre; ++u) {
+      const long long i = i0 + (long long)u * kThreads + tid;
+      sv[u] = i < sp1 ? topk_idx[i] : -1;
     }
+#pragma unroll
+    for (int u = 0; u < kPre; ++u)
+      if (sv[u] >= 0 && sv[u] < E) atomicAdd(&sub[sv[u]], 1);
   }
   __syncthreads();
   if (tid < E) {
@@ -270,13 +304,21 @@ perm_rank_copy_kernel(const int32_t* __restrict__ topk_idx, const int32_t* __res
     bef_s[tid] = bef + sub[tid];            // rows of expert tid before t0
   }
   __syncthreads();
-  // 2. inclusive scan of the bucket totals (Hillis-Steele over E <= 256 entries)
-  if (tid < E) scan[tid] = total[tid];
-  __syncthreads();
-  for (int d = 1; d < E; d <<= 1) {
-    const int v = (tid < E && tid >= d) ? scan[tid - d] : 0;
+  // 2. inclusive scan of the bucket totals: a shuffle scan per warp of 32
+  //    buckets, then the warps' sums (E <= 256: at most 8 warps)
+  {
+    int v = tid < E ? total[tid] : 0;
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+      const int o = __shfl_up_sync(0xffffffffu, v, d);
+      if (lane >= d) v += o;
+    }
+    if (lane == 31 && warp < kMaxE / 32) part_tot[warp] = v;  // (part_tot is free again)
     __syncthreads();
-    if (tid < E) scan[tid] += v;
+    if (tid < E) {
+      for (int w = 0; w < warp; ++w) v += part_tot[w];
+      scan[tid] = v;
+    }
     __syncthreads();
   }
   const int sum = E > 0 ? scan[E - 1] : 0;
@@ -300,12 +342,11 @@ perm_rank_copy_kernel(const int32_t* __restrict__ topk_idx, const int32_t* __res
   __syncthreads();
 
   // 3. stable ranking of the pairs [t0 * k_max, t1 * k_max), kThreads per round
-  const long long pe = (long long)t1 * k_max;
-  for (long long base = (long long)t0 * k_max; base < pe; base += kThreads) {
+  for (long long base = pb; base < pe; base += kThreads) {
     const long long p = base + tid;
     int key = E;  // E = "no bucket" (padding slot or past the end)
     if (p < pe) {
-      const int e = topk_idx[p];
+      const int e = base == pb ? e_first : topk_idx[p];
       if (e >= E) flag(SEMMOE_DEVERR_EXPERT);
       else if (e >= 0) key = phys_s[e];
     }
@@ -333,13 +374,11 @@ perm_rank_copy_kernel(const int32_t* __restrict__ topk_idx, const int32_t* __res
   }
 
   // 4. the rows (this CTA's own pair_to_sorted entries, written above)
-  if (x != nullptr && P > 0) {
-    unsigned char* slot = slots_smem + (size_t)warp * kSlotBytes;
-    uint64_t* bar = &cbar[warp];
+  if (copy) {
     volatile int* abort_flag = &abort_s;
     const int kk = k_max < 32 ? k_max : 32;
     uint32_t phase = 0;
-    bool used = false, ok = true;
+    bool used = false, ok = true, loaded = true;  // the first segment was loaded at the start
     for (int t = t0 + warp; ok && t < t1; t += kWarps) {
       const int32_t* slots = pair_to_sorted + (size_t)t * k_max;
       int q_l = -1;
@@ -351,9 +390,12 @@ perm_rank_copy_kernel(const int32_t* __restrict__ topk_idx, const int32_t* __res
         const uint32_t bytes = (uint32_t)(row_bytes - off < kSlotBytes ? row_bytes - off : kSlotBytes);
         int good = 1;
         if (lane == 0) {
-          if (used) tc::bulk_wait_read<0>();  // the slot's previous stores have read it
-          tc::mbar_expect_tx(bar, bytes);
-          tc::bulk_load_1d(slot, x + (size_t)t * row_bytes + off, bytes, bar);
+          if (!loaded) {
+            if (used) tc::bulk_wait_read<0>();  // the slot's previous stores have read it
+            tc::mbar_expect_tx(bar, bytes);
+            tc::bulk_load_1d(slot, x + (size_t)t * row_bytes + off, bytes, bar);
+          }
+          loaded = false;
           good = tc::mbar_wait(bar, phase, abort_flag, &g_err);
           if (!good) tc::mbar_drain(bar, phase, &g_err);  // bounded: no load may land after the CTA exits
           phase ^= 1;
