@@ -206,9 +206,10 @@ perm_rank_copy_kernel(const int32_t* __restrict__ topk_idx, const int32_t* __res
   const int G = kThreads / E;  // threads per expert for the table (>= 2: E <= 256)
   const int ge = tid % E, gg = tid / E;
   const int4* crow = reinterpret_cast<const int4*>(counts + (size_t)ge * ncp);
-  int4 cv[kPre];  // first batch of this thread's table vectors: vector gg + u * G of expert ge
+  constexpr int kCv = 4;  // table vectors per thread per batch
+  int4 cv[kCv];  // first batch of this thread's table vectors: vector gg + u * G of expert ge
 #pragma unroll
-  for (int u = 0; u < kPre; ++u) {
+  for (int u = 0; u < kCv; ++u) {
     const int vi = gg + u * G;
     cv[u] = (tid < G * E && vi * 4 < nc) ? crow[vi] : make_int4(0, 0, 0, 0);
   }
@@ -263,16 +264,16 @@ perm_rank_copy_kernel(const int32_t* __restrict__ topk_idx, const int32_t* __res
         }
     };
 #pragma unroll
-    for (int u = 0; u < kPre; ++u) add(cv[u], (gg + u * G) * 4);
+    for (int u = 0; u < kCv; ++u) add(cv[u], (gg + u * G) * 4);
     if (tid < G * E)
-      for (int v0 = gg + kPre * G; v0 * 4 < nc; v0 += kPre * G) {  // tables of more than 8 G vectors
+      for (int v0 = gg + kCv * G; v0 * 4 < nc; v0 += kCv * G) {  // tables of more than 4 G vectors
 #pragma unroll
-        for (int u = 0; u < kPre; ++u) {
+        for (int u = 0; u < kCv; ++u) {
           const int vi = v0 + u * G;
           cv[u] = vi * 4 < nc ? crow[vi] : make_int4(0, 0, 0, 0);
         }
 #pragma unroll
-        for (int u = 0; u < kPre; ++u) add(cv[u], (v0 + u * G) * 4);
+        for (int u = 0; u < kCv; ++u) add(cv[u], (v0 + u * G) * 4);
       }
     if (tid < G * E) {
       part_tot[tid] = tot;
