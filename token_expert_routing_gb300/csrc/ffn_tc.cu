@@ -64,6 +64,7 @@ struct Shared {
   uint64_t full[STAGES], empty[STAGES], tfull[2], tempty[2], done;
   uint32_t tmem_base;
   int abort_flag;
+  int armed, producer_done;  // gathering warps: stage positions the producer armed, and its exit
   int total_mtiles;
   int off[MAX_GROUPS + 1];
   int pe[MAX_GROUPS];
@@ -265,6 +266,8 @@ ffn_tc_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__
     }
     mbar_init(&sh.done, 1);
     sh.abort_flag = 0;
+    sh.armed = 0;
+    sh.producer_done = 0;
     mbar_init_fence();
     prefetch_map(&map_a);
     prefetch_map(&map_b);
@@ -360,6 +363,11 @@ ffn_tc_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__
         ++it;
       }
       if (!ok) break;
+    }
+    if (lane == 0) {  // positions armed: how far gathering warps arrive, and what is drained, on an abort
+      *reinterpret_cast<volatile int*>(&sh.armed) = (int)it;
+      __threadfence_block();
+      *reinterpret_cast<volatile int*>(&sh.producer_done) = 1;
     }
     if (lane == 0 && *abort_flag) {  // no TMA write may still be landing when the CTA exits
       for (uint32_t j = it > (uint32_t)STAGES ? it - STAGES : 0; j < it; ++j)
@@ -515,6 +523,7 @@ ffn_tc_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__
     for (int u = 0; u < D - 1; ++u)
       if (u < npos) load_next(v[u]);
     bool ok = true;
+    int stop = npos;  // the first position this warp did not fill (on abort)
     for (int base = 0; ok && base < npos; base += D) {
 #pragma unroll
       for (int u = 0; u < D; ++u) {
@@ -523,7 +532,11 @@ ffn_tc_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__
         if (it + D - 1 < npos) load_next(v[(u + D - 1) % D]);
         const int s = it % STAGES;
         const uint32_t ph = (it / STAGES) & 1;
-        if (!mbar_wait(&sh.empty[s], ph ^ 1, abort_flag, &g_err)) { ok = false; break; }
+        if (!mbar_wait(&sh.empty[s], ph ^ 1, abort_flag, &g_err)) {
+          ok = false;
+          stop = it;
+          break;
+        }
         unsigned char* a = stage_a + s * A_BYTES;
 #pragma unroll
         for (int j = 0; j < RPL; ++j) {
@@ -534,10 +547,31 @@ ffn_tc_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__
         mbar_arrive(&sh.full[s]);
       }
     }
+    if (!ok) {
+      // Abort: the producer armed its positions up to sh.armed with the weight
+      // tile's bytes; arriving (once per lane) on those this warp did not fill
+      // lets each complete when its weight tile lands, so the producer's drain
+      // sees the copies end instead of running to its bound.  Every position
+      // before `stop` was filled, and the producer is at most STAGES positions
+      // ahead, so each of these barriers is in the phase of that position.
+      volatile int* done_flag = &sh.producer_done;
+      const uint64_t t_start = globaltimer_ns();
+      for (uint32_t polls = 0; *done_flag == 0; ++polls)
+        if (globaltimer_ns() - t_start > kWaitNs || polls > kWaitPolls) break;
+      if (*done_flag != 0) {
+        const int armed = *reinterpret_cast<volatile int*>(&sh.armed);
+        for (int q2 = stop; q2 < armed; ++q2) mbar_arrive(&sh.full[q2 % STAGES]);
+      }
+    }
   }
 
   fence_before();
   __syncthreads();
+  if (warp == 0 && lane == 0 && *abort_flag) {  // also an abort raised after the producer left its loop
+    const int armed = sh.armed;
+    for (int j = armed > STAGES ? armed - STAGES : 0; j < armed; ++j)
+      mbar_drain(&sh.full[j % STAGES], (j / STAGES) & 1, &g_err);
+  }
   if (warp == 1) {
     __syncwarp();
     fence_after();
