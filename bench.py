@@ -489,6 +489,52 @@ def _time_stages_graph(serial, inp, steps, warmup, dev):
     return {n: sum(v) / len(v) for n, v in stage_ms.items()}
 
 
+def _event_node_overhead(dev, n=20, replays=10):
+    """What an event pair around one kernel adds to that kernel's time inside a
+    CUDA graph (the event nodes and the kernel's launch after one): a small
+    combine (T=64, H=2048, k=6, bf16) captured n times back to back with events
+    only at the two ends, and n times between event pairs of its own.  Returns
+    ms = mean event-pair time - back-to-back time per kernel, or None."""
+    from token_expert_routing_gb300 import _abi
+    try:
+        torch.cuda.Event(enable_timing=True, external=True)
+    except TypeError:
+        return None
+    gen = torch.Generator().manual_seed(7)
+    T, H, k = 64, 2048, 6
+    P = T * k
+    p2s = torch.randperm(P, generator=gen).to(torch.int32).to(dev)
+    w = torch.rand(T, k, generator=gen).to(dev)
+    y = torch.randn(P, H, generator=gen).to(torch.bfloat16).to(dev)
+    out = torch.empty(T, H, dtype=torch.bfloat16, device=dev)
+    side = torch.cuda.Stream(device=dev)
+    side.wait_stream(torch.cuda.current_stream(dev))
+    _abi.semmoe_combine(y, p2s, w, None, T, H, k, P, out, side)
+    torch.cuda.synchronize(dev)
+    per_kernel = {}
+    for mode in ("ends", "pairs"):
+        evs = [torch.cuda.Event(enable_timing=True, external=True) for _ in range(2 * n)]
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=side):
+            for i in range(n):
+                if mode == "pairs" or i == 0:
+                    evs[2 * i].record(side)
+                _abi.semmoe_combine(y, p2s, w, None, T, H, k, P, out, side)
+                if mode == "pairs" or i == n - 1:
+                    evs[2 * i + 1].record(side)
+        vals = []
+        for r in range(replays + 3):
+            g.replay()
+            torch.cuda.synchronize(dev)
+            if r >= 3:
+                vals.append(evs[0].elapsed_time(evs[2 * n - 1]) / n if mode == "ends" else
+                            sum(evs[2 * i].elapsed_time(evs[2 * i + 1]) for i in range(n)) / n)
+        per_kernel[mode] = sorted(vals)[len(vals) // 2]
+        del g
+    _abi.semmoe_check_errors()
+    return max(0.0, per_kernel["pairs"] - per_kernel["ends"])
+
+
 def _time_graph(layer, spec, d, inp, steps, warmup, world, dev, local):
     """The same forward as one CUDA-graph replay per step (static buffers)."""
     from token_expert_routing_gb300 import CapturedLayer, _abi
@@ -525,8 +571,11 @@ def _time_graph(layer, spec, d, inp, steps, warmup, world, dev, local):
             "clocks": clocks_graph.summary()}
 
 
-def _roofline_and_stages(spec, P, active, fused_gather, stage_avg, peaks):
-    """The grouped FFN's roofline object and every stage's fraction of its bound."""
+def _roofline_and_stages(spec, P, active, fused_gather, stage_avg, peaks, event_ms=None):
+    """The grouped FFN's roofline object and every stage's fraction of its bound.
+    With event_ms (what the event pair around a step adds to it in graph
+    replay), each stage also gets its time and fractions less that overhead
+    (ms_net, frac_*_net)."""
     fb = _flops_bytes(spec, P, active, fused_gather)
     ffn_ms = stage_avg["grouped_ffn"]
     ffn = fb["grouped_ffn"]
@@ -567,6 +616,13 @@ def _roofline_and_stages(spec, P, active, fused_gather, stage_avg, peaks):
         if "bytes" in f:
             ent["gbs"] = f["bytes"] / (avg * 1e-3) / 1e9
             ent["frac_hbm"] = ent["gbs"] / peaks["hbm_gbs"]
+        if event_ms is not None and avg > event_ms:
+            net = avg - event_ms
+            ent["ms_net"] = net
+            if "flops" in f:
+                ent["frac_tensor_net"] = f["flops"] / (net * 1e-3) / 1e12 / peaks["bf16_tflops"]
+            if "bytes" in f:
+                ent["frac_hbm_net"] = f["bytes"] / (net * 1e-3) / 1e9 / peaks["hbm_gbs"]
         stages[name] = ent
     return roofline, stages
 
@@ -577,7 +633,7 @@ def _inputs_on(spec, d, dev):
             None if per_token else spec.k, int(d["k_per_token"].sum()))
 
 
-def _other_workloads(args, world, dev, stream, local, peaks):
+def _other_workloads(args, world, dev, stream, local, peaks, event_ms=None):
     """The other large workloads, timed the same way with fewer steps: their
     graph-replay throughput, FFN roofline and the permute / combine / route
     fractions of HBM (the survey's HBM targets apply on each)."""
@@ -593,7 +649,8 @@ def _other_workloads(args, world, dev, stream, local, peaks):
         gst = None if args.no_graph else _time_stages_graph(serial, inp, steps, args.warmup, dev)
         res = layer.forward(*inp[:4], inp[4], stream=stream)
         active = int((res.expert_counts > 0).sum())
-        roof, stages = _roofline_and_stages(spec, inp[4], active, serial.fused_gather, gst or ev["stage_avg"], peaks)
+        roof, stages = _roofline_and_stages(spec, inp[4], active, serial.fused_gather, gst or ev["stage_avg"], peaks,
+                                            event_ms if gst else None)
         eager_value = spec.T * steps * world / (ev["ms_max"] * 1e-3)
         best = gr if gr is not None and gr["ms_per_step"] < ev["ms_max"] / steps else None
         out[name] = {
@@ -674,14 +731,16 @@ def run_ours(args, world, rank, local):
     around = None if args.no_around else _time_around_layer(args, spec, d, layer, dev, stream)
 
     peaks = _peaks()
-    others = None if args.no_also else _other_workloads(args, world, dev, stream, local, peaks)
+    event_ms = None if args.no_graph else _event_node_overhead(dev)
+    others = None if args.no_also else _other_workloads(args, world, dev, stream, local, peaks, event_ms)
 
     if rank != 0:
         return
     res = layer.forward(x, ids, kpt, k, P, stream=stream)
     active = int((res.expert_counts > 0).sum())
     counts = res.counts.cpu().numpy()
-    roofline, stages = _roofline_and_stages(spec, P, active, serial.fused_gather, graph_stages or stage_avg, peaks)
+    roofline, stages = _roofline_and_stages(spec, P, active, serial.fused_gather, graph_stages or stage_avg, peaks,
+                                            event_ms if graph_stages else None)
     _, stages_eager = _roofline_and_stages(spec, P, active, serial.fused_gather, stage_avg, peaks)
     roofline["timed_in"] = ("the one-stream forward captured as a CUDA graph, events between its steps (one "
                             "replay per step, mean over the replays)" if graph_stages else
@@ -715,6 +774,10 @@ def run_ours(args, world, rank, local):
         "roofline": roofline,
         "stages": stages,
         "stages_eager": stages_eager,
+        "stages_event_overhead_ms": event_ms,
+        "stages_event_overhead_how": ("what an event pair adds to one kernel inside a CUDA graph: a small combine "
+                                      "20x back to back against 20x each between its own event pair; ms_net and "
+                                      "frac_*_net are the graph-timed stages less this"),
         "cpu_baseline": cpu,
         "clocks": best["clocks"],
         "local_activation_rate": float(np.trace(counts) / counts.sum()),

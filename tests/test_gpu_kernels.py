@@ -163,6 +163,9 @@ def test_combine(dtype, shared):
     ("bf16", 129, 520, 64, 32, False),      # every lane holds a slot
     ("bf16", 65, 264, 64, 33, True),        # budgets above 32: the slot read directly
     ("f32", 3, 4, 8, 2, False),             # rows of 16 bytes
+    ("bf16", 700, 2048, 256, 24, False),    # the MoE-Prism budget: eight batches of three slots
+    ("bf16", 500, 1032, 64, 23, True),      # 23 slots + the shared row, a ragged last pass
+    ("f32", 2000, 1024, 64, 8, True),       # fp32 rows, many passes per warp
 ])
 def test_combine_shapes(dtype, T, H, E, k_max, shared):
     """Combine against the oracle on ragged widths and budgets, output

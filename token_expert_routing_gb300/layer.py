@@ -90,7 +90,8 @@ class MoELayer:
         # the FFN; overlap_shared: the shared experts' FFN runs there too, from
         # the start of the forward (shared_at="start": it fills the SMs the
         # router and permute leave idle), after the router ("route", measured
-        # the same) or after the permute ("permute", 4-7% slower)
+        # the same) or after the permute ("permute", 4-7% slower); without
+        # overlap_shared it runs at that point in order on the caller's stream
         self.overlap, self.overlap_shared = overlap, overlap_shared
         if shared_at not in ("start", "route", "permute"):
             raise ValueError("shared_at is 'start', 'route' or 'permute'")
@@ -200,18 +201,23 @@ class MoELayer:
         y_shared = None
         shared_side = self.ws13 is not None and self.overlap_shared
 
-        def shared_on_side():
+        def run_shared():  # the shared experts' FFN: on the second stream, or in order on this one
             nonlocal y_shared
             y_shared = torch.empty(T, H, dtype=x.dtype, device=dev)
             wss = self._workspace("shared", abi.semmoe_shared_ffn_workspace_size(T, self.I_s, dcode))
+            if not shared_side:
+                abi.semmoe_shared_ffn(x, self.ws13, self.ws2, T, H, self.I_s, y_shared, wss, s)
+                mark("shared_ffn")
+                return
             fork()
             ev1 = side_event() if side_marks is not None else None
             abi.semmoe_shared_ffn(x, self.ws13, self.ws2, T, H, self.I_s, y_shared, wss, side)
             if side_marks is not None:
                 side_marks.append(("shared_ffn", ev1, side_event()))
 
-        if shared_side and self.shared_at == "start":
-            shared_on_side()
+        has_shared = self.ws13 is not None
+        if has_shared and self.shared_at == "start":
+            run_shared()
         if k_per_token is None:
             if k is None:
                 raise ValueError("give k or k_per_token")
@@ -237,8 +243,8 @@ class MoELayer:
                                   k or 0, T, H, Ep, k_max, topk_idx, topk_w, ws, stream, w_dtype=wd,
                                   pair_counts=pair_counts)
         mark("route")
-        if shared_side and self.shared_at == "route":
-            shared_on_side()
+        if has_shared and self.shared_at == "route":
+            run_shared()
         ts = s
         if self.overlap:  # lookup .. counts on the second stream
             fork()
@@ -285,8 +291,8 @@ class MoELayer:
         mark("permute")
         y_perm = None if self.fused_combine else torch.empty(P, H, dtype=x.dtype, device=dev)
         acc = torch.empty(T, H, dtype=torch.float32, device=dev) if self.fused_combine else None
-        if shared_side and self.shared_at == "permute":  # the shared experts beside the routed FFN
-            shared_on_side()
+        if has_shared and self.shared_at == "permute":  # the shared experts beside the routed FFN
+            run_shared()
         ws = self._workspace("ffn", abi.semmoe_grouped_ffn_workspace_size(P, I, dcode))
         if self.fused_combine:  # GEMM2 adds its rows into the token order
             abi.semmoe_grouped_ffn_combine(x if self.fused_gather else x_perm, self.fused_gather, sorted_to_pair,
@@ -299,11 +305,6 @@ class MoELayer:
             abi.semmoe_grouped_ffn(x_perm, expert_offsets, phys_to_expert, self.w13, self.w2, P, E, H, I,
                                    y_perm, ws, stream)
         mark("grouped_ffn")
-        if self.ws13 is not None and not shared_side:
-            y_shared = torch.empty(T, H, dtype=x.dtype, device=dev)
-            ws = self._workspace("shared", abi.semmoe_shared_ffn_workspace_size(T, self.I_s, dcode))
-            abi.semmoe_shared_ffn(x, self.ws13, self.ws2, T, H, self.I_s, y_shared, ws, stream)
-            mark("shared_ffn")
         if forked:
             join()  # the second stream's steps are done before the combine (and the call's end)
         out = torch.empty(T, H, dtype=x.dtype, device=dev)
