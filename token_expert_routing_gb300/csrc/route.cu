@@ -108,7 +108,9 @@ __device__ __forceinline__ void warp_load_logits(const float* row, int ks, size_
 // below every float including -inf).  Two forms with the same picks: rescanning
 // the lane's keys every round (cheaper for 2-4 scores per lane), or sorting them
 // once (13% faster than rescanning at 8 per lane, E = 256, k <= 24; 3-6% slower
-// at 2-4).
+// at 2-4).  In the sorted form the winning lane's next key comes from shared
+// memory instead of shifting its registers: 16.2 against 17.5 us per top-k of
+// 8192 tokens at E = 256, k <= 24 (CUDA graph of 20 calls).
 
 // Few scores per lane (NPER <= 4): each round rescans the lane's keys -- two
 // warp reductions (the largest key, then the lowest index holding it), and the
@@ -150,13 +152,16 @@ __device__ __forceinline__ void warp_select_rescan(const float (&v)[NPER], int n
 
 // Many scores per lane (NPER >= 8): each score's key is packed with its inverted
 // index into a 64-bit word that orders (score descending, index ascending).
-// Each lane sorts its NPER words once; a round is then two warp reductions over
-// the lanes' heads (the largest key, then the lowest index holding it) and the
-// winning lane drops its head.  A head with the round's key is its lane's
-// lowest index with that key, so the lowest index among heads is the lowest
-// overall.
+// Each lane sorts its NPER words once and keeps the first in a register (its
+// head) and the rest, then a 0, in `lists` (shared memory, [NPER][32] words
+// for the warp, entry i of lane l at i * 32 + l).  A round is two warp
+// reductions over the heads (the largest key, then the lowest index holding
+// it); the winning lane loads its next word as its new head.  A head with the
+// round's key is its lane's lowest index with that key, so the lowest index
+// among heads is the lowest overall.
 template <int NPER>
-__device__ __forceinline__ void warp_select_sorted(const float (&v)[NPER], int n, int kt, float* my_v, int* my_e) {
+__device__ __forceinline__ void warp_select_sorted(const float (&v)[NPER], int n, int kt, float* my_v, int* my_e,
+                                                   unsigned long long* lists) {
   const int lane = threadIdx.x % 32;
   unsigned long long c[NPER];
 #pragma unroll
@@ -173,18 +178,19 @@ __device__ __forceinline__ void warp_select_sorted(const float (&v)[NPER], int n
       c[j - 1] = a > d ? a : d;
       c[j] = a > d ? d : a;
     }
+#pragma unroll
+  for (int i = 1; i < NPER; ++i) lists[(i - 1) * 32 + lane] = c[i];
+  lists[(NPER - 1) * 32 + lane] = 0ull;  // a lane can win NPER times, then its head is 0
+  unsigned long long head = c[0];
+  int pos = 0;
   for (int j = 0; j < kt; ++j) {
-    const uint32_t hk = (uint32_t)(c[0] >> 32);
+    const uint32_t hk = (uint32_t)(head >> 32);
     const uint32_t m = __reduce_max_sync(0xffffffffu, hk);
     int be = -1;
     if (m != 0u) {
-      const uint32_t mine = hk == m ? ~(uint32_t)c[0] : 0xffffffffu;  // the head's index
+      const uint32_t mine = hk == m ? ~(uint32_t)head : 0xffffffffu;  // the head's index
       be = (int)__reduce_min_sync(0xffffffffu, mine);
-      if (mine == (uint32_t)be) {  // this lane's head is the pick: drop it
-#pragma unroll
-        for (int i = 0; i + 1 < NPER; ++i) c[i] = c[i + 1];
-        c[NPER - 1] = 0ull;
-      }
+      if (mine == (uint32_t)be) head = lists[(pos++) * 32 + lane];  // this lane's head is the pick
     } else if (lane == 0) {
       flag(SEMMOE_DEVERR_NONFINITE);  // fewer than kt scores
     }
@@ -196,25 +202,31 @@ __device__ __forceinline__ void warp_select_sorted(const float (&v)[NPER], int n
   __syncwarp();
 }
 
+// lists: the warp's [NPER][32] words of shared memory when NPER >= 8 (else unused)
 template <int NPER>
-__device__ __forceinline__ void warp_select(const float (&v)[NPER], int n, int kt, float* my_v, int* my_e) {
-  if constexpr (NPER >= 8) warp_select_sorted<NPER>(v, n, kt, my_v, my_e);
+__device__ __forceinline__ void warp_select(const float (&v)[NPER], int n, int kt, float* my_v, int* my_e,
+                                            unsigned long long* lists) {
+  if constexpr (NPER >= 8) warp_select_sorted<NPER>(v, n, kt, my_v, my_e, lists);
   else warp_select_rescan<NPER>(v, n, kt, my_v, my_e);
 }
+
+// Words of selection lists per warp (warp_select) for NPER scores per lane.
+__host__ __device__ constexpr int sel_list_words(int nper) { return nper >= 8 ? 32 * nper : 1; }
 
 // One warp routes token t: its logits (see warp_load_logits), k_t picks (see
 // warp_select), then the gates, the softmax of the selected logits
 // renormalised over the selection (fp32).  my_v / my_e: k_max floats / ints of
-// scratch for this warp.
+// scratch for this warp; lists: its selection lists (warp_select).
 template <int NPER>  // logits held per lane: E <= 32 * NPER
 __device__ void warp_topk(const float* row, int ks, size_t slice_stride, float* logits_out, int E, int t,
                           const int32_t* __restrict__ k_per_token, int k_uniform, int k_max, float* my_v, int* my_e,
-                          int32_t* __restrict__ topk_idx, float* __restrict__ topk_w, const PairCounts& pc) {
+                          unsigned long long* lists, int32_t* __restrict__ topk_idx, float* __restrict__ topk_w,
+                          const PairCounts& pc) {
   const int lane = threadIdx.x % 32;
   const int kt = warp_budget(k_per_token, k_uniform, k_max, t);
   float v[NPER];
   warp_load_logits<NPER>(row, ks, slice_stride, logits_out, E, v);
-  warp_select<NPER>(v, E, kt, my_v, my_e);
+  warp_select<NPER>(v, E, kt, my_v, my_e, lists);
   const float m = my_v[0];
   float den = 0.f;
   for (int j = lane; j < kt; j += 32) den += my_e[j] >= 0 ? expf(my_v[j] - m) : 0.f;
@@ -301,12 +313,14 @@ route_kernel(const TX* __restrict__ x, const TW* __restrict__ w, const float* __
   __syncthreads();
 
   // Top-k_t per token, one warp per token.
+  __shared__ unsigned long long sel_lists[kWarps * sel_list_words(kRouteMaxE / 32)];
   const int warp = tid / 32;
   for (int tl = warp; tl < kRouteTok; tl += kWarps) {
     const int t = t0 + tl;
     if (t >= T) break;
     warp_topk<kRouteMaxE / 32>(lg + tl * Epad, 1, 0, nullptr, E, t, k_per_token, k_uniform, k_max,
-                               sel_v + warp * k_max, sel_e + warp * k_max, topk_idx, topk_w, pc);
+                               sel_v + warp * k_max, sel_e + warp * k_max,
+                               sel_lists + warp * sel_list_words(kRouteMaxE / 32), topk_idx, topk_w, pc);
   }
 }
 
@@ -321,13 +335,15 @@ topk_kernel(const float* __restrict__ logits, int ks, float* __restrict__ logits
             const int32_t* __restrict__ k_per_token, int k_uniform, int T, int E, int k_max,
             int32_t* __restrict__ topk_idx, float* __restrict__ topk_w, PairCounts pc) {
   extern __shared__ __align__(16) unsigned char smem_raw[];
+  __shared__ unsigned long long sel_lists[kTopkWarps * sel_list_words(NPER)];
   float* sel_v = reinterpret_cast<float*>(smem_raw);
   int* sel_e = reinterpret_cast<int*>(sel_v + kTopkWarps * k_max);
   const int warp = threadIdx.x / 32;
   const int t = blockIdx.x * kTopkWarps + warp;
   if (t >= T) return;
   warp_topk<NPER>(logits + (size_t)t * E, ks, (size_t)T * E, logits_out != nullptr ? logits_out + (size_t)t * E : nullptr,
-            E, t, k_per_token, k_uniform, k_max, sel_v + warp * k_max, sel_e + warp * k_max, topk_idx, topk_w, pc);
+            E, t, k_per_token, k_uniform, k_max, sel_v + warp * k_max, sel_e + warp * k_max,
+            sel_lists + warp * sel_list_words(NPER), topk_idx, topk_w, pc);
 }
 
 // MoE-Prism's training-free hierarchical gating, one warp per token: the
@@ -342,6 +358,7 @@ hier_topk_kernel(const float* __restrict__ logits, int ks, float* __restrict__ l
                  int T, int Ep, int k_max, int32_t* __restrict__ topk_idx, float* __restrict__ topk_w,
                  PairCounts pc) {
   extern __shared__ __align__(16) unsigned char smem_raw[];
+  __shared__ unsigned long long sel_lists[kTopkWarps * sel_list_words(NPER)];
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   float* base = reinterpret_cast<float*>(smem_raw);
   float* lg = base + warp * Ep;
@@ -371,7 +388,7 @@ hier_topk_kernel(const float* __restrict__ logits, int ks, float* __restrict__ l
       else flag(SEMMOE_DEVERR_NONFINITE);
     }
   }
-  warp_select<NPER>(sc, E, kt, sel_v, sel_e);
+  warp_select<NPER>(sc, E, kt, sel_v, sel_e, sel_lists + warp * sel_list_words(NPER));
   float m = -INFINITY;
   for (int j = lane; j < kt; j += 32)
     if (sel_e[j] >= 0) m = fmaxf(m, lg[sel_e[j] / N]);
@@ -472,7 +489,8 @@ cudaError_t launch_route_t(const void* x, const void* w, const float* li, float*
                            cudaStream_t s, PairCounts pc = PairCounts()) {
   size_t sm = route_smem_bytes(E, k_max);
   auto kern = route_kernel<TX, TW>;
-  if (sm > 48 * 1024) {  // raise the limit once to the largest layout (E = k_max = 256)
+  {  // raise the limit once to the largest layout (E = k_max = 256; with the 16 KB of
+     // static selection lists, layouts above 32 KB need it)
     static std::atomic<unsigned long long> smem_set{0};
     cudaError_t e = ensure_smem_limit(kern, (int)route_smem_bytes(kRouteMaxE, kRouteMaxE), smem_set);
     if (e != cudaSuccess) return e;
