@@ -144,7 +144,10 @@ def _flops_bytes(spec, P, active_experts, fused_gather=False):
     T, H, E, I, k = spec.T, spec.H, spec.E, spec.I, spec.k_max
     Is = spec.I_shared
     return {
-        "route": dict(flops=2 * T * H * E, bytes=T * H * s + E * H * sr + T * k * 8),
+        # an fp32 router weight times bf16 activations runs on the tensor cores as three
+        # exact bf16 parts: three times the GEMM's flops executed (flops_executed)
+        "route": dict(flops=2 * T * H * E, bytes=T * H * s + E * H * sr + T * k * 8,
+                      flops_executed=(3 if spec.router_dtype == "f32" and spec.dtype == "bf16" else 1) * 2 * T * H * E),
         "permute": dict(bytes=4 * T * k * 2 + 4 * P + 4 * T * k + (0 if fused_gather else T * H * s + P * H * s)),
         "grouped_ffn": dict(flops=6 * H * I * P,
                             bytes=active_experts * 3 * H * I * s + (T if fused_gather else P) * H * s
@@ -616,6 +619,8 @@ def _roofline_and_stages(spec, P, active, fused_gather, stage_avg, peaks, event_
         if "bytes" in f:
             ent["gbs"] = f["bytes"] / (avg * 1e-3) / 1e9
             ent["frac_hbm"] = ent["gbs"] / peaks["hbm_gbs"]
+        if "flops_executed" in f:
+            ent["frac_tensor_executed"] = f["flops_executed"] / (avg * 1e-3) / 1e12 / peaks["bf16_tflops"]
         if event_ms is not None and avg > event_ms:
             net = avg - event_ms
             ent["ms_net"] = net
