@@ -289,13 +289,15 @@ SPLIT_COUNTS = [0, 1, 127, 128, 129, 255, 256, 257, 384, 511, 512, 640, 1000, 3,
 
 
 @pytest.mark.parametrize("P,E,H,I", [(1000, 8, 256, 160), (5000, 64, 512, 352), (3000, 16, 512, 640),
-                                     (sum(SPLIT_COUNTS), 16, 256, 576), (30000, 64, 512, 704)])
+                                     (sum(SPLIT_COUNTS), 16, 256, 576), (30000, 64, 512, 704),
+                                     (384, 64, 512, 1408), (3072, 64, 256, 200)])
 def test_grouped_ffn_forms_are_bit_identical(P, E, H, I):
     """Every form of the grouped GEMM -- independent CTAs, 2-SM MMA pairs with
     one or two accumulator buffers, and the shape-chosen default -- returns
     exactly the same bits, and those bits match the oracle's grouped FFN row by
     row within the bf16 tolerance; one case pins group sizes around the 128-
-    and 256-row boundaries (empty groups, 1, 127..129, 255..257 rows)."""
+    and 256-row boundaries (empty groups, 1, 127..129, 255..257 rows), two have
+    decode-sized groups (6 and 48 rows on average; I not a multiple of 128)."""
     rng = np.random.default_rng(P + E)
     if P == sum(SPLIT_COUNTS) and E == len(SPLIT_COUNTS):
         cnt = np.array(SPLIT_COUNTS)
