@@ -641,7 +641,7 @@ def _inputs_on(spec, d, dev):
 def _other_workloads(args, world, dev, stream, local, peaks, event_ms=None):
     """The other large workloads, timed the same way with fewer steps: their
     graph-replay throughput, FFN roofline and the permute / combine / route
-    fractions of HBM (the survey's HBM targets apply on each)."""
+    fractions of HBM (the 70% HBM targets of the permute and combine apply on each)."""
     out = {}
     for name in [n for n in args.also.split(",") if n and n != args.config]:
         spec = wl.CONFIGS[name]
