@@ -728,17 +728,26 @@ def test_hier_route_pair_counts():
 @pytest.mark.parametrize("T,H,E,k_max,wd,per_token", [
     (9800, 128, 8, 1, "bf16", False), (9800, 256, 64, 6, "bf16", True), (16384 + 45, 2048, 128, 8, "bf16", False),
     (20485, 256, 256, 24, "bf16", True), (9800, 200, 7, 3, "f32", True), (9800, 512, 64, 16, "f32", False),
-    (9800, 128, 64, 32, "bf16", True), (4096, 2048, 64, 6, "f32", False), (300, 200, 7, 3, "f32", True)])
+    (9800, 128, 64, 32, "bf16", True),
+    # fewer than 76 tiles: a cluster of 2, 4 or 8 CTAs per tile, each a slice of H
+    (4096, 2048, 64, 6, "f32", False), (300, 200, 7, 3, "f32", True), (64, 2048, 64, 6, "f32", True),
+    (3000, 2048, 64, 6, "f32", False), (9000, 1024, 128, 8, "bf16", True), (700, 256, 256, 24, "bf16", True),
+    (129, 512, 7, 3, "f32", True),
+    # the split-K router and a top-k kernel: H of two k-blocks, and an fp32 weight over 64 experts
+    (300, 128, 7, 3, "f32", True), (3000, 256, 256, 8, "f32", False)])
 def test_router_with_top_k_in_the_gemm_epilogue(T, H, E, k_max, wd, per_token):
     """The one-kernel router (tensor-core GEMM, top-k in the epilogue: one
     thread per token and column range, lists merged in column order), taken
-    from 76 tiles of 128 tokens on: logits within the logit tolerance of the
-    oracle, picks bit-exact against the oracle's top-k of the GPU's own logits,
-    gates within the gate tolerance, and the count table equal to the per-chunk
-    histogram of the picks.  Covers ragged last tiles, per-token budgets, a grid
-    beyond one CTA per SM (T = 20485), k_max of 8, 16 and 32, fp32 weights split
-    into bf16 parts, column groups left empty (E = 7), and two grids below 76
-    tiles that take the split-K router and a top-k kernel instead."""
+    from 76 tiles of 128 tokens on, and below that its cluster form (each CTA
+    of a tile's cluster contracts a slice of H; the partial logits are added in
+    slice order through distributed shared memory, CS threads per row select):
+    logits within the logit tolerance of the oracle, picks bit-exact against
+    the oracle's top-k of the GPU's own logits, gates within the gate
+    tolerance, and the count table equal to the per-chunk histogram of the
+    picks.  Covers ragged last tiles, per-token budgets, a grid beyond one CTA
+    per SM (T = 20485), k_max of 8, 16 and 32, fp32 weights split into bf16
+    parts, column groups left empty (E = 7), clusters of 2, 4 and 8, and two
+    shapes that take the split-K router and a top-k kernel."""
     a = abi()
     rng = np.random.default_rng(T + E + k_max)
     x = torch.from_numpy((rng.standard_normal((T, H)) / np.sqrt(H)).astype(np.float32)).to(torch.bfloat16)

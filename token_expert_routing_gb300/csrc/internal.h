@@ -37,6 +37,13 @@ bool route_topk_tc_ok(int E, int k_max, int w_dtype);
 cudaError_t launch_route_topk_tc(const void* x, const void* w, int w_dtype, int T, int H, int E, int k_max,
                                  float* logits_out, const int32_t* kpt, int k_uniform, int32_t* topk_idx,
                                  float* topk_w, int32_t* counts, int count_stride, void* split, cudaStream_t s);
+// The same for fewer token tiles than SMs: a cluster of CS CTAs per tile, each
+// contracting a slice of H, reduced through distributed shared memory.
+// route_topk_cl_slices gives CS (0: not applicable).
+int route_topk_cl_slices(int T, int H, int E, int k_max, int w_dtype);
+cudaError_t launch_route_topk_cl(const void* x, const void* w, int w_dtype, int T, int H, int E, int k_max, int CS,
+                                 float* logits_out, const int32_t* kpt, int k_uniform, int32_t* topk_idx,
+                                 float* topk_w, int32_t* counts, int count_stride, void* split, cudaStream_t s);
 // pair_counts (nullable): zeroed here, then the live picks are counted into it
 // (layout of pair_counts_bytes).
 cudaError_t launch_route(const void* x, int x_dtype, const void* w, int w_dtype,

@@ -447,6 +447,272 @@ route_topk_tc_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_con
   }
 }
 
+// ---------------------------------------------------------------------------
+// Router GEMM and top-k in one launch for fewer token tiles than SMs: a
+// cluster of CS CTAs per 128-token tile, CTA s of the cluster contracting the
+// s-th of CS slices of H into its own TMEM accumulator.  Each CTA leaves its
+// partial logits (the weight parts already added, as in route_tc_kernel) in its
+// shared memory; after a cluster barrier CTA r takes the tile rows
+// [r * 128 / CS, (r + 1) * 128 / CS) and adds the CS partials of each row in
+// slice order, which it receives by bulk copies that each CTA pushes into the
+// others' shared memory (a fixed order: the logits do not depend on timing;
+// loads of the other CTAs' shared memory, thread by thread, measured 9-25 us
+// for this), one warp per row, then selects as the top-k kernel
+// does: k_t rounds of a warp argmax over order-preserving keys (ties to the
+// lower expert), then the gates and the picks.  (Per-thread sorted lists
+// merged across the row's threads measured slower here: the merge is one long
+// dependent chain per row.)  The CTAs' pick histograms are added
+// by the cluster's CTA 0, which writes the tile's column of the count table.
+// No logits in memory, no second launch; every cluster barrier is reached by
+// every thread on every path.  One CTA per SM (the host keeps tiles x CS <= SMs).
+// ---------------------------------------------------------------------------
+constexpr int kClThreads = 64 + 4 * 128;  // producer, MMA, 16 epilogue / selection warps
+
+template <int S, int NPER>  // NPER experts per lane in the selection: E <= 32 * NPER
+__global__ void __launch_bounds__(kClThreads, 1)
+route_topk_cl_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_constant__ CUtensorMap map_w, int T,
+                     int H, int E, int E16, int CS, int stages, int kb_slice, float* __restrict__ logits_out,
+                     const int32_t* __restrict__ k_per_token, int k_uniform, int k_max,
+                     int32_t* __restrict__ topk_idx, float* __restrict__ topk_w, int32_t* __restrict__ counts,
+                     int count_stride) {
+  extern __shared__ __align__(1024) unsigned char smem_raw[];
+  const uint32_t pad = (1024u - (smem_u32(smem_raw) & 1023u)) & 1023u;
+  unsigned char* ring = smem_raw + pad;
+  Shared& sh = *reinterpret_cast<Shared*>(ring + stage_budget(1));
+  __shared__ int hist[256];
+  __shared__ uint64_t recv_bar;  // the other CTAs' partial rows for this CTA's rows have landed
+  volatile int* abort_flag = &sh.abort_flag;
+
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  const int NB = S * E16;
+  const uint32_t b_bytes = (uint32_t)NB * BK * 2;
+  const uint32_t stage_bytes = A_BYTES + b_bytes;
+  const int rank = (int)cluster_ctarank();
+  const int tile = blockIdx.x / CS;
+  const int t0 = tile * BM;
+  const int kb_all = (H + BK - 1) / BK;
+  const int kb0 = rank * kb_slice;
+  const int kb_n = kb_all - kb0 < kb_slice ? kb_all - kb0 : kb_slice;  // >= 1 by the host's choice of CS
+  const int kb_first = tile % kb_n;  // tiles start at different k-blocks of their slice
+  // after the MMAs, in the operand ring: this CTA's partial logits [128][E16 + 4]
+  // fp32, then what the others send of theirs for this CTA's rows: recv[s] =
+  // slice s's rows [rank * rpc, (rank + 1) * rpc)
+  const int pstride = E16 + 4;
+  const int rpc = BM / CS;
+  float* part = reinterpret_cast<float*>(ring);
+  float* recv = part + (size_t)BM * pstride;
+  const uint32_t slice_bytes = (uint32_t)(rpc * pstride * 4);
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < stages; ++s) {
+      mbar_init(&sh.full[s], 1);
+      mbar_init(&sh.empty[s], 1);
+    }
+    mbar_init(&sh.tfull, 1);
+    mbar_init(&sh.done, 1);
+    mbar_init(&recv_bar, 1);
+    mbar_expect_tx(&recv_bar, (uint32_t)(CS - 1) * slice_bytes);  // the one arrival; the copies' bytes follow
+    sh.abort_flag = 0;
+    mbar_init_fence();
+    prefetch_map(&map_x);
+    prefetch_map(&map_w);
+  }
+  for (int e = threadIdx.x; e < 256; e += blockDim.x) hist[e] = 0;
+  if (warp == 1) tmem_alloc(&sh.tmem_base, TMEM_COLS);
+  fence_before();
+  __syncthreads();  // (the other CTAs see the receive barrier once past the cluster barrier before the copies)
+  fence_after();
+  const uint32_t tmem = sh.tmem_base;
+
+  if (warp == 0) {
+    if (lane == 0) {  // TMA producer: this CTA's k-blocks
+      int it = 0;
+      for (int i = 0; i < kb_n; ++i) {
+        const int kb = kb0 + (kb_first + i < kb_n ? kb_first + i : kb_first + i - kb_n);
+        const int s = i % stages;
+        const uint32_t ph = (i / stages) & 1;
+        if (!mbar_wait(&sh.empty[s], ph ^ 1, abort_flag, &g_err)) break;
+        unsigned char* st = ring + (size_t)s * stage_bytes;
+        mbar_expect_tx(&sh.full[s], stage_bytes);
+        tma_load_2d(st, &map_x, &sh.full[s], kb * BK, t0);
+        tma_load_2d(st + A_BYTES, &map_w, &sh.full[s], kb * BK, 0);
+        ++it;
+      }
+      if (*abort_flag)
+        for (int j = it > stages ? it - stages : 0; j < it; ++j)
+          mbar_drain(&sh.full[j % stages], (j / stages) & 1, &g_err);
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {  // MMA issuer
+      const uint32_t idesc = idesc_bf16_f32(BM, NB);
+      bool ok = true;
+      for (int i = 0; i < kb_n; ++i) {
+        const int s = i % stages;
+        const uint32_t ph = (i / stages) & 1;
+        if (!mbar_wait(&sh.full[s], ph, abort_flag, &g_err)) { ok = false; break; }
+        fence_after();
+        const uint32_t sa = smem_u32(ring + (size_t)s * stage_bytes), sb = sa + A_BYTES;
+#pragma unroll
+        for (int k = 0; k < BK / UK; ++k)
+          mma_bf16(tmem, sw128_desc(sa + k * UK * 2), sw128_desc(sb + k * UK * 2), idesc, (i | k) != 0);
+        commit(&sh.empty[s]);
+      }
+      if (ok) commit(&sh.tfull);
+      commit(&sh.done);
+      mbar_drain(&sh.done, 0, &g_err);
+    }
+  } else {  // 16 epilogue warps: the rows of their TMEM lane quarter, a quarter of the columns, into `part`
+    const int q = warp & 3, r = q * 32 + lane, g = (warp - 2) / 4;
+    const int nch = E16 / 16, c_lo = (g * nch / 4) * 16, c_hi = ((g + 1) * nch / 4) * 16;
+    int ok = 1;
+    if (lane == 0) ok = mbar_wait(&sh.tfull, 0, abort_flag, &g_err);
+    ok = __shfl_sync(0xffffffffu, ok, 0);
+    if (ok) {
+      fence_after();
+      const uint32_t trow = tmem + ((uint32_t)(q * 32) << 16);
+      for (int c = c_lo; c < c_hi; c += 16) {
+        uint32_t v0[16], v1[16], v2[16];
+        tmem_ld16(trow + c, v0);
+        if (S == 3) {
+          tmem_ld16(trow + E16 + c, v1);
+          tmem_ld16(trow + 2 * E16 + c, v2);
+        }
+        tmem_ld_wait();
+        float l[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          l[i] = __uint_as_float(v0[i]);
+          if (S == 3) l[i] = (l[i] + __uint_as_float(v1[i])) + __uint_as_float(v2[i]);
+        }
+#pragma unroll
+        for (int j = 0; j < 4; ++j)  // row stride E16 + 4 words: the 16-byte stores of 8 lanes hit 8 bank groups
+          *reinterpret_cast<float4*>(part + (size_t)r * pstride + c + 4 * j) =
+              make_float4(l[4 * j], l[4 * j + 1], l[4 * j + 2], l[4 * j + 3]);
+      }
+    }
+    fence_async_smem();  // the rows are read by bulk copies next
+  }
+  fence_before();
+  cluster_sync_all();  // every CTA is done with its operand ring, where the copies land
+  // push: the rows of CTA q go to q (even after an abort, so that every receive completes)
+  if (threadIdx.x == 64)
+    for (int q = 0; q < CS; ++q)
+      if (q != rank)
+        bulk_copy_to_peer(mapa_rank(recv + (size_t)rank * rpc * pstride, (uint32_t)q),
+                          part + (size_t)q * rpc * pstride, slice_bytes, mapa_rank(&recv_bar, (uint32_t)q));
+
+  // selection: CTA `rank` takes rows [rank * rpc, (rank + 1) * rpc); one warp
+  // per row (16 warps: a row's chain of rounds is latency, so rows run side by
+  // side), lane l holding experts l + 32 i; k_t rounds of a warp argmax (the
+  // largest key, then the lowest expert holding it, which is taken out)
+  if (warp >= 2) {
+    const bool got = mbar_wait(&recv_bar, 0, abort_flag, &g_err);  // every lane: acquire the copies
+    for (int row = rank * rpc + (warp - 2); got && row < (rank + 1) * rpc; row += kClThreads / 32 - 2) {
+      const int t = t0 + row;
+      int kt = 0;  // loaded first: its latency overlaps the sums
+      if (t < T) kt = k_per_token != nullptr ? k_per_token[t] : k_uniform;
+      float l[NPER];
+#pragma unroll
+      for (int s = 0; s < 8; ++s) {  // slice order
+        if (s < CS) {
+          const float* src = s == rank ? part + (size_t)row * pstride
+                                       : recv + ((size_t)s * rpc + (row - rank * rpc)) * pstride;
+#pragma unroll
+          for (int i = 0; i < NPER; ++i) {
+            const float v = lane + 32 * i < E ? src[lane + 32 * i] : 0.f;
+            l[i] = s == 0 ? v : l[i] + v;
+          }
+        }
+      }
+      bool nonfinite = false;
+      uint32_t key[NPER];
+#pragma unroll
+      for (int i = 0; i < NPER; ++i) {
+        const int e = lane + 32 * i;
+        key[i] = 0u;
+        if (e < E) {
+          if (logits_out != nullptr && t < T) logits_out[(size_t)t * E + e] = l[i];
+          float lv = l[i];
+          if (!isfinite(lv)) {
+            nonfinite = true;
+            lv = -INFINITY;
+          }
+          key[i] = score_key(lv);
+        }
+      }
+      if (t < T) {
+        if (kt < 1 || kt > k_max) {
+          if (lane == 0) atomicOr(&g_err, SEMMOE_DEVERR_K);
+          kt = kt < 1 ? 1 : k_max;
+        }
+        uint32_t pk = 0u;  // lane j: the j-th pick (key, expert)
+        int pe = -1;
+        for (int j = 0; j < kt; ++j) {
+          uint32_t mk = key[0];
+#pragma unroll
+          for (int i = 1; i < NPER; ++i) mk = max(mk, key[i]);
+          const uint32_t m = __reduce_max_sync(0xffffffffu, mk);
+          int be = -1;
+          if (m != 0u) {
+            uint32_t mine = 0xffffffffu;
+#pragma unroll
+            for (int i = NPER - 1; i >= 0; --i)
+              if (key[i] == m) mine = (uint32_t)(lane + 32 * i);
+            be = (int)__reduce_min_sync(0xffffffffu, mine);
+#pragma unroll
+            for (int i = 0; i < NPER; ++i)
+              if (be == lane + 32 * i) key[i] = 0u;
+          }
+          if (lane == j) {
+            pk = m;
+            pe = be;
+          }
+        }
+        const float mx = key_score(__shfl_sync(0xffffffffu, pk, 0));
+        float ex = lane < kt && pe >= 0 ? expf(key_score(pk) - mx) : 0.f;
+        float den = ex;
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) den += __shfl_xor_sync(0xffffffffu, den, off);
+        if (lane < k_max) {
+          int e = -1;
+          float gw = 0.f;
+          if (lane < kt) {
+            if (pe >= 0) {
+              e = pe;
+              gw = ex / den;
+              atomicAdd(&hist[e], 1);
+            } else {
+              atomicOr(&g_err, SEMMOE_DEVERR_NONFINITE);  // fewer than k_t scores
+            }
+          }
+          topk_idx[(size_t)t * k_max + lane] = e;
+          topk_w[(size_t)t * k_max + lane] = gw;
+        }
+        if (nonfinite) atomicOr(&g_err, SEMMOE_DEVERR_NONFINITE);
+      }
+    }
+  }
+  __syncthreads();
+  if (rank != 0 && counts != nullptr)  // this CTA's picks into CTA 0's histogram
+    for (int e = threadIdx.x; e < E; e += kClThreads)
+      if (hist[e] != 0) red_cluster_add_u32(mapa_rank(&hist[e], 0u), (uint32_t)hist[e]);
+  cluster_sync_all();  // every copy has landed, every pick is in CTA 0's histogram; then nobody
+                       // touches another CTA's shared memory
+  if (rank == 0 && counts != nullptr) {  // the tile's column of the count table
+    for (int e = threadIdx.x; e < E; e += kClThreads) counts[(size_t)e * count_stride + tile] = hist[e];
+    if (tile == 0) {  // entries past the last chunk are 0
+      const int nchunk = (int)gridDim.x / CS, padn = count_stride - nchunk;
+      for (int j = threadIdx.x; j < E * padn; j += kClThreads)
+        counts[(size_t)(j / padn) * count_stride + nchunk + j % padn] = 0;
+    }
+  }
+  if (warp == 1) {
+    __syncwarp();
+    fence_after();
+    tmem_dealloc(tmem, TMEM_COLS);
+  }
+}
+
 // Epilogue column groups: four with one CTA per SM and k_max <= 16 (the lists'
 // registers allow it), else fewer.
 template <int S, int KM, int CPS>
@@ -620,6 +886,85 @@ cudaError_t launch_route_topk_tc(const void* x, const void* w, int w_dtype, int 
   else if (km == 8) e = launch_topk_km<3, 8>(grid, cps, mx, mw, T, H, E, E16, stages, logits_out, kpt, k_uniform, k_max, topk_idx, topk_w, counts, count_stride, s);
   else if (km == 16) e = launch_topk_km<3, 16>(grid, cps, mx, mw, T, H, E, E16, stages, logits_out, kpt, k_uniform, k_max, topk_idx, topk_w, counts, count_stride, s);
   else e = launch_topk_km<3, 32>(grid, cps, mx, mw, T, H, E, E16, stages, logits_out, kpt, k_uniform, k_max, topk_idx, topk_w, counts, count_stride, s);
+  if (e != cudaSuccess) return e;
+  count_launches(1);
+  return cudaGetLastError();
+}
+
+// K slices of the cluster router: the largest CS in {2, 4, 8} with one CTA per
+// SM for every (tile, slice) and at least 2 k-blocks per slice; 0 when none
+// applies (the one-kernel router or the split-K path takes the call).  Its
+// partial and received logits (2 x 128 rows of E16 + 4 fp32) must fit the
+// 200 KB operand ring: E16 <= 192.
+int route_topk_cl_slices(int T, int H, int E, int k_max, int w_dtype) {
+  if (!route_topk_tc_ok(E, k_max, w_dtype) || (E + 15) / 16 * 16 > 192) return 0;
+  const long long tiles = (T + BM - 1) / BM;
+  const int kb_all = (H + BK - 1) / BK;
+  int cs = 0;
+  for (int c = 2; c <= 8; c *= 2)
+    if (tiles * c <= sm_count() && kb_all >= 2 * c) cs = c;
+  return cs;
+}
+
+cudaError_t launch_route_topk_cl(const void* x, const void* w, int w_dtype, int T, int H, int E, int k_max, int CS,
+                                 float* logits_out, const int32_t* kpt, int k_uniform, int32_t* topk_idx,
+                                 float* topk_w, int32_t* counts, int count_stride, void* split, cudaStream_t s) {
+  const int S = w_dtype == SEMMOE_BF16 ? 1 : 3;
+  const int E16 = (E + 15) / 16 * 16;
+  const void* wb = w;
+  int w_rows = E;
+  if (S == 3) {
+    if (w_dtype == SEMMOE_F32) {
+      cudaError_t e = launch_route_split(static_cast<const float*>(w), H, E, split, s);
+      if (e != cudaSuccess) return e;
+      wb = split;
+    }
+    w_rows = 3 * E16;
+  }
+  CUtensorMap mx, mw;
+  {
+    const cuuint64_t dims[2] = {(cuuint64_t)H, (cuuint64_t)T};
+    const cuuint64_t str[1] = {(cuuint64_t)H * 2};
+    const cuuint32_t box[2] = {BK, BM};
+    if (!make_map_bf16(&mx, x, 2, dims, str, box)) return cudaErrorInvalidValue;
+  }
+  {
+    const cuuint64_t dims[2] = {(cuuint64_t)H, (cuuint64_t)w_rows};
+    const cuuint64_t str[1] = {(cuuint64_t)H * 2};
+    const cuuint32_t box[2] = {BK, (cuuint32_t)(S * E16)};
+    if (!make_map_bf16(&mw, wb, 2, dims, str, box)) return cudaErrorInvalidValue;
+  }
+  const int kb_all = (H + BK - 1) / BK, kb_slice = (kb_all + CS - 1) / CS;
+  if ((CS - 1) * kb_slice >= kb_all) return cudaErrorInvalidValue;  // every slice holds k-blocks
+  const size_t stage_bytes = A_BYTES + (size_t)S * E16 * BK * 2;
+  int stages = (int)(stage_budget(1) / stage_bytes);
+  if (stages > MAX_STAGES) stages = MAX_STAGES;
+  using K = void (*)(CUtensorMap, CUtensorMap, int, int, int, int, int, int, int, float*, const int32_t*, int, int,
+                     int32_t*, float*, int32_t*, int);
+  // experts per lane in the selection: E16 <= 192 here, and <= 64 with an fp32 weight
+  const int np = E16 <= 32 ? 1 : (E16 <= 64 ? 2 : (E16 <= 128 ? 4 : 8));
+  const int ki = (S == 1 ? 0 : 4) + (np == 1 ? 0 : (np == 2 ? 1 : (np == 4 ? 2 : 3)));
+  static const K kerns[8] = {route_topk_cl_kernel<1, 1>, route_topk_cl_kernel<1, 2>, route_topk_cl_kernel<1, 4>,
+                             route_topk_cl_kernel<1, 8>, route_topk_cl_kernel<3, 1>, route_topk_cl_kernel<3, 2>,
+                             route_topk_cl_kernel<3, 2>, route_topk_cl_kernel<3, 2>};
+  const K kern = kerns[ki];
+  static std::atomic<unsigned long long> smem_set[8];
+  cudaError_t e = ensure_smem_limit(kern, (int)smem_bytes(1), smem_set[ki]);
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = (unsigned)CS;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.gridDim = dim3((unsigned)(((T + BM - 1) / BM) * CS));
+  cfg.blockDim = dim3(kClThreads);
+  cfg.dynamicSmemBytes = smem_bytes(1);
+  cfg.stream = s;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  e = cudaLaunchKernelEx(&cfg, kern, mx, mw, T, H, E, E16, CS, stages, kb_slice, logits_out, kpt, k_uniform, k_max,
+                         topk_idx, topk_w, counts, count_stride);
   if (e != cudaSuccess) return e;
   count_launches(1);
   return cudaGetLastError();

@@ -173,6 +173,15 @@ __device__ __forceinline__ void bulk_store_1d(void* dst, const void* src, uint32
                "r"(smem_u32(src)), "r"(bytes)
                : "memory");
 }
+// This CTA's shared memory -> another CTA's (dst and bar are shared::cluster
+// addresses in that CTA, e.g. from mapa), completing `bytes` on that CTA's
+// mbarrier, which is the only completion (the source is read before it fires);
+// both addresses 16-byte aligned, bytes a multiple of 16.
+__device__ __forceinline__ void bulk_copy_to_peer(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
+  asm volatile("cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+               "r"(smem_u32(src)), "r"(bytes), "r"(bar)
+               : "memory");
+}
 __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
 // At most N of this thread's committed bulk groups still reading shared memory.
 template <int N>
@@ -188,6 +197,11 @@ __device__ __forceinline__ uint32_t mapa_rank(const void* p, uint32_t rank) {
   uint32_t r;
   asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(smem_u32(p)), "r"(rank));
   return r;
+}
+
+// Atomic add to a shared::cluster address (possibly another CTA's shared memory).
+__device__ __forceinline__ void red_cluster_add_u32(uint32_t addr, uint32_t v) {
+  asm volatile("red.shared::cluster.add.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
 }
 
 // Arrive on an mbarrier given by its shared::cluster address (possibly another CTA's).
