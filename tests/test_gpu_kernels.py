@@ -731,10 +731,11 @@ def test_hier_route_pair_counts():
     (9800, 128, 64, 32, "bf16", True),
     # fewer than 76 tiles: a cluster of 2, 4 or 8 CTAs per tile, each a slice of H
     (4096, 2048, 64, 6, "f32", False), (300, 200, 7, 3, "f32", True), (64, 2048, 64, 6, "f32", True),
-    (3000, 2048, 64, 6, "f32", False), (9000, 1024, 128, 8, "bf16", True), (700, 256, 256, 24, "bf16", True),
-    (129, 512, 7, 3, "f32", True),
-    # the split-K router and a top-k kernel: H of two k-blocks, and an fp32 weight over 64 experts
-    (300, 128, 7, 3, "f32", True), (3000, 256, 256, 8, "f32", False)])
+    (3000, 2048, 64, 6, "f32", False), (9000, 1024, 128, 8, "bf16", True), (129, 512, 7, 3, "f32", True),
+    # the split-K router and a top-k kernel: an fp32 weight over more than 64 experts (several passes,
+    # a partial last one at E = 100), H of two k-blocks, a bf16 weight over 192 experts with few tiles
+    (3000, 256, 256, 8, "f32", False), (8192 + 5, 512, 256, 24, "f32", True), (500, 256, 100, 5, "f32", True),
+    (300, 128, 7, 3, "f32", True), (700, 256, 256, 24, "bf16", True), (40000, 128, 256, 8, "f32", False)])
 def test_router_with_top_k_in_the_gemm_epilogue(T, H, E, k_max, wd, per_token):
     """The one-kernel router (tensor-core GEMM, top-k in the epilogue: one
     thread per token and column range, lists merged in column order), taken
@@ -746,8 +747,8 @@ def test_router_with_top_k_in_the_gemm_epilogue(T, H, E, k_max, wd, per_token):
     tolerance, and the count table equal to the per-chunk histogram of the
     picks.  Covers ragged last tiles, per-token budgets, a grid beyond one CTA
     per SM (T = 20485), k_max of 8, 16 and 32, fp32 weights split into bf16
-    parts, column groups left empty (E = 7), clusters of 2, 4 and 8, and two
-    shapes that take the split-K router and a top-k kernel."""
+    parts, column groups left empty (E = 7), clusters of 2, 4 and 8 slices of H,
+    and six shapes that take the split-K router and a top-k kernel."""
     a = abi()
     rng = np.random.default_rng(T + E + k_max)
     x = torch.from_numpy((rng.standard_normal((T, H)) / np.sqrt(H)).astype(np.float32)).to(torch.bfloat16)

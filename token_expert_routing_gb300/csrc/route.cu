@@ -556,16 +556,16 @@ cudaError_t launch_route(const void* x, int x_dtype, const void* w, int w_dtype,
   // for the split-K GEMM and a top-k kernel); below that its cluster form splits
   // H over 2-8 CTAs per tile (route stage 18.6 against 20.6 us there, 14.5
   // against 16.7 us at 64 tokens); the split-K path stays for the rest.
-  if (logits_in == nullptr && route_on_tensor_cores(x_dtype, H) && route_topk_tc_ok(E, k_max, w_dtype)) {
+  if (logits_in == nullptr && route_on_tensor_cores(x_dtype, H)) {
     void* split = static_cast<unsigned char*>(ws) + route_partials_bytes(T, H, E, w_dtype);
     const int cstride = pair_counts != nullptr ? pair_counts_stride(T) : 0;
-    if (2LL * ((T + 127) / 128) >= sm_count())
+    if (route_topk_tc_ok(E, k_max, w_dtype) && 2LL * ((T + 127) / 128) >= sm_count())
       return launch_route_topk_tc(x, w, w_dtype, T, H, E, k_max, logits_out, kpt, k_uniform, topk_idx, topk_w,
                                   pair_counts, cstride, split, s);
-    // fewer tiles: slices of H over a cluster of CTAs per tile
-    const int cs = route_topk_cl_slices(T, H, E, k_max, w_dtype);
-    if (cs >= 2)
-      return launch_route_topk_cl(x, w, w_dtype, T, H, E, k_max, cs, logits_out, kpt, k_uniform, topk_idx, topk_w,
+    // fewer tiles (slices of H), or several passes of experts: a cluster of CTAs per tile
+    const int ks = route_topk_cl_slices(T, H, E, k_max, w_dtype);
+    if (ks >= 1)
+      return launch_route_topk_cl(x, w, w_dtype, T, H, E, k_max, ks, logits_out, kpt, k_uniform, topk_idx, topk_w,
                                   pair_counts, cstride, split, s);
   }
   PairCounts pc;

@@ -449,29 +449,31 @@ route_topk_tc_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_con
 
 // ---------------------------------------------------------------------------
 // Router GEMM and top-k in one launch for fewer token tiles than SMs: a
-// cluster of CS CTAs per 128-token tile, CTA s of the cluster contracting the
-// s-th of CS slices of H into its own TMEM accumulator.  Each CTA leaves its
-// partial logits (the weight parts already added, as in route_tc_kernel) in its
-// shared memory; after a cluster barrier CTA r takes the tile rows
-// [r * 128 / CS, (r + 1) * 128 / CS) and adds the CS partials of each row in
-// slice order, which it receives by bulk copies that each CTA pushes into the
-// others' shared memory (a fixed order: the logits do not depend on timing;
-// loads of the other CTAs' shared memory, thread by thread, measured 9-25 us
-// for this), one warp per row, then selects as the top-k kernel
-// does: k_t rounds of a warp argmax over order-preserving keys (ties to the
-// lower expert), then the gates and the picks.  (Per-thread sorted lists
-// merged across the row's threads measured slower here: the merge is one long
-// dependent chain per row.)  The CTAs' pick histograms are added
-// by the cluster's CTA 0, which writes the tile's column of the count table.
-// No logits in memory, no second launch; every cluster barrier is reached by
-// every thread on every path.  One CTA per SM (the host keeps tiles x CS <= SMs).
+// cluster of CS = passes x KS CTAs per 128-token tile, CTA r contracting the
+// (r % KS)-th of KS slices of H for the experts of pass r / KS (EC of them)
+// into its own TMEM accumulator (the host runs one pass: CS = KS).  Each CTA
+// leaves its partial logits (the weight parts already added, as in
+// route_tc_kernel) in its shared memory; after a cluster barrier each CTA
+// pushes to CTA q, by one bulk copy into q's shared memory, its partials of
+// the rows [q * 128 / CS, (q + 1) * 128 / CS) that q selects.  CTA q adds an
+// expert's KS slices in slice order (a fixed order: the logits do not depend on
+// timing) and selects with one warp per row as the top-k kernel does: k_t
+// rounds of a warp argmax over order-preserving keys (ties to the lower
+// expert), then the gates and the picks.  The CTAs add their pick histograms
+// into CTA 0's (shared-memory atomics across the cluster), which writes the
+// tile's column of the count table.  No logits in memory, no second launch;
+// every cluster barrier is reached by every thread on every path.  One CTA per
+// SM (the host keeps tiles x CS <= SMs).  Measured on the way (64 tokens,
+// %globaltimer stamps): loads of the other CTAs' shared memory, thread by
+// thread, took 9-25 us where the pushed copies take ~0.7 us; sorted lists per
+// thread merged across a row's threads are one long dependent chain per row.
 // ---------------------------------------------------------------------------
 constexpr int kClThreads = 64 + 4 * 128;  // producer, MMA, 16 epilogue / selection warps
 
 template <int S, int NPER>  // NPER experts per lane in the selection: E <= 32 * NPER
 __global__ void __launch_bounds__(kClThreads, 1)
 route_topk_cl_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_constant__ CUtensorMap map_w, int T,
-                     int H, int E, int E16, int CS, int stages, int kb_slice, float* __restrict__ logits_out,
+                     int H, int E, int EC, int KS, int CS, int stages, int kb_slice, float* __restrict__ logits_out,
                      const int32_t* __restrict__ k_per_token, int k_uniform, int k_max,
                      int32_t* __restrict__ topk_idx, float* __restrict__ topk_w, int32_t* __restrict__ counts,
                      int count_stride) {
@@ -484,20 +486,21 @@ route_topk_cl_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_con
   volatile int* abort_flag = &sh.abort_flag;
 
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-  const int NB = S * E16;
+  const int NB = S * EC;
   const uint32_t b_bytes = (uint32_t)NB * BK * 2;
   const uint32_t stage_bytes = A_BYTES + b_bytes;
   const int rank = (int)cluster_ctarank();
+  const int pass = rank / KS, slice = rank % KS;  // this CTA: experts [pass * EC, +EC), k-block slice
   const int tile = blockIdx.x / CS;
   const int t0 = tile * BM;
   const int kb_all = (H + BK - 1) / BK;
-  const int kb0 = rank * kb_slice;
+  const int kb0 = slice * kb_slice;
   const int kb_n = kb_all - kb0 < kb_slice ? kb_all - kb0 : kb_slice;  // >= 1 by the host's choice of CS
   const int kb_first = tile % kb_n;  // tiles start at different k-blocks of their slice
-  // after the MMAs, in the operand ring: this CTA's partial logits [128][E16 + 4]
-  // fp32, then what the others send of theirs for this CTA's rows: recv[s] =
-  // slice s's rows [rank * rpc, (rank + 1) * rpc)
-  const int pstride = E16 + 4;
+  // after the MMAs, in the operand ring: this CTA's partial logits [128][EC + 4]
+  // fp32, then what the others send of theirs for this CTA's rows: recv[q] =
+  // CTA q's rows [rank * rpc, (rank + 1) * rpc)
+  const int pstride = EC + 4;
   const int rpc = BM / CS;
   float* part = reinterpret_cast<float*>(ring);
   float* recv = part + (size_t)BM * pstride;
@@ -535,7 +538,7 @@ route_topk_cl_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_con
         unsigned char* st = ring + (size_t)s * stage_bytes;
         mbar_expect_tx(&sh.full[s], stage_bytes);
         tma_load_2d(st, &map_x, &sh.full[s], kb * BK, t0);
-        tma_load_2d(st + A_BYTES, &map_w, &sh.full[s], kb * BK, 0);
+        tma_load_2d(st + A_BYTES, &map_w, &sh.full[s], kb * BK, pass * NB);
         ++it;
       }
       if (*abort_flag)
@@ -563,7 +566,7 @@ route_topk_cl_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_con
     }
   } else {  // 16 epilogue warps: the rows of their TMEM lane quarter, a quarter of the columns, into `part`
     const int q = warp & 3, r = q * 32 + lane, g = (warp - 2) / 4;
-    const int nch = E16 / 16, c_lo = (g * nch / 4) * 16, c_hi = ((g + 1) * nch / 4) * 16;
+    const int nch = EC / 16, c_lo = (g * nch / 4) * 16, c_hi = ((g + 1) * nch / 4) * 16;
     int ok = 1;
     if (lane == 0) ok = mbar_wait(&sh.tfull, 0, abort_flag, &g_err);
     ok = __shfl_sync(0xffffffffu, ok, 0);
@@ -574,8 +577,8 @@ route_topk_cl_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_con
         uint32_t v0[16], v1[16], v2[16];
         tmem_ld16(trow + c, v0);
         if (S == 3) {
-          tmem_ld16(trow + E16 + c, v1);
-          tmem_ld16(trow + 2 * E16 + c, v2);
+          tmem_ld16(trow + EC + c, v1);
+          tmem_ld16(trow + 2 * EC + c, v2);
         }
         tmem_ld_wait();
         float l[16];
@@ -585,7 +588,7 @@ route_topk_cl_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_con
           if (S == 3) l[i] = (l[i] + __uint_as_float(v1[i])) + __uint_as_float(v2[i]);
         }
 #pragma unroll
-        for (int j = 0; j < 4; ++j)  // row stride E16 + 4 words: the 16-byte stores of 8 lanes hit 8 bank groups
+        for (int j = 0; j < 4; ++j)  // row stride EC + 4 words: the 16-byte stores of 8 lanes hit 8 bank groups
           *reinterpret_cast<float4*>(part + (size_t)r * pstride + c + 4 * j) =
               make_float4(l[4 * j], l[4 * j + 1], l[4 * j + 2], l[4 * j + 3]);
       }
@@ -603,8 +606,9 @@ route_topk_cl_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_con
 
   // selection: CTA `rank` takes rows [rank * rpc, (rank + 1) * rpc); one warp
   // per row (16 warps: a row's chain of rounds is latency, so rows run side by
-  // side), lane l holding experts l + 32 i; k_t rounds of a warp argmax (the
-  // largest key, then the lowest expert holding it, which is taken out)
+  // side), lane l holding experts l + 32 i, each the sum of its pass's KS
+  // slices in slice order; k_t rounds of a warp argmax (the largest key, then
+  // the lowest expert holding it, which is taken out)
   if (warp >= 2) {
     const bool got = mbar_wait(&recv_bar, 0, abort_flag, &g_err);  // every lane: acquire the copies
     for (int row = rank * rpc + (warp - 2); got && row < (rank + 1) * rpc; row += kClThreads / 32 - 2) {
@@ -613,16 +617,17 @@ route_topk_cl_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_con
       if (t < T) kt = k_per_token != nullptr ? k_per_token[t] : k_uniform;
       float l[NPER];
 #pragma unroll
-      for (int s = 0; s < 8; ++s) {  // slice order
-        if (s < CS) {
-          const float* src = s == rank ? part + (size_t)row * pstride
-                                       : recv + ((size_t)s * rpc + (row - rank * rpc)) * pstride;
-#pragma unroll
-          for (int i = 0; i < NPER; ++i) {
-            const float v = lane + 32 * i < E ? src[lane + 32 * i] : 0.f;
-            l[i] = s == 0 ? v : l[i] + v;
+      for (int i = 0; i < NPER; ++i) {
+        const int e = lane + 32 * i;
+        const int pe = e / EC, c = e - pe * EC;  // the expert's pass and column in it
+        l[i] = 0.f;
+        if (e < E)
+          for (int sk = 0; sk < KS; ++sk) {  // slice order
+            const int qc = pe * KS + sk;
+            const float* src = qc == rank ? part + (size_t)row * pstride
+                                          : recv + ((size_t)qc * rpc + (row - rank * rpc)) * pstride;
+            l[i] = sk == 0 ? src[c] : l[i] + src[c];
           }
-        }
       }
       bool nonfinite = false;
       uint32_t key[NPER];
@@ -891,26 +896,35 @@ cudaError_t launch_route_topk_tc(const void* x, const void* w, int w_dtype, int 
   return cudaGetLastError();
 }
 
-// K slices of the cluster router: the largest CS in {2, 4, 8} with one CTA per
-// SM for every (tile, slice) and at least 2 k-blocks per slice; 0 when none
-// applies (the one-kernel router or the split-K path takes the call).  Its
-// partial and received logits (2 x 128 rows of E16 + 4 fp32) must fit the
-// 200 KB operand ring: E16 <= 192.
+// K slices of the cluster router; 0 when it does not apply (the one-kernel
+// router or the split-K path takes the call): the largest KS in {2, 4, 8} with
+// one CTA per SM for every (tile, slice) and at least 2 k-blocks per slice, for
+// routers whose experts fit one pass (a bf16 weight, or an fp32 one with
+// E <= 64).  The kernel also takes several passes of experts as further CTAs of
+// the cluster, but with the whole of H per CTA that measured slower than the
+// split-K path for an fp32 weight over 128 or 256 experts (T = 1024 .. 8192:
+// 25-60 against 16-41 us per call), so it is not used for them.  The partial and
+// received logits (2 x 128 rows of EC + 4 fp32) must fit the 200 KB operand
+// ring: EC <= 192.
 int route_topk_cl_slices(int T, int H, int E, int k_max, int w_dtype) {
-  if (!route_topk_tc_ok(E, k_max, w_dtype) || (E + 15) / 16 * 16 > 192) return 0;
+  if (k_max > 32) return 0;
+  const int S = w_dtype == SEMMOE_BF16 ? 1 : 3;
+  const int EC = experts_per_pass(E, S), n_pass = (E + EC - 1) / EC;
+  if (EC > 192 || n_pass > 1) return 0;
   const long long tiles = (T + BM - 1) / BM;
   const int kb_all = (H + BK - 1) / BK;
-  int cs = 0;
+  int ks = 0;
   for (int c = 2; c <= 8; c *= 2)
-    if (tiles * c <= sm_count() && kb_all >= 2 * c) cs = c;
-  return cs;
+    if (tiles * c <= sm_count() && kb_all >= 2 * c) ks = c;
+  return ks;
 }
 
-cudaError_t launch_route_topk_cl(const void* x, const void* w, int w_dtype, int T, int H, int E, int k_max, int CS,
+cudaError_t launch_route_topk_cl(const void* x, const void* w, int w_dtype, int T, int H, int E, int k_max, int KS,
                                  float* logits_out, const int32_t* kpt, int k_uniform, int32_t* topk_idx,
                                  float* topk_w, int32_t* counts, int count_stride, void* split, cudaStream_t s) {
   const int S = w_dtype == SEMMOE_BF16 ? 1 : 3;
   const int E16 = (E + 15) / 16 * 16;
+  const int EC = experts_per_pass(E, S), n_pass = (E + EC - 1) / EC, CS = n_pass * KS;
   const void* wb = w;
   int w_rows = E;
   if (S == 3) {
@@ -919,7 +933,7 @@ cudaError_t launch_route_topk_cl(const void* x, const void* w, int w_dtype, int 
       if (e != cudaSuccess) return e;
       wb = split;
     }
-    w_rows = 3 * E16;
+    w_rows = n_pass * 3 * EC;  // [pass][part][EC][H]
   }
   CUtensorMap mx, mw;
   {
@@ -931,22 +945,22 @@ cudaError_t launch_route_topk_cl(const void* x, const void* w, int w_dtype, int 
   {
     const cuuint64_t dims[2] = {(cuuint64_t)H, (cuuint64_t)w_rows};
     const cuuint64_t str[1] = {(cuuint64_t)H * 2};
-    const cuuint32_t box[2] = {BK, (cuuint32_t)(S * E16)};
+    const cuuint32_t box[2] = {BK, (cuuint32_t)(S * EC)};
     if (!make_map_bf16(&mw, wb, 2, dims, str, box)) return cudaErrorInvalidValue;
   }
-  const int kb_all = (H + BK - 1) / BK, kb_slice = (kb_all + CS - 1) / CS;
-  if ((CS - 1) * kb_slice >= kb_all) return cudaErrorInvalidValue;  // every slice holds k-blocks
-  const size_t stage_bytes = A_BYTES + (size_t)S * E16 * BK * 2;
+  const int kb_all = (H + BK - 1) / BK, kb_slice = (kb_all + KS - 1) / KS;
+  if (CS < 2 || CS > 8 || (KS - 1) * kb_slice >= kb_all) return cudaErrorInvalidValue;  // every slice holds k-blocks
+  const size_t stage_bytes = A_BYTES + (size_t)S * EC * BK * 2;
   int stages = (int)(stage_budget(1) / stage_bytes);
   if (stages > MAX_STAGES) stages = MAX_STAGES;
-  using K = void (*)(CUtensorMap, CUtensorMap, int, int, int, int, int, int, int, float*, const int32_t*, int, int,
-                     int32_t*, float*, int32_t*, int);
-  // experts per lane in the selection: E16 <= 192 here, and <= 64 with an fp32 weight
+  using K = void (*)(CUtensorMap, CUtensorMap, int, int, int, int, int, int, int, int, float*, const int32_t*, int,
+                     int, int32_t*, float*, int32_t*, int);
+  // experts per lane in the selection (E <= 32 NPER)
   const int np = E16 <= 32 ? 1 : (E16 <= 64 ? 2 : (E16 <= 128 ? 4 : 8));
   const int ki = (S == 1 ? 0 : 4) + (np == 1 ? 0 : (np == 2 ? 1 : (np == 4 ? 2 : 3)));
   static const K kerns[8] = {route_topk_cl_kernel<1, 1>, route_topk_cl_kernel<1, 2>, route_topk_cl_kernel<1, 4>,
                              route_topk_cl_kernel<1, 8>, route_topk_cl_kernel<3, 1>, route_topk_cl_kernel<3, 2>,
-                             route_topk_cl_kernel<3, 2>, route_topk_cl_kernel<3, 2>};
+                             route_topk_cl_kernel<3, 4>, route_topk_cl_kernel<3, 8>};
   const K kern = kerns[ki];
   static std::atomic<unsigned long long> smem_set[8];
   cudaError_t e = ensure_smem_limit(kern, (int)smem_bytes(1), smem_set[ki]);
@@ -963,8 +977,8 @@ cudaError_t launch_route_topk_cl(const void* x, const void* w, int w_dtype, int 
   cfg.stream = s;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  e = cudaLaunchKernelEx(&cfg, kern, mx, mw, T, H, E, E16, CS, stages, kb_slice, logits_out, kpt, k_uniform, k_max,
-                         topk_idx, topk_w, counts, count_stride);
+  e = cudaLaunchKernelEx(&cfg, kern, mx, mw, T, H, E, EC, KS, CS, stages, kb_slice, logits_out, kpt, k_uniform,
+                         k_max, topk_idx, topk_w, counts, count_stride);
   if (e != cudaSuccess) return e;
   count_launches(1);
   return cudaGetLastError();
