@@ -378,6 +378,11 @@ int semmoe_grouped_ffn_gather(const void* x, const int32_t* sorted_to_pair, int 
  *                                  SM, rows fetched by TMA four-row gathers
  *   SEMMOE_FORM_CUDA_CORE          both GEMMs on CUDA cores (form1 and form2
  *                                  both this value)
+ *   SEMMOE_FORM_FUSED              both GEMMs in one persistent launch of
+ *                                  independent CTAs, GEMM2's tiles of an m-tile
+ *                                  starting once GEMM1's tiles of it are stored
+ *                                  (form1 and form2 both this value; rows read
+ *                                  from x_perm, not gathered)
  * bf16 accepts all of them; fp32 only SEMMOE_FORM_DEFAULT or
  * SEMMOE_FORM_CUDA_CORE (it always runs on CUDA cores).  Any other combination
  * returns SEMMOE_ERR_INVALID_ARG.  Arguments, workspace, limits and device
@@ -390,7 +395,8 @@ enum {
   SEMMOE_FORM_PAIR1 = 2,
   SEMMOE_FORM_PAIR = 3,
   SEMMOE_FORM_SINGLE_TMA_GATHER = 4,
-  SEMMOE_FORM_CUDA_CORE = 5
+  SEMMOE_FORM_CUDA_CORE = 5,
+  SEMMOE_FORM_FUSED = 6
 };
 int semmoe_grouped_ffn_form(const void* x, const int32_t* sorted_to_pair, int k_max, int T,
                             const int32_t* expert_offsets, const int32_t* phys_to_expert, const void* w13,

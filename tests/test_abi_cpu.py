@@ -171,6 +171,10 @@ def test_ffn_form_validation(lib):
     assert call(a.SEMMOE_FORM_SINGLE, a.SEMMOE_FORM_SINGLE_TMA_GATHER, s2p=p) == 1
     # fp32 runs on CUDA cores only
     assert call(a.SEMMOE_FORM_PAIR, a.SEMMOE_FORM_PAIR, dtype=0) == 1 and "fp32" in _err(lib)
+    # the one-launch form covers both GEMMs, from x_perm
+    assert call(a.SEMMOE_FORM_FUSED, a.SEMMOE_FORM_SINGLE) == 1 and "form" in _err(lib)
+    assert call(a.SEMMOE_FORM_FUSED, a.SEMMOE_FORM_FUSED, s2p=p) == 1 and "FUSED" in _err(lib)
+    assert call(a.SEMMOE_FORM_FUSED + 1, a.SEMMOE_FORM_FUSED + 1) == 1
     # no rows: nothing is launched, for any valid form pair
     assert lib.semmoe_grouped_ffn_form(None, None, 1, 0, p, p, p, p, 1, 0, 4, 128, 128, None, p, 1 << 30,
                                        a.SEMMOE_FORM_PAIR, a.SEMMOE_FORM_SINGLE, None) == 0

@@ -293,7 +293,8 @@ SPLIT_COUNTS = [0, 1, 127, 128, 129, 255, 256, 257, 384, 511, 512, 640, 1000, 3,
                                      (384, 64, 512, 1408), (3072, 64, 256, 200)])
 def test_grouped_ffn_forms_are_bit_identical(P, E, H, I):
     """Every form of the grouped GEMM -- independent CTAs, 2-SM MMA pairs with
-    one or two accumulator buffers, and the shape-chosen default -- returns
+    one or two accumulator buffers, both GEMMs in one launch (GEMM2's tiles
+    waiting on GEMM1's per m-tile), and the shape-chosen default -- returns
     exactly the same bits, and those bits match the oracle's grouped FFN row by
     row within the bf16 tolerance; one case pins group sizes around the 128-
     and 256-row boundaries (empty groups, 1, 127..129, 255..257 rows), two have
@@ -311,7 +312,8 @@ def test_grouped_ffn_forms_are_bit_identical(P, E, H, I):
     ws = torch.empty(abi().semmoe_grouped_ffn_workspace_size(P, I, 1), dtype=torch.uint8, device="cuda")
     outs = []
     a = abi()
-    for form in (a.SEMMOE_FORM_SINGLE, a.SEMMOE_FORM_PAIR1, a.SEMMOE_FORM_PAIR, a.SEMMOE_FORM_DEFAULT):
+    for form in (a.SEMMOE_FORM_SINGLE, a.SEMMOE_FORM_PAIR1, a.SEMMOE_FORM_PAIR, a.SEMMOE_FORM_FUSED,
+                 a.SEMMOE_FORM_DEFAULT):
         y = torch.empty(P, H, dtype=torch.bfloat16, device="cuda")
         a.semmoe_grouped_ffn_form(x, None, 1, 0, off, pe, w13, w2, P, E, H, I, y, ws, form, form)
         assert a.semmoe_check_errors() == 0
@@ -492,14 +494,15 @@ def test_permute_flags_bad_expert_and_pair_count():
     np.testing.assert_array_equal(np_(eo), ref["expert_offsets"])
 
 
-@pytest.mark.parametrize("mode,dtype", [("single", "bf16"), ("pair", "bf16"), ("default", "f32")])
+@pytest.mark.parametrize("mode,dtype", [("single", "bf16"), ("pair", "bf16"), ("fused", "bf16"), ("default", "f32")])
 def test_grouped_ffn_flags_bad_group_table(mode, dtype):
     """Group offsets that decrease or run past P (SEMMOE_DEVERR_PAIRS) and an
     expert id past E (SEMMOE_DEVERR_EXPERT) are flagged by the kernels' checks
     in every form; those groups are skipped, the valid ones are still computed
     exactly as with a clean table."""
     a = abi()
-    form = {"single": a.SEMMOE_FORM_SINGLE, "pair": a.SEMMOE_FORM_PAIR, "default": a.SEMMOE_FORM_DEFAULT}[mode]
+    form = {"single": a.SEMMOE_FORM_SINGLE, "pair": a.SEMMOE_FORM_PAIR, "fused": a.SEMMOE_FORM_FUSED,
+            "default": a.SEMMOE_FORM_DEFAULT}[mode]
 
     def ffn(xx, off, pe, y):
         a.semmoe_grouped_ffn_form(xx, None, 1, 0, off, pe, w13, w2, P, E, H, I, y, ws, form, form)

@@ -21,7 +21,7 @@ SEMMOE_F32, SEMMOE_BF16 = 0, 1
 SEMMOE_F32_SPLIT = 2   # router weight only: the output of semmoe_route_split_weight
 # grouped-FFN kernel forms (semmoe_grouped_ffn_form)
 SEMMOE_FORM_DEFAULT, SEMMOE_FORM_SINGLE, SEMMOE_FORM_PAIR1, SEMMOE_FORM_PAIR, SEMMOE_FORM_SINGLE_TMA_GATHER, \
-    SEMMOE_FORM_CUDA_CORE = range(6)
+    SEMMOE_FORM_CUDA_CORE, SEMMOE_FORM_FUSED = range(7)
 # device error word bits (semmoe_check_errors)
 SEMMOE_DEVERR_EXPERT, SEMMOE_DEVERR_TOKEN_ID, SEMMOE_DEVERR_LUT, SEMMOE_DEVERR_K, SEMMOE_DEVERR_PAIRS, \
     SEMMOE_DEVERR_TIMEOUT, SEMMOE_DEVERR_NONFINITE, SEMMOE_DEVERR_OFFSETS, SEMMOE_DEVERR_RANK = \

@@ -353,9 +353,11 @@ int semmoe_grouped_ffn_form(const void* x, const int32_t* sorted_to_pair, int k_
     REQUIRE(P <= (long long)T * k_max, "%s: P = %d > T * k_max", fn, P);
   }
   const bool cc1 = form1 == SEMMOE_FORM_CUDA_CORE, cc2 = form2 == SEMMOE_FORM_CUDA_CORE;
-  REQUIRE(form1 >= SEMMOE_FORM_DEFAULT && form1 <= SEMMOE_FORM_CUDA_CORE && form2 >= SEMMOE_FORM_DEFAULT &&
-              form2 <= SEMMOE_FORM_CUDA_CORE && cc1 == cc2,
+  const bool fu1 = form1 == SEMMOE_FORM_FUSED, fu2 = form2 == SEMMOE_FORM_FUSED;
+  REQUIRE(form1 >= SEMMOE_FORM_DEFAULT && form1 <= SEMMOE_FORM_FUSED && form2 >= SEMMOE_FORM_DEFAULT &&
+              form2 <= SEMMOE_FORM_FUSED && cc1 == cc2 && fu1 == fu2,
           "%s: bad form pair (%d, %d)", fn, form1, form2);
+  REQUIRE(!fu1 || !gathered, "%s: SEMMOE_FORM_FUSED reads x_perm (no gathered rows)", fn);
   REQUIRE(form2 != SEMMOE_FORM_SINGLE_TMA_GATHER && (form1 != SEMMOE_FORM_SINGLE_TMA_GATHER || gathered),
           "%s: SEMMOE_FORM_SINGLE_TMA_GATHER applies to a GEMM1 with gathered rows only", fn);
   REQUIRE(dtype != SEMMOE_F32 || ((form1 == SEMMOE_FORM_DEFAULT || cc1) && (form2 == SEMMOE_FORM_DEFAULT || cc2)),

@@ -26,7 +26,9 @@ int ffn_take_errors(cudaStream_t s, int* bits) {
 // Workspace: the SwiGLU activation h [P, I] in the activation type.
 size_t ffn_ws_bytes(int P, int I, int dtype) {
   const size_t es = dtype == SEMMOE_BF16 ? 2 : 4;
-  return align_up((size_t)(P > 0 ? P : 1) * I * es, 256);
+  // h [P, I], then one readiness counter per m-tile for the one-launch form
+  // (at most ceil(P / 128) + 256 m-tiles: one partial tile per group)
+  return align_up((size_t)(P > 0 ? P : 1) * I * es, 256) + ffn_ready_bytes(P);
 }
 
 cudaError_t launch_ffn(const void* x, const int32_t* offsets, const int32_t* p2e, const void* w13,

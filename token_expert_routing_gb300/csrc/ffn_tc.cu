@@ -580,6 +580,329 @@ ffn_tc_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__
 }
 
 // ---------------------------------------------------------------------------
+// Both GEMMs in one persistent launch (independent CTAs): each CTA walks the
+// list of GEMM1 tiles and then of GEMM2 tiles (round robin over the CTAs), so a
+// CTA whose GEMM1 share ends early goes on with GEMM2 tiles while others finish
+// GEMM1, instead of idling until the last GEMM1 CTA ends.  A GEMM2 tile reads
+// the h rows of one m-tile, written by that m-tile's nt1 GEMM1 tiles: each of
+// the four epilogue warps of a GEMM1 tile, once its h stores have completed,
+// adds 1 to ready[m-tile] (release), and the producer of a GEMM2 tile waits,
+// bounded, until ready[m-tile] = 4 nt1 (acquire) before loading the rows.  A
+// GEMM1 tile waits for nothing and every CTA's GEMM1 tiles come before its
+// GEMM2 tiles, so every wait ends once the CTAs holding those GEMM1 tiles run;
+// the grid has at most one CTA per SM, all resident once any other kernel on
+// the GPU has finished.
+// ---------------------------------------------------------------------------
+// Upper bound on the m-tiles of P rows in G groups: the size of the ready counters.
+__host__ __device__ __forceinline__ int mtiles_max_of(int P, int G) { return (P + BM - 1) / BM + G; }
+
+__device__ __forceinline__ int ld_acquire_gpu(const int* p) {
+  int v;
+  asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+// Orders this thread's async-proxy (TMA) global accesses with its generic ones.
+__device__ __forceinline__ void fence_async_global() { asm volatile("fence.proxy.async.global;" ::: "memory"); }
+
+__global__ void __launch_bounds__(THREADS, 1)
+ffn_fused_kernel(const __grid_constant__ CUtensorMap map_a1, const __grid_constant__ CUtensorMap map_b1,
+                 const __grid_constant__ CUtensorMap map_o1, const __grid_constant__ CUtensorMap map_a2,
+                 const __grid_constant__ CUtensorMap map_b2, const __grid_constant__ CUtensorMap map_o2,
+                 const int32_t* __restrict__ offsets, const int32_t* __restrict__ phys_to_expert, int G, int P,
+                 int E, int H, int I, int nt1, int nt2, __nv_bfloat16* __restrict__ h, __nv_bfloat16* __restrict__ y,
+                 int* __restrict__ ready) {
+  extern __shared__ __align__(1024) unsigned char smem_raw[];
+  const uint32_t pad = (1024u - (smem_u32(smem_raw) & 1023u)) & 1023u;
+  unsigned char* stage_a = smem_raw + pad;
+  unsigned char* stage_b = stage_a + STAGES * A_BYTES;
+  unsigned char* out_stage = stage_a + STAGES * STAGE_BYTES;
+  Shared& sh = *reinterpret_cast<Shared*>(out_stage + OUT_STAGE_BYTES);
+  // tiles are claimed one at a time from a counter (next, after the ready
+  // counters); the producer passes each to the MMA and the epilogue through a
+  // ring (the producer runs at most STAGES tiles ahead of the MMA and that at
+  // most 2 ahead of the epilogue, so 16 slots are never overtaken)
+  constexpr int kRing = 16;
+  __shared__ int tile_ring[kRing];
+  __shared__ uint64_t tile_bar[kRing];
+  volatile int* abort_flag = &sh.abort_flag;
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(&sh.full[s], 1);
+      mbar_init(&sh.empty[s], 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(&sh.tfull[a], 1);
+      mbar_init(&sh.tempty[a], 128);
+    }
+    mbar_init(&sh.done, 1);
+    for (int i = 0; i < kRing; ++i) mbar_init(&tile_bar[i], 1);
+    sh.abort_flag = 0;
+    sh.armed = 0;
+    mbar_init_fence();
+    prefetch_map(&map_a1);
+    prefetch_map(&map_b1);
+    prefetch_map(&map_o1);
+    prefetch_map(&map_a2);
+    prefetch_map(&map_b2);
+    prefetch_map(&map_o2);
+  }
+  for (int g = threadIdx.x; g <= G; g += blockDim.x) sh.off[g] = offsets ? offsets[g] : (g == 0 ? 0 : P);
+  for (int g = threadIdx.x; g < G; g += blockDim.x) sh.pe[g] = phys_to_expert ? phys_to_expert[g] : 0;
+  __syncthreads();
+  if (warp == 1) tmem_alloc(&sh.tmem_base, TMEM_COLS);
+  if (warp == 0) {  // exclusive prefix of m-tiles per group, 8 groups per lane
+    int cnt[8], sum = 0;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const int g = lane * 8 + i;
+      int c = 0;
+      if (g < G) {
+        const int lo = sh.off[g], hi = sh.off[g + 1], e = sh.pe[g];
+        if (lo < 0 || hi < lo || hi > P) atomicOr(&g_err, SEMMOE_DEVERR_PAIRS);
+        else if (e < 0 || e >= E) atomicOr(&g_err, SEMMOE_DEVERR_EXPERT);
+        else c = (hi - lo + BM - 1) / BM;
+      }
+      cnt[i] = c;
+      sum += c;
+    }
+    int incl = sum;
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+      const int v = __shfl_up_sync(0xffffffffu, incl, d);
+      if (lane >= d) incl += v;
+    }
+    int run = incl - sum;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const int g = lane * 8 + i;
+      if (g < G) sh.tp[g] = run;
+      run += cnt[i];
+    }
+    if (lane == 31) {
+      sh.tp[G] = incl;
+      sh.total_mtiles = incl;
+    }
+  }
+  fence_before();
+  __syncthreads();
+  fence_after();
+
+  const uint32_t tmem = sh.tmem_base;
+  const int mtiles = sh.total_mtiles;
+  const int total1 = mtiles * nt1, total = total1 + mtiles * nt2;
+  int* next = ready + (mtiles_max_of(P, G));  // the tile counter
+  // tile u: GEMM1 (m-tile, n-tile) for u < total1, else GEMM2
+  auto tile_of = [&](int u, bool& g2, int& mt, int& nt) {
+    g2 = u >= total1;
+    const int v = g2 ? u - total1 : u, nn = g2 ? nt2 : nt1;
+    mt = v / nn;
+    nt = v - mt * nn;
+  };
+
+  if (warp == 0) {
+    if (lane == 0) {  // TMA producer: claims tiles, hands each to the MMA and the epilogue
+      uint32_t it = 0;
+      for (int k = 0;; ++k) {
+        const int u = *abort_flag ? total : atomicAdd(next, 1);
+        tile_ring[k % kRing] = u;  // total or more: no more tiles
+        mbar_arrive(&tile_bar[k % kRing]);
+        if (u >= total) break;
+        bool g2;
+        int mt, nt, row0, rows, e;
+        tile_of(u, g2, mt, nt);
+        decode_mtile<1>(sh, G, mt, 0, row0, rows, e);
+        if (g2) {  // the m-tile's h rows: all its GEMM1 tiles published (4 epilogue warps each)
+          const uint64_t t_start = globaltimer_ns();
+          bool ok = true;
+          for (uint32_t polls = 0; ld_acquire_gpu(ready + mt) < 4 * nt1; ++polls) {
+            if (*abort_flag) { ok = false; break; }
+            if (globaltimer_ns() - t_start > kWaitNs || polls > kWaitPolls) {
+              atomicOr(&g_err, SEMMOE_DEVERR_TIMEOUT);
+              *abort_flag = 1;
+              ok = false;
+              break;
+            }
+          }
+          if (!ok) break;
+          fence_async_global();  // the TMA loads below come after the acquire
+        }
+        const int kb_n = ((g2 ? I : H) + BK - 1) / BK;
+        bool ok = true;
+        for (int kb = 0; kb < kb_n; ++kb) {
+          const int s = it % STAGES;
+          const uint32_t ph = (it / STAGES) & 1;
+          if (!mbar_wait(&sh.empty[s], ph ^ 1, abort_flag, &g_err)) { ok = false; break; }
+          mbar_expect_tx(&sh.full[s], STAGE_BYTES);
+          unsigned char* b = stage_b + s * B_BYTES;
+          if (g2) {
+            tma_load_2d(stage_a + s * A_BYTES, &map_a2, &sh.full[s], kb * BK, row0);
+            tma_load_3d(b, &map_b2, &sh.full[s], kb * BK, nt * BN, e);
+          } else {
+            tma_load_2d(stage_a + s * A_BYTES, &map_a1, &sh.full[s], kb * BK, row0);
+            tma_load_4d(b, &map_b1, &sh.full[s], kb * BK, nt * 128, 0, e);
+            tma_load_4d(b + B_BYTES / 2, &map_b1, &sh.full[s], kb * BK, nt * 128, 1, e);
+          }
+          ++it;
+        }
+        if (!ok) break;
+      }
+      *reinterpret_cast<volatile int*>(&sh.armed) = (int)it;  // for the drain after an abort
+      if (*abort_flag)  // no TMA write may still be landing when the CTA exits
+        for (uint32_t j = it > (uint32_t)STAGES ? it - STAGES : 0; j < it; ++j)
+          mbar_drain(&sh.full[j % STAGES], (j / STAGES) & 1, &g_err);
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {  // MMA issuer
+      uint32_t it = 0, acc_it = 0;
+      for (int tk = 0;; ++tk) {
+        if (!mbar_wait(&tile_bar[tk % kRing], (uint32_t)(tk / kRing) & 1, abort_flag, &g_err)) break;
+        const int u = tile_ring[tk % kRing];
+        const uint32_t a = acc_it & 1, aph = (acc_it >> 1) & 1;
+        if (!mbar_wait(&sh.tempty[a], aph ^ 1, abort_flag, &g_err)) break;
+        if (u >= total) {  // tell the epilogue: a completion of the next accumulator phase with no tile
+          mbar_arrive(&sh.tfull[a]);
+          break;
+        }
+        bool g2;
+        int mt, nt;
+        tile_of(u, g2, mt, nt);
+        const int kb_n = ((g2 ? I : H) + BK - 1) / BK;
+        fence_after();
+        const uint32_t d = tmem + a * ACC_COLS;
+        bool ok = true;
+        for (int kb = 0; kb < kb_n; ++kb) {
+          const int s = it % STAGES;
+          const uint32_t ph = (it / STAGES) & 1;
+          if (!mbar_wait(&sh.full[s], ph, abort_flag, &g_err)) { ok = false; break; }
+          fence_after();
+          const uint32_t sa = smem_u32(stage_a + s * A_BYTES), sb = smem_u32(stage_b + s * B_BYTES);
+#pragma unroll
+          for (int k = 0; k < BK / UK; ++k)
+            mma_bf16(d, sw128_desc(sa + k * UK * 2), sw128_desc(sb + k * UK * 2), kIdesc, (kb | k) != 0);
+          commit(&sh.empty[s]);
+          ++it;
+        }
+        if (!ok) break;
+        commit(&sh.tfull[a]);
+        ++acc_it;
+      }
+      commit(&sh.done);
+      mbar_drain(&sh.done, 0, &g_err);
+    }
+  } else {
+    // ---------------- epilogue (warps 2..5) ----------------
+    const int q = warp & 3, r = q * 32 + lane;
+    uint32_t acc_it = 0;
+    ChunkOut co{&map_o1, out_stage + q * 4096, 0};
+    for (int k = 0;; ++k) {
+      const uint32_t a = acc_it & 1, aph = (acc_it >> 1) & 1;
+      int ok = 1, u = 0;
+      if (lane == 0) {
+        ok = mbar_wait(&tile_bar[k % kRing], (uint32_t)(k / kRing) & 1, abort_flag, &g_err) &&
+             mbar_wait(&sh.tfull[a], aph, abort_flag, &g_err);
+        if (ok) u = tile_ring[k % kRing];
+      }
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+      u = __shfl_sync(0xffffffffu, u, 0);
+      if (!ok || u >= total) break;
+      bool g2;
+      int mt, nt, row0, rows, e;
+      tile_of(u, g2, mt, nt);
+      decode_mtile<1>(sh, G, mt, 0, row0, rows, e);
+      fence_after();
+      const uint32_t t_row = tmem + ((uint32_t)(q * 32) << 16) + a * ACC_COLS;
+      const bool row_ok = r < rows;
+      const bool full = q * 32 + 32 <= rows;  // all 32 rows of this warp lie in the group
+      co.map = g2 ? &map_o2 : &map_o1;
+      if (!g2) {  // GEMM1: accumulator columns [0, 128) gate, [128, 256) up; 128 h columns
+        __nv_bfloat16* orow = h + (size_t)(row0 + (row_ok ? r : 0)) * I;
+#pragma unroll 1
+        for (int c = 0; c < 128; c += 64) {
+          uint32_t g0[32], g1[32], u0[32], u1[32], w[32];
+          tmem_ld32(t_row + c, g0);
+          tmem_ld32(t_row + c + 32, g1);
+          tmem_ld32(t_row + 128 + c, u0);
+          tmem_ld32(t_row + 128 + c + 32, u1);
+          tmem_ld_wait();
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            w[i] = pack_bf16x2(swiglu(g0[2 * i], u0[2 * i]), swiglu(g0[2 * i + 1], u0[2 * i + 1]));
+            w[16 + i] = pack_bf16x2(swiglu(g1[2 * i], u1[2 * i]), swiglu(g1[2 * i + 1], u1[2 * i + 1]));
+          }
+          emit_chunk(co, w, full, row_ok, orow, nt * 128 + c, I, row0 + q * 32, lane);
+        }
+      } else {  // GEMM2: 256 y columns
+        __nv_bfloat16* orow = y + (size_t)(row0 + (row_ok ? r : 0)) * H;
+#pragma unroll 1
+        for (int c = 0; c < BN; c += 64) {
+          uint32_t y0[32], y1[32], w[32];
+          tmem_ld32(t_row + c, y0);
+          tmem_ld32(t_row + c + 32, y1);
+          tmem_ld_wait();
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            w[i] = pack_bf16x2(__uint_as_float(y0[2 * i]), __uint_as_float(y0[2 * i + 1]));
+            w[16 + i] = pack_bf16x2(__uint_as_float(y1[2 * i]), __uint_as_float(y1[2 * i + 1]));
+          }
+          emit_chunk(co, w, full, row_ok, orow, nt * BN + c, H, row0 + q * 32, lane);
+        }
+      }
+      fence_before();
+      mbar_arrive(&sh.tempty[a]);  // the MMA may reuse the accumulator while this warp publishes
+      ++acc_it;
+      if (!g2) {  // this warp's h rows of the m-tile, written (TMA stores and direct stores) and visible
+        if (lane == 0) {
+          bulk_wait_all();       // its TMA stores have completed
+          fence_async_global();  // ... and are ordered before the release below
+        }
+        __threadfence();
+        __syncwarp();
+        if (lane == 0) {
+          __threadfence();
+          atomicAdd(ready + mt, 1);
+        }
+      }
+    }
+    if (lane == 0) bulk_wait_all();  // this warp's output stores are complete
+  }
+
+  fence_before();
+  __syncthreads();
+  if (warp == 0 && lane == 0 && *abort_flag) {  // also an abort raised after the producer left its loop
+    const int armed = sh.armed;
+    for (int j = armed > STAGES ? armed - STAGES : 0; j < armed; ++j)
+      mbar_drain(&sh.full[j % STAGES], (j / STAGES) & 1, &g_err);
+  }
+  if (warp == 1) {
+    __syncwarp();
+    fence_after();
+    tmem_dealloc(tmem, TMEM_COLS);
+  }
+}
+
+cudaError_t launch_fused(const CUtensorMap& ma1, const CUtensorMap& mb1, const CUtensorMap& mo1,
+                         const CUtensorMap& ma2, const CUtensorMap& mb2, const CUtensorMap& mo2, const int32_t* offsets,
+                         const int32_t* p2e, int G, int P, int E, int H, int I, __nv_bfloat16* h, __nv_bfloat16* y,
+                         int* ready, cudaStream_t s) {
+  static std::atomic<unsigned long long> smem_set{0};
+  cudaError_t e = ensure_smem_limit(ffn_fused_kernel, (int)kSmemBytes, smem_set);
+  if (e != cudaSuccess) return e;
+  const int nt1 = (I + 127) / 128, nt2 = (H + BN - 1) / BN;
+  const long long mtiles_max = mtiles_max_of(P, G);
+  e = cudaMemsetAsync(ready, 0, (size_t)(mtiles_max + 1) * sizeof(int), s);  // + the tile counter
+  if (e != cudaSuccess) return e;
+  const long long max_units = mtiles_max * (nt1 + nt2);
+  int grid = sm_count();  // one CTA per SM (shared memory)
+  if (max_units < grid) grid = (int)max_units;
+  ffn_fused_kernel<<<grid, THREADS, kSmemBytes, s>>>(ma1, mb1, mo1, ma2, mb2, mo2, offsets, p2e, G, P, E, H, I, nt1,
+                                                     nt2, h, y, ready);
+  count_launches(1);
+  return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------------------
 // 2-SM variant: clusters of two CTAs on two SMs run
 // tcgen05.mma.cta_group::2 with M = 256.  Each CTA stages its own 128 A rows and
 // half of the 256-row weight tile (CTA 0 the gate / first half, CTA 1 the up /
@@ -960,9 +1283,17 @@ cudaError_t launch_ffn_tc(const void* x, const int32_t* offsets, const int32_t* 
                           const float* topk_w, int k_max, int T_acc, float* acc) {
   if (P == 0) return cudaSuccess;
   const int G = offsets ? E : 1;
-  const int mode1 = resolve_form(form1, true, I, P, G, gather_rows != nullptr);
-  const int mode2 = resolve_form(form2, false, I, P, G, false);
-  const int CL = mode2 == SEMMOE_FORM_SINGLE ? 1 : 2;  // CTAs of a pair each load half of GEMM2's weight tile
+  int mode1 = resolve_form(form1, true, I, P, G, gather_rows != nullptr);
+  int mode2 = resolve_form(form2, false, I, P, G, false);
+  // where both GEMMs run in independent CTAs by default (groups of few rows), one
+  // launch for both: routed FFN, decode T = 64 / 256 / 512, 171 / 175 / 179 us
+  // against 180 / 184 / 189 us (GEMM1's last wave no longer idles half the SMs)
+  if (form1 == SEMMOE_FORM_DEFAULT && form2 == SEMMOE_FORM_DEFAULT && gather_rows == nullptr && acc == nullptr &&
+      mode1 == SEMMOE_FORM_SINGLE && mode2 == SEMMOE_FORM_SINGLE)
+    mode1 = mode2 = SEMMOE_FORM_FUSED;
+  const bool fused = mode1 == SEMMOE_FORM_FUSED && gather_rows == nullptr && acc == nullptr;
+  // GEMM2's weight box: 256 rows for independent CTAs, 128 for a pair CTA's half of the tile
+  const int CL = (mode2 == SEMMOE_FORM_SINGLE || fused) ? 1 : 2;
   const cuuint64_t es = 2;
   CUtensorMap ma1, mb1, ma2, mb2;
   Gather ga;
@@ -1024,6 +1355,10 @@ cudaError_t launch_ffn_tc(const void* x, const int32_t* offsets, const int32_t* 
   sc.acc = acc;
   __nv_bfloat16* h = static_cast<__nv_bfloat16*>(ws);
   __nv_bfloat16* yb = static_cast<__nv_bfloat16*>(y);
+  if (fused) {
+    int* ready = reinterpret_cast<int*>(static_cast<unsigned char*>(ws) + align_up((size_t)P * I * 2, 256));
+    return launch_fused(ma1, mb1, mo1, ma2, mb2, mo2, offsets, p2e, G, P, E, H, I, h, yb, ready, s);
+  }
   cudaError_t e = launch_gemm<true>(mode1, ma1, mb1, mo1, offsets, p2e, G, P, E, I, H, (I + 127) / 128, ga, h, s);
   if (e != cudaSuccess) return e;
   return launch_gemm<false>(mode2, ma2, mb2, mo2, offsets, p2e, G, P, E, H, I, (H + BN - 1) / BN, Gather(), yb, s,

@@ -86,6 +86,8 @@ cudaError_t launch_permute_noalloc(const int32_t* topk_idx, const int32_t* exper
                                    void* x_perm, cudaStream_t s);
 
 size_t ffn_ws_bytes(int P, int I, int dtype);
+// Readiness counters of the one-launch grouped FFN (one int per m-tile), after h in its workspace.
+inline size_t ffn_ready_bytes(int P) { return align_up((size_t)((P > 0 ? P : 1) + 127) / 128 * 4 + 257 * 4, 256); }
 // offsets == nullptr: one group of rows [0, P) using expert 0 of w13/w2.
 // gather != nullptr: x is [T_x, H] unpermuted and GEMM1's sorted row q reads x
 // row gather[q] / gather_div; otherwise x holds the P sorted rows.
