@@ -534,6 +534,22 @@ int semmoe_transition_lookup(const int32_t* topk_idx, const int32_t* k_per_token
  */
 int semmoe_selftest_bounded_wait(void* stream);
 
+/*
+ * semmoe_selftest_fused_ready_wait -- exercises the failure path of the
+ * one-launch grouped FFN (SEMMOE_FORM_FUSED), whose GEMM2 tiles wait on
+ * counters that GEMM1's epilogue raises (not part of the layer; the pages have
+ * no counterpart).  It runs one group of P bf16 rows (0 < P <= 4096; x_perm
+ * [P, H], w13 [1, 2I, H], w2 [1, H, I], y_perm [P, H], workspace as
+ * semmoe_grouped_ffn_workspace_size(P, I, SEMMOE_BF16)) with every GEMM2 tile
+ * waiting for one count more than its GEMM1 tiles publish.  Each such wait gives
+ * up after its 2 s bound, sets SEMMOE_DEVERR_TIMEOUT and stops its CTA (in-flight
+ * copies drained, tensor memory freed), so the next semmoe_check_errors() on
+ * the stream returns SEMMOE_ERR_DEVICE_TIMEOUT and the CUDA context stays
+ * usable; y_perm is left unspecified.  Argument errors as semmoe_grouped_ffn.
+ */
+int semmoe_selftest_fused_ready_wait(const void* x_perm, const void* w13, const void* w2, int P, int H, int I,
+                                     void* y_perm, void* ws, size_t ws_bytes, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -178,3 +178,15 @@ def test_ffn_form_validation(lib):
     # no rows: nothing is launched, for any valid form pair
     assert lib.semmoe_grouped_ffn_form(None, None, 1, 0, p, p, p, p, 1, 0, 4, 128, 128, None, p, 1 << 30,
                                        a.SEMMOE_FORM_PAIR, a.SEMMOE_FORM_SINGLE, None) == 0
+
+
+def test_fused_ready_wait_selftest_validation(lib):
+    """The one-launch FFN's failure-path self-test checks its arguments like
+    semmoe_grouped_ffn before touching a device."""
+    p = ctypes.c_void_p(1 << 12)
+    call = lib.semmoe_selftest_fused_ready_wait
+    assert call(p, p, p, 0, 128, 128, p, p, 1 << 30, None) == 1 and "P" in _err(lib)
+    assert call(p, p, p, 5000, 128, 128, p, p, 1 << 30, None) == 1 and "P" in _err(lib)
+    assert call(p, p, p, 64, 100, 128, p, p, 1 << 30, None) == 1 and "multiples of 8" in _err(lib)
+    assert call(p, p, p, 64, 128, 128, p, p, 16, None) == 1 and "workspace" in _err(lib)
+    assert call(p, None, p, 64, 128, 128, p, p, 1 << 30, None) == 1 and "null" in _err(lib)

@@ -428,6 +428,38 @@ def test_bounded_wait_reports_timeout_and_context_survives():
     test_combine("f32", True)  # the context still runs kernels
 
 
+def test_fused_ffn_ready_wait_runs_out_and_context_survives():
+    """The one-launch grouped FFN with GEMM2's readiness waits made unreachable:
+    every such wait gives up after its bound, the host reads
+    SEMMOE_ERR_DEVICE_TIMEOUT with the timeout bit, and the next one-launch FFN
+    on the same workspace (counters zeroed again at launch) is exact."""
+    import time
+    a = abi()
+    rng = np.random.default_rng(2024)
+    P, H, I = 300, 256, 200
+    x = torch.from_numpy(rng.standard_normal((P, H)).astype(np.float32)).to(torch.bfloat16).cuda()
+    w13 = torch.from_numpy((rng.standard_normal((1, 2 * I, H)) / np.sqrt(H)).astype(np.float32)).to(torch.bfloat16).cuda()
+    w2 = torch.from_numpy((rng.standard_normal((1, H, I)) / np.sqrt(I)).astype(np.float32)).to(torch.bfloat16).cuda()
+    ws = torch.empty(a.semmoe_grouped_ffn_workspace_size(P, I, 1), dtype=torch.uint8, device="cuda")
+    y = torch.zeros(P, H, dtype=torch.bfloat16, device="cuda")
+    t0 = time.perf_counter()
+    a.semmoe_selftest_fused_ready_wait(x, w13, w2, P, H, I, y, ws)
+    with pytest.raises(a.SemMoEError) as ei:
+        a.semmoe_check_errors()
+    assert ei.value.code == a.SEMMOE_ERR_DEVICE_TIMEOUT
+    assert ei.value.bits & a.SEMMOE_DEVERR_TIMEOUT
+    assert 0.1 < time.perf_counter() - t0 < 60
+    assert a.semmoe_check_errors() == 0
+    off = torch.tensor([0, P], dtype=torch.int32, device="cuda")
+    pe = torch.zeros(1, dtype=torch.int32, device="cuda")
+    a.semmoe_grouped_ffn_form(x, None, 1, 0, off, pe, w13, w2, P, 1, H, I, y, ws, a.SEMMOE_FORM_FUSED,
+                              a.SEMMOE_FORM_FUSED)
+    assert a.semmoe_check_errors() == 0
+    ref = oracle.grouped_ffn(x.cpu(), off.cpu(), pe.cpu(), w13.cpu().to(torch.float64).numpy(),
+                             w2.cpu().to(torch.float64).numpy(), "bf16")
+    assert max_rel(y.cpu().to(torch.float64).numpy(), ref) < TOL["bf16"]
+
+
 def test_empty_batch_through_every_step():
     """T = 0 (and so P = 0) through the router, lookup, remote count, permute,
     grouped FFN and combine: every call succeeds, the tables come out as the

@@ -66,6 +66,7 @@ SIGNATURES = {
     "semmoe_shared_ffn": (_i, [_vp, _vp, _vp, _i, _i, _i, _i, _vp, _vp, _sz, _vp]),
     "semmoe_combine": (_i, [_vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _vp, _vp]),
     "semmoe_selftest_bounded_wait": (_i, [_vp]),
+    "semmoe_selftest_fused_ready_wait": (_i, [_vp, _vp, _vp, _i, _i, _i, _vp, _vp, _sz, _vp]),
     "semmoe_dp_schedule": (_i, [_vp, _vp, _i, _i, _i, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp]),
     "semmoe_transition_lookup": (_i, [_vp, _vp, _i, _vp, _i, _i, _i, _i, _vp, _vp]),
 }
@@ -312,3 +313,11 @@ def semmoe_selftest_bounded_wait(stream=None):
     """Launch the wait that can never complete (it gives up after 2 s and sets
     the timeout bit); see include/semmoe.h."""
     _check(lib().semmoe_selftest_bounded_wait(_stream(stream)))
+
+
+def semmoe_selftest_fused_ready_wait(x_perm, w13, w2, P, H, I, y_perm, ws, stream=None):
+    """Run the one-launch grouped FFN with GEMM2's readiness waits made
+    unreachable (each gives up after 2 s and sets the timeout bit); see
+    include/semmoe.h."""
+    _check(lib().semmoe_selftest_fused_ready_wait(_p(x_perm), _p(w13), _p(w2), P, H, I, _p(y_perm), _p(ws),
+                                                  ws.numel() * ws.element_size(), _stream(stream)))

@@ -479,4 +479,16 @@ int semmoe_selftest_bounded_wait(void* stream) {
   return cuda_status(launch_selftest_bounded_wait(static_cast<cudaStream_t>(stream)), "semmoe_selftest_bounded_wait");
 }
 
+int semmoe_selftest_fused_ready_wait(const void* x_perm, const void* w13, const void* w2, int P, int H, int I,
+                                     void* y_perm, void* ws, size_t ws_bytes, void* stream) {
+  int rc = check_ffn_args("semmoe_selftest_fused_ready_wait", x_perm, w13, w2, SEMMOE_BF16, P, H, I, y_perm, ws,
+                          ws_bytes);
+  if (rc != SEMMOE_OK) return rc;
+  REQUIRE(P > 0 && P <= 4096, "semmoe_selftest_fused_ready_wait: need 0 < P <= 4096 (P=%d)", P);
+  CHECK_DEVICE("semmoe_selftest_fused_ready_wait");
+  return cuda_status(launch_selftest_fused_ready_wait(x_perm, w13, w2, P, H, I, y_perm, ws,
+                                                      static_cast<cudaStream_t>(stream)),
+                     "semmoe_selftest_fused_ready_wait");
+}
+
 }  // extern "C"

@@ -14,7 +14,7 @@ cudaError_t launch_ffn_tc(const void* x, const int32_t* offsets, const int32_t* 
                           const void* w2, int P, int E, int H, int I, void* y, void* ws, const int32_t* gather,
                           int gather_div, int T_x, int form1, int form2, cudaStream_t s,
                           const int32_t* sorted_to_pair = nullptr, const float* topk_w = nullptr, int k_max = 1,
-                          int T_acc = 0, float* acc = nullptr);
+                          int T_acc = 0, float* acc = nullptr, int fused_stall = 0);
 int ffn_simt_take_errors(cudaStream_t s, int* bits);
 int ffn_tc_take_errors(cudaStream_t s, int* bits);
 
@@ -47,6 +47,15 @@ cudaError_t launch_ffn_combine(const void* x, bool gathered, const int32_t* sort
   if (e != cudaSuccess || P == 0) return e;
   return launch_ffn_tc(x, offsets, p2e, w13, w2, P, E, H, I, nullptr, ws, gathered ? sorted_to_pair : nullptr, k_max,
                        T, SEMMOE_FORM_DEFAULT, SEMMOE_FORM_DEFAULT, s, sorted_to_pair, topk_w, k_max, T, acc);
+}
+
+// One group of P rows through the one-launch FFN with GEMM2's readiness waits
+// made unreachable: every GEMM2 tile's wait runs out after its bound, sets the
+// timeout bit and stops its CTA (bf16 only; the failure-path self-test).
+cudaError_t launch_selftest_fused_ready_wait(const void* x, const void* w13, const void* w2, int P, int H, int I,
+                                             void* y, void* ws, cudaStream_t s) {
+  return launch_ffn_tc(x, nullptr, nullptr, w13, w2, P, 1, H, I, y, ws, nullptr, 1, 0, SEMMOE_FORM_FUSED,
+                       SEMMOE_FORM_FUSED, s, nullptr, nullptr, 1, 0, nullptr, 1);
 }
 
 }  // namespace semmoe

@@ -30,7 +30,11 @@
 //    A rows and half of the weight tile, a third less shared-memory traffic per
 //    SM; pairs cover two m-tiles of one expert, so groups with an odd m-tile
 //    count leave one half idle, which costs more than it saves on short
-//    (I < 512) tiles.
+//    (I < 512) tiles;
+//  * both GEMMs in one launch of independent CTAs (ffn_fused_kernel, the
+//    default where both GEMMs would run as independent CTAs): GEMM2 tiles
+//    start while GEMM1 tiles of other m-tiles still run, so the grid's last
+//    partial wave and the launch boundary between the GEMMs are paid once.
 //
 // Every wait is bounded (%globaltimer and a poll count); a wait that runs out sets the timeout
 // bit of the device error word and an abort flag, after which every role
@@ -580,18 +584,20 @@ ffn_tc_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__
 }
 
 // ---------------------------------------------------------------------------
-// Both GEMMs in one persistent launch (independent CTAs): each CTA walks the
-// list of GEMM1 tiles and then of GEMM2 tiles (round robin over the CTAs), so a
-// CTA whose GEMM1 share ends early goes on with GEMM2 tiles while others finish
-// GEMM1, instead of idling until the last GEMM1 CTA ends.  A GEMM2 tile reads
-// the h rows of one m-tile, written by that m-tile's nt1 GEMM1 tiles: each of
-// the four epilogue warps of a GEMM1 tile, once its h stores have completed,
-// adds 1 to ready[m-tile] (release), and the producer of a GEMM2 tile waits,
-// bounded, until ready[m-tile] = 4 nt1 (acquire) before loading the rows.  A
-// GEMM1 tile waits for nothing and every CTA's GEMM1 tiles come before its
-// GEMM2 tiles, so every wait ends once the CTAs holding those GEMM1 tiles run;
-// the grid has at most one CTA per SM, all resident once any other kernel on
-// the GPU has finished.
+// Both GEMMs in one persistent launch (independent CTAs).  The tiles are
+// numbered GEMM1 first (m-tile major), then GEMM2, and each CTA's producer
+// claims the next number from a global counter whenever it starts a tile, so a
+// CTA whose last GEMM1 tile ends early goes on with GEMM2 tiles while others
+// finish GEMM1, instead of idling until the last GEMM1 CTA ends.  A GEMM2 tile
+// reads the h rows of one m-tile, written by that m-tile's nt1 GEMM1 tiles:
+// each of the four epilogue warps of a GEMM1 tile, once its h stores have
+// completed, adds 1 to ready[m-tile] (release), and the producer of a GEMM2
+// tile waits, bounded, until ready[m-tile] = 4 nt1 (acquire) before loading the
+// rows.  A tile is claimed only by a CTA that is running, GEMM1 tiles wait for
+// nothing, and every GEMM1 tile is numbered before every GEMM2 tile, so each
+// GEMM1 tile a GEMM2 tile waits for belongs to a running CTA that finishes it:
+// no CTA has to be resident for another to progress (a kernel on another stream
+// may hold SMs meanwhile).
 // ---------------------------------------------------------------------------
 // Upper bound on the m-tiles of P rows in G groups: the size of the ready counters.
 __host__ __device__ __forceinline__ int mtiles_max_of(int P, int G) { return (P + BM - 1) / BM + G; }
@@ -610,7 +616,7 @@ ffn_fused_kernel(const __grid_constant__ CUtensorMap map_a1, const __grid_consta
                  const __grid_constant__ CUtensorMap map_b2, const __grid_constant__ CUtensorMap map_o2,
                  const int32_t* __restrict__ offsets, const int32_t* __restrict__ phys_to_expert, int G, int P,
                  int E, int H, int I, int nt1, int nt2, __nv_bfloat16* __restrict__ h, __nv_bfloat16* __restrict__ y,
-                 int* __restrict__ ready) {
+                 int* __restrict__ ready, int ready_extra) {
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   const uint32_t pad = (1024u - (smem_u32(smem_raw) & 1023u)) & 1023u;
   unsigned char* stage_a = smem_raw + pad;
@@ -716,7 +722,7 @@ ffn_fused_kernel(const __grid_constant__ CUtensorMap map_a1, const __grid_consta
         if (g2) {  // the m-tile's h rows: all its GEMM1 tiles published (4 epilogue warps each)
           const uint64_t t_start = globaltimer_ns();
           bool ok = true;
-          for (uint32_t polls = 0; ld_acquire_gpu(ready + mt) < 4 * nt1; ++polls) {
+          for (uint32_t polls = 0; ld_acquire_gpu(ready + mt) < 4 * nt1 + ready_extra; ++polls) {
             if (*abort_flag) { ok = false; break; }
             if (globaltimer_ns() - t_start > kWaitNs || polls > kWaitPolls) {
               atomicOr(&g_err, SEMMOE_DEVERR_TIMEOUT);
@@ -885,7 +891,7 @@ ffn_fused_kernel(const __grid_constant__ CUtensorMap map_a1, const __grid_consta
 cudaError_t launch_fused(const CUtensorMap& ma1, const CUtensorMap& mb1, const CUtensorMap& mo1,
                          const CUtensorMap& ma2, const CUtensorMap& mb2, const CUtensorMap& mo2, const int32_t* offsets,
                          const int32_t* p2e, int G, int P, int E, int H, int I, __nv_bfloat16* h, __nv_bfloat16* y,
-                         int* ready, cudaStream_t s) {
+                         int* ready, cudaStream_t s, int ready_extra) {
   static std::atomic<unsigned long long> smem_set{0};
   cudaError_t e = ensure_smem_limit(ffn_fused_kernel, (int)kSmemBytes, smem_set);
   if (e != cudaSuccess) return e;
@@ -897,7 +903,7 @@ cudaError_t launch_fused(const CUtensorMap& ma1, const CUtensorMap& mb1, const C
   int grid = sm_count();  // one CTA per SM (shared memory)
   if (max_units < grid) grid = (int)max_units;
   ffn_fused_kernel<<<grid, THREADS, kSmemBytes, s>>>(ma1, mb1, mo1, ma2, mb2, mo2, offsets, p2e, G, P, E, H, I, nt1,
-                                                     nt2, h, y, ready);
+                                                     nt2, h, y, ready, ready_extra);
   count_launches(1);
   return cudaGetLastError();
 }
@@ -1277,10 +1283,13 @@ static cudaError_t launch_gemm(int form, const CUtensorMap& ma, const CUtensorMa
 // acc != nullptr: GEMM2 adds each row, weighted by topk_w[sorted_to_pair[q]],
 // into acc [T_acc, H] fp32 (row of token sorted_to_pair[q] / k_max) instead of
 // writing y.
+// fused_stall != 0 (failure-path self-test only): both GEMMs in one launch,
+// with every GEMM2 tile waiting for one readiness count more than its m-tile's
+// GEMM1 tiles ever publish, so each of those waits runs out.
 cudaError_t launch_ffn_tc(const void* x, const int32_t* offsets, const int32_t* p2e, const void* w13,
                           const void* w2, int P, int E, int H, int I, void* y, void* ws, const int32_t* gather_rows,
                           int gather_div, int T_x, int form1, int form2, cudaStream_t s, const int32_t* sorted_to_pair,
-                          const float* topk_w, int k_max, int T_acc, float* acc) {
+                          const float* topk_w, int k_max, int T_acc, float* acc, int fused_stall) {
   if (P == 0) return cudaSuccess;
   const int G = offsets ? E : 1;
   int mode1 = resolve_form(form1, true, I, P, G, gather_rows != nullptr);
@@ -1291,6 +1300,7 @@ cudaError_t launch_ffn_tc(const void* x, const int32_t* offsets, const int32_t* 
   if (form1 == SEMMOE_FORM_DEFAULT && form2 == SEMMOE_FORM_DEFAULT && gather_rows == nullptr && acc == nullptr &&
       mode1 == SEMMOE_FORM_SINGLE && mode2 == SEMMOE_FORM_SINGLE)
     mode1 = mode2 = SEMMOE_FORM_FUSED;
+  if (fused_stall) mode1 = mode2 = SEMMOE_FORM_FUSED;
   const bool fused = mode1 == SEMMOE_FORM_FUSED && gather_rows == nullptr && acc == nullptr;
   // GEMM2's weight box: 256 rows for independent CTAs, 128 for a pair CTA's half of the tile
   const int CL = (mode2 == SEMMOE_FORM_SINGLE || fused) ? 1 : 2;
@@ -1357,7 +1367,7 @@ cudaError_t launch_ffn_tc(const void* x, const int32_t* offsets, const int32_t* 
   __nv_bfloat16* yb = static_cast<__nv_bfloat16*>(y);
   if (fused) {
     int* ready = reinterpret_cast<int*>(static_cast<unsigned char*>(ws) + align_up((size_t)P * I * 2, 256));
-    return launch_fused(ma1, mb1, mo1, ma2, mb2, mo2, offsets, p2e, G, P, E, H, I, h, yb, ready, s);
+    return launch_fused(ma1, mb1, mo1, ma2, mb2, mo2, offsets, p2e, G, P, E, H, I, h, yb, ready, s, fused_stall ? 1 : 0);
   }
   cudaError_t e = launch_gemm<true>(mode1, ma1, mb1, mo1, offsets, p2e, G, P, E, I, H, (I + 127) / 128, ga, h, s);
   if (e != cudaSuccess) return e;

@@ -20,6 +20,8 @@ int combine_take_errors(cudaStream_t s, int* bits);
 int schedule_take_errors(cudaStream_t s, int* bits);
 int selftest_take_errors(cudaStream_t s, int* bits);
 cudaError_t launch_selftest_bounded_wait(cudaStream_t s);
+cudaError_t launch_selftest_fused_ready_wait(const void* x, const void* w13, const void* w2, int P, int H, int I,
+                                             void* y, void* ws, cudaStream_t s);
 
 size_t route_ws_bytes(int T, int H, int E, int x_dtype, int w_dtype);
 // Tensor-core router (route_tc.cu): fp32 logits of bf16 activations.
