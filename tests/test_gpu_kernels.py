@@ -290,7 +290,8 @@ SPLIT_COUNTS = [0, 1, 127, 128, 129, 255, 256, 257, 384, 511, 512, 640, 1000, 3,
 
 @pytest.mark.parametrize("P,E,H,I", [(1000, 8, 256, 160), (5000, 64, 512, 352), (3000, 16, 512, 640),
                                      (sum(SPLIT_COUNTS), 16, 256, 576), (30000, 64, 512, 704),
-                                     (384, 64, 512, 1408), (3072, 64, 256, 200)])
+                                     (384, 64, 512, 1408), (3072, 64, 256, 200),
+                                     (1, 1, 64, 8), (7, 3, 8, 24), (130, 256, 128, 136)])
 def test_grouped_ffn_forms_are_bit_identical(P, E, H, I):
     """Every form of the grouped GEMM -- independent CTAs, 2-SM MMA pairs with
     one or two accumulator buffers, both GEMMs in one launch (GEMM2's tiles
@@ -298,7 +299,9 @@ def test_grouped_ffn_forms_are_bit_identical(P, E, H, I):
     exactly the same bits, and those bits match the oracle's grouped FFN row by
     row within the bf16 tolerance; one case pins group sizes around the 128-
     and 256-row boundaries (empty groups, 1, 127..129, 255..257 rows), two have
-    decode-sized groups (6 and 48 rows on average; I not a multiple of 128)."""
+    decode-sized groups (6 and 48 rows on average; I not a multiple of 128), and
+    three are tiny (one row; H = 8, smaller than one k-block and one output box;
+    256 groups, most of them empty)."""
     rng = np.random.default_rng(P + E)
     if P == sum(SPLIT_COUNTS) and E == len(SPLIT_COUNTS):
         cnt = np.array(SPLIT_COUNTS)
