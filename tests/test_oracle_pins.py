@@ -372,6 +372,29 @@ def test_single_expert_is_plain_swiglu_mlp():
     np.testing.assert_array_equal(res["topk_w"], 1.0)
 
 
+def test_grouped_ffn_routes_each_bucket_to_its_expert():
+    """Bucket b's rows [off[b], off[b+1]) go through expert phys_to_expert[b]
+    and only those rows: the experts are identical up to a factor e + 1 on W2,
+    so each output row names the expert it used (uneven buckets, an empty one,
+    a physical order that is not the identity)."""
+    rng = np.random.default_rng(12)
+    H, I, E = 8, 6, 4
+    base13 = rng.standard_normal((2 * I, H))
+    base2 = rng.standard_normal((H, I))
+    w13 = np.stack([base13] * E)
+    w2 = np.stack([(e + 1) * base2 for e in range(E)])
+    off = np.array([0, 3, 3, 7, 9])
+    pe = np.array([2, 0, 3, 1])
+    x = rng.standard_normal((9, H))
+    y = oracle.grouped_ffn(x, off, pe, w13, w2, "f64")
+    g = x @ base13[:I].T
+    u = x @ base13[I:].T
+    one = (g * scipy.special.expit(g) * u) @ base2.T  # the factor-1 expert on every row
+    for b in range(E):
+        for q in range(off[b], off[b + 1]):
+            np.testing.assert_allclose(y[q], (pe[b] + 1) * one[q], rtol=1e-12, atol=1e-14)
+
+
 def test_shared_expert_adds_with_gate_one():
     rng = np.random.default_rng(10)
     T, H, E, I, R, Is = 15, 8, 4, 6, 2, 10
