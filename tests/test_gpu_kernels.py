@@ -335,6 +335,37 @@ def test_grouped_ffn_forms_are_bit_identical(P, E, H, I):
             assert max_rel(got[hi - 1], ref[hi - 1]) < TOL["bf16"], b
 
 
+@pytest.mark.parametrize("seed", range(10))
+def test_grouped_ffn_one_launch_matches_two_launches_random_groups(seed):
+    """Both GEMMs in one launch (GEMM2 tiles waiting on GEMM1's per m-tile)
+    against the two single-CTA launches, bit for bit, over seeded random group
+    tables: skewed sizes, empty groups, one group holding most rows, one-row
+    groups, H and I from 8 up and not multiples of the tile sizes."""
+    rng = np.random.default_rng(500 + seed)
+    a = abi()
+    E = int(rng.choice([1, 3, 17, 64, 200, 256]))
+    H = int(rng.integers(1, 65)) * 8
+    I = int(rng.integers(1, 97)) * 8
+    P = int(rng.integers(1, 3000))
+    w = rng.dirichlet(np.full(E, 0.3))
+    if seed % 3 == 0:
+        w[rng.integers(E)] += 5.0  # one group holds most rows
+    cnt = rng.multinomial(P, w / w.sum())
+    off = torch.from_numpy(np.r_[0, np.cumsum(cnt)].astype(np.int32)).cuda()
+    pe = torch.from_numpy(rng.permutation(E).astype(np.int32)).cuda()
+    x = torch.from_numpy(rng.standard_normal((P, H)).astype(np.float32)).to(torch.bfloat16).cuda()
+    w13 = torch.from_numpy((rng.standard_normal((E, 2 * I, H)) / np.sqrt(H)).astype(np.float32)).to(torch.bfloat16).cuda()
+    w2 = torch.from_numpy((rng.standard_normal((E, H, I)) / np.sqrt(I)).astype(np.float32)).to(torch.bfloat16).cuda()
+    ws = torch.empty(a.semmoe_grouped_ffn_workspace_size(P, I, 1), dtype=torch.uint8, device="cuda")
+    outs = []
+    for form in (a.SEMMOE_FORM_SINGLE, a.SEMMOE_FORM_FUSED, a.SEMMOE_FORM_FUSED):
+        y = torch.full((P, H), 3.0, dtype=torch.bfloat16, device="cuda")
+        a.semmoe_grouped_ffn_form(x, None, 1, 0, off, pe, w13, w2, P, E, H, I, y, ws, form, form)
+        assert a.semmoe_check_errors() == 0
+        outs.append(y.cpu())
+    assert torch.equal(outs[0], outs[1]) and torch.equal(outs[1], outs[2]), (P, E, H, I)
+
+
 @pytest.mark.parametrize("dtype,T,E,k_max,H,I", [("bf16", 1000, 16, 4, 256, 640), ("bf16", 3001, 64, 6, 512, 1408),
                                                  ("bf16", 257, 8, 8, 128, 160), ("bf16", 700, 8, 4, 200, 96),
                                                  ("f32", 300, 8, 3, 64, 96)])
