@@ -265,6 +265,40 @@ def test_route_tensor_core_per_token_budgets(E, k_max, wd):
     np.testing.assert_allclose(np_(gw), ref_w, rtol=0, atol=GATE_ATOL)
 
 
+@pytest.mark.parametrize("seed", range(10))
+def test_route_random_shapes_every_router_path(seed):
+    """Seeded random router shapes (token counts from one tile to several waves,
+    E from 1 to 256, fp32 or bf16 weights, uniform or per-token budgets), so
+    that every router form runs -- one CTA per token tile, a cluster of CTAs
+    per tile, split-K + top-k: logits within tolerance, picks and gates exact
+    given the GPU's logits, and the count table equal to the per-chunk
+    histogram of the picks."""
+    rng = np.random.default_rng(900 + seed)
+    a = abi()
+    T = int(rng.choice([1, 37, 128, 129, 700, 3000, 9000, 20000]))
+    H = int(rng.integers(1, 49)) * 64 if seed % 2 == 0 else int(rng.integers(1, 257)) * 8
+    E = int(rng.choice([1, 6, 16, 64, 100, 128, 256]))
+    k_max = int(rng.integers(1, min(E, 32) + 1))
+    wd = torch.float32 if seed % 3 else torch.bfloat16
+    per_token = seed % 4 == 1
+    x = torch.from_numpy(rng.standard_normal((T, H)).astype(np.float32) / np.sqrt(H)).to(torch.bfloat16)
+    wr = torch.from_numpy(rng.standard_normal((E, H)).astype(np.float32) / np.sqrt(H)).to(wd)
+    k = rng.integers(1, k_max + 1, size=T).astype(np.int32) if per_token else np.full(T, k_max, np.int32)
+    idx = torch.empty(T, k_max, **i32)
+    gw = torch.empty(T, k_max, dtype=torch.float32, device="cuda")
+    lg = torch.empty(T, E, dtype=torch.float32, device="cuda")
+    stride = a.semmoe_pair_counts_stride(T)
+    counts = torch.full((E * stride,), -3, **i32)
+    a.semmoe_route(x.cuda(), wr.cuda(), None, lg, torch.from_numpy(k).cuda() if per_token else None,
+                   0 if per_token else k_max, T, H, E, k_max, idx, gw, pair_counts=counts)
+    assert a.semmoe_check_errors() == 0
+    assert max_rel(np_(lg), oracle.router_logits(x, wr)) < LOGIT_TOL, (T, H, E, k_max, wd)
+    ref_idx, ref_w = oracle.topk_route(np_(lg), k, k_max)
+    np.testing.assert_array_equal(np_(idx), ref_idx)
+    np.testing.assert_allclose(np_(gw), ref_w, rtol=0, atol=GATE_ATOL)
+    np.testing.assert_array_equal(np_(counts).reshape(E, stride), _chunk_histogram(ref_idx, k, E, stride))
+
+
 @pytest.mark.parametrize("wd", [torch.bfloat16, torch.float32])
 def test_route_tensor_core_grid_beyond_one_wave(wd):
     """More token tiles than SMs: the router GEMM runs two resident CTAs per SM
