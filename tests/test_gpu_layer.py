@@ -36,6 +36,27 @@ FULL = ["tiny_fp32_T256_E8", "dsv2lite_decode_T64", "dsv2lite_decode_T256", "dsv
         "dsv2lite_prefill_T4096", "qwen3_30b_a3b_T16384", "prism_subexpert_T8192"]
 
 
+@pytest.mark.parametrize("seed", range(8))
+def test_layer_random_small(seed):
+    """Seeded random small layers on the four model shapes (token count, hidden
+    and intermediate sizes drawn at random, rows gathered in GEMM1 or copied by
+    the permute), compared with the oracle element by element."""
+    import numpy as np
+    rng = np.random.default_rng(700 + seed)
+    name = ["dsv2lite_prefill_T4096", "qwen3_30b_a3b_T16384", "prism_subexpert_T8192",
+            "dsv2lite_decode_T64"][seed % 4]
+    h_lo = max(2, (wl.CONFIGS[name].E + 7) // 8)  # biased routing builds E orthonormal router rows: H >= E
+    over = dict(T=int(rng.integers(1, 700)), H=int(rng.integers(h_lo, 65)) * 8, I=int(rng.integers(1, 65)) * 8,
+                V=3000)
+    if wl.CONFIGS[name].I_shared:
+        over["I_shared"] = int(rng.integers(1, 65)) * 8
+    if wl.CONFIGS[name].k_choices:
+        over["tokens_per_request"] = int(rng.integers(1, 80))
+    d = wl.make_inputs(wl.scaled(name, **over))
+    res, P = run_gpu(d, fused_gather=bool(seed % 2))
+    check_layer_full(d, res, P)
+
+
 @pytest.mark.parametrize("name", FULL)
 def test_layer_full_size(name):
     d = wl.make_inputs(wl.CONFIGS[name])
