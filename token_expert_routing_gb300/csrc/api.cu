@@ -418,8 +418,10 @@ int semmoe_shared_ffn(const void* x, const void* ws13, const void* ws2, int dtyp
   if (rc != SEMMOE_OK) return rc;
   if (T == 0) return SEMMOE_OK;
   CHECK_DEVICE("semmoe_shared_ffn");
+  // not as programmatic dependents: it runs beside the layer's steps on another
+  // stream, where CTAs waiting for their turn would hold SMs those steps could use
   return cuda_status(launch_ffn(x, nullptr, nullptr, ws13, ws2, dtype, T, 1, H, I_s, y_shared, ws, nullptr, 1, 0,
-                                static_cast<cudaStream_t>(stream)),
+                                static_cast<cudaStream_t>(stream), SEMMOE_FORM_DEFAULT, SEMMOE_FORM_DEFAULT, false),
                      "semmoe_shared_ffn");
 }
 

@@ -66,6 +66,8 @@ combine_kernel(const T* __restrict__ y_perm, const int32_t* __restrict__ pair_to
                const float* __restrict__ topk_w, const T* __restrict__ y_shared, int T_, int H, int k_max,
                int P, T* __restrict__ out) {
   using V = Vec16<T>;
+  pdl_trigger();
+  pdl_wait();  // y_perm (the grouped FFN before it)
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   const int kk = k_max < 32 ? k_max : 32;
   const int pass_elems = 32 * V::N * CH;
@@ -151,6 +153,8 @@ combine_kernel(const T* __restrict__ y_perm, const int32_t* __restrict__ pair_to
 __global__ void __launch_bounds__(kThreads)
 combine_finish_kernel(const float4* __restrict__ acc, const uint4* __restrict__ y_shared, long long n8,
                       uint4* __restrict__ out) {
+  pdl_trigger();
+  pdl_wait();  // acc (the grouped FFN before it)
   for (long long i = blockIdx.x * (long long)kThreads + threadIdx.x; i < n8; i += (long long)gridDim.x * kThreads) {
     const float4 a = acc[2 * i], b = acc[2 * i + 1];
     float v[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
@@ -176,9 +180,10 @@ cudaError_t launch_combine_finish(const float* acc, const void* y_shared, int T,
   long long blocks = (n8 + kThreads - 1) / kThreads;
   const long long cap = 8LL * sm_count();
   if (blocks > cap) blocks = cap;
-  combine_finish_kernel<<<(int)blocks, kThreads, 0, s>>>(reinterpret_cast<const float4*>(acc),
-                                                         static_cast<const uint4*>(y_shared), n8,
-                                                         static_cast<uint4*>(out));
+  cudaError_t e = launch_kernel(combine_finish_kernel, dim3((unsigned)blocks), dim3(kThreads), 0, s, 1, true,
+                                reinterpret_cast<const float4*>(acc), static_cast<const uint4*>(y_shared), n8,
+                                static_cast<uint4*>(out));
+  if (e != cudaSuccess) return e;
   count_launches(1);
   return cudaGetLastError();
 }
@@ -195,14 +200,16 @@ cudaError_t launch_combine(const void* y_perm, const int32_t* pair_to_sorted, co
   long long blocks = (units + kWarps - 1) / kWarps;
   const long long cap = 8LL * sm_count();
   if (blocks > cap) blocks = cap;
+  cudaError_t e;
   if (dtype == SEMMOE_BF16)
-    combine_kernel<__nv_bfloat16, kCH, kJB><<<(int)blocks, kThreads, 0, s>>>(
-        static_cast<const __nv_bfloat16*>(y_perm), pair_to_sorted, topk_w,
-        static_cast<const __nv_bfloat16*>(y_shared), T, H, k_max, P, static_cast<__nv_bfloat16*>(out));
+    e = launch_kernel(combine_kernel<__nv_bfloat16, kCH, kJB>, dim3((unsigned)blocks), dim3(kThreads), 0, s, 1, true,
+                      static_cast<const __nv_bfloat16*>(y_perm), pair_to_sorted, topk_w,
+                      static_cast<const __nv_bfloat16*>(y_shared), T, H, k_max, P, static_cast<__nv_bfloat16*>(out));
   else
-    combine_kernel<float, kCH, kJB><<<(int)blocks, kThreads, 0, s>>>(
-        static_cast<const float*>(y_perm), pair_to_sorted, topk_w, static_cast<const float*>(y_shared), T, H,
-        k_max, P, static_cast<float*>(out));
+    e = launch_kernel(combine_kernel<float, kCH, kJB>, dim3((unsigned)blocks), dim3(kThreads), 0, s, 1, true,
+                      static_cast<const float*>(y_perm), pair_to_sorted, topk_w, static_cast<const float*>(y_shared),
+                      T, H, k_max, P, static_cast<float*>(out));
+  if (e != cudaSuccess) return e;
   count_launches(1);
   return cudaGetLastError();
 }

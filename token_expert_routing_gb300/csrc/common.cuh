@@ -6,6 +6,7 @@
 #include <stdint.h>
 
 #include <atomic>
+#include <utility>
 
 #include "semmoe.h"
 
@@ -37,6 +38,18 @@ __device__ __forceinline__ uint64_t globaltimer_ns() {
   asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
   return t;
 }
+
+// Programmatic dependent launch.  The kernels of the layer follow one another
+// on a stream; each launched as a dependent may start -- and run its setup
+// (barriers, tensor memory, tensor-map prefetches: nothing in global memory) --
+// once every CTA of the kernel before it has run pdl_trigger, and it waits in
+// pdl_wait until that kernel has completed and its writes are visible.  So each
+// kernel calls pdl_trigger at its start and, when it can be launched as a
+// dependent (launch_kernel), pdl_wait before its first global load or store (a kernel that waits
+// completes only after the kernel before it, so the guarantee chains).  Both
+// are no-ops for a kernel launched without the attribute.
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 
 // Read and clear one translation unit's device error word.
 template <typename Sym>
@@ -72,6 +85,38 @@ inline cudaError_t ensure_smem_limit(K kernel, int bytes, std::atomic<unsigned l
   return e;
 }
 inline int ceil_div(int a, int b) { return (a + b - 1) / b; }
+
+// Launch `kern` on `s` with an optional cluster size; dependent = true makes it
+// a programmatic dependent of the kernel before it on `s`
+// (cudaLaunchAttributeProgrammaticStreamSerialization; see pdl_wait).  Its CTAs
+// may then occupy SMs while they wait, so only the layer's chain of steps on the
+// caller's stream launches this way, not work beside it on another stream.
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_kernel(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                                 unsigned cluster, bool dependent, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[2];
+  int n = 0;
+  if (dependent) {
+    attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[n].val.programmaticStreamSerializationAllowed = 1;
+    ++n;
+  }
+  if (cluster > 1) {
+    attr[n].id = cudaLaunchAttributeClusterDimension;
+    attr[n].val.clusterDim.x = cluster;
+    attr[n].val.clusterDim.y = 1;
+    attr[n].val.clusterDim.z = 1;
+    ++n;
+  }
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cfg.attrs = attr;
+  cfg.numAttrs = n;
+  return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
+}
 
 // Streaming multiprocessors of the current device.
 inline int sm_count() {

@@ -14,7 +14,7 @@ cudaError_t launch_ffn_tc(const void* x, const int32_t* offsets, const int32_t* 
                           const void* w2, int P, int E, int H, int I, void* y, void* ws, const int32_t* gather,
                           int gather_div, int T_x, int form1, int form2, cudaStream_t s,
                           const int32_t* sorted_to_pair = nullptr, const float* topk_w = nullptr, int k_max = 1,
-                          int T_acc = 0, float* acc = nullptr, int fused_stall = 0);
+                          int T_acc = 0, float* acc = nullptr, int fused_stall = 0, bool dependent = true);
 int ffn_simt_take_errors(cudaStream_t s, int* bits);
 int ffn_tc_take_errors(cudaStream_t s, int* bits);
 
@@ -33,9 +33,11 @@ size_t ffn_ws_bytes(int P, int I, int dtype) {
 
 cudaError_t launch_ffn(const void* x, const int32_t* offsets, const int32_t* p2e, const void* w13,
                        const void* w2, int dtype, int P, int E, int H, int I, void* y, void* ws,
-                       const int32_t* gather, int gather_div, int T_x, cudaStream_t s, int form1, int form2) {
+                       const int32_t* gather, int gather_div, int T_x, cudaStream_t s, int form1, int form2,
+                       bool dependent) {
   if (dtype == SEMMOE_BF16 && form1 != SEMMOE_FORM_CUDA_CORE)
-    return launch_ffn_tc(x, offsets, p2e, w13, w2, P, E, H, I, y, ws, gather, gather_div, T_x, form1, form2, s);
+    return launch_ffn_tc(x, offsets, p2e, w13, w2, P, E, H, I, y, ws, gather, gather_div, T_x, form1, form2, s,
+                         nullptr, nullptr, 1, 0, nullptr, 0, dependent);
   return launch_ffn_simt(x, offsets, p2e, w13, w2, dtype, P, E, H, I, y, ws, gather, gather_div, T_x, s);
 }
 

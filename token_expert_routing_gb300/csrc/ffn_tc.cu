@@ -248,6 +248,7 @@ ffn_tc_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__
               const int32_t* __restrict__ offsets, const int32_t* __restrict__ phys_to_expert, int G, int P,
               int E, int N, int K, int n_tiles, const int32_t* __restrict__ gather, int gather_div, int gather_rows,
               __nv_bfloat16* __restrict__ out, const __nv_bfloat16* __restrict__ gx, Scatter sc) {
+  pdl_trigger();  // the kernel after it may start its setup
   static_assert(GW == 0 || GW * 32 * RPL * 16 == BM * BK * 2, "gather warps cover one A stage");
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   const uint32_t pad = (1024u - (smem_u32(smem_raw) & 1023u)) & 1023u;
@@ -277,13 +278,14 @@ ffn_tc_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__
     prefetch_map(&map_b);
     prefetch_map(&map_out);
   }
+  if (warp == 1) {  // whole warp: allocate all 512 TMEM columns
+    tmem_alloc(&sh.tmem_base, TMEM_COLS);
+  }
+  pdl_wait();  // the rows and group offsets the kernels before it wrote
   for (int g = threadIdx.x; g <= G; g += blockDim.x) sh.off[g] = offsets ? offsets[g] : (g == 0 ? 0 : P);
   for (int g = threadIdx.x; g < G; g += blockDim.x) sh.pe[g] = phys_to_expert ? phys_to_expert[g] : 0;
   __syncthreads();
 
-  if (warp == 1) {  // whole warp: allocate all 512 TMEM columns
-    tmem_alloc(&sh.tmem_base, TMEM_COLS);
-  }
   if (warp == 0) {  // exclusive prefix of m-tiles per group, 8 groups per lane
     int cnt[8], sum = 0;
 #pragma unroll
@@ -617,6 +619,7 @@ ffn_fused_kernel(const __grid_constant__ CUtensorMap map_a1, const __grid_consta
                  const int32_t* __restrict__ offsets, const int32_t* __restrict__ phys_to_expert, int G, int P,
                  int E, int H, int I, int nt1, int nt2, __nv_bfloat16* __restrict__ h, __nv_bfloat16* __restrict__ y,
                  int* __restrict__ ready, int ready_extra) {
+  pdl_trigger();  // the kernel after it may start its setup
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   const uint32_t pad = (1024u - (smem_u32(smem_raw) & 1023u)) & 1023u;
   unsigned char* stage_a = smem_raw + pad;
@@ -654,10 +657,11 @@ ffn_fused_kernel(const __grid_constant__ CUtensorMap map_a1, const __grid_consta
     prefetch_map(&map_b2);
     prefetch_map(&map_o2);
   }
+  if (warp == 1) tmem_alloc(&sh.tmem_base, TMEM_COLS);
+  pdl_wait();  // the rows and group offsets the kernels before it wrote
   for (int g = threadIdx.x; g <= G; g += blockDim.x) sh.off[g] = offsets ? offsets[g] : (g == 0 ? 0 : P);
   for (int g = threadIdx.x; g < G; g += blockDim.x) sh.pe[g] = phys_to_expert ? phys_to_expert[g] : 0;
   __syncthreads();
-  if (warp == 1) tmem_alloc(&sh.tmem_base, TMEM_COLS);
   if (warp == 0) {  // exclusive prefix of m-tiles per group, 8 groups per lane
     int cnt[8], sum = 0;
 #pragma unroll
@@ -888,22 +892,35 @@ ffn_fused_kernel(const __grid_constant__ CUtensorMap map_a1, const __grid_consta
   }
 }
 
+// Zeroes the one-launch FFN's readiness and tile counters; waits for the
+// kernel before it so that the FFN after it, waiting for this one, also
+// finds that kernel's writes (see pdl_wait).
+__global__ void __launch_bounds__(256) zero_counters_kernel(int* __restrict__ p, int n) {
+  pdl_trigger();
+  for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n; i += gridDim.x * blockDim.x) p[i] = 0;
+  pdl_wait();
+}
+
 cudaError_t launch_fused(const CUtensorMap& ma1, const CUtensorMap& mb1, const CUtensorMap& mo1,
                          const CUtensorMap& ma2, const CUtensorMap& mb2, const CUtensorMap& mo2, const int32_t* offsets,
                          const int32_t* p2e, int G, int P, int E, int H, int I, __nv_bfloat16* h, __nv_bfloat16* y,
-                         int* ready, cudaStream_t s, int ready_extra) {
+                         int* ready, cudaStream_t s, int ready_extra, bool dependent) {
   static std::atomic<unsigned long long> smem_set{0};
   cudaError_t e = ensure_smem_limit(ffn_fused_kernel, (int)kSmemBytes, smem_set);
   if (e != cudaSuccess) return e;
   const int nt1 = (I + 127) / 128, nt2 = (H + BN - 1) / BN;
   const long long mtiles_max = mtiles_max_of(P, G);
-  e = cudaMemsetAsync(ready, 0, (size_t)(mtiles_max + 1) * sizeof(int), s);  // + the tile counter
+  const int n_counters = (int)(mtiles_max + 1);  // + the tile counter
+  e = launch_kernel(zero_counters_kernel, dim3((n_counters + 255) / 256), dim3(256), 0, s, 1, dependent, ready,
+                    n_counters);
   if (e != cudaSuccess) return e;
+  count_launches(1);
   const long long max_units = mtiles_max * (nt1 + nt2);
   int grid = sm_count();  // one CTA per SM (shared memory)
   if (max_units < grid) grid = (int)max_units;
-  ffn_fused_kernel<<<grid, THREADS, kSmemBytes, s>>>(ma1, mb1, mo1, ma2, mb2, mo2, offsets, p2e, G, P, E, H, I, nt1,
-                                                     nt2, h, y, ready, ready_extra);
+  e = launch_kernel(ffn_fused_kernel, dim3(grid), dim3(THREADS), kSmemBytes, s, 1, dependent, ma1, mb1, mo1, ma2, mb2,
+                    mo2, offsets, p2e, G, P, E, H, I, nt1, nt2, h, y, ready, ready_extra);
+  if (e != cudaSuccess) return e;
   count_launches(1);
   return cudaGetLastError();
 }
@@ -940,6 +957,7 @@ ffn_pair_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant
                 const int32_t* __restrict__ offsets, const int32_t* __restrict__ phys_to_expert, int G, int P,
                 int E, int N, int K, int n_tiles, const int32_t* __restrict__ gather, int gather_div, int gather_rows,
                 __nv_bfloat16* __restrict__ out, Scatter sc) {
+  pdl_trigger();  // the kernel after it may start its setup
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   const uint32_t pad = (1024u - (smem_u32(smem_raw) & 1023u)) & 1023u;
   unsigned char* ring = smem_raw + pad;  // stage s: A [128 x 64] then B half [128 x 64]
@@ -966,10 +984,11 @@ ffn_pair_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant
     prefetch_map(&map_b);
     prefetch_map(&map_out);
   }
+  if (warp == 1) tmem_alloc_pair(&sh.tmem_base, NBUF * ACC_COLS);
+  pdl_wait();  // the rows and group offsets the kernels before it wrote
   for (int g = threadIdx.x; g <= G; g += THREADS) sh.off[g] = offsets ? offsets[g] : (g == 0 ? 0 : P);
   for (int g = threadIdx.x; g < G; g += THREADS) sh.pe[g] = phys_to_expert ? phys_to_expert[g] : 0;
   __syncthreads();
-  if (warp == 1) tmem_alloc_pair(&sh.tmem_base, NBUF * ACC_COLS);
   if (warp == 0) {  // exclusive prefix of m-tile pairs per group, 8 groups per lane
     int cnt[8], sum = 0;
 #pragma unroll
@@ -1180,7 +1199,7 @@ template <bool GLU, int GW = 0, bool SC = false>
 cudaError_t launch_one(const CUtensorMap& ma, const CUtensorMap& mb, const CUtensorMap& mo, const int32_t* offsets,
                        const int32_t* p2e,
                        int G, int P, int E, int N, int K, int n_tiles, Gather ga, __nv_bfloat16* out,
-                       cudaStream_t s, Scatter sc = Scatter()) {
+                       cudaStream_t s, bool dependent, Scatter sc = Scatter()) {
   auto kern = ffn_tc_kernel<GLU, GW, SC>;
   static std::atomic<unsigned long long> smem_set{0};
   cudaError_t e = ensure_smem_limit(kern, (int)kSmemBytes, smem_set);
@@ -1188,8 +1207,9 @@ cudaError_t launch_one(const CUtensorMap& ma, const CUtensorMap& mb, const CUten
   const long long max_units = ((long long)(P + BM - 1) / BM + G) * n_tiles;  // >= tile units of any grouping
   int grid = sm_count();
   if (max_units < grid) grid = (int)max_units;
-  kern<<<grid, THREADS + 32 * GW, kSmemBytes, s>>>(ma, mb, mo, offsets, p2e, G, P, E, N, K, n_tiles, ga.rows, ga.div,
-                                                   ga.n, out, ga.x, sc);
+  e = launch_kernel(kern, dim3(grid), dim3(THREADS + 32 * GW), kSmemBytes, s, 1, dependent, ma, mb, mo, offsets, p2e,
+                    G, P, E, N, K, n_tiles, ga.rows, ga.div, ga.n, out, ga.x, sc);
+  if (e != cudaSuccess) return e;
   count_launches(1);
   return cudaGetLastError();
 }
@@ -1198,7 +1218,7 @@ template <bool GLU, int NBUF, bool SC = false>
 cudaError_t launch_pair(const CUtensorMap& ma, const CUtensorMap& mb, const CUtensorMap& mo, const int32_t* offsets,
                         const int32_t* p2e,
                         int G, int P, int E, int N, int K, int n_tiles, Gather ga, __nv_bfloat16* out,
-                        cudaStream_t s, Scatter sc = Scatter()) {
+                        cudaStream_t s, bool dependent, Scatter sc = Scatter()) {
   auto kern = ffn_pair_kernel<GLU, NBUF, SC>;
   static std::atomic<unsigned long long> smem_set{0};
   cudaError_t e = ensure_smem_limit(kern, (int)kPairSmemBytes, smem_set);
@@ -1222,9 +1242,8 @@ cudaError_t launch_pair(const CUtensorMap& ma, const CUtensorMap& mb, const CUte
   if (clusters < 1) return cudaErrorInvalidConfiguration;
   long long units = clusters;
   if (max_units < units) units = max_units;
-  cfg.gridDim = dim3((unsigned)(units * 2));
-  e = cudaLaunchKernelEx(&cfg, kern, ma, mb, mo, offsets, p2e, G, P, E, N, K, n_tiles, ga.rows, ga.div, ga.n, out,
-                         sc);
+  e = launch_kernel(kern, dim3((unsigned)(units * 2)), dim3(THREADS), kPairSmemBytes, s, 2, dependent, ma, mb, mo,
+                    offsets, p2e, G, P, E, N, K, n_tiles, ga.rows, ga.div, ga.n, out, sc);
   if (e != cudaSuccess) return e;
   count_launches(1);
   return cudaGetLastError();
@@ -1253,28 +1272,30 @@ static int resolve_form(int form, bool glu, int I, int P, int G, bool gathered) 
 template <bool GLU>
 static cudaError_t launch_gemm(int form, const CUtensorMap& ma, const CUtensorMap& mb, const CUtensorMap& mo,
                                const int32_t* offsets, const int32_t* p2e, int G, int P, int E, int N, int K,
-                               int n_tiles, Gather ga, __nv_bfloat16* out, cudaStream_t s,
+                               int n_tiles, Gather ga, __nv_bfloat16* out, cudaStream_t s, bool dep,
                                const Scatter* sc = nullptr) {
   if constexpr (!GLU) {
     if (sc != nullptr) {  // GEMM2 adding its rows into the token-order output
       if (form == SEMMOE_FORM_PAIR1)
-        return launch_pair<false, 1, true>(ma, mb, mo, offsets, p2e, G, P, E, N, K, n_tiles, ga, out, s, *sc);
+        return launch_pair<false, 1, true>(ma, mb, mo, offsets, p2e, G, P, E, N, K, n_tiles, ga, out, s, dep, *sc);
       if (form == SEMMOE_FORM_PAIR)
-        return launch_pair<false, 2, true>(ma, mb, mo, offsets, p2e, G, P, E, N, K, n_tiles, ga, out, s, *sc);
-      return launch_one<false, 0, true>(ma, mb, mo, offsets, p2e, G, P, E, N, K, n_tiles, ga, out, s, *sc);
+        return launch_pair<false, 2, true>(ma, mb, mo, offsets, p2e, G, P, E, N, K, n_tiles, ga, out, s, dep, *sc);
+      return launch_one<false, 0, true>(ma, mb, mo, offsets, p2e, G, P, E, N, K, n_tiles, ga, out, s, dep, *sc);
     }
   }
   switch (form) {
-    case SEMMOE_FORM_PAIR1: return launch_pair<GLU, 1>(ma, mb, mo, offsets, p2e, G, P, E, N, K, n_tiles, ga, out, s);
-    case SEMMOE_FORM_PAIR: return launch_pair<GLU, 2>(ma, mb, mo, offsets, p2e, G, P, E, N, K, n_tiles, ga, out, s);
+    case SEMMOE_FORM_PAIR1:
+      return launch_pair<GLU, 1>(ma, mb, mo, offsets, p2e, G, P, E, N, K, n_tiles, ga, out, s, dep);
+    case SEMMOE_FORM_PAIR:
+      return launch_pair<GLU, 2>(ma, mb, mo, offsets, p2e, G, P, E, N, K, n_tiles, ga, out, s, dep);
     case SEMMOE_FORM_SINGLE_TMA_GATHER:  // gathered rows by TMA four-row gathers from the producer warp
-      return launch_one<GLU>(ma, mb, mo, offsets, p2e, G, P, E, N, K, n_tiles, ga, out, s);
+      return launch_one<GLU>(ma, mb, mo, offsets, p2e, G, P, E, N, K, n_tiles, ga, out, s, dep);
     default:
       if constexpr (GLU) {
         if (ga.rows != nullptr)  // gathered rows: gathering warps
-          return launch_one<GLU, GATHER_WARPS>(ma, mb, mo, offsets, p2e, G, P, E, N, K, n_tiles, ga, out, s);
+          return launch_one<GLU, GATHER_WARPS>(ma, mb, mo, offsets, p2e, G, P, E, N, K, n_tiles, ga, out, s, dep);
       }
-      return launch_one<GLU>(ma, mb, mo, offsets, p2e, G, P, E, N, K, n_tiles, ga, out, s);
+      return launch_one<GLU>(ma, mb, mo, offsets, p2e, G, P, E, N, K, n_tiles, ga, out, s, dep);
   }
 }
 
@@ -1286,10 +1307,12 @@ static cudaError_t launch_gemm(int form, const CUtensorMap& ma, const CUtensorMa
 // fused_stall != 0 (failure-path self-test only): both GEMMs in one launch,
 // with every GEMM2 tile waiting for one readiness count more than its m-tile's
 // GEMM1 tiles ever publish, so each of those waits runs out.
+// dependent: every launch is a programmatic dependent of the kernel before it
+// on s (launch_kernel); false for work that runs beside the layer's chain.
 cudaError_t launch_ffn_tc(const void* x, const int32_t* offsets, const int32_t* p2e, const void* w13,
                           const void* w2, int P, int E, int H, int I, void* y, void* ws, const int32_t* gather_rows,
                           int gather_div, int T_x, int form1, int form2, cudaStream_t s, const int32_t* sorted_to_pair,
-                          const float* topk_w, int k_max, int T_acc, float* acc, int fused_stall) {
+                          const float* topk_w, int k_max, int T_acc, float* acc, int fused_stall, bool dependent) {
   if (P == 0) return cudaSuccess;
   const int G = offsets ? E : 1;
   int mode1 = resolve_form(form1, true, I, P, G, gather_rows != nullptr);
@@ -1367,12 +1390,14 @@ cudaError_t launch_ffn_tc(const void* x, const int32_t* offsets, const int32_t* 
   __nv_bfloat16* yb = static_cast<__nv_bfloat16*>(y);
   if (fused) {
     int* ready = reinterpret_cast<int*>(static_cast<unsigned char*>(ws) + align_up((size_t)P * I * 2, 256));
-    return launch_fused(ma1, mb1, mo1, ma2, mb2, mo2, offsets, p2e, G, P, E, H, I, h, yb, ready, s, fused_stall ? 1 : 0);
+    return launch_fused(ma1, mb1, mo1, ma2, mb2, mo2, offsets, p2e, G, P, E, H, I, h, yb, ready, s, fused_stall ? 1 : 0,
+                        dependent);
   }
-  cudaError_t e = launch_gemm<true>(mode1, ma1, mb1, mo1, offsets, p2e, G, P, E, I, H, (I + 127) / 128, ga, h, s);
+  cudaError_t e = launch_gemm<true>(mode1, ma1, mb1, mo1, offsets, p2e, G, P, E, I, H, (I + 127) / 128, ga, h, s,
+                                    dependent);
   if (e != cudaSuccess) return e;
   return launch_gemm<false>(mode2, ma2, mb2, mo2, offsets, p2e, G, P, E, H, I, (H + BN - 1) / BN, Gather(), yb, s,
-                            acc != nullptr ? &sc : nullptr);
+                            dependent, acc != nullptr ? &sc : nullptr);
 }
 
 }  // namespace semmoe

@@ -95,10 +95,12 @@ inline size_t ffn_ready_bytes(int P) { return align_up((size_t)((P > 0 ? P : 1) 
 // row gather[q] / gather_div; otherwise x holds the P sorted rows.
 // form1 / form2: SEMMOE_FORM_* of GEMM1 / GEMM2 (SEMMOE_FORM_DEFAULT: chosen from
 // the shapes; SEMMOE_FORM_CUDA_CORE in form1 runs both GEMMs on CUDA cores).
+// dependent: the tensor-core kernels launch as programmatic dependents of the
+// kernel before them on s (the layer's own chain; false beside it).
 cudaError_t launch_ffn(const void* x, const int32_t* offsets, const int32_t* phys_to_expert,
                        const void* w13, const void* w2, int dtype, int P, int E, int H, int I,
                        void* y, void* ws, const int32_t* gather, int gather_div, int T_x, cudaStream_t s,
-                       int form1 = SEMMOE_FORM_DEFAULT, int form2 = SEMMOE_FORM_DEFAULT);
+                       int form1 = SEMMOE_FORM_DEFAULT, int form2 = SEMMOE_FORM_DEFAULT, bool dependent = true);
 
 // The combine folded into GEMM2 (bf16): acc [T, H] fp32 zeroed, then the grouped
 // FFN whose GEMM2 adds its gate-weighted rows into acc; launch_combine_finish

@@ -62,6 +62,8 @@ inline int internal_chunk_tokens(int T) {
 __global__ void __launch_bounds__(kHistThreads)
 perm_count_kernel(const int32_t* __restrict__ topk_idx, int T, int k_max, int E, int chunk, int ncp,
                   int32_t* __restrict__ counts) {
+  pdl_trigger();
+  pdl_wait();  // topk_idx (the router before it)
   __shared__ int h[kMaxE];
   for (int e = threadIdx.x; e < E; e += kHistThreads) h[e] = 0;
   __syncthreads();
@@ -147,6 +149,8 @@ __device__ __forceinline__ void copy_token_row(const unsigned char* __restrict__
 __global__ void __launch_bounds__(kHistThreads)
 perm_copy_kernel(const unsigned char* __restrict__ x, const int32_t* __restrict__ pair_to_sorted, int T, int k_max,
                  int P, int row_bytes, unsigned char* __restrict__ x_perm) {
+  pdl_trigger();
+  pdl_wait();  // pair_to_sorted (the ranking kernel before it)
   const int warp = threadIdx.x / 32;
   for (int t = blockIdx.x * 8 + warp; t < T; t += gridDim.x * 8)
     copy_token_row(x, pair_to_sorted + (size_t)t * k_max, t, k_max, P, row_bytes, x_perm);
@@ -179,6 +183,7 @@ perm_rank_copy_kernel(const int32_t* __restrict__ topk_idx, const int32_t* __res
   __shared__ int abort_s;
   extern __shared__ __align__(128) unsigned char slots_smem[];  // kWarps x kSlotBytes (copy only)
   const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
+  pdl_trigger();
   if (tid == 0) {
     for (int w = 0; w < kWarps; ++w) tc::mbar_init(&cbar[w], 1);
     abort_s = 0;
@@ -189,6 +194,7 @@ perm_rank_copy_kernel(const int32_t* __restrict__ topk_idx, const int32_t* __res
   for (int i = tid; i < E; i += kThreads) sub[i] = 0;
   for (int i = tid; i < kWarps * kMaxE; i += kThreads) (&wcnt[0][0])[i] = 0;
   __syncthreads();
+  pdl_wait();  // topk_idx and the count table (the router before it)
 
   // Every load that depends on nothing computed here is issued first, so that
   // their latencies overlap: the first row each warp copies (the row does not
@@ -460,7 +466,9 @@ cudaError_t launch_permute(const int32_t* topk_idx, const int32_t* expert_rank, 
     nc = (T + chunk - 1) / chunk;
     int32_t* own = static_cast<int32_t*>(ws);
     if (nc > 0) {
-      perm_count_kernel<<<nc, kHistThreads, 0, s>>>(topk_idx, T, k_max, E, chunk, padded_chunks(nc), own);
+      cudaError_t e = launch_kernel(perm_count_kernel, dim3(nc), dim3(kHistThreads), 0, s, 1, true, topk_idx, T,
+                                    k_max, E, chunk, padded_chunks(nc), own);
+      if (e != cudaSuccess) return e;
       count_launches(1);
     }
     counts = own;
@@ -483,17 +491,21 @@ cudaError_t launch_permute(const int32_t* topk_idx, const int32_t* expert_rank, 
   static std::atomic<unsigned long long> smem_set{0};
   cudaError_t e = ensure_smem_limit(perm_rank_copy_kernel, (int)(kWarps * kSlotBytes), smem_set);
   if (e != cudaSuccess) return e;
-  perm_rank_copy_kernel<<<grid, kThreads, dyn, s>>>(
-      topk_idx, expert_rank, counts, nc, padded_chunks(nc), chunk, T, k_max, E, R, P, tpc, expert_offsets,
-      rank_offsets, phys_to_expert, expert_counts, sorted_to_pair, pair_to_sorted,
-      copy ? static_cast<const unsigned char*>(x) : nullptr, row_bytes, static_cast<unsigned char*>(x_perm));
+  e = launch_kernel(perm_rank_copy_kernel, dim3(grid), dim3(kThreads), dyn, s, 1, true, topk_idx, expert_rank,
+                    counts, nc, padded_chunks(nc), chunk, T, k_max, E, R, P, tpc, expert_offsets, rank_offsets,
+                    phys_to_expert, expert_counts, sorted_to_pair, pair_to_sorted,
+                    copy ? static_cast<const unsigned char*>(x) : static_cast<const unsigned char*>(nullptr),
+                    row_bytes, static_cast<unsigned char*>(x_perm));
+  if (e != cudaSuccess) return e;
   count_launches(1);
   if (separate) {
     int blocks = (T + 7) / 8;
     const int cap = sm_count() * 16;
     if (blocks > cap) blocks = cap;
-    perm_copy_kernel<<<blocks, kHistThreads, 0, s>>>(static_cast<const unsigned char*>(x), pair_to_sorted, T, k_max,
-                                                     P, row_bytes, static_cast<unsigned char*>(x_perm));
+    e = launch_kernel(perm_copy_kernel, dim3(blocks), dim3(kHistThreads), 0, s, 1, true,
+                      static_cast<const unsigned char*>(x), static_cast<const int32_t*>(pair_to_sorted), T, k_max, P,
+                      row_bytes, static_cast<unsigned char*>(x_perm));
+    if (e != cudaSuccess) return e;
     count_launches(1);
   }
   return cudaGetLastError();

@@ -253,6 +253,7 @@ route_kernel(const TX* __restrict__ x, const TW* __restrict__ w, const float* __
              int T, int H, int E, int k_max, int32_t* __restrict__ topk_idx,
              float* __restrict__ topk_w, PairCounts pc) {
   extern __shared__ __align__(16) unsigned char smem_raw[];
+  pdl_trigger();  // the permute after it may start its setup
   const int Epad = (E + 31) / 32 * 32;
   float* lg = reinterpret_cast<float*>(smem_raw);
   float* xs = lg + kRouteTok * Epad;

@@ -79,6 +79,7 @@ template <int S, int CPS>  // CPS: resident CTAs per SM the ring is sized for
 __global__ void __launch_bounds__(THREADS, CPS)
 route_tc_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_constant__ CUtensorMap map_w, int T, int H,
                 int E, int EC, int stages, int kb_per_slice, float* __restrict__ partials) {
+  pdl_trigger();  // the kernel after it may start its setup
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   const uint32_t pad = (1024u - (smem_u32(smem_raw) & 1023u)) & 1023u;
   unsigned char* ring = smem_raw + pad;  // stage s: A tile then B tile, stage_bytes apart
@@ -257,6 +258,7 @@ route_topk_tc_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_con
                      const int32_t* __restrict__ k_per_token, int k_uniform, int k_max,
                      int32_t* __restrict__ topk_idx, float* __restrict__ topk_w, int32_t* __restrict__ counts,
                      int count_stride) {
+  pdl_trigger();  // the kernel after it may start its setup
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   const uint32_t pad = (1024u - (smem_u32(smem_raw) & 1023u)) & 1023u;
   unsigned char* ring = smem_raw + pad;
@@ -477,6 +479,7 @@ route_topk_cl_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_con
                      const int32_t* __restrict__ k_per_token, int k_uniform, int k_max,
                      int32_t* __restrict__ topk_idx, float* __restrict__ topk_w, int32_t* __restrict__ counts,
                      int count_stride) {
+  pdl_trigger();  // the kernel after it may start its setup
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   const uint32_t pad = (1024u - (smem_u32(smem_raw) & 1023u)) & 1023u;
   unsigned char* ring = smem_raw + pad;
